@@ -1,0 +1,143 @@
+"""Double-precision CPU oracle for RMSNorm, SwiGLU and varlen QK-RoPE.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, by ``__graft_entry__.smoke()``
+and by ``bench.py``'s CPU-baseline / reference leg, never by the
+``fine_tuning_gb300`` package.  It shares no code with the CUDA library.
+
+Every function takes array-likes (numpy or CPU torch tensors of any float
+dtype), upcasts them exactly to float64 and returns float64 numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from .build import LIB, build_oracle
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build_oracle()
+        lib = ctypes.CDLL(LIB)
+        D = ctypes.POINTER(ctypes.c_double)
+        I64 = ctypes.POINTER(ctypes.c_int64)
+        I32 = ctypes.POINTER(ctypes.c_int32)
+        i64, i32, f64 = ctypes.c_int64, ctypes.c_int32, ctypes.c_double
+        lib.oracle_rmsnorm_fwd.argtypes = [D, D, D, D, i64, i64, f64]
+        lib.oracle_rmsnorm_fwd.restype = None
+        lib.oracle_rmsnorm_bwd.argtypes = [D, D, D, D, D, D, D, i64, i64, f64]
+        lib.oracle_rmsnorm_bwd.restype = None
+        lib.oracle_swiglu_fwd.argtypes = [D, D, D, i64]
+        lib.oracle_swiglu_fwd.restype = None
+        lib.oracle_swiglu_bwd.argtypes = [D, D, D, D, D, D, i64]
+        lib.oracle_swiglu_bwd.restype = None
+        lib.oracle_qk_rope.argtypes = [D, D, D, D, D, D, I64, i64, I32, i32,
+                                       i32, i32, i32, f64, ctypes.c_int]
+        lib.oracle_qk_rope.restype = ctypes.c_int
+        lib.oracle_positions.argtypes = [I64, I64, i64, I32, i32]
+        lib.oracle_positions.restype = ctypes.c_int
+        lib.oracle_threads.argtypes = []
+        lib.oracle_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    if hasattr(a, "detach"):  # torch tensor: exact upcast on the CPU
+        import torch
+        a = a.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _p(a, ctype=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def rmsnorm_fwd(x, w, eps):
+    """Returns (y [T,H], rstd [T])."""
+    x, w = _f64(x), _f64(w)
+    T, H = x.shape
+    y = np.empty_like(x)
+    rstd = np.empty(T)
+    _load().oracle_rmsnorm_fwd(_p(x), _p(w), _p(y), _p(rstd), T, H, float(eps))
+    return y, rstd
+
+
+def rmsnorm_bwd(dy, x, w, eps, scales=False):
+    """Returns (dx, dw) or, with scales=True, (dx, dw, dx_scale, dw_scale)."""
+    dy, x, w = _f64(dy), _f64(x), _f64(w)
+    T, H = x.shape
+    dx = np.empty_like(x)
+    dw = np.empty(H)
+    dxs = np.empty_like(x) if scales else None
+    dws = np.empty(H) if scales else None
+    _load().oracle_rmsnorm_bwd(_p(dy), _p(x), _p(w), _p(dx), _p(dw), _p(dxs),
+                               _p(dws), T, H, float(eps))
+    return (dx, dw, dxs, dws) if scales else (dx, dw)
+
+
+def swiglu_fwd(g, u):
+    g, u = _f64(g), _f64(u)
+    h = np.empty_like(g)
+    _load().oracle_swiglu_fwd(_p(g), _p(u), _p(h), g.size)
+    return h
+
+
+def swiglu_bwd(dh, g, u, scales=False):
+    """Returns (dg, du) or (dg, du, dg_scale)."""
+    dh, g, u = _f64(dh), _f64(g), _f64(u)
+    dg, du = np.empty_like(g), np.empty_like(g)
+    dgs = np.empty_like(g) if scales else None
+    _load().oracle_swiglu_bwd(_p(dh), _p(g), _p(u), _p(dg), _p(du), _p(dgs), g.size)
+    return (dg, du, dgs) if scales else (dg, du)
+
+
+def qk_rope(q, k, cu_seqlens, theta, sign=+1, tok=None, scales=False):
+    """Rotate q [n,Hq,D] and k [n,Hkv,D] (row r = global token tok[r]).
+
+    sign=+1 is the forward rotation, -1 the backward (transposed) one.
+    Returns (q_out, k_out) or (q_out, k_out, q_scale, k_scale).
+    """
+    q, k = _f64(q), _f64(k)
+    n, Hq, D = q.shape
+    Hkv = k.shape[1]
+    assert k.shape[0] == n and k.shape[2] == D
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    B = cu.size - 1
+    tk = None if tok is None else np.ascontiguousarray(np.asarray(tok, dtype=np.int64))
+    qo, ko = np.empty_like(q), np.empty_like(k)
+    qs = np.empty_like(q) if scales else None
+    ks = np.empty_like(k) if scales else None
+    rc = _load().oracle_qk_rope(_p(q), _p(k), _p(qo), _p(ko), _p(qs), _p(ks),
+                                _p(tk, ctypes.c_int64), n, _p(cu, ctypes.c_int32),
+                                B, Hq, Hkv, D, float(theta), int(sign))
+    if rc != 0:
+        raise ValueError("oracle_qk_rope: token outside the packed batch or odd D")
+    return (qo, ko, qs, ks) if scales else (qo, ko)
+
+
+def positions(cu_seqlens, tok=None, n=None):
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    if tok is None:
+        n = int(cu[-1]) if n is None else n
+        tk = None
+    else:
+        tk = np.ascontiguousarray(np.asarray(tok, dtype=np.int64))
+        n = tk.size
+    pos = np.empty(n, dtype=np.int64)
+    rc = _load().oracle_positions(_p(pos, ctypes.c_int64), _p(tk, ctypes.c_int64),
+                                  n, _p(cu, ctypes.c_int32), cu.size - 1)
+    if rc != 0:
+        raise ValueError("oracle_positions: token outside the packed batch")
+    return pos
+
+
+def threads() -> int:
+    """Threads the oracle's parallel loops run on."""
+    return int(_load().oracle_threads())

@@ -1,0 +1,293 @@
+"""Pins of the CPU oracle against what the mathematics fixes.
+
+None of these re-types an oracle formula.  Each checks one of: a closed form
+worked by hand, an invariant of the op, central finite differences of the
+oracle's own (separately pinned) forward pass, or a textbook special case
+(complex multiplication for D=2 RoPE).  Together they are chosen so that a
+dropped term, a wrong sign, a wrong frequency index or pairing, an
+off-by-one position or a transposed operand in the oracle fails at least one.
+"""
+import cmath
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+RNG = np.random.default_rng(12345)
+
+
+# ---------------------------------------------------------------- RMSNorm fwd
+
+@pytest.mark.parametrize("c", [2.0, -3.0, 0.5])
+@pytest.mark.parametrize("eps", [1e-6, 0.25])
+def test_rmsnorm_constant_row(c, eps):
+    # x = c * 1  ->  mean x^2 = c^2  ->  y = w c / sqrt(c^2 + eps)
+    H = 37
+    w = 1.0 + 0.1 * RNG.standard_normal(H)
+    y, r = oracle.rmsnorm_fwd(np.full((1, H), c), w, eps)
+    np.testing.assert_allclose(y[0], w * c / math.sqrt(c * c + eps), rtol=1e-14)
+    np.testing.assert_allclose(r[0], 1 / math.sqrt(c * c + eps), rtol=1e-14)
+    if eps == 1e-6:  # returns w (with the sign of c) as eps -> 0
+        np.testing.assert_allclose(y[0], w * math.copysign(1, c), rtol=eps / c ** 2)
+
+
+def test_rmsnorm_hand_example():
+    # x = (3, 4): mean square = 25/2; w = (1, 2)
+    y, r = oracle.rmsnorm_fwd(np.array([[3.0, 4.0]]), np.array([1.0, 2.0]), 0.0)
+    s = math.sqrt(12.5)
+    np.testing.assert_allclose(y[0], [3 / s, 8 / s], rtol=1e-15)
+    np.testing.assert_allclose(r[0], 1 / s, rtol=1e-15)
+
+
+def test_rmsnorm_eps_inside_root():
+    # x = (1, 1), eps = 1: r = 1/sqrt(1 + 1), not 1/(1 + 1) or 1/sqrt(1) + 1
+    y, r = oracle.rmsnorm_fwd(np.ones((1, 2)), np.ones(2), 1.0)
+    np.testing.assert_allclose(r[0], 1 / math.sqrt(2), rtol=1e-15)
+
+
+def test_rmsnorm_scale_invariance_and_rows_independent():
+    x = RNG.standard_normal((6, 33))
+    w = 1.0 + 0.1 * RNG.standard_normal(33)
+    y, _ = oracle.rmsnorm_fwd(x, w, 0.0)
+    y2, _ = oracle.rmsnorm_fwd(7.5 * x, w, 0.0)
+    np.testing.assert_allclose(y2, y, rtol=1e-13)
+    perm = RNG.permutation(6)
+    y3, _ = oracle.rmsnorm_fwd(x[perm], w, 0.0)
+    np.testing.assert_allclose(y3, y[perm], rtol=0, atol=0)
+    # unit RMS of every output row when w = 1, eps = 0
+    y4, _ = oracle.rmsnorm_fwd(x, np.ones(33), 0.0)
+    np.testing.assert_allclose(np.sqrt((y4 ** 2).mean(axis=1)), 1.0, rtol=1e-13)
+
+
+# ------------------------------------------------ finite-difference helpers
+
+def _central_fd(f, arr, h_rel=1e-6):
+    """d f / d arr by central differences, f: array -> scalar (float64)."""
+    g = np.zeros_like(arr)
+    flat, gflat = arr.reshape(-1), g.reshape(-1)
+    for i in range(flat.size):
+        h = h_rel * max(1.0, abs(flat[i]))
+        old = flat[i]
+        flat[i] = old + h
+        fp = f(arr)
+        flat[i] = old - h
+        fm = f(arr)
+        flat[i] = old
+        gflat[i] = (fp - fm) / (2 * h)
+    return g
+
+
+def _fd_close(fd, an, rel=1e-7):
+    scale = max(1.0, float(np.abs(an).max()))
+    assert np.abs(fd - an).max() <= rel * scale * 10, (np.abs(fd - an).max(), scale)
+
+
+# ---------------------------------------------------------------- RMSNorm bwd
+
+@pytest.mark.parametrize("eps", [1e-6, 0.3])
+def test_rmsnorm_bwd_matches_finite_differences(eps):
+    T, H = 5, 12
+    x = RNG.standard_normal((T, H))
+    w = 1.0 + 0.1 * RNG.standard_normal(H)
+    ghat = RNG.standard_normal((T, H))
+
+    def loss_x(xx):
+        return float((ghat * oracle.rmsnorm_fwd(xx, w, eps)[0]).sum())
+
+    def loss_w(ww):
+        return float((ghat * oracle.rmsnorm_fwd(x, ww, eps)[0]).sum())
+
+    dx, dw = oracle.rmsnorm_bwd(ghat, x, w, eps)
+    _fd_close(_central_fd(loss_x, x.copy()), dx)
+    _fd_close(_central_fd(loss_w, w.copy()), dw)
+
+
+def test_rmsnorm_bwd_scales_bound_values():
+    T, H = 9, 40
+    x, dy = RNG.standard_normal((T, H)), RNG.standard_normal((T, H))
+    w = 1.0 + 0.1 * RNG.standard_normal(H)
+    dx, dw, dxs, dws = oracle.rmsnorm_bwd(dy, x, w, 1e-6, scales=True)
+    assert np.all(np.abs(dx) <= dxs * (1 + 1e-12))
+    assert np.all(np.abs(dw) <= dws * (1 + 1e-12))
+    # the scale form does not change the values
+    dx2, dw2 = oracle.rmsnorm_bwd(dy, x, w, 1e-6)
+    np.testing.assert_array_equal(dx, dx2)
+    np.testing.assert_array_equal(dw, dw2)
+
+
+def test_rmsnorm_bwd_zero_upstream():
+    x = RNG.standard_normal((3, 8))
+    dx, dw = oracle.rmsnorm_bwd(np.zeros((3, 8)), x, np.ones(8), 1e-6)
+    assert not dx.any() and not dw.any()
+
+
+# ---------------------------------------------------------------- SwiGLU
+
+def test_swiglu_special_values():
+    u = np.array([1.7, -0.3, 2.0, 5.0])
+    # silu(0) = 0
+    assert np.all(oracle.swiglu_fwd(np.zeros(4), u) == 0)
+    # sigmoid(ln 3) = 3/4 exactly in real arithmetic
+    g = np.full(4, math.log(3.0))
+    np.testing.assert_allclose(oracle.swiglu_fwd(g, u), 0.75 * math.log(3.0) * u, rtol=1e-15)
+    # silu(g) -> g as g -> +inf and -> 0 as g -> -inf
+    np.testing.assert_allclose(oracle.swiglu_fwd(np.full(4, 40.0), u), 40.0 * u, rtol=1e-15)
+    assert np.all(np.abs(oracle.swiglu_fwd(np.full(4, -40.0), u)) < 1e-15)
+    # swiglu_bwd at g = 0: sigmoid(0) = 1/2 -> dg = dh u / 2, du = 0
+    dh = np.array([0.5, -2.0, 1.0, 3.0])
+    dg, du = oracle.swiglu_bwd(dh, np.zeros(4), u)
+    np.testing.assert_allclose(dg, dh * u / 2, rtol=1e-15)
+    assert not du.any()
+
+
+def test_swiglu_bwd_matches_finite_differences():
+    n = 23
+    g, u, dh = RNG.standard_normal(n) * 2, RNG.standard_normal(n), RNG.standard_normal(n)
+    dg, du = oracle.swiglu_bwd(dh, g, u)
+    fd_g = _central_fd(lambda gg: float((dh * oracle.swiglu_fwd(gg, u)).sum()), g.copy())
+    fd_u = _central_fd(lambda uu: float((dh * oracle.swiglu_fwd(g, uu)).sum()), u.copy())
+    _fd_close(fd_g, dg)
+    _fd_close(fd_u, du)
+    dg2, du2, dgs = oracle.swiglu_bwd(dh, g, u, scales=True)
+    np.testing.assert_array_equal(dg, dg2)
+    assert np.all(np.abs(dg) <= dgs * (1 + 1e-12))
+
+
+# ---------------------------------------------------------------- QK-RoPE
+
+def _single(q, k, p, theta, sign=+1):
+    """Rotate one token at position p (a one-sequence batch of p+1 tokens)."""
+    n = p + 1
+    qq = np.zeros((n,) + q.shape)
+    kk = np.zeros((n,) + k.shape)
+    qq[p], kk[p] = q, k
+    qo, ko = oracle.qk_rope(qq[p:p + 1], kk[p:p + 1], [0, n], theta, sign, tok=[p])
+    return qo[0], ko[0]
+
+
+def test_rope_hand_example_d4():
+    # D = 4, theta = 100: pair 0 = (x0, x2) turns by p * 1, pair 1 = (x1, x3)
+    # turns by p * 100^(-1/2) = p / 10.  Position 1.
+    e = np.eye(4)
+    k0 = np.zeros((1, 4))
+    out = [_single(e[i][None, :], k0, 1, 100.0)[0][0] for i in range(4)]
+    c1, s1, c2, s2 = math.cos(1), math.sin(1), math.cos(0.1), math.sin(0.1)
+    np.testing.assert_allclose(out[0], [c1, 0, s1, 0], atol=1e-15)
+    np.testing.assert_allclose(out[1], [0, c2, 0, s2], atol=1e-15)
+    np.testing.assert_allclose(out[2], [-s1, 0, c1, 0], atol=1e-15)
+    np.testing.assert_allclose(out[3], [0, -s2, 0, c2], atol=1e-15)
+    # the backward rotation is the transpose
+    back = _single(e[0][None, :], k0, 1, 100.0, sign=-1)[0][0]
+    np.testing.assert_allclose(back, [c1, 0, -s1, 0], atol=1e-15)
+
+
+@pytest.mark.parametrize("p", [0, 1, 7, 1000, 524287])
+def test_rope_d2_is_complex_multiplication(p):
+    # D = 2: the single frequency is theta^0 = 1, so (a, b) -> (a + ib) e^{ip}
+    a, b = 0.8, -1.3
+    z = complex(a, b) * cmath.exp(1j * p)
+    qo, _ = _single(np.array([[a, b]]), np.zeros((1, 2)), p, 1e6)
+    np.testing.assert_allclose(qo[0], [z.real, z.imag], rtol=0, atol=1e-12)
+
+
+def _packed_case(D=16, Hq=4, Hkv=2, lens=(5, 17, 0, 32, 10)):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    q = RNG.standard_normal((T, Hq, D))
+    k = RNG.standard_normal((T, Hkv, D))
+    return cu, q, k
+
+
+def test_rope_identity_at_sequence_starts_and_positions():
+    cu, q, k = _packed_case()
+    qo, ko = oracle.qk_rope(q, k, cu, 1e4)
+    starts = sorted(set(int(c) for c in cu[:-1]) - {int(cu[-1])})
+    for t in starts:
+        np.testing.assert_array_equal(qo[t], q[t])
+        np.testing.assert_array_equal(ko[t], k[t])
+    pos = oracle.positions(cu)
+    expect = np.concatenate([np.arange(l) for l in np.diff(cu)])
+    np.testing.assert_array_equal(pos, expect)
+    # no other token is left unrotated
+    rotated = [t for t in range(int(cu[-1])) if t not in starts]
+    assert all(np.abs(qo[t] - q[t]).max() > 0 for t in rotated)
+
+
+def test_rope_preserves_pair_norms():
+    cu, q, k = _packed_case(D=64, Hq=3, Hkv=1, lens=(100,))
+    qo, ko = oracle.qk_rope(q, k, cu, 1e6)
+    h = 32
+    for a, b in ((q, qo), (k, ko)):
+        n_in = a[..., :h] ** 2 + a[..., h:] ** 2
+        n_out = b[..., :h] ** 2 + b[..., h:] ** 2
+        np.testing.assert_allclose(n_out, n_in, rtol=1e-13)
+
+
+def test_rope_relative_position_and_gqa():
+    # q_m . k_n depends only on m - n inside one sequence; q-head h reads
+    # kv-head floor(h * Hkv / Hq)
+    D, Hq, Hkv = 16, 4, 2
+    L = 64
+    cu = np.array([0, 3, 3 + L], dtype=np.int32)
+    T = 3 + L
+    qv = RNG.standard_normal((Hq, D))
+    kv = RNG.standard_normal((Hkv, D))
+    q = np.broadcast_to(qv, (T, Hq, D)).copy()
+    k = np.broadcast_to(kv, (T, Hkv, D)).copy()
+    qo, ko = oracle.qk_rope(q, k, cu, 1e4)
+
+    def score(m, n, h):
+        return float(qo[3 + m, h] @ ko[3 + n, h * Hkv // Hq])
+
+    for h in range(Hq):
+        for (m, n), s in (((9, 4), 11), ((20, 20), 30), ((5, 17), 40)):
+            assert abs(score(m, n, h) - score(m + s, n + s, h)) < 1e-12
+    # tokens of the first sequence restart at position 0 in the second one
+    np.testing.assert_array_equal(qo[3], q[3])
+    np.testing.assert_allclose(qo[1], qo[4], rtol=0, atol=0)
+
+
+def test_rope_packing_invariance():
+    lens = (5, 17, 0, 32, 10)
+    cu, q, k = _packed_case(lens=lens)
+    qo, ko = oracle.qk_rope(q, k, cu, 1e4)
+    for b in range(len(lens)):
+        s, e = int(cu[b]), int(cu[b + 1])
+        if s == e:
+            continue
+        qs, ks = oracle.qk_rope(q[s:e], k[s:e], [0, e - s], 1e4)
+        np.testing.assert_array_equal(qs, qo[s:e])
+        np.testing.assert_array_equal(ks, ko[s:e])
+
+
+def test_rope_bwd_is_transpose_and_inverse():
+    cu, q, k = _packed_case(D=32)
+    gq = RNG.standard_normal(q.shape)
+    gk = RNG.standard_normal(k.shape)
+    qo, ko = oracle.qk_rope(q, k, cu, 5e5, +1)
+    gqb, gkb = oracle.qk_rope(gq, gk, cu, 5e5, -1)
+    # <R x, y> = <x, R^T y>
+    lhs = float((qo * gq).sum() + (ko * gk).sum())
+    rhs = float((q * gqb).sum() + (k * gkb).sum())
+    assert abs(lhs - rhs) < 1e-11 * max(1.0, abs(lhs))
+    # R^T R = I
+    qi, ki = oracle.qk_rope(qo, ko, cu, 5e5, -1)
+    np.testing.assert_allclose(qi, q, atol=1e-13)
+    np.testing.assert_allclose(ki, k, atol=1e-13)
+
+
+def test_rope_sampled_rows_equal_full():
+    cu, q, k = _packed_case()
+    qo, ko = oracle.qk_rope(q, k, cu, 1e4)
+    tok = np.array([63, 0, 22, 21, 5])
+    qs, ks = oracle.qk_rope(q[tok], k[tok], cu, 1e4, tok=tok)
+    np.testing.assert_array_equal(qs, qo[tok])
+    np.testing.assert_array_equal(ks, ko[tok])
+
+
+def test_rope_rejects_out_of_batch_token():
+    cu, q, k = _packed_case()
+    with pytest.raises(ValueError):
+        oracle.qk_rope(q[:1], k[:1], cu, 1e4, tok=[int(cu[-1])])
