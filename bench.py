@@ -1,0 +1,553 @@
+#!/usr/bin/env python
+"""Throughput of the fused per-token layer path on one packed batch.
+
+One step = RMSNorm fwd, SwiGLU fwd, QK-RoPE fwd, QK-RoPE bwd, SwiGLU bwd,
+RMSNorm bwd (+ its dw reduction) over one batch, inputs resident in HBM.
+Reported: achieved HBM GB/s over the algorithmic bytes of the step (every
+input read once, every output written once), tokens/s, and the same per
+kernel; the roofline of the dominant kernel against the measured HBM copy
+bandwidth; an end-to-end figure through the same API with pinned host
+buffers copied in and out every step; and the CPU oracle timed on a bounded
+sample of the workload (which also re-checks parity in the same run).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle arm
+
+Under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and tokens/s per fused fwd+bwd kernel"
+OPS = ("rmsnorm_fwd", "swiglu_fwd", "qk_rope_fwd", "qk_rope_bwd", "swiglu_bwd", "rmsnorm_bwd")
+LAUNCHES_PER_STEP = 7  # rmsnorm_bwd is two kernels (rows + fixed-order dw reduction)
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="qwen2.5-0.5b")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="CPU work of the oracle baseline sample")
+    p.add_argument("--reference-seconds", type=float, default=90.0,
+                   help="total CPU time budget of the --impl reference run")
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------- helpers
+
+def rank_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def reduce_timing(elapsed_s: float, units: float, group=None):
+    """(max elapsed over ranks, sum of units over ranks): whole-job numbers."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "fine_tuning_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel \
+                and parts[1] == workload and parts[3] == src:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def _mine(self):
+        uuids = {s[0] for _, s in self.samples}
+        if self.uuid in uuids:
+            return [(t, s) for t, s in self.samples if s[0] == self.uuid]
+        return self.samples if len(uuids) == 1 else []
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        mine = self._mine()
+        inside = [s for t, s in mine if t0 <= t <= t1]
+        window = inside or [s for t, s in mine if t0 - 0.5 <= t <= t1 + 0.5]
+        if not window:
+            return None
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for s in window for n, v in zip(names, s[4:8]) if v == "Active"})
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in window if num(s[1]) is not None]
+        mx = [num(s[2]) for s in window if num(s[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(window), "samples_inside_timed_region": len(inside)}
+
+
+# --------------------------------------------------------- the device step
+
+class Batch:
+    """Every tensor of one step, resident on the device."""
+
+    def __init__(self, wl, device, seed_offset=0):
+        import dataclasses
+
+        import torch
+
+        from fine_tuning_gb300 import ftk
+        from fine_tuning_gb300 import workloads as W
+        if seed_offset:
+            wl = dataclasses.replace(wl, seed=wl.seed + 1000 * seed_offset)
+        self.wl = wl
+        r = W.rmsnorm_inputs(wl, device)
+        s = W.swiglu_inputs(wl, device)
+        q = W.rope_inputs(wl, device)
+        self.cu_host = W.cu_seqlens_from_lengths(W.draw_lengths(wl))
+        self.inputs = {**r, **s, **q,
+                       "cu": torch.as_tensor(self.cu_host, device=device)}
+        dt = wl.torch_dtype
+        T, H, I, Ts = wl.T, wl.H, wl.I, wl.T_swiglu
+        ws_bytes = ftk.rmsnorm_bwd_workspace_bytes(T, H, dt)
+        self.outputs = {
+            "y": torch.empty((T, H), dtype=dt, device=device),
+            "rstd": torch.empty((T,), dtype=torch.float32, device=device),
+            "dx": torch.empty((T, H), dtype=dt, device=device),
+            "dw": torch.empty((H,), dtype=torch.float32, device=device),
+            "h": torch.empty((Ts, I), dtype=dt, device=device),
+            "dg": torch.empty((Ts, I), dtype=dt, device=device),
+            "du": torch.empty((Ts, I), dtype=dt, device=device),
+        }
+        self.ws = torch.empty(((ws_bytes + 15) // 16) * 4, dtype=torch.float32, device=device)
+
+    def ops(self):
+        """The step as six callables, in order."""
+        from fine_tuning_gb300 import ftk
+        i, o, wl = self.inputs, self.outputs, self.wl
+        return (
+            lambda: ftk.rmsnorm_fwd(i["x"], i["w"], wl.eps, y=o["y"], rstd=o["rstd"]),
+            lambda: ftk.swiglu_fwd(i["g"], i["u"], h=o["h"]),
+            lambda: ftk.qk_rope_fwd(i["q"], i["k"], i["cu"], wl.theta),
+            lambda: ftk.qk_rope_bwd(i["dq"], i["dk"], i["cu"], wl.theta),
+            lambda: ftk.swiglu_bwd(i["dh"], i["g"], i["u"], dg=o["dg"], du=o["du"]),
+            lambda: ftk.rmsnorm_bwd(i["dy"], i["x"], i["w"], o["rstd"], wl.eps, dx=o["dx"],
+                                    dw=o["dw"], workspace=self.ws),
+        )
+
+    # tensors a user copies in / out around one step (RoPE is in place, so
+    # q, k, dq, dk go both ways)
+    IN = ("x", "w", "dy", "g", "u", "dh", "q", "k", "dq", "dk", "cu")
+    OUT_FROM_INPUTS = ("q", "k", "dq", "dk")
+    OUT = ("y", "rstd", "dx", "dw", "h", "dg", "du")
+
+
+def sample_tokens(batch, n):
+    """CPU copies of the first n tokens of every input (the oracle sample)."""
+    i = batch.inputs
+    cut = {k: i[k][:n].cpu() for k in ("x", "dy", "g", "u", "dh", "q", "k", "dq", "dk")}
+    cut["w"] = i["w"].cpu()
+    return cut
+
+
+def sample_outputs(batch, n):
+    o, i = batch.outputs, batch.inputs
+    out = {k: o[k][:n].cpu() for k in ("y", "rstd", "dx", "h", "dg", "du")}
+    out.update({k: i[k][:n].cpu() for k in ("q", "k", "dq", "dk")})
+    return out
+
+
+def oracle_step(wl, cut, cu_host, n, scales=False):
+    """The whole path in the CPU oracle over the first n tokens."""
+    import numpy as np
+
+    import oracle
+    cu = np.asarray(cu_host)
+    cu = np.append(cu[cu < n], n)
+    res = {}
+    res["y"], res["rstd"] = oracle.rmsnorm_fwd(cut["x"][:n], cut["w"], wl.eps)
+    r = oracle.rmsnorm_bwd(cut["dy"][:n], cut["x"][:n], cut["w"], wl.eps, scales=scales)
+    res["dx"], res["dw"] = r[0], r[1]
+    if scales:
+        res["dx_s"] = r[2]
+    res["h"] = oracle.swiglu_fwd(cut["g"][:n], cut["u"][:n])
+    r = oracle.swiglu_bwd(cut["dh"][:n], cut["g"][:n], cut["u"][:n], scales=scales)
+    res["dg"], res["du"] = r[0], r[1]
+    if scales:
+        res["dg_s"] = r[2]
+    r = oracle.qk_rope(cut["q"][:n], cut["k"][:n], cu, wl.theta, +1, scales=scales)
+    res["q"], res["k"] = r[0], r[1]
+    if scales:
+        res["q_s"], res["k_s"] = r[2], r[3]
+    r = oracle.qk_rope(cut["dq"][:n], cut["dk"][:n], cu, wl.theta, -1, scales=scales)
+    res["dq"], res["dk"] = r[0], r[1]
+    if scales:
+        res["dq_s"], res["dk_s"] = r[2], r[3]
+    return res
+
+
+def f64_inputs(cut):
+    import torch
+    return {k: v.to(torch.float64).numpy() for k, v in cut.items()}
+
+
+def calibrate_tokens(wl, cut64, cu_host, seconds, cap):
+    """Tokens of oracle work that take about `seconds` on this host."""
+    n0 = min(cap, 64)
+    t = time.perf_counter()
+    oracle_step(wl, cut64, cu_host, n0)
+    per_tok = max((time.perf_counter() - t) / n0, 1e-7)
+    return max(1, min(cap, int(seconds / per_tok)))
+
+
+def cpu_leg(wl, batch, gpu_out, cut, seconds):
+    """Oracle on the host cores over a bounded sample; also the parity gate."""
+    import oracle
+    from fine_tuning_gb300 import workloads as W
+    from oracle.tolerance import assert_close
+    cap = cut["x"].shape[0]
+    cut64 = f64_inputs(cut)
+    n = calibrate_tokens(wl, cut64, batch.cu_host, seconds, cap)
+    t = time.perf_counter()
+    res = oracle_step(wl, cut64, batch.cu_host, n)
+    el = time.perf_counter() - t
+    ib = W.ideal_bytes(wl)
+    sample_bytes = sum(v * n / (wl.T_swiglu if "swiglu" in k else wl.T) for k, v in ib.items())
+    # parity of the GPU step on the same tokens (the CPU sample is a prefix)
+    code = "f32" if wl.dtype == "f32" else "bf16"
+    m = min(n, 256)
+    ref = oracle_step(wl, cut64, batch.cu_host, m, scales=True)
+    worst = 0.0
+    worst = max(worst, assert_close("y", gpu_out["y"][:m], ref["y"], dtype=code))
+    worst = max(worst, assert_close("rstd", gpu_out["rstd"][:m], ref["rstd"], dtype="f32"))
+    worst = max(worst, assert_close("dx", gpu_out["dx"][:m], ref["dx"], ref["dx_s"], dtype=code))
+    worst = max(worst, assert_close("h", gpu_out["h"][:m], ref["h"], dtype=code))
+    worst = max(worst, assert_close("dg", gpu_out["dg"][:m], ref["dg"], ref["dg_s"], dtype=code))
+    worst = max(worst, assert_close("du", gpu_out["du"][:m], ref["du"], dtype=code))
+    for k in ("q", "k", "dq", "dk"):
+        worst = max(worst, assert_close(k, gpu_out[k][:m], ref[k], ref[k + "_s"], dtype=code))
+    del res
+    return {
+        "value": sample_bytes / el / 1e9, "unit": "GB/s", "cores": oracle.threads(),
+        "kind": "oracle", "tokens_per_s": n / el, "seconds": round(el, 3),
+        "sample": f"first {n} of {wl.T} tokens, all six ops (oracle in double, "
+                  f"OpenMP over rows), GB/s over the sample's algorithmic bytes",
+    }, {"tokens_checked": m, "ops": 10, "max_err_over_bound": round(worst, 4)}
+
+
+# -------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from fine_tuning_gb300 import build, ftk
+    from fine_tuning_gb300 import workloads as W
+
+    rank, local_rank, world = rank_info()
+    torch.cuda.set_device(local_rank)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    build.build()
+    ftk.library()
+    wl = W.WORKLOADS[args.workload]
+    batch = Batch(wl, dev, seed_offset=rank)
+    ops = batch.ops()
+    ib = W.ideal_bytes(wl)
+    step_bytes = sum(ib[k] for k in OPS)
+
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    cut = sample_tokens(batch, min(wl.T, 8192)) if do_cpu else None
+    for op in ops:  # the parity step, on the untouched inputs
+        op()
+    torch.cuda.synchronize(dev)
+    gpu_out = sample_outputs(batch, min(wl.T, 256)) if do_cpu else None
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 0)):
+        flush.fill_(1)
+        for op in ops:
+            op()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(K)]
+    whole0, whole1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = ""
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid).start()
+    time.sleep(0.6)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    whole0.record()
+    for s in range(K):
+        flush.fill_(s & 0xFF)
+        e = ev[s]
+        e[0].record()
+        for j, op in enumerate(ops):
+            op()
+            e[j + 1].record()
+    whole1.record()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    time.sleep(0.3)
+    sampler.stop()
+
+    per_op = [0.0] * len(ops)
+    step_ms = 0.0
+    for e in ev:
+        for j in range(len(ops)):
+            per_op[j] += e[j].elapsed_time(e[j + 1])
+        step_ms += e[0].elapsed_time(e[-1])
+    step_ms /= K
+    per_op = [t / K for t in per_op]
+    wall_ms = whole0.elapsed_time(whole1)
+
+    el_max, bytes_all = reduce_timing(step_ms * K / 1e3, step_bytes * K)
+    _, tok_all = reduce_timing(0.0, float(wl.T) * K)
+    value = bytes_all / el_max / 1e9
+    hbm, src = peaks()
+    kernels = {}
+    for j, name in enumerate(OPS):
+        gbs = ib[name] / (per_op[j] * 1e-3) / 1e9
+        toks = W.tokens_per_call(wl)[name]
+        kernels[name] = {"us": round(per_op[j] * 1e3, 2), "GB_s": round(gbs, 1),
+                         "frac_of_measured_hbm" if src == "measured" else "frac_of_fallback_hbm":
+                             round(gbs / hbm, 4),
+                         "tokens_per_s": round(toks / (per_op[j] * 1e-3), 1),
+                         "ideal_bytes": ib[name]}
+    dom = max(range(len(ops)), key=lambda j: per_op[j])
+    dname = OPS[dom]
+    achieved = ib[dname] / (per_op[dom] * 1e-3) / 1e9
+    traffic = ncu_traffic(dname, wl.name)
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(el_max * 1e3 / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded packed batch; no dataset, no weights)",
+        "config": {"workload": wl.name, "T": wl.T, "B": int(len(batch.cu_host) - 1),
+                   "H": wl.H, "I": wl.I, "T_swiglu": wl.T_swiglu, "Hq": wl.Hq, "Hkv": wl.Hkv,
+                   "D": wl.D, "theta": wl.theta, "eps": wl.eps,
+                   "parallelism": f"replicas x{world} (one batch per GPU, no collective)",
+                   "l2": "flushed before every step (256 MiB write, outside the step events)",
+                   "step": list(OPS)},
+        "tokens_per_s": round(tok_all / el_max, 1),
+        "frac_of_hbm": round(value / hbm, 4), "hbm_peak_GB_s": hbm, "hbm_peak_source": src,
+        "kernels": kernels,
+        "roofline": {"kernel": dname, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": traffic, "algorithmic_bytes": ib[dname],
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+                     else "fallback 6.8 TB/s"},
+        "gpu_launches": LAUNCHES_PER_STEP * K,
+        "wall_ms_timed_region": round(wall_ms, 3),
+    }
+    out["clocks"] = sampler.summary(t0, t1)
+
+    if not args.no_e2e:
+        out["e2e"] = e2e_leg(batch, ops, dev, args.e2e_steps, step_bytes)
+    if do_cpu:
+        out["cpu_baseline"], out["parity"] = cpu_leg(wl, batch, gpu_out, cut, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def e2e_leg(batch, ops, dev, steps, step_bytes):
+    """Same step through the public API, with every input copied in from
+    pinned host memory and every output copied back inside the timed region."""
+    import torch
+    host_in = {k: batch.inputs[k].cpu().pin_memory() for k in Batch.IN}
+    outs = {**batch.outputs, **{k: batch.inputs[k] for k in Batch.OUT_FROM_INPUTS}}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def one():
+        for k, v in host_in.items():
+            batch.inputs[k].copy_(v, non_blocking=True)
+        for op in ops:
+            op()
+        for k, v in outs.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / steps
+    el_max, bytes_all = reduce_timing(ms * steps / 1e3, step_bytes * steps)
+    return {"value": round(bytes_all / el_max / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(el_max * 1e3 / steps, 3), "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# -------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle as the reference arm, on rank 0 only."""
+    rank, _, world = rank_info()
+    if rank != 0:
+        return
+    import oracle
+    from fine_tuning_gb300 import workloads as W
+    from oracle.build import build_oracle
+    build_oracle()
+    wl = W.WORKLOADS[args.workload]
+    lens = W.draw_lengths(wl)
+    cu = W.cu_seqlens_from_lengths(lens)
+    cap = min(wl.T, 4096)
+    cut = {}
+    for k, v in (("x", W.rmsnorm_inputs(wl, "cpu", T=cap)), ("g", W.swiglu_inputs(wl, "cpu", T=cap)),
+                 ("q", W.rope_inputs(wl, "cpu", T=cap))):
+        cut.update(v)
+    cut64 = f64_inputs(cut)
+    per_step_s = args.reference_seconds / max(1, args.steps + args.warmup)
+    n = calibrate_tokens(wl, cut64, cu, per_step_s, cap)
+    for _ in range(args.warmup):
+        oracle_step(wl, cut64, cu, n)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(wl, cut64, cu, n)
+    el = time.perf_counter() - t
+    ib = W.ideal_bytes(wl)
+    sample_bytes = sum(v * (n / (wl.T_swiglu if "swiglu" in k else wl.T)) for k, v in ib.items())
+    value = sample_bytes * args.steps / el / 1e9
+    sample = (f"first {n} of {wl.T} tokens per step, all six ops, oracle in double "
+              f"(OpenMP over rows) on the host cores")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded packed batch; no dataset, no weights)",
+        "config": {"workload": wl.name, "T": wl.T, "tokens_per_step": n},
+        "tokens_per_s": round(n * args.steps / el, 1),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

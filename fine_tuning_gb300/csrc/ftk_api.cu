@@ -1,0 +1,320 @@
+// The C ABI declared in include/ftk.h: argument validation, choice of index
+// width and packet width, and dispatch to the kernel launchers.  Nothing here
+// touches device memory or synchronises; every error is found on the host
+// before a launch.
+#include <stdint.h>
+
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "ftk.h"
+#include "launch.h"
+
+namespace {
+
+using ftk::DType;
+
+thread_local std::string g_last_cuda_error;
+
+ftk_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e);
+  return FTK_ERR_CUDA;
+}
+
+ftk_status finish(cudaError_t e) { return e == cudaSuccess ? FTK_OK : cuda_fail(e); }
+
+bool valid_dtype(ftk_dtype d) { return d == FTK_F32 || d == FTK_BF16; }
+
+// 32-bit offsets are used only while every offset a kernel can form, plus
+// the overshoot of its last loop step, stays below 2^31.
+constexpr int64_t kNarrowLimit = (int64_t(1) << 31) - (int64_t(1) << 24);
+
+// A [rows, len] view with row stride ld (elements of es bytes).
+struct View {
+  uintptr_t base;
+  int64_t rows, ld, len, es;
+  uintptr_t end() const { return base + (uintptr_t)(((rows - 1) * ld + len) * es); }
+  int64_t max_offset() const { return (rows - 1) * ld + len; }
+};
+
+View view(const void *p, int64_t rows, int64_t ld, int64_t len, int64_t es) {
+  return View{(uintptr_t)p, rows, ld, len, es};
+}
+
+bool same_view(const View &a, const View &b) {
+  return a.base == b.base && a.ld == b.ld && a.len == b.len && a.es == b.es;
+}
+
+// Conservative: false only when the two element sets are provably disjoint
+// (disjoint byte ranges, or equal strides with interleaved row slices as in a
+// fused QKV or gate_up buffer).
+bool may_overlap(const View &a, const View &b) {
+  if (a.rows <= 0 || b.rows <= 0 || a.len <= 0 || b.len <= 0) return false;
+  if (a.end() <= b.base || b.end() <= a.base) return false;
+  if (a.ld == b.ld && a.es == b.es) {
+    const int64_t period = a.ld * a.es;
+    const int64_t la = a.len * a.es, lb = b.len * b.es;
+    int64_t d = (int64_t)(b.base - a.base) % period;
+    if (d < 0) d += period;
+    if (d >= la && d + lb <= period) return false;
+  }
+  return true;
+}
+
+bool aligned(const void *p, size_t n) { return ((uintptr_t)p % n) == 0; }
+
+std::mutex g_dev_mutex;
+ftk::DeviceInfo g_dev_cache[64];
+bool g_dev_known[64];
+
+cudaError_t device_info(ftk::DeviceInfo *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_dev_known[dev]) {
+      *out = g_dev_cache[dev];
+      return cudaSuccess;
+    }
+  }
+  ftk::DeviceInfo d;
+  d.device = dev;
+  e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    g_dev_cache[dev] = d;
+    g_dev_known[dev] = true;
+  }
+  *out = d;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+namespace ftk {
+cudaError_t current_device_info(DeviceInfo *out) { return device_info(out); }
+}  // namespace ftk
+
+extern "C" {
+
+FTK_API const char *ftk_version(void) { return "0.1.0"; }
+
+FTK_API const char *ftk_status_str(ftk_status s) {
+  switch (s) {
+    case FTK_OK: return "ok";
+    case FTK_ERR_NULL: return "a required pointer is NULL";
+    case FTK_ERR_SHAPE: return "invalid size or stride";
+    case FTK_ERR_ALIGN: return "pointer not aligned to its element size";
+    case FTK_ERR_DTYPE: return "unknown dtype";
+    case FTK_ERR_WORKSPACE: return "workspace missing or too small";
+    case FTK_ERR_CUDA: return "CUDA error";
+    case FTK_ERR_ALIAS: return "buffers overlap where that is not allowed";
+  }
+  return "unknown status";
+}
+
+FTK_API const char *ftk_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+// ------------------------------------------------------------------ RMSNorm
+
+FTK_API ftk_status ftk_rmsnorm_fwd(const void *x, int64_t ldx, const void *w, void *y,
+                                   int64_t ldy, float *rstd, int64_t T, int64_t H, float eps,
+                                   ftk_dtype dtype, ftk_stream_t stream) {
+  if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
+  if (T < 0 || H < 1 || ldx < H || ldy < H || T >= (int64_t(1) << 31)) return FTK_ERR_SHAPE;
+  if (T == 0) return FTK_OK;
+  if (!x || !w || !y) return FTK_ERR_NULL;
+  const DType dt = (DType)dtype;
+  const int64_t es = ftk::dtype_bytes(dt);
+  if (!aligned(x, es) || !aligned(w, es) || !aligned(y, es) || !aligned(rstd, 4))
+    return FTK_ERR_ALIGN;
+  const View vx = view(x, T, ldx, H, es), vy = view(y, T, ldy, H, es);
+  const View vw = view(w, 1, H, H, es), vr = view(rstd, 1, T, T, 4);
+  if (!same_view(vx, vy) && may_overlap(vx, vy)) return FTK_ERR_ALIAS;
+  if (may_overlap(vy, vw)) return FTK_ERR_ALIAS;
+  if (rstd && (may_overlap(vr, vx) || may_overlap(vr, vy) || may_overlap(vr, vw)))
+    return FTK_ERR_ALIAS;
+
+  const int n = dt == DType::F32 ? 4 : 8;
+  const bool vec = aligned(x, 16) && aligned(y, 16) && aligned(w, 16) && H % n == 0 &&
+                   ldx % n == 0 && ldy % n == 0;
+  const bool wide = vx.max_offset() > kNarrowLimit || vy.max_offset() > kNarrowLimit;
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ftk::RmsNormFwdArgs a{x, ldx, w, y, ldy, rstd, T, H, eps};
+  return finish(ftk::launch_rmsnorm_fwd(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+FTK_API size_t ftk_rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, ftk_dtype dtype) {
+  if (!valid_dtype(dtype) || T <= 0 || H <= 0) return 0;
+  ftk::DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return 0;
+  return (size_t)ftk::rmsnorm_bwd_partial_rows(T, dev) * (size_t)H * sizeof(float);
+}
+
+FTK_API ftk_status ftk_rmsnorm_bwd(const void *dy, int64_t lddy, const void *x, int64_t ldx,
+                                   const void *w, const float *rstd, void *dx, int64_t lddx,
+                                   float *dw, void *workspace, size_t workspace_bytes, int64_t T,
+                                   int64_t H, float eps, ftk_dtype dtype, ftk_stream_t stream) {
+  if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
+  if (T < 0 || H < 1 || lddy < H || ldx < H || lddx < H || T >= (int64_t(1) << 31))
+    return FTK_ERR_SHAPE;
+  if (T == 0) return FTK_OK;
+  if (!dy || !x || !w || !dx || !dw) return FTK_ERR_NULL;
+  if (!workspace) return FTK_ERR_WORKSPACE;
+  const DType dt = (DType)dtype;
+  const int64_t es = ftk::dtype_bytes(dt);
+  if (!aligned(dy, es) || !aligned(x, es) || !aligned(w, es) || !aligned(dx, es) ||
+      !aligned(rstd, 4) || !aligned(dw, 4) || !aligned(workspace, 16))
+    return FTK_ERR_ALIGN;
+  const int64_t ws_rows = (int64_t)(workspace_bytes / ((size_t)H * sizeof(float)));
+  if (ws_rows < 1) return FTK_ERR_WORKSPACE;
+
+  const View vdy = view(dy, T, lddy, H, es), vx = view(x, T, ldx, H, es);
+  const View vdx = view(dx, T, lddx, H, es), vw = view(w, 1, H, H, es);
+  const View vr = view(rstd, 1, T, T, 4), vdw = view(dw, 1, H, H, 4);
+  const View vws = view(workspace, 1, ws_rows * H, ws_rows * H, 4);
+  if (!same_view(vdx, vdy) && may_overlap(vdx, vdy)) return FTK_ERR_ALIAS;
+  const View outs[3] = {vdx, vdw, vws};
+  for (int i = 0; i < 3; ++i) {
+    if (i != 0 && may_overlap(outs[i], vdy)) return FTK_ERR_ALIAS;
+    if (may_overlap(outs[i], vx) || may_overlap(outs[i], vw)) return FTK_ERR_ALIAS;
+    if (rstd && may_overlap(outs[i], vr)) return FTK_ERR_ALIAS;
+    for (int k = i + 1; k < 3; ++k)
+      if (may_overlap(outs[i], outs[k])) return FTK_ERR_ALIAS;
+  }
+
+  const int n = dt == DType::F32 ? 4 : 8;
+  const bool vec = aligned(dy, 16) && aligned(x, 16) && aligned(w, 16) && aligned(dx, 16) &&
+                   H % n == 0 && lddy % n == 0 && ldx % n == 0 && lddx % n == 0;
+  const bool wide = vdy.max_offset() > kNarrowLimit || vx.max_offset() > kNarrowLimit ||
+                    vdx.max_offset() > kNarrowLimit;
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ftk::RmsNormBwdArgs a{dy, lddy, x, ldx, w, rstd, dx, lddx, dw, (float *)workspace, ws_rows,
+                        T, H, eps};
+  return finish(ftk::launch_rmsnorm_bwd(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+// ------------------------------------------------------------------- SwiGLU
+
+FTK_API ftk_status ftk_swiglu_fwd(const void *g, const void *u, int64_t ld_gu, void *h,
+                                  int64_t ld_h, int64_t T, int64_t I, ftk_dtype dtype,
+                                  ftk_stream_t stream) {
+  if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
+  if (T < 0 || I < 0 || ld_gu < I || ld_h < I) return FTK_ERR_SHAPE;
+  if (T == 0 || I == 0) return FTK_OK;
+  if (!g || !u || !h) return FTK_ERR_NULL;
+  const DType dt = (DType)dtype;
+  const int64_t es = ftk::dtype_bytes(dt);
+  if (!aligned(g, es) || !aligned(u, es) || !aligned(h, es)) return FTK_ERR_ALIGN;
+  const View vg = view(g, T, ld_gu, I, es), vu = view(u, T, ld_gu, I, es);
+  const View vh = view(h, T, ld_h, I, es);
+  if (!same_view(vh, vg) && may_overlap(vh, vg)) return FTK_ERR_ALIAS;
+  if (!same_view(vh, vu) && may_overlap(vh, vu)) return FTK_ERR_ALIAS;
+
+  const int n = dt == DType::F32 ? 4 : 8;
+  const bool vec = aligned(g, 16) && aligned(u, 16) && aligned(h, 16) && I % n == 0 &&
+                   ld_gu % n == 0 && ld_h % n == 0;
+  const bool wide = vg.max_offset() > kNarrowLimit || vu.max_offset() > kNarrowLimit ||
+                    vh.max_offset() > kNarrowLimit || T * I > kNarrowLimit;
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ftk::SwigluFwdArgs a{g, u, ld_gu, h, ld_h, T, I};
+  return finish(ftk::launch_swiglu_fwd(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+FTK_API ftk_status ftk_swiglu_bwd(const void *dh, int64_t ld_dh, const void *g, const void *u,
+                                  int64_t ld_gu, void *dg, void *du, int64_t ld_dgu, int64_t T,
+                                  int64_t I, ftk_dtype dtype, ftk_stream_t stream) {
+  if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
+  if (T < 0 || I < 0 || ld_dh < I || ld_gu < I || ld_dgu < I) return FTK_ERR_SHAPE;
+  if (T == 0 || I == 0) return FTK_OK;
+  if (!dh || !g || !u || !dg || !du) return FTK_ERR_NULL;
+  const DType dt = (DType)dtype;
+  const int64_t es = ftk::dtype_bytes(dt);
+  if (!aligned(dh, es) || !aligned(g, es) || !aligned(u, es) || !aligned(dg, es) ||
+      !aligned(du, es))
+    return FTK_ERR_ALIGN;
+  const View vdh = view(dh, T, ld_dh, I, es), vg = view(g, T, ld_gu, I, es);
+  const View vu = view(u, T, ld_gu, I, es), vdg = view(dg, T, ld_dgu, I, es);
+  const View vdu = view(du, T, ld_dgu, I, es);
+  if (may_overlap(vdg, vdu)) return FTK_ERR_ALIAS;
+  const View ins[3] = {vdh, vg, vu};
+  for (const View &o : {vdg, vdu})
+    for (const View &i : ins)
+      if (!same_view(o, i) && may_overlap(o, i)) return FTK_ERR_ALIAS;
+
+  const int n = dt == DType::F32 ? 4 : 8;
+  const bool vec = aligned(dh, 16) && aligned(g, 16) && aligned(u, 16) && aligned(dg, 16) &&
+                   aligned(du, 16) && I % n == 0 && ld_dh % n == 0 && ld_gu % n == 0 &&
+                   ld_dgu % n == 0;
+  const bool wide = vdh.max_offset() > kNarrowLimit || vg.max_offset() > kNarrowLimit ||
+                    vu.max_offset() > kNarrowLimit || vdg.max_offset() > kNarrowLimit ||
+                    vdu.max_offset() > kNarrowLimit || T * I > kNarrowLimit;
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ftk::SwigluBwdArgs a{dh, ld_dh, g, u, ld_gu, dg, du, ld_dgu, T, I};
+  return finish(ftk::launch_swiglu_bwd(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+// ------------------------------------------------------------------ QK-RoPE
+
+static ftk_status qk_rope(void *q, int64_t ld_q, void *k, int64_t ld_k, const int32_t *cu,
+                          int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D, double theta,
+                          ftk_dtype dtype, ftk_stream_t stream, bool backward) {
+  if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
+  if (T < 0 || B < 0 || Hq < 0 || Hkv < 0 || Hq + Hkv < 1 || D < 2 || D % 2 != 0 ||
+      D / 2 > ftk::kRopeMaxHalf || T >= (int64_t(1) << 31))
+    return FTK_ERR_SHAPE;
+  if (!(theta > 0.0)) return FTK_ERR_SHAPE;
+  if ((Hq > 0 && ld_q < (int64_t)Hq * D) || (Hkv > 0 && ld_k < (int64_t)Hkv * D))
+    return FTK_ERR_SHAPE;
+  if (T == 0) return FTK_OK;
+  if (B < 1) return FTK_ERR_SHAPE;
+  if (!cu || (Hq > 0 && !q) || (Hkv > 0 && !k)) return FTK_ERR_NULL;
+  const DType dt = (DType)dtype;
+  const int64_t es = ftk::dtype_bytes(dt);
+  if ((Hq > 0 && !aligned(q, es)) || (Hkv > 0 && !aligned(k, es)) || !aligned(cu, 4))
+    return FTK_ERR_ALIGN;
+  const View vq = view(q, Hq > 0 ? T : 0, ld_q, (int64_t)Hq * D, es);
+  const View vk = view(k, Hkv > 0 ? T : 0, ld_k, (int64_t)Hkv * D, es);
+  const View vc = view(cu, 1, (int64_t)B + 1, (int64_t)B + 1, 4);
+  if (may_overlap(vq, vk) || may_overlap(vc, vq) || may_overlap(vc, vk)) return FTK_ERR_ALIAS;
+
+  const int n = dt == DType::F32 ? 4 : 8;
+  const bool vec = (D / 2) % n == 0 && (Hq == 0 || (aligned(q, 16) && ld_q % n == 0)) &&
+                   (Hkv == 0 || (aligned(k, 16) && ld_k % n == 0));
+  const bool wide = (Hq > 0 && vq.max_offset() > kNarrowLimit) ||
+                    (Hkv > 0 && vk.max_offset() > kNarrowLimit);
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ftk::RopeArgs a{q, ld_q, k, ld_k, cu, B, T, Hq, Hkv, D, theta, backward};
+  return finish(ftk::launch_qk_rope(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+FTK_API ftk_status ftk_qk_rope_fwd(void *q, int64_t ld_q, void *k, int64_t ld_k,
+                                   const int32_t *cu_seqlens, int32_t B, int64_t T, int32_t Hq,
+                                   int32_t Hkv, int32_t D, double theta, ftk_dtype dtype,
+                                   ftk_stream_t stream) {
+  return qk_rope(q, ld_q, k, ld_k, cu_seqlens, B, T, Hq, Hkv, D, theta, dtype, stream, false);
+}
+
+FTK_API ftk_status ftk_qk_rope_bwd(void *dq, int64_t ld_q, void *dk, int64_t ld_k,
+                                   const int32_t *cu_seqlens, int32_t B, int64_t T, int32_t Hq,
+                                   int32_t Hkv, int32_t D, double theta, ftk_dtype dtype,
+                                   ftk_stream_t stream) {
+  return qk_rope(dq, ld_q, dk, ld_k, cu_seqlens, B, T, Hq, Hkv, D, theta, dtype, stream, true);
+}
+
+}  // extern "C"

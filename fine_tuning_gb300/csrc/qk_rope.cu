@@ -1,0 +1,230 @@
+// In-place rotary position embedding of Q and K together, rotate-half
+// layout, over a packed batch of variable-length sequences.
+//
+// Sources: "Unsloth prétend accélérer 5 fois l'entraînement des LLM avec de
+// nouveaux noyaux Triton et un auto-packing" (seventnews.com): Q and K are
+// rotated by ONE kernel instead of two, variable-length RoPE, fully in place
+// (no clone, no contiguous transpose); blocks are launched for groups of
+// heads; LONG_INDEXING (64-bit offsets) for 500k-token runs; packing keeps
+// the sequence-length metadata so positions restart in every sequence.
+// Chronicals (arXiv 2601.02609), abstract, optimisation (1): fused QK-RoPE.
+//
+// For token t of sequence b, p = t - cu[b]; for i < D/2,
+// phi_i = p * theta^(-2i/D) and every head vector v of Q and K becomes
+//   v[i] <- v[i] cos phi_i - v[i+D/2] sin phi_i
+//   v[i+D/2] <- v[i+D/2] cos phi_i + v[i] sin phi_i
+// (backward: phi -> -phi, the transpose).
+//
+// A CTA owns TOK consecutive tokens.  Per token, TPT = NV * S threads: NV
+// packet slots across one half of a head times S head slots; the thread with
+// (slot s, packet j) rotates packet j of heads s, s+S, s+2S, ... (HPT heads
+// per pass).  Its loads are issued first; while they are in flight the CTA
+// finds each token's position (binary search of the device cu_seqlens, no
+// host synchronisation) and computes cos/sin of the TOK x D/2 angles once
+// into shared memory, shared by every head of the token.  No cos/sin table
+// is read from HBM.
+//
+// The angle is formed in turns, phi / 2pi = p * f_i with f_i split on the
+// host into two floats (hi + lo, ~48 significant bits); p is split into a
+// multiple of 4096 and a remainder so each partial product is exact or
+// nearly so (Dekker's two-product via fma), the integer turns are dropped
+// from every term, and sincospif() of the remaining fraction gives cos and
+// sin.  The angle error stays near 1e-7 rad at p = 5e5, where a plain fp32
+// p * inv_freq would be off by up to ~0.03 rad.
+#include <cmath>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace ftk {
+
+namespace {
+
+struct RopeFreqs {
+  float hi[kRopeMaxHalf];
+  float lo[kRopeMaxHalf];
+};
+
+constexpr int kCtaThreads = 256;
+
+__device__ __forceinline__ float frac_turns(float a) { return a - rintf(a); }
+
+// cos and sin of 2*pi*p*(fhi + flo).
+__device__ __forceinline__ void rope_cos_sin(int p, float fhi, float flo, float *c, float *s) {
+  const float ph = (float)(p & ~4095);  // exact: at most 19 significant bits
+  const float pl = (float)(p & 4095);   // exact
+  const float a1 = __fmul_rn(ph, fhi);
+  const float e1 = fmaf(ph, fhi, -a1);  // ph*fhi = a1 + e1 exactly
+  const float a2 = __fmul_rn(pl, fhi);
+  const float e2 = fmaf(pl, fhi, -a2);  // pl*fhi = a2 + e2 exactly
+  const float a3 = __fmul_rn(ph, flo);
+  const float a4 = __fmul_rn(pl, flo);
+  float r = frac_turns(a1) + frac_turns(a2);
+  r += frac_turns(a3) + frac_turns(e1);
+  r += e2 + a4;
+  r = frac_turns(r);
+  sincospif(2.0f * r, s, c);
+}
+
+// Sequence of token t: largest b < B with cu[b] <= t (zero-length sequences
+// are skipped because their boundary repeats).  Clamped to [0, B-1], so a
+// malformed cu can only give wrong positions, never a wrong address.
+template <typename Idx>
+__device__ __forceinline__ int position_of(Idx t, const int32_t *__restrict__ cu, int B) {
+  int lo = 1, hi = B;  // first i in [1, B] with cu[i] > t
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((Idx)__ldg(cu + mid) <= t)
+      lo = mid + 1;
+    else
+      hi = mid - 1;
+  }
+  int b = lo - 1;
+  b = b < 0 ? 0 : (b > B - 1 ? B - 1 : b);
+  return (int)(t - (Idx)__ldg(cu + b));
+}
+
+template <typename T, typename Idx, int N, int HPT>
+__global__ void __launch_bounds__(kCtaThreads)
+qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int B,
+               Idx rows, int Hq, int NH, int D, int S, int NV, int TOK, float sgn,
+               const __grid_constant__ RopeFreqs fr) {
+  extern __shared__ float2 cs[];  // [TOK][D/2] (cos, sgn*sin)
+  __shared__ int pos[kCtaThreads];
+
+  const int half = D >> 1;
+  const int TPT = NV * S;
+  const int tl = threadIdx.x / TPT;
+  const int rem = threadIdx.x - tl * TPT;
+  const int slot = rem / NV, j = rem - slot * NV;
+  const Idx t = (Idx)blockIdx.x * TOK + tl;
+  const bool active = tl < TOK && t < rows;
+
+  // pass 0: loads for the first HPT heads of this thread
+  Packet<T, N> a[HPT], b[HPT];
+  T *ptr[HPT];
+#pragma unroll
+  for (int m = 0; m < HPT; ++m) {
+    const int h = m * S + slot;
+    ptr[m] = nullptr;
+    if (active && h < NH) {
+      ptr[m] = (h < Hq ? q + t * ld_q + (Idx)h * D : k + t * ld_k + (Idx)(h - Hq) * D) +
+               (Idx)j * N;
+      a[m] = load_packet<T, N>(ptr[m]);
+      b[m] = load_packet<T, N>(ptr[m] + half);
+    }
+  }
+
+  // positions, then cos/sin of every (token, frequency) of the CTA
+  for (int i = threadIdx.x; i < TOK; i += blockDim.x) {
+    const Idx tt = (Idx)blockIdx.x * TOK + i;
+    pos[i] = tt < rows ? position_of<Idx>(tt, cu, B) : 0;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < TOK * half; e += blockDim.x) {
+    const int tt = e / half, i = e - tt * half;
+    float c, s;
+    rope_cos_sin(pos[tt], fr.hi[i], fr.lo[i], &c, &s);
+    cs[e] = make_float2(c, sgn * s);
+  }
+  __syncthreads();
+
+  if (!active) return;
+  const float2 *row_cs = cs + tl * half + j * N;
+  float cv[N], sv[N];
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    const float2 v = row_cs[e];
+    cv[e] = v.x;
+    sv[e] = v.y;
+  }
+
+  for (int h0 = 0;; h0 += HPT * S) {
+#pragma unroll
+    for (int m = 0; m < HPT; ++m) {
+      if (ptr[m] != nullptr) {
+        Packet<T, N> oa, ob;
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float x1 = a[m].get(e), x2 = b[m].get(e);
+          oa.set(e, fmaf(x1, cv[e], -x2 * sv[e]));
+          ob.set(e, fmaf(x2, cv[e], x1 * sv[e]));
+        }
+        store_packet<T, N>(ptr[m], oa);
+        store_packet<T, N>(ptr[m] + half, ob);
+      }
+    }
+    // heads beyond the first HPT * S (only for very wide rows)
+    const int next = h0 + HPT * S;
+    if (next >= NH) break;
+#pragma unroll
+    for (int m = 0; m < HPT; ++m) {
+      const int h = next + m * S + slot;
+      ptr[m] = nullptr;
+      if (h < NH) {
+        ptr[m] = (h < Hq ? q + t * ld_q + (Idx)h * D : k + t * ld_k + (Idx)(h - Hq) * D) +
+                 (Idx)j * N;
+        a[m] = load_packet<T, N>(ptr[m]);
+        b[m] = load_packet<T, N>(ptr[m] + half);
+      }
+    }
+  }
+}
+
+template <typename T, typename Idx, int N, int HPT>
+cudaError_t rope_launch(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
+  const int NH = a.Hq + a.Hkv;
+  const int half = a.D / 2;
+  const int NV = half / N;
+  int S = (NH + HPT - 1) / HPT;
+  if (S * NV > kCtaThreads) S = kCtaThreads / NV > 0 ? kCtaThreads / NV : 1;
+  const int TPT = NV * S;
+  int TOK = kCtaThreads / TPT;
+  if (TOK < 1) TOK = 1;
+  const int threads = TOK * TPT;
+  const size_t smem = sizeof(float2) * (size_t)TOK * half;
+  const int64_t grid = ceil_div(a.T, (int64_t)TOK);
+  qk_rope_kernel<T, Idx, N, HPT><<<(unsigned)grid, threads, smem, s>>>(
+      (T *)a.q, (Idx)a.ld_q, (T *)a.k, (Idx)a.ld_k, a.cu, a.B, (Idx)a.T, a.Hq, NH, a.D, S, NV,
+      TOK, a.backward ? -1.0f : 1.0f, fr);
+  return cudaGetLastError();
+}
+
+template <typename T, typename Idx, int N>
+cudaError_t rope_heads(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
+  const int NH = a.Hq + a.Hkv;
+  if (NH <= 1) return rope_launch<T, Idx, N, 1>(a, fr, s);
+  if (NH <= 2) return rope_launch<T, Idx, N, 2>(a, fr, s);
+  if (NH <= 4) return rope_launch<T, Idx, N, 4>(a, fr, s);
+  return rope_launch<T, Idx, N, 8>(a, fr, s);
+}
+
+template <typename T, typename Idx>
+cudaError_t rope_typed(bool vec, const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
+  constexpr int NV = VecWidth<T>::value;
+  return vec ? rope_heads<T, Idx, NV>(a, fr, s) : rope_heads<T, Idx, 1>(a, fr, s);
+}
+
+}  // namespace
+
+cudaError_t launch_qk_rope(DType dt, bool vec, bool wide, const RopeArgs &a, const DeviceInfo &,
+                           cudaStream_t s) {
+  // f_i = theta^(-2i/D) / (2 pi) in double, split into two floats.
+  RopeFreqs fr;
+  const int half = a.D / 2;
+  for (int i = 0; i < kRopeMaxHalf; ++i) {
+    if (i < half) {
+      const double f = std::pow(a.theta, -2.0 * (double)i / (double)a.D) / 6.283185307179586476925;
+      const float hi = (float)f;
+      fr.hi[i] = hi;
+      fr.lo[i] = (float)(f - (double)hi);
+    } else {
+      fr.hi[i] = fr.lo[i] = 0.f;
+    }
+  }
+  if (dt == DType::F32)
+    return wide ? rope_typed<float, int64_t>(vec, a, fr, s) : rope_typed<float, int32_t>(vec, a, fr, s);
+  return wide ? rope_typed<bf16, int64_t>(vec, a, fr, s) : rope_typed<bf16, int32_t>(vec, a, fr, s);
+}
+
+}  // namespace ftk

@@ -1,0 +1,325 @@
+// RMSNorm backward (gradient of sum(dy * y), y = x * r * w):
+//   c[t]    = sum_j dy[t,j] w[j] x[t,j]
+//   dx[t,j] = r[t] w[j] dy[t,j] - r[t]^3 x[t,j] c[t] / H
+//   dw[j]   = sum_t dy[t,j] x[t,j] r[t]
+// (Chronicals, arXiv 2601.02609, abstract, optimisation (1): fused RMSNorm;
+// the page gives no formula, this is the standard gradient.)
+//
+// Pass 1 (rmsnorm_bwd_rows): a persistent grid of P CTAs walks the rows with
+// a fixed stride.  Each thread keeps its slice of w in registers for the
+// whole kernel and accumulates dy*x*r for its columns in fp32 registers over
+// the rows its group visits.  At the end the R row groups of a CTA are summed
+// in shared memory in a fixed order and the CTA writes one fp32 row of
+// partials to the workspace.
+// Pass 2 (dw_reduce): dw[j] = sum_p ws[p, j], rows in a fixed order.
+// The row -> CTA map and every summation order are fixed, so dw is bitwise
+// reproducible; no CTA ever waits on another.
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace ftk {
+
+namespace {
+
+constexpr int kMaxBlocksPerSm = 8;
+
+template <typename T, typename Idx, int N, int V, bool HAS_RSTD>
+__global__ void __launch_bounds__(256)
+rmsnorm_bwd_rows(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restrict__ w,
+                 const float *__restrict__ rstd, T *dx, Idx lddx, float *__restrict__ ws,
+                 Idx rows, int hp, int H, float inv_h, float eps, int W, int R) {
+  // [2][R][W] float2 reduction slots (double-buffered by row parity), then,
+  // when R > 1, [R][H] fp32 dw partials for the final combine.
+  extern __shared__ float smem[];
+  float2 *red = reinterpret_cast<float2 *>(smem);
+  float *part = smem + 4 * R * W;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / W, wig = warp - grp * W;
+  const int gi = wig * 32 + lane, G = W * 32;
+
+  Packet<T, N> wv[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int c = gi + k * G;
+    if (c < hp) wv[k] = load_packet<T, N>(w + (Idx)c * N);
+  }
+  float acc[V][N];
+#pragma unroll
+  for (int k = 0; k < V; ++k)
+#pragma unroll
+    for (int e = 0; e < N; ++e) acc[k][e] = 0.f;
+
+  int parity = 0;
+  const Idx step = (Idx)gridDim.x * R;
+  for (Idx base = (Idx)blockIdx.x * R; base < rows; base += step, parity ^= 1) {
+    const Idx row = base + grp;
+    const bool active = row < rows;
+    Packet<T, N> xv[V], gv[V];
+    float r = 0.f;
+    float2 cs = make_float2(0.f, 0.f);  // (sum dy*w*x, sum x*x)
+    if (active) {
+      const T *xr = x + row * ldx;
+      const T *gr = dy + row * lddy;
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const int c = gi + k * G;
+        if (c < hp) {
+          xv[k] = load_packet_stream<T, N>(xr + (Idx)c * N);
+          gv[k] = load_packet_stream<T, N>(gr + (Idx)c * N);
+        }
+      }
+      if (HAS_RSTD) r = rstd[row];
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        if (gi + k * G < hp) {
+#pragma unroll
+          for (int e = 0; e < N; ++e) {
+            const float xf = xv[k].get(e);
+            cs.x = fmaf(gv[k].get(e) * wv[k].get(e), xf, cs.x);
+            if (!HAS_RSTD) cs.y = fmaf(xf, xf, cs.y);
+          }
+        }
+      }
+    }
+    if (HAS_RSTD) {
+      cs.x = warp_sum(cs.x);
+    } else {
+      cs = warp_sum2(cs);
+    }
+    if (W > 1) {
+      float2 *slot = red + (parity * R + grp) * W;
+      if (lane == 0) slot[wig] = cs;
+      __syncthreads();
+      cs = make_float2(0.f, 0.f);
+      for (int i = 0; i < W; ++i) {
+        cs.x += slot[i].x;
+        cs.y += slot[i].y;
+      }
+    }
+    if (active) {
+      if (!HAS_RSTD) r = rsqrtf(fmaf(cs.y, inv_h, eps));
+      const float a = r * r * r * cs.x * inv_h;
+      T *dr = dx + row * lddx;
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const int c = gi + k * G;
+        if (c < hp) {
+          Packet<T, N> o;
+#pragma unroll
+          for (int e = 0; e < N; ++e) {
+            const float xf = xv[k].get(e), gf = gv[k].get(e);
+            o.set(e, fmaf(-a, xf, r * wv[k].get(e) * gf));
+            acc[k][e] = fmaf(gf * xf, r, acc[k][e]);
+          }
+          store_packet<T, N>(dr + (Idx)c * N, o);
+        }
+      }
+    }
+  }
+
+  float *dst = ws + (size_t)blockIdx.x * H;
+  if (R == 1) {
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const int c = gi + k * G;
+      if (c < hp)
+#pragma unroll
+        for (int e = 0; e < N; ++e) dst[c * N + e] = acc[k][e];
+    }
+    return;
+  }
+  float *mine = part + grp * H;
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int c = gi + k * G;
+    if (c < hp)
+#pragma unroll
+      for (int e = 0; e < N; ++e) mine[c * N + e] = acc[k][e];
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < H; j += blockDim.x) {
+    float sum = 0.f;
+    for (int g = 0; g < R; ++g) sum += part[g * H + j];
+    dst[j] = sum;
+  }
+}
+
+// Rows too long for registers: one CTA per row at a time, persistent grid,
+// two passes over the row; the CTA's dw partial row lives in the workspace
+// and is updated in place (each CTA owns its row, so no atomics).
+template <typename T, typename Idx, bool HAS_RSTD>
+__global__ void __launch_bounds__(256)
+rmsnorm_bwd_generic(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restrict__ w,
+                    const float *__restrict__ rstd, T *dx, Idx lddx, float *__restrict__ ws,
+                    Idx rows, Idx H, float inv_h, float eps) {
+  __shared__ float2 red[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float *mine = ws + (size_t)blockIdx.x * H;
+  for (Idx j = threadIdx.x; j < H; j += blockDim.x) mine[j] = 0.f;
+  for (Idx row = blockIdx.x; row < rows; row += gridDim.x) {
+    const T *xr = x + row * ldx;
+    const T *gr = dy + row * lddy;
+    float2 cs = make_float2(0.f, 0.f);
+    for (Idx j = threadIdx.x; j < H; j += blockDim.x) {
+      const float xf = to_float(xr[j]);
+      cs.x = fmaf(to_float(gr[j]) * to_float(w[j]), xf, cs.x);
+      cs.y = fmaf(xf, xf, cs.y);
+    }
+    cs = warp_sum2(cs);
+    if (lane == 0) red[warp] = cs;
+    __syncthreads();
+    cs = make_float2(0.f, 0.f);
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+      cs.x += red[i].x;
+      cs.y += red[i].y;
+    }
+    __syncthreads();
+    const float r = HAS_RSTD ? rstd[row] : rsqrtf(fmaf(cs.y, inv_h, eps));
+    const float a = r * r * r * cs.x * inv_h;
+    T *dr = dx + row * lddx;
+    for (Idx j = threadIdx.x; j < H; j += blockDim.x) {
+      const float xf = to_float(xr[j]), gf = to_float(gr[j]);
+      dr[j] = from_float<T>(fmaf(-a, xf, r * to_float(w[j]) * gf));
+      mine[j] = fmaf(gf * xf, r, mine[j]);
+    }
+  }
+}
+
+// dw[j] = sum_{p < P} ws[p, j]: a CTA owns 32 columns, its 8 warps take the
+// rows p = warp, warp + 8, ... and their sums are added in warp order.
+__global__ void __launch_bounds__(256)
+dw_reduce(const float *__restrict__ ws, int P, int H, float *__restrict__ dw) {
+  __shared__ float part[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = blockIdx.x * 32 + lane;
+  float s = 0.f;
+  if (col < H) {
+#pragma unroll 8
+    for (int p = warp; p < P; p += 8) s += ws[(size_t)p * H + col];
+  }
+  part[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && col < H) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += part[i][lane];
+    dw[col] = t;
+  }
+}
+
+// Resident CTAs per SM of one kernel instance at one launch shape, cached
+// per (kernel, device, shared memory); capped at kMaxBlocksPerSm.
+struct OccEntry {
+  const void *kernel;
+  int device, threads;
+  size_t smem;
+  int blocks;
+};
+std::mutex g_occ_mutex;
+std::vector<OccEntry> g_occ;
+
+int blocks_per_sm(const void *kernel, int threads, size_t smem, const DeviceInfo &dev) {
+  {
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    for (const OccEntry &e : g_occ)
+      if (e.kernel == kernel && e.device == dev.device && e.threads == threads && e.smem == smem)
+        return e.blocks;
+  }
+  int n = 0;
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess ||
+      n < 1) {
+    cudaGetLastError();
+    n = 1;
+  }
+  if (n > kMaxBlocksPerSm) n = kMaxBlocksPerSm;
+  std::lock_guard<std::mutex> lock(g_occ_mutex);
+  g_occ.push_back(OccEntry{kernel, dev.device, threads, smem, n});
+  return n;
+}
+
+template <typename T, typename Idx, int N, int V, bool HAS_RSTD>
+cudaError_t bwd_rows_v(const RowPlan &p, const RmsNormBwdArgs &a, const DeviceInfo &dev,
+                       cudaStream_t s) {
+  auto kern = rmsnorm_bwd_rows<T, Idx, N, V, HAS_RSTD>;
+  const int threads = p.threads();
+  const size_t smem = sizeof(float) * (4 * p.R * p.W + (p.R > 1 ? (size_t)p.R * a.H : 0));
+  if (smem > (size_t)dev.max_smem_optin) return cudaErrorInvalidConfiguration;
+  const int occ = blocks_per_sm((const void *)kern, threads, smem, dev);
+  int64_t P = ceil_div(a.T, (int64_t)p.R);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  if (P > a.ws_rows) P = a.ws_rows;
+  kern<<<(unsigned)P, threads, smem, s>>>(
+      (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
+      (T *)a.dx, (Idx)a.lddx, a.ws, (Idx)a.T, (int)(a.H / N), (int)a.H,
+      (float)(1.0 / (double)a.H), a.eps, p.W, p.R);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 256, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
+  return cudaGetLastError();
+}
+
+template <typename T, typename Idx, int N, bool HAS_RSTD>
+cudaError_t bwd_rows(const RowPlan &p, const RmsNormBwdArgs &a, const DeviceInfo &dev,
+                     cudaStream_t s) {
+  switch (p.V) {
+    case 1: return bwd_rows_v<T, Idx, N, 1, HAS_RSTD>(p, a, dev, s);
+    case 2: return bwd_rows_v<T, Idx, N, 2, HAS_RSTD>(p, a, dev, s);
+    case 3: return bwd_rows_v<T, Idx, N, 3, HAS_RSTD>(p, a, dev, s);
+    case 4: return bwd_rows_v<T, Idx, N, 4, HAS_RSTD>(p, a, dev, s);
+    case 6: return bwd_rows_v<T, Idx, N, 6, HAS_RSTD>(p, a, dev, s);
+    case 8: return bwd_rows_v<T, Idx, N, 8, HAS_RSTD>(p, a, dev, s);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
+template <typename T, typename Idx, bool HAS_RSTD>
+cudaError_t bwd_generic(const RmsNormBwdArgs &a, const DeviceInfo &dev, cudaStream_t s) {
+  int64_t P = a.T < (int64_t)dev.sms * 4 ? a.T : (int64_t)dev.sms * 4;
+  if (P > a.ws_rows) P = a.ws_rows;
+  rmsnorm_bwd_generic<T, Idx, HAS_RSTD><<<(unsigned)P, 256, 0, s>>>(
+      (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
+      (T *)a.dx, (Idx)a.lddx, a.ws, (Idx)a.T, (Idx)a.H, (float)(1.0 / (double)a.H), a.eps);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 256, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
+  return cudaGetLastError();
+}
+
+template <typename T, typename Idx>
+cudaError_t bwd_typed(bool vec, const RmsNormBwdArgs &a, const DeviceInfo &dev,
+                      cudaStream_t s) {
+  constexpr int NV = VecWidth<T>::value;
+  const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1);
+  const bool has_rstd = a.rstd != nullptr;
+  if (p.generic)
+    return has_rstd ? bwd_generic<T, Idx, true>(a, dev, s) : bwd_generic<T, Idx, false>(a, dev, s);
+  if (vec)
+    return has_rstd ? bwd_rows<T, Idx, NV, true>(p, a, dev, s)
+                    : bwd_rows<T, Idx, NV, false>(p, a, dev, s);
+  return has_rstd ? bwd_rows<T, Idx, 1, true>(p, a, dev, s)
+                  : bwd_rows<T, Idx, 1, false>(p, a, dev, s);
+}
+
+}  // namespace
+
+int64_t rmsnorm_bwd_partial_rows(int64_t T, const DeviceInfo &dev) {
+  const int64_t cap = (int64_t)dev.sms * kMaxBlocksPerSm;
+  return T < cap ? T : cap;
+}
+
+cudaError_t launch_rmsnorm_bwd(DType dt, bool vec, bool wide, const RmsNormBwdArgs &a,
+                               const DeviceInfo &dev, cudaStream_t s) {
+  if (dt == DType::F32)
+    return wide ? bwd_typed<float, int64_t>(vec, a, dev, s)
+                : bwd_typed<float, int32_t>(vec, a, dev, s);
+  return wide ? bwd_typed<bf16, int64_t>(vec, a, dev, s)
+              : bwd_typed<bf16, int32_t>(vec, a, dev, s);
+}
+
+}  // namespace ftk

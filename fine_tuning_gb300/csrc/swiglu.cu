@@ -1,0 +1,160 @@
+// SwiGLU forward and backward, elementwise over T rows of I features
+// (Chronicals, arXiv 2601.02609, abstract, optimisation (1): fused SwiGLU;
+// the page gives no formula, these are the standard definitions):
+//   forward:   h  = silu(g) * u = g * s * u,   s = sigmoid(g) = 1 / (1 + e^-g)
+//   backward:  dg = dh * u * s * (1 + g * (1 - s)),   du = dh * g * s
+//
+// Every input element is read once and every output written once.  A thread
+// moves U 16-byte packets of each operand per launch, all loads issued before
+// any arithmetic so that U * (operands) packets are in flight per thread.
+// Rows may be strided (ld >= I) so a fused [T, 2I] gate_up buffer can be
+// passed as two views; the contiguous case skips the row arithmetic.
+#include "common.cuh"
+#include "launch.h"
+
+namespace ftk {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float sigmoid(float g) {
+  return __frcp_rn(1.0f + expf(-g));
+}
+
+// Packet v of a [rows, ip packets] view -> element offset in a row-strided buffer.
+template <typename Idx, int N, bool CONTIG>
+__device__ __forceinline__ Idx packet_offset(Idx v, Idx ip, Idx ld) {
+  if (CONTIG) return v * N;
+  const Idx row = v / ip;
+  return row * ld + (v - row * ip) * N;
+}
+
+template <typename T, typename Idx, int N, int U, bool CONTIG>
+__global__ void __launch_bounds__(kThreads)
+swiglu_fwd_kernel(const T *g, const T *u, Idx ld_gu, T *h, Idx ld_h, Idx npk, Idx ip) {
+  const Idx base = (Idx)blockIdx.x * (kThreads * U) + threadIdx.x;
+  Packet<T, N> gv[U], uv[U];
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const Idx v = base + k * kThreads;
+    if (v < npk) {
+      const Idx o = packet_offset<Idx, N, CONTIG>(v, ip, ld_gu);
+      gv[k] = load_packet_stream<T, N>(g + o);
+      uv[k] = load_packet_stream<T, N>(u + o);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const Idx v = base + k * kThreads;
+    if (v < npk) {
+      Packet<T, N> o;
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        const float gf = gv[k].get(e);
+        o.set(e, gf * sigmoid(gf) * uv[k].get(e));
+      }
+      store_packet<T, N>(h + packet_offset<Idx, N, CONTIG>(v, ip, ld_h), o);
+    }
+  }
+}
+
+template <typename T, typename Idx, int N, int U, bool CONTIG>
+__global__ void __launch_bounds__(kThreads)
+swiglu_bwd_kernel(const T *dh, Idx ld_dh, const T *g, const T *u, Idx ld_gu, T *dg, T *du,
+                  Idx ld_dgu, Idx npk, Idx ip) {
+  const Idx base = (Idx)blockIdx.x * (kThreads * U) + threadIdx.x;
+  Packet<T, N> hv[U], gv[U], uv[U];
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const Idx v = base + k * kThreads;
+    if (v < npk) {
+      const Idx o = packet_offset<Idx, N, CONTIG>(v, ip, ld_gu);
+      hv[k] = load_packet_stream<T, N>(dh + packet_offset<Idx, N, CONTIG>(v, ip, ld_dh));
+      gv[k] = load_packet_stream<T, N>(g + o);
+      uv[k] = load_packet_stream<T, N>(u + o);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const Idx v = base + k * kThreads;
+    if (v < npk) {
+      Packet<T, N> og, ou;
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        const float gf = gv[k].get(e), uf = uv[k].get(e), hf = hv[k].get(e);
+        const float s = sigmoid(gf);
+        og.set(e, hf * uf * (s * fmaf(gf, 1.0f - s, 1.0f)));
+        ou.set(e, hf * (gf * s));
+      }
+      const Idx o = packet_offset<Idx, N, CONTIG>(v, ip, ld_dgu);
+      store_packet<T, N>(dg + o, og);
+      store_packet<T, N>(du + o, ou);
+    }
+  }
+}
+
+template <typename T, typename Idx, int N, int U, bool CONTIG>
+cudaError_t fwd_launch(const SwigluFwdArgs &a, cudaStream_t s) {
+  const Idx ip = (Idx)(a.I / N);
+  const Idx npk = (Idx)a.T * ip;
+  const int64_t grid = ceil_div((int64_t)npk, (int64_t)kThreads * U);
+  swiglu_fwd_kernel<T, Idx, N, U, CONTIG><<<(unsigned)grid, kThreads, 0, s>>>(
+      (const T *)a.g, (const T *)a.u, (Idx)a.ld_gu, (T *)a.h, (Idx)a.ld_h, npk, ip);
+  return cudaGetLastError();
+}
+
+template <typename T, typename Idx, int N, int U, bool CONTIG>
+cudaError_t bwd_launch(const SwigluBwdArgs &a, cudaStream_t s) {
+  const Idx ip = (Idx)(a.I / N);
+  const Idx npk = (Idx)a.T * ip;
+  const int64_t grid = ceil_div((int64_t)npk, (int64_t)kThreads * U);
+  swiglu_bwd_kernel<T, Idx, N, U, CONTIG><<<(unsigned)grid, kThreads, 0, s>>>(
+      (const T *)a.dh, (Idx)a.ld_dh, (const T *)a.g, (const T *)a.u, (Idx)a.ld_gu, (T *)a.dg,
+      (T *)a.du, (Idx)a.ld_dgu, npk, ip);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_swiglu_fwd(DType dt, bool vec, bool wide, const SwigluFwdArgs &a,
+                              const DeviceInfo &, cudaStream_t s) {
+  constexpr int U = 4;
+  const bool contig = a.ld_gu == a.I && a.ld_h == a.I;
+#define FTK_SWIGLU_FWD(T, Idx)                                                     \
+  if (vec) {                                                                       \
+    constexpr int NV = VecWidth<T>::value;                                         \
+    return contig ? fwd_launch<T, Idx, NV, U, true>(a, s)                          \
+                  : fwd_launch<T, Idx, NV, U, false>(a, s);                        \
+  }                                                                                \
+  return contig ? fwd_launch<T, Idx, 1, U, true>(a, s) : fwd_launch<T, Idx, 1, U, false>(a, s);
+  if (dt == DType::F32) {
+    if (wide) { FTK_SWIGLU_FWD(float, int64_t) }
+    FTK_SWIGLU_FWD(float, int32_t)
+  }
+  if (wide) { FTK_SWIGLU_FWD(bf16, int64_t) }
+  FTK_SWIGLU_FWD(bf16, int32_t)
+#undef FTK_SWIGLU_FWD
+}
+
+cudaError_t launch_swiglu_bwd(DType dt, bool vec, bool wide, const SwigluBwdArgs &a,
+                              const DeviceInfo &, cudaStream_t s) {
+  constexpr int U = 2;
+  const bool contig = a.ld_dh == a.I && a.ld_gu == a.I && a.ld_dgu == a.I;
+#define FTK_SWIGLU_BWD(T, Idx)                                                     \
+  if (vec) {                                                                       \
+    constexpr int NV = VecWidth<T>::value;                                         \
+    return contig ? bwd_launch<T, Idx, NV, U, true>(a, s)                          \
+                  : bwd_launch<T, Idx, NV, U, false>(a, s);                        \
+  }                                                                                \
+  return contig ? bwd_launch<T, Idx, 1, U, true>(a, s) : bwd_launch<T, Idx, 1, U, false>(a, s);
+  if (dt == DType::F32) {
+    if (wide) { FTK_SWIGLU_BWD(float, int64_t) }
+    FTK_SWIGLU_BWD(float, int32_t)
+  }
+  if (wide) { FTK_SWIGLU_BWD(bf16, int64_t) }
+  FTK_SWIGLU_BWD(bf16, int32_t)
+#undef FTK_SWIGLU_BWD
+}
+
+}  // namespace ftk

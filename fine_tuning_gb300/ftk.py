@@ -1,0 +1,236 @@
+"""Python binding of libftk.so (the C ABI in include/ftk.h).
+
+Argument marshalling only: each function checks that its tensors are CUDA
+tensors with unit inner stride, allocates missing outputs with torch, and
+calls the C entry point of the same name on the current torch stream.  Every
+step of every op runs in the library's CUDA kernels; there is no other path.
+If libftk.so is missing this module raises ImportError on first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+F32, BF16 = 0, 1
+_DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
+
+STATUS = {0: "FTK_OK", 1: "FTK_ERR_NULL", 2: "FTK_ERR_SHAPE", 3: "FTK_ERR_ALIGN",
+          4: "FTK_ERR_DTYPE", 5: "FTK_ERR_WORKSPACE", 6: "FTK_ERR_CUDA", 7: "FTK_ERR_ALIAS"}
+
+
+class FtkError(RuntimeError):
+    def __init__(self, fn: str, status: int, lib):
+        self.status = status
+        msg = f"{fn}: {STATUS.get(status, status)} ({lib.ftk_status_str(status).decode()})"
+        if status == 6:
+            msg += f": {lib.ftk_last_cuda_error().decode()}"
+        super().__init__(msg)
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libftk.so (raises ImportError if it was never built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is missing: build it with fine_tuning_gb300.build.build() "
+            "(nvcc, sm_103a); the ftk ops have no other implementation")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i64, i32, f32, f64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                              ctypes.c_float, ctypes.c_double)
+    st, dt, sz = ctypes.c_int, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "ftk_rmsnorm_fwd": (st, [vp, i64, vp, vp, i64, vp, i64, i64, f32, dt, vp]),
+        "ftk_rmsnorm_bwd_workspace_bytes": (sz, [i64, i64, dt]),
+        "ftk_rmsnorm_bwd": (st, [vp, i64, vp, i64, vp, vp, vp, i64, vp, vp, sz, i64, i64,
+                                 f32, dt, vp]),
+        "ftk_swiglu_fwd": (st, [vp, vp, i64, vp, i64, i64, i64, dt, vp]),
+        "ftk_swiglu_bwd": (st, [vp, i64, vp, vp, i64, vp, vp, i64, i64, i64, dt, vp]),
+        "ftk_qk_rope_fwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, dt, vp]),
+        "ftk_qk_rope_bwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, dt, vp]),
+        "ftk_status_str": (ctypes.c_char_p, [st]),
+        "ftk_last_cuda_error": (ctypes.c_char_p, []),
+        "ftk_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    _lib = lib
+    return lib
+
+
+def _call(name: str, *args) -> None:
+    lib = library()
+    status = getattr(lib, name)(*args)
+    if status != 0:
+        raise FtkError(name, status, lib)
+
+
+def _code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"ftk supports float32 and bfloat16 storage, got {t.dtype}") from None
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("ftk ops take CUDA tensors (move inputs with .cuda())")
+
+
+def _rows(t: torch.Tensor, name: str) -> int:
+    """Row stride (elements) of a [rows, n] view with unit inner stride."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D [tokens, features], got {tuple(t.shape)}")
+    if t.stride(1) != 1 and t.shape[1] > 1:
+        raise ValueError(f"{name} needs unit stride along features")
+    return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], t.stride(0))
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+# ---------------------------------------------------------------- RMSNorm
+
+def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, y: Optional[torch.Tensor] = None,
+                rstd: Optional[torch.Tensor] = None, save_rstd: bool = True
+                ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """y = x * rsqrt(mean(x^2) + eps) * w over rows of x [T, H]; returns (y, rstd)."""
+    _cuda(x, w, y, rstd)
+    T, H = x.shape
+    if y is None:
+        y = torch.empty((T, H), dtype=x.dtype, device=x.device)
+    if rstd is None and save_rstd:
+        rstd = torch.empty((T,), dtype=torch.float32, device=x.device)
+    if w.dtype != x.dtype or y.dtype != x.dtype or w.numel() != H or not w.is_contiguous():
+        raise ValueError("w must be a contiguous [H] tensor and y must match x's dtype")
+    if rstd is not None and (rstd.dtype != torch.float32 or rstd.numel() != T or not rstd.is_contiguous()):
+        raise ValueError("rstd must be a contiguous fp32 [T] tensor")
+    _call("ftk_rmsnorm_fwd", _ptr(x), _rows(x, "x"), _ptr(w), _ptr(y), _rows(y, "y"),
+          _ptr(rstd), T, H, float(eps), _code(x), _stream(x))
+    return y, rstd
+
+
+def rmsnorm_bwd_workspace_bytes(T: int, H: int, dtype: torch.dtype) -> int:
+    return int(library().ftk_rmsnorm_bwd_workspace_bytes(T, H, _DTYPES[dtype]))
+
+
+def rmsnorm_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, rstd: Optional[torch.Tensor],
+                eps: float, dx: Optional[torch.Tensor] = None, dw: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Returns (dx [T, H] in x's dtype, dw [H] fp32).  rstd=None recomputes it."""
+    _cuda(dy, x, w, rstd, dx, dw, workspace)
+    T, H = x.shape
+    if dx is None:
+        dx = torch.empty((T, H), dtype=x.dtype, device=x.device)
+    if dw is None:
+        dw = torch.empty((H,), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        nbytes = max(16, rmsnorm_bwd_workspace_bytes(T, H, x.dtype))
+        workspace = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=x.device)
+    if dy.shape != x.shape or dy.dtype != x.dtype or dx.dtype != x.dtype:
+        raise ValueError("dy and dx must match x in shape and dtype")
+    if dw.dtype != torch.float32 or dw.numel() != H or not dw.is_contiguous():
+        raise ValueError("dw must be a contiguous fp32 [H] tensor")
+    _call("ftk_rmsnorm_bwd", _ptr(dy), _rows(dy, "dy"), _ptr(x), _rows(x, "x"), _ptr(w),
+          _ptr(rstd), _ptr(dx), _rows(dx, "dx"), _ptr(dw), _ptr(workspace),
+          workspace.numel() * workspace.element_size(), T, H, float(eps), _code(x), _stream(x))
+    return dx, dw
+
+
+# ----------------------------------------------------------------- SwiGLU
+
+def swiglu_fwd(g: torch.Tensor, u: torch.Tensor, h: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """h = silu(g) * u for g, u [T, I] (equal row strides, e.g. two halves of gate_up)."""
+    _cuda(g, u, h)
+    T, I = g.shape
+    if u.shape != g.shape or u.dtype != g.dtype:
+        raise ValueError("g and u must have the same shape and dtype")
+    ld = _rows(g, "g")
+    if _rows(u, "u") != ld:
+        raise ValueError("g and u must share one row stride")
+    if h is None:
+        h = torch.empty((T, I), dtype=g.dtype, device=g.device)
+    _call("ftk_swiglu_fwd", _ptr(g), _ptr(u), ld, _ptr(h), _rows(h, "h"), T, I, _code(g),
+          _stream(g))
+    return h
+
+
+def swiglu_bwd(dh: torch.Tensor, g: torch.Tensor, u: torch.Tensor,
+               dg: Optional[torch.Tensor] = None, du: Optional[torch.Tensor] = None
+               ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(dg, du) of h = silu(g) * u; dg/du may be g/u themselves (in place)."""
+    _cuda(dh, g, u, dg, du)
+    T, I = g.shape
+    ld = _rows(g, "g")
+    if _rows(u, "u") != ld or u.shape != g.shape or dh.shape != g.shape:
+        raise ValueError("dh, g and u must have one shape; g and u one row stride")
+    if dg is None and du is None:
+        dg = torch.empty((T, I), dtype=g.dtype, device=g.device)
+        du = torch.empty((T, I), dtype=g.dtype, device=g.device)
+    elif dg is None or du is None:
+        raise ValueError("pass both dg and du, or neither")
+    ldo = _rows(dg, "dg")
+    if _rows(du, "du") != ldo:
+        raise ValueError("dg and du must share one row stride")
+    _call("ftk_swiglu_bwd", _ptr(dh), _rows(dh, "dh"), _ptr(g), _ptr(u), ld, _ptr(dg), _ptr(du),
+          ldo, T, I, _code(g), _stream(g))
+    return dg, du
+
+
+# ---------------------------------------------------------------- QK-RoPE
+
+def _heads(t: Optional[torch.Tensor], name: str):
+    """(row stride, heads, head_dim) of a [T, heads, D] view with contiguous heads."""
+    if t is None:
+        return 0, 0, 0
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be [T, heads, head_dim], got {tuple(t.shape)}")
+    T, nh, D = t.shape
+    if (D > 1 and t.stride(2) != 1) or (nh > 1 and t.stride(1) != D):
+        raise ValueError(f"{name} needs contiguous heads of contiguous head_dim values")
+    return (t.stride(0) if T > 1 else nh * D), nh, D
+
+
+def _rope(name, q, k, cu_seqlens, theta):
+    _cuda(q, k, cu_seqlens)
+    ldq, Hq, Dq = _heads(q, "q")
+    ldk, Hkv, Dk = _heads(k, "k")
+    D = Dq or Dk
+    if q is not None and k is not None and (q.shape[0] != k.shape[0] or Dq != Dk or q.dtype != k.dtype):
+        raise ValueError("q and k must agree in tokens, head_dim and dtype")
+    ref = q if q is not None else k
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous int32 [B+1] device tensor")
+    _call(name, _ptr(q), ldq, _ptr(k), ldk, _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+          ref.shape[0], Hq, Hkv, D, float(theta), _code(ref), _stream(ref))
+    return q, k
+
+
+def qk_rope_fwd(q, k, cu_seqlens, theta):
+    """Rotate q [T, Hq, D] and k [T, Hkv, D] IN PLACE at packed positions; returns (q, k)."""
+    return _rope("ftk_qk_rope_fwd", q, k, cu_seqlens, theta)
+
+
+def qk_rope_bwd(dq, dk, cu_seqlens, theta):
+    """Backward of qk_rope_fwd: rotate dq, dk by -phi IN PLACE; returns (dq, dk)."""
+    return _rope("ftk_qk_rope_bwd", dq, dk, cu_seqlens, theta)
+
+
+def version() -> str:
+    return library().ftk_version().decode()

@@ -1,0 +1,177 @@
+/*
+ * ftk.h: C ABI of the fused per-token layer ops of LLM fine-tuning
+ * (RMSNorm, SwiGLU, in-place varlen QK-RoPE; forward and backward),
+ * implemented as hand-written CUDA kernels for GB300 (sm_103a).
+ *
+ * Where each op comes from:
+ *   - "Chronicals: A High-Performance Framework for LLM Fine-Tuning with
+ *     3.51x Speedup over Unsloth" (arXiv 2601.02609), abstract,
+ *     optimisation (1): fused RMSNorm, SwiGLU and QK-RoPE kernels that cut
+ *     memory traffic.  The page names the ops but prints no formula; the
+ *     standard definitions written beside each call below are used.
+ *   - "Unsloth prétend accélérer 5 fois l'entraînement des LLM avec de
+ *     nouveaux noyaux Triton et un auto-packing" (seventnews.com): the
+ *     paragraph on the fused QK RoPE kernel (Q and K rotated by ONE kernel,
+ *     in place, variable-length sequences), the paragraph on LONG_INDEXING
+ *     (64-bit offsets for 500k-token contexts) and the paragraph on
+ *     auto-packing (one 1-D token tensor plus sequence-length metadata).
+ *   - "Unsloth und NVIDIA optimieren LLM-Training um zusätzliche 25%"
+ *     (lumeric.app), item (1): packed-sequence metadata kept on the device so
+ *     no GPU-to-CPU synchronisation is needed; these calls read cu_seqlens on
+ *     the device and never synchronise.
+ *
+ * Conventions shared by every call:
+ *   - Pointers without a "host" note are DEVICE pointers.  The caller owns
+ *     every buffer; the library never allocates, frees or keeps a buffer.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream) and never synchronises the host.
+ *   - Argument errors are detected on the host before anything is launched
+ *     and returned as a status; nothing is written then.  A failed launch
+ *     returns FTK_ERR_CUDA (the CUDA error text is kept per thread, see
+ *     ftk_last_cuda_error).
+ *   - Storage dtype is FTK_F32 or FTK_BF16; arithmetic is always fp32, bf16
+ *     results are rounded to nearest even once on store.
+ *   - Tensors are row-major.  A row stride `ld*` counts ELEMENTS between the
+ *     starts of consecutive token rows; it must be >= the row length.
+ *   - Element offsets switch from 32-bit to 64-bit arithmetic automatically
+ *     when any offset reached by a call can exceed 2^31 - 1.
+ *   - 16-byte aligned pointers, and row lengths and strides that are a
+ *     multiple of 16 bytes, take the vectorised kernels; anything else takes
+ *     the element-wise kernels (still on the GPU, same results).
+ *   - T = 0 (or I = 0) is a valid empty call: FTK_OK, nothing launched.
+ */
+#ifndef FTK_H_
+#define FTK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FTK_API __attribute__((visibility("default")))
+#else
+#define FTK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* the CUDA runtime's cudaStream_t is `struct CUstream_st *` */
+typedef struct CUstream_st *ftk_stream_t;
+
+typedef enum {
+    FTK_OK = 0,
+    FTK_ERR_NULL = 1,      /* a required pointer is NULL */
+    FTK_ERR_SHAPE = 2,     /* a size or stride is negative / inconsistent */
+    FTK_ERR_ALIGN = 3,     /* a pointer is not aligned to its element size */
+    FTK_ERR_DTYPE = 4,     /* unknown dtype */
+    FTK_ERR_WORKSPACE = 5, /* workspace missing or smaller than required */
+    FTK_ERR_CUDA = 6,      /* a CUDA call failed (see ftk_last_cuda_error) */
+    FTK_ERR_ALIAS = 7      /* two buffers overlap where that is not allowed */
+} ftk_status;
+
+typedef enum { FTK_F32 = 0, FTK_BF16 = 1 } ftk_dtype;
+
+/* ------------------------------------------------------------- RMSNorm */
+
+/* Forward RMSNorm of T token rows of H features:
+ *   r[t]   = 1 / sqrt( (1/H) sum_j x[t,j]^2 + eps )
+ *   y[t,j] = x[t,j] * r[t] * w[j]
+ * x [T, ldx], y [T, ldy] (dtype), w [H] (dtype, contiguous),
+ * rstd [T] fp32 contiguous, nullable: receives r[t] for the backward pass.
+ * y may alias x exactly (ldy == ldx) for an in-place norm. */
+FTK_API ftk_status ftk_rmsnorm_fwd(const void *x, int64_t ldx, const void *w, void *y,
+                           int64_t ldy, float *rstd, int64_t T, int64_t H,
+                           float eps, ftk_dtype dtype, ftk_stream_t stream);
+
+/* Bytes of device workspace ftk_rmsnorm_bwd needs for T rows of H features
+ * of `dtype` on the CURRENT device (it depends on the device's SM count).
+ * Returns 0 when T or H is 0 or the arguments are invalid. */
+FTK_API size_t ftk_rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H,
+                                               ftk_dtype dtype);
+
+/* Backward RMSNorm (gradient of sum(dy * y) for the forward above):
+ *   c[t]    = sum_j dy[t,j] w[j] x[t,j]
+ *   dx[t,j] = r[t] w[j] dy[t,j] - r[t]^3 x[t,j] c[t] / H
+ *   dw[j]   = sum_t dy[t,j] x[t,j] r[t]          (fp32, OVERWRITTEN)
+ * dy [T, lddy], x [T, ldx], dx [T, lddx] (dtype); w [H] (dtype); dw [H]
+ * fp32; rstd [T] fp32 from the forward pass, or NULL to recompute r from x
+ * and eps.  workspace: >= ftk_rmsnorm_bwd_workspace_bytes(T, H, dtype) bytes,
+ * 16-byte aligned, contents ignored and clobbered.  dw is the sum of
+ * per-CTA fp32 partials reduced in a fixed order by a second kernel, so it
+ * is bitwise reproducible run to run on the same device.  dx may alias dy
+ * exactly (same pointer and stride). */
+FTK_API ftk_status ftk_rmsnorm_bwd(const void *dy, int64_t lddy, const void *x,
+                           int64_t ldx, const void *w, const float *rstd,
+                           void *dx, int64_t lddx, float *dw, void *workspace,
+                           size_t workspace_bytes, int64_t T, int64_t H,
+                           float eps, ftk_dtype dtype, ftk_stream_t stream);
+
+/* -------------------------------------------------------------- SwiGLU */
+
+/* Forward SwiGLU, elementwise over T rows of I features:
+ *   h = silu(g) * u = g * sigmoid(g) * u,   sigmoid(g) = 1 / (1 + e^-g)
+ * g, u: [T, ld_gu] (so a fused [T, 2I] gate_up projection can be passed as
+ * g = gu, u = gu + I, ld_gu = 2I); h: [T, ld_h]. */
+FTK_API ftk_status ftk_swiglu_fwd(const void *g, const void *u, int64_t ld_gu, void *h,
+                          int64_t ld_h, int64_t T, int64_t I, ftk_dtype dtype,
+                          ftk_stream_t stream);
+
+/* Backward SwiGLU (gradient of sum(dh * h)), s = sigmoid(g):
+ *   dg = dh * u * s * (1 + g * (1 - s)),   du = dh * g * s
+ * dh: [T, ld_dh]; g, u: [T, ld_gu]; dg, du: [T, ld_dgu].  dg may alias g and
+ * du may alias u exactly (same pointer, ld_dgu == ld_gu): every element is
+ * read before it is written by the same thread. */
+FTK_API ftk_status ftk_swiglu_bwd(const void *dh, int64_t ld_dh, const void *g,
+                          const void *u, int64_t ld_gu, void *dg, void *du,
+                          int64_t ld_dgu, int64_t T, int64_t I,
+                          ftk_dtype dtype, ftk_stream_t stream);
+
+/* ------------------------------------------------------------- QK-RoPE */
+
+/* In-place rotary embedding of Q and K together, rotate-half (NeoX) layout,
+ * over a packed batch of B variable-length sequences:
+ *   token t of sequence b (cu_seqlens[b] <= t < cu_seqlens[b+1]) sits at
+ *   position p = t - cu_seqlens[b]; for i < D/2, phi = p * theta^(-2i/D);
+ *   every head vector v of Q and K at t becomes
+ *     v[i]       <- v[i] cos(phi) - v[i+D/2] sin(phi)
+ *     v[i+D/2]   <- v[i+D/2] cos(phi) + v[i] sin(phi)
+ * q: [T, ld_q] holding Hq heads of D contiguous values per token,
+ * k: [T, ld_k] holding Hkv heads (any GQA ratio: Hq, Hkv >= 0, Hq + Hkv
+ * >= 1; q may be NULL when Hq == 0 and k when Hkv == 0).  q and k must not
+ * overlap; they may be interleaved slices of one fused QKV buffer.  cu_seqlens: DEVICE int32 [B+1], cu[0] = 0, non-decreasing,
+ * cu[B] = T; read on the device, never copied to the host.  Tokens outside
+ * every sequence are impossible when that holds; if it does not, results are
+ * unspecified but every access stays inside q and k.  0 < D <= 512, D even.
+ * The angle is formed in extended precision (position times a two-float
+ * split of theta^(-2i/D) / 2pi), so it is accurate to ~1e-7 rad at
+ * positions beyond 500k; no cos/sin table is read. */
+FTK_API ftk_status ftk_qk_rope_fwd(void *q, int64_t ld_q, void *k, int64_t ld_k,
+                           const int32_t *cu_seqlens, int32_t B, int64_t T,
+                           int32_t Hq, int32_t Hkv, int32_t D, double theta,
+                           ftk_dtype dtype, ftk_stream_t stream);
+
+/* Backward of the above on dq, dk in place: the same rotation by -phi (the
+ * transpose of the forward rotation).  Same arguments and rules. */
+FTK_API ftk_status ftk_qk_rope_bwd(void *dq, int64_t ld_q, void *dk, int64_t ld_k,
+                           const int32_t *cu_seqlens, int32_t B, int64_t T,
+                           int32_t Hq, int32_t Hkv, int32_t D, double theta,
+                           ftk_dtype dtype, ftk_stream_t stream);
+
+/* ------------------------------------------------------------ utilities */
+
+/* Static text for a status code. */
+FTK_API const char *ftk_status_str(ftk_status status);
+
+/* Text of the last CUDA error seen by a call on this host thread ("" if
+ * none).  The pointer stays valid until the next call on the thread. */
+FTK_API const char *ftk_last_cuda_error(void);
+
+/* Library version, e.g. "0.1.0". */
+FTK_API const char *ftk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FTK_H_ */

@@ -1,0 +1,54 @@
+"""Tolerance rules for comparing the CUDA results with the double oracle.
+
+Test infrastructure, like the rest of oracle/: used by tests/, by
+__graft_entry__.smoke() and by bench.py's CPU-baseline leg.
+
+Bars (fused per-token ops, fine-tuning precision targets):
+  * fp32 storage:   |gpu - ref| <= 1e-5 * s
+  * bf16 outputs:   |gpu - ref| <= 2 * ulp_bf16(ref) + 2^-17 * s
+  * fp32 dw (bf16 inputs): |gpu - ref| <= 2e-3 * |ref| + 2^-16 * s
+where s is the oracle's condition scale of the element: the sum of the
+absolute values of the terms that form it.  For outputs that cannot cancel
+(y, h, du) s = |ref| and the bars are exactly "relative 1e-5", "2 bf16 ulps"
+and "relative 2e-3".  For outputs that can cancel to ~0 (dx, dg, RoPE, dw)
+the s-term is the floor a correct fp32 computation needs.
+"""
+import numpy as np
+import torch
+
+
+def f64(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        return t.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def ulp_bf16(ref: np.ndarray) -> np.ndarray:
+    a = np.abs(ref)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def bound(ref, scale, dtype: str, kind: str = "out"):
+    ref = np.asarray(ref)
+    scale = np.abs(ref) if scale is None else np.asarray(scale)
+    if dtype == "f32":
+        return 1e-5 * scale
+    if kind == "dw":
+        return 2e-3 * np.abs(ref) + 2.0 ** -16 * scale
+    return 2.0 * ulp_bf16(ref) + 2.0 ** -17 * scale
+
+
+def assert_close(name, got, ref, scale=None, dtype="bf16", kind="out"):
+    got, ref = f64(got), np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    b = bound(ref, scale, dtype, kind)
+    err = np.abs(got - ref)
+    bad = ~(err <= b)  # NaN counts as bad
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        rows = [f"{tuple(i)}: gpu={got[tuple(i)]!r} ref={ref[tuple(i)]!r} "
+                f"err={err[tuple(i)]:.3e} bound={b[tuple(i)]:.3e}" for i in idx]
+        raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} elements out of "
+                             f"tolerance ({dtype}/{kind}):\n  " + "\n  ".join(rows))
+    return float((err / np.maximum(b, 1e-300)).max()) if err.size else 0.0

@@ -1,0 +1,142 @@
+"""Host-side checks of the C ABI, no GPU needed.
+
+The library must build, load and export every function include/ftk.h
+declares; argument errors must come back as the documented status before
+any CUDA call is made (the pointers below are never dereferenced).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ftk.h")
+
+OK, NULL, SHAPE, ALIGN, DTYPE, WORKSPACE, CUDA, ALIAS = range(8)
+F32, BF16 = 0, 1
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fine_tuning_gb300 import build
+    build.build()
+    from fine_tuning_gb300 import ftk
+    return ftk.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"FTK_API\s+[\w\s\*]+?\b(ftk_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for n in ("ftk_rmsnorm_fwd", "ftk_rmsnorm_bwd", "ftk_rmsnorm_bwd_workspace_bytes",
+              "ftk_swiglu_fwd", "ftk_swiglu_bwd", "ftk_qk_rope_fwd", "ftk_qk_rope_bwd"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_exports_nothing_undeclared(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
+                         text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l and "ftk_" in l}
+    assert exported == set(declared_functions())
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.ftk_status_str(s)
+    assert lib.ftk_version().decode().count(".") == 2
+
+
+A = 1 << 20  # a 1 MiB-aligned fake device address, never dereferenced
+
+
+def test_rmsnorm_fwd_argument_errors(lib):
+    f = lib.ftk_rmsnorm_fwd
+    assert f(A, 64, A + 4096, A + 8192, 64, None, 0, 64, 1e-6, BF16, None) == OK  # T = 0
+    assert f(A, 64, A + 4096, A + 8192, 64, None, 4, 64, 1e-6, 7, None) == DTYPE
+    assert f(A, 64, A + 4096, A + 8192, 64, None, -1, 64, 1e-6, BF16, None) == SHAPE
+    assert f(A, 63, A + 4096, A + 8192, 64, None, 4, 64, 1e-6, BF16, None) == SHAPE  # ld < H
+    assert f(A, 64, A + 4096, A + 8192, 64, None, 4, 0, 1e-6, BF16, None) == SHAPE
+    assert f(None, 64, A + 4096, A + 8192, 64, None, 4, 64, 1e-6, BF16, None) == NULL
+    assert f(A + 1, 64, A + 4096, A + 8192, 64, None, 4, 64, 1e-6, BF16, None) == ALIGN
+    assert f(A, 64, A + 4096, A + 8192, 64, A + 2, 4, 64, 1e-6, F32, None) == ALIGN
+    # y overlapping x without being x
+    assert f(A, 64, A + 4096, A + 2, 64, None, 4, 64, 1e-6, BF16, None) == ALIAS
+    # rstd inside y
+    assert f(A, 64, A + 4096, A + 8192, 64, A + 8192 + 16, 4, 64, 1e-6, BF16, None) == ALIAS
+
+
+def test_rmsnorm_bwd_argument_errors(lib):
+    f = lib.ftk_rmsnorm_bwd
+    dy, x, w, dx, dw, ws = A, A + 65536, A + 2 * 65536, A + 3 * 65536, A + 4 * 65536, A + 5 * 65536
+    args = lambda **k: [k.get("dy", dy), 64, k.get("x", x), 64, w, None, k.get("dx", dx), 64,
+                        k.get("dw", dw), k.get("ws", ws), k.get("wsb", 1 << 16),
+                        k.get("T", 4), 64, 1e-6, k.get("dt", BF16), None]
+    assert f(*args(T=0)) == OK
+    assert f(*args(dt=3)) == DTYPE
+    assert f(*args(ws=None)) == WORKSPACE
+    assert f(*args(wsb=64)) == WORKSPACE  # less than one row of partials
+    assert f(*args(dw=None)) == NULL
+    assert f(*args(ws=A + 5 * 65536 + 8)) == ALIGN
+    assert f(*args(dw=x + 16)) == ALIAS       # dw inside x
+    assert f(*args(ws=dx + 64)) == ALIAS      # workspace overlapping dx
+    assert f(*args(dx=dy + 2)) == ALIAS       # dx partially over dy
+
+
+def test_swiglu_argument_errors(lib):
+    f, b = lib.ftk_swiglu_fwd, lib.ftk_swiglu_bwd
+    g, u, h = A, A + 65536, A + 2 * 65536
+    assert f(g, u, 64, h, 64, 0, 64, BF16, None) == OK
+    assert f(g, u, 64, h, 64, 4, 0, BF16, None) == OK
+    assert f(g, u, 32, h, 64, 4, 64, BF16, None) == SHAPE
+    assert f(g, None, 64, h, 64, 4, 64, BF16, None) == NULL
+    assert f(g, u, 64, g + 2, 64, 4, 64, BF16, None) == ALIAS
+    # fused gate_up view: g and u interleave in one [T, 2I] buffer, h separate
+    assert f(g, g + 128, 128, h, 64, 0, 64, BF16, None) == OK
+    dh, dg, du = A + 3 * 65536, A + 4 * 65536, A + 5 * 65536
+    assert b(dh, 64, g, u, 64, dg, dg + 16, 64, 4, 64, BF16, None) == ALIAS  # dg/du overlap
+    assert b(dh, 64, g, u, 64, dg, du, 64, 4, 64, 9, None) == DTYPE
+
+
+def test_qk_rope_argument_errors(lib):
+    f = lib.ftk_qk_rope_fwd
+    q, k, cu = A, A + (1 << 22), A + (1 << 23)
+    ok = [q, 4 * 16, k, 2 * 16, cu, 4, 64, 4, 2, 16, 1e4, F32, None]
+
+    def call(**kw):
+        a = list(ok)
+        names = ["q", "ldq", "k", "ldk", "cu", "B", "T", "Hq", "Hkv", "D", "theta", "dt", "s"]
+        for n, v in kw.items():
+            a[names.index(n)] = v
+        return f(*a)
+
+    assert call(T=0) == OK
+    assert call(D=15) == SHAPE
+    assert call(D=0) == SHAPE
+    assert call(D=1026) == SHAPE
+    assert call(Hq=0, Hkv=0) == SHAPE
+    assert call(ldq=60) == SHAPE
+    assert call(theta=0.0) == SHAPE
+    assert call(B=0) == SHAPE
+    assert call(cu=None) == NULL
+    assert call(k=None) == NULL
+    assert call(q=q + 2) == ALIGN
+    assert call(k=q + 64) == ALIAS            # k inside q
+    # fused QKV layout: q and k interleaved with the same row stride
+    assert call(ldq=8 * 16, k=q + 4 * 16 * 4, ldk=8 * 16, T=0) == OK
+    assert call(dt=5) == DTYPE
+
+
+def test_workspace_query_rejects_bad_arguments(lib):
+    assert lib.ftk_rmsnorm_bwd_workspace_bytes(0, 64, BF16) == 0
+    assert lib.ftk_rmsnorm_bwd_workspace_bytes(16, 0, BF16) == 0
+    assert lib.ftk_rmsnorm_bwd_workspace_bytes(16, 64, 9) == 0
