@@ -19,10 +19,10 @@
 // packet slots across one half of a head times S head slots; the thread with
 // (slot s, packet j) rotates packet j of heads s, s+S, s+2S, ... (HPT heads
 // per pass).  Its loads are issued first; while they are in flight the CTA
-// finds each token's position (binary search of the device cu_seqlens, no
-// host synchronisation) and computes cos/sin of the TOK x D/2 angles once
-// into shared memory, shared by every head of the token.  No cos/sin table
-// is read from HBM.
+// copies the frequency table to shared memory, finds each token's position
+// (binary search of the device cu_seqlens, no host synchronisation) and
+// computes cos/sin of the TOK x D/2 angles once into shared memory, shared
+// by every head of the token.  No cos/sin table is read from HBM.
 //
 // The angle is formed in turns, phi / 2pi = p * f_i with f_i split on the
 // host into two floats (hi + lo, ~48 significant bits); p is split into a
@@ -90,6 +90,7 @@ qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
                Idx rows, int Hq, int NH, int D, int S, int NV, int TOK, float sgn,
                const __grid_constant__ RopeFreqs fr) {
   extern __shared__ float2 cs[];  // [TOK][D/2] (cos, sgn*sin)
+  __shared__ float2 freq[kRopeMaxHalf];  // (hi, lo) turns per position
   __shared__ int pos[kCtaThreads];
 
   const int half = D >> 1;
@@ -99,23 +100,23 @@ qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   const int slot = rem / NV, j = rem - slot * NV;
   const Idx t = (Idx)blockIdx.x * TOK + tl;
   const bool active = tl < TOK && t < rows;
+  T *const qrow = q + t * ld_q + (Idx)j * N;
+  T *const krow = k + t * ld_k + (Idx)j * N - (Idx)Hq * D;
+  auto head = [&](int h) -> T * { return (h < Hq ? qrow : krow) + (Idx)h * D; };
 
-  // pass 0: loads for the first HPT heads of this thread
+  // loads of this thread's first HPT heads go out first ...
   Packet<T, N> a[HPT], b[HPT];
-  T *ptr[HPT];
 #pragma unroll
   for (int m = 0; m < HPT; ++m) {
     const int h = m * S + slot;
-    ptr[m] = nullptr;
     if (active && h < NH) {
-      ptr[m] = (h < Hq ? q + t * ld_q + (Idx)h * D : k + t * ld_k + (Idx)(h - Hq) * D) +
-               (Idx)j * N;
-      a[m] = load_packet<T, N>(ptr[m]);
-      b[m] = load_packet<T, N>(ptr[m] + half);
+      a[m] = load_packet<T, N>(head(h));
+      b[m] = load_packet<T, N>(head(h) + half);
     }
   }
 
-  // positions, then cos/sin of every (token, frequency) of the CTA
+  // ... and while they are in flight: frequencies, positions, cos/sin
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   for (int i = threadIdx.x; i < TOK; i += blockDim.x) {
     const Idx tt = (Idx)blockIdx.x * TOK + i;
     pos[i] = tt < rows ? position_of<Idx>(tt, cu, B) : 0;
@@ -123,8 +124,9 @@ qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   __syncthreads();
   for (int e = threadIdx.x; e < TOK * half; e += blockDim.x) {
     const int tt = e / half, i = e - tt * half;
+    const float2 f = freq[i];
     float c, s;
-    rope_cos_sin(pos[tt], fr.hi[i], fr.lo[i], &c, &s);
+    rope_cos_sin(pos[tt], f.x, f.y, &c, &s);
     cs[e] = make_float2(c, sgn * s);
   }
   __syncthreads();
@@ -142,7 +144,8 @@ qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   for (int h0 = 0;; h0 += HPT * S) {
 #pragma unroll
     for (int m = 0; m < HPT; ++m) {
-      if (ptr[m] != nullptr) {
+      const int h = h0 + m * S + slot;
+      if (h < NH) {
         Packet<T, N> oa, ob;
 #pragma unroll
         for (int e = 0; e < N; ++e) {
@@ -150,22 +153,19 @@ qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
           oa.set(e, fmaf(x1, cv[e], -x2 * sv[e]));
           ob.set(e, fmaf(x2, cv[e], x1 * sv[e]));
         }
-        store_packet<T, N>(ptr[m], oa);
-        store_packet<T, N>(ptr[m] + half, ob);
+        store_packet<T, N>(head(h), oa);
+        store_packet<T, N>(head(h) + half, ob);
       }
     }
-    // heads beyond the first HPT * S (only for very wide rows)
+    // heads beyond the first HPT * S (wide rows only)
     const int next = h0 + HPT * S;
     if (next >= NH) break;
 #pragma unroll
     for (int m = 0; m < HPT; ++m) {
       const int h = next + m * S + slot;
-      ptr[m] = nullptr;
       if (h < NH) {
-        ptr[m] = (h < Hq ? q + t * ld_q + (Idx)h * D : k + t * ld_k + (Idx)(h - Hq) * D) +
-                 (Idx)j * N;
-        a[m] = load_packet<T, N>(ptr[m]);
-        b[m] = load_packet<T, N>(ptr[m] + half);
+        a[m] = load_packet<T, N>(head(h));
+        b[m] = load_packet<T, N>(head(h) + half);
       }
     }
   }
@@ -190,12 +190,14 @@ cudaError_t rope_launch(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) 
   return cudaGetLastError();
 }
 
+// Heads per thread: enough packets in flight, few enough registers that
+// three or more CTAs fit on an SM (16-byte packets: at most 4 heads).
 template <typename T, typename Idx, int N>
 cudaError_t rope_heads(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
   const int NH = a.Hq + a.Hkv;
   if (NH <= 1) return rope_launch<T, Idx, N, 1>(a, fr, s);
   if (NH <= 2) return rope_launch<T, Idx, N, 2>(a, fr, s);
-  if (NH <= 4) return rope_launch<T, Idx, N, 4>(a, fr, s);
+  if (NH <= 4 || N > 1) return rope_launch<T, Idx, N, 4>(a, fr, s);
   return rope_launch<T, Idx, N, 8>(a, fr, s);
 }
 

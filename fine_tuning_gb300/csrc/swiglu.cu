@@ -18,8 +18,15 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ float sigmoid(float g) {
-  return __frcp_rn(1.0f + expf(-g));
+// sigmoid(g) and 1 - sigmoid(g) from e = exp(-|g|), which never overflows:
+// for g >= 0, s = 1/(1+e) and 1-s = e/(1+e); for g < 0 the two swap.  Both
+// stay accurate where the other form would round to 0 or 1.
+__device__ __forceinline__ void sigmoid2(float g, float *s, float *one_minus_s) {
+  const float e = expf(-fabsf(g));
+  const float r = __frcp_rn(1.0f + e);
+  const float er = e * r;
+  *s = g >= 0.0f ? r : er;
+  *one_minus_s = g >= 0.0f ? er : r;
 }
 
 // Packet v of a [rows, ip packets] view -> element offset in a row-strided buffer.
@@ -52,7 +59,9 @@ swiglu_fwd_kernel(const T *g, const T *u, Idx ld_gu, T *h, Idx ld_h, Idx npk, Id
 #pragma unroll
       for (int e = 0; e < N; ++e) {
         const float gf = gv[k].get(e);
-        o.set(e, gf * sigmoid(gf) * uv[k].get(e));
+        float sg, sc;
+        sigmoid2(gf, &sg, &sc);
+        o.set(e, gf * sg * uv[k].get(e));
       }
       store_packet<T, N>(h + packet_offset<Idx, N, CONTIG>(v, ip, ld_h), o);
     }
@@ -83,8 +92,9 @@ swiglu_bwd_kernel(const T *dh, Idx ld_dh, const T *g, const T *u, Idx ld_gu, T *
 #pragma unroll
       for (int e = 0; e < N; ++e) {
         const float gf = gv[k].get(e), uf = uv[k].get(e), hf = hv[k].get(e);
-        const float s = sigmoid(gf);
-        og.set(e, hf * uf * (s * fmaf(gf, 1.0f - s, 1.0f)));
+        float s, sc;
+        sigmoid2(gf, &s, &sc);
+        og.set(e, hf * uf * (s * fmaf(gf, sc, 1.0f)));
         ou.set(e, hf * (gf * s));
       }
       const Idx o = packet_offset<Idx, N, CONTIG>(v, ip, ld_dgu);

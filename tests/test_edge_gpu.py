@@ -196,13 +196,14 @@ def test_swiglu_fused_gate_up_and_in_place():
 
 
 def test_swiglu_extremes():
-    g = torch.tensor([[0.0, 40.0, -40.0, 100.0, -100.0, 1e-30, -1e-30, 3.0]],
-                     dtype=torch.float32, device=DEV)
+    # +-89: e^89 overflows fp32, so sigmoid must not be formed as 1/(1+e^-g)
+    g = torch.tensor([[0.0, 40.0, -40.0, 100.0, -100.0, 1e-30, -1e-30, 3.0,
+                       -87.0, -89.0, 89.0, 20.0]], dtype=torch.float32, device=DEV)
     u = torch.full_like(g, 2.0)
     h = ftk.swiglu_fwd(g, u)
     assert_close("h extremes", h, oracle.swiglu_fwd(g.cpu(), u.cpu()), dtype="f32")
     dg, du = ftk.swiglu_bwd(torch.ones_like(g), g, u)
-    dgr, dur, dgs = oracle.swiglu_bwd(np.ones(8)[None], g.cpu(), u.cpu(), scales=True)
+    dgr, dur, dgs = oracle.swiglu_bwd(np.ones(12)[None], g.cpu(), u.cpu(), scales=True)
     assert_close("dg extremes", dg, dgr, dgs, dtype="f32")
     assert_close("du extremes", du, dur, dtype="f32")
     assert torch.isfinite(dg).all() and torch.isfinite(h).all()
