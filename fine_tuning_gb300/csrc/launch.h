@@ -19,8 +19,19 @@ struct DeviceInfo {
   int max_smem_optin = 0;  // dynamic shared memory a CTA may opt into
 };
 
-// Cached per device; the only state the library keeps.
+// Cached per device; with the status word below, the only state the
+// library keeps.
 cudaError_t current_device_info(DeviceInfo *out);
+
+// Device address of the status word (bit kStatusWaitTimeout: a bounded
+// wait in some kernel ran out); cached per device.
+cudaError_t device_status_ptr(const DeviceInfo &dev, unsigned **out);
+cudaError_t read_device_status(unsigned *flags, bool clear);
+cudaError_t launch_wait_timeout_selftest(const DeviceInfo &dev, long long limit_cycles,
+                                         cudaStream_t s);
+
+// SM clock cycles a pipeline wait may take before it gives up (~1 s).
+constexpr long long kWaitLimitCycles = 2000000000LL;
 
 // How one RMSNorm row is spread over threads: W warps per row, V packets of
 // `pack` elements per thread, R rows per CTA.  `generic` = the row does not
@@ -32,6 +43,23 @@ struct RowPlan {
   int threads() const { return generic ? 256 : 32 * W * R; }
 };
 RowPlan plan_rmsnorm_row(int64_t H, int pack);
+
+// The bulk-copy pipeline on top of a row plan: every row group owns a ring
+// of S shared-memory stages, each holding `nbuf` rows (x, or x and dy).
+// Shared memory layout: [R*S mbarriers][R*W float2 reduction slots]
+// [R*S stages of stage_bytes], stages 128-byte aligned.  S = 0 means the
+// pipeline does not fit and the register kernels are used.
+struct StagedPlan {
+  int S = 0;
+  uint32_t row_bytes = 0, stage_bytes = 0;
+  size_t off_red = 0, off_stage = 0, smem = 0;
+};
+StagedPlan plan_rmsnorm_staged(const RowPlan &p, int64_t H, int elem_bytes, int nbuf,
+                               const DeviceInfo &dev);
+
+// Resident CTAs per SM of `kernel` at this shape (cached; applies the
+// dynamic shared memory opt-in when smem > 48 KiB), capped at `cap`.
+int blocks_per_sm(const void *kernel, int threads, size_t smem, const DeviceInfo &dev, int cap);
 
 struct RmsNormFwdArgs {
   const void *x;

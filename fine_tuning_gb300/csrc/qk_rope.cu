@@ -19,10 +19,11 @@
 // packet slots across one half of a head times S head slots; the thread with
 // (slot s, packet j) rotates packet j of heads s, s+S, s+2S, ... (HPT heads
 // per pass).  Its loads are issued first; while they are in flight the CTA
-// copies the frequency table to shared memory, finds each token's position
-// (binary search of the device cu_seqlens, no host synchronisation) and
-// computes cos/sin of the TOK x D/2 angles once into shared memory, shared
-// by every head of the token.  No cos/sin table is read from HBM.
+// copies the frequency table and the sequence boundaries (cu_seqlens, read
+// on the device: no host synchronisation) to shared memory, finds each
+// token's position by binary search there and computes cos/sin of its
+// TOK x D/2 angles once into shared memory, shared by every head of the
+// token.  No cos/sin table is read from HBM.
 //
 // The angle is formed in turns, phi / 2pi = p * f_i with f_i split on the
 // host into two floats (hi + lo, ~48 significant bits); p is split into a
@@ -46,6 +47,7 @@ struct RopeFreqs {
 };
 
 constexpr int kCtaThreads = 256;
+constexpr int kCuInShared = 2048;  // cu_seqlens entries a CTA stages in shared memory
 
 __device__ __forceinline__ float frac_turns(float a) { return a - rintf(a); }
 
@@ -69,29 +71,31 @@ __device__ __forceinline__ void rope_cos_sin(int p, float fhi, float flo, float 
 // Sequence of token t: largest b < B with cu[b] <= t (zero-length sequences
 // are skipped because their boundary repeats).  Clamped to [0, B-1], so a
 // malformed cu can only give wrong positions, never a wrong address.
+// `cu` is a generic pointer: the CTA's shared-memory copy when it fits,
+// else the device array itself.
 template <typename Idx>
-__device__ __forceinline__ int position_of(Idx t, const int32_t *__restrict__ cu, int B) {
+__device__ __forceinline__ int position_of(Idx t, const int32_t *cu, int B) {
   int lo = 1, hi = B;  // first i in [1, B] with cu[i] > t
   while (lo <= hi) {
     const int mid = (lo + hi) >> 1;
-    if ((Idx)__ldg(cu + mid) <= t)
+    if ((Idx)cu[mid] <= t)
       lo = mid + 1;
     else
       hi = mid - 1;
   }
   int b = lo - 1;
   b = b < 0 ? 0 : (b > B - 1 ? B - 1 : b);
-  return (int)(t - (Idx)__ldg(cu + b));
+  return (int)(t - (Idx)cu[b]);
 }
 
 template <typename T, typename Idx, int N, int HPT>
-__global__ void __launch_bounds__(kCtaThreads)
+__global__ void __launch_bounds__(kCtaThreads, 3)
 qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int B,
                Idx rows, int Hq, int NH, int D, int S, int NV, int TOK, float sgn,
                const __grid_constant__ RopeFreqs fr) {
   extern __shared__ float2 cs[];  // [TOK][D/2] (cos, sgn*sin)
   __shared__ float2 freq[kRopeMaxHalf];  // (hi, lo) turns per position
-  __shared__ int pos[kCtaThreads];
+  __shared__ int32_t cu_s[kCuInShared];
 
   const int half = D >> 1;
   const int TPT = NV * S;
@@ -115,18 +119,22 @@ qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
     }
   }
 
-  // ... and while they are in flight: frequencies, positions, cos/sin
+  // ... and while they are in flight: frequencies and sequence boundaries
+  // into shared memory (one coalesced read each), then positions and
+  // cos/sin of every (token, frequency) of the CTA
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
-  for (int i = threadIdx.x; i < TOK; i += blockDim.x) {
-    const Idx tt = (Idx)blockIdx.x * TOK + i;
-    pos[i] = tt < rows ? position_of<Idx>(tt, cu, B) : 0;
-  }
+  const bool cu_staged = B < kCuInShared;
+  if (cu_staged)
+    for (int i = threadIdx.x; i <= B; i += blockDim.x) cu_s[i] = __ldg(cu + i);
   __syncthreads();
+  const int32_t *bounds = cu_staged ? cu_s : cu;
   for (int e = threadIdx.x; e < TOK * half; e += blockDim.x) {
     const int tt = e / half, i = e - tt * half;
+    const Idx tok = (Idx)blockIdx.x * TOK + tt;
+    const int p = tok < rows ? position_of<Idx>(tok, bounds, B) : 0;
     const float2 f = freq[i];
     float c, s;
-    rope_cos_sin(pos[tt], f.x, f.y, &c, &s);
+    rope_cos_sin(p, f.x, f.y, &c, &s);
     cs[e] = make_float2(c, sgn * s);
   }
   __syncthreads();
@@ -190,15 +198,25 @@ cudaError_t rope_launch(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) 
   return cudaGetLastError();
 }
 
-// Heads per thread: enough packets in flight, few enough registers that
-// three or more CTAs fit on an SM (16-byte packets: at most 4 heads).
+// Heads per thread: as many packets in flight as fit in the 80 registers
+// that let three CTAs share an SM (bf16 16-byte packets: 2 heads; fp32: 4;
+// element-wise: 8).
 template <typename T, typename Idx, int N>
 cudaError_t rope_heads(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
+  constexpr int kMaxHpt = N >= 8 ? 2 : (N >= 4 ? 4 : 8);
   const int NH = a.Hq + a.Hkv;
   if (NH <= 1) return rope_launch<T, Idx, N, 1>(a, fr, s);
-  if (NH <= 2) return rope_launch<T, Idx, N, 2>(a, fr, s);
-  if (NH <= 4 || N > 1) return rope_launch<T, Idx, N, 4>(a, fr, s);
-  return rope_launch<T, Idx, N, 8>(a, fr, s);
+  if constexpr (kMaxHpt == 2) {
+    return rope_launch<T, Idx, N, 2>(a, fr, s);
+  } else {
+    if (NH <= 2) return rope_launch<T, Idx, N, 2>(a, fr, s);
+    if constexpr (kMaxHpt == 4) {
+      return rope_launch<T, Idx, N, 4>(a, fr, s);
+    } else {
+      if (NH <= 4) return rope_launch<T, Idx, N, 4>(a, fr, s);
+      return rope_launch<T, Idx, N, 8>(a, fr, s);
+    }
+  }
 }
 
 template <typename T, typename Idx>

@@ -181,7 +181,12 @@ static int64_t position_of(int64_t t, const int32_t *cu, int32_t B)
  *   phi_i = p * theta^(-2i/D),  i < D/2
  *   (v_i, v_{i+D/2}) <- (v_i cos phi - v_{i+D/2} sin phi,
  *                        v_{i+D/2} cos phi + v_i sin phi)
- * sign = -1 rotates by -phi (the transpose, used by the backward pass). */
+ * sign = -1 rotates by -phi (the transpose, used by the backward pass).
+ * Condition scale of each output: its two terms, where cos phi and sin phi
+ * each count with their sensitivity to the angle reduced to [-pi, pi]
+ * (|cos| + |phi_r sin| and |sin| + |phi_r cos|): no finite-precision angle
+ * is exact, and near cos phi = 0 the output moves with the angle even
+ * though the term itself is ~0. */
 static void rotate_head(const double *v, double *out, double *scale,
                         int64_t p, int32_t D, double theta, int sign)
 {
@@ -194,8 +199,10 @@ static void rotate_head(const double *v, double *out, double *scale,
         out[i] = a * c - b * s;
         out[i + half] = b * c + a * s;
         if (scale) {
-            scale[i] = fabs(a * c) + fabs(b * s);
-            scale[i + half] = fabs(b * c) + fabs(a * s);
+            double r = fabs(remainder(phi, 6.283185307179586476925));
+            double cc = fabs(c) + r * fabs(s), ss = fabs(s) + r * fabs(c);
+            scale[i] = fabs(a) * cc + fabs(b) * ss;
+            scale[i + half] = fabs(b) * cc + fabs(a) * ss;
         }
     }
 }

@@ -278,6 +278,18 @@ def test_rope_bwd_is_transpose_and_inverse():
     np.testing.assert_allclose(ki, k, atol=1e-13)
 
 
+def test_rope_scale_bounds_output_and_is_unchanged_by_it():
+    cu, q, k = _packed_case(D=32)
+    qo, ko = oracle.qk_rope(q, k, cu, 1e4)
+    qs_, ks_, qsc, ksc = oracle.qk_rope(q, k, cu, 1e4, scales=True)
+    np.testing.assert_array_equal(qo, qs_)
+    np.testing.assert_array_equal(ko, ks_)
+    assert np.all(np.abs(qo) <= qsc * (1 + 1e-12))
+    assert np.all(np.abs(ko) <= ksc * (1 + 1e-12))
+    # at a token's own position 0 the scale is the plain |x| (no angle)
+    np.testing.assert_allclose(qsc[0], np.abs(q[0]), rtol=1e-15)
+
+
 def test_rope_sampled_rows_equal_full():
     cu, q, k = _packed_case()
     qo, ko = oracle.qk_rope(q, k, cu, 1e4)
