@@ -107,6 +107,29 @@ FTK_API ftk_status ftk_rmsnorm_bwd(const void *dy, int64_t lddy, const void *x,
                            size_t workspace_bytes, int64_t T, int64_t H,
                            float eps, ftk_dtype dtype, ftk_stream_t stream);
 
+/* Same operation, arguments and results as ftk_rmsnorm_bwd, for callers
+ * that cannot allocate device memory (for example code that runs inside a
+ * fixed memory pool or a runtime that forbids cudaMalloc after start-up, or
+ * a plugin that is handed only input and output pointers).  The pages have
+ * no counterpart: it exists for those callers only.  Instead of a workspace
+ * it uses a 4 MiB scratch array built into the library (held by every device
+ * that loads the library until the process exits); it allocates nothing.
+ *   - H must be <= 1,048,576 (one row of fp32 partial sums must fit in the
+ *     scratch), else FTK_ERR_WORKSPACE; larger H values leave fewer partial
+ *     rows, hence fewer CTAs, than ftk_rmsnorm_bwd would use.
+ *   - The first call on a device looks up the scratch array's device
+ *     address and caches it; make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the scratch and leaves its contents
+ *     behind; nothing in it needs clearing (each call writes every partial
+ *     row it sums).  Calls that overlap on the GPU race on it: serialise
+ *     them. */
+FTK_API ftk_status ftk_rmsnorm_bwd_noalloc(const void *dy, int64_t lddy, const void *x,
+                                           int64_t ldx, const void *w, const float *rstd,
+                                           void *dx, int64_t lddx, float *dw, int64_t T,
+                                           int64_t H, float eps, ftk_dtype dtype,
+                                           ftk_stream_t stream);
+
 /* -------------------------------------------------------------- SwiGLU */
 
 /* Forward SwiGLU, elementwise over T rows of I features:
