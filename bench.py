@@ -446,6 +446,7 @@ def run_ours(args):
         "wall_ms_timed_region": round(wall_ms, 3),
     }
     out["clocks"] = sampler.summary(t0, t1)
+    out["device_status"] = ftk.device_status(clear=True)  # 0: no pipeline wait ran out
 
     if not args.no_e2e:
         out["e2e"] = e2e_leg(batch, ops, dev, args.e2e_steps, step_bytes)

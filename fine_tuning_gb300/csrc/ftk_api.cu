@@ -120,6 +120,23 @@ FTK_API const char *ftk_status_str(ftk_status s) {
 
 FTK_API const char *ftk_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
+FTK_API ftk_status ftk_device_status(uint32_t *flags, int clear) {
+  if (!flags) return FTK_ERR_NULL;
+  unsigned v = 0;
+  cudaError_t e = ftk::read_device_status(&v, clear != 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *flags = v;
+  return FTK_OK;
+}
+
+FTK_API ftk_status ftk_selftest_wait_timeout(int64_t limit_cycles, ftk_stream_t stream) {
+  if (limit_cycles < 0) return FTK_ERR_SHAPE;
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return finish(ftk::launch_wait_timeout_selftest(dev, limit_cycles, (cudaStream_t)stream));
+}
+
 // ------------------------------------------------------------------ RMSNorm
 
 FTK_API ftk_status ftk_rmsnorm_fwd(const void *x, int64_t ldx, const void *w, void *y,

@@ -57,8 +57,9 @@ struct StagedPlan {
 StagedPlan plan_rmsnorm_staged(const RowPlan &p, int64_t H, int elem_bytes, int nbuf,
                                const DeviceInfo &dev);
 
-// Resident CTAs per SM of `kernel` at this shape (cached; applies the
-// dynamic shared memory opt-in when smem > 48 KiB), capped at `cap`.
+// Resident CTAs per SM of `kernel` at this shape, capped at `cap` (cached).
+// Also lifts the kernel's dynamic shared memory limit to the device maximum
+// the first time it sees the kernel on a device.
 int blocks_per_sm(const void *kernel, int threads, size_t smem, const DeviceInfo &dev, int cap);
 
 struct RmsNormFwdArgs {

@@ -179,6 +179,157 @@ qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   }
 }
 
+// 16-byte aligned rows: a persistent grid over blocks of TB tokens.  Each
+// CTA keeps a ring of S shared-memory stages, each holding one block's Q
+// rows then K rows.  Thread 0 bulk-loads the blocks ahead (cp.async.bulk
+// completing on one mbarrier per stage); while a block lands the CTA
+// computes its positions and cos/sin; the warps rotate it in shared memory;
+// thread 0 bulk-stores it back in place and, once that store has read the
+// stage, refills the stage with the block S iterations ahead.
+template <typename T, typename Idx, int N>
+__global__ void __launch_bounds__(kCtaThreads)
+qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int B, Idx rows,
+               int Hq, int Hkv, int D, int TB, int S, float sgn, uint32_t off_cs,
+               uint32_t off_stage, uint32_t stage_bytes, unsigned *status, long long wait_limit,
+               const __grid_constant__ RopeFreqs fr) {
+  extern __shared__ __align__(128) unsigned char sbuf[];
+  __shared__ float2 freq[kRopeMaxHalf];
+  __shared__ int32_t cu_s[kCuInShared];
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf);          // [S]
+  float2 *cs = reinterpret_cast<float2 *>(sbuf + off_cs);        // [TB][D/2]
+  unsigned char *stages = sbuf + off_stage;                     // [S][stage_bytes]
+
+  const int half = D >> 1, NV = half / N, NH = Hq + Hkv;
+  const Idx nblocks = (rows + TB - 1) / TB;
+  const size_t qrow_b = (size_t)Hq * D * sizeof(T), krow_b = (size_t)Hkv * D * sizeof(T);
+  const bool q_contig = ld_q == (Idx)Hq * D, k_contig = ld_k == (Idx)Hkv * D;
+
+  for (int i = threadIdx.x; i < S; i += blockDim.x) mbar_init(&bars[i], 1);
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  const bool cu_staged = B < kCuInShared;
+  if (cu_staged)
+    for (int i = threadIdx.x; i <= B; i += blockDim.x) cu_s[i] = __ldg(cu + i);
+  if (threadIdx.x == 0) fence_mbar_init();
+  __syncthreads();
+  const int32_t *bounds = cu_staged ? cu_s : cu;
+
+  // block b <-> stage s: Q rows [TB][Hq*D] then K rows [TB][Hkv*D]
+  auto load = [&](int s, Idx b) {
+    const Idx t0 = b * TB;
+    const int nt = (int)((rows - t0) < (Idx)TB ? (rows - t0) : (Idx)TB);
+    unsigned char *st = stages + (size_t)s * stage_bytes;
+    mbar_arrive_expect_tx(&bars[s], (uint32_t)(nt * (qrow_b + krow_b)));
+    if (qrow_b) {
+      if (q_contig)
+        bulk_copy_g2s(st, q + t0 * ld_q, (uint32_t)(nt * qrow_b), &bars[s]);
+      else
+        for (int i = 0; i < nt; ++i)
+          bulk_copy_g2s(st + i * qrow_b, q + (t0 + i) * ld_q, (uint32_t)qrow_b, &bars[s]);
+    }
+    if (krow_b) {
+      unsigned char *sk = st + (size_t)TB * qrow_b;
+      if (k_contig)
+        bulk_copy_g2s(sk, k + t0 * ld_k, (uint32_t)(nt * krow_b), &bars[s]);
+      else
+        for (int i = 0; i < nt; ++i)
+          bulk_copy_g2s(sk + i * krow_b, k + (t0 + i) * ld_k, (uint32_t)krow_b, &bars[s]);
+    }
+  };
+  auto store = [&](int s, Idx b) {
+    const Idx t0 = b * TB;
+    const int nt = (int)((rows - t0) < (Idx)TB ? (rows - t0) : (Idx)TB);
+    const unsigned char *st = stages + (size_t)s * stage_bytes;
+    if (qrow_b) {
+      if (q_contig)
+        bulk_copy_s2g(q + t0 * ld_q, st, (uint32_t)(nt * qrow_b));
+      else
+        for (int i = 0; i < nt; ++i)
+          bulk_copy_s2g(q + (t0 + i) * ld_q, st + i * qrow_b, (uint32_t)qrow_b);
+    }
+    if (krow_b) {
+      const unsigned char *sk = st + (size_t)TB * qrow_b;
+      if (k_contig)
+        bulk_copy_s2g(k + t0 * ld_k, sk, (uint32_t)(nt * krow_b));
+      else
+        for (int i = 0; i < nt; ++i)
+          bulk_copy_s2g(k + (t0 + i) * ld_k, sk + i * krow_b, (uint32_t)krow_b);
+    }
+    bulk_commit_group();
+  };
+
+  const bool leader = threadIdx.x == 0;
+  int issued = 0;
+  if (leader)
+    for (int i = 0; i < S; ++i) {
+      const Idx b = (Idx)blockIdx.x + (Idx)i * gridDim.x;
+      if (b >= nblocks) break;
+      load(i, b);
+      ++issued;
+    }
+
+  bool live = true;
+  int it = 0;
+  for (Idx b = blockIdx.x; b < nblocks; b += gridDim.x, ++it) {
+    const int s = it % S;
+    const Idx t0 = b * TB;
+    const int nt = (int)((rows - t0) < (Idx)TB ? (rows - t0) : (Idx)TB);
+    // cos/sin of this block while its rows land
+    for (int e = threadIdx.x; e < nt * half; e += blockDim.x) {
+      const int tt = e / half, i = e - tt * half;
+      const int p = position_of<Idx>(t0 + tt, bounds, B);
+      const float2 f = freq[i];
+      float c, sn;
+      rope_cos_sin(p, f.x, f.y, &c, &sn);
+      cs[e] = make_float2(c, sgn * sn);
+    }
+    if (live) live = mbar_wait_bounded(&bars[s], (uint32_t)((it / S) & 1), wait_limit, status);
+    __syncthreads();
+    unsigned char *st = stages + (size_t)s * stage_bytes;
+    const int items = nt * NH * NV;
+    for (int m = threadIdx.x; m < items; m += blockDim.x) {
+      const int j = m % NV, rest = m / NV;
+      const int h = rest % NH, tt = rest / NH;
+      T *v = reinterpret_cast<T *>(h < Hq ? st + ((size_t)tt * Hq + h) * D * sizeof(T)
+                                          : st + (size_t)TB * qrow_b +
+                                                ((size_t)tt * Hkv + (h - Hq)) * D * sizeof(T)) +
+             j * N;
+      Packet<T, N> pa = *reinterpret_cast<const Packet<T, N> *>(v);
+      Packet<T, N> pb = *reinterpret_cast<const Packet<T, N> *>(v + half);
+      const float2 *c2 = cs + tt * half + j * N;
+      Packet<T, N> oa, ob;
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        const float2 r = c2[e];
+        const float x1 = pa.get(e), x2 = pb.get(e);
+        oa.set(e, fmaf(x1, r.x, -x2 * r.y));
+        ob.set(e, fmaf(x2, r.x, x1 * r.y));
+      }
+      *reinterpret_cast<Packet<T, N> *>(v) = oa;
+      *reinterpret_cast<Packet<T, N> *>(v + half) = ob;
+    }
+    fence_proxy_async_smem();  // this thread's stage writes before the bulk store reads them
+    __syncthreads();
+    if (leader) {
+      store(s, b);
+      if (it >= 1) {
+        // the previous block's store has read its stage: refill that stage
+        bulk_wait_group_read<1>();
+        const Idx nb = b - (Idx)gridDim.x + (Idx)S * gridDim.x;
+        if (nb < nblocks) {
+          load((it - 1) % S, nb);
+          ++issued;
+        }
+      }
+    }
+  }
+  if (leader) {
+    if (!live)  // let loads still in flight land (bounded) before the CTA exits
+      for (int i = it; i < issued; ++i)
+        mbar_wait_bounded(&bars[i % S], (uint32_t)((i / S) & 1), wait_limit, status);
+    bulk_wait_group_all();
+  }
+}
+
 template <typename T, typename Idx, int N, int HPT>
 cudaError_t rope_launch(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
   const int NH = a.Hq + a.Hkv;
@@ -219,16 +370,56 @@ cudaError_t rope_heads(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
   }
 }
 
+template <typename T, typename Idx, int N>
+cudaError_t rope_staged_launch(const RopeArgs &a, const RopeFreqs &fr, const DeviceInfo &dev,
+                               cudaStream_t s, bool *launched) {
+  *launched = false;
+  const int NH = a.Hq + a.Hkv, half = a.D / 2;
+  const size_t tok_bytes = (size_t)NH * a.D * sizeof(T);
+  // ~16 KiB blocks of whole tokens, ~64 KiB of stages per CTA
+  int TB = (int)(16384 / tok_bytes);
+  TB = TB < 1 ? 1 : (TB > 32 ? 32 : TB);
+  const size_t stage_bytes = (size_t)TB * tok_bytes;
+  int S = (int)(65536 / stage_bytes);
+  S = S < 2 ? 2 : (S > 8 ? 8 : S);
+  const size_t off_cs = ((size_t)S * 8 + 15) / 16 * 16;
+  const size_t off_stage = (off_cs + (size_t)TB * half * sizeof(float2) + 127) / 128 * 128;
+  const size_t smem = off_stage + (size_t)S * stage_bytes;
+  const size_t static_smem = sizeof(float2) * kRopeMaxHalf + sizeof(int32_t) * kCuInShared;
+  if (smem + static_smem > (size_t)dev.max_smem_optin || stage_bytes >= (1u << 20)) return cudaSuccess;
+  auto kern = qk_rope_staged<T, Idx, N>;
+  const int occ = blocks_per_sm((const void *)kern, kCtaThreads, smem, dev, 8);
+  const int64_t nblocks = ceil_div(a.T, (int64_t)TB);
+  int64_t P = (int64_t)dev.sms * occ;
+  if (P > nblocks) P = nblocks;
+  unsigned *status = nullptr;
+  cudaError_t e = device_status_ptr(dev, &status);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)P, kCtaThreads, smem, s>>>(
+      (T *)a.q, (Idx)a.ld_q, (T *)a.k, (Idx)a.ld_k, a.cu, a.B, (Idx)a.T, a.Hq, a.Hkv, a.D, TB, S,
+      a.backward ? -1.0f : 1.0f, (uint32_t)off_cs, (uint32_t)off_stage, (uint32_t)stage_bytes,
+      status, kWaitLimitCycles, fr);
+  *launched = true;
+  return cudaGetLastError();
+}
+
 template <typename T, typename Idx>
-cudaError_t rope_typed(bool vec, const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
+cudaError_t rope_typed(bool vec, const RopeArgs &a, const RopeFreqs &fr, const DeviceInfo &dev,
+                       cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
-  return vec ? rope_heads<T, Idx, NV>(a, fr, s) : rope_heads<T, Idx, 1>(a, fr, s);
+  if (vec) {
+    bool launched = false;
+    cudaError_t e = rope_staged_launch<T, Idx, NV>(a, fr, dev, s, &launched);
+    if (e != cudaSuccess || launched) return e;
+    return rope_heads<T, Idx, NV>(a, fr, s);
+  }
+  return rope_heads<T, Idx, 1>(a, fr, s);
 }
 
 }  // namespace
 
-cudaError_t launch_qk_rope(DType dt, bool vec, bool wide, const RopeArgs &a, const DeviceInfo &,
-                           cudaStream_t s) {
+cudaError_t launch_qk_rope(DType dt, bool vec, bool wide, const RopeArgs &a,
+                           const DeviceInfo &dev, cudaStream_t s) {
   // f_i = theta^(-2i/D) / (2 pi) in double, split into two floats.
   RopeFreqs fr;
   const int half = a.D / 2;
@@ -243,8 +434,10 @@ cudaError_t launch_qk_rope(DType dt, bool vec, bool wide, const RopeArgs &a, con
     }
   }
   if (dt == DType::F32)
-    return wide ? rope_typed<float, int64_t>(vec, a, fr, s) : rope_typed<float, int32_t>(vec, a, fr, s);
-  return wide ? rope_typed<bf16, int64_t>(vec, a, fr, s) : rope_typed<bf16, int32_t>(vec, a, fr, s);
+    return wide ? rope_typed<float, int64_t>(vec, a, fr, dev, s)
+                : rope_typed<float, int32_t>(vec, a, fr, dev, s);
+  return wide ? rope_typed<bf16, int64_t>(vec, a, fr, dev, s)
+              : rope_typed<bf16, int32_t>(vec, a, fr, dev, s);
 }
 
 }  // namespace ftk

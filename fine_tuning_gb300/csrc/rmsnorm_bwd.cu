@@ -5,18 +5,19 @@
 // (Chronicals, arXiv 2601.02609, abstract, optimisation (1): fused RMSNorm;
 // the page gives no formula, this is the standard gradient.)
 //
-// Pass 1 (rmsnorm_bwd_rows): a persistent grid of P CTAs walks the rows with
-// a fixed stride.  Each thread keeps its slice of w in registers for the
-// whole kernel and accumulates dy*x*r for its columns in fp32 registers over
-// the rows its group visits.  At the end the R row groups of a CTA are summed
-// in shared memory in a fixed order and the CTA writes one fp32 row of
-// partials to the workspace.
+// Pass 1: a persistent grid of P CTAs walks the rows with a fixed stride.
+// Each thread keeps its slice of w in registers for the whole kernel and
+// accumulates dy*x*r for its columns in fp32 registers over the rows its
+// group visits.  At the end the R row groups of a CTA are summed in shared
+// memory in a fixed order and the CTA writes one fp32 row of partials to the
+// workspace.  For 16-byte aligned rows (rmsnorm_bwd_staged) one elected
+// thread per row group streams the next S rows of x and dy into a ring of
+// shared-memory stages with bulk copies (cp.async.bulk, completing on
+// mbarriers) and the warps compute from shared memory; other rows hold their
+// packets in registers (rmsnorm_bwd_rows).
 // Pass 2 (dw_reduce): dw[j] = sum_p ws[p, j], rows in a fixed order.
 // The row -> CTA map and every summation order are fixed, so dw is bitwise
 // reproducible; no CTA ever waits on another.
-#include <mutex>
-#include <vector>
-
 #include "common.cuh"
 #include "launch.h"
 
@@ -148,6 +149,160 @@ rmsnorm_bwd_rows(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restrict
   }
 }
 
+template <typename T, typename Idx, int N, int V, bool HAS_RSTD>
+__global__ void __launch_bounds__(256)
+rmsnorm_bwd_staged(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restrict__ w,
+                   const float *__restrict__ rstd, T *dx, Idx lddx, float *__restrict__ ws,
+                   Idx rows, int hp, int H, float inv_h, float eps, int W, int R, int S,
+                   uint32_t off_red, uint32_t off_stage, uint32_t row_bytes, unsigned *status,
+                   long long wait_limit) {
+  extern __shared__ __align__(128) unsigned char sbuf[];
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf);  // [R][S]
+  float2 *red = reinterpret_cast<float2 *>(sbuf + off_red);  // [R][W]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / W, wig = warp - grp * W;
+  const int gi = wig * 32 + lane, G = W * 32;
+  const bool leader = gi == 0;
+  const uint32_t stage_bytes = 2 * row_bytes;  // x row, then dy row
+
+  for (int i = threadIdx.x; i < R * S; i += blockDim.x) mbar_init(&bars[i], 1);
+  if (threadIdx.x == 0) fence_mbar_init();
+  __syncthreads();
+
+  uint64_t *gb = bars + grp * S;
+  unsigned char *ring = sbuf + off_stage + (size_t)grp * S * stage_bytes;
+  const Idx stride = (Idx)gridDim.x * R;
+  const Idx first = (Idx)blockIdx.x * R + grp;
+
+  auto issue = [&](int s, Idx row) {
+    unsigned char *st = ring + (size_t)s * stage_bytes;
+    mbar_arrive_expect_tx(&gb[s], stage_bytes);
+    bulk_copy_g2s(st, x + row * ldx, row_bytes, &gb[s]);
+    bulk_copy_g2s(st + row_bytes, dy + row * lddy, row_bytes, &gb[s]);
+  };
+  int issued = 0;
+  if (leader) {
+    for (int s = 0; s < S; ++s) {
+      const Idx row = first + (Idx)s * stride;
+      if (row >= rows) break;
+      issue(s, row);
+      ++issued;
+    }
+  }
+  Packet<T, N> wv[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int c = gi + k * G;
+    if (c < hp) wv[k] = load_packet<T, N>(w + (Idx)c * N);
+  }
+  float acc[V][N];
+#pragma unroll
+  for (int k = 0; k < V; ++k)
+#pragma unroll
+    for (int e = 0; e < N; ++e) acc[k][e] = 0.f;
+
+  bool live = true;
+  int it = 0;
+  for (Idx row = first; row < rows; row += stride, ++it) {
+    const int s = it % S;
+    float r = HAS_RSTD ? rstd[row] : 0.f;
+    if (live) live = mbar_wait_bounded(&gb[s], (uint32_t)((it / S) & 1), wait_limit, status);
+    const T *xs = reinterpret_cast<const T *>(ring + (size_t)s * stage_bytes);
+    const T *gs = reinterpret_cast<const T *>(ring + (size_t)s * stage_bytes + row_bytes);
+    float2 cs = make_float2(0.f, 0.f);  // (sum dy*w*x, sum x*x)
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const int c = gi + k * G;
+      if (c < hp) {
+        const Packet<T, N> xv = *reinterpret_cast<const Packet<T, N> *>(xs + c * N);
+        const Packet<T, N> gv = *reinterpret_cast<const Packet<T, N> *>(gs + c * N);
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float xf = xv.get(e);
+          cs.x = fmaf(gv.get(e) * wv[k].get(e), xf, cs.x);
+          if (!HAS_RSTD) cs.y = fmaf(xf, xf, cs.y);
+        }
+      }
+    }
+    if (HAS_RSTD)
+      cs.x = warp_sum(cs.x);
+    else
+      cs = warp_sum2(cs);
+    if (W > 1) {
+      if (lane == 0) red[grp * W + wig] = cs;
+      named_barrier(1 + grp, G);
+      cs = make_float2(0.f, 0.f);
+      for (int i = 0; i < W; ++i) {
+        cs.x += red[grp * W + i].x;
+        cs.y += red[grp * W + i].y;
+      }
+    }
+    if (!HAS_RSTD) r = rsqrtf(fmaf(cs.y, inv_h, eps));
+    const float a = r * r * r * cs.x * inv_h;
+    T *dr = dx + row * lddx;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const int c = gi + k * G;
+      if (c < hp) {
+        const Packet<T, N> xv = *reinterpret_cast<const Packet<T, N> *>(xs + c * N);
+        const Packet<T, N> gv = *reinterpret_cast<const Packet<T, N> *>(gs + c * N);
+        Packet<T, N> o;
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float xf = xv.get(e), gf = gv.get(e);
+          o.set(e, fmaf(-a, xf, r * wv[k].get(e) * gf));
+          acc[k][e] = fmaf(gf * xf, r, acc[k][e]);
+        }
+        store_packet<T, N>(dr + (Idx)c * N, o);
+      }
+    }
+    if (W > 1)
+      named_barrier(1 + grp, G);
+    else
+      __syncwarp();
+    if (leader) {
+      const Idx next = row + (Idx)S * stride;
+      if (next < rows) {
+        fence_proxy_async_smem();
+        issue(s, next);
+        ++issued;
+      }
+    }
+  }
+  if (leader && !live)
+    for (int i = it; i < issued; ++i)
+      mbar_wait_bounded(&gb[i % S], (uint32_t)((i / S) & 1), wait_limit, status);
+
+  float *dst = ws + (size_t)blockIdx.x * H;
+  if (R == 1) {
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const int c = gi + k * G;
+      if (c < hp)
+#pragma unroll
+        for (int e = 0; e < N; ++e) dst[c * N + e] = acc[k][e];
+    }
+    return;
+  }
+  // the stages are free now: combine the R groups there in a fixed order
+  __syncthreads();
+  float *part = reinterpret_cast<float *>(sbuf + off_stage);
+  float *mine = part + grp * H;
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int c = gi + k * G;
+    if (c < hp)
+#pragma unroll
+      for (int e = 0; e < N; ++e) mine[c * N + e] = acc[k][e];
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < H; j += blockDim.x) {
+    float sum = 0.f;
+    for (int g = 0; g < R; ++g) sum += part[g * H + j];
+    dst[j] = sum;
+  }
+}
+
 // Rows too long for registers: one CTA per row at a time, persistent grid,
 // two passes over the row; the CTA's dw partial row lives in the workspace
 // and is updated in place (each CTA owns its row, so no atomics).
@@ -211,38 +366,6 @@ dw_reduce(const float *__restrict__ ws, int P, int H, float *__restrict__ dw) {
   }
 }
 
-// Resident CTAs per SM of one kernel instance at one launch shape, cached
-// per (kernel, device, shared memory); capped at kMaxBlocksPerSm.
-struct OccEntry {
-  const void *kernel;
-  int device, threads;
-  size_t smem;
-  int blocks;
-};
-std::mutex g_occ_mutex;
-std::vector<OccEntry> g_occ;
-
-int blocks_per_sm(const void *kernel, int threads, size_t smem, const DeviceInfo &dev) {
-  {
-    std::lock_guard<std::mutex> lock(g_occ_mutex);
-    for (const OccEntry &e : g_occ)
-      if (e.kernel == kernel && e.device == dev.device && e.threads == threads && e.smem == smem)
-        return e.blocks;
-  }
-  int n = 0;
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess ||
-      n < 1) {
-    cudaGetLastError();
-    n = 1;
-  }
-  if (n > kMaxBlocksPerSm) n = kMaxBlocksPerSm;
-  std::lock_guard<std::mutex> lock(g_occ_mutex);
-  g_occ.push_back(OccEntry{kernel, dev.device, threads, smem, n});
-  return n;
-}
-
 template <typename T, typename Idx, int N, int V, bool HAS_RSTD>
 cudaError_t bwd_rows_v(const RowPlan &p, const RmsNormBwdArgs &a, const DeviceInfo &dev,
                        cudaStream_t s) {
@@ -250,7 +373,7 @@ cudaError_t bwd_rows_v(const RowPlan &p, const RmsNormBwdArgs &a, const DeviceIn
   const int threads = p.threads();
   const size_t smem = sizeof(float) * (4 * p.R * p.W + (p.R > 1 ? (size_t)p.R * a.H : 0));
   if (smem > (size_t)dev.max_smem_optin) return cudaErrorInvalidConfiguration;
-  const int occ = blocks_per_sm((const void *)kern, threads, smem, dev);
+  const int occ = blocks_per_sm((const void *)kern, threads, smem, dev, kMaxBlocksPerSm);
   int64_t P = ceil_div(a.T, (int64_t)p.R);
   if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
   if (P > a.ws_rows) P = a.ws_rows;
@@ -262,6 +385,43 @@ cudaError_t bwd_rows_v(const RowPlan &p, const RmsNormBwdArgs &a, const DeviceIn
   if (e != cudaSuccess) return e;
   dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 256, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
   return cudaGetLastError();
+}
+
+template <typename T, typename Idx, int N, int V, bool HAS_RSTD>
+cudaError_t bwd_staged_v(const RowPlan &p, const StagedPlan &sp, const RmsNormBwdArgs &a,
+                         const DeviceInfo &dev, cudaStream_t s) {
+  auto kern = rmsnorm_bwd_staged<T, Idx, N, V, HAS_RSTD>;
+  const int threads = p.threads();
+  const int occ = blocks_per_sm((const void *)kern, threads, sp.smem, dev, kMaxBlocksPerSm);
+  int64_t P = ceil_div(a.T, (int64_t)p.R);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  if (P > a.ws_rows) P = a.ws_rows;
+  unsigned *status = nullptr;
+  cudaError_t e = device_status_ptr(dev, &status);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)P, threads, sp.smem, s>>>(
+      (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
+      (T *)a.dx, (Idx)a.lddx, a.ws, (Idx)a.T, (int)(a.H / N), (int)a.H,
+      (float)(1.0 / (double)a.H), a.eps, p.W, p.R, sp.S, (uint32_t)sp.off_red,
+      (uint32_t)sp.off_stage, sp.row_bytes, status, kWaitLimitCycles);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 256, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
+  return cudaGetLastError();
+}
+
+template <typename T, typename Idx, int N, bool HAS_RSTD>
+cudaError_t bwd_staged(const RowPlan &p, const StagedPlan &sp, const RmsNormBwdArgs &a,
+                       const DeviceInfo &dev, cudaStream_t s) {
+  switch (p.V) {
+    case 1: return bwd_staged_v<T, Idx, N, 1, HAS_RSTD>(p, sp, a, dev, s);
+    case 2: return bwd_staged_v<T, Idx, N, 2, HAS_RSTD>(p, sp, a, dev, s);
+    case 3: return bwd_staged_v<T, Idx, N, 3, HAS_RSTD>(p, sp, a, dev, s);
+    case 4: return bwd_staged_v<T, Idx, N, 4, HAS_RSTD>(p, sp, a, dev, s);
+    case 6: return bwd_staged_v<T, Idx, N, 6, HAS_RSTD>(p, sp, a, dev, s);
+    case 8: return bwd_staged_v<T, Idx, N, 8, HAS_RSTD>(p, sp, a, dev, s);
+    default: return cudaErrorInvalidConfiguration;
+  }
 }
 
 template <typename T, typename Idx, int N, bool HAS_RSTD>
@@ -297,6 +457,12 @@ cudaError_t bwd_typed(bool vec, const RmsNormBwdArgs &a, const DeviceInfo &dev,
   constexpr int NV = VecWidth<T>::value;
   const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1);
   const bool has_rstd = a.rstd != nullptr;
+  if (vec && !p.generic) {
+    const StagedPlan sp = plan_rmsnorm_staged(p, a.H, (int)sizeof(T), 2, dev);
+    if (sp.S > 0)
+      return has_rstd ? bwd_staged<T, Idx, NV, true>(p, sp, a, dev, s)
+                      : bwd_staged<T, Idx, NV, false>(p, sp, a, dev, s);
+  }
   if (p.generic)
     return has_rstd ? bwd_generic<T, Idx, true>(a, dev, s) : bwd_generic<T, Idx, false>(a, dev, s);
   if (vec)

@@ -3,11 +3,17 @@
 // (Chronicals, arXiv 2601.02609, abstract, optimisation (1): fused RMSNorm.)
 //
 // One row is read from HBM once and written once.  A group of W warps owns a
-// row: each thread holds V packets of the row in registers, the sum of
-// squares is reduced with warp shuffles (and, for W > 1, through shared
-// memory in a fixed order), then every thread scales its own packets.  R row
-// groups share a CTA so that CTAs stay at 128-256 threads for any H.
-// Rows too long for registers take a CTA-per-row two-pass kernel.
+// row; the sum of squares is reduced with warp shuffles (and, for W > 1,
+// through shared memory in a fixed order), then every thread scales its own
+// packets.  R row groups share a CTA so that CTAs stay at 128-256 threads.
+//
+// 16-byte aligned rows take rmsnorm_fwd_staged: a persistent grid in which
+// one elected thread per row group streams the group's next S rows into a
+// ring of shared-memory stages with bulk copies (cp.async.bulk, the TMA
+// engine's 1-D mode) completing on mbarriers; the warps compute from shared
+// memory.  Bytes in flight then cost no registers, and a row's copy starts
+// S rows before it is needed.  Other rows hold their packets in registers
+// (rmsnorm_fwd_rows); rows too long for either take a CTA-per-row kernel.
 #include "common.cuh"
 #include "launch.h"
 
@@ -32,6 +38,132 @@ RowPlan plan_rmsnorm_row(int64_t H, int pack) {
   p.V = v;
   p.R = (int)(8 / W) > 0 ? (int)(8 / W) : 1;
   return p;
+}
+
+StagedPlan plan_rmsnorm_staged(const RowPlan &p, int64_t H, int elem_bytes, int nbuf,
+                               const DeviceInfo &dev) {
+  StagedPlan sp;
+  if (p.generic || p.pack == 1) return sp;
+  sp.row_bytes = (uint32_t)(H * elem_bytes);
+  sp.stage_bytes = sp.row_bytes * (uint32_t)nbuf;
+  // Aim for ~6 row groups computing per SM (at least 2 CTAs) and ~200 KiB of
+  // stages per SM in all; each group gets 2..8 stages.
+  const int ctas = p.R >= 3 ? 2 : (6 + p.R - 1) / p.R;
+  int S = (int)((204800 / ctas) / ((size_t)p.R * sp.stage_bytes));
+  S = S < 2 ? 2 : (S > 8 ? 8 : S);
+  for (; S >= 2; --S) {
+    sp.off_red = ((size_t)p.R * S * 8 + 15) / 16 * 16;
+    sp.off_stage = (sp.off_red + (size_t)p.R * p.W * 8 + 127) / 128 * 128;
+    sp.smem = sp.off_stage + (size_t)p.R * S * sp.stage_bytes;
+    if (sp.smem <= (size_t)dev.max_smem_optin) {
+      sp.S = S;
+      return sp;
+    }
+  }
+  sp.S = 0;
+  return sp;
+}
+
+template <typename T, typename Idx, int N, int V>
+__global__ void __launch_bounds__(256)
+rmsnorm_fwd_staged(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
+                   float *__restrict__ rstd, Idx rows, int hp, float inv_h, float eps, int W,
+                   int R, int S, uint32_t off_red, uint32_t off_stage, uint32_t row_bytes,
+                   unsigned *status, long long wait_limit) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // [R][S]
+  float *red = reinterpret_cast<float *>(smem + off_red);  // [R][W]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / W, wig = warp - grp * W;
+  const int gi = wig * 32 + lane, G = W * 32;
+  const bool leader = gi == 0;
+
+  for (int i = threadIdx.x; i < R * S; i += blockDim.x) mbar_init(&bars[i], 1);
+  if (threadIdx.x == 0) fence_mbar_init();
+  __syncthreads();
+
+  uint64_t *gb = bars + grp * S;
+  unsigned char *ring = smem + off_stage + (size_t)grp * S * row_bytes;
+  const Idx stride = (Idx)gridDim.x * R;
+  const Idx first = (Idx)blockIdx.x * R + grp;
+
+  int issued = 0;  // copies issued by the leader
+  if (leader) {
+    for (int s = 0; s < S; ++s) {
+      const Idx row = first + (Idx)s * stride;
+      if (row >= rows) break;
+      mbar_arrive_expect_tx(&gb[s], row_bytes);
+      bulk_copy_g2s(ring + (size_t)s * row_bytes, x + row * ldx, row_bytes, &gb[s]);
+      ++issued;
+    }
+  }
+  Packet<T, N> wv[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int c = gi + k * G;
+    if (c < hp) wv[k] = load_packet<T, N>(w + (Idx)c * N);
+  }
+
+  bool live = true;  // false once one of this thread's waits has run out
+  int it = 0;
+  for (Idx row = first; row < rows; row += stride, ++it) {
+    const int s = it % S;
+    if (live) live = mbar_wait_bounded(&gb[s], (uint32_t)((it / S) & 1), wait_limit, status);
+    const T *xs = reinterpret_cast<const T *>(ring + (size_t)s * row_bytes);
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const int c = gi + k * G;
+      if (c < hp) {
+        const Packet<T, N> v = *reinterpret_cast<const Packet<T, N> *>(xs + c * N);
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float f = v.get(e);
+          ss = fmaf(f, f, ss);
+        }
+      }
+    }
+    ss = warp_sum(ss);
+    if (W > 1) {
+      if (lane == 0) red[grp * W + wig] = ss;
+      named_barrier(1 + grp, G);
+      ss = 0.f;
+      for (int i = 0; i < W; ++i) ss += red[grp * W + i];
+    }
+    const float r = rsqrtf(fmaf(ss, inv_h, eps));
+    if (rstd != nullptr && leader) rstd[row] = r;
+    T *yr = y + row * ldy;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const int c = gi + k * G;
+      if (c < hp) {
+        const Packet<T, N> v = *reinterpret_cast<const Packet<T, N> *>(xs + c * N);
+        Packet<T, N> o;
+#pragma unroll
+        for (int e = 0; e < N; ++e) o.set(e, (v.get(e) * r) * wv[k].get(e));
+        store_packet<T, N>(yr + (Idx)c * N, o);
+      }
+    }
+    // the whole group has read stage s (and the reduction slots): refill it
+    if (W > 1)
+      named_barrier(1 + grp, G);
+    else
+      __syncwarp();
+    if (leader) {
+      const Idx next = row + (Idx)S * stride;
+      if (next < rows) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&gb[s], row_bytes);
+        bulk_copy_g2s(ring + (size_t)s * row_bytes, x + next * ldx, row_bytes, &gb[s]);
+        ++issued;
+      }
+    }
+  }
+  // after a wait ran out, let the copies still in flight land (bounded)
+  // before the CTA's shared memory is released
+  if (leader && !live)
+    for (int i = it; i < issued; ++i)
+      mbar_wait_bounded(&gb[i % S], (uint32_t)((i / S) & 1), wait_limit, status);
 }
 
 template <typename T, typename Idx, int N, int V>
@@ -147,11 +279,47 @@ static cudaError_t fwd_rows(const RowPlan &p, const RmsNormFwdArgs &a, cudaStrea
   return cudaGetLastError();
 }
 
+template <typename T, typename Idx, int N, int V>
+static cudaError_t fwd_staged_v(const RowPlan &p, const StagedPlan &sp, const RmsNormFwdArgs &a,
+                                const DeviceInfo &dev, cudaStream_t s) {
+  auto kern = rmsnorm_fwd_staged<T, Idx, N, V>;
+  const int threads = p.threads();
+  const int occ = blocks_per_sm((const void *)kern, threads, sp.smem, dev, 8);
+  int64_t P = ceil_div(a.T, (int64_t)p.R);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  unsigned *status = nullptr;
+  cudaError_t e = device_status_ptr(dev, &status);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)P, threads, sp.smem, s>>>(
+      (const T *)a.x, (Idx)a.ldx, (const T *)a.w, (T *)a.y, (Idx)a.ldy, a.rstd, (Idx)a.T,
+      (int)(a.H / N), (float)(1.0 / (double)a.H), a.eps, p.W, p.R, sp.S, (uint32_t)sp.off_red,
+      (uint32_t)sp.off_stage, sp.row_bytes, status, kWaitLimitCycles);
+  return cudaGetLastError();
+}
+
+template <typename T, typename Idx, int N>
+static cudaError_t fwd_staged(const RowPlan &p, const StagedPlan &sp, const RmsNormFwdArgs &a,
+                              const DeviceInfo &dev, cudaStream_t s) {
+  switch (p.V) {
+    case 1: return fwd_staged_v<T, Idx, N, 1>(p, sp, a, dev, s);
+    case 2: return fwd_staged_v<T, Idx, N, 2>(p, sp, a, dev, s);
+    case 3: return fwd_staged_v<T, Idx, N, 3>(p, sp, a, dev, s);
+    case 4: return fwd_staged_v<T, Idx, N, 4>(p, sp, a, dev, s);
+    case 6: return fwd_staged_v<T, Idx, N, 6>(p, sp, a, dev, s);
+    case 8: return fwd_staged_v<T, Idx, N, 8>(p, sp, a, dev, s);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
 template <typename T, typename Idx>
 static cudaError_t fwd_typed(bool vec, const RmsNormFwdArgs &a, const DeviceInfo &dev,
                              cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
   const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1);
+  if (vec && !p.generic) {
+    const StagedPlan sp = plan_rmsnorm_staged(p, a.H, (int)sizeof(T), 1, dev);
+    if (sp.S > 0) return fwd_staged<T, Idx, NV>(p, sp, a, dev, s);
+  }
   if (p.generic) {
     int64_t grid = a.T < (int64_t)dev.sms * 16 ? a.T : (int64_t)dev.sms * 16;
     rmsnorm_fwd_generic<T, Idx><<<(unsigned)grid, 256, 0, s>>>(

@@ -57,6 +57,8 @@ def library() -> ctypes.CDLL:
         "ftk_swiglu_bwd": (st, [vp, i64, vp, vp, i64, vp, vp, i64, i64, i64, dt, vp]),
         "ftk_qk_rope_fwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, dt, vp]),
         "ftk_qk_rope_bwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, dt, vp]),
+        "ftk_device_status": (st, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
+        "ftk_selftest_wait_timeout": (st, [i64, vp]),
         "ftk_status_str": (ctypes.c_char_p, [st]),
         "ftk_last_cuda_error": (ctypes.c_char_p, []),
         "ftk_version": (ctypes.c_char_p, []),
@@ -230,6 +232,24 @@ def qk_rope_fwd(q, k, cu_seqlens, theta):
 def qk_rope_bwd(dq, dk, cu_seqlens, theta):
     """Backward of qk_rope_fwd: rotate dq, dk by -phi IN PLACE; returns (dq, dk)."""
     return _rope("ftk_qk_rope_bwd", dq, dk, cu_seqlens, theta)
+
+
+WAIT_TIMEOUT = 1  # FTK_DEVSTAT_WAIT_TIMEOUT
+
+
+def device_status(clear: bool = True) -> int:
+    """Status word of the current device (bit WAIT_TIMEOUT: a kernel's
+    bounded pipeline wait ran out, so some launch's results are invalid)."""
+    v = ctypes.c_uint32(0)
+    _call("ftk_device_status", ctypes.byref(v), 1 if clear else 0)
+    return int(v.value)
+
+
+def selftest_wait_timeout(limit_cycles: int = 1_000_000) -> None:
+    """Run the bounded-wait timeout path on purpose (one CTA waits on a
+    barrier nothing completes); afterwards device_status() has WAIT_TIMEOUT."""
+    _call("ftk_selftest_wait_timeout", int(limit_cycles),
+          torch.cuda.current_stream().cuda_stream)
 
 
 def version() -> str:

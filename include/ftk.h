@@ -183,6 +183,24 @@ FTK_API ftk_status ftk_qk_rope_bwd(void *dq, int64_t ld_q, void *dk, int64_t ld_
 
 /* ------------------------------------------------------------ utilities */
 
+/* Bits of the device status word. */
+#define FTK_DEVSTAT_WAIT_TIMEOUT 1u /* a kernel's pipeline wait ran out */
+
+/* The device status word of the current device, into *flags (host
+ * pointer); cleared afterwards when clear != 0.  Kernels that stream data
+ * through shared memory wait on barriers for bulk copies; every such wait
+ * gives up after ~1 s of SM clock, sets FTK_DEVSTAT_WAIT_TIMEOUT and lets
+ * the kernel finish instead of hanging.  A set bit means some launch since
+ * the last clear produced invalid results.  This call synchronises with
+ * the device (it reads device memory). */
+FTK_API ftk_status ftk_device_status(uint32_t *flags, int clear);
+
+/* Launches one CTA that waits, bounded by limit_cycles SM clock cycles, on
+ * a barrier nothing will ever complete, so the timeout path runs for real:
+ * afterwards ftk_device_status reports FTK_DEVSTAT_WAIT_TIMEOUT.  For
+ * testing failure detection; faults and hangs nothing. */
+FTK_API ftk_status ftk_selftest_wait_timeout(int64_t limit_cycles, ftk_stream_t stream);
+
 /* Static text for a status code. */
 FTK_API const char *ftk_status_str(ftk_status status);
 

@@ -299,3 +299,22 @@ def test_rope_wide_index_matches_narrow():
     ftk.qk_rope_fwd(qs, None, cu, 1e6)
     torch.cuda.synchronize()
     assert torch.equal(q, qs)
+
+
+# --------------------------------------------------------- failure detection
+
+def test_bounded_wait_times_out_and_reports():
+    """A kernel whose barrier is never completed gives up after its cycle
+    limit, sets the status bit and returns: the GPU stays usable."""
+    ftk.device_status(clear=True)
+    ftk.selftest_wait_timeout(2_000_000)
+    torch.cuda.synchronize()
+    assert ftk.device_status(clear=True) & ftk.WAIT_TIMEOUT
+    assert ftk.device_status(clear=False) == 0
+    # ordinary work afterwards runs and leaves the word clean
+    x = randn((64, 896), torch.bfloat16, 90)
+    w = torch.ones(896, dtype=torch.bfloat16, device=DEV)
+    y, _ = ftk.rmsnorm_fwd(x, w, 1e-6)
+    dx, dw = ftk.rmsnorm_bwd(x, x, w, None, 1e-6)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y.float()).all() and ftk.device_status() == 0

@@ -27,8 +27,16 @@ LARGE = ("llama-3.2-1b", "qwen3-8b")
 def _lib():
     build.build()
     ftk.library()
+    ftk.device_status(clear=True)
     yield
     torch.cuda.empty_cache()
+
+
+@pytest.fixture(autouse=True)
+def _no_wait_timeouts():
+    yield
+    # no kernel's bounded pipeline wait may have run out during the test
+    assert ftk.device_status(clear=True) == 0
 
 
 def dt(wl):
