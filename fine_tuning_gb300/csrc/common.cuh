@@ -32,6 +32,15 @@ template <typename T, int N> struct alignas(sizeof(T) * N) Packet {
 
   __device__ __forceinline__ float get(int i) const { return to_float(v[i]); }
   __device__ __forceinline__ void set(int i, float f) { v[i] = from_float<T>(f); }
+  // elements i and i+1 (i even) in one conversion
+  __device__ __forceinline__ void set2(int i, float a, float b) {
+    if constexpr (sizeof(T) == 2 && N % 2 == 0) {
+      *reinterpret_cast<__nv_bfloat162 *>(&v[i]) = __floats2bfloat162_rn(a, b);
+    } else {
+      set(i, a);
+      if (i + 1 < N) set(i + 1, b);
+    }
+  }
 };
 
 // 16-byte packets go through explicit vector accesses so that the compiler

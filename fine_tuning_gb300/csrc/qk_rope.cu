@@ -179,32 +179,42 @@ qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   }
 }
 
-// 16-byte aligned rows: a persistent grid over blocks of TB tokens.  Each
-// CTA keeps a ring of S shared-memory stages, each holding one block's Q
-// rows then K rows.  Thread 0 bulk-loads the blocks ahead (cp.async.bulk
-// completing on one mbarrier per stage); while a block lands the CTA
-// computes its positions and cos/sin; the warps rotate it in shared memory;
-// thread 0 bulk-stores it back in place and, once that store has read the
-// stage, refills the stage with the block S iterations ahead.
+// 16-byte aligned rows: a persistent grid of independent row groups.  A
+// group (W warps) owns a ring of S shared-memory stages; a stage holds TB
+// whole tokens (their Q rows, then their K rows).  The group's leader lane
+// bulk-loads the group's blocks ahead (cp.async.bulk completing on the
+// stage's mbarrier); while a block lands the group computes the block's
+// positions and cos/sin; the warps rotate it in shared memory; the leader
+// bulk-stores it back in place, and at the start of the next iteration, once
+// that store has read the stage, refills the stage with the group's block S
+// iterations ahead (so with S = 2 one block loads while the other rotates).  Groups
+// synchronise only among their own warps, so the R groups of a CTA (and the
+// CTAs of an SM) overlap each other's latencies.
 template <typename T, typename Idx, int N>
 __global__ void __launch_bounds__(kCtaThreads)
 qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int B, Idx rows,
-               int Hq, int Hkv, int D, int TB, int S, float sgn, uint32_t off_cs,
-               uint32_t off_stage, uint32_t stage_bytes, unsigned *status, long long wait_limit,
-               const __grid_constant__ RopeFreqs fr) {
+               int Hq, int Hkv, int D, int TB, int S, int W, int R, float sgn,
+               uint32_t off_cs, uint32_t off_stage, uint32_t stage_bytes, unsigned *status,
+               long long wait_limit, const __grid_constant__ RopeFreqs fr) {
   extern __shared__ __align__(128) unsigned char sbuf[];
   __shared__ float2 freq[kRopeMaxHalf];
   __shared__ int32_t cu_s[kCuInShared];
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf);          // [S]
-  float2 *cs = reinterpret_cast<float2 *>(sbuf + off_cs);        // [TB][D/2]
-  unsigned char *stages = sbuf + off_stage;                     // [S][stage_bytes]
 
   const int half = D >> 1, NV = half / N, NH = Hq + Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / W, wig = warp - grp * W;
+  const int gi = wig * 32 + lane, G = W * 32;
+  const bool leader = gi == 0;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf) + grp * S;               // [R][S]
+  float2 *cs = reinterpret_cast<float2 *>(sbuf + off_cs) + (size_t)grp * TB * half;  // [R][TB][half]
+  unsigned char *ring = sbuf + off_stage + (size_t)grp * S * stage_bytes;      // [R][S][stage]
+
   const Idx nblocks = (rows + TB - 1) / TB;
   const size_t qrow_b = (size_t)Hq * D * sizeof(T), krow_b = (size_t)Hkv * D * sizeof(T);
   const bool q_contig = ld_q == (Idx)Hq * D, k_contig = ld_k == (Idx)Hkv * D;
 
-  for (int i = threadIdx.x; i < S; i += blockDim.x) mbar_init(&bars[i], 1);
+  if (leader)
+    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   const bool cu_staged = B < kCuInShared;
   if (cu_staged)
@@ -213,11 +223,15 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   __syncthreads();
   const int32_t *bounds = cu_staged ? cu_s : cu;
 
+  auto ntok = [&](Idx b) -> int {
+    const Idx left = rows - b * TB;
+    return (int)(left < (Idx)TB ? left : (Idx)TB);
+  };
   // block b <-> stage s: Q rows [TB][Hq*D] then K rows [TB][Hkv*D]
   auto load = [&](int s, Idx b) {
     const Idx t0 = b * TB;
-    const int nt = (int)((rows - t0) < (Idx)TB ? (rows - t0) : (Idx)TB);
-    unsigned char *st = stages + (size_t)s * stage_bytes;
+    const int nt = ntok(b);
+    unsigned char *st = ring + (size_t)s * stage_bytes;
     mbar_arrive_expect_tx(&bars[s], (uint32_t)(nt * (qrow_b + krow_b)));
     if (qrow_b) {
       if (q_contig)
@@ -237,8 +251,8 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   };
   auto store = [&](int s, Idx b) {
     const Idx t0 = b * TB;
-    const int nt = (int)((rows - t0) < (Idx)TB ? (rows - t0) : (Idx)TB);
-    const unsigned char *st = stages + (size_t)s * stage_bytes;
+    const int nt = ntok(b);
+    const unsigned char *st = ring + (size_t)s * stage_bytes;
     if (qrow_b) {
       if (q_contig)
         bulk_copy_s2g(q + t0 * ld_q, st, (uint32_t)(nt * qrow_b));
@@ -256,12 +270,19 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
     }
     bulk_commit_group();
   };
+  auto group_sync = [&]() {
+    if (W > 1)
+      named_barrier(1 + grp, G);
+    else
+      __syncwarp();
+  };
 
-  const bool leader = threadIdx.x == 0;
+  const Idx first = (Idx)blockIdx.x * R + grp;
+  const Idx stride = (Idx)gridDim.x * R;
   int issued = 0;
   if (leader)
     for (int i = 0; i < S; ++i) {
-      const Idx b = (Idx)blockIdx.x + (Idx)i * gridDim.x;
+      const Idx b = first + (Idx)i * stride;
       if (b >= nblocks) break;
       load(i, b);
       ++issued;
@@ -269,12 +290,22 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
 
   bool live = true;
   int it = 0;
-  for (Idx b = blockIdx.x; b < nblocks; b += gridDim.x, ++it) {
+  for (Idx b = first; b < nblocks; b += stride, ++it) {
     const int s = it % S;
     const Idx t0 = b * TB;
-    const int nt = (int)((rows - t0) < (Idx)TB ? (rows - t0) : (Idx)TB);
+    const int nt = ntok(b);
+    if (leader && it >= 1) {
+      // the previous block's store has read its stage: refill that stage
+      // with the block S iterations after it, before working on this one
+      bulk_wait_group_read<0>();
+      const Idx nb = b - stride + (Idx)S * stride;
+      if (nb < nblocks) {
+        load((it - 1) % S, nb);
+        ++issued;
+      }
+    }
     // cos/sin of this block while its rows land
-    for (int e = threadIdx.x; e < nt * half; e += blockDim.x) {
+    for (int e = gi; e < nt * half; e += G) {
       const int tt = e / half, i = e - tt * half;
       const int p = position_of<Idx>(t0 + tt, bounds, B);
       const float2 f = freq[i];
@@ -283,18 +314,18 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
       cs[e] = make_float2(c, sgn * sn);
     }
     if (live) live = mbar_wait_bounded(&bars[s], (uint32_t)((it / S) & 1), wait_limit, status);
-    __syncthreads();
-    unsigned char *st = stages + (size_t)s * stage_bytes;
+    group_sync();
+    unsigned char *st = ring + (size_t)s * stage_bytes;
     const int items = nt * NH * NV;
-    for (int m = threadIdx.x; m < items; m += blockDim.x) {
+    for (int m = gi; m < items; m += G) {
       const int j = m % NV, rest = m / NV;
       const int h = rest % NH, tt = rest / NH;
       T *v = reinterpret_cast<T *>(h < Hq ? st + ((size_t)tt * Hq + h) * D * sizeof(T)
                                           : st + (size_t)TB * qrow_b +
                                                 ((size_t)tt * Hkv + (h - Hq)) * D * sizeof(T)) +
              j * N;
-      Packet<T, N> pa = *reinterpret_cast<const Packet<T, N> *>(v);
-      Packet<T, N> pb = *reinterpret_cast<const Packet<T, N> *>(v + half);
+      const Packet<T, N> pa = *reinterpret_cast<const Packet<T, N> *>(v);
+      const Packet<T, N> pb = *reinterpret_cast<const Packet<T, N> *>(v + half);
       const float2 *c2 = cs + tt * half + j * N;
       Packet<T, N> oa, ob;
 #pragma unroll
@@ -308,19 +339,8 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
       *reinterpret_cast<Packet<T, N> *>(v + half) = ob;
     }
     fence_proxy_async_smem();  // this thread's stage writes before the bulk store reads them
-    __syncthreads();
-    if (leader) {
-      store(s, b);
-      if (it >= 1) {
-        // the previous block's store has read its stage: refill that stage
-        bulk_wait_group_read<1>();
-        const Idx nb = b - (Idx)gridDim.x + (Idx)S * gridDim.x;
-        if (nb < nblocks) {
-          load((it - 1) % S, nb);
-          ++issued;
-        }
-      }
-    }
+    group_sync();
+    if (leader) store(s, b);
   }
   if (leader) {
     if (!live)  // let loads still in flight land (bounded) before the CTA exits
@@ -374,31 +394,43 @@ template <typename T, typename Idx, int N>
 cudaError_t rope_staged_launch(const RopeArgs &a, const RopeFreqs &fr, const DeviceInfo &dev,
                                cudaStream_t s, bool *launched) {
   *launched = false;
-  const int NH = a.Hq + a.Hkv, half = a.D / 2;
+  const int NH = a.Hq + a.Hkv, half = a.D / 2, NV = half / N;
   const size_t tok_bytes = (size_t)NH * a.D * sizeof(T);
-  // ~16 KiB blocks of whole tokens, ~64 KiB of stages per CTA
-  int TB = (int)(16384 / tok_bytes);
-  TB = TB < 1 ? 1 : (TB > 32 ? 32 : TB);
+  // ~8 KiB of whole tokens per stage; W warps per group so that each lane
+  // rotates ~8 packet pairs per block; R groups per CTA (<= 256 threads).
+  int TB = (int)(8192 / tok_bytes);
+  TB = TB < 1 ? 1 : (TB > 16 ? 16 : TB);
+  int W = (int)ceil_div((int64_t)TB * NH * NV, (int64_t)256);
+  W = W < 1 ? 1 : (W > 8 ? 8 : W);
+  const int R = 8 / W > 0 ? 8 / W : 1;
   const size_t stage_bytes = (size_t)TB * tok_bytes;
-  int S = (int)(65536 / stage_bytes);
-  S = S < 2 ? 2 : (S > 8 ? 8 : S);
-  const size_t off_cs = ((size_t)S * 8 + 15) / 16 * 16;
-  const size_t off_stage = (off_cs + (size_t)TB * half * sizeof(float2) + 127) / 128 * 128;
-  const size_t smem = off_stage + (size_t)S * stage_bytes;
+  // ~150 KiB of stages per SM over two CTAs, 2..6 stages per group
+  int S = (int)(76800 / ((size_t)R * stage_bytes));
+  S = S < 2 ? 2 : (S > 6 ? 6 : S);
   const size_t static_smem = sizeof(float2) * kRopeMaxHalf + sizeof(int32_t) * kCuInShared;
-  if (smem + static_smem > (size_t)dev.max_smem_optin || stage_bytes >= (1u << 20)) return cudaSuccess;
+  size_t off_cs = 0, off_stage = 0, smem = 0;
+  for (; S >= 2; --S) {
+    off_cs = ((size_t)R * S * 8 + 15) / 16 * 16;
+    off_stage = (off_cs + (size_t)R * TB * half * sizeof(float2) + 127) / 128 * 128;
+    smem = off_stage + (size_t)R * S * stage_bytes;
+    if (smem + static_smem <= (size_t)dev.max_smem_optin) break;
+  }
+  if (S < 2 || stage_bytes >= (1u << 20)) return cudaSuccess;  // register kernel instead
   auto kern = qk_rope_staged<T, Idx, N>;
-  const int occ = blocks_per_sm((const void *)kern, kCtaThreads, smem, dev, 8);
+  const int threads = 32 * W * R;
+  const int occ = blocks_per_sm((const void *)kern, threads, smem, dev, 8);
   const int64_t nblocks = ceil_div(a.T, (int64_t)TB);
   int64_t P = (int64_t)dev.sms * occ;
-  if (P > nblocks) P = nblocks;
+  // the pipeline pays off once every group streams several blocks; smaller
+  // batches go to the one-pass register kernel
+  if (nblocks < (int64_t)6 * P * R) return cudaSuccess;
   unsigned *status = nullptr;
   cudaError_t e = device_status_ptr(dev, &status);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)P, kCtaThreads, smem, s>>>(
+  kern<<<(unsigned)P, threads, smem, s>>>(
       (T *)a.q, (Idx)a.ld_q, (T *)a.k, (Idx)a.ld_k, a.cu, a.B, (Idx)a.T, a.Hq, a.Hkv, a.D, TB, S,
-      a.backward ? -1.0f : 1.0f, (uint32_t)off_cs, (uint32_t)off_stage, (uint32_t)stage_bytes,
-      status, kWaitLimitCycles, fr);
+      W, R, a.backward ? -1.0f : 1.0f, (uint32_t)off_cs, (uint32_t)off_stage,
+      (uint32_t)stage_bytes, status, kWaitLimitCycles, fr);
   *launched = true;
   return cudaGetLastError();
 }

@@ -344,24 +344,26 @@ rmsnorm_bwd_generic(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restr
   }
 }
 
-// dw[j] = sum_{p < P} ws[p, j]: a CTA owns 32 columns, its 8 warps take the
-// rows p = warp, warp + 8, ... and their sums are added in warp order.
-__global__ void __launch_bounds__(256)
+// dw[j] = sum_{p < P} ws[p, j]: a CTA owns 32 columns; its 32 warps take
+// the rows p = warp, warp + 32, ... and their sums are added in warp order.
+constexpr int kReduceWarps = 32;
+
+__global__ void __launch_bounds__(32 * kReduceWarps)
 dw_reduce(const float *__restrict__ ws, int P, int H, float *__restrict__ dw) {
-  __shared__ float part[8][32];
+  __shared__ float part[kReduceWarps][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col = blockIdx.x * 32 + lane;
   float s = 0.f;
   if (col < H) {
-#pragma unroll 8
-    for (int p = warp; p < P; p += 8) s += ws[(size_t)p * H + col];
+#pragma unroll 4
+    for (int p = warp; p < P; p += kReduceWarps) s += ws[(size_t)p * H + col];
   }
   part[warp][lane] = s;
   __syncthreads();
   if (warp == 0 && col < H) {
     float t = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) t += part[i][lane];
+    for (int i = 0; i < kReduceWarps; ++i) t += part[i][lane];
     dw[col] = t;
   }
 }
@@ -383,7 +385,7 @@ cudaError_t bwd_rows_v(const RowPlan &p, const RmsNormBwdArgs &a, const DeviceIn
       (float)(1.0 / (double)a.H), a.eps, p.W, p.R);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 256, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
+  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 32 * kReduceWarps, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
   return cudaGetLastError();
 }
 
@@ -406,7 +408,7 @@ cudaError_t bwd_staged_v(const RowPlan &p, const StagedPlan &sp, const RmsNormBw
       (uint32_t)sp.off_stage, sp.row_bytes, status, kWaitLimitCycles);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 256, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
+  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 32 * kReduceWarps, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
   return cudaGetLastError();
 }
 
@@ -447,7 +449,7 @@ cudaError_t bwd_generic(const RmsNormBwdArgs &a, const DeviceInfo &dev, cudaStre
       (T *)a.dx, (Idx)a.lddx, a.ws, (Idx)a.T, (Idx)a.H, (float)(1.0 / (double)a.H), a.eps);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 256, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
+  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 32 * kReduceWarps, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
   return cudaGetLastError();
 }
 

@@ -316,7 +316,10 @@ static cudaError_t fwd_typed(bool vec, const RmsNormFwdArgs &a, const DeviceInfo
                              cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
   const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1);
-  if (vec && !p.generic) {
+  // The staged pipeline pays off once every row group streams a dozen rows
+  // or more; smaller batches finish sooner with one row per group and the
+  // hardware scheduler refilling SMs (rmsnorm_fwd_rows).
+  if (vec && !p.generic && a.T >= (int64_t)12 * p.R * 2 * dev.sms) {
     const StagedPlan sp = plan_rmsnorm_staged(p, a.H, (int)sizeof(T), 1, dev);
     if (sp.S > 0) return fwd_staged<T, Idx, NV>(p, sp, a, dev, s);
   }
