@@ -192,6 +192,21 @@ __device__ __forceinline__ void bulk_wait_group_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Programmatic dependent launch.  Every ftk kernel calls pdl_wait() before
+// its first global memory access: when it was launched as a programmatic
+// dependent of the previous kernel in the stream, this waits until that
+// kernel has completed and its writes are visible (otherwise it returns at
+// once).  pdl_trigger() then lets the next kernel in the stream be launched
+// as soon as every CTA of this one has started, so its launch and prologue
+// overlap this kernel's tail; it still waits for this kernel's completion
+// before touching memory.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 // Named barrier over `threads` threads (a multiple of 32) with id 1..15.
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

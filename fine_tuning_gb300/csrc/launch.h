@@ -30,6 +30,24 @@ cudaError_t read_device_status(unsigned *flags, bool clear);
 cudaError_t launch_wait_timeout_selftest(const DeviceInfo &dev, long long limit_cycles,
                                          cudaStream_t s);
 
+// Launches `kernel` on `s` as a programmatic dependent of the previous
+// kernel in the stream (see pdl_wait in common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // SM clock cycles a pipeline wait may take before it gives up (~1 s).
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
@@ -42,7 +60,9 @@ struct RowPlan {
   bool generic = false;
   int threads() const { return generic ? 256 : 32 * W * R; }
 };
-RowPlan plan_rmsnorm_row(int64_t H, int pack);
+// W = ceil(packets / (32 * vmax)) warps per row (at most 8), then V packets
+// per thread rounded up to 1, 2, 3, 4, 6 or 8.
+RowPlan plan_rmsnorm_row(int64_t H, int pack, int vmax);
 
 // The bulk-copy pipeline on top of a row plan: every row group owns a ring
 // of S shared-memory stages, each holding `nbuf` rows (x, or x and dy).

@@ -96,6 +96,8 @@ qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   extern __shared__ float2 cs[];  // [TOK][D/2] (cos, sgn*sin)
   __shared__ float2 freq[kRopeMaxHalf];  // (hi, lo) turns per position
   __shared__ int32_t cu_s[kCuInShared];
+  pdl_wait();
+  pdl_trigger();
 
   const int half = D >> 1;
   const int TPT = NV * S;
@@ -216,6 +218,8 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   if (leader)
     for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
   const bool cu_staged = B < kCuInShared;
   if (cu_staged)
     for (int i = threadIdx.x; i <= B; i += blockDim.x) cu_s[i] = __ldg(cu + i);
@@ -363,9 +367,12 @@ cudaError_t rope_launch(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) 
   const int threads = TOK * TPT;
   const size_t smem = sizeof(float2) * (size_t)TOK * half;
   const int64_t grid = ceil_div(a.T, (int64_t)TOK);
-  qk_rope_kernel<T, Idx, N, HPT><<<(unsigned)grid, threads, smem, s>>>(
+  {
+    cudaError_t le_ = launch_pdl(qk_rope_kernel<T, Idx, N, HPT>, dim3((unsigned)grid), dim3(threads), smem, s, 
       (T *)a.q, (Idx)a.ld_q, (T *)a.k, (Idx)a.ld_k, a.cu, a.B, (Idx)a.T, a.Hq, NH, a.D, S, NV,
       TOK, a.backward ? -1.0f : 1.0f, fr);
+    if (le_ != cudaSuccess) return le_;
+  }
   return cudaGetLastError();
 }
 
@@ -427,10 +434,13 @@ cudaError_t rope_staged_launch(const RopeArgs &a, const RopeFreqs &fr, const Dev
   unsigned *status = nullptr;
   cudaError_t e = device_status_ptr(dev, &status);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)P, threads, smem, s>>>(
+  {
+    cudaError_t le_ = launch_pdl(kern, dim3((unsigned)P), dim3(threads), smem, s, 
       (T *)a.q, (Idx)a.ld_q, (T *)a.k, (Idx)a.ld_k, a.cu, a.B, (Idx)a.T, a.Hq, a.Hkv, a.D, TB, S,
       W, R, a.backward ? -1.0f : 1.0f, (uint32_t)off_cs, (uint32_t)off_stage,
       (uint32_t)stage_bytes, status, kWaitLimitCycles, fr);
+    if (le_ != cudaSuccess) return le_;
+  }
   *launched = true;
   return cudaGetLastError();
 }

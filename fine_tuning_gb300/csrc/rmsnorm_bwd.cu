@@ -37,6 +37,8 @@ rmsnorm_bwd_rows(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restrict
   extern __shared__ float smem[];
   float2 *red = reinterpret_cast<float2 *>(smem);
   float *part = smem + 4 * R * W;
+  pdl_wait();
+  pdl_trigger();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / W, wig = warp - grp * W;
@@ -168,6 +170,8 @@ rmsnorm_bwd_staged(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restri
   for (int i = threadIdx.x; i < R * S; i += blockDim.x) mbar_init(&bars[i], 1);
   if (threadIdx.x == 0) fence_mbar_init();
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
 
   uint64_t *gb = bars + grp * S;
   unsigned char *ring = sbuf + off_stage + (size_t)grp * S * stage_bytes;
@@ -312,6 +316,8 @@ rmsnorm_bwd_generic(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restr
                     const float *__restrict__ rstd, T *dx, Idx lddx, float *__restrict__ ws,
                     Idx rows, Idx H, float inv_h, float eps) {
   __shared__ float2 red[8];
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float *mine = ws + (size_t)blockIdx.x * H;
   for (Idx j = threadIdx.x; j < H; j += blockDim.x) mine[j] = 0.f;
@@ -351,6 +357,8 @@ constexpr int kReduceWarps = 32;
 __global__ void __launch_bounds__(32 * kReduceWarps)
 dw_reduce(const float *__restrict__ ws, int P, int H, float *__restrict__ dw) {
   __shared__ float part[kReduceWarps][33];
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col = blockIdx.x * 32 + lane;
   float s = 0.f;
@@ -379,13 +387,20 @@ cudaError_t bwd_rows_v(const RowPlan &p, const RmsNormBwdArgs &a, const DeviceIn
   int64_t P = ceil_div(a.T, (int64_t)p.R);
   if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
   if (P > a.ws_rows) P = a.ws_rows;
-  kern<<<(unsigned)P, threads, smem, s>>>(
-      (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
+  {
+    cudaError_t le_ = launch_pdl(kern, dim3((unsigned)P), dim3(threads), smem, s,
+                                 (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
       (T *)a.dx, (Idx)a.lddx, a.ws, (Idx)a.T, (int)(a.H / N), (int)a.H,
       (float)(1.0 / (double)a.H), a.eps, p.W, p.R);
+    if (le_ != cudaSuccess) return le_;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 32 * kReduceWarps, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
+  {
+    cudaError_t le_ = launch_pdl(dw_reduce, dim3((unsigned)ceil_div(a.H, (int64_t)32)), dim3(32 * kReduceWarps), 0, s,
+                                 a.ws, (int)P, (int)a.H, a.dw);
+    if (le_ != cudaSuccess) return le_;
+  }
   return cudaGetLastError();
 }
 
@@ -401,14 +416,21 @@ cudaError_t bwd_staged_v(const RowPlan &p, const StagedPlan &sp, const RmsNormBw
   unsigned *status = nullptr;
   cudaError_t e = device_status_ptr(dev, &status);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)P, threads, sp.smem, s>>>(
-      (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
+  {
+    cudaError_t le_ = launch_pdl(kern, dim3((unsigned)P), dim3(threads), sp.smem, s,
+                                 (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
       (T *)a.dx, (Idx)a.lddx, a.ws, (Idx)a.T, (int)(a.H / N), (int)a.H,
       (float)(1.0 / (double)a.H), a.eps, p.W, p.R, sp.S, (uint32_t)sp.off_red,
       (uint32_t)sp.off_stage, sp.row_bytes, status, kWaitLimitCycles);
+    if (le_ != cudaSuccess) return le_;
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 32 * kReduceWarps, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
+  {
+    cudaError_t le_ = launch_pdl(dw_reduce, dim3((unsigned)ceil_div(a.H, (int64_t)32)), dim3(32 * kReduceWarps), 0, s,
+                                 a.ws, (int)P, (int)a.H, a.dw);
+    if (le_ != cudaSuccess) return le_;
+  }
   return cudaGetLastError();
 }
 
@@ -444,12 +466,19 @@ template <typename T, typename Idx, bool HAS_RSTD>
 cudaError_t bwd_generic(const RmsNormBwdArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   int64_t P = a.T < (int64_t)dev.sms * 4 ? a.T : (int64_t)dev.sms * 4;
   if (P > a.ws_rows) P = a.ws_rows;
-  rmsnorm_bwd_generic<T, Idx, HAS_RSTD><<<(unsigned)P, 256, 0, s>>>(
-      (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
+  {
+    cudaError_t le_ = launch_pdl(rmsnorm_bwd_generic<T, Idx, HAS_RSTD>, dim3((unsigned)P), dim3(256), 0, s,
+                                 (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
       (T *)a.dx, (Idx)a.lddx, a.ws, (Idx)a.T, (Idx)a.H, (float)(1.0 / (double)a.H), a.eps);
+    if (le_ != cudaSuccess) return le_;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dw_reduce<<<(unsigned)ceil_div(a.H, (int64_t)32), 32 * kReduceWarps, 0, s>>>(a.ws, (int)P, (int)a.H, a.dw);
+  {
+    cudaError_t le_ = launch_pdl(dw_reduce, dim3((unsigned)ceil_div(a.H, (int64_t)32)), dim3(32 * kReduceWarps), 0, s,
+                                 a.ws, (int)P, (int)a.H, a.dw);
+    if (le_ != cudaSuccess) return le_;
+  }
   return cudaGetLastError();
 }
 
@@ -457,7 +486,10 @@ template <typename T, typename Idx>
 cudaError_t bwd_typed(bool vec, const RmsNormBwdArgs &a, const DeviceInfo &dev,
                       cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
-  const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1);
+  // rows under 8 KiB: at most two packets per thread (the backward also holds
+  // dw accumulators and w in registers; more warps per row keep it to ~64
+  // registers and more CTAs per SM); longer rows have enough warps already
+  const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1, a.H * (int64_t)sizeof(T) < 8192 ? 2 : 4);
   const bool has_rstd = a.rstd != nullptr;
   if (vec && !p.generic) {
     const StagedPlan sp = plan_rmsnorm_staged(p, a.H, (int)sizeof(T), 2, dev);

@@ -19,11 +19,11 @@
 
 namespace ftk {
 
-RowPlan plan_rmsnorm_row(int64_t H, int pack) {
+RowPlan plan_rmsnorm_row(int64_t H, int pack, int vmax) {
   RowPlan p;
   p.pack = pack;
   const int64_t hp = H / pack;  // packets per row
-  int64_t W = ceil_div(hp, (int64_t)128);
+  int64_t W = ceil_div(hp, (int64_t)32 * vmax);
   if (W > 8) W = 8;
   int64_t V = ceil_div(hp, 32 * W);
   static const int kV[] = {1, 2, 3, 4, 6, 8};
@@ -81,6 +81,8 @@ rmsnorm_fwd_staged(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
   for (int i = threadIdx.x; i < R * S; i += blockDim.x) mbar_init(&bars[i], 1);
   if (threadIdx.x == 0) fence_mbar_init();
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
 
   uint64_t *gb = bars + grp * S;
   unsigned char *ring = smem + off_stage + (size_t)grp * S * row_bytes;
@@ -172,6 +174,8 @@ rmsnorm_fwd_rows(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
                  float *__restrict__ rstd, Idx rows, int hp, float inv_h, float eps,
                  int W, int R) {
   extern __shared__ float red[];  // [R][W] warp partial sums
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / W, wig = warp - grp * W;
   const int gi = wig * 32 + lane, G = W * 32;
@@ -230,6 +234,8 @@ __global__ void __launch_bounds__(256)
 rmsnorm_fwd_generic(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
                     float *__restrict__ rstd, Idx rows, Idx H, float inv_h, float eps) {
   __shared__ float red[8];
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (Idx row = blockIdx.x; row < rows; row += gridDim.x) {
     const T *xr = x + row * ldx;
@@ -261,9 +267,11 @@ static cudaError_t fwd_rows(const RowPlan &p, const RmsNormFwdArgs &a, cudaStrea
   const float inv_h = (float)(1.0 / (double)a.H);
 #define FTK_FWD_CASE(VV)                                                          \
   case VV:                                                                        \
-    rmsnorm_fwd_rows<T, Idx, N, VV><<<grid, p.threads(), smem, s>>>(               \
-        (const T *)a.x, (Idx)a.ldx, (const T *)a.w, (T *)a.y, (Idx)a.ldy, a.rstd, \
-        rows, hp, inv_h, a.eps, p.W, p.R);                                        \
+    {                                                                             \
+      cudaError_t le_ = launch_pdl(rmsnorm_fwd_rows<T, Idx, N, VV>, dim3(grid), dim3(p.threads()), smem, s, \
+                                    (const T *)a.x, (Idx)a.ldx, (const T *)a.w, (T *)a.y, (Idx)a.ldy, a.rstd, rows, hp, inv_h, a.eps, p.W, p.R); \
+      if (le_ != cudaSuccess) return le_;                                          \
+    }                                        \
     break;
   switch (p.V) {
     FTK_FWD_CASE(1)
@@ -290,10 +298,13 @@ static cudaError_t fwd_staged_v(const RowPlan &p, const StagedPlan &sp, const Rm
   unsigned *status = nullptr;
   cudaError_t e = device_status_ptr(dev, &status);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)P, threads, sp.smem, s>>>(
-      (const T *)a.x, (Idx)a.ldx, (const T *)a.w, (T *)a.y, (Idx)a.ldy, a.rstd, (Idx)a.T,
+  {
+    cudaError_t le_ = launch_pdl(kern, dim3((unsigned)P), dim3(threads), sp.smem, s,
+                                 (const T *)a.x, (Idx)a.ldx, (const T *)a.w, (T *)a.y, (Idx)a.ldy, a.rstd, (Idx)a.T,
       (int)(a.H / N), (float)(1.0 / (double)a.H), a.eps, p.W, p.R, sp.S, (uint32_t)sp.off_red,
       (uint32_t)sp.off_stage, sp.row_bytes, status, kWaitLimitCycles);
+    if (le_ != cudaSuccess) return le_;
+  }
   return cudaGetLastError();
 }
 
@@ -315,7 +326,7 @@ template <typename T, typename Idx>
 static cudaError_t fwd_typed(bool vec, const RmsNormFwdArgs &a, const DeviceInfo &dev,
                              cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
-  const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1);
+  const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1, 4);
   // The staged pipeline pays off once every row group streams a dozen rows
   // or more; smaller batches finish sooner with one row per group and the
   // hardware scheduler refilling SMs (rmsnorm_fwd_rows).
@@ -325,9 +336,12 @@ static cudaError_t fwd_typed(bool vec, const RmsNormFwdArgs &a, const DeviceInfo
   }
   if (p.generic) {
     int64_t grid = a.T < (int64_t)dev.sms * 16 ? a.T : (int64_t)dev.sms * 16;
-    rmsnorm_fwd_generic<T, Idx><<<(unsigned)grid, 256, 0, s>>>(
-        (const T *)a.x, (Idx)a.ldx, (const T *)a.w, (T *)a.y, (Idx)a.ldy, a.rstd,
+    {
+      cudaError_t le_ = launch_pdl(rmsnorm_fwd_generic<T, Idx>, dim3((unsigned)grid), dim3(256), 0, s,
+                                   (const T *)a.x, (Idx)a.ldx, (const T *)a.w, (T *)a.y, (Idx)a.ldy, a.rstd,
         (Idx)a.T, (Idx)a.H, (float)(1.0 / (double)a.H), a.eps);
+      if (le_ != cudaSuccess) return le_;
+    }
     return cudaGetLastError();
   }
   return vec ? fwd_rows<T, Idx, NV>(p, a, s) : fwd_rows<T, Idx, 1>(p, a, s);

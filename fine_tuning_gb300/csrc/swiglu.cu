@@ -51,6 +51,8 @@ __device__ __forceinline__ Idx packet_offset(Idx v, Idx ip, Idx ld) {
 template <typename T, typename Idx, int N, int U, bool CONTIG>
 __global__ void __launch_bounds__(kThreads)
 swiglu_fwd_kernel(const T *g, const T *u, Idx ld_gu, T *h, Idx ld_h, Idx npk, Idx ip) {
+  pdl_wait();
+  pdl_trigger();
   const Idx base = (Idx)blockIdx.x * (kThreads * U) + threadIdx.x;
   Packet<T, N> gv[U], uv[U];
 #pragma unroll
@@ -89,6 +91,8 @@ template <typename T, typename Idx, int N, int U, bool CONTIG>
 __global__ void __launch_bounds__(kThreads)
 swiglu_bwd_kernel(const T *dh, Idx ld_dh, const T *g, const T *u, Idx ld_gu, T *dg, T *du,
                   Idx ld_dgu, Idx npk, Idx ip) {
+  pdl_wait();
+  pdl_trigger();
   const Idx base = (Idx)blockIdx.x * (kThreads * U) + threadIdx.x;
   Packet<T, N> hv[U], gv[U], uv[U];
 #pragma unroll
@@ -140,8 +144,11 @@ cudaError_t fwd_launch(const SwigluFwdArgs &a, cudaStream_t s) {
   const Idx ip = (Idx)(a.I / N);
   const Idx npk = (Idx)a.T * ip;
   const int64_t grid = ceil_div((int64_t)npk, (int64_t)kThreads * U);
-  swiglu_fwd_kernel<T, Idx, N, U, CONTIG><<<(unsigned)grid, kThreads, 0, s>>>(
-      (const T *)a.g, (const T *)a.u, (Idx)a.ld_gu, (T *)a.h, (Idx)a.ld_h, npk, ip);
+  {
+    cudaError_t le_ = launch_pdl(swiglu_fwd_kernel<T, Idx, N, U, CONTIG>, dim3((unsigned)grid), dim3(kThreads), 0, s,
+                                 (const T *)a.g, (const T *)a.u, (Idx)a.ld_gu, (T *)a.h, (Idx)a.ld_h, npk, ip);
+    if (le_ != cudaSuccess) return le_;
+  }
   return cudaGetLastError();
 }
 
@@ -150,9 +157,12 @@ cudaError_t bwd_launch(const SwigluBwdArgs &a, cudaStream_t s) {
   const Idx ip = (Idx)(a.I / N);
   const Idx npk = (Idx)a.T * ip;
   const int64_t grid = ceil_div((int64_t)npk, (int64_t)kThreads * U);
-  swiglu_bwd_kernel<T, Idx, N, U, CONTIG><<<(unsigned)grid, kThreads, 0, s>>>(
-      (const T *)a.dh, (Idx)a.ld_dh, (const T *)a.g, (const T *)a.u, (Idx)a.ld_gu, (T *)a.dg,
+  {
+    cudaError_t le_ = launch_pdl(swiglu_bwd_kernel<T, Idx, N, U, CONTIG>, dim3((unsigned)grid), dim3(kThreads), 0, s,
+                                 (const T *)a.dh, (Idx)a.ld_dh, (const T *)a.g, (const T *)a.u, (Idx)a.ld_gu, (T *)a.dg,
       (T *)a.du, (Idx)a.ld_dgu, npk, ip);
+    if (le_ != cudaSuccess) return le_;
+  }
   return cudaGetLastError();
 }
 
