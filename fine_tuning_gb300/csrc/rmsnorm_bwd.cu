@@ -486,10 +486,9 @@ template <typename T, typename Idx>
 cudaError_t bwd_typed(bool vec, const RmsNormBwdArgs &a, const DeviceInfo &dev,
                       cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
-  // rows under 8 KiB: at most two packets per thread (the backward also holds
-  // dw accumulators and w in registers; more warps per row keep it to ~64
-  // registers and more CTAs per SM); longer rows have enough warps already
-  const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1, a.H * (int64_t)sizeof(T) < 8192 ? 2 : 4);
+  // the forward's plan: the same per-thread columns and summation order, so
+  // an rstd recomputed here equals the one the forward saved bit for bit
+  const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1, 4);
   const bool has_rstd = a.rstd != nullptr;
   if (vec && !p.generic) {
     const StagedPlan sp = plan_rmsnorm_staged(p, a.H, (int)sizeof(T), 2, dev);
