@@ -354,6 +354,111 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   }
 }
 
+// One warp per token (half a head fits in the warp's lanes, NV <= 32): lane
+// (slot, j) rotates packet j of heads slot, slot + S, ... (S = 32 / NV).
+// The warp's head loads go out first; all lanes then find the token's
+// position (the same cu_seqlens addresses, so the loads are broadcast) and
+// compute its cos/sin table into the warp's own shared-memory slice;
+// __syncwarp orders the table, so apart from the one barrier that publishes
+// the frequency table at the start, warps never wait on each other.
+template <typename T, typename Idx, int N, int HPT>
+__global__ void __launch_bounds__(kCtaThreads, 3)
+qk_rope_warp(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int B, Idx rows,
+             int Hq, int NH, int D, float sgn, const __grid_constant__ RopeFreqs fr) {
+  extern __shared__ float2 tab[];  // [warps][D/2] (cos, sgn*sin)
+  __shared__ float2 freq[kRopeMaxHalf];
+  const int half = D >> 1, NV = half / N, S = 32 / NV;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = lane % NV, slot = lane / NV;
+  const Idx t = (Idx)blockIdx.x * (blockDim.x >> 5) + warp;
+  const bool active = t < rows && slot < S;
+  T *const qrow = q + t * ld_q + (Idx)j * N;
+  T *const krow = k + t * ld_k + (Idx)j * N - (Idx)Hq * D;
+  auto head = [&](int h) -> T * { return (h < Hq ? qrow : krow) + (Idx)h * D; };
+
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
+  Packet<T, N> a[HPT], b[HPT];
+#pragma unroll
+  for (int m = 0; m < HPT; ++m) {
+    const int h = slot + m * S;
+    if (active && h < NH) {
+      a[m] = load_packet<T, N>(head(h));
+      b[m] = load_packet<T, N>(head(h) + half);
+    }
+  }
+  __syncthreads();  // the frequency table
+  if (t >= rows) return;
+
+  const int p = position_of<Idx>(t, cu, B);
+  float2 *wt = tab + warp * half;
+  for (int i = lane; i < half; i += 32) {
+    const float2 f = freq[i];
+    float c, sn;
+    rope_cos_sin(p, f.x, f.y, &c, &sn);
+    wt[i] = make_float2(c, sgn * sn);
+  }
+  __syncwarp();
+  if (slot >= S) return;
+  float cv[N], sv[N];
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    const float2 v = wt[j * N + e];
+    cv[e] = v.x;
+    sv[e] = v.y;
+  }
+  for (int h0 = 0;; h0 += HPT * S) {
+#pragma unroll
+    for (int m = 0; m < HPT; ++m) {
+      const int h = h0 + slot + m * S;
+      if (h < NH) {
+        Packet<T, N> oa, ob;
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float x1 = a[m].get(e), x2 = b[m].get(e);
+          oa.set(e, fmaf(x1, cv[e], -x2 * sv[e]));
+          ob.set(e, fmaf(x2, cv[e], x1 * sv[e]));
+        }
+        store_packet<T, N>(head(h), oa);
+        store_packet<T, N>(head(h) + half, ob);
+      }
+    }
+    const int next = h0 + HPT * S;
+    if (next >= NH) break;
+#pragma unroll
+    for (int m = 0; m < HPT; ++m) {
+      const int h = next + slot + m * S;
+      if (h < NH) {
+        a[m] = load_packet<T, N>(head(h));
+        b[m] = load_packet<T, N>(head(h) + half);
+      }
+    }
+  }
+}
+
+template <typename T, typename Idx, int N>
+cudaError_t rope_warp_launch(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
+  const int NH = a.Hq + a.Hkv, half = a.D / 2, NV = half / N, S = 32 / NV;
+  const int per_lane = (NH + S - 1) / S;
+  constexpr int kWarps = kCtaThreads / 32;
+  const dim3 grid((unsigned)ceil_div(a.T, (int64_t)kWarps));
+  const size_t smem = sizeof(float2) * (size_t)kWarps * half;
+  const float sgn = a.backward ? -1.0f : 1.0f;
+#define FTK_ROPE_WARP(H)                                                                     \
+  {                                                                                          \
+    cudaError_t le_ = launch_pdl(qk_rope_warp<T, Idx, N, H>, grid, dim3(kCtaThreads), smem, s, \
+                                 (T *)a.q, (Idx)a.ld_q, (T *)a.k, (Idx)a.ld_k, a.cu, a.B,     \
+                                 (Idx)a.T, a.Hq, NH, a.D, sgn, fr);                          \
+    if (le_ != cudaSuccess) return le_;                                                      \
+    return cudaGetLastError();                                                               \
+  }
+  if (per_lane <= 1) FTK_ROPE_WARP(1)
+  if (per_lane <= 2 || N >= 8) FTK_ROPE_WARP(2)
+  FTK_ROPE_WARP(4)
+#undef FTK_ROPE_WARP
+}
+
 template <typename T, typename Idx, int N, int HPT>
 cudaError_t rope_launch(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
   const int NH = a.Hq + a.Hkv;
@@ -453,8 +558,10 @@ cudaError_t rope_typed(bool vec, const RopeArgs &a, const RopeFreqs &fr, const D
     bool launched = false;
     cudaError_t e = rope_staged_launch<T, Idx, NV>(a, fr, dev, s, &launched);
     if (e != cudaSuccess || launched) return e;
+    if (a.D / 2 / NV <= 32) return rope_warp_launch<T, Idx, NV>(a, fr, s);
     return rope_heads<T, Idx, NV>(a, fr, s);
   }
+  if (a.D / 2 <= 32) return rope_warp_launch<T, Idx, 1>(a, fr, s);
   return rope_heads<T, Idx, 1>(a, fr, s);
 }
 
