@@ -19,7 +19,6 @@ the data path); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -88,11 +87,19 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {"rmsnorm_fwd": "rmsnorm_fwd.cu", "rmsnorm_bwd": "rmsnorm_bwd.cu",
+                  "swiglu_fwd": "swiglu.cu", "swiglu_bwd": "swiglu.cu",
+                  "qk_rope_fwd": "qk_rope.cu", "qk_rope_bwd": "qk_rope.cu"}
+
+
+def kernel_source_hash(op: str) -> str:
+    """Hash of the sources an op's kernels are built from (its .cu file and
+    the shared device/launch headers)."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "fine_tuning_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+    csrc = os.path.join(ROOT, "fine_tuning_gb300", "csrc")
+    for name in sorted((KERNEL_SOURCES[op], "common.cuh", "launch.h")):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -102,7 +109,7 @@ def ncu_traffic(kernel: str, workload: str):
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(kernel)
     for line in open(path):
         parts = line.split()
         if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel \
@@ -365,20 +372,26 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
 
     # The step as one CUDA graph (its 7 launches replayed without host
-    # overhead, as a training loop would run it); per-kernel durations come
-    # from one graph per op, replayed back to back with events between them.
+    # overhead, as a training loop would run it).
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for op in ops:
             op()
+    # per kernel: a graph [L2 flush, op] and a graph [L2 flush]; the op's
+    # time is the difference of their replay times, so the graph launch
+    # latency cancels while the flush-to-op gap of a real stream stays in
     op_graphs = []
     for op in ops:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
+            flush.fill_(3)
             op()
         op_graphs.append(g)
+    flush_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(flush_graph):
+        flush.fill_(3)
     graph.replay()
-    for g in op_graphs:
+    for g in op_graphs + [flush_graph]:
         g.replay()
     torch.cuda.synchronize(dev)
 
@@ -386,7 +399,8 @@ def run_ours(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     Kk = max(1, min(K, 300))
-    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(Kk)]
+    evk = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(len(ops) + 1)] for _ in range(Kk)]
     whole0, whole1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = ""
     try:
@@ -412,18 +426,18 @@ def run_ours(args):
         dist.barrier()
     t1 = time.time()
     for i in range(Kk):
-        flush.fill_(i & 0xFF)
-        e = evk[i]
-        e[0].record()
-        for j, g in enumerate(op_graphs):
+        for (a, b), g in zip(evk[i], op_graphs + [flush_graph]):
+            a.record()
             g.replay()
-            e[j + 1].record()
+            b.record()
     torch.cuda.synchronize(dev)
     time.sleep(0.3)
     sampler.stop()
 
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    per_op = [sum(e[j].elapsed_time(e[j + 1]) for e in evk) / Kk for j in range(len(ops))]
+    t_flush = sum(e[-1][0].elapsed_time(e[-1][1]) for e in evk) / Kk
+    per_op = [sum(e[j][0].elapsed_time(e[j][1]) for e in evk) / Kk - t_flush
+              for j in range(len(ops))]
     wall_ms = whole0.elapsed_time(whole1)
 
     el_max, bytes_all = reduce_timing(step_ms * K / 1e3, step_bytes * K)
@@ -465,8 +479,8 @@ def run_ours(args):
                      else "fallback 6.8 TB/s"},
         "gpu_launches": LAUNCHES_PER_STEP * (K + Kk),
         "timing": (f"step: {K} replays of a CUDA graph of the step's {LAUNCHES_PER_STEP} "
-                   f"launches, CUDA events around each replay; per kernel: {Kk} steps of "
-                   "one-op graphs replayed back to back, CUDA events between them"),
+                   f"launches, CUDA events around each replay; per kernel: {Kk} replays of a "
+                   "graph [L2 flush, op] minus a graph [L2 flush], CUDA events around each"),
         "wall_ms_timed_region": round(wall_ms, 3),
     }
     out["clocks"] = sampler.summary(t0, t1)

@@ -207,6 +207,8 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   const int grp = warp / W, wig = warp - grp * W;
   const int gi = wig * 32 + lane, G = W * 32;
   const bool leader = gi == 0;
+  const int HS = G / NV;  // head slots of the group (NV <= G: the launcher checks)
+  const int j = gi % NV, slot = gi / NV;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf) + grp * S;               // [R][S]
   float2 *cs = reinterpret_cast<float2 *>(sbuf + off_cs) + (size_t)grp * TB * half;  // [R][TB][half]
   unsigned char *ring = sbuf + off_stage + (size_t)grp * S * stage_bytes;      // [R][S][stage]
@@ -320,27 +322,36 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
     if (live) live = mbar_wait_bounded(&bars[s], (uint32_t)((it / S) & 1), wait_limit, status);
     group_sync();
     unsigned char *st = ring + (size_t)s * stage_bytes;
-    const int items = nt * NH * NV;
-    for (int m = gi; m < items; m += G) {
-      const int j = m % NV, rest = m / NV;
-      const int h = rest % NH, tt = rest / NH;
-      T *v = reinterpret_cast<T *>(h < Hq ? st + ((size_t)tt * Hq + h) * D * sizeof(T)
-                                          : st + (size_t)TB * qrow_b +
-                                                ((size_t)tt * Hkv + (h - Hq)) * D * sizeof(T)) +
-             j * N;
-      const Packet<T, N> pa = *reinterpret_cast<const Packet<T, N> *>(v);
-      const Packet<T, N> pb = *reinterpret_cast<const Packet<T, N> *>(v + half);
-      const float2 *c2 = cs + tt * half + j * N;
-      Packet<T, N> oa, ob;
+    // lane (slot, j): packet j of heads slot, slot + HS, ... of every token;
+    // its N cos/sin pairs are read once per token
+    if (slot < HS) {
+      for (int tt = 0; tt < nt; ++tt) {
+        const float2 *c2 = cs + tt * half + j * N;
+        float cv[N], sv[N];
 #pragma unroll
-      for (int e = 0; e < N; ++e) {
-        const float2 r = c2[e];
-        const float x1 = pa.get(e), x2 = pb.get(e);
-        oa.set(e, fmaf(x1, r.x, -x2 * r.y));
-        ob.set(e, fmaf(x2, r.x, x1 * r.y));
+        for (int e = 0; e < N; ++e) {
+          const float2 r = c2[e];
+          cv[e] = r.x;
+          sv[e] = r.y;
+        }
+        T *qt = reinterpret_cast<T *>(st) + (size_t)tt * Hq * D + j * N;
+        T *kt = reinterpret_cast<T *>(st + (size_t)TB * qrow_b) + ((size_t)tt * Hkv - Hq) * D + j * N;
+#pragma unroll 2
+        for (int h = slot; h < NH; h += HS) {
+          T *v = (h < Hq ? qt : kt) + (size_t)h * D;
+          const Packet<T, N> pa = *reinterpret_cast<const Packet<T, N> *>(v);
+          const Packet<T, N> pb = *reinterpret_cast<const Packet<T, N> *>(v + half);
+          Packet<T, N> oa, ob;
+#pragma unroll
+          for (int e = 0; e < N; ++e) {
+            const float x1 = pa.get(e), x2 = pb.get(e);
+            oa.set(e, fmaf(x1, cv[e], -x2 * sv[e]));
+            ob.set(e, fmaf(x2, cv[e], x1 * sv[e]));
+          }
+          *reinterpret_cast<Packet<T, N> *>(v) = oa;
+          *reinterpret_cast<Packet<T, N> *>(v + half) = ob;
+        }
       }
-      *reinterpret_cast<Packet<T, N> *>(v) = oa;
-      *reinterpret_cast<Packet<T, N> *>(v + half) = ob;
     }
     fence_proxy_async_smem();  // this thread's stage writes before the bulk store reads them
     group_sync();
@@ -527,7 +538,7 @@ cudaError_t rope_staged_launch(const RopeArgs &a, const RopeFreqs &fr, const Dev
     smem = off_stage + (size_t)R * S * stage_bytes;
     if (smem + static_smem <= (size_t)dev.max_smem_optin) break;
   }
-  if (S < 2 || stage_bytes >= (1u << 20)) return cudaSuccess;  // register kernel instead
+  if (S < 2 || stage_bytes >= (1u << 20) || NV > 32 * W) return cudaSuccess;  // register kernel
   auto kern = qk_rope_staged<T, Idx, N>;
   const int threads = 32 * W * R;
   const int occ = blocks_per_sm((const void *)kern, threads, smem, dev, 8);
