@@ -490,6 +490,7 @@ def run_ours(args):
         out["e2e"] = e2e_leg(batch, ops, dev, args.e2e_steps, step_bytes)
     if do_cpu:
         out["cpu_baseline"], out["parity"] = cpu_leg(wl, batch, gpu_out, cut, args.cpu_seconds)
+        out["packing"] = packing_leg(wl)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -563,6 +564,50 @@ def e2e_leg(batch, ops, dev, steps, step_bytes):
             "ms_per_step": round(el_max * 1e3 / steps, 3), "steps": steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "overlap": "3 streams: copy-in of step k+1, kernels of step k, copy-out of step k-1"}
+
+
+# ------------------------------------------------------ packing (host)
+
+def packing_leg(wl, n_seq=200_000, batch=8):
+    """Best-Fit-Decreasing packing of a corpus with the workload's length mix
+    into bins of T tokens: host throughput of the library routine and of the
+    oracle (bounded sample), and how much of the padding waste of plain
+    padded batching (batches of `batch` sequences padded to their longest)
+    the packing recovers."""
+    import numpy as np
+
+    from fine_tuning_gb300 import ftk
+    from fine_tuning_gb300 import workloads as W
+    from oracle.packing import bfd_pack as oracle_bfd
+    reps = []
+    total = 0
+    i = 0
+    while total < n_seq:
+        lens = W.draw_lengths(__import__("dataclasses").replace(wl, seed=wl.seed + 7919 * i))
+        reps.append(lens)
+        total += lens.size
+        i += 1
+    lens = np.concatenate(reps)[:n_seq].astype(np.int32)
+    t = time.perf_counter()
+    bin_of, order, bin_start = ftk.bfd_pack(lens, wl.T)
+    el = time.perf_counter() - t
+    bins = len(bin_start) - 1
+    real = int(lens.sum())
+    m = 20_000
+    t = time.perf_counter()
+    oracle_bfd(lens[:m].tolist(), wl.T)
+    el_o = time.perf_counter() - t
+    nb = (lens.size + batch - 1) // batch
+    padded = sum(int(lens[b * batch:(b + 1) * batch].max()) * min(batch, lens.size - b * batch)
+                 for b in range(nb))
+    waste_pad = padded - real
+    waste_pack = bins * wl.T - real
+    return {"sequences": int(lens.size), "capacity_tokens": wl.T, "bins": bins,
+            "sequences_per_s": round(lens.size / el, 1),
+            "oracle_sequences_per_s": round(m / el_o, 1), "oracle_sample": m,
+            "fill": round(real / (bins * wl.T), 4),
+            "padding_waste_recovered": round(1 - waste_pack / waste_pad, 4),
+            "vs": f"batches of {batch} padded to their longest sequence"}
 
 
 # -------------------------------------------------------- reference arm

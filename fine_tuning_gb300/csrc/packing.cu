@@ -1,0 +1,65 @@
+// Best-Fit-Decreasing packing of variable-length sequences into bins of a
+// fixed token capacity: the step that produces the packed batches (and
+// their cu_seqlens) the QK-RoPE kernels consume.
+//
+// Chronicals (arXiv 2601.02609), abstract, optimisation (4): Best-Fit
+// Decreasing sequence packing.  Host code (the data loader's side of the
+// path); no device memory is touched.
+//
+// Longest sequence first (equal lengths: lower index first); each goes to
+// the open bin with the least room that still holds it (equal room: lower
+// bin index), else to a new bin.  Open bins are kept in an ordered set keyed
+// by (room, bin), so the best fit is one lower_bound: O(n log n) in all.
+#include <algorithm>
+#include <climits>
+#include <new>
+#include <set>
+#include <utility>
+#include <vector>
+
+#include "ftk.h"
+
+extern "C" FTK_API ftk_status ftk_bfd_pack(const int32_t *lengths, int64_t n, int32_t capacity,
+                                           int32_t *bin_of, int64_t *order, int64_t *bin_start,
+                                           int64_t *n_bins) {
+  if (n < 0 || capacity < 1 || n >= INT32_MAX) return FTK_ERR_SHAPE;
+  if (!n_bins || (n > 0 && (!lengths || !bin_of || !order || !bin_start)) || (!bin_start && n == 0))
+    return FTK_ERR_NULL;
+  for (int64_t i = 0; i < n; ++i)
+    if (lengths[i] < 0 || lengths[i] > capacity) return FTK_ERR_SHAPE;
+  try {
+    std::vector<int32_t> by_len(n);
+    for (int64_t i = 0; i < n; ++i) by_len[i] = (int32_t)i;
+    std::stable_sort(by_len.begin(), by_len.end(),
+                     [&](int32_t a, int32_t b) { return lengths[a] > lengths[b]; });
+    std::set<std::pair<int32_t, int32_t>> open;  // (room left, bin)
+    std::vector<int64_t> count;
+    int32_t bins = 0;
+    for (int32_t i : by_len) {
+      const int32_t len = lengths[i];
+      auto it = open.lower_bound({len, INT32_MIN});
+      int32_t b, room;
+      if (it == open.end()) {
+        b = bins++;
+        room = capacity - len;
+        count.push_back(0);
+      } else {
+        b = it->second;
+        room = it->first - len;
+        open.erase(it);
+      }
+      open.insert({room, b});
+      bin_of[i] = b;
+      ++count[b];
+    }
+    // members of each bin, in the order they were placed
+    bin_start[0] = 0;
+    for (int32_t b = 0; b < bins; ++b) bin_start[b + 1] = bin_start[b] + count[b];
+    std::vector<int64_t> fill(bin_start, bin_start + bins);
+    for (int32_t i : by_len) order[fill[bin_of[i]]++] = i;
+    *n_bins = bins;
+  } catch (const std::bad_alloc &) {
+    return FTK_ERR_WORKSPACE;
+  }
+  return FTK_OK;
+}

@@ -57,6 +57,7 @@ def library() -> ctypes.CDLL:
         "ftk_swiglu_bwd": (st, [vp, i64, vp, vp, i64, vp, vp, i64, i64, i64, dt, vp]),
         "ftk_qk_rope_fwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, dt, vp]),
         "ftk_qk_rope_bwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, dt, vp]),
+        "ftk_bfd_pack": (st, [vp, i64, i32, vp, vp, vp, vp]),
         "ftk_device_status": (st, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
         "ftk_selftest_wait_timeout": (st, [i64, vp]),
         "ftk_status_str": (ctypes.c_char_p, [st]),
@@ -232,6 +233,32 @@ def qk_rope_fwd(q, k, cu_seqlens, theta):
 def qk_rope_bwd(dq, dk, cu_seqlens, theta):
     """Backward of qk_rope_fwd: rotate dq, dk by -phi IN PLACE; returns (dq, dk)."""
     return _rope("ftk_qk_rope_bwd", dq, dk, cu_seqlens, theta)
+
+
+# ---------------------------------------------------------------- packing
+
+def bfd_pack(lengths, capacity: int):
+    """Best-Fit-Decreasing packing (host).  Returns (bin_of, order, bin_start):
+    numpy arrays; bin b holds sequences order[bin_start[b]:bin_start[b+1]]."""
+    import numpy as np
+    lens = np.ascontiguousarray(np.asarray(lengths, dtype=np.int32))
+    n = lens.size
+    bin_of = np.empty(n, dtype=np.int32)
+    order = np.empty(n, dtype=np.int64)
+    bin_start = np.empty(n + 1, dtype=np.int64)
+    nb = ctypes.c_int64(0)
+    _call("ftk_bfd_pack", lens.ctypes.data, n, int(capacity), bin_of.ctypes.data,
+          order.ctypes.data, bin_start.ctypes.data, ctypes.byref(nb))
+    return bin_of, order, bin_start[: nb.value + 1].copy()
+
+
+def packed_cu_seqlens(lengths, order, bin_start, b: int):
+    """int32 cu_seqlens of packed bin b (its sequences in placement order)."""
+    import numpy as np
+    members = np.asarray(order)[bin_start[b]:bin_start[b + 1]]
+    cu = np.zeros(members.size + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(np.asarray(lengths, dtype=np.int64)[members])
+    return cu.astype(np.int32)
 
 
 WAIT_TIMEOUT = 1  # FTK_DEVSTAT_WAIT_TIMEOUT

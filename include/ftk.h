@@ -181,6 +181,27 @@ FTK_API ftk_status ftk_qk_rope_bwd(void *dq, int64_t ld_q, void *dk, int64_t ld_
                            int32_t Hq, int32_t Hkv, int32_t D, double theta,
                            ftk_dtype dtype, ftk_stream_t stream);
 
+/* -------------------------------------------------------------- packing */
+
+/* Best-Fit-Decreasing packing of n sequences into bins of `capacity` tokens
+ * ("Chronicals", arXiv 2601.02609, abstract, optimisation (4): Best-Fit
+ * Decreasing sequence packing recovers the compute padding wastes).  Host
+ * code; every pointer is a HOST pointer.
+ *   Sequences are taken longest first (equal lengths: lower index first);
+ *   each goes to the open bin with the least room that still holds it
+ *   (equal room: lower bin index), else to a new bin.
+ * lengths: int32 [n], each in [0, capacity].  Outputs, caller-allocated:
+ * bin_of: int32 [n], the bin of each sequence; order: int64 [n], the
+ * sequence indices bin by bin, each bin's in the order they were placed
+ * (concatenating them gives the packed batch); bin_start: int64 [n + 1]
+ * (room for the worst case of one bin per sequence), bin b holds
+ * order[bin_start[b] .. bin_start[b+1]); *n_bins: the number of bins.
+ * A length outside [0, capacity] gives FTK_ERR_SHAPE and writes nothing.
+ * O(n log n) time, O(n) memory. */
+FTK_API ftk_status ftk_bfd_pack(const int32_t *lengths, int64_t n, int32_t capacity,
+                                int32_t *bin_of, int64_t *order, int64_t *bin_start,
+                                int64_t *n_bins);
+
 /* ------------------------------------------------------------ utilities */
 
 /* Bits of the device status word. */

@@ -1,0 +1,59 @@
+"""The library's Best-Fit-Decreasing packing (host C++) against the oracle:
+the same bins, members and order, exactly (integer work is bit-exact)."""
+import numpy as np
+import pytest
+
+from oracle.packing import bfd_pack as oracle_bfd, cu_seqlens_of_bin
+from fine_tuning_gb300 import build, workloads as W
+
+
+@pytest.fixture(scope="module")
+def ftk():
+    build.build()
+    from fine_tuning_gb300 import ftk
+    ftk.library()
+    return ftk
+
+
+def check(ftk, lens, cap):
+    bin_of, order, bin_start = ftk.bfd_pack(lens, cap)
+    ob, obins = oracle_bfd(list(lens), cap)
+    assert bin_of.tolist() == ob
+    assert len(bin_start) - 1 == len(obins)
+    for b, members in enumerate(obins):
+        assert order[bin_start[b]:bin_start[b + 1]].tolist() == members
+        assert ftk.packed_cu_seqlens(lens, order, bin_start, b).tolist() == \
+            cu_seqlens_of_bin(lens, members)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_random_small(ftk, seed):
+    rng = np.random.default_rng(seed)
+    cap = int(rng.integers(1, 200))
+    lens = rng.integers(0, cap + 1, size=int(rng.integers(0, 300))).tolist()
+    check(ftk, lens, cap)
+
+
+@pytest.mark.parametrize("name", ["qwen2.5-0.5b", "llama-3.2-1b", "qwen3-8b"])
+def test_workload_length_mixes(ftk, name):
+    # a corpus of sequences with the workload's length mix, packed into bins
+    # of the workload's token budget
+    wl = W.WORKLOADS[name]
+    lens = np.concatenate([W.draw_lengths(wl)] * 3)[:400]
+    check(ftk, lens.tolist(), wl.T)
+
+
+def test_edges(ftk):
+    check(ftk, [], 5)
+    check(ftk, [5], 5)
+    check(ftk, [0, 0, 0], 1)
+    check(ftk, [3] * 50, 6)
+    check(ftk, [1] * 100 + [99] * 10, 100)
+    lib = ftk.library()
+    import ctypes
+    a = (ctypes.c_int32 * 1)(6)
+    out32 = (ctypes.c_int32 * 1)()
+    out64 = (ctypes.c_int64 * 2)()
+    nb = ctypes.c_int64()
+    assert lib.ftk_bfd_pack(a, 1, 5, out32, out64, out64, ctypes.byref(nb)) == 2  # too long
+    assert lib.ftk_bfd_pack(a, 1, 0, out32, out64, out64, ctypes.byref(nb)) == 2  # no capacity
