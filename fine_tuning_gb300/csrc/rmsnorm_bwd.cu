@@ -207,9 +207,14 @@ rmsnorm_bwd_staged(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restri
 
   bool live = true;
   int it = 0;
+  // the saved r of each row is loaded one iteration ahead: the rows arrive
+  // through the stages long before they are needed, so a load issued at the
+  // row's own iteration would put a DRAM round trip on every row's path
+  float r_next = (HAS_RSTD && first < rows) ? rstd[first] : 0.f;
   for (Idx row = first; row < rows; row += stride, ++it) {
     const int s = it % S;
-    float r = HAS_RSTD ? rstd[row] : 0.f;
+    float r = r_next;
+    if (HAS_RSTD && row + stride < rows) r_next = rstd[row + stride];
     if (live) live = mbar_wait_bounded(&gb[s], (uint32_t)((it / S) & 1), wait_limit, status);
     const T *xs = reinterpret_cast<const T *>(ring + (size_t)s * stage_bytes);
     const T *gs = reinterpret_cast<const T *>(ring + (size_t)s * stage_bytes + row_bytes);
