@@ -40,6 +40,10 @@ def _load():
         lib.oracle_qk_rope.restype = ctypes.c_int
         lib.oracle_positions.argtypes = [I64, I64, i64, I32, i32]
         lib.oracle_positions.restype = ctypes.c_int
+        lib.oracle_rmsnorm_add_fwd.argtypes = [D, D, D, D, D, D, i64, i64, f64, ctypes.c_int]
+        lib.oracle_rmsnorm_add_fwd.restype = None
+        lib.oracle_rmsnorm_add_bwd.argtypes = [D, D, D, D, D, D, D, D, i64, i64, f64]
+        lib.oracle_rmsnorm_add_bwd.restype = None
         lib.oracle_threads.argtypes = []
         lib.oracle_threads.restype = ctypes.c_int
         _lib = lib
@@ -79,6 +83,33 @@ def rmsnorm_bwd(dy, x, w, eps, scales=False):
     dws = np.empty(H) if scales else None
     _load().oracle_rmsnorm_bwd(_p(dy), _p(x), _p(w), _p(dx), _p(dw), _p(dxs),
                                _p(dws), T, H, float(eps))
+    return (dx, dw, dxs, dws) if scales else (dx, dw)
+
+
+STORAGE = {"f32": 0, "bf16": 1, "exact": 2}
+
+
+def rmsnorm_add_fwd(x, res, w, eps, storage="bf16"):
+    """Returns (h, y, rstd): h = x + res added in fp32 and rounded to the
+    storage type ("f32", "bf16", or "exact" = no rounding), y = rmsnorm(h)*w."""
+    x, res, w = _f64(x), _f64(res), _f64(w)
+    T, H = x.shape
+    h, y, rstd = np.empty_like(x), np.empty_like(x), np.empty(T)
+    _load().oracle_rmsnorm_add_fwd(_p(x), _p(res), _p(w), _p(h), _p(y), _p(rstd), T, H,
+                                   float(eps), STORAGE[storage])
+    return h, y, rstd
+
+
+def rmsnorm_add_bwd(dy, dh, h, w, eps, scales=False):
+    """Returns (dx, dw) or (dx, dw, dx_scale, dw_scale); dx is the gradient
+    of both x and res."""
+    dy, dh, h, w = _f64(dy), _f64(dh), _f64(h), _f64(w)
+    T, H = h.shape
+    dx, dw = np.empty_like(h), np.empty(H)
+    dxs = np.empty_like(h) if scales else None
+    dws = np.empty(H) if scales else None
+    _load().oracle_rmsnorm_add_bwd(_p(dy), _p(dh), _p(h), _p(w), _p(dx), _p(dw), _p(dxs),
+                                   _p(dws), T, H, float(eps))
     return (dx, dw, dxs, dws) if scales else (dx, dw)
 
 

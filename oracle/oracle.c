@@ -131,6 +131,65 @@ ORACLE_API void oracle_rmsnorm_bwd(const double *dy, const double *x,
     free(r);
 }
 
+/* ---------------------------------------------- RMSNorm with residual add */
+
+/* The storage rounding of a sum: the two stored values are added in fp32
+ * (the precision the kernels add in), then the fp32 sum is rounded to the
+ * storage type: kept (storage 0 = fp32), rounded to nearest even on its low
+ * 16 bits (storage 1 = bf16), or not rounded at all (storage 2 = exact, the
+ * double sum; used by the finite-difference pins). */
+static double stored_sum(double a, double b, int storage)
+{
+    if (storage == 2)
+        return a + b;
+    float f = (float)a + (float)b;
+    if (storage == 0)
+        return (double)f;
+    union {
+        float f;
+        uint32_t u;
+    } v;
+    v.f = f;
+    uint32_t lsb = (v.u >> 16) & 1u;
+    v.u = (v.u + 0x7FFFu + lsb) & 0xFFFF0000u;
+    return (double)v.f;
+}
+
+/* Pre-norm residual step: h = x + res, stored (see stored_sum), then
+ * y = rmsnorm(h) * w with r[t] = 1/sqrt(mean_j h[t,j]^2 + eps).
+ * h, y, rstd are outputs (rstd nullable). */
+ORACLE_API void oracle_rmsnorm_add_fwd(const double *x, const double *res,
+                                       const double *w, double *h, double *y,
+                                       double *rstd, int64_t T, int64_t H,
+                                       double eps, int storage)
+{
+    int64_t n = T * H, i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < n; ++i)
+        h[i] = stored_sum(x[i], res[i], storage);
+    oracle_rmsnorm_fwd(h, w, y, rstd, T, H, eps);
+}
+
+/* Backward of the step above: the gradient reaching h is dh (from the
+ * residual stream) plus the norm's backward of dy, and it is the gradient of
+ * both x and res:  dx = dh + (r w dy - r^3 h c / H),  dw as in
+ * oracle_rmsnorm_bwd.  dx_scale adds |dh| to the norm's scale (nullable). */
+ORACLE_API void oracle_rmsnorm_add_bwd(const double *dy, const double *dh,
+                                       const double *h, const double *w,
+                                       double *dx, double *dw, double *dx_scale,
+                                       double *dw_scale, int64_t T, int64_t H,
+                                       double eps)
+{
+    oracle_rmsnorm_bwd(dy, h, w, dx, dw, dx_scale, dw_scale, T, H, eps);
+    int64_t n = T * H, i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < n; ++i) {
+        dx[i] += dh[i];
+        if (dx_scale)
+            dx_scale[i] += fabs(dh[i]);
+    }
+}
+
 /* ----------------------------------------------------------------- SwiGLU */
 
 static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }

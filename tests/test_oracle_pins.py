@@ -303,3 +303,55 @@ def test_rope_rejects_out_of_batch_token():
     cu, q, k = _packed_case()
     with pytest.raises(ValueError):
         oracle.qk_rope(q[:1], k[:1], cu, 1e4, tok=[int(cu[-1])])
+
+
+# ------------------------------------------------- RMSNorm with residual add
+
+def test_rmsnorm_add_reduces_to_rmsnorm():
+    # res = 0: h = x exactly (a stored value plus zero), y = rmsnorm(x)
+    x = RNG.standard_normal((7, 24)).astype(np.float32).astype(np.float64)
+    w = 1.0 + 0.1 * RNG.standard_normal(24)
+    h, y, r = oracle.rmsnorm_add_fwd(x, np.zeros_like(x), w, 1e-6, storage="f32")
+    y0, r0 = oracle.rmsnorm_fwd(x, w, 1e-6)
+    np.testing.assert_array_equal(h, x)
+    np.testing.assert_array_equal(y, y0)
+    np.testing.assert_array_equal(r, r0)
+
+
+def test_rmsnorm_add_storage_rounding():
+    # bf16 keeps 8 significant bits: ulp(1) = 2^-7.  1 + 2^-8 is a tie between
+    # 1 and 1 + 2^-7 and rounds to the even 1; 1 + 3*2^-8 is a tie between
+    # 1 + 2^-7 (odd) and 1 + 2^-6 (even) and rounds up; 1 + 2^-8 + 2^-12 is
+    # above the tie and rounds up.
+    x = np.array([[1.0, 1.0, 1.0, -1.0]])
+    res = np.array([[2.0 ** -8, 3 * 2.0 ** -8, 2.0 ** -8 + 2.0 ** -12, -(2.0 ** -8)]])
+    h, _, _ = oracle.rmsnorm_add_fwd(x, res, np.ones(4), 1e-6, storage="bf16")
+    np.testing.assert_array_equal(h[0], [1.0, 1 + 2.0 ** -6, 1 + 2.0 ** -7, -1.0])
+    hf, _, _ = oracle.rmsnorm_add_fwd(x, res, np.ones(4), 1e-6, storage="f32")
+    np.testing.assert_array_equal(hf[0], x[0] + res[0])  # exact in fp32
+    # fp32 rounding: 1 + 2^-24 is a tie between 1 and 1 + 2^-23 -> 1
+    hf, _, _ = oracle.rmsnorm_add_fwd(np.ones((1, 1)), np.full((1, 1), 2.0 ** -24),
+                                      np.ones(1), 1e-6, storage="f32")
+    assert hf[0, 0] == 1.0
+
+
+def test_rmsnorm_add_bwd_matches_finite_differences():
+    # L = sum(gy * y) + sum(gh * h) with h = x + res unrounded; dL/dx = dL/dres
+    T, H = 4, 10
+    x, res = RNG.standard_normal((T, H)), RNG.standard_normal((T, H))
+    w = 1.0 + 0.1 * RNG.standard_normal(H)
+    gy, gh = RNG.standard_normal((T, H)), RNG.standard_normal((T, H))
+
+    def loss(xx, rr, ww):
+        h, y, _ = oracle.rmsnorm_add_fwd(xx, rr, ww, 1e-6, storage="exact")
+        return float((gy * y).sum() + (gh * h).sum())
+
+    h, _, _ = oracle.rmsnorm_add_fwd(x, res, w, 1e-6, storage="exact")
+    dx, dw = oracle.rmsnorm_add_bwd(gy, gh, h, w, 1e-6)
+    _fd_close(_central_fd(lambda xx: loss(xx, res, w), x.copy()), dx)
+    _fd_close(_central_fd(lambda rr: loss(x, rr, w), res.copy()), dx)
+    _fd_close(_central_fd(lambda ww: loss(x, res, ww), w.copy()), dw)
+    # linear in the residual gradient
+    dx0, dw0 = oracle.rmsnorm_add_bwd(gy, np.zeros_like(gh), h, w, 1e-6)
+    np.testing.assert_allclose(dx - dx0, gh, atol=1e-14)
+    np.testing.assert_array_equal(dw, dw0)
