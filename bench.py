@@ -48,6 +48,7 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="qwen2.5-0.5b")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-ext", action="store_true", help="skip timing the widened ops")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU work of the oracle baseline sample")
@@ -87,9 +88,14 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = {"rmsnorm_fwd": "rmsnorm_fwd.cu", "rmsnorm_bwd": "rmsnorm_bwd.cu",
-                  "swiglu_fwd": "swiglu.cu", "swiglu_bwd": "swiglu.cu",
-                  "qk_rope_fwd": "qk_rope.cu", "qk_rope_bwd": "qk_rope.cu"}
+KERNEL_SOURCES = {"rmsnorm_fwd": ("rmsnorm_fwd.cu",),
+                  "rmsnorm_bwd": ("rmsnorm_bwd.cu", "rmsnorm_bwd.cuh"),
+                  "swiglu_fwd": ("swiglu.cu",), "swiglu_bwd": ("swiglu.cu",),
+                  "qk_rope_fwd": ("qk_rope.cu",), "qk_rope_bwd": ("qk_rope.cu",),
+                  "rmsnorm_add_fwd": ("rmsnorm_fwd.cu",),
+                  "rmsnorm_add_bwd": ("rmsnorm_add_bwd.cu", "rmsnorm_bwd.cuh")}
+# widened ops timed beside the step (not part of it)
+EXT_OPS = ("rmsnorm_add_fwd", "rmsnorm_add_bwd")
 
 
 def kernel_source_hash(op: str) -> str:
@@ -97,7 +103,7 @@ def kernel_source_hash(op: str) -> str:
     the shared device/launch headers)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fine_tuning_gb300", "csrc")
-    for name in sorted((KERNEL_SOURCES[op], "common.cuh", "launch.h")):
+    for name in sorted(KERNEL_SOURCES[op] + ("common.cuh", "launch.h")):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -483,6 +489,9 @@ def run_ours(args):
                    "graph [L2 flush, op] minus a graph [L2 flush], CUDA events around each"),
         "wall_ms_timed_region": round(wall_ms, 3),
     }
+    if not args.no_ext:
+        out["extensions"] = ext_leg(batch, flush, flush_graph, dev, Kk, hbm, src)
+        out["gpu_launches"] += 3 * Kk  # add-norm forward (1) and backward (2) launches
     out["clocks"] = sampler.summary(t0, t1)
     out["device_status"] = ftk.device_status(clear=True)  # 0: no pipeline wait ran out
 
@@ -496,6 +505,68 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
+    """The widened ops (not part of the step), each timed like a step kernel:
+    replays of a graph [L2 flush, op] minus the graph [L2 flush].  They run
+    after the timed step region, on the same batch (the residual stream and
+    its gradient drawn beside it)."""
+    import torch
+
+    from fine_tuning_gb300 import ftk
+    from fine_tuning_gb300 import workloads as W
+    wl, i = batch.wl, batch.inputs
+    extra = W.rmsnorm_add_inputs(wl, dev)
+    res, dres = extra["res"], extra["dh"]
+    T, H, dt = wl.T, wl.H, wl.torch_dtype
+    h = torch.empty((T, H), dtype=dt, device=dev)
+    y = torch.empty((T, H), dtype=dt, device=dev)
+    rstd = torch.empty((T,), dtype=torch.float32, device=dev)
+    dx = torch.empty((T, H), dtype=dt, device=dev)
+    dw = torch.empty((H,), dtype=torch.float32, device=dev)
+    ops = {
+        "rmsnorm_add_fwd": lambda: ftk.rmsnorm_add_fwd(i["x"], res, i["w"], wl.eps, h=h, y=y,
+                                                       rstd=rstd),
+        "rmsnorm_add_bwd": lambda: ftk.rmsnorm_add_bwd(i["dy"], dres, h, i["w"], rstd, wl.eps,
+                                                       dx=dx, dw=dw, workspace=batch.ws),
+    }
+    for op in ops.values():  # warm-up (and the first, allocating, launch)
+        op()
+    graphs = {}
+    for name, op in ops.items():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            flush.fill_(5)
+            op()
+        graphs[name] = g
+    for g in list(graphs.values()) * 3:
+        g.replay()
+    torch.cuda.synchronize(dev)
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)] for n in list(graphs) + ["flush"]}
+    for k in range(reps):
+        for n, g in list(graphs.items()) + [("flush", flush_graph)]:
+            a, b = ev[n][k]
+            a.record()
+            g.replay()
+            b.record()
+    torch.cuda.synchronize(dev)
+    t_flush = sum(a.elapsed_time(b) for a, b in ev["flush"]) / reps
+    ib, toks = W.ideal_bytes(wl), W.tokens_per_call(wl)
+    out = {}
+    for n in graphs:
+        ms = sum(a.elapsed_time(b) for a, b in ev[n]) / reps - t_flush
+        gbs = ib[n] / (ms * 1e-3) / 1e9
+        out[n] = {"us": round(ms * 1e3, 2), "GB_s": round(gbs, 1),
+                  "frac_of_measured_hbm" if src == "measured" else "frac_of_fallback_hbm":
+                      round(gbs / hbm, 4),
+                  "tokens_per_s": round(toks[n] / (ms * 1e-3), 1), "ideal_bytes": ib[n],
+                  "launches": 1 if n.endswith("fwd") else 2}
+    out["timing"] = (f"{reps} replays of a graph [L2 flush, op] minus a graph [L2 flush], "
+                     "CUDA events around each; outside the step's timed region")
+    del h, y, rstd, dx, dw, res, dres, extra
+    return out
 
 
 def e2e_leg(batch, ops, dev, steps, step_bytes):

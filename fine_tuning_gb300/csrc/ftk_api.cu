@@ -139,33 +139,140 @@ FTK_API ftk_status ftk_selftest_wait_timeout(int64_t limit_cycles, ftk_stream_t 
 
 // ------------------------------------------------------------------ RMSNorm
 
-FTK_API ftk_status ftk_rmsnorm_fwd(const void *x, int64_t ldx, const void *w, void *y,
-                                   int64_t ldy, float *rstd, int64_t T, int64_t H, float eps,
-                                   ftk_dtype dtype, ftk_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by the plain and the residual-add forward; res == nullptr is the
+// plain norm (h unused).
+ftk_status rmsnorm_fwd_checked(const void *x, int64_t ldx, const void *res, int64_t ldr,
+                               const void *w, void *h, int64_t ldh, void *y, int64_t ldy,
+                               float *rstd, int64_t T, int64_t H, float eps, ftk_dtype dtype,
+                               ftk_stream_t stream) {
+  const bool add = res != nullptr;
   if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
   if (T < 0 || H < 1 || ldx < H || ldy < H || T >= (int64_t(1) << 31)) return FTK_ERR_SHAPE;
+  if (add && (ldr < H || ldh < H)) return FTK_ERR_SHAPE;
   if (T == 0) return FTK_OK;
-  if (!x || !w || !y) return FTK_ERR_NULL;
+  if (!x || !w || !y || (add && !h)) return FTK_ERR_NULL;
   const DType dt = (DType)dtype;
   const int64_t es = ftk::dtype_bytes(dt);
-  if (!aligned(x, es) || !aligned(w, es) || !aligned(y, es) || !aligned(rstd, 4))
+  if (!aligned(x, es) || !aligned(w, es) || !aligned(y, es) || !aligned(rstd, 4) ||
+      !aligned(res, es) || !aligned(h, es))
     return FTK_ERR_ALIGN;
   const View vx = view(x, T, ldx, H, es), vy = view(y, T, ldy, H, es);
   const View vw = view(w, 1, H, H, es), vr = view(rstd, 1, T, T, 4);
-  if (!same_view(vx, vy) && may_overlap(vx, vy)) return FTK_ERR_ALIAS;
+  const View vres = view(res, add ? T : 0, ldr, H, es), vh = view(h, add ? T : 0, ldh, H, es);
+  if (!add) {
+    if (!same_view(vx, vy) && may_overlap(vx, vy)) return FTK_ERR_ALIAS;
+  } else {
+    // h may replace x or res in place; y overlaps nothing
+    if (!same_view(vh, vx) && may_overlap(vh, vx)) return FTK_ERR_ALIAS;
+    if (!same_view(vh, vres) && may_overlap(vh, vres)) return FTK_ERR_ALIAS;
+    if (may_overlap(vh, vw) || may_overlap(vh, vy)) return FTK_ERR_ALIAS;
+    if (may_overlap(vy, vx) || may_overlap(vy, vres)) return FTK_ERR_ALIAS;
+    if (rstd && (may_overlap(vr, vres) || may_overlap(vr, vh))) return FTK_ERR_ALIAS;
+  }
   if (may_overlap(vy, vw)) return FTK_ERR_ALIAS;
   if (rstd && (may_overlap(vr, vx) || may_overlap(vr, vy) || may_overlap(vr, vw)))
     return FTK_ERR_ALIAS;
 
   const int n = dt == DType::F32 ? 4 : 8;
-  const bool vec = aligned(x, 16) && aligned(y, 16) && aligned(w, 16) && H % n == 0 &&
-                   ldx % n == 0 && ldy % n == 0;
-  const bool wide = vx.max_offset() > kNarrowLimit || vy.max_offset() > kNarrowLimit;
+  bool vec = aligned(x, 16) && aligned(y, 16) && aligned(w, 16) && H % n == 0 && ldx % n == 0 &&
+             ldy % n == 0;
+  if (add) vec = vec && aligned(res, 16) && aligned(h, 16) && ldr % n == 0 && ldh % n == 0;
+  bool wide = vx.max_offset() > kNarrowLimit || vy.max_offset() > kNarrowLimit;
+  if (add) wide = wide || vres.max_offset() > kNarrowLimit || vh.max_offset() > kNarrowLimit;
   ftk::DeviceInfo dev;
   cudaError_t e = device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   ftk::RmsNormFwdArgs a{x, ldx, w, y, ldy, rstd, T, H, eps};
+  if (add) {
+    a.res = res;
+    a.ldr = ldr;
+    a.h = h;
+    a.ldh = ldh;
+  }
   return finish(ftk::launch_rmsnorm_fwd(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+// Shared by the plain and the residual-add backward; dh == nullptr is the
+// plain norm.  x is the norm's input (the stored h of the add form).
+ftk_status rmsnorm_bwd_checked(const void *dy, int64_t lddy, const void *dh, int64_t lddh,
+                               const void *x, int64_t ldx, const void *w, const float *rstd,
+                               void *dx, int64_t lddx, float *dw, void *workspace,
+                               size_t workspace_bytes, int64_t T, int64_t H, float eps,
+                               ftk_dtype dtype, ftk_stream_t stream) {
+  const bool add = dh != nullptr;
+  if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
+  if (T < 0 || H < 1 || lddy < H || ldx < H || lddx < H || T >= (int64_t(1) << 31))
+    return FTK_ERR_SHAPE;
+  if (add && lddh < H) return FTK_ERR_SHAPE;
+  if (T == 0) return FTK_OK;
+  if (!dy || !x || !w || !dx || !dw) return FTK_ERR_NULL;
+  if (!workspace) return FTK_ERR_WORKSPACE;
+  const DType dt = (DType)dtype;
+  const int64_t es = ftk::dtype_bytes(dt);
+  if (!aligned(dy, es) || !aligned(x, es) || !aligned(w, es) || !aligned(dx, es) ||
+      !aligned(dh, es) || !aligned(rstd, 4) || !aligned(dw, 4) || !aligned(workspace, 16))
+    return FTK_ERR_ALIGN;
+  const int64_t ws_rows = (int64_t)(workspace_bytes / ((size_t)H * sizeof(float)));
+  if (ws_rows < 1) return FTK_ERR_WORKSPACE;
+
+  const View vdy = view(dy, T, lddy, H, es), vx = view(x, T, ldx, H, es);
+  const View vdh = view(dh, add ? T : 0, lddh, H, es);
+  const View vdx = view(dx, T, lddx, H, es), vw = view(w, 1, H, H, es);
+  const View vr = view(rstd, 1, T, T, 4), vdw = view(dw, 1, H, H, 4);
+  const View vws = view(workspace, 1, ws_rows * H, ws_rows * H, 4);
+  if (!same_view(vdx, vdy) && may_overlap(vdx, vdy)) return FTK_ERR_ALIAS;
+  if (!same_view(vdx, vdh) && may_overlap(vdx, vdh)) return FTK_ERR_ALIAS;
+  const View outs[3] = {vdx, vdw, vws};
+  for (int i = 0; i < 3; ++i) {
+    if (i != 0 && (may_overlap(outs[i], vdy) || may_overlap(outs[i], vdh))) return FTK_ERR_ALIAS;
+    if (may_overlap(outs[i], vx) || may_overlap(outs[i], vw)) return FTK_ERR_ALIAS;
+    if (rstd && may_overlap(outs[i], vr)) return FTK_ERR_ALIAS;
+    for (int k = i + 1; k < 3; ++k)
+      if (may_overlap(outs[i], outs[k])) return FTK_ERR_ALIAS;
+  }
+
+  const int n = dt == DType::F32 ? 4 : 8;
+  bool vec = aligned(dy, 16) && aligned(x, 16) && aligned(w, 16) && aligned(dx, 16) &&
+             H % n == 0 && lddy % n == 0 && ldx % n == 0 && lddx % n == 0;
+  if (add) vec = vec && aligned(dh, 16) && lddh % n == 0;
+  const bool wide = vdy.max_offset() > kNarrowLimit || vx.max_offset() > kNarrowLimit ||
+                    vdx.max_offset() > kNarrowLimit ||
+                    (add && vdh.max_offset() > kNarrowLimit);
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ftk::RmsNormBwdArgs a{dy, lddy, x, ldx, w, rstd, dx, lddx, dw, (float *)workspace, ws_rows,
+                        T, H, eps};
+  if (add) {
+    a.dh = dh;
+    a.lddh = lddh;
+  }
+  return finish(ftk::launch_rmsnorm_bwd(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+FTK_API ftk_status ftk_rmsnorm_fwd(const void *x, int64_t ldx, const void *w, void *y,
+                                   int64_t ldy, float *rstd, int64_t T, int64_t H, float eps,
+                                   ftk_dtype dtype, ftk_stream_t stream) {
+  return rmsnorm_fwd_checked(x, ldx, nullptr, 0, w, nullptr, 0, y, ldy, rstd, T, H, eps, dtype,
+                             stream);
+}
+
+FTK_API ftk_status ftk_rmsnorm_add_fwd(const void *x, int64_t ldx, const void *res,
+                                       int64_t ldr, const void *w, void *h, int64_t ldh,
+                                       void *y, int64_t ldy, float *rstd, int64_t T,
+                                       int64_t H, float eps, ftk_dtype dtype,
+                                       ftk_stream_t stream) {
+  if (!res && T > 0) return FTK_ERR_NULL;
+  return rmsnorm_fwd_checked(x, ldx, res, ldr, w, h, ldh, y, ldy, rstd, T, H, eps, dtype,
+                             stream);
 }
 
 FTK_API size_t ftk_rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, ftk_dtype dtype) {
@@ -179,45 +286,19 @@ FTK_API ftk_status ftk_rmsnorm_bwd(const void *dy, int64_t lddy, const void *x, 
                                    const void *w, const float *rstd, void *dx, int64_t lddx,
                                    float *dw, void *workspace, size_t workspace_bytes, int64_t T,
                                    int64_t H, float eps, ftk_dtype dtype, ftk_stream_t stream) {
-  if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
-  if (T < 0 || H < 1 || lddy < H || ldx < H || lddx < H || T >= (int64_t(1) << 31))
-    return FTK_ERR_SHAPE;
-  if (T == 0) return FTK_OK;
-  if (!dy || !x || !w || !dx || !dw) return FTK_ERR_NULL;
-  if (!workspace) return FTK_ERR_WORKSPACE;
-  const DType dt = (DType)dtype;
-  const int64_t es = ftk::dtype_bytes(dt);
-  if (!aligned(dy, es) || !aligned(x, es) || !aligned(w, es) || !aligned(dx, es) ||
-      !aligned(rstd, 4) || !aligned(dw, 4) || !aligned(workspace, 16))
-    return FTK_ERR_ALIGN;
-  const int64_t ws_rows = (int64_t)(workspace_bytes / ((size_t)H * sizeof(float)));
-  if (ws_rows < 1) return FTK_ERR_WORKSPACE;
+  return rmsnorm_bwd_checked(dy, lddy, nullptr, 0, x, ldx, w, rstd, dx, lddx, dw, workspace,
+                             workspace_bytes, T, H, eps, dtype, stream);
+}
 
-  const View vdy = view(dy, T, lddy, H, es), vx = view(x, T, ldx, H, es);
-  const View vdx = view(dx, T, lddx, H, es), vw = view(w, 1, H, H, es);
-  const View vr = view(rstd, 1, T, T, 4), vdw = view(dw, 1, H, H, 4);
-  const View vws = view(workspace, 1, ws_rows * H, ws_rows * H, 4);
-  if (!same_view(vdx, vdy) && may_overlap(vdx, vdy)) return FTK_ERR_ALIAS;
-  const View outs[3] = {vdx, vdw, vws};
-  for (int i = 0; i < 3; ++i) {
-    if (i != 0 && may_overlap(outs[i], vdy)) return FTK_ERR_ALIAS;
-    if (may_overlap(outs[i], vx) || may_overlap(outs[i], vw)) return FTK_ERR_ALIAS;
-    if (rstd && may_overlap(outs[i], vr)) return FTK_ERR_ALIAS;
-    for (int k = i + 1; k < 3; ++k)
-      if (may_overlap(outs[i], outs[k])) return FTK_ERR_ALIAS;
-  }
-
-  const int n = dt == DType::F32 ? 4 : 8;
-  const bool vec = aligned(dy, 16) && aligned(x, 16) && aligned(w, 16) && aligned(dx, 16) &&
-                   H % n == 0 && lddy % n == 0 && ldx % n == 0 && lddx % n == 0;
-  const bool wide = vdy.max_offset() > kNarrowLimit || vx.max_offset() > kNarrowLimit ||
-                    vdx.max_offset() > kNarrowLimit;
-  ftk::DeviceInfo dev;
-  cudaError_t e = device_info(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  ftk::RmsNormBwdArgs a{dy, lddy, x, ldx, w, rstd, dx, lddx, dw, (float *)workspace, ws_rows,
-                        T, H, eps};
-  return finish(ftk::launch_rmsnorm_bwd(dt, vec, wide, a, dev, (cudaStream_t)stream));
+FTK_API ftk_status ftk_rmsnorm_add_bwd(const void *dy, int64_t lddy, const void *dh,
+                                       int64_t lddh, const void *h, int64_t ldh,
+                                       const void *w, const float *rstd, void *dx,
+                                       int64_t lddx, float *dw, void *workspace,
+                                       size_t workspace_bytes, int64_t T, int64_t H,
+                                       float eps, ftk_dtype dtype, ftk_stream_t stream) {
+  if (!dh && T > 0) return FTK_ERR_NULL;
+  return rmsnorm_bwd_checked(dy, lddy, dh, lddh, h, ldh, w, rstd, dx, lddx, dw, workspace,
+                             workspace_bytes, T, H, eps, dtype, stream);
 }
 
 // ------------------------------------------------------------------- SwiGLU

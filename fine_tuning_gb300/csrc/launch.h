@@ -91,6 +91,11 @@ struct RmsNormFwdArgs {
   float *rstd;  // nullable
   int64_t T, H;
   float eps;
+  // residual add fused in front (h = x + res stored, norm of h); res null: plain norm
+  const void *res = nullptr;
+  int64_t ldr = 0;
+  void *h = nullptr;
+  int64_t ldh = 0;
 };
 cudaError_t launch_rmsnorm_fwd(DType dt, bool vec, bool wide, const RmsNormFwdArgs &a,
                                const DeviceInfo &dev, cudaStream_t s);
@@ -109,11 +114,18 @@ struct RmsNormBwdArgs {
   int64_t ws_rows;
   int64_t T, H;
   float eps;
+  // residual add fused in front: x is the stored h, and dx = dh + norm backward;
+  // dh null: plain norm
+  const void *dh = nullptr;
+  int64_t lddh = 0;
 };
 // Upper bound on the partial rows the backward kernel writes (any plan).
 int64_t rmsnorm_bwd_partial_rows(int64_t T, const DeviceInfo &dev);
 cudaError_t launch_rmsnorm_bwd(DType dt, bool vec, bool wide, const RmsNormBwdArgs &a,
                                const DeviceInfo &dev, cudaStream_t s);
+// the dh != nullptr form (called by launch_rmsnorm_bwd)
+cudaError_t launch_rmsnorm_add_bwd(DType dt, bool vec, bool wide, const RmsNormBwdArgs &a,
+                                   const DeviceInfo &dev, cudaStream_t s);
 
 struct SwigluFwdArgs {
   const void *g, *u;

@@ -1,516 +1,8 @@
-// RMSNorm backward (gradient of sum(dy * y), y = x * r * w):
-//   c[t]    = sum_j dy[t,j] w[j] x[t,j]
-//   dx[t,j] = r[t] w[j] dy[t,j] - r[t]^3 x[t,j] c[t] / H
-//   dw[j]   = sum_t dy[t,j] x[t,j] r[t]
-// (Chronicals, arXiv 2601.02609, abstract, optimisation (1): fused RMSNorm;
-// the page gives no formula, this is the standard gradient.)
-//
-// Pass 1: a persistent grid of P CTAs walks the rows with a fixed stride.
-// Each thread keeps its slice of w in registers for the whole kernel and
-// accumulates dy*x*r for its columns in fp32 registers over the rows its
-// group visits.  At the end the R row groups of a CTA are summed in shared
-// memory in a fixed order and the CTA writes one fp32 row of partials to the
-// workspace.  For 16-byte aligned rows (rmsnorm_bwd_staged) one elected
-// thread per row group streams the next S rows of x and dy into a ring of
-// shared-memory stages with bulk copies (cp.async.bulk, completing on
-// mbarriers) and the warps compute from shared memory; other rows hold their
-// packets in registers (rmsnorm_bwd_rows).
-// Pass 2 (dw_reduce): dw[j] = sum_p ws[p, j], rows in a fixed order.
-// The row -> CTA map and every summation order are fixed, so dw is bitwise
-// reproducible; no CTA ever waits on another.
-#include "common.cuh"
-#include "launch.h"
+// RMSNorm backward, plain form (the kernels are in rmsnorm_bwd.cuh); the
+// residual-add form is instantiated in rmsnorm_add_bwd.cu.
+#include "rmsnorm_bwd.cuh"
 
 namespace ftk {
-
-namespace {
-
-constexpr int kMaxBlocksPerSm = 8;
-
-template <typename T, typename Idx, int N, int V, bool HAS_RSTD>
-__global__ void __launch_bounds__(256)
-rmsnorm_bwd_rows(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restrict__ w,
-                 const float *__restrict__ rstd, T *dx, Idx lddx, float *__restrict__ ws,
-                 Idx rows, int hp, int H, float inv_h, float eps, int W, int R) {
-  // [2][R][W] float2 reduction slots (double-buffered by row parity), then,
-  // when R > 1, [R][H] fp32 dw partials for the final combine.
-  extern __shared__ float smem[];
-  float2 *red = reinterpret_cast<float2 *>(smem);
-  float *part = smem + 4 * R * W;
-  pdl_wait();
-  pdl_trigger();
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = warp / W, wig = warp - grp * W;
-  const int gi = wig * 32 + lane, G = W * 32;
-
-  Packet<T, N> wv[V];
-#pragma unroll
-  for (int k = 0; k < V; ++k) {
-    const int c = gi + k * G;
-    if (c < hp) wv[k] = load_packet<T, N>(w + (Idx)c * N);
-  }
-  float acc[V][N];
-#pragma unroll
-  for (int k = 0; k < V; ++k)
-#pragma unroll
-    for (int e = 0; e < N; ++e) acc[k][e] = 0.f;
-
-  int parity = 0;
-  const Idx step = (Idx)gridDim.x * R;
-  for (Idx base = (Idx)blockIdx.x * R; base < rows; base += step, parity ^= 1) {
-    const Idx row = base + grp;
-    const bool active = row < rows;
-    Packet<T, N> xv[V], gv[V];
-    float r = 0.f;
-    float2 cs = make_float2(0.f, 0.f);  // (sum dy*w*x, sum x*x)
-    if (active) {
-      const T *xr = x + row * ldx;
-      const T *gr = dy + row * lddy;
-#pragma unroll
-      for (int k = 0; k < V; ++k) {
-        const int c = gi + k * G;
-        if (c < hp) {
-          xv[k] = load_packet_stream<T, N>(xr + (Idx)c * N);
-          gv[k] = load_packet_stream<T, N>(gr + (Idx)c * N);
-        }
-      }
-      if (HAS_RSTD) r = rstd[row];
-#pragma unroll
-      for (int k = 0; k < V; ++k) {
-        if (gi + k * G < hp) {
-#pragma unroll
-          for (int e = 0; e < N; ++e) {
-            const float xf = xv[k].get(e);
-            cs.x = fmaf(gv[k].get(e) * wv[k].get(e), xf, cs.x);
-            if (!HAS_RSTD) cs.y = fmaf(xf, xf, cs.y);
-          }
-        }
-      }
-    }
-    if (HAS_RSTD) {
-      cs.x = warp_sum(cs.x);
-    } else {
-      cs = warp_sum2(cs);
-    }
-    if (W > 1) {
-      float2 *slot = red + (parity * R + grp) * W;
-      if (lane == 0) slot[wig] = cs;
-      __syncthreads();
-      cs = make_float2(0.f, 0.f);
-      for (int i = 0; i < W; ++i) {
-        cs.x += slot[i].x;
-        cs.y += slot[i].y;
-      }
-    }
-    if (active) {
-      if (!HAS_RSTD) r = rsqrtf(fmaf(cs.y, inv_h, eps));
-      const float a = r * r * r * cs.x * inv_h;
-      T *dr = dx + row * lddx;
-#pragma unroll
-      for (int k = 0; k < V; ++k) {
-        const int c = gi + k * G;
-        if (c < hp) {
-          Packet<T, N> o;
-#pragma unroll
-          for (int e = 0; e < N; ++e) {
-            const float xf = xv[k].get(e), gf = gv[k].get(e);
-            o.set(e, fmaf(-a, xf, r * wv[k].get(e) * gf));
-            acc[k][e] = fmaf(gf * xf, r, acc[k][e]);
-          }
-          store_packet<T, N>(dr + (Idx)c * N, o);
-        }
-      }
-    }
-  }
-
-  float *dst = ws + (size_t)blockIdx.x * H;
-  if (R == 1) {
-#pragma unroll
-    for (int k = 0; k < V; ++k) {
-      const int c = gi + k * G;
-      if (c < hp)
-#pragma unroll
-        for (int e = 0; e < N; ++e) dst[c * N + e] = acc[k][e];
-    }
-    return;
-  }
-  float *mine = part + grp * H;
-#pragma unroll
-  for (int k = 0; k < V; ++k) {
-    const int c = gi + k * G;
-    if (c < hp)
-#pragma unroll
-      for (int e = 0; e < N; ++e) mine[c * N + e] = acc[k][e];
-  }
-  __syncthreads();
-  for (int j = threadIdx.x; j < H; j += blockDim.x) {
-    float sum = 0.f;
-    for (int g = 0; g < R; ++g) sum += part[g * H + j];
-    dst[j] = sum;
-  }
-}
-
-template <typename T, typename Idx, int N, int V, bool HAS_RSTD>
-__global__ void __launch_bounds__(256)
-rmsnorm_bwd_staged(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restrict__ w,
-                   const float *__restrict__ rstd, T *dx, Idx lddx, float *__restrict__ ws,
-                   Idx rows, int hp, int H, float inv_h, float eps, int W, int R, int S,
-                   uint32_t off_red, uint32_t off_stage, uint32_t row_bytes, unsigned *status,
-                   long long wait_limit) {
-  extern __shared__ __align__(128) unsigned char sbuf[];
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf);  // [R][S]
-  float2 *red = reinterpret_cast<float2 *>(sbuf + off_red);  // [R][W]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = warp / W, wig = warp - grp * W;
-  const int gi = wig * 32 + lane, G = W * 32;
-  const bool leader = gi == 0;
-  const uint32_t stage_bytes = 2 * row_bytes;  // x row, then dy row
-
-  for (int i = threadIdx.x; i < R * S; i += blockDim.x) mbar_init(&bars[i], 1);
-  if (threadIdx.x == 0) fence_mbar_init();
-  __syncthreads();
-  pdl_wait();
-  pdl_trigger();
-
-  uint64_t *gb = bars + grp * S;
-  unsigned char *ring = sbuf + off_stage + (size_t)grp * S * stage_bytes;
-  const Idx stride = (Idx)gridDim.x * R;
-  const Idx first = (Idx)blockIdx.x * R + grp;
-
-  auto issue = [&](int s, Idx row) {
-    unsigned char *st = ring + (size_t)s * stage_bytes;
-    mbar_arrive_expect_tx(&gb[s], stage_bytes);
-    bulk_copy_g2s(st, x + row * ldx, row_bytes, &gb[s]);
-    bulk_copy_g2s(st + row_bytes, dy + row * lddy, row_bytes, &gb[s]);
-  };
-  int issued = 0;
-  if (leader) {
-    for (int s = 0; s < S; ++s) {
-      const Idx row = first + (Idx)s * stride;
-      if (row >= rows) break;
-      issue(s, row);
-      ++issued;
-    }
-  }
-  Packet<T, N> wv[V];
-#pragma unroll
-  for (int k = 0; k < V; ++k) {
-    const int c = gi + k * G;
-    if (c < hp) wv[k] = load_packet<T, N>(w + (Idx)c * N);
-  }
-  float acc[V][N];
-#pragma unroll
-  for (int k = 0; k < V; ++k)
-#pragma unroll
-    for (int e = 0; e < N; ++e) acc[k][e] = 0.f;
-
-  bool live = true;
-  int it = 0;
-  // the saved r of each row is loaded one iteration ahead: the rows arrive
-  // through the stages long before they are needed, so a load issued at the
-  // row's own iteration would put a DRAM round trip on every row's path
-  float r_next = (HAS_RSTD && first < rows) ? rstd[first] : 0.f;
-  for (Idx row = first; row < rows; row += stride, ++it) {
-    const int s = it % S;
-    float r = r_next;
-    if (HAS_RSTD && row + stride < rows) r_next = rstd[row + stride];
-    if (live) live = mbar_wait_bounded(&gb[s], (uint32_t)((it / S) & 1), wait_limit, status);
-    const T *xs = reinterpret_cast<const T *>(ring + (size_t)s * stage_bytes);
-    const T *gs = reinterpret_cast<const T *>(ring + (size_t)s * stage_bytes + row_bytes);
-    float2 cs = make_float2(0.f, 0.f);  // (sum dy*w*x, sum x*x)
-#pragma unroll
-    for (int k = 0; k < V; ++k) {
-      const int c = gi + k * G;
-      if (c < hp) {
-        const Packet<T, N> xv = *reinterpret_cast<const Packet<T, N> *>(xs + c * N);
-        const Packet<T, N> gv = *reinterpret_cast<const Packet<T, N> *>(gs + c * N);
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-          const float xf = xv.get(e);
-          cs.x = fmaf(gv.get(e) * wv[k].get(e), xf, cs.x);
-          if (!HAS_RSTD) cs.y = fmaf(xf, xf, cs.y);
-        }
-      }
-    }
-    if (HAS_RSTD)
-      cs.x = warp_sum(cs.x);
-    else
-      cs = warp_sum2(cs);
-    if (W > 1) {
-      if (lane == 0) red[grp * W + wig] = cs;
-      named_barrier(1 + grp, G);
-      cs = make_float2(0.f, 0.f);
-      for (int i = 0; i < W; ++i) {
-        cs.x += red[grp * W + i].x;
-        cs.y += red[grp * W + i].y;
-      }
-    }
-    if (!HAS_RSTD) r = rsqrtf(fmaf(cs.y, inv_h, eps));
-    const float a = r * r * r * cs.x * inv_h;
-    T *dr = dx + row * lddx;
-#pragma unroll
-    for (int k = 0; k < V; ++k) {
-      const int c = gi + k * G;
-      if (c < hp) {
-        const Packet<T, N> xv = *reinterpret_cast<const Packet<T, N> *>(xs + c * N);
-        const Packet<T, N> gv = *reinterpret_cast<const Packet<T, N> *>(gs + c * N);
-        Packet<T, N> o;
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-          const float xf = xv.get(e), gf = gv.get(e);
-          o.set(e, fmaf(-a, xf, r * wv[k].get(e) * gf));
-          acc[k][e] = fmaf(gf * xf, r, acc[k][e]);
-        }
-        store_packet<T, N>(dr + (Idx)c * N, o);
-      }
-    }
-    if (W > 1)
-      named_barrier(1 + grp, G);
-    else
-      __syncwarp();
-    if (leader) {
-      const Idx next = row + (Idx)S * stride;
-      if (next < rows) {
-        fence_proxy_async_smem();
-        issue(s, next);
-        ++issued;
-      }
-    }
-  }
-  if (leader && !live)
-    for (int i = it; i < issued; ++i)
-      mbar_wait_bounded(&gb[i % S], (uint32_t)((i / S) & 1), wait_limit, status);
-
-  float *dst = ws + (size_t)blockIdx.x * H;
-  if (R == 1) {
-#pragma unroll
-    for (int k = 0; k < V; ++k) {
-      const int c = gi + k * G;
-      if (c < hp)
-#pragma unroll
-        for (int e = 0; e < N; ++e) dst[c * N + e] = acc[k][e];
-    }
-    return;
-  }
-  // the stages are free now: combine the R groups there in a fixed order
-  __syncthreads();
-  float *part = reinterpret_cast<float *>(sbuf + off_stage);
-  float *mine = part + grp * H;
-#pragma unroll
-  for (int k = 0; k < V; ++k) {
-    const int c = gi + k * G;
-    if (c < hp)
-#pragma unroll
-      for (int e = 0; e < N; ++e) mine[c * N + e] = acc[k][e];
-  }
-  __syncthreads();
-  for (int j = threadIdx.x; j < H; j += blockDim.x) {
-    float sum = 0.f;
-    for (int g = 0; g < R; ++g) sum += part[g * H + j];
-    dst[j] = sum;
-  }
-}
-
-// Rows too long for registers: one CTA per row at a time, persistent grid,
-// two passes over the row; the CTA's dw partial row lives in the workspace
-// and is updated in place (each CTA owns its row, so no atomics).
-template <typename T, typename Idx, bool HAS_RSTD>
-__global__ void __launch_bounds__(256)
-rmsnorm_bwd_generic(const T *dy, Idx lddy, const T *x, Idx ldx, const T *__restrict__ w,
-                    const float *__restrict__ rstd, T *dx, Idx lddx, float *__restrict__ ws,
-                    Idx rows, Idx H, float inv_h, float eps) {
-  __shared__ float2 red[8];
-  pdl_wait();
-  pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float *mine = ws + (size_t)blockIdx.x * H;
-  for (Idx j = threadIdx.x; j < H; j += blockDim.x) mine[j] = 0.f;
-  for (Idx row = blockIdx.x; row < rows; row += gridDim.x) {
-    const T *xr = x + row * ldx;
-    const T *gr = dy + row * lddy;
-    float2 cs = make_float2(0.f, 0.f);
-    for (Idx j = threadIdx.x; j < H; j += blockDim.x) {
-      const float xf = to_float(xr[j]);
-      cs.x = fmaf(to_float(gr[j]) * to_float(w[j]), xf, cs.x);
-      cs.y = fmaf(xf, xf, cs.y);
-    }
-    cs = warp_sum2(cs);
-    if (lane == 0) red[warp] = cs;
-    __syncthreads();
-    cs = make_float2(0.f, 0.f);
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
-      cs.x += red[i].x;
-      cs.y += red[i].y;
-    }
-    __syncthreads();
-    const float r = HAS_RSTD ? rstd[row] : rsqrtf(fmaf(cs.y, inv_h, eps));
-    const float a = r * r * r * cs.x * inv_h;
-    T *dr = dx + row * lddx;
-    for (Idx j = threadIdx.x; j < H; j += blockDim.x) {
-      const float xf = to_float(xr[j]), gf = to_float(gr[j]);
-      dr[j] = from_float<T>(fmaf(-a, xf, r * to_float(w[j]) * gf));
-      mine[j] = fmaf(gf * xf, r, mine[j]);
-    }
-  }
-}
-
-// dw[j] = sum_{p < P} ws[p, j]: a CTA owns 32 columns; its 32 warps take
-// the rows p = warp, warp + 32, ... and their sums are added in warp order.
-constexpr int kReduceWarps = 32;
-
-__global__ void __launch_bounds__(32 * kReduceWarps)
-dw_reduce(const float *__restrict__ ws, int P, int H, float *__restrict__ dw) {
-  __shared__ float part[kReduceWarps][33];
-  pdl_wait();
-  pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col = blockIdx.x * 32 + lane;
-  float s = 0.f;
-  if (col < H) {
-#pragma unroll 4
-    for (int p = warp; p < P; p += kReduceWarps) s += ws[(size_t)p * H + col];
-  }
-  part[warp][lane] = s;
-  __syncthreads();
-  if (warp == 0 && col < H) {
-    float t = 0.f;
-#pragma unroll
-    for (int i = 0; i < kReduceWarps; ++i) t += part[i][lane];
-    dw[col] = t;
-  }
-}
-
-template <typename T, typename Idx, int N, int V, bool HAS_RSTD>
-cudaError_t bwd_rows_v(const RowPlan &p, const RmsNormBwdArgs &a, const DeviceInfo &dev,
-                       cudaStream_t s) {
-  auto kern = rmsnorm_bwd_rows<T, Idx, N, V, HAS_RSTD>;
-  const int threads = p.threads();
-  const size_t smem = sizeof(float) * (4 * p.R * p.W + (p.R > 1 ? (size_t)p.R * a.H : 0));
-  if (smem > (size_t)dev.max_smem_optin) return cudaErrorInvalidConfiguration;
-  const int occ = blocks_per_sm((const void *)kern, threads, smem, dev, kMaxBlocksPerSm);
-  int64_t P = ceil_div(a.T, (int64_t)p.R);
-  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
-  if (P > a.ws_rows) P = a.ws_rows;
-  {
-    cudaError_t le_ = launch_pdl(kern, dim3((unsigned)P), dim3(threads), smem, s,
-                                 (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
-      (T *)a.dx, (Idx)a.lddx, a.ws, (Idx)a.T, (int)(a.H / N), (int)a.H,
-      (float)(1.0 / (double)a.H), a.eps, p.W, p.R);
-    if (le_ != cudaSuccess) return le_;
-  }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  {
-    cudaError_t le_ = launch_pdl(dw_reduce, dim3((unsigned)ceil_div(a.H, (int64_t)32)), dim3(32 * kReduceWarps), 0, s,
-                                 a.ws, (int)P, (int)a.H, a.dw);
-    if (le_ != cudaSuccess) return le_;
-  }
-  return cudaGetLastError();
-}
-
-template <typename T, typename Idx, int N, int V, bool HAS_RSTD>
-cudaError_t bwd_staged_v(const RowPlan &p, const StagedPlan &sp, const RmsNormBwdArgs &a,
-                         const DeviceInfo &dev, cudaStream_t s) {
-  auto kern = rmsnorm_bwd_staged<T, Idx, N, V, HAS_RSTD>;
-  const int threads = p.threads();
-  const int occ = blocks_per_sm((const void *)kern, threads, sp.smem, dev, kMaxBlocksPerSm);
-  int64_t P = ceil_div(a.T, (int64_t)p.R);
-  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
-  if (P > a.ws_rows) P = a.ws_rows;
-  unsigned *status = nullptr;
-  cudaError_t e = device_status_ptr(dev, &status);
-  if (e != cudaSuccess) return e;
-  {
-    cudaError_t le_ = launch_pdl(kern, dim3((unsigned)P), dim3(threads), sp.smem, s,
-                                 (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
-      (T *)a.dx, (Idx)a.lddx, a.ws, (Idx)a.T, (int)(a.H / N), (int)a.H,
-      (float)(1.0 / (double)a.H), a.eps, p.W, p.R, sp.S, (uint32_t)sp.off_red,
-      (uint32_t)sp.off_stage, sp.row_bytes, status, kWaitLimitCycles);
-    if (le_ != cudaSuccess) return le_;
-  }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  {
-    cudaError_t le_ = launch_pdl(dw_reduce, dim3((unsigned)ceil_div(a.H, (int64_t)32)), dim3(32 * kReduceWarps), 0, s,
-                                 a.ws, (int)P, (int)a.H, a.dw);
-    if (le_ != cudaSuccess) return le_;
-  }
-  return cudaGetLastError();
-}
-
-template <typename T, typename Idx, int N, bool HAS_RSTD>
-cudaError_t bwd_staged(const RowPlan &p, const StagedPlan &sp, const RmsNormBwdArgs &a,
-                       const DeviceInfo &dev, cudaStream_t s) {
-  switch (p.V) {
-    case 1: return bwd_staged_v<T, Idx, N, 1, HAS_RSTD>(p, sp, a, dev, s);
-    case 2: return bwd_staged_v<T, Idx, N, 2, HAS_RSTD>(p, sp, a, dev, s);
-    case 3: return bwd_staged_v<T, Idx, N, 3, HAS_RSTD>(p, sp, a, dev, s);
-    case 4: return bwd_staged_v<T, Idx, N, 4, HAS_RSTD>(p, sp, a, dev, s);
-    case 6: return bwd_staged_v<T, Idx, N, 6, HAS_RSTD>(p, sp, a, dev, s);
-    case 8: return bwd_staged_v<T, Idx, N, 8, HAS_RSTD>(p, sp, a, dev, s);
-    default: return cudaErrorInvalidConfiguration;
-  }
-}
-
-template <typename T, typename Idx, int N, bool HAS_RSTD>
-cudaError_t bwd_rows(const RowPlan &p, const RmsNormBwdArgs &a, const DeviceInfo &dev,
-                     cudaStream_t s) {
-  switch (p.V) {
-    case 1: return bwd_rows_v<T, Idx, N, 1, HAS_RSTD>(p, a, dev, s);
-    case 2: return bwd_rows_v<T, Idx, N, 2, HAS_RSTD>(p, a, dev, s);
-    case 3: return bwd_rows_v<T, Idx, N, 3, HAS_RSTD>(p, a, dev, s);
-    case 4: return bwd_rows_v<T, Idx, N, 4, HAS_RSTD>(p, a, dev, s);
-    case 6: return bwd_rows_v<T, Idx, N, 6, HAS_RSTD>(p, a, dev, s);
-    case 8: return bwd_rows_v<T, Idx, N, 8, HAS_RSTD>(p, a, dev, s);
-    default: return cudaErrorInvalidConfiguration;
-  }
-}
-
-template <typename T, typename Idx, bool HAS_RSTD>
-cudaError_t bwd_generic(const RmsNormBwdArgs &a, const DeviceInfo &dev, cudaStream_t s) {
-  int64_t P = a.T < (int64_t)dev.sms * 4 ? a.T : (int64_t)dev.sms * 4;
-  if (P > a.ws_rows) P = a.ws_rows;
-  {
-    cudaError_t le_ = launch_pdl(rmsnorm_bwd_generic<T, Idx, HAS_RSTD>, dim3((unsigned)P), dim3(256), 0, s,
-                                 (const T *)a.dy, (Idx)a.lddy, (const T *)a.x, (Idx)a.ldx, (const T *)a.w, a.rstd,
-      (T *)a.dx, (Idx)a.lddx, a.ws, (Idx)a.T, (Idx)a.H, (float)(1.0 / (double)a.H), a.eps);
-    if (le_ != cudaSuccess) return le_;
-  }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  {
-    cudaError_t le_ = launch_pdl(dw_reduce, dim3((unsigned)ceil_div(a.H, (int64_t)32)), dim3(32 * kReduceWarps), 0, s,
-                                 a.ws, (int)P, (int)a.H, a.dw);
-    if (le_ != cudaSuccess) return le_;
-  }
-  return cudaGetLastError();
-}
-
-template <typename T, typename Idx>
-cudaError_t bwd_typed(bool vec, const RmsNormBwdArgs &a, const DeviceInfo &dev,
-                      cudaStream_t s) {
-  constexpr int NV = VecWidth<T>::value;
-  // the forward's plan: the same per-thread columns and summation order, so
-  // an rstd recomputed here equals the one the forward saved bit for bit
-  const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1, 4);
-  const bool has_rstd = a.rstd != nullptr;
-  if (vec && !p.generic) {
-    const StagedPlan sp = plan_rmsnorm_staged(p, a.H, (int)sizeof(T), 2, dev);
-    if (sp.S > 0)
-      return has_rstd ? bwd_staged<T, Idx, NV, true>(p, sp, a, dev, s)
-                      : bwd_staged<T, Idx, NV, false>(p, sp, a, dev, s);
-  }
-  if (p.generic)
-    return has_rstd ? bwd_generic<T, Idx, true>(a, dev, s) : bwd_generic<T, Idx, false>(a, dev, s);
-  if (vec)
-    return has_rstd ? bwd_rows<T, Idx, NV, true>(p, a, dev, s)
-                    : bwd_rows<T, Idx, NV, false>(p, a, dev, s);
-  return has_rstd ? bwd_rows<T, Idx, 1, true>(p, a, dev, s)
-                  : bwd_rows<T, Idx, 1, false>(p, a, dev, s);
-}
-
-}  // namespace
 
 int64_t rmsnorm_bwd_partial_rows(int64_t T, const DeviceInfo &dev) {
   const int64_t cap = (int64_t)dev.sms * kMaxBlocksPerSm;
@@ -519,11 +11,8 @@ int64_t rmsnorm_bwd_partial_rows(int64_t T, const DeviceInfo &dev) {
 
 cudaError_t launch_rmsnorm_bwd(DType dt, bool vec, bool wide, const RmsNormBwdArgs &a,
                                const DeviceInfo &dev, cudaStream_t s) {
-  if (dt == DType::F32)
-    return wide ? bwd_typed<float, int64_t>(vec, a, dev, s)
-                : bwd_typed<float, int32_t>(vec, a, dev, s);
-  return wide ? bwd_typed<bf16, int64_t>(vec, a, dev, s)
-              : bwd_typed<bf16, int32_t>(vec, a, dev, s);
+  if (a.dh) return launch_rmsnorm_add_bwd(dt, vec, wide, a, dev, s);
+  return launch_bwd_form<false>(dt, vec, wide, a, dev, s);
 }
 
 }  // namespace ftk

@@ -1,6 +1,9 @@
 // RMSNorm forward:  y[t,j] = x[t,j] * r[t] * w[j],
 //                   r[t]   = 1 / sqrt(mean_j x[t,j]^2 + eps)
 // (Chronicals, arXiv 2601.02609, abstract, optimisation (1): fused RMSNorm.)
+// With ADD, the pre-norm residual step fused in front of it: h = x + res is
+// added in fp32, rounded to the storage type and stored, and the norm runs
+// on that stored h (exactly what a separate add followed by the norm gives).
 //
 // One row is read from HBM once and written once.  A group of W warps owns a
 // row; the sum of squares is reduced with warp shuffles (and, for W > 1,
@@ -64,19 +67,64 @@ StagedPlan plan_rmsnorm_staged(const RowPlan &p, int64_t H, int elem_bytes, int 
   return sp;
 }
 
-template <typename T, typename Idx, int N, int V>
+namespace {
+
+template <typename T, typename Idx> struct FwdParams {
+  const T *x;
+  Idx ldx;
+  const T *res;  // ADD only
+  Idx ldr;
+  const T *w;
+  T *y;
+  Idx ldy;
+  T *h;  // ADD only
+  Idx ldh;
+  float *rstd;  // nullable
+  Idx rows;
+  int hp;  // packets per row
+  float inv_h, eps;
+  int W, R;
+};
+
+// The row's value as the norm sees it: x, or (ADD) x + res rounded to T.
+template <typename T, int N, bool ADD>
+__device__ __forceinline__ Packet<T, N> norm_input(const Packet<T, N> &xv,
+                                                   const Packet<T, N> &rv) {
+  if constexpr (!ADD) {
+    return xv;
+  } else {
+    Packet<T, N> h;
+#pragma unroll
+    for (int e = 0; e < N; ++e) h.set(e, xv.get(e) + rv.get(e));
+    return h;
+  }
+}
+
+// Packet c of a staged row as the norm sees it; the res row (read only with
+// ADD) follows the x row in the stage.
+template <typename T, int N, bool ADD>
+__device__ __forceinline__ Packet<T, N> staged_input(const T *xs, const T *rs, int c) {
+  const Packet<T, N> xv = *reinterpret_cast<const Packet<T, N> *>(xs + c * N);
+  if constexpr (!ADD) {
+    return xv;
+  } else {
+    return norm_input<T, N, true>(xv, *reinterpret_cast<const Packet<T, N> *>(rs + c * N));
+  }
+}
+
+template <typename T, typename Idx, int N, int V, bool ADD>
 __global__ void __launch_bounds__(256)
-rmsnorm_fwd_staged(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
-                   float *__restrict__ rstd, Idx rows, int hp, float inv_h, float eps, int W,
-                   int R, int S, uint32_t off_red, uint32_t off_stage, uint32_t row_bytes,
-                   unsigned *status, long long wait_limit) {
+rmsnorm_fwd_staged(const FwdParams<T, Idx> a, int S, uint32_t off_red, uint32_t off_stage,
+                   uint32_t row_bytes, unsigned *status, long long wait_limit) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // [R][S]
   float *red = reinterpret_cast<float *>(smem + off_red);  // [R][W]
+  const int W = a.W, R = a.R;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / W, wig = warp - grp * W;
   const int gi = wig * 32 + lane, G = W * 32;
   const bool leader = gi == 0;
+  const uint32_t stage_bytes = (ADD ? 2 : 1) * row_bytes;  // x row (then res row)
 
   for (int i = threadIdx.x; i < R * S; i += blockDim.x) mbar_init(&bars[i], 1);
   if (threadIdx.x == 0) fence_mbar_init();
@@ -85,17 +133,22 @@ rmsnorm_fwd_staged(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
   pdl_trigger();
 
   uint64_t *gb = bars + grp * S;
-  unsigned char *ring = smem + off_stage + (size_t)grp * S * row_bytes;
+  unsigned char *ring = smem + off_stage + (size_t)grp * S * stage_bytes;
   const Idx stride = (Idx)gridDim.x * R;
   const Idx first = (Idx)blockIdx.x * R + grp;
 
+  auto issue = [&](int s, Idx row) {
+    unsigned char *st = ring + (size_t)s * stage_bytes;
+    mbar_arrive_expect_tx(&gb[s], stage_bytes);
+    bulk_copy_g2s(st, a.x + row * a.ldx, row_bytes, &gb[s]);
+    if (ADD) bulk_copy_g2s(st + row_bytes, a.res + row * a.ldr, row_bytes, &gb[s]);
+  };
   int issued = 0;  // copies issued by the leader
   if (leader) {
     for (int s = 0; s < S; ++s) {
       const Idx row = first + (Idx)s * stride;
-      if (row >= rows) break;
-      mbar_arrive_expect_tx(&gb[s], row_bytes);
-      bulk_copy_g2s(ring + (size_t)s * row_bytes, x + row * ldx, row_bytes, &gb[s]);
+      if (row >= a.rows) break;
+      issue(s, row);
       ++issued;
     }
   }
@@ -103,21 +156,22 @@ rmsnorm_fwd_staged(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
 #pragma unroll
   for (int k = 0; k < V; ++k) {
     const int c = gi + k * G;
-    if (c < hp) wv[k] = load_packet<T, N>(w + (Idx)c * N);
+    if (c < a.hp) wv[k] = load_packet<T, N>(a.w + (Idx)c * N);
   }
 
   bool live = true;  // false once one of this thread's waits has run out
   int it = 0;
-  for (Idx row = first; row < rows; row += stride, ++it) {
+  for (Idx row = first; row < a.rows; row += stride, ++it) {
     const int s = it % S;
     if (live) live = mbar_wait_bounded(&gb[s], (uint32_t)((it / S) & 1), wait_limit, status);
-    const T *xs = reinterpret_cast<const T *>(ring + (size_t)s * row_bytes);
+    const T *xs = reinterpret_cast<const T *>(ring + (size_t)s * stage_bytes);
+    const T *rs = reinterpret_cast<const T *>(ring + (size_t)s * stage_bytes + row_bytes);
     float ss = 0.f;
 #pragma unroll
     for (int k = 0; k < V; ++k) {
       const int c = gi + k * G;
-      if (c < hp) {
-        const Packet<T, N> v = *reinterpret_cast<const Packet<T, N> *>(xs + c * N);
+      if (c < a.hp) {
+        const Packet<T, N> v = staged_input<T, N, ADD>(xs, rs, c);
 #pragma unroll
         for (int e = 0; e < N; ++e) {
           const float f = v.get(e);
@@ -132,14 +186,15 @@ rmsnorm_fwd_staged(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
       ss = 0.f;
       for (int i = 0; i < W; ++i) ss += red[grp * W + i];
     }
-    const float r = rsqrtf(fmaf(ss, inv_h, eps));
-    if (rstd != nullptr && leader) rstd[row] = r;
-    T *yr = y + row * ldy;
+    const float r = rsqrtf(fmaf(ss, a.inv_h, a.eps));
+    if (a.rstd != nullptr && leader) a.rstd[row] = r;
+    T *yr = a.y + row * a.ldy;
 #pragma unroll
     for (int k = 0; k < V; ++k) {
       const int c = gi + k * G;
-      if (c < hp) {
-        const Packet<T, N> v = *reinterpret_cast<const Packet<T, N> *>(xs + c * N);
+      if (c < a.hp) {
+        const Packet<T, N> v = staged_input<T, N, ADD>(xs, rs, c);
+        if (ADD) store_packet<T, N>(a.h + row * a.ldh + (Idx)c * N, v);
         Packet<T, N> o;
 #pragma unroll
         for (int e = 0; e < N; ++e) o.set(e, (v.get(e) * r) * wv[k].get(e));
@@ -153,10 +208,9 @@ rmsnorm_fwd_staged(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
       __syncwarp();
     if (leader) {
       const Idx next = row + (Idx)S * stride;
-      if (next < rows) {
+      if (next < a.rows) {
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&gb[s], row_bytes);
-        bulk_copy_g2s(ring + (size_t)s * row_bytes, x + next * ldx, row_bytes, &gb[s]);
+        issue(s, next);
         ++issued;
       }
     }
@@ -168,32 +222,36 @@ rmsnorm_fwd_staged(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
       mbar_wait_bounded(&gb[i % S], (uint32_t)((i / S) & 1), wait_limit, status);
 }
 
-template <typename T, typename Idx, int N, int V>
-__global__ void __launch_bounds__(256)
-rmsnorm_fwd_rows(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
-                 float *__restrict__ rstd, Idx rows, int hp, float inv_h, float eps,
-                 int W, int R) {
+template <typename T, typename Idx, int N, int V, bool ADD>
+__global__ void __launch_bounds__(256) rmsnorm_fwd_rows(const FwdParams<T, Idx> a) {
   extern __shared__ float red[];  // [R][W] warp partial sums
   pdl_wait();
   pdl_trigger();
+  const int W = a.W, R = a.R;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / W, wig = warp - grp * W;
   const int gi = wig * 32 + lane, G = W * 32;
   const Idx row = (Idx)blockIdx.x * R + grp;
-  const bool active = row < rows;
+  const bool active = row < a.rows;
 
   Packet<T, N> xv[V];
   float ss = 0.f;
   if (active) {
-    const T *xr = x + row * ldx;
+    const T *xr = a.x + row * a.ldx;
+    const T *rr = ADD ? a.res + row * a.ldr : nullptr;
+    Packet<T, N> rv[ADD ? V : 1];
 #pragma unroll
     for (int k = 0; k < V; ++k) {
       const int c = gi + k * G;
-      if (c < hp) xv[k] = load_packet_stream<T, N>(xr + (Idx)c * N);
+      if (c < a.hp) {
+        xv[k] = load_packet_stream<T, N>(xr + (Idx)c * N);
+        if (ADD) rv[ADD ? k : 0] = load_packet_stream<T, N>(rr + (Idx)c * N);
+      }
     }
 #pragma unroll
     for (int k = 0; k < V; ++k) {
-      if (gi + k * G < hp) {
+      if (gi + k * G < a.hp) {
+        if (ADD) xv[k] = norm_input<T, N, ADD>(xv[k], rv[ADD ? k : 0]);
 #pragma unroll
         for (int e = 0; e < N; ++e) {
           const float f = xv[k].get(e);
@@ -211,14 +269,15 @@ rmsnorm_fwd_rows(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
   }
   if (!active) return;
 
-  const float r = rsqrtf(fmaf(ss, inv_h, eps));
-  if (rstd != nullptr && gi == 0) rstd[row] = r;
-  T *yr = y + row * ldy;
+  const float r = rsqrtf(fmaf(ss, a.inv_h, a.eps));
+  if (a.rstd != nullptr && gi == 0) a.rstd[row] = r;
+  T *yr = a.y + row * a.ldy;
 #pragma unroll
   for (int k = 0; k < V; ++k) {
     const int c = gi + k * G;
-    if (c < hp) {
-      const Packet<T, N> wv = load_packet<T, N>(w + (Idx)c * N);
+    if (c < a.hp) {
+      if (ADD) store_packet<T, N>(a.h + row * a.ldh + (Idx)c * N, xv[k]);
+      const Packet<T, N> wv = load_packet<T, N>(a.w + (Idx)c * N);
       Packet<T, N> o;
 #pragma unroll
       for (int e = 0; e < N; ++e) o.set(e, (xv[k].get(e) * r) * wv.get(e));
@@ -228,132 +287,132 @@ rmsnorm_fwd_rows(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
 }
 
 // Rows longer than the register plan: one CTA per row (grid-stride over
-// rows), sum of squares first, then a second pass that re-reads x (from L2).
-template <typename T, typename Idx>
-__global__ void __launch_bounds__(256)
-rmsnorm_fwd_generic(const T *x, Idx ldx, const T *__restrict__ w, T *y, Idx ldy,
-                    float *__restrict__ rstd, Idx rows, Idx H, float inv_h, float eps) {
+// rows), sum of squares first (writing h when ADD), then a second pass that
+// re-reads the row (from L2).
+template <typename T, typename Idx, bool ADD>
+__global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams<T, Idx> a, Idx H) {
   __shared__ float red[8];
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (Idx row = blockIdx.x; row < rows; row += gridDim.x) {
-    const T *xr = x + row * ldx;
+  for (Idx row = blockIdx.x; row < a.rows; row += gridDim.x) {
+    const T *xr = a.x + row * a.ldx;
+    const T *rr = ADD ? a.res + row * a.ldr : nullptr;
+    T *hr = ADD ? a.h + row * a.ldh : nullptr;
     float ss = 0.f;
     for (Idx j = threadIdx.x; j < H; j += blockDim.x) {
-      const float f = to_float(xr[j]);
+      T v = xr[j];
+      if (ADD) {
+        v = from_float<T>(to_float(v) + to_float(rr[j]));
+        hr[j] = v;
+      }
+      const float f = to_float(v);
       ss = fmaf(f, f, ss);
     }
     ss = warp_sum(ss);
     if (lane == 0) red[warp] = ss;
-    __syncthreads();
+    __syncthreads();  // also orders this CTA's h writes before the re-reads
     ss = 0.f;
     for (int i = 0; i < (int)(blockDim.x >> 5); ++i) ss += red[i];
     __syncthreads();  // red is reused by the next row
-    const float r = rsqrtf(fmaf(ss, inv_h, eps));
-    if (rstd != nullptr && threadIdx.x == 0) rstd[row] = r;
-    T *yr = y + row * ldy;
+    const float r = rsqrtf(fmaf(ss, a.inv_h, a.eps));
+    if (a.rstd != nullptr && threadIdx.x == 0) a.rstd[row] = r;
+    T *yr = a.y + row * a.ldy;
+    const T *src = ADD ? hr : xr;
     for (Idx j = threadIdx.x; j < H; j += blockDim.x)
-      yr[j] = from_float<T>((to_float(xr[j]) * r) * to_float(w[j]));
+      yr[j] = from_float<T>((to_float(src[j]) * r) * to_float(a.w[j]));
   }
 }
 
-template <typename T, typename Idx, int N>
-static cudaError_t fwd_rows(const RowPlan &p, const RmsNormFwdArgs &a, cudaStream_t s) {
-  const Idx rows = (Idx)a.T;
-  const dim3 grid((unsigned)ceil_div(a.T, (int64_t)p.R));
+template <typename T, typename Idx, int N, int V, bool ADD>
+cudaError_t fwd_rows_v(const RowPlan &p, const FwdParams<T, Idx> &k, cudaStream_t s) {
+  const dim3 grid((unsigned)ceil_div((int64_t)k.rows, (int64_t)p.R));
   const size_t smem = sizeof(float) * p.R * p.W;
-  const int hp = (int)(a.H / N);
-  const float inv_h = (float)(1.0 / (double)a.H);
-#define FTK_FWD_CASE(VV)                                                          \
-  case VV:                                                                        \
-    {                                                                             \
-      cudaError_t le_ = launch_pdl(rmsnorm_fwd_rows<T, Idx, N, VV>, dim3(grid), dim3(p.threads()), smem, s, \
-                                    (const T *)a.x, (Idx)a.ldx, (const T *)a.w, (T *)a.y, (Idx)a.ldy, a.rstd, rows, hp, inv_h, a.eps, p.W, p.R); \
-      if (le_ != cudaSuccess) return le_;                                          \
-    }                                        \
-    break;
-  switch (p.V) {
-    FTK_FWD_CASE(1)
-    FTK_FWD_CASE(2)
-    FTK_FWD_CASE(3)
-    FTK_FWD_CASE(4)
-    FTK_FWD_CASE(6)
-    FTK_FWD_CASE(8)
-    default:
-      return cudaErrorInvalidConfiguration;
-  }
-#undef FTK_FWD_CASE
+  cudaError_t le = launch_pdl(rmsnorm_fwd_rows<T, Idx, N, V, ADD>, grid, dim3(p.threads()), smem,
+                              s, k);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 
-template <typename T, typename Idx, int N, int V>
-static cudaError_t fwd_staged_v(const RowPlan &p, const StagedPlan &sp, const RmsNormFwdArgs &a,
-                                const DeviceInfo &dev, cudaStream_t s) {
-  auto kern = rmsnorm_fwd_staged<T, Idx, N, V>;
+template <typename T, typename Idx, int N, int V, bool ADD>
+cudaError_t fwd_staged_v(const RowPlan &p, const StagedPlan &sp, const FwdParams<T, Idx> &k,
+                         const DeviceInfo &dev, cudaStream_t s) {
+  auto kern = rmsnorm_fwd_staged<T, Idx, N, V, ADD>;
   const int threads = p.threads();
   const int occ = blocks_per_sm((const void *)kern, threads, sp.smem, dev, 8);
-  int64_t P = ceil_div(a.T, (int64_t)p.R);
+  int64_t P = ceil_div((int64_t)k.rows, (int64_t)p.R);
   if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
   unsigned *status = nullptr;
   cudaError_t e = device_status_ptr(dev, &status);
   if (e != cudaSuccess) return e;
-  {
-    cudaError_t le_ = launch_pdl(kern, dim3((unsigned)P), dim3(threads), sp.smem, s,
-                                 (const T *)a.x, (Idx)a.ldx, (const T *)a.w, (T *)a.y, (Idx)a.ldy, a.rstd, (Idx)a.T,
-      (int)(a.H / N), (float)(1.0 / (double)a.H), a.eps, p.W, p.R, sp.S, (uint32_t)sp.off_red,
-      (uint32_t)sp.off_stage, sp.row_bytes, status, kWaitLimitCycles);
-    if (le_ != cudaSuccess) return le_;
-  }
+  cudaError_t le = launch_pdl(kern, dim3((unsigned)P), dim3(threads), sp.smem, s, k, sp.S,
+                              (uint32_t)sp.off_red, (uint32_t)sp.off_stage, sp.row_bytes, status,
+                              kWaitLimitCycles);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 
-template <typename T, typename Idx, int N>
-static cudaError_t fwd_staged(const RowPlan &p, const StagedPlan &sp, const RmsNormFwdArgs &a,
-                              const DeviceInfo &dev, cudaStream_t s) {
+template <typename T, typename Idx, int N, bool ADD>
+cudaError_t fwd_planned(const RowPlan &p, const StagedPlan *sp, const FwdParams<T, Idx> &k,
+                        const DeviceInfo &dev, cudaStream_t s) {
+#define FTK_FWD_V(VV)                                                   \
+  case VV:                                                              \
+    return sp ? fwd_staged_v<T, Idx, N, VV, ADD>(p, *sp, k, dev, s)     \
+              : fwd_rows_v<T, Idx, N, VV, ADD>(p, k, s);
   switch (p.V) {
-    case 1: return fwd_staged_v<T, Idx, N, 1>(p, sp, a, dev, s);
-    case 2: return fwd_staged_v<T, Idx, N, 2>(p, sp, a, dev, s);
-    case 3: return fwd_staged_v<T, Idx, N, 3>(p, sp, a, dev, s);
-    case 4: return fwd_staged_v<T, Idx, N, 4>(p, sp, a, dev, s);
-    case 6: return fwd_staged_v<T, Idx, N, 6>(p, sp, a, dev, s);
-    case 8: return fwd_staged_v<T, Idx, N, 8>(p, sp, a, dev, s);
-    default: return cudaErrorInvalidConfiguration;
+    FTK_FWD_V(1)
+    FTK_FWD_V(2)
+    FTK_FWD_V(3)
+    FTK_FWD_V(4)
+    FTK_FWD_V(6)
+    FTK_FWD_V(8)
+    default:
+      return cudaErrorInvalidConfiguration;
   }
+#undef FTK_FWD_V
 }
 
-template <typename T, typename Idx>
-static cudaError_t fwd_typed(bool vec, const RmsNormFwdArgs &a, const DeviceInfo &dev,
-                             cudaStream_t s) {
+template <typename T, typename Idx, bool ADD>
+cudaError_t fwd_typed(bool vec, const RmsNormFwdArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
   const RowPlan p = plan_rmsnorm_row(a.H, vec ? NV : 1, 4);
+  FwdParams<T, Idx> k{(const T *)a.x, (Idx)a.ldx, (const T *)a.res, (Idx)a.ldr,
+                      (const T *)a.w, (T *)a.y,   (Idx)a.ldy,         (T *)a.h,
+                      (Idx)a.ldh,     a.rstd,     (Idx)a.T,           (int)(a.H / (vec ? NV : 1)),
+                      (float)(1.0 / (double)a.H), a.eps, p.W, p.R};
+  if (p.generic) {
+    const int64_t grid = a.T < (int64_t)dev.sms * 16 ? a.T : (int64_t)dev.sms * 16;
+    cudaError_t le = launch_pdl(rmsnorm_fwd_generic<T, Idx, ADD>, dim3((unsigned)grid), dim3(256),
+                                0, s, k, (Idx)a.H);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+  }
   // The staged pipeline pays off once every row group streams a dozen rows
   // or more; smaller batches finish sooner with one row per group and the
   // hardware scheduler refilling SMs (rmsnorm_fwd_rows).
-  if (vec && !p.generic && a.T >= (int64_t)12 * p.R * 2 * dev.sms) {
-    const StagedPlan sp = plan_rmsnorm_staged(p, a.H, (int)sizeof(T), 1, dev);
-    if (sp.S > 0) return fwd_staged<T, Idx, NV>(p, sp, a, dev, s);
+  if (vec && a.T >= (int64_t)12 * p.R * 2 * dev.sms) {
+    const StagedPlan sp = plan_rmsnorm_staged(p, a.H, (int)sizeof(T), ADD ? 2 : 1, dev);
+    if (sp.S > 0) return fwd_planned<T, Idx, NV, ADD>(p, &sp, k, dev, s);
   }
-  if (p.generic) {
-    int64_t grid = a.T < (int64_t)dev.sms * 16 ? a.T : (int64_t)dev.sms * 16;
-    {
-      cudaError_t le_ = launch_pdl(rmsnorm_fwd_generic<T, Idx>, dim3((unsigned)grid), dim3(256), 0, s,
-                                   (const T *)a.x, (Idx)a.ldx, (const T *)a.w, (T *)a.y, (Idx)a.ldy, a.rstd,
-        (Idx)a.T, (Idx)a.H, (float)(1.0 / (double)a.H), a.eps);
-      if (le_ != cudaSuccess) return le_;
-    }
-    return cudaGetLastError();
-  }
-  return vec ? fwd_rows<T, Idx, NV>(p, a, s) : fwd_rows<T, Idx, 1>(p, a, s);
+  return vec ? fwd_planned<T, Idx, NV, ADD>(p, nullptr, k, dev, s)
+             : fwd_planned<T, Idx, 1, ADD>(p, nullptr, k, dev, s);
 }
+
+template <typename T, typename Idx>
+cudaError_t fwd_add_or_not(bool vec, const RmsNormFwdArgs &a, const DeviceInfo &dev,
+                           cudaStream_t s) {
+  return a.res ? fwd_typed<T, Idx, true>(vec, a, dev, s) : fwd_typed<T, Idx, false>(vec, a, dev, s);
+}
+
+}  // namespace
 
 cudaError_t launch_rmsnorm_fwd(DType dt, bool vec, bool wide, const RmsNormFwdArgs &a,
                                const DeviceInfo &dev, cudaStream_t s) {
   if (dt == DType::F32)
-    return wide ? fwd_typed<float, int64_t>(vec, a, dev, s)
-                : fwd_typed<float, int32_t>(vec, a, dev, s);
-  return wide ? fwd_typed<bf16, int64_t>(vec, a, dev, s)
-              : fwd_typed<bf16, int32_t>(vec, a, dev, s);
+    return wide ? fwd_add_or_not<float, int64_t>(vec, a, dev, s)
+                : fwd_add_or_not<float, int32_t>(vec, a, dev, s);
+  return wide ? fwd_add_or_not<bf16, int64_t>(vec, a, dev, s)
+              : fwd_add_or_not<bf16, int32_t>(vec, a, dev, s);
 }
 
 }  // namespace ftk

@@ -53,6 +53,10 @@ def library() -> ctypes.CDLL:
         "ftk_rmsnorm_bwd_workspace_bytes": (sz, [i64, i64, dt]),
         "ftk_rmsnorm_bwd": (st, [vp, i64, vp, i64, vp, vp, vp, i64, vp, vp, sz, i64, i64,
                                  f32, dt, vp]),
+        "ftk_rmsnorm_add_fwd": (st, [vp, i64, vp, i64, vp, vp, i64, vp, i64, vp, i64, i64, f32,
+                                     dt, vp]),
+        "ftk_rmsnorm_add_bwd": (st, [vp, i64, vp, i64, vp, i64, vp, vp, vp, i64, vp, vp, sz,
+                                     i64, i64, f32, dt, vp]),
         "ftk_swiglu_fwd": (st, [vp, vp, i64, vp, i64, i64, i64, dt, vp]),
         "ftk_swiglu_bwd": (st, [vp, i64, vp, vp, i64, vp, vp, i64, i64, i64, dt, vp]),
         "ftk_qk_rope_fwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, dt, vp]),
@@ -144,8 +148,7 @@ def rmsnorm_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, rstd: Option
     if dw is None:
         dw = torch.empty((H,), dtype=torch.float32, device=x.device)
     if workspace is None:
-        nbytes = max(16, rmsnorm_bwd_workspace_bytes(T, H, x.dtype))
-        workspace = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=x.device)
+        workspace = _workspace(T, H, x)
     if dy.shape != x.shape or dy.dtype != x.dtype or dx.dtype != x.dtype:
         raise ValueError("dy and dx must match x in shape and dtype")
     if dw.dtype != torch.float32 or dw.numel() != H or not dw.is_contiguous():
@@ -153,6 +156,64 @@ def rmsnorm_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, rstd: Option
     _call("ftk_rmsnorm_bwd", _ptr(dy), _rows(dy, "dy"), _ptr(x), _rows(x, "x"), _ptr(w),
           _ptr(rstd), _ptr(dx), _rows(dx, "dx"), _ptr(dw), _ptr(workspace),
           workspace.numel() * workspace.element_size(), T, H, float(eps), _code(x), _stream(x))
+    return dx, dw
+
+
+def _workspace(T: int, H: int, like: torch.Tensor) -> torch.Tensor:
+    nbytes = max(16, rmsnorm_bwd_workspace_bytes(T, H, like.dtype))
+    return torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=like.device)
+
+
+def rmsnorm_add_fwd(x: torch.Tensor, res: torch.Tensor, w: torch.Tensor, eps: float,
+                    h: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
+                    rstd: Optional[torch.Tensor] = None, save_rstd: bool = True
+                    ) -> Tuple[torch.Tensor, torch.Tensor, Optional[torch.Tensor]]:
+    """h = x + res (stored, x's dtype), y = rmsnorm(h) * w; returns (h, y, rstd).
+    Pass h=res (or h=x) to update the residual stream in place."""
+    _cuda(x, res, w, h, y, rstd)
+    T, H = x.shape
+    if h is None:
+        h = torch.empty((T, H), dtype=x.dtype, device=x.device)
+    if y is None:
+        y = torch.empty((T, H), dtype=x.dtype, device=x.device)
+    if rstd is None and save_rstd:
+        rstd = torch.empty((T,), dtype=torch.float32, device=x.device)
+    for t in (res, h, y):
+        if t.shape != x.shape or t.dtype != x.dtype:
+            raise ValueError("res, h and y must match x in shape and dtype")
+    if w.dtype != x.dtype or w.numel() != H or not w.is_contiguous():
+        raise ValueError("w must be a contiguous [H] tensor of x's dtype")
+    if rstd is not None and (rstd.dtype != torch.float32 or rstd.numel() != T or not rstd.is_contiguous()):
+        raise ValueError("rstd must be a contiguous fp32 [T] tensor")
+    _call("ftk_rmsnorm_add_fwd", _ptr(x), _rows(x, "x"), _ptr(res), _rows(res, "res"), _ptr(w),
+          _ptr(h), _rows(h, "h"), _ptr(y), _rows(y, "y"), _ptr(rstd), T, H, float(eps),
+          _code(x), _stream(x))
+    return h, y, rstd
+
+
+def rmsnorm_add_bwd(dy: torch.Tensor, dh: torch.Tensor, h: torch.Tensor, w: torch.Tensor,
+                    rstd: Optional[torch.Tensor], eps: float, dx: Optional[torch.Tensor] = None,
+                    dw: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None
+                    ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Backward of rmsnorm_add_fwd: dx = dh + the norm's gradient at h (the
+    gradient of both x and res), dw [H] fp32.  rstd=None recomputes it."""
+    _cuda(dy, dh, h, w, rstd, dx, dw, workspace)
+    T, H = h.shape
+    if dx is None:
+        dx = torch.empty((T, H), dtype=h.dtype, device=h.device)
+    if dw is None:
+        dw = torch.empty((H,), dtype=torch.float32, device=h.device)
+    if workspace is None:
+        workspace = _workspace(T, H, h)
+    for t in (dy, dh, dx):
+        if t.shape != h.shape or t.dtype != h.dtype:
+            raise ValueError("dy, dh and dx must match h in shape and dtype")
+    if dw.dtype != torch.float32 or dw.numel() != H or not dw.is_contiguous():
+        raise ValueError("dw must be a contiguous fp32 [H] tensor")
+    _call("ftk_rmsnorm_add_bwd", _ptr(dy), _rows(dy, "dy"), _ptr(dh), _rows(dh, "dh"), _ptr(h),
+          _rows(h, "h"), _ptr(w), _ptr(rstd), _ptr(dx), _rows(dx, "dx"), _ptr(dw),
+          _ptr(workspace), workspace.numel() * workspace.element_size(), T, H, float(eps),
+          _code(h), _stream(h))
     return dx, dw
 
 

@@ -29,7 +29,7 @@ from typing import Dict, Optional, Sequence
 import numpy as np
 import torch
 
-TENSOR_SLOTS = ("x", "w", "dy", "g", "u", "dh", "q", "k", "dq", "dk")
+TENSOR_SLOTS = ("x", "w", "dy", "g", "u", "dh", "q", "k", "dq", "dk", "res", "dres")
 
 
 @dataclasses.dataclass(frozen=True)
@@ -142,6 +142,18 @@ def rmsnorm_inputs(wl: Workload, device="cpu", T: Optional[int] = None):
     }
 
 
+def rmsnorm_add_inputs(wl: Workload, device="cpu", T: Optional[int] = None):
+    """Inputs of the norm with the residual add in front: x (the sublayer's
+    output, N(0, 1)), the residual stream res (N(0, 2^2), larger than one
+    sublayer's contribution), w, dy, and dh, the gradient the residual stream
+    carries back into h (N(0, 1))."""
+    T = wl.T if T is None else T
+    d = rmsnorm_inputs(wl, device, T)
+    d["res"] = draw(wl, "res", (T, wl.H), device, std=2.0)
+    d["dh"] = draw(wl, "dres", (T, wl.H), device)
+    return d
+
+
 def swiglu_inputs(wl: Workload, device="cpu", T: Optional[int] = None):
     T = wl.T_swiglu if T is None else T
     return {
@@ -174,6 +186,10 @@ def ideal_bytes(wl: Workload) -> Dict[str, int]:
         "swiglu_bwd": 5 * e * Ts * I,
         "qk_rope_fwd": rope,
         "qk_rope_bwd": rope,
+        # the residual-add variant of the norm: x and res in, h and y out;
+        # backward: dy, dh and h in, dx out
+        "rmsnorm_add_fwd": 4 * e * T * H + 4 * T + e * H,
+        "rmsnorm_add_bwd": 4 * e * T * H + 4 * T + e * H + 4 * H,
     }
 
 
@@ -182,4 +198,5 @@ def tokens_per_call(wl: Workload) -> Dict[str, int]:
         "rmsnorm_fwd": wl.T, "rmsnorm_bwd": wl.T,
         "swiglu_fwd": wl.T_swiglu, "swiglu_bwd": wl.T_swiglu,
         "qk_rope_fwd": wl.T, "qk_rope_bwd": wl.T,
+        "rmsnorm_add_fwd": wl.T, "rmsnorm_add_bwd": wl.T,
     }

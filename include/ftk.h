@@ -130,6 +130,42 @@ FTK_API ftk_status ftk_rmsnorm_bwd_noalloc(const void *dy, int64_t lddy, const v
                                            int64_t H, float eps, ftk_dtype dtype,
                                            ftk_stream_t stream);
 
+/* Forward RMSNorm with the pre-norm block's residual add fused in front
+ * (the variant of optimisation (1) of "Chronicals", arXiv 2601.02609,
+ * abstract, in which the norm also performs the add of the residual stream
+ * that precedes it; the page prints no formula):
+ *   h[t,j] = x[t,j] + res[t,j]    added in fp32, rounded to dtype, STORED
+ *   then ftk_rmsnorm_fwd of h:  r[t] from h,  y[t,j] = h[t,j] * r[t] * w[j]
+ * The norm reads the stored (rounded) h, so the results equal a separate add
+ * followed by ftk_rmsnorm_fwd, bit for bit.  x [T, ldx], res [T, ldr],
+ * h [T, ldh], y [T, ldy] (dtype); w [H] (dtype); rstd [T] fp32, nullable.
+ * h may alias x or res exactly (same pointer and stride) to update the
+ * residual stream in place; y must not overlap any other argument.
+ * Each row of x and res is read once and h, y written once. */
+FTK_API ftk_status ftk_rmsnorm_add_fwd(const void *x, int64_t ldx, const void *res,
+                                       int64_t ldr, const void *w, void *h, int64_t ldh,
+                                       void *y, int64_t ldy, float *rstd, int64_t T,
+                                       int64_t H, float eps, ftk_dtype dtype,
+                                       ftk_stream_t stream);
+
+/* Backward of ftk_rmsnorm_add_fwd.  The gradient reaching h is dh (from the
+ * later users of the residual stream) plus the norm's backward at h; it is
+ * the gradient of x and of res alike, returned once as dx:
+ *   c[t]    = sum_j dy[t,j] w[j] h[t,j]
+ *   dx[t,j] = dh[t,j] + r[t] w[j] dy[t,j] - r[t]^3 h[t,j] c[t] / H
+ *   dw[j]   = sum_t dy[t,j] h[t,j] r[t]          (fp32, OVERWRITTEN)
+ * dy [T, lddy], dh [T, lddh], h [T, ldh] (the forward's stored h),
+ * dx [T, lddx] (dtype); w, rstd, dw, workspace and the workspace size as in
+ * ftk_rmsnorm_bwd (ftk_rmsnorm_bwd_workspace_bytes gives it; rstd NULL
+ * recomputes r from h).  dx may alias dy or dh exactly; it must not overlap
+ * h, w, rstd, dw or the workspace.  dw is bitwise reproducible run to run. */
+FTK_API ftk_status ftk_rmsnorm_add_bwd(const void *dy, int64_t lddy, const void *dh,
+                                       int64_t lddh, const void *h, int64_t ldh,
+                                       const void *w, const float *rstd, void *dx,
+                                       int64_t lddx, float *dw, void *workspace,
+                                       size_t workspace_bytes, int64_t T, int64_t H,
+                                       float eps, ftk_dtype dtype, ftk_stream_t stream);
+
 /* -------------------------------------------------------------- SwiGLU */
 
 /* Forward SwiGLU, elementwise over T rows of I features:

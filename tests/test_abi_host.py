@@ -92,6 +92,63 @@ def test_rmsnorm_bwd_argument_errors(lib):
     assert f(*args(dx=dy + 2)) == ALIAS       # dx partially over dy
 
 
+def test_rmsnorm_add_fwd_argument_errors(lib):
+    f = lib.ftk_rmsnorm_add_fwd
+    x, res, w, h, y, r = (A + i * 65536 for i in range(6))
+    names = ["x", "ldx", "res", "ldr", "w", "h", "ldh", "y", "ldy", "rstd", "T", "H", "eps",
+             "dt", "s"]
+    ok = [x, 64, res, 64, w, h, 64, y, 64, r, 4, 64, 1e-6, BF16, None]
+
+    def call(**kw):
+        a = list(ok)
+        for n, v in kw.items():
+            a[names.index(n)] = v
+        return f(*a)
+
+    assert call(T=0) == OK
+    assert call(res=None, T=0) == OK
+    assert call(dt=4) == DTYPE
+    assert call(ldr=63) == SHAPE
+    assert call(ldh=32) == SHAPE
+    assert call(res=None) == NULL
+    assert call(h=None) == NULL
+    assert call(res=res + 1) == ALIGN
+    assert call(h=h + 2, dt=F32) == ALIGN
+    assert call(h=x + 2) == ALIAS               # h partly over x
+    assert call(h=res + 64) == ALIAS            # h partly over res
+    assert call(y=x) == ALIAS                   # y over an input
+    assert call(y=h) == ALIAS                   # y over h
+    assert call(rstd=h + 16) == ALIAS           # rstd inside h
+    assert call(rstd=res + 16) == ALIAS         # rstd inside res
+    assert call(h=x, T=0) == OK and call(h=res, T=0) == OK
+
+
+def test_rmsnorm_add_bwd_argument_errors(lib):
+    f = lib.ftk_rmsnorm_add_bwd
+    dy, dh, h, w, dx, dw, ws = (A + i * 65536 for i in range(7))
+    names = ["dy", "lddy", "dh", "lddh", "h", "ldh", "w", "rstd", "dx", "lddx", "dw", "ws",
+             "wsb", "T", "H", "eps", "dt", "s"]
+    ok = [dy, 64, dh, 64, h, 64, w, None, dx, 64, dw, ws, 1 << 16, 4, 64, 1e-6, BF16, None]
+
+    def call(**kw):
+        a = list(ok)
+        for n, v in kw.items():
+            a[names.index(n)] = v
+        return f(*a)
+
+    assert call(T=0) == OK
+    assert call(dt=2) == DTYPE
+    assert call(lddh=60) == SHAPE
+    assert call(dh=None) == NULL
+    assert call(h=None) == NULL
+    assert call(ws=None) == WORKSPACE
+    assert call(dh=dh + 1) == ALIGN
+    assert call(dx=dh + 2) == ALIAS             # dx partly over dh
+    assert call(dx=h) == ALIAS                  # dx over h
+    assert call(dw=dh + 16) == ALIAS            # dw inside dh
+    assert call(ws=dh) == ALIAS                 # workspace over dh
+
+
 def test_swiglu_argument_errors(lib):
     f, b = lib.ftk_swiglu_fwd, lib.ftk_swiglu_bwd
     g, u, h = A, A + 65536, A + 2 * 65536
