@@ -93,9 +93,10 @@ KERNEL_SOURCES = {"rmsnorm_fwd": ("rmsnorm_fwd.cu",),
                   "swiglu_fwd": ("swiglu.cu",), "swiglu_bwd": ("swiglu.cu",),
                   "qk_rope_fwd": ("qk_rope.cu",), "qk_rope_bwd": ("qk_rope.cu",),
                   "rmsnorm_add_fwd": ("rmsnorm_fwd.cu",),
-                  "rmsnorm_add_bwd": ("rmsnorm_add_bwd.cu", "rmsnorm_bwd.cuh")}
-# widened ops timed beside the step (not part of it)
-EXT_OPS = ("rmsnorm_add_fwd", "rmsnorm_add_bwd")
+                  "rmsnorm_add_bwd": ("rmsnorm_add_bwd.cu", "rmsnorm_bwd.cuh"),
+                  "swiglu_bwd_h": ("swiglu.cu",)}
+# widened ops timed beside the step (not part of it), with their launches
+EXT_OPS = {"rmsnorm_add_fwd": 1, "rmsnorm_add_bwd": 2, "swiglu_bwd_h": 1}
 
 
 def kernel_source_hash(op: str) -> str:
@@ -491,7 +492,7 @@ def run_ours(args):
     }
     if not args.no_ext:
         out["extensions"] = ext_leg(batch, flush, flush_graph, dev, Kk, hbm, src)
-        out["gpu_launches"] += 3 * Kk  # add-norm forward (1) and backward (2) launches
+        out["gpu_launches"] += sum(EXT_OPS.values()) * Kk
     out["clocks"] = sampler.summary(t0, t1)
     out["device_status"] = ftk.device_status(clear=True)  # 0: no pipeline wait ran out
 
@@ -516,7 +517,7 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
 
     from fine_tuning_gb300 import ftk
     from fine_tuning_gb300 import workloads as W
-    wl, i = batch.wl, batch.inputs
+    wl, i, o = batch.wl, batch.inputs, batch.outputs
     extra = W.rmsnorm_add_inputs(wl, dev)
     res, dres = extra["res"], extra["dh"]
     T, H, dt = wl.T, wl.H, wl.torch_dtype
@@ -530,7 +531,10 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
                                                        rstd=rstd),
         "rmsnorm_add_bwd": lambda: ftk.rmsnorm_add_bwd(i["dy"], dres, h, i["w"], rstd, wl.eps,
                                                        dx=dx, dw=dw, workspace=batch.ws),
+        "swiglu_bwd_h": lambda: ftk.swiglu_bwd_h(i["dh"], i["g"], i["u"], dg=o["dg"],
+                                                 du=o["du"], h=o["h"]),
     }
+    assert set(ops) == set(EXT_OPS)
     for op in ops.values():  # warm-up (and the first, allocating, launch)
         op()
     graphs = {}
@@ -562,7 +566,7 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
                   "frac_of_measured_hbm" if src == "measured" else "frac_of_fallback_hbm":
                       round(gbs / hbm, 4),
                   "tokens_per_s": round(toks[n] / (ms * 1e-3), 1), "ideal_bytes": ib[n],
-                  "launches": 1 if n.endswith("fwd") else 2}
+                  "launches": EXT_OPS[n]}
     out["timing"] = (f"{reps} replays of a graph [L2 flush, op] minus a graph [L2 flush], "
                      "CUDA events around each; outside the step's timed region")
     del h, y, rstd, dx, dw, res, dres, extra

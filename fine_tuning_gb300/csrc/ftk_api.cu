@@ -330,39 +330,74 @@ FTK_API ftk_status ftk_swiglu_fwd(const void *g, const void *u, int64_t ld_gu, v
   return finish(ftk::launch_swiglu_fwd(dt, vec, wide, a, dev, (cudaStream_t)stream));
 }
 
-FTK_API ftk_status ftk_swiglu_bwd(const void *dh, int64_t ld_dh, const void *g, const void *u,
-                                  int64_t ld_gu, void *dg, void *du, int64_t ld_dgu, int64_t T,
-                                  int64_t I, ftk_dtype dtype, ftk_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by ftk_swiglu_bwd and ftk_swiglu_bwd_h; h == nullptr: no re-emitted h.
+ftk_status swiglu_bwd_checked(const void *dh, int64_t ld_dh, const void *g, const void *u,
+                              int64_t ld_gu, void *dg, void *du, int64_t ld_dgu, void *h,
+                              int64_t ld_h, int64_t T, int64_t I, ftk_dtype dtype,
+                              ftk_stream_t stream) {
+  const bool emit = h != nullptr;
   if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
-  if (T < 0 || I < 0 || ld_dh < I || ld_gu < I || ld_dgu < I) return FTK_ERR_SHAPE;
+  if (T < 0 || I < 0 || ld_dh < I || ld_gu < I || ld_dgu < I || (emit && ld_h < I))
+    return FTK_ERR_SHAPE;
   if (T == 0 || I == 0) return FTK_OK;
   if (!dh || !g || !u || !dg || !du) return FTK_ERR_NULL;
   const DType dt = (DType)dtype;
   const int64_t es = ftk::dtype_bytes(dt);
   if (!aligned(dh, es) || !aligned(g, es) || !aligned(u, es) || !aligned(dg, es) ||
-      !aligned(du, es))
+      !aligned(du, es) || !aligned(h, es))
     return FTK_ERR_ALIGN;
   const View vdh = view(dh, T, ld_dh, I, es), vg = view(g, T, ld_gu, I, es);
   const View vu = view(u, T, ld_gu, I, es), vdg = view(dg, T, ld_dgu, I, es);
-  const View vdu = view(du, T, ld_dgu, I, es);
-  if (may_overlap(vdg, vdu)) return FTK_ERR_ALIAS;
+  const View vdu = view(du, T, ld_dgu, I, es), vh = view(h, emit ? T : 0, ld_h, I, es);
+  // every thread reads all its inputs before it writes, so an output may
+  // replace an input exactly; outputs never overlap one another
+  if (may_overlap(vdg, vdu) || may_overlap(vh, vdg) || may_overlap(vh, vdu))
+    return FTK_ERR_ALIAS;
   const View ins[3] = {vdh, vg, vu};
-  for (const View &o : {vdg, vdu})
+  for (const View &o : {vdg, vdu, vh})
     for (const View &i : ins)
       if (!same_view(o, i) && may_overlap(o, i)) return FTK_ERR_ALIAS;
 
   const int n = dt == DType::F32 ? 4 : 8;
-  const bool vec = aligned(dh, 16) && aligned(g, 16) && aligned(u, 16) && aligned(dg, 16) &&
-                   aligned(du, 16) && I % n == 0 && ld_dh % n == 0 && ld_gu % n == 0 &&
-                   ld_dgu % n == 0;
+  bool vec = aligned(dh, 16) && aligned(g, 16) && aligned(u, 16) && aligned(dg, 16) &&
+             aligned(du, 16) && I % n == 0 && ld_dh % n == 0 && ld_gu % n == 0 &&
+             ld_dgu % n == 0;
+  if (emit) vec = vec && aligned(h, 16) && ld_h % n == 0;
   const bool wide = vdh.max_offset() > kNarrowLimit || vg.max_offset() > kNarrowLimit ||
                     vu.max_offset() > kNarrowLimit || vdg.max_offset() > kNarrowLimit ||
-                    vdu.max_offset() > kNarrowLimit || T * I > kNarrowLimit;
+                    vdu.max_offset() > kNarrowLimit || (emit && vh.max_offset() > kNarrowLimit) ||
+                    T * I > kNarrowLimit;
   ftk::DeviceInfo dev;
   cudaError_t e = device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   ftk::SwigluBwdArgs a{dh, ld_dh, g, u, ld_gu, dg, du, ld_dgu, T, I};
+  a.h = h;
+  a.ld_h = ld_h;
   return finish(ftk::launch_swiglu_bwd(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+FTK_API ftk_status ftk_swiglu_bwd(const void *dh, int64_t ld_dh, const void *g, const void *u,
+                                  int64_t ld_gu, void *dg, void *du, int64_t ld_dgu, int64_t T,
+                                  int64_t I, ftk_dtype dtype, ftk_stream_t stream) {
+  return swiglu_bwd_checked(dh, ld_dh, g, u, ld_gu, dg, du, ld_dgu, nullptr, 0, T, I, dtype,
+                            stream);
+}
+
+FTK_API ftk_status ftk_swiglu_bwd_h(const void *dh, int64_t ld_dh, const void *g, const void *u,
+                                    int64_t ld_gu, void *dg, void *du, int64_t ld_dgu, void *h,
+                                    int64_t ld_h, int64_t T, int64_t I, ftk_dtype dtype,
+                                    ftk_stream_t stream) {
+  if (!h && T > 0 && I > 0) return FTK_ERR_NULL;
+  return swiglu_bwd_checked(dh, ld_dh, g, u, ld_gu, dg, du, ld_dgu, h, ld_h, T, I, dtype,
+                            stream);
 }
 
 // ------------------------------------------------------------------ QK-RoPE

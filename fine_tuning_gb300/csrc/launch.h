@@ -145,6 +145,8 @@ struct SwigluBwdArgs {
   void *dg, *du;
   int64_t ld_dgu;
   int64_t T, I;
+  void *h = nullptr;  // nullable: re-emit the forward's h
+  int64_t ld_h = 0;
 };
 cudaError_t launch_swiglu_bwd(DType dt, bool vec, bool wide, const SwigluBwdArgs &a,
                               const DeviceInfo &dev, cudaStream_t s);

@@ -3,6 +3,10 @@
 // the page gives no formula, these are the standard definitions):
 //   forward:   h  = silu(g) * u = g * s * u,   s = sigmoid(g) = 1 / (1 + e^-g)
 //   backward:  dg = dh * u * s * (1 + g * (1 - s)),   du = dh * g * s
+// The backward can also re-emit h (EMIT_H), computed exactly as the forward
+// computes it, for a caller that keeps g and u but not h (the down
+// projection's weight gradient needs h); that costs one extra write instead
+// of storing h in the forward and reading it back.
 //
 // Every input element is read once and every output written once.  A thread
 // moves U 16-byte packets of each operand per launch, all loads issued before
@@ -87,10 +91,10 @@ swiglu_fwd_kernel(const T *g, const T *u, Idx ld_gu, T *h, Idx ld_h, Idx npk, Id
   }
 }
 
-template <typename T, typename Idx, int N, int U, bool CONTIG>
+template <typename T, typename Idx, int N, int U, bool CONTIG, bool EMIT_H>
 __global__ void __launch_bounds__(kThreads)
 swiglu_bwd_kernel(const T *dh, Idx ld_dh, const T *g, const T *u, Idx ld_gu, T *dg, T *du,
-                  Idx ld_dgu, Idx npk, Idx ip) {
+                  Idx ld_dgu, T *h, Idx ld_h, Idx npk, Idx ip) {
   pdl_wait();
   pdl_trigger();
   const Idx base = (Idx)blockIdx.x * (kThreads * U) + threadIdx.x;
@@ -109,8 +113,8 @@ swiglu_bwd_kernel(const T *dh, Idx ld_dh, const T *g, const T *u, Idx ld_gu, T *
   for (int k = 0; k < U; ++k) {
     const Idx v = base + k * kThreads;
     if (v < npk) {
-      Packet<T, N> og, ou;
-      float dgv[N], duv[N];
+      Packet<T, N> og, ou, oh;
+      float dgv[N], duv[N], hv_out[N];
 #pragma unroll
       for (int e = 0; e < N; ++e) {
         const float gf = gv[k].get(e), uf = uv[k].get(e), hf = hv[k].get(e);
@@ -118,23 +122,27 @@ swiglu_bwd_kernel(const T *dh, Idx ld_dh, const T *g, const T *u, Idx ld_gu, T *
         sigmoid2<T>(gf, &s, &sc);
         dgv[e] = hf * uf * (s * fmaf(gf, sc, 1.0f));
         duv[e] = hf * (gf * s);
+        if (EMIT_H) hv_out[e] = gf * s * uf;  // the forward's expression
       }
       if constexpr (N % 2 == 0) {
 #pragma unroll
         for (int e = 0; e < N; e += 2) {
           og.set2(e, dgv[e], dgv[e + 1]);
           ou.set2(e, duv[e], duv[e + 1]);
+          if (EMIT_H) oh.set2(e, hv_out[e], hv_out[e + 1]);
         }
       } else {
 #pragma unroll
         for (int e = 0; e < N; ++e) {
           og.set(e, dgv[e]);
           ou.set(e, duv[e]);
+          if (EMIT_H) oh.set(e, hv_out[e]);
         }
       }
       const Idx o = packet_offset<Idx, N, CONTIG>(v, ip, ld_dgu);
       store_packet<T, N>(dg + o, og);
       store_packet<T, N>(du + o, ou);
+      if (EMIT_H) store_packet<T, N>(h + packet_offset<Idx, N, CONTIG>(v, ip, ld_h), oh);
     }
   }
 }
@@ -152,18 +160,23 @@ cudaError_t fwd_launch(const SwigluFwdArgs &a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <typename T, typename Idx, int N, int U, bool CONTIG>
-cudaError_t bwd_launch(const SwigluBwdArgs &a, cudaStream_t s) {
+template <typename T, typename Idx, int N, int U, bool CONTIG, bool EMIT_H>
+cudaError_t bwd_launch_form(const SwigluBwdArgs &a, cudaStream_t s) {
   const Idx ip = (Idx)(a.I / N);
   const Idx npk = (Idx)a.T * ip;
   const int64_t grid = ceil_div((int64_t)npk, (int64_t)kThreads * U);
-  {
-    cudaError_t le_ = launch_pdl(swiglu_bwd_kernel<T, Idx, N, U, CONTIG>, dim3((unsigned)grid), dim3(kThreads), 0, s,
-                                 (const T *)a.dh, (Idx)a.ld_dh, (const T *)a.g, (const T *)a.u, (Idx)a.ld_gu, (T *)a.dg,
-      (T *)a.du, (Idx)a.ld_dgu, npk, ip);
-    if (le_ != cudaSuccess) return le_;
-  }
+  cudaError_t e = launch_pdl(swiglu_bwd_kernel<T, Idx, N, U, CONTIG, EMIT_H>,
+                             dim3((unsigned)grid), dim3(kThreads), 0, s, (const T *)a.dh,
+                             (Idx)a.ld_dh, (const T *)a.g, (const T *)a.u, (Idx)a.ld_gu,
+                             (T *)a.dg, (T *)a.du, (Idx)a.ld_dgu, (T *)a.h, (Idx)a.ld_h, npk, ip);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <typename T, typename Idx, int N, int U, bool CONTIG>
+cudaError_t bwd_launch(const SwigluBwdArgs &a, cudaStream_t s) {
+  return a.h ? bwd_launch_form<T, Idx, N, U, CONTIG, true>(a, s)
+             : bwd_launch_form<T, Idx, N, U, CONTIG, false>(a, s);
 }
 
 }  // namespace
@@ -191,7 +204,8 @@ cudaError_t launch_swiglu_fwd(DType dt, bool vec, bool wide, const SwigluFwdArgs
 cudaError_t launch_swiglu_bwd(DType dt, bool vec, bool wide, const SwigluBwdArgs &a,
                               const DeviceInfo &, cudaStream_t s) {
   constexpr int U = 2;
-  const bool contig = a.ld_dh == a.I && a.ld_gu == a.I && a.ld_dgu == a.I;
+  const bool contig =
+      a.ld_dh == a.I && a.ld_gu == a.I && a.ld_dgu == a.I && (!a.h || a.ld_h == a.I);
 #define FTK_SWIGLU_BWD(T, Idx)                                                     \
   if (vec) {                                                                       \
     constexpr int NV = VecWidth<T>::value;                                         \

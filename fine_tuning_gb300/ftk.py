@@ -59,6 +59,8 @@ def library() -> ctypes.CDLL:
                                      i64, i64, f32, dt, vp]),
         "ftk_swiglu_fwd": (st, [vp, vp, i64, vp, i64, i64, i64, dt, vp]),
         "ftk_swiglu_bwd": (st, [vp, i64, vp, vp, i64, vp, vp, i64, i64, i64, dt, vp]),
+        "ftk_swiglu_bwd_h": (st, [vp, i64, vp, vp, i64, vp, vp, i64, vp, i64, i64, i64, dt,
+                                  vp]),
         "ftk_qk_rope_fwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, dt, vp]),
         "ftk_qk_rope_bwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, dt, vp]),
         "ftk_bfd_pack": (st, [vp, i64, i32, vp, vp, vp, vp]),
@@ -255,6 +257,34 @@ def swiglu_bwd(dh: torch.Tensor, g: torch.Tensor, u: torch.Tensor,
     _call("ftk_swiglu_bwd", _ptr(dh), _rows(dh, "dh"), _ptr(g), _ptr(u), ld, _ptr(dg), _ptr(du),
           ldo, T, I, _code(g), _stream(g))
     return dg, du
+
+
+def swiglu_bwd_h(dh: torch.Tensor, g: torch.Tensor, u: torch.Tensor,
+                 dg: Optional[torch.Tensor] = None, du: Optional[torch.Tensor] = None,
+                 h: Optional[torch.Tensor] = None
+                 ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(dg, du, h): swiglu_bwd plus the forward's h, recomputed bit-identically
+    (h may be dh, g or u themselves; not dg or du)."""
+    _cuda(dh, g, u, dg, du, h)
+    T, I = g.shape
+    ld = _rows(g, "g")
+    if _rows(u, "u") != ld or u.shape != g.shape or dh.shape != g.shape:
+        raise ValueError("dh, g and u must have one shape; g and u one row stride")
+    if dg is None and du is None:
+        dg = torch.empty((T, I), dtype=g.dtype, device=g.device)
+        du = torch.empty((T, I), dtype=g.dtype, device=g.device)
+    elif dg is None or du is None:
+        raise ValueError("pass both dg and du, or neither")
+    if h is None:
+        h = torch.empty((T, I), dtype=g.dtype, device=g.device)
+    if h.shape != g.shape or h.dtype != g.dtype:
+        raise ValueError("h must match g in shape and dtype")
+    ldo = _rows(dg, "dg")
+    if _rows(du, "du") != ldo:
+        raise ValueError("dg and du must share one row stride")
+    _call("ftk_swiglu_bwd_h", _ptr(dh), _rows(dh, "dh"), _ptr(g), _ptr(u), ld, _ptr(dg),
+          _ptr(du), ldo, _ptr(h), _rows(h, "h"), T, I, _code(g), _stream(g))
+    return dg, du, h
 
 
 # ---------------------------------------------------------------- QK-RoPE

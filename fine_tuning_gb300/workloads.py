@@ -190,6 +190,8 @@ def ideal_bytes(wl: Workload) -> Dict[str, int]:
         # backward: dy, dh and h in, dx out
         "rmsnorm_add_fwd": 4 * e * T * H + 4 * T + e * H,
         "rmsnorm_add_bwd": 4 * e * T * H + 4 * T + e * H + 4 * H,
+        # SwiGLU backward that re-emits h: dh, g, u in; dg, du, h out
+        "swiglu_bwd_h": 6 * e * Ts * I,
     }
 
 
@@ -198,5 +200,5 @@ def tokens_per_call(wl: Workload) -> Dict[str, int]:
         "rmsnorm_fwd": wl.T, "rmsnorm_bwd": wl.T,
         "swiglu_fwd": wl.T_swiglu, "swiglu_bwd": wl.T_swiglu,
         "qk_rope_fwd": wl.T, "qk_rope_bwd": wl.T,
-        "rmsnorm_add_fwd": wl.T, "rmsnorm_add_bwd": wl.T,
+        "rmsnorm_add_fwd": wl.T, "rmsnorm_add_bwd": wl.T, "swiglu_bwd_h": wl.T_swiglu,
     }

@@ -186,6 +186,20 @@ FTK_API ftk_status ftk_swiglu_bwd(const void *dh, int64_t ld_dh, const void *g,
                           int64_t ld_dgu, int64_t T, int64_t I,
                           ftk_dtype dtype, ftk_stream_t stream);
 
+/* ftk_swiglu_bwd that also re-emits the forward's h (optimisation (1) of
+ * "Chronicals", arXiv 2601.02609, abstract: the fused SwiGLU; re-emitting h
+ * is this library's variant): besides dg and du it writes
+ *   h = g * sigmoid(g) * u,
+ * computed exactly as ftk_swiglu_fwd computes it (bit-identical), so a
+ * training step can drop h after the forward and get it back here, where
+ * the down projection's weight gradient needs it.  h: [T, ld_h], written
+ * once.  h may replace dh, g or u exactly (same pointer and stride) but must
+ * not overlap dg or du; the other arguments and rules are ftk_swiglu_bwd's. */
+FTK_API ftk_status ftk_swiglu_bwd_h(const void *dh, int64_t ld_dh, const void *g,
+                                    const void *u, int64_t ld_gu, void *dg, void *du,
+                                    int64_t ld_dgu, void *h, int64_t ld_h, int64_t T,
+                                    int64_t I, ftk_dtype dtype, ftk_stream_t stream);
+
 /* ------------------------------------------------------------- QK-RoPE */
 
 /* In-place rotary embedding of Q and K together, rotate-half (NeoX) layout,

@@ -162,6 +162,14 @@ def test_swiglu_argument_errors(lib):
     dh, dg, du = A + 3 * 65536, A + 4 * 65536, A + 5 * 65536
     assert b(dh, 64, g, u, 64, dg, dg + 16, 64, 4, 64, BF16, None) == ALIAS  # dg/du overlap
     assert b(dh, 64, g, u, 64, dg, du, 64, 4, 64, 9, None) == DTYPE
+    bh, h2 = lib.ftk_swiglu_bwd_h, A + 6 * 65536
+    assert bh(dh, 64, g, u, 64, dg, du, 64, h2, 64, 0, 64, BF16, None) == OK
+    assert bh(dh, 64, g, u, 64, dg, du, 64, None, 64, 4, 64, BF16, None) == NULL
+    assert bh(dh, 64, g, u, 64, dg, du, 64, h2, 32, 4, 64, BF16, None) == SHAPE
+    assert bh(dh, 64, g, u, 64, dg, du, 64, h2 + 1, 64, 4, 64, BF16, None) == ALIGN
+    assert bh(dh, 64, g, u, 64, dg, du, 64, dg, 64, 4, 64, BF16, None) == ALIAS   # h over dg
+    assert bh(dh, 64, g, u, 64, dg, du, 64, du + 8, 64, 4, 64, BF16, None) == ALIAS
+    assert bh(dh, 64, g, u, 64, dg, du, 64, g + 2, 64, 4, 64, BF16, None) == ALIAS  # partly over g
 
 
 def test_qk_rope_argument_errors(lib):

@@ -178,6 +178,13 @@ def test_swiglu_shapes(dtype, T, I):
     assert_close("h", hg.t, hr, dtype=code(dtype))
     assert_close("dg", dgg.t, dgr, dgs, dtype=code(dtype))
     assert_close("du", dug.t, dur, dtype=code(dtype))
+    # the backward that re-emits h, into guarded buffers of its own
+    h2, dg2, du2 = Guarded((T, I), dtype), Guarded((T, I), dtype), Guarded((T, I), dtype)
+    ftk.swiglu_bwd_h(dh, g, u, dg=dg2.t, du=du2.t, h=h2.t)
+    torch.cuda.synchronize()
+    for gd in (h2, dg2, du2):
+        gd.check()
+    assert torch.equal(h2.t, hg.t) and torch.equal(dg2.t, dgg.t) and torch.equal(du2.t, dug.t)
 
 
 def test_swiglu_fused_gate_up_and_in_place():
@@ -191,6 +198,23 @@ def test_swiglu_fused_gate_up_and_in_place():
     dgr, dur, dgs = oracle.swiglu_bwd(dh.cpu(), g0, u0, scales=True)
     ftk.swiglu_bwd(dh, g, u, dg=g, du=u)  # gradients written over gate_up
     torch.cuda.synchronize()
+    assert_close("dg in place", g, dgr, dgs)
+    assert_close("du in place", u, dur)
+
+
+def test_swiglu_bwd_h_fused_gate_up_in_place():
+    """Fused [T, 2I] gate_up: dg, du written over it, and h over dh."""
+    T, I = 129, 4864
+    gu = randn((T, 2 * I), torch.bfloat16, 33)
+    g, u = gu[:, :I], gu[:, I:]
+    g0, u0 = g.cpu(), u.cpu()
+    dh = randn((T, I), torch.bfloat16, 34)
+    dh0 = dh.cpu()
+    h_fwd = ftk.swiglu_fwd(g, u)
+    ftk.swiglu_bwd_h(dh, g, u, dg=g, du=u, h=dh)
+    torch.cuda.synchronize()
+    assert torch.equal(dh, h_fwd)
+    dgr, dur, dgs = oracle.swiglu_bwd(dh0, g0, u0, scales=True)
     assert_close("dg in place", g, dgr, dgs)
     assert_close("du in place", u, dur)
 

@@ -110,7 +110,11 @@ def check_swiglu(wl, n_rows=None):
     g, u, dh = d["g"], d["u"], d["dh"]
     h = ftk.swiglu_fwd(g, u)
     dg, du = ftk.swiglu_bwd(dh, g, u)
+    dg2, du2, h2 = ftk.swiglu_bwd_h(dh, g, u)
     torch.cuda.synchronize()
+    # the backward that re-emits h: h exactly as the forward wrote it, and
+    # the same dg, du
+    assert torch.equal(h2, h) and torch.equal(dg2, dg) and torch.equal(du2, du)
     rows = np.arange(wl.T_swiglu) if n_rows is None else sample_rows(wl.T_swiglu, n_rows)
     ri = torch.as_tensor(rows, device=DEV)
     gs, us, dhs = g[ri].cpu(), u[ri].cpu(), dh[ri].cpu()
