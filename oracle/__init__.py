@@ -38,6 +38,13 @@ def _load():
         lib.oracle_qk_rope.argtypes = [D, D, D, D, D, D, I64, i64, I32, i32,
                                        i32, i32, i32, f64, ctypes.c_int]
         lib.oracle_qk_rope.restype = ctypes.c_int
+        lib.oracle_qk_rope_freq.argtypes = [D, D, D, D, D, D, I64, i64, I32, i32,
+                                            i32, i32, i32, D, ctypes.c_int]
+        lib.oracle_qk_rope_freq.restype = ctypes.c_int
+        lib.oracle_rope_inv_freq.argtypes = [i32, f64, D]
+        lib.oracle_rope_inv_freq.restype = None
+        lib.oracle_rope_llama3_inv_freq.argtypes = [i32, f64, f64, f64, f64, f64, D]
+        lib.oracle_rope_llama3_inv_freq.restype = ctypes.c_int
         lib.oracle_positions.argtypes = [I64, I64, i64, I32, i32]
         lib.oracle_positions.restype = ctypes.c_int
         lib.oracle_rmsnorm_add_fwd.argtypes = [D, D, D, D, D, D, i64, i64, f64, ctypes.c_int]
@@ -151,6 +158,48 @@ def qk_rope(q, k, cu_seqlens, theta, sign=+1, tok=None, scales=False):
     if rc != 0:
         raise ValueError("oracle_qk_rope: token outside the packed batch or odd D")
     return (qo, ko, qs, ks) if scales else (qo, ko)
+
+
+def qk_rope_freq(q, k, cu_seqlens, inv_freq, sign=+1, tok=None, scales=False):
+    """qk_rope with an explicit inverse-frequency table inv_freq[D/2]
+    (phi_i = p * inv_freq[i]) instead of theta."""
+    q, k = _f64(q), _f64(k)
+    n, Hq, D = q.shape
+    Hkv = k.shape[1]
+    assert k.shape[0] == n and k.shape[2] == D
+    f = _f64(inv_freq)
+    assert f.shape == (D // 2,)
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    B = cu.size - 1
+    tk = None if tok is None else np.ascontiguousarray(np.asarray(tok, dtype=np.int64))
+    qo, ko = np.empty_like(q), np.empty_like(k)
+    qs = np.empty_like(q) if scales else None
+    ks = np.empty_like(k) if scales else None
+    rc = _load().oracle_qk_rope_freq(_p(q), _p(k), _p(qo), _p(ko), _p(qs), _p(ks),
+                                     _p(tk, ctypes.c_int64), n, _p(cu, ctypes.c_int32),
+                                     B, Hq, Hkv, D, _p(f), int(sign))
+    if rc != 0:
+        raise ValueError("oracle_qk_rope_freq: token outside the packed batch or odd D")
+    return (qo, ko, qs, ks) if scales else (qo, ko)
+
+
+def rope_inv_freq(D, theta):
+    """theta^(-2i/D), i < D/2."""
+    out = np.empty(D // 2)
+    _load().oracle_rope_inv_freq(int(D), float(theta), _p(out))
+    return out
+
+
+def rope_llama3_inv_freq(D, theta, factor, low_freq_factor, high_freq_factor,
+                         original_max_position):
+    """The "llama3"-scaled inverse frequencies (see oracle.c)."""
+    out = np.empty(D // 2)
+    rc = _load().oracle_rope_llama3_inv_freq(int(D), float(theta), float(factor),
+                                             float(low_freq_factor), float(high_freq_factor),
+                                             float(original_max_position), _p(out))
+    if rc != 0:
+        raise ValueError("llama3 scaling needs D even and high_freq_factor > low_freq_factor")
+    return out
 
 
 def positions(cu_seqlens, tok=None, n=None):

@@ -237,7 +237,7 @@ static int64_t position_of(int64_t t, const int32_t *cu, int32_t B)
 }
 
 /* Rotate-half RoPE of one head vector v[0..D) at position p:
- *   phi_i = p * theta^(-2i/D),  i < D/2
+ *   phi_i = p * inv_freq[i],  i < D/2
  *   (v_i, v_{i+D/2}) <- (v_i cos phi - v_{i+D/2} sin phi,
  *                        v_{i+D/2} cos phi + v_i sin phi)
  * sign = -1 rotates by -phi (the transpose, used by the backward pass).
@@ -247,12 +247,11 @@ static int64_t position_of(int64_t t, const int32_t *cu, int32_t B)
  * is exact, and near cos phi = 0 the output moves with the angle even
  * though the term itself is ~0. */
 static void rotate_head(const double *v, double *out, double *scale,
-                        int64_t p, int32_t D, double theta, int sign)
+                        int64_t p, int32_t D, const double *inv_freq, int sign)
 {
     int32_t half = D / 2;
     for (int32_t i = 0; i < half; ++i) {
-        double inv_freq = pow(theta, -2.0 * (double)i / (double)D);
-        double phi = (double)sign * (double)p * inv_freq;
+        double phi = (double)sign * (double)p * inv_freq[i];
         double c = cos(phi), s = sin(phi);
         double a = v[i], b = v[i + half];
         out[i] = a * c - b * s;
@@ -266,16 +265,17 @@ static void rotate_head(const double *v, double *out, double *scale,
     }
 }
 
-/* Q and K of n packed tokens rotated together.  Row r of q/k is global token
- * tok[r] (tok may be NULL: row r is token r).  q: [n, Hq, D], k: [n, Hkv, D]
- * (contiguous), cu: int32 [B+1] sequence boundaries.  sign = +1 forward,
- * -1 backward.  Returns 0, or -1 if a token lies outside the batch or D is
- * odd.  q_scale/k_scale are nullable. */
-ORACLE_API int oracle_qk_rope(const double *q, const double *k, double *q_out,
-                              double *k_out, double *q_scale, double *k_scale,
-                              const int64_t *tok, int64_t n, const int32_t *cu,
-                              int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
-                              double theta, int sign)
+/* Q and K of n packed tokens rotated together with the inverse frequencies
+ * inv_freq[D/2].  Row r of q/k is global token tok[r] (tok may be NULL: row
+ * r is token r).  q: [n, Hq, D], k: [n, Hkv, D] (contiguous), cu: int32
+ * [B+1] sequence boundaries.  sign = +1 forward, -1 backward.  Returns 0,
+ * or -1 if a token lies outside the batch or D is odd.  q_scale/k_scale are
+ * nullable. */
+ORACLE_API int oracle_qk_rope_freq(const double *q, const double *k, double *q_out,
+                                   double *k_out, double *q_scale, double *k_scale,
+                                   const int64_t *tok, int64_t n, const int32_t *cu,
+                                   int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                   const double *inv_freq, int sign)
 {
     if (D % 2 != 0)
         return -1;
@@ -292,15 +292,77 @@ ORACLE_API int oracle_qk_rope(const double *q, const double *k, double *q_out,
         for (int32_t h = 0; h < Hq; ++h) {
             int64_t o = (r * Hq + h) * D;
             rotate_head(q + o, q_out + o, q_scale ? q_scale + o : NULL, p, D,
-                        theta, sign);
+                        inv_freq, sign);
         }
         for (int32_t h = 0; h < Hkv; ++h) {
             int64_t o = (r * Hkv + h) * D;
             rotate_head(k + o, k_out + o, k_scale ? k_scale + o : NULL, p, D,
-                        theta, sign);
+                        inv_freq, sign);
         }
     }
     return bad ? -1 : 0;
+}
+
+/* The unscaled inverse frequencies: inv_freq[i] = theta^(-2i/D). */
+ORACLE_API void oracle_rope_inv_freq(int32_t D, double theta, double *inv_freq)
+{
+    for (int32_t i = 0; i < D / 2; ++i)
+        inv_freq[i] = pow(theta, -2.0 * (double)i / (double)D);
+}
+
+/* The plain rotation (no scaling): oracle_qk_rope_freq with theta's table. */
+ORACLE_API int oracle_qk_rope(const double *q, const double *k, double *q_out,
+                              double *k_out, double *q_scale, double *k_scale,
+                              const int64_t *tok, int64_t n, const int32_t *cu,
+                              int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                              double theta, int sign)
+{
+    if (D % 2 != 0 || D <= 0)
+        return -1;
+    double *f = (double *)malloc(sizeof(double) * (size_t)(D / 2));
+    if (!f)
+        return -1;
+    oracle_rope_inv_freq(D, theta, f);
+    int rc = oracle_qk_rope_freq(q, k, q_out, k_out, q_scale, k_scale, tok, n, cu, B,
+                                 Hq, Hkv, D, f, sign);
+    free(f);
+    return rc;
+}
+
+/* "llama3" rope scaling, the rule published with Llama 3.1 for stretching a
+ * model trained on contexts of L = original_max_position tokens: with the
+ * wavelength of dimension i, lambda_i = 2 pi / inv_freq_i,
+ *   lambda_i < L / high_freq_factor  (fast-turning):  inv_freq_i unchanged;
+ *   lambda_i > L / low_freq_factor   (slow-turning):  inv_freq_i / factor;
+ *   in between: a blend,  s = (L / lambda_i - low_freq_factor)
+ *                            / (high_freq_factor - low_freq_factor),
+ *               (1 - s) * inv_freq_i / factor + s * inv_freq_i.
+ * Returns 0, or -1 for D odd / non-positive or high_freq_factor <=
+ * low_freq_factor. */
+ORACLE_API int oracle_rope_llama3_inv_freq(int32_t D, double theta, double factor,
+                                           double low_freq_factor,
+                                           double high_freq_factor,
+                                           double original_max_position,
+                                           double *inv_freq)
+{
+    if (D <= 0 || D % 2 != 0 || !(high_freq_factor > low_freq_factor))
+        return -1;
+    const double two_pi = 6.283185307179586476925;
+    const double L = original_max_position;
+    oracle_rope_inv_freq(D, theta, inv_freq);
+    for (int32_t i = 0; i < D / 2; ++i) {
+        double f = inv_freq[i];
+        double lambda = two_pi / f;
+        if (lambda < L / high_freq_factor)
+            continue;
+        if (lambda > L / low_freq_factor) {
+            inv_freq[i] = f / factor;
+            continue;
+        }
+        double s = (L / lambda - low_freq_factor) / (high_freq_factor - low_freq_factor);
+        inv_freq[i] = (1.0 - s) * f / factor + s * f;
+    }
+    return 0;
 }
 
 /* Positions alone (for the packing tests): pos[r] = position of tok[r]. */

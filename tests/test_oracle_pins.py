@@ -305,6 +305,86 @@ def test_rope_rejects_out_of_batch_token():
         oracle.qk_rope(q[:1], k[:1], cu, 1e4, tok=[int(cu[-1])])
 
 
+# ------------------------------------------------ RoPE with a frequency table
+
+@pytest.mark.parametrize("p", [0, 3, 40000])
+def test_rope_freq_d2_is_complex_multiplication(p):
+    # D = 2 with an arbitrary frequency f: (a, b) -> (a + ib) e^{i p f}
+    f, a, b = 0.37, -0.6, 1.9
+    z = complex(a, b) * cmath.exp(1j * p * f)
+    qo, _ = oracle.qk_rope_freq(np.array([[[a, b]]]), np.zeros((1, 1, 2)), [0, p + 1], [f],
+                                tok=[p])
+    np.testing.assert_allclose(qo[0, 0], [z.real, z.imag], rtol=0, atol=1e-12)
+    back, _ = oracle.qk_rope_freq(np.array([[[a, b]]]), np.zeros((1, 1, 2)), [0, p + 1], [f],
+                                  sign=-1, tok=[p])
+    zb = complex(a, b) * cmath.exp(-1j * p * f)
+    np.testing.assert_allclose(back[0, 0], [zb.real, zb.imag], rtol=0, atol=1e-12)
+
+
+def test_rope_inv_freq_closed_forms():
+    # theta^(-2i/D): 1 at i = 0, theta^(-1/2) at i = D/4, a geometric sequence
+    f = oracle.rope_inv_freq(128, 5e5)
+    assert f[0] == 1.0
+    assert math.isclose(f[32], 5e5 ** -0.5, rel_tol=1e-15)
+    np.testing.assert_allclose(f[1:] / f[:-1], 5e5 ** (-2 / 128), rtol=1e-13)
+
+
+def test_rope_freq_table_drives_each_pair():
+    # pair i turns by p * f[i]: with f = e_1 (only pair 1 turns) a unit vector
+    # in pair 0 stays put and one in pair 1 turns by p
+    D, p = 8, 5
+    f = np.array([0.0, 1.0, 0.0, 0.0])
+    e = np.eye(D)
+    qo, _ = oracle.qk_rope_freq(e[None, :, :], np.zeros((1, 0, D)), [0, p + 1], f, tok=[p])
+    np.testing.assert_allclose(qo[0, 0], e[0], atol=1e-15)
+    np.testing.assert_allclose(qo[0, 1], math.cos(p) * e[1] + math.sin(p) * e[5], atol=1e-15)
+
+
+LLAMA32 = dict(factor=32.0, low_freq_factor=1.0, high_freq_factor=4.0,
+               original_max_position=8192.0)
+
+
+def test_llama3_factor_one_is_unscaled():
+    for lo, hi in ((1.0, 4.0), (2.0, 3.0)):
+        f = oracle.rope_llama3_inv_freq(64, 5e5, 1.0, lo, hi, 8192.0)
+        np.testing.assert_allclose(f, oracle.rope_inv_freq(64, 5e5), rtol=1e-15)
+
+
+def test_llama3_bands_for_llama32_shapes():
+    # D = 64, theta = 5e5: wavelength 2 pi 5e5^(i/32) is below 8192/4 = 2048
+    # for i <= 14 (1956 at i = 14), above 8192/1 for i >= 18 (10081 at i =
+    # 18), and in between for i = 15, 16, 17 (2949 .. 6692)
+    f0 = oracle.rope_inv_freq(64, 5e5)
+    f = oracle.rope_llama3_inv_freq(64, 5e5, **LLAMA32)
+    assert np.array_equal(f[:15], f0[:15])
+    np.testing.assert_allclose(f[18:], f0[18:] / 32, rtol=1e-15)
+    mid = f[15:18] / f0[15:18]
+    assert np.all(mid > 1 / 32) and np.all(mid < 1)
+    # the kept share falls as the wavelength grows
+    assert np.all(np.diff(mid) < 0)
+
+
+def test_llama3_blend_endpoints_and_midpoint():
+    # pick L so that dimension i sits exactly on a band edge or halfway: the
+    # blend must meet the unscaled frequency at L/lambda = high, the divided
+    # one at L/lambda = low, and their mean halfway between
+    D, theta, factor, lo, hi = 32, 1e4, 8.0, 1.0, 4.0
+    f0 = oracle.rope_inv_freq(D, theta)
+    i = 9
+    lam = 2 * math.pi / f0[i]
+    for L, want in ((hi * lam, f0[i]), (lo * lam, f0[i] / factor),
+                    ((lo + hi) / 2 * lam, 0.5 * (f0[i] + f0[i] / factor))):
+        f = oracle.rope_llama3_inv_freq(D, theta, factor, lo, hi, L)
+        assert math.isclose(f[i], want, rel_tol=1e-12), (L, f[i], want)
+
+
+def test_llama3_rejects_bad_bands():
+    with pytest.raises(ValueError):
+        oracle.rope_llama3_inv_freq(64, 5e5, 32.0, 4.0, 4.0, 8192.0)
+    with pytest.raises(ValueError):
+        oracle.rope_llama3_inv_freq(63, 5e5, 32.0, 1.0, 4.0, 8192.0)
+
+
 # ------------------------------------------------- RMSNorm with residual add
 
 def test_rmsnorm_add_reduces_to_rmsnorm():
