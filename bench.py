@@ -94,9 +94,9 @@ KERNEL_SOURCES = {"rmsnorm_fwd": ("rmsnorm_fwd.cu",),
                   "qk_rope_fwd": ("qk_rope.cu",), "qk_rope_bwd": ("qk_rope.cu",),
                   "rmsnorm_add_fwd": ("rmsnorm_fwd.cu",),
                   "rmsnorm_add_bwd": ("rmsnorm_add_bwd.cu", "rmsnorm_bwd.cuh"),
-                  "swiglu_bwd_h": ("swiglu.cu",)}
+                  "swiglu_bwd_h": ("swiglu.cu",), "qk_rope_freq_fwd": ("qk_rope.cu",)}
 # widened ops timed beside the step (not part of it), with their launches
-EXT_OPS = {"rmsnorm_add_fwd": 1, "rmsnorm_add_bwd": 2, "swiglu_bwd_h": 1}
+EXT_OPS = {"rmsnorm_add_fwd": 1, "rmsnorm_add_bwd": 2, "swiglu_bwd_h": 1, "qk_rope_freq_fwd": 1}
 
 
 def kernel_source_hash(op: str) -> str:
@@ -526,6 +526,7 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
     rstd = torch.empty((T,), dtype=torch.float32, device=dev)
     dx = torch.empty((T, H), dtype=dt, device=dev)
     dw = torch.empty((H,), dtype=torch.float32, device=dev)
+    llama3 = ftk.rope_llama3_inv_freq(wl.D, wl.theta, 32.0, 1.0, 4.0, 8192.0)
     ops = {
         "rmsnorm_add_fwd": lambda: ftk.rmsnorm_add_fwd(i["x"], res, i["w"], wl.eps, h=h, y=y,
                                                        rstd=rstd),
@@ -533,6 +534,8 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
                                                        dx=dx, dw=dw, workspace=batch.ws),
         "swiglu_bwd_h": lambda: ftk.swiglu_bwd_h(i["dh"], i["g"], i["u"], dg=o["dg"],
                                                  du=o["du"], h=o["h"]),
+        # the Llama-3.2 rope_scaling table (factor 32, low 1, high 4, 8192)
+        "qk_rope_freq_fwd": lambda: ftk.qk_rope_freq_fwd(i["q"], i["k"], i["cu"], llama3),
     }
     assert set(ops) == set(EXT_OPS)
     for op in ops.values():  # warm-up (and the first, allocating, launch)

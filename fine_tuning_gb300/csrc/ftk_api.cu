@@ -402,14 +402,21 @@ FTK_API ftk_status ftk_swiglu_bwd_h(const void *dh, int64_t ld_dh, const void *g
 
 // ------------------------------------------------------------------ QK-RoPE
 
+// inv_freq (HOST, nullable) replaces theta's table when given.
 static ftk_status qk_rope(void *q, int64_t ld_q, void *k, int64_t ld_k, const int32_t *cu,
                           int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D, double theta,
-                          ftk_dtype dtype, ftk_stream_t stream, bool backward) {
+                          const double *inv_freq, ftk_dtype dtype, ftk_stream_t stream,
+                          bool backward) {
   if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
   if (T < 0 || B < 0 || Hq < 0 || Hkv < 0 || Hq + Hkv < 1 || D < 2 || D % 2 != 0 ||
       D / 2 > ftk::kRopeMaxHalf || T >= (int64_t(1) << 31))
     return FTK_ERR_SHAPE;
-  if (!(theta > 0.0)) return FTK_ERR_SHAPE;
+  if (inv_freq) {
+    for (int32_t i = 0; i < D / 2; ++i)
+      if (!(inv_freq[i] >= 0.0 && inv_freq[i] <= 1.0)) return FTK_ERR_SHAPE;  // NaN fails too
+  } else if (!(theta > 0.0)) {
+    return FTK_ERR_SHAPE;
+  }
   if ((Hq > 0 && ld_q < (int64_t)Hq * D) || (Hkv > 0 && ld_k < (int64_t)Hkv * D))
     return FTK_ERR_SHAPE;
   if (T == 0) return FTK_OK;
@@ -433,6 +440,7 @@ static ftk_status qk_rope(void *q, int64_t ld_q, void *k, int64_t ld_k, const in
   cudaError_t e = device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   ftk::RopeArgs a{q, ld_q, k, ld_k, cu, B, T, Hq, Hkv, D, theta, backward};
+  a.inv_freq = inv_freq;
   return finish(ftk::launch_qk_rope(dt, vec, wide, a, dev, (cudaStream_t)stream));
 }
 
@@ -440,14 +448,36 @@ FTK_API ftk_status ftk_qk_rope_fwd(void *q, int64_t ld_q, void *k, int64_t ld_k,
                                    const int32_t *cu_seqlens, int32_t B, int64_t T, int32_t Hq,
                                    int32_t Hkv, int32_t D, double theta, ftk_dtype dtype,
                                    ftk_stream_t stream) {
-  return qk_rope(q, ld_q, k, ld_k, cu_seqlens, B, T, Hq, Hkv, D, theta, dtype, stream, false);
+  return qk_rope(q, ld_q, k, ld_k, cu_seqlens, B, T, Hq, Hkv, D, theta, nullptr, dtype, stream,
+                 false);
 }
 
 FTK_API ftk_status ftk_qk_rope_bwd(void *dq, int64_t ld_q, void *dk, int64_t ld_k,
                                    const int32_t *cu_seqlens, int32_t B, int64_t T, int32_t Hq,
                                    int32_t Hkv, int32_t D, double theta, ftk_dtype dtype,
                                    ftk_stream_t stream) {
-  return qk_rope(dq, ld_q, dk, ld_k, cu_seqlens, B, T, Hq, Hkv, D, theta, dtype, stream, true);
+  return qk_rope(dq, ld_q, dk, ld_k, cu_seqlens, B, T, Hq, Hkv, D, theta, nullptr, dtype, stream,
+                 true);
+}
+
+FTK_API ftk_status ftk_qk_rope_freq_fwd(void *q, int64_t ld_q, void *k, int64_t ld_k,
+                                        const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                        int32_t Hq, int32_t Hkv, int32_t D,
+                                        const double *inv_freq, ftk_dtype dtype,
+                                        ftk_stream_t stream) {
+  if (!inv_freq) return FTK_ERR_NULL;
+  return qk_rope(q, ld_q, k, ld_k, cu_seqlens, B, T, Hq, Hkv, D, 0.0, inv_freq, dtype, stream,
+                 false);
+}
+
+FTK_API ftk_status ftk_qk_rope_freq_bwd(void *dq, int64_t ld_q, void *dk, int64_t ld_k,
+                                        const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                        int32_t Hq, int32_t Hkv, int32_t D,
+                                        const double *inv_freq, ftk_dtype dtype,
+                                        ftk_stream_t stream) {
+  if (!inv_freq) return FTK_ERR_NULL;
+  return qk_rope(dq, ld_q, dk, ld_k, cu_seqlens, B, T, Hq, Hkv, D, 0.0, inv_freq, dtype, stream,
+                 true);
 }
 
 }  // extern "C"

@@ -164,6 +164,7 @@ struct RopeArgs {
   int32_t Hq, Hkv, D;
   double theta;
   bool backward;
+  const double *inv_freq = nullptr;  // HOST [D/2]: replaces theta^(-2i/D) when set
 };
 cudaError_t launch_qk_rope(DType dt, bool vec, bool wide, const RopeArgs &a,
                            const DeviceInfo &dev, cudaStream_t s);

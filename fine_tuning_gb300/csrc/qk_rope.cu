@@ -13,7 +13,10 @@
 // phi_i = p * theta^(-2i/D) and every head vector v of Q and K becomes
 //   v[i] <- v[i] cos phi_i - v[i+D/2] sin phi_i
 //   v[i+D/2] <- v[i+D/2] cos phi_i + v[i] sin phi_i
-// (backward: phi -> -phi, the transpose).
+// (backward: phi -> -phi, the transpose).  A caller may pass its own table
+// of inverse frequencies instead of theta^(-2i/D) (a scaled RoPE such as
+// the llama3 rule; the table is built on the host, rope_freqs.cu); the
+// kernels only ever see f_i = inv_freq_i / 2pi.
 //
 // A CTA owns TOK consecutive tokens.  Per token, TPT = NV * S threads: NV
 // packet slots across one half of a head times S head slots; the thread with
@@ -580,12 +583,15 @@ cudaError_t rope_typed(bool vec, const RopeArgs &a, const RopeFreqs &fr, const D
 
 cudaError_t launch_qk_rope(DType dt, bool vec, bool wide, const RopeArgs &a,
                            const DeviceInfo &dev, cudaStream_t s) {
-  // f_i = theta^(-2i/D) / (2 pi) in double, split into two floats.
+  // f_i = inv_freq_i / (2 pi) in double, split into two floats; inv_freq_i
+  // is theta^(-2i/D), or the caller's (scaled) table.
   RopeFreqs fr;
   const int half = a.D / 2;
   for (int i = 0; i < kRopeMaxHalf; ++i) {
     if (i < half) {
-      const double f = std::pow(a.theta, -2.0 * (double)i / (double)a.D) / 6.283185307179586476925;
+      const double inv = a.inv_freq ? a.inv_freq[i]
+                                    : std::pow(a.theta, -2.0 * (double)i / (double)a.D);
+      const double f = inv / 6.283185307179586476925;
       const float hi = (float)f;
       fr.hi[i] = hi;
       fr.lo[i] = (float)(f - (double)hi);

@@ -12,6 +12,7 @@ import ctypes
 import os
 from typing import Optional, Tuple
 
+import numpy as np
 import torch
 
 from .build import LIB as _LIB_PATH
@@ -63,6 +64,11 @@ def library() -> ctypes.CDLL:
                                   vp]),
         "ftk_qk_rope_fwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, dt, vp]),
         "ftk_qk_rope_bwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, dt, vp]),
+        "ftk_qk_rope_freq_fwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, vp, dt,
+                                      vp]),
+        "ftk_qk_rope_freq_bwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, vp, dt,
+                                      vp]),
+        "ftk_rope_llama3_inv_freq": (st, [i32, f64, f64, f64, f64, f64, vp]),
         "ftk_bfd_pack": (st, [vp, i64, i32, vp, vp, vp, vp]),
         "ftk_device_status": (st, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
         "ftk_selftest_wait_timeout": (st, [i64, vp]),
@@ -301,7 +307,7 @@ def _heads(t: Optional[torch.Tensor], name: str):
     return (t.stride(0) if T > 1 else nh * D), nh, D
 
 
-def _rope(name, q, k, cu_seqlens, theta):
+def _rope(name, q, k, cu_seqlens, theta, inv_freq=None):
     _cuda(q, k, cu_seqlens)
     ldq, Hq, Dq = _heads(q, "q")
     ldk, Hkv, Dk = _heads(k, "k")
@@ -311,8 +317,15 @@ def _rope(name, q, k, cu_seqlens, theta):
     ref = q if q is not None else k
     if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
         raise ValueError("cu_seqlens must be a contiguous int32 [B+1] device tensor")
+    if inv_freq is None:
+        last = float(theta)
+    else:
+        table = np.ascontiguousarray(np.asarray(inv_freq, dtype=np.float64))
+        if table.shape != (D // 2,):
+            raise ValueError("inv_freq must hold D/2 values")
+        last = table.ctypes.data_as(ctypes.c_void_p)
     _call(name, _ptr(q), ldq, _ptr(k), ldk, _ptr(cu_seqlens), cu_seqlens.numel() - 1,
-          ref.shape[0], Hq, Hkv, D, float(theta), _code(ref), _stream(ref))
+          ref.shape[0], Hq, Hkv, D, last, _code(ref), _stream(ref))
     return q, k
 
 
@@ -324,6 +337,26 @@ def qk_rope_fwd(q, k, cu_seqlens, theta):
 def qk_rope_bwd(dq, dk, cu_seqlens, theta):
     """Backward of qk_rope_fwd: rotate dq, dk by -phi IN PLACE; returns (dq, dk)."""
     return _rope("ftk_qk_rope_bwd", dq, dk, cu_seqlens, theta)
+
+
+def qk_rope_freq_fwd(q, k, cu_seqlens, inv_freq):
+    """qk_rope_fwd with a host table of D/2 inverse frequencies (a scaled RoPE)."""
+    return _rope("ftk_qk_rope_freq_fwd", q, k, cu_seqlens, None, inv_freq)
+
+
+def qk_rope_freq_bwd(dq, dk, cu_seqlens, inv_freq):
+    """Backward of qk_rope_freq_fwd, in place."""
+    return _rope("ftk_qk_rope_freq_bwd", dq, dk, cu_seqlens, None, inv_freq)
+
+
+def rope_llama3_inv_freq(D: int, theta: float, factor: float, low_freq_factor: float,
+                         high_freq_factor: float, original_max_position: float) -> np.ndarray:
+    """The llama3-scaled inverse frequencies (host; float64 [D/2])."""
+    out = np.empty(D // 2, dtype=np.float64)
+    _call("ftk_rope_llama3_inv_freq", int(D), float(theta), float(factor), float(low_freq_factor),
+          float(high_freq_factor), float(original_max_position),
+          out.ctypes.data_as(ctypes.c_void_p))
+    return out
 
 
 # ---------------------------------------------------------------- packing

@@ -192,6 +192,8 @@ def ideal_bytes(wl: Workload) -> Dict[str, int]:
         "rmsnorm_add_bwd": 4 * e * T * H + 4 * T + e * H + 4 * H,
         # SwiGLU backward that re-emits h: dh, g, u in; dg, du, h out
         "swiglu_bwd_h": 6 * e * Ts * I,
+        # RoPE with a caller's (llama3-scaled) frequency table: same bytes
+        "qk_rope_freq_fwd": rope,
     }
 
 
@@ -201,4 +203,5 @@ def tokens_per_call(wl: Workload) -> Dict[str, int]:
         "swiglu_fwd": wl.T_swiglu, "swiglu_bwd": wl.T_swiglu,
         "qk_rope_fwd": wl.T, "qk_rope_bwd": wl.T,
         "rmsnorm_add_fwd": wl.T, "rmsnorm_add_bwd": wl.T, "swiglu_bwd_h": wl.T_swiglu,
+        "qk_rope_freq_fwd": wl.T,
     }

@@ -231,6 +231,42 @@ FTK_API ftk_status ftk_qk_rope_bwd(void *dq, int64_t ld_q, void *dk, int64_t ld_
                            int32_t Hq, int32_t Hkv, int32_t D, double theta,
                            ftk_dtype dtype, ftk_stream_t stream);
 
+/* The rotation above with the caller's inverse frequencies in place of
+ * theta^(-2i/D):  phi_i = p * inv_freq[i].  Any scaled RoPE whose angle is
+ * position times a per-dimension frequency (linear, "llama3", NTK-style)
+ * comes down to such a table; the pages apply no scaling, this is the
+ * library's variant of the same kernels.  inv_freq: HOST double [D/2], read
+ * during the call only (it may be freed on return); each entry must lie in
+ * [0, 1] (every such rule only slows theta's frequencies, and theta^0 = 1),
+ * else FTK_ERR_SHAPE.  The angle keeps the same ~1e-7 rad accuracy.  Other
+ * arguments and rules are ftk_qk_rope_fwd's / ftk_qk_rope_bwd's. */
+FTK_API ftk_status ftk_qk_rope_freq_fwd(void *q, int64_t ld_q, void *k, int64_t ld_k,
+                                        const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                        int32_t Hq, int32_t Hkv, int32_t D,
+                                        const double *inv_freq, ftk_dtype dtype,
+                                        ftk_stream_t stream);
+FTK_API ftk_status ftk_qk_rope_freq_bwd(void *dq, int64_t ld_q, void *dk, int64_t ld_k,
+                                        const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                        int32_t Hq, int32_t Hkv, int32_t D,
+                                        const double *inv_freq, ftk_dtype dtype,
+                                        ftk_stream_t stream);
+
+/* The "llama3" scaled table (the rule published with Llama 3.1, used by the
+ * Llama-3.2 models) for ftk_qk_rope_freq_*.  Host code; inv_freq: HOST
+ * double [D/2], written.  With base_i = theta^(-2i/D), wavelength
+ * lambda_i = 2 pi / base_i and L = original_max_position:
+ *   lambda_i < L / high_freq_factor:  inv_freq[i] = base_i
+ *   lambda_i > L / low_freq_factor:   inv_freq[i] = base_i / factor
+ *   otherwise, s = (L / lambda_i - low_freq_factor)
+ *                  / (high_freq_factor - low_freq_factor):
+ *                                     inv_freq[i] = s base_i + (1 - s) base_i / factor
+ * Needs D even in [2, 512], theta > 1, factor >= 1, 0 < low_freq_factor <
+ * high_freq_factor, L > 0 (all finite), else FTK_ERR_SHAPE.  Llama-3.2:
+ * theta 5e5, factor 32, low 1, high 4, L 8192. */
+FTK_API ftk_status ftk_rope_llama3_inv_freq(int32_t D, double theta, double factor,
+                                            double low_freq_factor, double high_freq_factor,
+                                            double original_max_position, double *inv_freq);
+
 /* -------------------------------------------------------------- packing */
 
 /* Best-Fit-Decreasing packing of n sequences into bins of `capacity` tokens

@@ -201,6 +201,42 @@ def test_qk_rope_argument_errors(lib):
     assert call(dt=5) == DTYPE
 
 
+def test_qk_rope_freq_argument_errors(lib):
+    import numpy as np
+    f = lib.ftk_qk_rope_freq_fwd
+    q, k, cu = A, A + (1 << 22), A + (1 << 23)
+    good = np.full(8, 0.5)
+    bad_hi, bad_nan = np.full(8, 0.5), np.full(8, 0.5)
+    bad_hi[3], bad_nan[5] = 1.5, np.nan
+    ptr = lambda a: a.ctypes.data
+    base = [q, 4 * 16, k, 2 * 16, cu, 4, 64, 4, 2, 16]
+    assert f(*(base[:6] + [0] + base[7:]), ptr(good), F32, None) == OK       # T = 0
+    assert f(*base, None, F32, None) == NULL
+    assert f(*base, ptr(bad_hi), F32, None) == SHAPE
+    assert f(*base, ptr(bad_nan), F32, None) == SHAPE
+    assert lib.ftk_qk_rope_freq_bwd(*base, ptr(good), 7, None) == DTYPE
+
+
+def test_llama3_table_host(lib):
+    # host code: runs here, against the oracle's table
+    import numpy as np
+    import oracle
+    from fine_tuning_gb300 import ftk
+    for D, theta, fac, lo, hi, L in ((64, 5e5, 32.0, 1.0, 4.0, 8192.0),
+                                     (128, 5e5, 8.0, 1.0, 4.0, 8192.0),
+                                     (128, 1e6, 16.0, 2.0, 5.0, 4096.0),
+                                     (32, 1e4, 1.0, 1.0, 4.0, 2048.0)):
+        got = ftk.rope_llama3_inv_freq(D, theta, fac, lo, hi, L)
+        ref = oracle.rope_llama3_inv_freq(D, theta, fac, lo, hi, L)
+        np.testing.assert_allclose(got, ref, rtol=1e-14, atol=0)
+    out = np.empty(32)
+    p = out.ctypes.data
+    assert lib.ftk_rope_llama3_inv_freq(63, 5e5, 32.0, 1.0, 4.0, 8192.0, p) == SHAPE
+    assert lib.ftk_rope_llama3_inv_freq(64, 5e5, 32.0, 4.0, 4.0, 8192.0, p) == SHAPE
+    assert lib.ftk_rope_llama3_inv_freq(64, 5e5, 0.5, 1.0, 4.0, 8192.0, p) == SHAPE
+    assert lib.ftk_rope_llama3_inv_freq(64, 5e5, 32.0, 1.0, 4.0, 8192.0, None) == NULL
+
+
 def test_workspace_query_rejects_bad_arguments(lib):
     assert lib.ftk_rmsnorm_bwd_workspace_bytes(0, 64, BF16) == 0
     assert lib.ftk_rmsnorm_bwd_workspace_bytes(16, 0, BF16) == 0

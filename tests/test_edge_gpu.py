@@ -268,6 +268,41 @@ def test_rope_shapes(dtype, lens, Hq, Hkv, D):
         assert_close("k", kg.t, kr, ks, dtype=code(dtype))
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("lens,Hq,Hkv,D", [
+    ((5, 17, 0, 32, 10), 4, 2, 16),
+    ((300, 1, 77), 14, 2, 64),
+    ((33, 12), 3, 1, 18),                  # element-wise path
+    ((7000,), 8, 2, 128),                  # staged path
+])
+def test_rope_freq_table(dtype, lens, Hq, Hkv, D):
+    """An arbitrary table in [0, 1] (both ends included) against the oracle;
+    an all-zero table leaves q and k bit for bit."""
+    rng = np.random.default_rng(D + Hq)
+    f = rng.random(D // 2)
+    f[0], f[-1] = 1.0, 0.0
+    cu, T, q, k = rope_case(lens, Hq, Hkv, D, 1e4, dtype, seed=50)
+    cu_d = torch.as_tensor(cu, device=DEV)
+    qg, kg = Guarded((T, Hq, D), dtype, fill=q), Guarded((T, Hkv, D), dtype, fill=k)
+    ftk.qk_rope_freq_fwd(qg.t, kg.t, cu_d, f)
+    torch.cuda.synchronize()
+    qg.check()
+    kg.check()
+    qr, kr, qs, ks = oracle.qk_rope_freq(q.cpu(), k.cpu(), cu, f, +1, scales=True)
+    assert_close("q", qg.t, qr, qs, dtype=code(dtype))
+    assert_close("k", kg.t, kr, ks, dtype=code(dtype))
+    # the backward on the forward's output, against the oracle's backward
+    q1, k1 = qg.t.cpu(), kg.t.cpu()
+    ftk.qk_rope_freq_bwd(qg.t, kg.t, cu_d, f)
+    q2, k2 = q.clone(), k.clone()
+    ftk.qk_rope_freq_fwd(q2, k2, cu_d, np.zeros(D // 2))
+    torch.cuda.synchronize()
+    dqr, dkr, dqs, dks = oracle.qk_rope_freq(q1, k1, cu, f, -1, scales=True)
+    assert_close("dq", qg.t, dqr, dqs, dtype=code(dtype))
+    assert_close("dk", kg.t, dkr, dks, dtype=code(dtype))
+    assert torch.equal(q2, q) and torch.equal(k2, k)
+
+
 def test_rope_fused_qkv_buffer():
     lens, Hq, Hkv, D, theta = (50, 13, 61), 16, 4, 128, 5e5
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)

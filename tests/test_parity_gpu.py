@@ -141,7 +141,13 @@ def test_swiglu_524k_slice_sampled():
 
 # ------------------------------------------------------------------ QK-RoPE
 
-def check_rope(wl, n_tok=None):
+LLAMA3 = dict(factor=32.0, low_freq_factor=1.0, high_freq_factor=4.0,
+              original_max_position=8192.0)  # the Llama-3.2 rope_scaling
+
+
+def check_rope(wl, n_tok=None, llama3=False):
+    """llama3=True rotates with the llama3-scaled table (the library's own
+    table on the GPU, the oracle's table on the CPU)."""
     lens = W.draw_lengths(wl)
     cu = W.cu_seqlens_from_lengths(lens)
     cu_d = torch.as_tensor(cu, device=DEV)
@@ -151,11 +157,20 @@ def check_rope(wl, n_tok=None):
         wl.T, n_tok, extra=starts[:64] + [s - 1 for s in starts[1:64]])
     ti = torch.as_tensor(tok, device=DEV)
     q0, k0, dq0, dk0 = (d[n][ti].cpu() for n in ("q", "k", "dq", "dk"))
-    ftk.qk_rope_fwd(d["q"], d["k"], cu_d, wl.theta)
-    ftk.qk_rope_bwd(d["dq"], d["dk"], cu_d, wl.theta)
-    torch.cuda.synchronize()
-    qr, kr, qs, ks = oracle.qk_rope(q0, k0, cu, wl.theta, +1, tok=tok, scales=True)
-    dqr, dkr, dqs, dks = oracle.qk_rope(dq0, dk0, cu, wl.theta, -1, tok=tok, scales=True)
+    if llama3:
+        f_gpu = ftk.rope_llama3_inv_freq(wl.D, wl.theta, **LLAMA3)
+        f_ref = oracle.rope_llama3_inv_freq(wl.D, wl.theta, **LLAMA3)
+        ftk.qk_rope_freq_fwd(d["q"], d["k"], cu_d, f_gpu)
+        ftk.qk_rope_freq_bwd(d["dq"], d["dk"], cu_d, f_gpu)
+        torch.cuda.synchronize()
+        qr, kr, qs, ks = oracle.qk_rope_freq(q0, k0, cu, f_ref, +1, tok=tok, scales=True)
+        dqr, dkr, dqs, dks = oracle.qk_rope_freq(dq0, dk0, cu, f_ref, -1, tok=tok, scales=True)
+    else:
+        ftk.qk_rope_fwd(d["q"], d["k"], cu_d, wl.theta)
+        ftk.qk_rope_bwd(d["dq"], d["dk"], cu_d, wl.theta)
+        torch.cuda.synchronize()
+        qr, kr, qs, ks = oracle.qk_rope(q0, k0, cu, wl.theta, +1, tok=tok, scales=True)
+        dqr, dkr, dqs, dks = oracle.qk_rope(dq0, dk0, cu, wl.theta, -1, tok=tok, scales=True)
     assert_close("q", d["q"][ti], qr, qs, dtype=dt(wl))
     assert_close("k", d["k"][ti], kr, ks, dtype=dt(wl))
     assert_close("dq", d["dq"][ti], dqr, dqs, dtype=dt(wl))
@@ -170,6 +185,17 @@ def test_rope_small_full(name):
 @pytest.mark.parametrize("name", LARGE)
 def test_rope_large_sampled(name):
     check_rope(W.WORKLOADS[name], n_tok=4096)
+
+
+@pytest.mark.parametrize("name", ("tiny_f32", "qwen2.5-0.5b", "llama-3.2-1b"))
+def test_rope_llama3_scaled(name):
+    wl = W.WORKLOADS[name]
+    check_rope(wl, n_tok=None if wl.T <= 16384 else 4096, llama3=True)
+
+
+@pytest.mark.slow
+def test_rope_llama3_scaled_524k_sampled():
+    check_rope(W.WORKLOADS["qwen3-32b-524k"], n_tok=2048, llama3=True)
 
 
 @pytest.mark.slow
