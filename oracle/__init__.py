@@ -183,6 +183,47 @@ def qk_rope_freq(q, k, cu_seqlens, inv_freq, sign=+1, tok=None, scales=False):
     return (qo, ko, qs, ks) if scales else (qo, ko)
 
 
+def qk_norm_rope_fwd(q, k, wq, wk, eps, cu_seqlens, inv_freq, tok=None, scales=False):
+    """Per-head RMSNorm of q [n,Hq,D] and k [n,Hkv,D] (weights wq, wk [D]),
+    then the rotation with inv_freq [D/2]: the two pinned steps above run
+    one after the other, in double, with no rounding between them.
+    Returns (q_out, k_out, rstd_q [n,Hq], rstd_k [n,Hkv]) and, with
+    scales=True, the rotation's condition scales of q_out and k_out."""
+    q, k = _f64(q), _f64(k)
+    n, Hq, D = q.shape
+    Hkv = k.shape[1]
+    nq, rq = rmsnorm_fwd(q.reshape(n * Hq, D), wq, eps)
+    nk, rk = rmsnorm_fwd(k.reshape(n * Hkv, D), wk, eps)
+    out = qk_rope_freq(nq.reshape(n, Hq, D), nk.reshape(n, Hkv, D), cu_seqlens, inv_freq, +1,
+                       tok=tok, scales=scales)
+    rq, rk = rq.reshape(n, Hq), rk.reshape(n, Hkv)
+    if scales:
+        return out[0], out[1], rq, rk, out[2], out[3]
+    return out[0], out[1], rq, rk
+
+
+def qk_norm_rope_bwd(dq, dk, q, k, wq, wk, eps, cu_seqlens, inv_freq, tok=None, scales=False):
+    """Gradient of qk_norm_rope_fwd: the rotation's transpose takes dq, dk
+    back to the normalised vectors, then the RMSNorm backward (per head
+    vector, rows of D) gives the gradients of the pre-norm q, k and of wq,
+    wk.  Returns (dq_in, dk_in, dwq, dwk) and, with scales=True, their
+    condition scales: the rotation's scale of the intermediate gradient
+    carried through the (linear in |dy|) RMSNorm scale."""
+    q, k = _f64(q), _f64(k)
+    n, Hq, D = q.shape
+    Hkv = k.shape[1]
+    dnq, dnk, sq, sk = qk_rope_freq(dq, dk, cu_seqlens, inv_freq, -1, tok=tok, scales=True)
+    dvq, dwq = rmsnorm_bwd(dnq.reshape(n * Hq, D), q.reshape(n * Hq, D), wq, eps)
+    dvk, dwk = rmsnorm_bwd(dnk.reshape(n * Hkv, D), k.reshape(n * Hkv, D), wk, eps)
+    dvq, dvk = dvq.reshape(n, Hq, D), dvk.reshape(n, Hkv, D)
+    if not scales:
+        return dvq, dvk, dwq, dwk
+    _, _, svq, swq = rmsnorm_bwd(sq.reshape(n * Hq, D), q.reshape(n * Hq, D), wq, eps, scales=True)
+    _, _, svk, swk = rmsnorm_bwd(sk.reshape(n * Hkv, D), k.reshape(n * Hkv, D), wk, eps,
+                                 scales=True)
+    return dvq, dvk, dwq, dwk, svq.reshape(n, Hq, D), svk.reshape(n, Hkv, D), swq, swk
+
+
 def rope_inv_freq(D, theta):
     """theta^(-2i/D), i < D/2."""
     out = np.empty(D // 2)

@@ -385,6 +385,80 @@ def test_llama3_rejects_bad_bands():
         oracle.rope_llama3_inv_freq(63, 5e5, 32.0, 1.0, 4.0, 8192.0)
 
 
+# ------------------------------------------- per-head QK-RMSNorm, then RoPE
+
+def test_qk_norm_rope_unit_rms_inputs_reduce_to_rope():
+    # entries of +-1 have mean square 1: with w = 1 and eps = 0 the norm is
+    # the identity, so the op is the rotation alone
+    cu, q, k = _packed_case(D=16)
+    q, k = np.sign(q), np.sign(k)
+    f = oracle.rope_inv_freq(16, 1e4)
+    qo, ko, rq, rk = oracle.qk_norm_rope_fwd(q, k, np.ones(16), np.ones(16), 0.0, cu, f)
+    qr, kr = oracle.qk_rope_freq(q, k, cu, f)
+    np.testing.assert_allclose(qo, qr, atol=1e-14)
+    np.testing.assert_allclose(ko, kr, atol=1e-14)
+    assert np.allclose(rq, 1.0) and np.allclose(rk, 1.0)
+
+
+def test_qk_norm_rope_head_norms():
+    # rotation keeps lengths: with w = 1 each output head vector has squared
+    # length D * ms / (ms + eps), ms its input's mean square
+    cu, q, k = _packed_case(D=32, Hq=3, Hkv=1)
+    eps = 0.25
+    f = oracle.rope_inv_freq(32, 1e6)
+    qo, ko, _, _ = oracle.qk_norm_rope_fwd(q, k, np.ones(32), np.ones(32), eps, cu, f)
+    for v, o in ((q, qo), (k, ko)):
+        ms = (v ** 2).mean(axis=-1)
+        np.testing.assert_allclose((o ** 2).sum(axis=-1), 32 * ms / (ms + eps), rtol=1e-12)
+
+
+def test_qk_norm_rope_hand_example_d2():
+    # v = (3, 4), w = (1, 2), eps = 0: ms = 12.5, r = 12.5^-1/2, normalised
+    # n = (3r, 8r); at p = 0 it is the output, at p = 2 with f = 1 it is
+    # turned by 2 rad: (3r + 8r i) e^{2i}
+    r = 12.5 ** -0.5
+    v = np.array([[[3.0, 4.0]]])
+    k0 = np.zeros((1, 0, 2))
+    for p, z in ((0, complex(3 * r, 8 * r)), (2, complex(3 * r, 8 * r) * cmath.exp(2j))):
+        qo, _, rq, _ = oracle.qk_norm_rope_fwd(v, k0, [1.0, 2.0], [1.0, 2.0], 0.0, [0, p + 1],
+                                               [1.0], tok=[p])
+        np.testing.assert_allclose(qo[0, 0], [z.real, z.imag], atol=1e-14)
+        assert math.isclose(rq[0, 0], r, rel_tol=1e-15)
+
+
+def test_qk_norm_rope_bwd_matches_finite_differences():
+    cu, q, k = _packed_case(D=8, Hq=2, Hkv=1, lens=(3, 0, 4))
+    wq, wk = 1 + 0.1 * RNG.standard_normal(8), 1 + 0.1 * RNG.standard_normal(8)
+    f = oracle.rope_llama3_inv_freq(8, 1e4, 4.0, 1.0, 4.0, 16.0)
+    eps = 1e-3
+    dq, dk = RNG.standard_normal(q.shape), RNG.standard_normal(k.shape)
+
+    def loss(q_, k_, wq_, wk_):
+        qo, ko, _, _ = oracle.qk_norm_rope_fwd(q_, k_, wq_, wk_, eps, cu, f)
+        return float((dq * qo).sum() + (dk * ko).sum())
+
+    gq, gk, gwq, gwk = oracle.qk_norm_rope_bwd(dq, dk, q, k, wq, wk, eps, cu, f)
+    h = 1e-6
+    for arr, g in ((q, gq), (k, gk), (wq, gwq), (wk, gwk)):
+        e = RNG.standard_normal(arr.shape)
+        args_p = [q, k, wq, wk]
+        args_m = [q, k, wq, wk]
+        i = [id(q), id(k), id(wq), id(wk)].index(id(arr))
+        args_p[i], args_m[i] = arr + h * e, arr - h * e
+        fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert math.isclose(fd, float((g * e).sum()), rel_tol=1e-6, abs_tol=1e-8)
+
+
+def test_qk_norm_rope_bwd_scales_bound_values():
+    cu, q, k = _packed_case(D=16)
+    w = 1 + 0.1 * RNG.standard_normal(16)
+    f = oracle.rope_inv_freq(16, 1e4)
+    dq, dk = RNG.standard_normal(q.shape), RNG.standard_normal(k.shape)
+    out = oracle.qk_norm_rope_bwd(dq, dk, q, k, w, w, 1e-6, cu, f, scales=True)
+    for v, sc in zip(out[:4], out[4:]):
+        assert np.all(np.abs(v) <= sc * (1 + 1e-12))
+
+
 # ------------------------------------------------- RMSNorm with residual add
 
 def test_rmsnorm_add_reduces_to_rmsnorm():
