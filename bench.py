@@ -88,15 +88,19 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+_ROPE = ("qk_rope.cu", "rope_common.cuh")
 KERNEL_SOURCES = {"rmsnorm_fwd": ("rmsnorm_fwd.cu",),
-                  "rmsnorm_bwd": ("rmsnorm_bwd.cu", "rmsnorm_bwd.cuh"),
+                  "rmsnorm_bwd": ("rmsnorm_bwd.cu", "rmsnorm_bwd.cuh", "dw_reduce.cuh"),
                   "swiglu_fwd": ("swiglu.cu",), "swiglu_bwd": ("swiglu.cu",),
-                  "qk_rope_fwd": ("qk_rope.cu",), "qk_rope_bwd": ("qk_rope.cu",),
+                  "qk_rope_fwd": _ROPE, "qk_rope_bwd": _ROPE,
                   "rmsnorm_add_fwd": ("rmsnorm_fwd.cu",),
-                  "rmsnorm_add_bwd": ("rmsnorm_add_bwd.cu", "rmsnorm_bwd.cuh"),
-                  "swiglu_bwd_h": ("swiglu.cu",), "qk_rope_freq_fwd": ("qk_rope.cu",)}
+                  "rmsnorm_add_bwd": ("rmsnorm_add_bwd.cu", "rmsnorm_bwd.cuh", "dw_reduce.cuh"),
+                  "swiglu_bwd_h": ("swiglu.cu",), "qk_rope_freq_fwd": _ROPE,
+                  "qk_norm_rope_fwd": ("qk_norm_rope.cu", "rope_common.cuh", "dw_reduce.cuh"),
+                  "qk_norm_rope_bwd": ("qk_norm_rope.cu", "rope_common.cuh", "dw_reduce.cuh")}
 # widened ops timed beside the step (not part of it), with their launches
-EXT_OPS = {"rmsnorm_add_fwd": 1, "rmsnorm_add_bwd": 2, "swiglu_bwd_h": 1, "qk_rope_freq_fwd": 1}
+EXT_OPS = {"rmsnorm_add_fwd": 1, "rmsnorm_add_bwd": 2, "swiglu_bwd_h": 1, "qk_rope_freq_fwd": 1,
+           "qk_norm_rope_fwd": 1, "qk_norm_rope_bwd": 3}
 
 
 def kernel_source_hash(op: str) -> str:
@@ -527,6 +531,13 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
     dx = torch.empty((T, H), dtype=dt, device=dev)
     dw = torch.empty((H,), dtype=torch.float32, device=dev)
     llama3 = ftk.rope_llama3_inv_freq(wl.D, wl.theta, 32.0, 1.0, 4.0, 8192.0)
+    nr = W.qk_norm_rope_inputs(wl, dev, T=1)  # only the weights wq, wk are used
+    wq, wk = nr["wq"], nr["wk"]
+    qo, ko = torch.empty_like(i["q"]), torch.empty_like(i["k"])
+    rq = torch.empty((T, wl.Hq), dtype=torch.float32, device=dev)
+    rk = torch.empty((T, wl.Hkv), dtype=torch.float32, device=dev)
+    nr_bytes = max(16, ftk.qk_norm_rope_bwd_workspace_bytes(T, wl.D, dt))
+    nr_ws = torch.empty((nr_bytes + 3) // 4, dtype=torch.float32, device=dev)
     ops = {
         "rmsnorm_add_fwd": lambda: ftk.rmsnorm_add_fwd(i["x"], res, i["w"], wl.eps, h=h, y=y,
                                                        rstd=rstd),
@@ -536,6 +547,12 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
                                                  du=o["du"], h=o["h"]),
         # the Llama-3.2 rope_scaling table (factor 32, low 1, high 4, 8192)
         "qk_rope_freq_fwd": lambda: ftk.qk_rope_freq_fwd(i["q"], i["k"], i["cu"], llama3),
+        "qk_norm_rope_fwd": lambda: ftk.qk_norm_rope_fwd(i["q"], i["k"], wq, wk, i["cu"], wl.eps,
+                                                         theta=wl.theta, q_out=qo, k_out=ko,
+                                                         rstd_q=rq, rstd_k=rk),
+        "qk_norm_rope_bwd": lambda: ftk.qk_norm_rope_bwd(
+            i["dq"], i["dk"], i["q"], i["k"], wq, wk, rq, rk, i["cu"], wl.eps, theta=wl.theta,
+            dq=qo, dk=ko, workspace=nr_ws),
     }
     assert set(ops) == set(EXT_OPS)
     for op in ops.values():  # warm-up (and the first, allocating, launch)
@@ -572,7 +589,7 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
                   "launches": EXT_OPS[n]}
     out["timing"] = (f"{reps} replays of a graph [L2 flush, op] minus a graph [L2 flush], "
                      "CUDA events around each; outside the step's timed region")
-    del h, y, rstd, dx, dw, res, dres, extra
+    del h, y, rstd, dx, dw, res, dres, extra, qo, ko, rq, rk, nr_ws
     return out
 
 

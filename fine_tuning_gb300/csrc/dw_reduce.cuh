@@ -1,0 +1,55 @@
+// Second pass of the deterministic weight gradients (RMSNorm's dw, the
+// per-head QK-norm's dwq and dwk): out[j] = sum_{p < P} ws[p, j] over the
+// fp32 partial rows the first pass wrote, one per CTA, in a fixed order.
+#pragma once
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace ftk {
+
+namespace {
+
+// dw[j] = sum_{p < P} ws[p * ld + j], j < H: a CTA owns 32 columns; its 32
+// warps take the rows p = warp, warp + 32, ... and their sums are added in
+// warp order.
+constexpr int kReduceWarps = 32;
+
+__global__ void __launch_bounds__(32 * kReduceWarps)
+dw_reduce(const float *__restrict__ ws, int P, int H, int ld, float *__restrict__ dw) {
+  __shared__ float part[kReduceWarps][33];
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = blockIdx.x * 32 + lane;
+  float s = 0.f;
+  if (col < H) {
+#pragma unroll 4
+    for (int p = warp; p < P; p += kReduceWarps) s += ws[(size_t)p * ld + col];
+  }
+  part[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && col < H) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < kReduceWarps; ++i) t += part[i][lane];
+    dw[col] = t;
+  }
+}
+
+// Launches dw_reduce on the P partial rows (row stride ld) of H columns
+// (PDL, like the first pass); also reports an error left by the first
+// pass's launch.
+inline cudaError_t launch_dw_reduce(const float *ws, int64_t P, int64_t H, int64_t ld,
+                                    float *out, cudaStream_t s) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(dw_reduce, dim3((unsigned)ceil_div(H, (int64_t)32)), dim3(32 * kReduceWarps), 0,
+                 s, ws, (int)P, (int)H, (int)ld, out);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+}  // namespace ftk

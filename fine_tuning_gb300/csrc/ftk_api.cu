@@ -4,6 +4,7 @@
 // before a launch.
 #include <stdint.h>
 
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -478,6 +479,193 @@ FTK_API ftk_status ftk_qk_rope_freq_bwd(void *dq, int64_t ld_q, void *dk, int64_
   if (!inv_freq) return FTK_ERR_NULL;
   return qk_rope(dq, ld_q, dk, ld_k, cu_seqlens, B, T, Hq, Hkv, D, 0.0, inv_freq, dtype, stream,
                  true);
+}
+
+// -------------------------------------------------- QK-RMSNorm fused with RoPE
+
+}  // extern "C"
+
+namespace {
+
+struct NormRopeShape {
+  int64_t T;
+  int32_t B, Hq, Hkv, D;
+};
+
+// Shape, frequency and eps checks shared by the fused forward and backward.
+ftk_status norm_rope_shape(const NormRopeShape &sh, double theta, const double *inv_freq,
+                           float eps) {
+  if (sh.T < 0 || sh.B < 0 || sh.Hq < 0 || sh.Hkv < 0 || sh.Hq + sh.Hkv < 1 || sh.D < 2 ||
+      sh.D % 2 != 0 || sh.D / 2 > ftk::kRopeMaxHalf || sh.T >= (int64_t(1) << 31))
+    return FTK_ERR_SHAPE;
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return FTK_ERR_SHAPE;
+  if (inv_freq) {
+    for (int32_t i = 0; i < sh.D / 2; ++i)
+      if (!(inv_freq[i] >= 0.0 && inv_freq[i] <= 1.0)) return FTK_ERR_SHAPE;
+  } else if (!(theta > 0.0)) {
+    return FTK_ERR_SHAPE;
+  }
+  return FTK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+FTK_API ftk_status ftk_qk_norm_rope_fwd(const void *q, int64_t ld_q, const void *k, int64_t ld_k,
+                                        const void *wq, const void *wk, void *q_out,
+                                        int64_t ld_qo, void *k_out, int64_t ld_ko,
+                                        float *rstd_q, float *rstd_k,
+                                        const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                        int32_t Hq, int32_t Hkv, int32_t D, double theta,
+                                        const double *inv_freq, float eps, ftk_dtype dtype,
+                                        ftk_stream_t stream) {
+  if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
+  const NormRopeShape sh{T, B, Hq, Hkv, D};
+  ftk_status st = norm_rope_shape(sh, theta, inv_freq, eps);
+  if (st != FTK_OK) return st;
+  const int64_t wq_ = (int64_t)Hq * D, wk_ = (int64_t)Hkv * D;
+  if ((Hq > 0 && (ld_q < wq_ || ld_qo < wq_)) || (Hkv > 0 && (ld_k < wk_ || ld_ko < wk_)))
+    return FTK_ERR_SHAPE;
+  if (T == 0) return FTK_OK;
+  if (B < 1) return FTK_ERR_SHAPE;
+  if (!cu_seqlens || (Hq > 0 && (!q || !wq || !q_out)) || (Hkv > 0 && (!k || !wk || !k_out)))
+    return FTK_ERR_NULL;
+  const DType dt = (DType)dtype;
+  const int64_t es = ftk::dtype_bytes(dt);
+  if (!aligned(q, es) || !aligned(k, es) || !aligned(wq, es) || !aligned(wk, es) ||
+      !aligned(q_out, es) || !aligned(k_out, es) || !aligned(rstd_q, 4) ||
+      !aligned(rstd_k, 4) || !aligned(cu_seqlens, 4))
+    return FTK_ERR_ALIGN;
+  const int64_t rq_n = Hq > 0 ? T : 0, rk_n = Hkv > 0 ? T : 0;
+  const View vq = view(q, rq_n, ld_q, wq_, es), vk = view(k, rk_n, ld_k, wk_, es);
+  const View voq = view(q_out, rq_n, ld_qo, wq_, es), vok = view(k_out, rk_n, ld_ko, wk_, es);
+  const View vwq = view(wq, Hq > 0 ? 1 : 0, D, D, es), vwk = view(wk, Hkv > 0 ? 1 : 0, D, D, es);
+  const View vrq = view(rstd_q, rstd_q && Hq > 0 ? 1 : 0, T * Hq, T * Hq, 4);
+  const View vrk = view(rstd_k, rstd_k && Hkv > 0 ? 1 : 0, T * Hkv, T * Hkv, 4);
+  const View vc = view(cu_seqlens, 1, (int64_t)B + 1, (int64_t)B + 1, 4);
+  // an output may replace its own input exactly; nothing else overlaps an output
+  if (!same_view(voq, vq) && may_overlap(voq, vq)) return FTK_ERR_ALIAS;
+  if (!same_view(vok, vk) && may_overlap(vok, vk)) return FTK_ERR_ALIAS;
+  const View outs[4] = {voq, vok, vrq, vrk};
+  const View ins[5] = {vq, vk, vwq, vwk, vc};
+  for (int i = 0; i < 4; ++i) {
+    for (int m = 0; m < 5; ++m) {
+      if ((i == 0 && m == 0) || (i == 1 && m == 1)) continue;  // handled above
+      if (may_overlap(outs[i], ins[m])) return FTK_ERR_ALIAS;
+    }
+    for (int m = i + 1; m < 4; ++m)
+      if (may_overlap(outs[i], outs[m])) return FTK_ERR_ALIAS;
+  }
+  const int n = dt == DType::F32 ? 4 : 8;
+  const bool vec = (D / 2) % n == 0 &&
+                   (Hq == 0 || (aligned(q, 16) && aligned(q_out, 16) && aligned(wq, 16) &&
+                                ld_q % n == 0 && ld_qo % n == 0)) &&
+                   (Hkv == 0 || (aligned(k, 16) && aligned(k_out, 16) && aligned(wk, 16) &&
+                                 ld_k % n == 0 && ld_ko % n == 0));
+  const int64_t hmax = Hq > Hkv ? Hq : Hkv;
+  const bool wide = vq.max_offset() > kNarrowLimit || vk.max_offset() > kNarrowLimit ||
+                    voq.max_offset() > kNarrowLimit || vok.max_offset() > kNarrowLimit ||
+                    T * hmax > kNarrowLimit;
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ftk::QkNormRopeArgs a{q,     ld_q,   k,      ld_k,      nullptr, 0,     nullptr, 0,
+                        q_out, ld_qo,  k_out,  ld_ko,     wq,      wk,    rstd_q,  rstd_k,
+                        nullptr, nullptr, nullptr, 0,     cu_seqlens, B,  T,       Hq,
+                        Hkv,   D,      theta,  inv_freq,  eps,     false};
+  return finish(ftk::launch_qk_norm_rope(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+FTK_API size_t ftk_qk_norm_rope_bwd_workspace_bytes(int64_t T, int32_t D, ftk_dtype dtype) {
+  if (!valid_dtype(dtype) || T <= 0 || D < 2 || D % 2 != 0) return 0;
+  ftk::DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return 0;
+  return (size_t)ftk::qk_norm_rope_partial_rows(T, dev) * 2 * (size_t)D * sizeof(float);
+}
+
+FTK_API ftk_status ftk_qk_norm_rope_bwd(const void *dq_out, int64_t ld_gq, const void *dk_out,
+                                        int64_t ld_gk, const void *q, int64_t ld_q,
+                                        const void *k, int64_t ld_k, const void *wq,
+                                        const void *wk, const float *rstd_q,
+                                        const float *rstd_k, void *dq, int64_t ld_dq, void *dk,
+                                        int64_t ld_dk, float *dwq, float *dwk, void *workspace,
+                                        size_t workspace_bytes, const int32_t *cu_seqlens,
+                                        int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D,
+                                        double theta, const double *inv_freq, float eps,
+                                        ftk_dtype dtype, ftk_stream_t stream) {
+  if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
+  const NormRopeShape sh{T, B, Hq, Hkv, D};
+  ftk_status st = norm_rope_shape(sh, theta, inv_freq, eps);
+  if (st != FTK_OK) return st;
+  const int64_t wq_ = (int64_t)Hq * D, wk_ = (int64_t)Hkv * D;
+  if ((Hq > 0 && (ld_q < wq_ || ld_gq < wq_ || ld_dq < wq_)) ||
+      (Hkv > 0 && (ld_k < wk_ || ld_gk < wk_ || ld_dk < wk_)))
+    return FTK_ERR_SHAPE;
+  if (T == 0) return FTK_OK;
+  if (B < 1) return FTK_ERR_SHAPE;
+  if (!cu_seqlens || (Hq > 0 && (!q || !wq || !dq_out || !dq || !dwq)) ||
+      (Hkv > 0 && (!k || !wk || !dk_out || !dk || !dwk)))
+    return FTK_ERR_NULL;
+  // rstd: every needed one, or none (recompute)
+  const bool have_r = (Hq > 0 && rstd_q) || (Hkv > 0 && rstd_k);
+  if (have_r && ((Hq > 0 && !rstd_q) || (Hkv > 0 && !rstd_k))) return FTK_ERR_NULL;
+  if (!workspace) return FTK_ERR_WORKSPACE;
+  const DType dt = (DType)dtype;
+  const int64_t es = ftk::dtype_bytes(dt);
+  if (!aligned(q, es) || !aligned(k, es) || !aligned(wq, es) || !aligned(wk, es) ||
+      !aligned(dq_out, es) || !aligned(dk_out, es) || !aligned(dq, es) || !aligned(dk, es) ||
+      !aligned(rstd_q, 4) || !aligned(rstd_k, 4) || !aligned(dwq, 4) || !aligned(dwk, 4) ||
+      !aligned(workspace, 16) || !aligned(cu_seqlens, 4))
+    return FTK_ERR_ALIGN;
+  const int64_t ws_rows = (int64_t)(workspace_bytes / (2 * (size_t)D * sizeof(float)));
+  if (ws_rows < 1) return FTK_ERR_WORKSPACE;
+  const int64_t rq_n = Hq > 0 ? T : 0, rk_n = Hkv > 0 ? T : 0;
+  const View vq = view(q, rq_n, ld_q, wq_, es), vk = view(k, rk_n, ld_k, wk_, es);
+  const View vgq = view(dq_out, rq_n, ld_gq, wq_, es), vgk = view(dk_out, rk_n, ld_gk, wk_, es);
+  const View vdq = view(dq, rq_n, ld_dq, wq_, es), vdk = view(dk, rk_n, ld_dk, wk_, es);
+  const View vwq = view(wq, Hq > 0 ? 1 : 0, D, D, es), vwk = view(wk, Hkv > 0 ? 1 : 0, D, D, es);
+  const View vrq = view(rstd_q, rstd_q && Hq > 0 ? 1 : 0, T * Hq, T * Hq, 4);
+  const View vrk = view(rstd_k, rstd_k && Hkv > 0 ? 1 : 0, T * Hkv, T * Hkv, 4);
+  const View vdwq = view(dwq, Hq > 0 ? 1 : 0, D, D, 4), vdwk = view(dwk, Hkv > 0 ? 1 : 0, D, D, 4);
+  const View vws = view(workspace, 1, ws_rows * 2 * D, ws_rows * 2 * D, 4);
+  const View vc = view(cu_seqlens, 1, (int64_t)B + 1, (int64_t)B + 1, 4);
+  // dq / dk may replace the output gradients exactly; nothing else overlaps an output
+  if (!same_view(vdq, vgq) && may_overlap(vdq, vgq)) return FTK_ERR_ALIAS;
+  if (!same_view(vdk, vgk) && may_overlap(vdk, vgk)) return FTK_ERR_ALIAS;
+  const View outs[5] = {vdq, vdk, vdwq, vdwk, vws};
+  const View ins[9] = {vgq, vgk, vq, vk, vwq, vwk, vrq, vrk, vc};
+  for (int i = 0; i < 5; ++i) {
+    for (int m = 0; m < 9; ++m) {
+      if ((i == 0 && m == 0) || (i == 1 && m == 1)) continue;  // handled above
+      if (may_overlap(outs[i], ins[m])) return FTK_ERR_ALIAS;
+    }
+    for (int m = i + 1; m < 5; ++m)
+      if (may_overlap(outs[i], outs[m])) return FTK_ERR_ALIAS;
+  }
+  const int n = dt == DType::F32 ? 4 : 8;
+  const bool vec =
+      (D / 2) % n == 0 &&
+      (Hq == 0 || (aligned(q, 16) && aligned(dq_out, 16) && aligned(dq, 16) && aligned(wq, 16) &&
+                   ld_q % n == 0 && ld_gq % n == 0 && ld_dq % n == 0)) &&
+      (Hkv == 0 || (aligned(k, 16) && aligned(dk_out, 16) && aligned(dk, 16) &&
+                    aligned(wk, 16) && ld_k % n == 0 && ld_gk % n == 0 && ld_dk % n == 0));
+  const int64_t hmax = Hq > Hkv ? Hq : Hkv;
+  const bool wide = vq.max_offset() > kNarrowLimit || vk.max_offset() > kNarrowLimit ||
+                    vgq.max_offset() > kNarrowLimit || vgk.max_offset() > kNarrowLimit ||
+                    vdq.max_offset() > kNarrowLimit || vdk.max_offset() > kNarrowLimit ||
+                    T * hmax > kNarrowLimit;
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ftk::QkNormRopeArgs a{q,      ld_q,   k,      ld_k,   dq_out,   ld_gq,  dk_out,
+                        ld_gk,  dq,     ld_dq,  dk,     ld_dk,    wq,     wk,
+                        have_r ? (float *)rstd_q : nullptr,
+                        have_r ? (float *)rstd_k : nullptr,
+                        Hq > 0 ? dwq : nullptr, Hkv > 0 ? dwk : nullptr,
+                        (float *)workspace, ws_rows, cu_seqlens, B, T, Hq, Hkv, D,
+                        theta,  inv_freq, eps,  true};
+  return finish(ftk::launch_qk_norm_rope(dt, vec, wide, a, dev, (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -169,4 +169,41 @@ struct RopeArgs {
 cudaError_t launch_qk_rope(DType dt, bool vec, bool wide, const RopeArgs &a,
                            const DeviceInfo &dev, cudaStream_t s);
 
+// Per-head QK-RMSNorm fused with RoPE (qk_norm_rope.cu).  Forward: q, k in,
+// oq, ok out (may be q, k), rq/rk written when set.  Backward: gq, gk (the
+// output gradients) and the pre-norm q, k in; oq, ok receive the pre-norm
+// gradients (may be gq, gk); rq/rk read when set (else recomputed); the
+// partial rows go to ws and dwq/dwk (nullable) receive the weight gradients.
+struct QkNormRopeArgs {
+  const void *q;
+  int64_t ld_q;
+  const void *k;
+  int64_t ld_k;
+  const void *gq;
+  int64_t ld_gq;
+  const void *gk;
+  int64_t ld_gk;
+  void *oq;
+  int64_t ld_oq;
+  void *ok;
+  int64_t ld_ok;
+  const void *wq, *wk;
+  float *rq, *rk;
+  float *dwq, *dwk;
+  float *ws;  // [ws_rows][2D]
+  int64_t ws_rows;
+  const int32_t *cu;
+  int32_t B;
+  int64_t T;
+  int32_t Hq, Hkv, D;
+  double theta;
+  const double *inv_freq;  // HOST [D/2], nullable
+  float eps;
+  bool backward;
+};
+// Upper bound on the partial rows the backward writes.
+int64_t qk_norm_rope_partial_rows(int64_t T, const DeviceInfo &dev);
+cudaError_t launch_qk_norm_rope(DType dt, bool vec, bool wide, const QkNormRopeArgs &a,
+                                const DeviceInfo &dev, cudaStream_t s);
+
 }  // namespace ftk

@@ -1,0 +1,561 @@
+// Per-head RMSNorm of Q and K (the q_norm / k_norm of Qwen3-style attention)
+// fused with the rotary embedding, forward and backward, over a packed batch
+// of variable-length sequences.
+//
+// For token t at position p and every head vector v (D values) of Q (weight
+// wq [D]) or K (weight wk [D]):
+//   r   = 1 / sqrt(mean_i v_i^2 + eps)
+//   n_i = v_i r w_i                      (fp32, never rounded)
+//   out = rotate-half RoPE of n at p      (inv_freq from theta or a table)
+// Backward, from the output gradient g:
+//   dn  = the rotation by -phi of g
+//   c   = sum_i dn_i w_i v_i
+//   dv  = r w dn - r^3 v c / D,  dw_i += dn_i v_i r  (over tokens and heads)
+// Sources: the fused QK-RoPE kernel of "Unsloth prétend accélérer 5 fois
+// l'entraînement des LLM avec de nouveaux noyaux Triton et un auto-packing"
+// (seventnews.com) and optimisation (1) of "Chronicals" (arXiv 2601.02609,
+// abstract); the norm in front of the rotation is this library's variant.
+//
+// One warp per token (the layout of qk_rope_warp): half a head is NV = D/2N
+// packets and NV divides 32, so lane (slot, j) owns packet j of both halves
+// of heads slot, slot + S, ... (S = 32 / NV).  A head's sum of squares is a
+// shuffle reduction over its NV lanes.  cos/sin of the token's D/2 angles
+// are computed once into the warp's shared-memory slice.  The backward is
+// persistent; each lane keeps its columns' dwq and dwk sums in registers,
+// the CTA combines its warps in a fixed order into one partial row [2D], and
+// dw_reduce sums the rows in a fixed order: bitwise reproducible.  Shapes
+// whose half head does not split evenly over lanes, or unaligned rows, take
+// the element-wise kernels (lane i owns pairs i, i + 32, ...).
+#include "common.cuh"
+#include "dw_reduce.cuh"
+#include "launch.h"
+#include "rope_common.cuh"
+
+namespace ftk {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxBlocksPerSm = 4;
+constexpr int kPairsPerLane = kRopeMaxHalf / 32;  // element-wise kernels
+
+template <typename T, typename Idx> struct NormRopeParams {
+  const T *q;  // pre-norm Q / K
+  Idx ld_q;
+  const T *k;
+  Idx ld_k;
+  const T *gq;  // backward: gradient of the outputs
+  Idx ld_gq;
+  const T *gk;
+  Idx ld_gk;
+  T *oq;  // forward: outputs; backward: gradient of the pre-norm Q / K
+  Idx ld_oq;
+  T *ok;
+  Idx ld_ok;
+  const T *wq, *wk;
+  float *rq, *rk;  // r per (token, head): written by the forward, read by the backward (nullable)
+  float *ws;       // backward: [gridDim.x][2D] partial rows (dwq | dwk)
+  const int32_t *cu;
+  int B;
+  Idx rows;
+  int Hq, Hkv, D;
+  float eps, inv_d;
+};
+
+// Sum over the NV lanes (a power of two dividing 32) that share a slot.
+__device__ __forceinline__ float slot_sum(float v, int NV) {
+  for (int o = NV >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float2 slot_sum2(float2 v, int NV) {
+  for (int o = NV >> 1; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+  }
+  return v;
+}
+
+// cos and sgn*sin of the token's D/2 angles into the warp's table.
+__device__ __forceinline__ void token_table(float2 *wt, const float2 *freq, int half, int p,
+                                            float sgn, int lane) {
+  for (int i = lane; i < half; i += 32) {
+    const float2 f = freq[i];
+    float c, sn;
+    rope_cos_sin(p, f.x, f.y, &c, &sn);
+    wt[i] = make_float2(c, sgn * sn);
+  }
+}
+
+template <typename T, typename Idx, int N, int HPT>
+__global__ void __launch_bounds__(kThreads, 2)
+qk_norm_rope_fwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ RopeFreqs fr) {
+  extern __shared__ float2 tab[];  // [warps][D/2] (cos, sin)
+  __shared__ float2 freq[kRopeMaxHalf];
+  const int D = a.D, half = D >> 1, NV = half / N, S = 32 / NV, NH = a.Hq + a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = lane % NV, slot = lane / NV;
+  const Idx t = (Idx)blockIdx.x * kWarps + warp;
+  const bool live = t < a.rows;
+  const T *qin = a.q + t * a.ld_q + (Idx)j * N, *kin = a.k + t * a.ld_k + (Idx)j * N;
+  auto src = [&](int h) { return h < a.Hq ? qin + (Idx)h * D : kin + (Idx)(h - a.Hq) * D; };
+
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
+  Packet<T, N> x1[HPT], x2[HPT];
+#pragma unroll
+  for (int m = 0; m < HPT; ++m) {
+    const int h = slot + m * S;
+    if (live && h < NH) {
+      x1[m] = load_packet<T, N>(src(h));
+      x2[m] = load_packet<T, N>(src(h) + half);
+    }
+  }
+  Packet<T, N> wq1, wq2, wk1, wk2;
+  if (a.Hq > 0) {
+    wq1 = load_packet<T, N>(a.wq + j * N);
+    wq2 = load_packet<T, N>(a.wq + half + j * N);
+  }
+  if (a.Hkv > 0) {
+    wk1 = load_packet<T, N>(a.wk + j * N);
+    wk2 = load_packet<T, N>(a.wk + half + j * N);
+  }
+  __syncthreads();  // the frequency table
+  if (!live) return;  // the whole warp: t is uniform across it
+
+  float2 *wt = tab + warp * half;
+  token_table(wt, freq, half, position_of<Idx>(t, a.cu, a.B), 1.0f, lane);
+  __syncwarp();
+  float cv[N], sv[N];
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    const float2 v = wt[j * N + e];
+    cv[e] = v.x;
+    sv[e] = v.y;
+  }
+  for (int h0 = 0; h0 < NH; h0 += HPT * S) {
+#pragma unroll
+    for (int m = 0; m < HPT; ++m) {
+      const int h = h0 + slot + m * S;
+      const bool act = h < NH;
+      float ss = 0.f;
+      if (act) {
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float u1 = x1[m].get(e), u2 = x2[m].get(e);
+          ss = fmaf(u1, u1, fmaf(u2, u2, ss));
+        }
+      }
+      ss = slot_sum(ss, NV);  // every lane takes part
+      if (act) {
+        const float r = rsqrtf(fmaf(ss, a.inv_d, a.eps));
+        const bool isq = h < a.Hq;
+        const Packet<T, N> &w1 = isq ? wq1 : wk1, &w2 = isq ? wq2 : wk2;
+        Packet<T, N> o1, o2;
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float n1 = x1[m].get(e) * r * w1.get(e), n2 = x2[m].get(e) * r * w2.get(e);
+          o1.set(e, fmaf(n1, cv[e], -n2 * sv[e]));
+          o2.set(e, fmaf(n2, cv[e], n1 * sv[e]));
+        }
+        T *dst = isq ? a.oq + t * a.ld_oq + (Idx)h * D : a.ok + t * a.ld_ok + (Idx)(h - a.Hq) * D;
+        store_packet<T, N>(dst + (Idx)j * N, o1);
+        store_packet<T, N>(dst + half + (Idx)j * N, o2);
+        if (j == 0) {
+          if (isq && a.rq) a.rq[t * a.Hq + h] = r;
+          if (!isq && a.rk) a.rk[t * a.Hkv + (h - a.Hq)] = r;
+        }
+      }
+    }
+    const int next = h0 + HPT * S;
+#pragma unroll
+    for (int m = 0; m < HPT; ++m) {
+      const int h = next + slot + m * S;
+      if (h < NH) {
+        x1[m] = load_packet<T, N>(src(h));
+        x2[m] = load_packet<T, N>(src(h) + half);
+      }
+    }
+  }
+}
+
+// The CTA's dwq | dwk partial row: sum over the warp's slots (lanes with the
+// same packet j), then over the CTA's warps in order, into ws[blockIdx.x].
+template <int N>
+__device__ __forceinline__ void write_partial(float (&acc)[4][N], float *part, float *ws, int D,
+                                              int NV, int j, int slot, int warp) {
+  const int half = D >> 1;
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+      for (int o = NV; o < 32; o <<= 1) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+  if (slot == 0) {
+    float *mine = part + warp * 2 * D;  // [warps][2D]
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      mine[j * N + e] = acc[0][e];
+      mine[half + j * N + e] = acc[1][e];
+      mine[D + j * N + e] = acc[2][e];
+      mine[D + half + j * N + e] = acc[3][e];
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < 2 * D; c += blockDim.x) {
+    float s = 0.f;
+    for (int w = 0; w < kWarps; ++w) s += part[w * 2 * D + c];
+    ws[(size_t)blockIdx.x * 2 * D + c] = s;
+  }
+}
+
+template <typename T, typename Idx, int N, bool HAS_RSTD>
+__global__ void __launch_bounds__(kThreads, 2)
+qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ RopeFreqs fr) {
+  extern __shared__ float2 tab[];  // [warps][D/2] (cos, -sin), then [warps][2D] fp32 partials
+  __shared__ float2 freq[kRopeMaxHalf];
+  const int D = a.D, half = D >> 1, NV = half / N, S = 32 / NV, NH = a.Hq + a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = lane % NV, slot = lane / NV;
+  float *part = reinterpret_cast<float *>(tab + kWarps * half);
+
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
+  Packet<T, N> wq1, wq2, wk1, wk2;
+  if (a.Hq > 0) {
+    wq1 = load_packet<T, N>(a.wq + j * N);
+    wq2 = load_packet<T, N>(a.wq + half + j * N);
+  }
+  if (a.Hkv > 0) {
+    wk1 = load_packet<T, N>(a.wk + j * N);
+    wk2 = load_packet<T, N>(a.wk + half + j * N);
+  }
+  float acc[4][N];  // dwq first half, dwq second half, dwk first half, dwk second half
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int e = 0; e < N; ++e) acc[g][e] = 0.f;
+  __syncthreads();  // the frequency table
+
+  float2 *wt = tab + warp * half;
+  const Idx step = (Idx)gridDim.x * kWarps;
+  for (Idx t = (Idx)blockIdx.x * kWarps + warp; t < a.rows; t += step) {
+    const T *gq = a.gq + t * a.ld_gq + (Idx)j * N, *gk = a.gk + t * a.ld_gk + (Idx)j * N;
+    const T *vq = a.q + t * a.ld_q + (Idx)j * N, *vk = a.k + t * a.ld_k + (Idx)j * N;
+    __syncwarp();  // the previous token's table has been read
+    token_table(wt, freq, half, position_of<Idx>(t, a.cu, a.B), -1.0f, lane);
+    __syncwarp();
+    float cv[N], sv[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      const float2 v = wt[j * N + e];
+      cv[e] = v.x;
+      sv[e] = v.y;
+    }
+    for (int h = slot; h - slot < NH; h += S) {  // uniform trip count across the warp
+      const bool act = h < NH;
+      const bool isq = h < a.Hq;
+      const int hk = h - a.Hq;
+      Packet<T, N> g1, g2, v1, v2;
+      float r = 0.f;
+      if (act) {
+        const T *gp = isq ? gq + (Idx)h * D : gk + (Idx)hk * D;
+        const T *vp = isq ? vq + (Idx)h * D : vk + (Idx)hk * D;
+        g1 = load_packet<T, N>(gp);
+        g2 = load_packet<T, N>(gp + half);
+        v1 = load_packet<T, N>(vp);
+        v2 = load_packet<T, N>(vp + half);
+        if (HAS_RSTD) r = isq ? a.rq[t * a.Hq + h] : a.rk[t * a.Hkv + hk];
+      }
+      const Packet<T, N> &w1 = isq ? wq1 : wk1, &w2 = isq ? wq2 : wk2;
+      float dn1[N], dn2[N];
+      float2 cs = make_float2(0.f, 0.f);  // (sum dn w v, sum v v)
+      if (act) {
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float a1 = g1.get(e), a2 = g2.get(e);
+          dn1[e] = fmaf(a1, cv[e], -a2 * sv[e]);
+          dn2[e] = fmaf(a2, cv[e], a1 * sv[e]);
+          const float u1 = v1.get(e), u2 = v2.get(e);
+          cs.x = fmaf(dn1[e] * w1.get(e), u1, fmaf(dn2[e] * w2.get(e), u2, cs.x));
+          if (!HAS_RSTD) cs.y = fmaf(u1, u1, fmaf(u2, u2, cs.y));
+        }
+      }
+      if (HAS_RSTD)
+        cs.x = slot_sum(cs.x, NV);
+      else
+        cs = slot_sum2(cs, NV);
+      if (act) {
+        if (!HAS_RSTD) r = rsqrtf(fmaf(cs.y, a.inv_d, a.eps));
+        const float am = r * r * r * cs.x * a.inv_d;
+        Packet<T, N> o1, o2;
+        const int g0 = isq ? 0 : 2;
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float u1 = v1.get(e), u2 = v2.get(e);
+          o1.set(e, fmaf(-am, u1, r * w1.get(e) * dn1[e]));
+          o2.set(e, fmaf(-am, u2, r * w2.get(e) * dn2[e]));
+          acc[g0][e] = fmaf(dn1[e] * u1, r, acc[g0][e]);
+          acc[g0 + 1][e] = fmaf(dn2[e] * u2, r, acc[g0 + 1][e]);
+        }
+        T *dst = isq ? a.oq + t * a.ld_oq + (Idx)h * D : a.ok + t * a.ld_ok + (Idx)hk * D;
+        store_packet<T, N>(dst + (Idx)j * N, o1);
+        store_packet<T, N>(dst + half + (Idx)j * N, o2);
+      }
+    }
+  }
+  write_partial<N>(acc, part, a.ws, D, NV, j, slot, warp);
+}
+
+// Element-wise forms: one warp per token, heads one after another, lane i
+// owning the pairs i, i + 32, ... of every head.
+template <typename T, typename Idx>
+__global__ void __launch_bounds__(kThreads)
+qk_norm_rope_fwd_generic(const NormRopeParams<T, Idx> a, const __grid_constant__ RopeFreqs fr) {
+  extern __shared__ float2 tab[];
+  __shared__ float2 freq[kRopeMaxHalf];
+  const int D = a.D, half = D >> 1, NH = a.Hq + a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Idx t = (Idx)blockIdx.x * kWarps + warp;
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
+  __syncthreads();
+  if (t >= a.rows) return;
+  float2 *wt = tab + warp * half;
+  token_table(wt, freq, half, position_of<Idx>(t, a.cu, a.B), 1.0f, lane);
+  __syncwarp();
+  for (int h = 0; h < NH; ++h) {
+    const bool isq = h < a.Hq;
+    const int hk = h - a.Hq;
+    const T *v = isq ? a.q + t * a.ld_q + (Idx)h * D : a.k + t * a.ld_k + (Idx)hk * D;
+    const T *w = isq ? a.wq : a.wk;
+    // the sum of squares in the backward's order (pairs), so that r
+    // recomputed there is bit-identical
+    float ss = 0.f;
+#pragma unroll
+    for (int m = 0; m < kPairsPerLane; ++m) {
+      const int i = lane + 32 * m;
+      if (i < half) {
+        const float u1 = to_float(v[i]), u2 = to_float(v[i + half]);
+        ss = fmaf(u1, u1, fmaf(u2, u2, ss));
+      }
+    }
+    ss = warp_sum(ss);
+    const float r = rsqrtf(fmaf(ss, a.inv_d, a.eps));
+    T *o = isq ? a.oq + t * a.ld_oq + (Idx)h * D : a.ok + t * a.ld_ok + (Idx)hk * D;
+    float n1[kPairsPerLane], n2[kPairsPerLane];
+#pragma unroll
+    for (int m = 0; m < kPairsPerLane; ++m) {
+      const int i = lane + 32 * m;
+      if (i < half) {
+        n1[m] = to_float(v[i]) * r * to_float(w[i]);
+        n2[m] = to_float(v[i + half]) * r * to_float(w[i + half]);
+      }
+    }
+    __syncwarp();  // every lane has read the head before any lane writes it (o may be v)
+#pragma unroll
+    for (int m = 0; m < kPairsPerLane; ++m) {
+      const int i = lane + 32 * m;
+      if (i < half) {
+        const float2 c = wt[i];
+        o[i] = from_float<T>(fmaf(n1[m], c.x, -n2[m] * c.y));
+        o[i + half] = from_float<T>(fmaf(n2[m], c.x, n1[m] * c.y));
+      }
+    }
+    if (lane == 0) {
+      if (isq && a.rq) a.rq[t * a.Hq + h] = r;
+      if (!isq && a.rk) a.rk[t * a.Hkv + hk] = r;
+    }
+  }
+}
+
+template <typename T, typename Idx, bool HAS_RSTD>
+__global__ void __launch_bounds__(kThreads)
+qk_norm_rope_bwd_generic(const NormRopeParams<T, Idx> a, const __grid_constant__ RopeFreqs fr) {
+  extern __shared__ float2 tab[];  // [warps][D/2], then [warps][2D] fp32 partials
+  __shared__ float2 freq[kRopeMaxHalf];
+  const int D = a.D, half = D >> 1, NH = a.Hq + a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float *part = reinterpret_cast<float *>(tab + kWarps * half);
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
+  float acc[4][kPairsPerLane];
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int m = 0; m < kPairsPerLane; ++m) acc[g][m] = 0.f;
+  __syncthreads();
+  float2 *wt = tab + warp * half;
+  const Idx step = (Idx)gridDim.x * kWarps;
+  for (Idx t = (Idx)blockIdx.x * kWarps + warp; t < a.rows; t += step) {
+    __syncwarp();
+    token_table(wt, freq, half, position_of<Idx>(t, a.cu, a.B), -1.0f, lane);
+    __syncwarp();
+    for (int h = 0; h < NH; ++h) {
+      const bool isq = h < a.Hq;
+      const int hk = h - a.Hq;
+      const T *g = isq ? a.gq + t * a.ld_gq + (Idx)h * D : a.gk + t * a.ld_gk + (Idx)hk * D;
+      const T *v = isq ? a.q + t * a.ld_q + (Idx)h * D : a.k + t * a.ld_k + (Idx)hk * D;
+      const T *w = isq ? a.wq : a.wk;
+      float dn1[kPairsPerLane], dn2[kPairsPerLane];
+      float2 cs = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < kPairsPerLane; ++m) {
+        const int i = lane + 32 * m;
+        if (i < half) {
+          const float2 c = wt[i];
+          const float a1 = to_float(g[i]), a2 = to_float(g[i + half]);
+          dn1[m] = fmaf(a1, c.x, -a2 * c.y);
+          dn2[m] = fmaf(a2, c.x, a1 * c.y);
+          const float u1 = to_float(v[i]), u2 = to_float(v[i + half]);
+          cs.x = fmaf(dn1[m] * to_float(w[i]), u1, fmaf(dn2[m] * to_float(w[i + half]), u2, cs.x));
+          cs.y = fmaf(u1, u1, fmaf(u2, u2, cs.y));
+        }
+      }
+      cs = warp_sum2(cs);
+      const float r = HAS_RSTD ? (isq ? a.rq[t * a.Hq + h] : a.rk[t * a.Hkv + hk])
+                               : rsqrtf(fmaf(cs.y, a.inv_d, a.eps));
+      const float am = r * r * r * cs.x * a.inv_d;
+      T *o = isq ? a.oq + t * a.ld_oq + (Idx)h * D : a.ok + t * a.ld_ok + (Idx)hk * D;
+      const int g0 = isq ? 0 : 2;
+      __syncwarp();  // every lane has read the head before any lane writes it (o may be g)
+#pragma unroll
+      for (int m = 0; m < kPairsPerLane; ++m) {
+        const int i = lane + 32 * m;
+        if (i < half) {
+          const float u1 = to_float(v[i]), u2 = to_float(v[i + half]);
+          o[i] = from_float<T>(fmaf(-am, u1, r * to_float(w[i]) * dn1[m]));
+          o[i + half] = from_float<T>(fmaf(-am, u2, r * to_float(w[i + half]) * dn2[m]));
+          acc[g0][m] = fmaf(dn1[m] * u1, r, acc[g0][m]);
+          acc[g0 + 1][m] = fmaf(dn2[m] * u2, r, acc[g0 + 1][m]);
+        }
+      }
+    }
+  }
+  float *mine = part + warp * 2 * D;
+#pragma unroll
+  for (int m = 0; m < kPairsPerLane; ++m) {
+    const int i = lane + 32 * m;
+    if (i < half) {
+      mine[i] = acc[0][m];
+      mine[half + i] = acc[1][m];
+      mine[D + i] = acc[2][m];
+      mine[D + half + i] = acc[3][m];
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < 2 * D; c += blockDim.x) {
+    float s = 0.f;
+    for (int w = 0; w < kWarps; ++w) s += part[w * 2 * D + c];
+    a.ws[(size_t)blockIdx.x * 2 * D + c] = s;
+  }
+}
+
+template <typename T, typename Idx>
+NormRopeParams<T, Idx> params_of(const QkNormRopeArgs &a) {
+  return NormRopeParams<T, Idx>{
+      (const T *)a.q,  (Idx)a.ld_q,  (const T *)a.k,  (Idx)a.ld_k,  (const T *)a.gq,
+      (Idx)a.ld_gq,    (const T *)a.gk, (Idx)a.ld_gk, (T *)a.oq,     (Idx)a.ld_oq,
+      (T *)a.ok,       (Idx)a.ld_ok, (const T *)a.wq, (const T *)a.wk, a.rq,
+      a.rk,            a.ws,         a.cu,            a.B,           (Idx)a.T,
+      a.Hq,            a.Hkv,        a.D,             a.eps,         (float)(1.0 / (double)a.D)};
+}
+
+cudaError_t finish_launch(cudaError_t e) { return e != cudaSuccess ? e : cudaGetLastError(); }
+
+template <typename T, typename Idx, int N>
+cudaError_t fwd_warp_launch(const QkNormRopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
+  const int NH = a.Hq + a.Hkv, half = a.D / 2, S = 32 / (half / N);
+  const int per_lane = (NH + S - 1) / S;
+  const dim3 grid((unsigned)ceil_div(a.T, (int64_t)kWarps));
+  const size_t smem = sizeof(float2) * (size_t)kWarps * half;
+  const NormRopeParams<T, Idx> k = params_of<T, Idx>(a);
+  // two heads per pass at most: four would spill at the 128-register cap
+  if (per_lane <= 1)
+    return finish_launch(launch_pdl(qk_norm_rope_fwd_warp<T, Idx, N, 1>, grid, dim3(kThreads),
+                                    smem, s, k, fr));
+  return finish_launch(launch_pdl(qk_norm_rope_fwd_warp<T, Idx, N, 2>, grid, dim3(kThreads), smem,
+                                  s, k, fr));
+}
+
+template <typename T, typename Idx>
+cudaError_t fwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &fr,
+                      cudaStream_t s) {
+  constexpr int NV = VecWidth<T>::value;
+  if (warp_path) return fwd_warp_launch<T, Idx, NV>(a, fr, s);
+  const size_t smem = sizeof(float2) * (size_t)kWarps * (a.D / 2);
+  return finish_launch(launch_pdl(qk_norm_rope_fwd_generic<T, Idx>,
+                                  dim3((unsigned)ceil_div(a.T, (int64_t)kWarps)), dim3(kThreads),
+                                  smem, s, params_of<T, Idx>(a), fr));
+}
+
+template <typename T, typename Idx>
+cudaError_t bwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &fr,
+                      const DeviceInfo &dev, cudaStream_t s) {
+  constexpr int NV = VecWidth<T>::value;
+  const size_t smem =
+      sizeof(float2) * (size_t)kWarps * (a.D / 2) + sizeof(float) * (size_t)kWarps * 2 * a.D;
+  const bool rstd = a.rq != nullptr || a.rk != nullptr;
+  const void *kern =
+      warp_path ? (rstd ? (const void *)qk_norm_rope_bwd_warp<T, Idx, NV, true>
+                        : (const void *)qk_norm_rope_bwd_warp<T, Idx, NV, false>)
+                : (rstd ? (const void *)qk_norm_rope_bwd_generic<T, Idx, true>
+                        : (const void *)qk_norm_rope_bwd_generic<T, Idx, false>);
+  const int occ = blocks_per_sm(kern, kThreads, smem, dev, kMaxBlocksPerSm);
+  int64_t P = ceil_div(a.T, (int64_t)kWarps);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  if (P > a.ws_rows) P = a.ws_rows;
+  const NormRopeParams<T, Idx> k = params_of<T, Idx>(a);
+  const dim3 grid((unsigned)P), block(kThreads);
+  cudaError_t e;
+  if (warp_path)
+    e = rstd ? launch_pdl(qk_norm_rope_bwd_warp<T, Idx, NV, true>, grid, block, smem, s, k, fr)
+             : launch_pdl(qk_norm_rope_bwd_warp<T, Idx, NV, false>, grid, block, smem, s, k, fr);
+  else
+    e = rstd ? launch_pdl(qk_norm_rope_bwd_generic<T, Idx, true>, grid, block, smem, s, k, fr)
+             : launch_pdl(qk_norm_rope_bwd_generic<T, Idx, false>, grid, block, smem, s, k, fr);
+  if (e != cudaSuccess) return e;
+  // dwq from columns [0, D) of the partial rows, dwk from [D, 2D)
+  if (a.dwq) {
+    e = launch_dw_reduce(a.ws, P, a.D, 2 * (int64_t)a.D, a.dwq, s);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.dwk) {
+    e = launch_dw_reduce(a.ws + a.D, P, a.D, 2 * (int64_t)a.D, a.dwk, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t qk_norm_rope_partial_rows(int64_t T, const DeviceInfo &dev) {
+  const int64_t cap = (int64_t)dev.sms * kMaxBlocksPerSm;
+  const int64_t need = ceil_div(T, (int64_t)kWarps);
+  return need < cap ? need : cap;
+}
+
+cudaError_t launch_qk_norm_rope(DType dt, bool vec, bool wide, const QkNormRopeArgs &a,
+                                const DeviceInfo &dev, cudaStream_t s) {
+  const RopeFreqs fr = make_rope_freqs(a.D, a.theta, a.inv_freq);
+  // the warp kernels need half a head to split evenly over a power-of-two
+  // number of lanes (NV divides 32)
+  const int n = dt == DType::F32 ? VecWidth<float>::value : VecWidth<bf16>::value;
+  const int nv = vec ? a.D / 2 / n : 0;
+  const bool warp_path = vec && nv >= 1 && nv <= 32 && (nv & (nv - 1)) == 0;
+#define FTK_NR(T, Idx) \
+  return a.backward ? bwd_typed<T, Idx>(warp_path, a, fr, dev, s) : fwd_typed<T, Idx>(warp_path, a, fr, s);
+  if (dt == DType::F32) {
+    if (wide) { FTK_NR(float, int64_t) }
+    FTK_NR(float, int32_t)
+  }
+  if (wide) { FTK_NR(bf16, int64_t) }
+  FTK_NR(bf16, int32_t)
+#undef FTK_NR
+}
+
+}  // namespace ftk

@@ -39,57 +39,13 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "rope_common.cuh"
 
 namespace ftk {
 
 namespace {
 
-struct RopeFreqs {
-  float hi[kRopeMaxHalf];
-  float lo[kRopeMaxHalf];
-};
-
 constexpr int kCtaThreads = 256;
-constexpr int kCuInShared = 2048;  // cu_seqlens entries a CTA stages in shared memory
-
-__device__ __forceinline__ float frac_turns(float a) { return a - rintf(a); }
-
-// cos and sin of 2*pi*p*(fhi + flo).
-__device__ __forceinline__ void rope_cos_sin(int p, float fhi, float flo, float *c, float *s) {
-  const float ph = (float)(p & ~4095);  // exact: at most 19 significant bits
-  const float pl = (float)(p & 4095);   // exact
-  const float a1 = __fmul_rn(ph, fhi);
-  const float e1 = fmaf(ph, fhi, -a1);  // ph*fhi = a1 + e1 exactly
-  const float a2 = __fmul_rn(pl, fhi);
-  const float e2 = fmaf(pl, fhi, -a2);  // pl*fhi = a2 + e2 exactly
-  const float a3 = __fmul_rn(ph, flo);
-  const float a4 = __fmul_rn(pl, flo);
-  float r = frac_turns(a1) + frac_turns(a2);
-  r += frac_turns(a3) + frac_turns(e1);
-  r += e2 + a4;
-  r = frac_turns(r);
-  sincospif(2.0f * r, s, c);
-}
-
-// Sequence of token t: largest b < B with cu[b] <= t (zero-length sequences
-// are skipped because their boundary repeats).  Clamped to [0, B-1], so a
-// malformed cu can only give wrong positions, never a wrong address.
-// `cu` is a generic pointer: the CTA's shared-memory copy when it fits,
-// else the device array itself.
-template <typename Idx>
-__device__ __forceinline__ int position_of(Idx t, const int32_t *cu, int B) {
-  int lo = 1, hi = B;  // first i in [1, B] with cu[i] > t
-  while (lo <= hi) {
-    const int mid = (lo + hi) >> 1;
-    if ((Idx)cu[mid] <= t)
-      lo = mid + 1;
-    else
-      hi = mid - 1;
-  }
-  int b = lo - 1;
-  b = b < 0 ? 0 : (b > B - 1 ? B - 1 : b);
-  return (int)(t - (Idx)cu[b]);
-}
 
 template <typename T, typename Idx, int N, int HPT>
 __global__ void __launch_bounds__(kCtaThreads, 3)
@@ -583,22 +539,7 @@ cudaError_t rope_typed(bool vec, const RopeArgs &a, const RopeFreqs &fr, const D
 
 cudaError_t launch_qk_rope(DType dt, bool vec, bool wide, const RopeArgs &a,
                            const DeviceInfo &dev, cudaStream_t s) {
-  // f_i = inv_freq_i / (2 pi) in double, split into two floats; inv_freq_i
-  // is theta^(-2i/D), or the caller's (scaled) table.
-  RopeFreqs fr;
-  const int half = a.D / 2;
-  for (int i = 0; i < kRopeMaxHalf; ++i) {
-    if (i < half) {
-      const double inv = a.inv_freq ? a.inv_freq[i]
-                                    : std::pow(a.theta, -2.0 * (double)i / (double)a.D);
-      const double f = inv / 6.283185307179586476925;
-      const float hi = (float)f;
-      fr.hi[i] = hi;
-      fr.lo[i] = (float)(f - (double)hi);
-    } else {
-      fr.hi[i] = fr.lo[i] = 0.f;
-    }
-  }
+  const RopeFreqs fr = make_rope_freqs(a.D, a.theta, a.inv_freq);
   if (dt == DType::F32)
     return wide ? rope_typed<float, int64_t>(vec, a, fr, dev, s)
                 : rope_typed<float, int32_t>(vec, a, fr, dev, s);

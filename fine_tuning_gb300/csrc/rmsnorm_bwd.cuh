@@ -28,6 +28,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "dw_reduce.cuh"
 #include "launch.h"
 
 namespace ftk {
@@ -392,39 +393,8 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams<T, Id
   }
 }
 
-// dw[j] = sum_{p < P} ws[p, j]: a CTA owns 32 columns; its 32 warps take
-// the rows p = warp, warp + 32, ... and their sums are added in warp order.
-constexpr int kReduceWarps = 32;
-
-__global__ void __launch_bounds__(32 * kReduceWarps)
-dw_reduce(const float *__restrict__ ws, int P, int H, float *__restrict__ dw) {
-  __shared__ float part[kReduceWarps][33];
-  pdl_wait();
-  pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col = blockIdx.x * 32 + lane;
-  float s = 0.f;
-  if (col < H) {
-#pragma unroll 4
-    for (int p = warp; p < P; p += kReduceWarps) s += ws[(size_t)p * H + col];
-  }
-  part[warp][lane] = s;
-  __syncthreads();
-  if (warp == 0 && col < H) {
-    float t = 0.f;
-#pragma unroll
-    for (int i = 0; i < kReduceWarps; ++i) t += part[i][lane];
-    dw[col] = t;
-  }
-}
-
 cudaError_t launch_dw_reduce(const RmsNormBwdArgs &a, int64_t P, cudaStream_t s) {
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(dw_reduce, dim3((unsigned)ceil_div(a.H, (int64_t)32)), dim3(32 * kReduceWarps),
-                 0, s, a.ws, (int)P, (int)a.H, a.dw);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_dw_reduce(a.ws, P, a.H, a.H, a.dw, s);
 }
 
 template <typename T, typename Idx, int N, int V, bool HAS_RSTD, bool ADD>

@@ -69,6 +69,12 @@ def library() -> ctypes.CDLL:
         "ftk_qk_rope_freq_bwd": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, vp, dt,
                                       vp]),
         "ftk_rope_llama3_inv_freq": (st, [i32, f64, f64, f64, f64, f64, vp]),
+        "ftk_qk_norm_rope_fwd": (st, [vp, i64, vp, i64, vp, vp, vp, i64, vp, i64, vp, vp, vp,
+                                      i32, i64, i32, i32, i32, f64, vp, f32, dt, vp]),
+        "ftk_qk_norm_rope_bwd_workspace_bytes": (sz, [i64, i32, dt]),
+        "ftk_qk_norm_rope_bwd": (st, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp,
+                                      i64, vp, i64, vp, vp, vp, sz, vp, i32, i64, i32, i32, i32,
+                                      f64, vp, f32, dt, vp]),
         "ftk_bfd_pack": (st, [vp, i64, i32, vp, vp, vp, vp]),
         "ftk_device_status": (st, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
         "ftk_selftest_wait_timeout": (st, [i64, vp]),
@@ -347,6 +353,96 @@ def qk_rope_freq_fwd(q, k, cu_seqlens, inv_freq):
 def qk_rope_freq_bwd(dq, dk, cu_seqlens, inv_freq):
     """Backward of qk_rope_freq_fwd, in place."""
     return _rope("ftk_qk_rope_freq_bwd", dq, dk, cu_seqlens, None, inv_freq)
+
+
+def _table(inv_freq, D):
+    if inv_freq is None:
+        return None, None
+    table = np.ascontiguousarray(np.asarray(inv_freq, dtype=np.float64))
+    if table.shape != (D // 2,):
+        raise ValueError("inv_freq must hold D/2 values")
+    return table, table.ctypes.data_as(ctypes.c_void_p)
+
+
+def _cu_check(cu_seqlens):
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous int32 [B+1] device tensor")
+
+
+def qk_norm_rope_fwd(q, k, wq, wk, cu_seqlens, eps: float, theta: float = 0.0, inv_freq=None,
+                     q_out=None, k_out=None, save_rstd: bool = True, rstd_q=None, rstd_k=None):
+    """Per-head RMSNorm (weights wq, wk [D]) then RoPE of q [T, Hq, D] and
+    k [T, Hkv, D]; returns (q_out, k_out, rstd_q [T, Hq], rstd_k [T, Hkv]).
+    q_out=q / k_out=k update in place.  inv_freq (host, D/2) replaces theta.
+    rstd_q / rstd_k: fp32 buffers to write r into (else allocated when
+    save_rstd)."""
+    _cuda(q, k, wq, wk, cu_seqlens, q_out, k_out, rstd_q, rstd_k)
+    _cu_check(cu_seqlens)
+    ldq, Hq, Dq = _heads(q, "q")
+    ldk, Hkv, Dk = _heads(k, "k")
+    D = Dq or Dk
+    ref = q if q is not None else k
+    T = ref.shape[0]
+    if q is not None and q_out is None:
+        q_out = torch.empty_like(q)
+    if k is not None and k_out is None:
+        k_out = torch.empty_like(k)
+    ldqo, _, _ = _heads(q_out, "q_out")
+    ldko, _, _ = _heads(k_out, "k_out")
+    rq, rk = rstd_q, rstd_k
+    if rq is None and save_rstd and Hq:
+        rq = torch.empty((T, Hq), dtype=torch.float32, device=ref.device)
+    if rk is None and save_rstd and Hkv:
+        rk = torch.empty((T, Hkv), dtype=torch.float32, device=ref.device)
+    for r, n in ((rq, Hq), (rk, Hkv)):
+        if r is not None and (r.dtype != torch.float32 or r.numel() != T * n
+                              or not r.is_contiguous()):
+            raise ValueError("rstd buffers must be contiguous fp32 [T, heads]")
+    table, tp = _table(inv_freq, D)
+    _call("ftk_qk_norm_rope_fwd", _ptr(q), ldq, _ptr(k), ldk, _ptr(wq), _ptr(wk), _ptr(q_out),
+          ldqo, _ptr(k_out), ldko, _ptr(rq), _ptr(rk), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+          T, Hq, Hkv, D, float(theta), tp, float(eps), _code(ref), _stream(ref))
+    del table
+    return q_out, k_out, rq, rk
+
+
+def qk_norm_rope_bwd_workspace_bytes(T: int, D: int, dtype: torch.dtype) -> int:
+    return int(library().ftk_qk_norm_rope_bwd_workspace_bytes(T, D, _DTYPES[dtype]))
+
+
+def qk_norm_rope_bwd(dq_out, dk_out, q, k, wq, wk, rstd_q, rstd_k, cu_seqlens, eps: float,
+                     theta: float = 0.0, inv_freq=None, dq=None, dk=None, workspace=None):
+    """Backward of qk_norm_rope_fwd from the output gradients and the
+    PRE-norm q, k; returns (dq, dk, dwq [D] fp32, dwk [D] fp32).  dq=dq_out
+    (dk=dk_out) writes in place.  rstd_q/rstd_k None: recomputed."""
+    _cuda(dq_out, dk_out, q, k, wq, wk, rstd_q, rstd_k, cu_seqlens, dq, dk, workspace)
+    _cu_check(cu_seqlens)
+    ldq, Hq, Dq = _heads(q, "q")
+    ldk, Hkv, Dk = _heads(k, "k")
+    D = Dq or Dk
+    ref = q if q is not None else k
+    T = ref.shape[0]
+    if q is not None and dq is None:
+        dq = torch.empty_like(q)
+    if k is not None and dk is None:
+        dk = torch.empty_like(k)
+    ldgq, _, _ = _heads(dq_out, "dq_out")
+    ldgk, _, _ = _heads(dk_out, "dk_out")
+    lddq, _, _ = _heads(dq, "dq")
+    lddk, _, _ = _heads(dk, "dk")
+    dwq = torch.empty(D, dtype=torch.float32, device=ref.device) if Hq else None
+    dwk = torch.empty(D, dtype=torch.float32, device=ref.device) if Hkv else None
+    if workspace is None:
+        nbytes = max(16, qk_norm_rope_bwd_workspace_bytes(T, D, ref.dtype))
+        workspace = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=ref.device)
+    table, tp = _table(inv_freq, D)
+    _call("ftk_qk_norm_rope_bwd", _ptr(dq_out), ldgq, _ptr(dk_out), ldgk, _ptr(q), ldq, _ptr(k),
+          ldk, _ptr(wq), _ptr(wk), _ptr(rstd_q), _ptr(rstd_k), _ptr(dq), lddq, _ptr(dk), lddk,
+          _ptr(dwq), _ptr(dwk), _ptr(workspace), workspace.numel() * workspace.element_size(),
+          _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, Hq, Hkv, D, float(theta), tp, float(eps),
+          _code(ref), _stream(ref))
+    del table
+    return dq, dk, dwq, dwk
 
 
 def rope_llama3_inv_freq(D: int, theta: float, factor: float, low_freq_factor: float,

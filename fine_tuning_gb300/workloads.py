@@ -29,7 +29,8 @@ from typing import Dict, Optional, Sequence
 import numpy as np
 import torch
 
-TENSOR_SLOTS = ("x", "w", "dy", "g", "u", "dh", "q", "k", "dq", "dk", "res", "dres")
+TENSOR_SLOTS = ("x", "w", "dy", "g", "u", "dh", "q", "k", "dq", "dk", "res", "dres", "wq",
+                "wk")
 
 
 @dataclasses.dataclass(frozen=True)
@@ -154,6 +155,15 @@ def rmsnorm_add_inputs(wl: Workload, device="cpu", T: Optional[int] = None):
     return d
 
 
+def qk_norm_rope_inputs(wl: Workload, device="cpu", T: Optional[int] = None):
+    """q, k, dq, dk as for RoPE plus the per-head norm weights wq, wk
+    (1 + 0.1 N(0,1), D each)."""
+    d = rope_inputs(wl, device, T)
+    d["wq"] = draw(wl, "wq", (wl.D,), device, mean=1.0, std=0.1)
+    d["wk"] = draw(wl, "wk", (wl.D,), device, mean=1.0, std=0.1)
+    return d
+
+
 def swiglu_inputs(wl: Workload, device="cpu", T: Optional[int] = None):
     T = wl.T_swiglu if T is None else T
     return {
@@ -194,6 +204,11 @@ def ideal_bytes(wl: Workload) -> Dict[str, int]:
         "swiglu_bwd_h": 6 * e * Ts * I,
         # RoPE with a caller's (llama3-scaled) frequency table: same bytes
         "qk_rope_freq_fwd": rope,
+        # per-head QK-RMSNorm fused into RoPE: q, k in, out written, r per
+        # (token, head) saved; backward: output grads and pre-norm q, k in,
+        # grads out, r read
+        "qk_norm_rope_fwd": rope + 4 * T * (wl.Hq + wl.Hkv) + 2 * e * wl.D,
+        "qk_norm_rope_bwd": 3 * rope // 2 + 4 * T * (wl.Hq + wl.Hkv) + 2 * e * wl.D + 8 * wl.D,
     }
 
 
@@ -203,5 +218,5 @@ def tokens_per_call(wl: Workload) -> Dict[str, int]:
         "swiglu_fwd": wl.T_swiglu, "swiglu_bwd": wl.T_swiglu,
         "qk_rope_fwd": wl.T, "qk_rope_bwd": wl.T,
         "rmsnorm_add_fwd": wl.T, "rmsnorm_add_bwd": wl.T, "swiglu_bwd_h": wl.T_swiglu,
-        "qk_rope_freq_fwd": wl.T,
+        "qk_rope_freq_fwd": wl.T, "qk_norm_rope_fwd": wl.T, "qk_norm_rope_bwd": wl.T,
     }

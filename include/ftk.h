@@ -267,6 +267,63 @@ FTK_API ftk_status ftk_rope_llama3_inv_freq(int32_t D, double theta, double fact
                                             double low_freq_factor, double high_freq_factor,
                                             double original_max_position, double *inv_freq);
 
+/* ------------------------------------- QK-RMSNorm fused into the QK-RoPE */
+
+/* Per-head RMSNorm of Q and K (the q_norm / k_norm of Qwen3-style attention)
+ * followed by the rotation of ftk_qk_rope_fwd, in one pass over Q and K.
+ * The pages fuse the QK-RoPE (the fused QK RoPE paragraph of the Unsloth
+ * item on seventnews.com; "Chronicals", arXiv 2601.02609, abstract,
+ * optimisation (1)); the norm in front of it is this library's variant.
+ * For token t at position p (as in ftk_qk_rope_fwd) and every head vector v
+ * of D values of Q (weight wq) or K (weight wk):
+ *   r[t,h] = 1 / sqrt( (1/D) sum_i v_i^2 + eps )
+ *   n_i    = v_i r w_i                    (fp32; not rounded)
+ *   out    = n rotated by phi_i = p * inv_freq_i (rotate-half pairs)
+ * inv_freq: HOST double [D/2] (entries in [0, 1]), or NULL for
+ * theta^(-2i/D).  q [T, ld_q] of Hq heads, k [T, ld_k] of Hkv heads;
+ * q_out [T, ld_qo], k_out [T, ld_ko]: each may BE its input (same pointer and
+ * stride) for an in-place update, but then the backward needs a copy of the
+ * pre-norm values.  wq, wk: [D] (dtype).  rstd_q [T, Hq], rstd_k [T, Hkv]:
+ * fp32 contiguous, nullable, receive r.  q, wq, q_out may be NULL when
+ * Hq == 0, and the k arguments when Hkv == 0.  cu_seqlens, B, T, D (even, <=
+ * 512) as in ftk_qk_rope_fwd; eps >= 0. */
+FTK_API ftk_status ftk_qk_norm_rope_fwd(const void *q, int64_t ld_q, const void *k, int64_t ld_k,
+                                        const void *wq, const void *wk, void *q_out,
+                                        int64_t ld_qo, void *k_out, int64_t ld_ko,
+                                        float *rstd_q, float *rstd_k,
+                                        const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                        int32_t Hq, int32_t Hkv, int32_t D, double theta,
+                                        const double *inv_freq, float eps, ftk_dtype dtype,
+                                        ftk_stream_t stream);
+
+/* Bytes of device workspace ftk_qk_norm_rope_bwd needs for T tokens and
+ * head dimension D on the CURRENT device; 0 for invalid arguments. */
+FTK_API size_t ftk_qk_norm_rope_bwd_workspace_bytes(int64_t T, int32_t D, ftk_dtype dtype);
+
+/* Backward of ftk_qk_norm_rope_fwd.  From the output gradients dq_out,
+ * dk_out and the PRE-norm q, k:
+ *   dn     = dq_out (or dk_out) rotated by -phi (the transpose)
+ *   c      = sum_i dn_i w_i v_i
+ *   dq     = r w dn - r^3 v c / D             (likewise dk)
+ *   dwq[i] = sum over tokens and Q heads of dn_i v_i r   (fp32, OVERWRITTEN;
+ *            dwk likewise over K heads)
+ * rstd_q/rstd_k from the forward, or both NULL to recompute r from v and
+ * eps.  dq [T, ld_dq] may be dq_out itself (same pointer and stride), dk
+ * likewise; no other output may overlap anything.  workspace: >=
+ * ftk_qk_norm_rope_bwd_workspace_bytes(T, D, dtype) bytes, 16-byte aligned.
+ * dwq and dwk are sums of per-CTA fp32 partials added in a fixed order:
+ * bitwise reproducible run to run.  Other rules as in the forward. */
+FTK_API ftk_status ftk_qk_norm_rope_bwd(const void *dq_out, int64_t ld_gq, const void *dk_out,
+                                        int64_t ld_gk, const void *q, int64_t ld_q,
+                                        const void *k, int64_t ld_k, const void *wq,
+                                        const void *wk, const float *rstd_q,
+                                        const float *rstd_k, void *dq, int64_t ld_dq, void *dk,
+                                        int64_t ld_dk, float *dwq, float *dwk, void *workspace,
+                                        size_t workspace_bytes, const int32_t *cu_seqlens,
+                                        int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D,
+                                        double theta, const double *inv_freq, float eps,
+                                        ftk_dtype dtype, ftk_stream_t stream);
+
 /* -------------------------------------------------------------- packing */
 
 /* Best-Fit-Decreasing packing of n sequences into bins of `capacity` tokens
