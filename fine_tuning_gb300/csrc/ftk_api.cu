@@ -668,4 +668,124 @@ FTK_API ftk_status ftk_qk_norm_rope_bwd(const void *dq_out, int64_t ld_gq, const
   return finish(ftk::launch_qk_norm_rope(dt, vec, wide, a, dev, (cudaStream_t)stream));
 }
 
+// ------------------------------------------------------ tensor-core GEMM
+
+FTK_API ftk_status ftk_gemm_bf16(const void *a, int64_t lda, const void *b, int64_t ldb,
+                                 float *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                 ftk_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < N || M >= (int64_t(1) << 31) ||
+      N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+    return FTK_ERR_SHAPE;
+  if (M == 0 || N == 0) return FTK_OK;
+  if (!a || !b || !c) return FTK_ERR_NULL;
+  if (K > 0 && (!aligned(a, 16) || !aligned(b, 16) || lda % 8 != 0 || ldb % 8 != 0))
+    return FTK_ERR_ALIGN;
+  if (!aligned(c, 4)) return FTK_ERR_ALIGN;
+  if (K == 0) return FTK_ERR_SHAPE;  // an empty contraction has nothing to run on
+  const View va = view(a, M, lda, K, 2), vb = view(b, N, ldb, K, 2), vc = view(c, M, ldc, N, 4);
+  if (may_overlap(vc, va) || may_overlap(vc, vb)) return FTK_ERR_ALIAS;
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return finish(ftk::launch_gemm_bf16(a, lda, b, ldb, c, ldc, M, N, K, dev, (cudaStream_t)stream));
+}
+
+// ------------------------------------------------------ Cut Cross-Entropy
+
+FTK_API size_t ftk_cce_fwd_workspace_bytes(int64_t T, int64_t V) {
+  if (T <= 0 || V <= 0) return 0;
+  return ftk::cce_fwd_workspace_bytes(T, V);
+}
+
+FTK_API size_t ftk_cce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
+  if (T <= 0 || H <= 0 || V <= 0) return 0;
+  return ftk::cce_bwd_workspace_bytes(T, H, V);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the CCE forward and backward: shapes, the TMA rules on
+// h and W (16-byte aligned bases, row strides a multiple of 8 elements), y.
+ftk_status cce_common(const void *h, int64_t ldh, const void *w, int64_t ldw, const int32_t *y,
+                      int64_t T, int64_t H, int64_t V, ftk_dtype dtype) {
+  if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
+  if (dtype != FTK_BF16) return FTK_ERR_DTYPE;  // the tensor-core path is bf16
+  if (T < 0 || H < 1 || V < 1 || ldh < H || ldw < H || T >= (int64_t(1) << 31) ||
+      V >= (int64_t(1) << 31) || H >= (int64_t(1) << 31))
+    return FTK_ERR_SHAPE;
+  if (T == 0) return FTK_OK;
+  if (!h || !w || !y) return FTK_ERR_NULL;
+  if (!aligned(h, 16) || !aligned(w, 16) || ldh % 8 != 0 || ldw % 8 != 0 || !aligned(y, 4))
+    return FTK_ERR_ALIGN;
+  return FTK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+FTK_API ftk_status ftk_cce_fwd(const void *h, int64_t ldh, const void *w, int64_t ldw,
+                               const int32_t *y, int64_t T, int64_t H, int64_t V, float *loss,
+                               float *lse, void *workspace, size_t workspace_bytes,
+                               ftk_dtype dtype, ftk_stream_t stream) {
+  ftk_status st = cce_common(h, ldh, w, ldw, y, T, H, V, dtype);
+  if (st != FTK_OK || T == 0) return st;
+  if (!loss || !lse) return FTK_ERR_NULL;
+  if (!workspace || workspace_bytes < ftk::cce_fwd_workspace_bytes(T, V))
+    return FTK_ERR_WORKSPACE;
+  if (!aligned(loss, 4) || !aligned(lse, 4) || !aligned(workspace, 256)) return FTK_ERR_ALIGN;
+  const View vh = view(h, T, ldh, H, 2), vw = view(w, V, ldw, H, 2), vy = view(y, 1, T, T, 4);
+  const View vl = view(loss, 1, 1, 1, 4), vs = view(lse, 1, T, T, 4);
+  const View vws = view(workspace, 1, (int64_t)workspace_bytes, (int64_t)workspace_bytes, 1);
+  const View outs[3] = {vl, vs, vws}, ins[3] = {vh, vw, vy};
+  for (int i = 0; i < 3; ++i) {
+    for (int m = 0; m < 3; ++m)
+      if (may_overlap(outs[i], ins[m])) return FTK_ERR_ALIAS;
+    for (int m = i + 1; m < 3; ++m)
+      if (may_overlap(outs[i], outs[m])) return FTK_ERR_ALIAS;
+  }
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ftk::CceArgs a{h, ldh, w, ldw, y, T, H, V, loss, lse, nullptr, nullptr, 0, nullptr, 0,
+                 workspace};
+  return finish(ftk::launch_cce_fwd(a, dev, (cudaStream_t)stream));
+}
+
+FTK_API ftk_status ftk_cce_bwd(const void *h, int64_t ldh, const void *w, int64_t ldw,
+                               const int32_t *y, const float *lse, const float *dloss,
+                               int64_t T, int64_t H, int64_t V, void *dh, int64_t lddh,
+                               float *dw, int64_t lddw, void *workspace,
+                               size_t workspace_bytes, ftk_dtype dtype, ftk_stream_t stream) {
+  ftk_status st = cce_common(h, ldh, w, ldw, y, T, H, V, dtype);
+  if (st != FTK_OK) return st;
+  if (lddh < H || lddw < H) return FTK_ERR_SHAPE;
+  if (T == 0) return FTK_OK;
+  if (!lse || !dloss || !dh || !dw) return FTK_ERR_NULL;
+  if (!workspace || workspace_bytes < ftk::cce_bwd_workspace_bytes(T, H, V))
+    return FTK_ERR_WORKSPACE;
+  if (!aligned(lse, 4) || !aligned(dloss, 4) || !aligned(dh, 2) || !aligned(dw, 4) ||
+      !aligned(workspace, 256))
+    return FTK_ERR_ALIGN;
+  const View vh = view(h, T, ldh, H, 2), vw = view(w, V, ldw, H, 2), vy = view(y, 1, T, T, 4);
+  const View vs = view(lse, 1, T, T, 4), vg = view(dloss, 1, 1, 1, 4);
+  const View vdh = view(dh, T, lddh, H, 2), vdw = view(dw, V, lddw, H, 4);
+  const View vws = view(workspace, 1, (int64_t)workspace_bytes, (int64_t)workspace_bytes, 1);
+  const View outs[3] = {vdh, vdw, vws}, ins[5] = {vh, vw, vy, vs, vg};
+  for (int i = 0; i < 3; ++i) {
+    for (int m = 0; m < 5; ++m)
+      if (may_overlap(outs[i], ins[m])) return FTK_ERR_ALIAS;
+    for (int m = i + 1; m < 3; ++m)
+      if (may_overlap(outs[i], outs[m])) return FTK_ERR_ALIAS;
+  }
+  ftk::DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ftk::CceArgs a{h, ldh, w, ldw, y, T, H, V, nullptr, (float *)lse, dloss, dh, lddh, dw, lddw,
+                 workspace};
+  return finish(ftk::launch_cce_bwd(a, dev, (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -206,4 +206,32 @@ int64_t qk_norm_rope_partial_rows(int64_t T, const DeviceInfo &dev);
 cudaError_t launch_qk_norm_rope(DType dt, bool vec, bool wide, const QkNormRopeArgs &a,
                                 const DeviceInfo &dev, cudaStream_t s);
 
+// Cross-entropy of the LM head (cce.cu).  bf16 h [T, ldh], W [V, ldw];
+// y int32 [T] (valid when 0 <= y < V).  Forward: loss (1 float) and lse [T].
+// Backward: dloss (1 float, device) in, dh bf16 [T, lddh] and dW fp32
+// [V, lddw] out.  ws: the workspace of the matching *_workspace_bytes.
+struct CceArgs {
+  const void *h;
+  int64_t ldh;
+  const void *w;
+  int64_t ldw;
+  const int32_t *y;
+  int64_t T, H, V;
+  float *loss, *lse;
+  const float *dloss;
+  void *dh;
+  int64_t lddh;
+  float *dw;
+  int64_t lddw;
+  void *ws;
+};
+size_t cce_fwd_workspace_bytes(int64_t T, int64_t V);
+size_t cce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V);
+cudaError_t launch_cce_fwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t s);
+cudaError_t launch_cce_bwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t s);
+// C fp32 [M, ldc] = A [M, lda] B [N, ldb]^T on the tensor cores (bf16, tc_gemm.cuh).
+cudaError_t launch_gemm_bf16(const void *a, int64_t lda, const void *b, int64_t ldb, float *c,
+                             int64_t ldc, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
+                             cudaStream_t s);
+
 }  // namespace ftk

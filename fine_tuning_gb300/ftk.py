@@ -75,6 +75,12 @@ def library() -> ctypes.CDLL:
         "ftk_qk_norm_rope_bwd": (st, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp,
                                       i64, vp, i64, vp, vp, vp, sz, vp, i32, i64, i32, i32, i32,
                                       f64, vp, f32, dt, vp]),
+        "ftk_gemm_bf16": (st, [vp, i64, vp, i64, vp, i64, i64, i64, i64, vp]),
+        "ftk_cce_fwd_workspace_bytes": (sz, [i64, i64]),
+        "ftk_cce_bwd_workspace_bytes": (sz, [i64, i64, i64]),
+        "ftk_cce_fwd": (st, [vp, i64, vp, i64, vp, i64, i64, i64, vp, vp, vp, sz, dt, vp]),
+        "ftk_cce_bwd": (st, [vp, i64, vp, i64, vp, vp, vp, i64, i64, i64, vp, i64, vp, i64, vp,
+                             sz, dt, vp]),
         "ftk_bfd_pack": (st, [vp, i64, i32, vp, vp, vp, vp]),
         "ftk_device_status": (st, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
         "ftk_selftest_wait_timeout": (st, [i64, vp]),
@@ -453,6 +459,65 @@ def rope_llama3_inv_freq(D: int, theta: float, factor: float, low_freq_factor: f
           float(high_freq_factor), float(original_max_position),
           out.ctypes.data_as(ctypes.c_void_p))
     return out
+
+
+# ------------------------------------------------------ Cut Cross-Entropy
+
+def gemm_bf16(a: torch.Tensor, b: torch.Tensor, c: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """C fp32 [M, N] = a [M, K] @ b [N, K]^T on the tensor cores (bf16 in)."""
+    _cuda(a, b, c)
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K or a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+        raise ValueError("a [M, K] and b [N, K] must be bf16")
+    c = torch.empty((M, N), dtype=torch.float32, device=a.device) if c is None else c
+    _call("ftk_gemm_bf16", _ptr(a), _rows(a, "a"), _ptr(b), _rows(b, "b"), _ptr(c),
+          _rows(c, "c"), M, N, K, _stream(a))
+    return c
+
+
+def _ws(nbytes: int, like: torch.Tensor) -> torch.Tensor:
+    return torch.empty(max(256, nbytes), dtype=torch.uint8, device=like.device)
+
+
+def cce_fwd(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, loss=None, lse=None,
+            workspace=None):
+    """Mean cross-entropy of logits h W^T against y (int32; y outside [0, V)
+    is ignored), without materialising the logits.  Returns (loss [1] fp32,
+    lse [T] fp32), both on the device."""
+    _cuda(h, W, y, loss, lse, workspace)
+    T, H = h.shape
+    V = W.shape[0]
+    if W.shape[1] != H or h.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise ValueError("h [T, H] and W [V, H] must be bf16")
+    if y.dtype != torch.int32 or y.numel() != T or not y.is_contiguous():
+        raise ValueError("y must be a contiguous int32 [T] tensor")
+    loss = torch.empty(1, dtype=torch.float32, device=h.device) if loss is None else loss
+    lse = torch.empty(T, dtype=torch.float32, device=h.device) if lse is None else lse
+    if workspace is None:
+        workspace = _ws(int(library().ftk_cce_fwd_workspace_bytes(T, V)), h)
+    _call("ftk_cce_fwd", _ptr(h), _rows(h, "h"), _ptr(W), _rows(W, "W"), _ptr(y), T, H, V,
+          _ptr(loss), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+          _code(h), _stream(h))
+    return loss, lse
+
+
+def cce_bwd(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, lse: torch.Tensor,
+            dloss: torch.Tensor, dh=None, dW=None, workspace=None):
+    """Gradients of dloss * cce_fwd(h, W, y): (dh bf16 [T, H], dW fp32 [V, H])."""
+    _cuda(h, W, y, lse, dloss, dh, dW, workspace)
+    T, H = h.shape
+    V = W.shape[0]
+    dh = torch.empty_like(h) if dh is None else dh
+    dW = torch.empty((V, H), dtype=torch.float32, device=h.device) if dW is None else dW
+    if dloss.dtype != torch.float32 or dloss.numel() != 1:
+        raise ValueError("dloss must be one fp32 value on the device")
+    if workspace is None:
+        workspace = _ws(int(library().ftk_cce_bwd_workspace_bytes(T, H, V)), h)
+    _call("ftk_cce_bwd", _ptr(h), _rows(h, "h"), _ptr(W), _rows(W, "W"), _ptr(y), _ptr(lse),
+          _ptr(dloss), T, H, V, _ptr(dh), _rows(dh, "dh"), _ptr(dW), _rows(dW, "dW"),
+          _ptr(workspace), workspace.numel() * workspace.element_size(), _code(h), _stream(h))
+    return dh, dW
 
 
 # ---------------------------------------------------------------- packing

@@ -220,3 +220,41 @@ def tokens_per_call(wl: Workload) -> Dict[str, int]:
         "rmsnorm_add_fwd": wl.T, "rmsnorm_add_bwd": wl.T, "swiglu_bwd_h": wl.T_swiglu,
         "qk_rope_freq_fwd": wl.T, "qk_norm_rope_fwd": wl.T, "qk_norm_rope_bwd": wl.T,
     }
+
+
+# ------------------------------------------------------------ LM-head loss
+
+@dataclasses.dataclass(frozen=True)
+class HeadWorkload:
+    """The cross-entropy of an LM head: T tokens of hidden size H against a
+    vocabulary of V rows.  h ~ N(0, 1); W ~ N(0, w_std^2) (w_std 0.02, the
+    usual LM-head initialisation, keeps the logits near N(0, 0.6^2) at
+    H = 896); targets uniform over the vocabulary, a share of them ignored
+    (y = -100) as padding would be."""
+    name: str
+    T: int
+    H: int
+    V: int
+    seed: int
+    w_std: float = 0.02
+    ignored: float = 0.05
+
+
+HEAD_WORKLOADS = {w.name: w for w in (
+    HeadWorkload("tiny-head", T=300, H=64, V=1000, seed=11, w_std=0.125),
+    # Qwen2.5-0.5B's head (hidden 896, vocabulary 151,936) on 8,192 tokens:
+    # the run whose fp32 logits the page puts at 5 GB
+    HeadWorkload("qwen2.5-0.5b-head", T=8192, H=896, V=151936, seed=12),
+)}
+
+
+def head_inputs(hw: HeadWorkload, device="cpu"):
+    g = torch.Generator(device=device)
+    g.manual_seed(hw.seed * 1000 + 1)
+    h = torch.randn((hw.T, hw.H), generator=g, device=device).to(torch.bfloat16)
+    W = (hw.w_std * torch.randn((hw.V, hw.H), generator=g, device=device)).to(torch.bfloat16)
+    y = torch.randint(0, hw.V, (hw.T,), generator=g, device=device, dtype=torch.int64)
+    drop = torch.rand((hw.T,), generator=g, device=device) < hw.ignored
+    y = torch.where(drop, torch.full_like(y, -100), y).to(torch.int32)
+    return {"h": h, "W": W, "y": y}
+

@@ -324,6 +324,58 @@ FTK_API ftk_status ftk_qk_norm_rope_bwd(const void *dq_out, int64_t ld_gq, const
                                         double theta, const double *inv_freq, float eps,
                                         ftk_dtype dtype, ftk_stream_t stream);
 
+/* ------------------------------------------------------ tensor-core GEMM */
+
+/* C = A B^T on the 5th-generation tensor cores: A bf16 [M, lda], B bf16
+ * [N, ldb] (both K contiguous), C fp32 [M, ldc] (overwritten), fp32
+ * accumulation in tensor memory.  The contraction the cross-entropy calls
+ * below are built on, exposed for reuse and testing; the pages have no
+ * counterpart.  A and B 16-byte aligned with lda, ldb multiples of 8;
+ * K >= 1 (FTK_ERR_SHAPE for K = 0 with M, N > 0); C must not overlap A or B. */
+FTK_API ftk_status ftk_gemm_bf16(const void *a, int64_t lda, const void *b, int64_t ldb,
+                                 float *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                 ftk_stream_t stream);
+
+/* ---------------------------------------------------- Cut Cross-Entropy */
+
+/* Cross-entropy loss of a linear LM head without materialised logits
+ * ("Chronicals", arXiv 2601.02609, abstract, optimisation (2): Cut
+ * Cross-Entropy, an online softmax that keeps the [T, V] logits out of
+ * memory, 5 GB down to 135 MB for its run):
+ *   z[t,v] = sum_j h[t,j] W[v,j]        (bf16 operands, fp32 accumulation)
+ *   lse[t] = log sum_v exp(z[t,v])
+ *   loss   = (1/N) sum_{valid t} (lse[t] - z[t, y_t]),  N = #valid tokens
+ * A token is valid when 0 <= y[t] < V (so -100, or any negative value, marks
+ * one to ignore); N = 0 gives loss 0.  bf16 only (FTK_ERR_DTYPE otherwise):
+ * the contraction runs on the tensor cores (tcgen05).
+ * h [T, ldh] and W [V, ldw] (bf16, 16-byte aligned, ldh and ldw multiples of
+ * 8); y int32 [T]; loss: ONE fp32 on the device; lse fp32 [T] (keep it for
+ * the backward).  workspace: >= ftk_cce_fwd_workspace_bytes(T, V) bytes,
+ * 256-byte aligned.  No output may overlap an input or another output.  The
+ * loss is summed in a fixed order: bitwise reproducible run to run. */
+FTK_API size_t ftk_cce_fwd_workspace_bytes(int64_t T, int64_t V);
+FTK_API ftk_status ftk_cce_fwd(const void *h, int64_t ldh, const void *w, int64_t ldw,
+                               const int32_t *y, int64_t T, int64_t H, int64_t V, float *loss,
+                               float *lse, void *workspace, size_t workspace_bytes,
+                               ftk_dtype dtype, ftk_stream_t stream);
+
+/* Backward of ftk_cce_fwd for an upstream gradient g of the loss (dloss:
+ * ONE fp32 on the device):
+ *   dz[t,v] = (g/N) (softmax(z[t])_v - [v == y_t])   (valid t; 0 otherwise)
+ *   dh = dz W  -> bf16 [T, lddh],     dW = dz^T h  -> fp32 [V, lddw]
+ * dz is rounded to bf16 before the two contractions (the tensor cores take
+ * bf16 operands); they accumulate in fp32.  The logits are recomputed a
+ * vocabulary chunk of 4,096 columns at a time.  lse from the forward.
+ * workspace: >= ftk_cce_bwd_workspace_bytes(T, H, V) bytes, 256-byte
+ * aligned.  dh and dW are overwritten; no output may overlap an input or
+ * another output. */
+FTK_API size_t ftk_cce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V);
+FTK_API ftk_status ftk_cce_bwd(const void *h, int64_t ldh, const void *w, int64_t ldw,
+                               const int32_t *y, const float *lse, const float *dloss,
+                               int64_t T, int64_t H, int64_t V, void *dh, int64_t lddh,
+                               float *dw, int64_t lddw, void *workspace,
+                               size_t workspace_bytes, ftk_dtype dtype, ftk_stream_t stream);
+
 /* -------------------------------------------------------------- packing */
 
 /* Best-Fit-Decreasing packing of n sequences into bins of `capacity` tokens

@@ -64,14 +64,14 @@ def lse_and_target(h, W, y, ignore_index=-100, tok=None, chunk=256):
     return lse, zy
 
 
-def cce_fwd(h, W, y, ignore_index=-100):
-    """Returns (loss, lse [T], n_valid)."""
+def cce_fwd(h, W, y, ignore_index=-100, with_target=False):
+    """Returns (loss, lse [T], n_valid), and z[t, y_t] [T] with_target."""
     y = _ints(y)
     lse, zy = lse_and_target(h, W, y, ignore_index)
     valid = y != ignore_index
     n = int(valid.sum())
     loss = float((lse[valid] - zy[valid]).sum() / n) if n else 0.0
-    return loss, lse, n
+    return (loss, lse, n, zy) if with_target else (loss, lse, n)
 
 
 def dz_rows(h, W, y, g, n_valid, ignore_index=-100, tok=None, chunk=256):
