@@ -36,6 +36,7 @@ METRIC = "achieved HBM GB/s (% of GB300 peak) and tokens/s per fused fwd+bwd ker
 OPS = ("rmsnorm_fwd", "swiglu_fwd", "qk_rope_fwd", "qk_rope_bwd", "swiglu_bwd", "rmsnorm_bwd")
 LAUNCHES_PER_STEP = 7  # rmsnorm_bwd is two kernels (rows + fixed-order dw reduction)
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -49,6 +50,7 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-ext", action="store_true", help="skip timing the widened ops")
+    p.add_argument("--no-cce", action="store_true", help="skip the LM-head cross-entropy leg")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU work of the oracle baseline sample")
@@ -86,6 +88,16 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 TFLOP/s for a kernel timed on its own (the burst figure)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 _ROPE = ("qk_rope.cu", "rope_common.cuh")
@@ -496,6 +508,9 @@ def run_ours(args):
     }
     if not args.no_ext:
         out["extensions"] = ext_leg(batch, flush, flush_graph, dev, Kk, hbm, src)
+        if rank == 0 and not args.no_cce:
+            out["cce"] = cce_leg(dev, flush, flush_graph, max(3, min(Kk, 20)))
+            out["gpu_launches"] += out["cce"].pop("launches")
         out["gpu_launches"] += sum(EXT_OPS.values()) * Kk
     out["clocks"] = sampler.summary(t0, t1)
     out["device_status"] = ftk.device_status(clear=True)  # 0: no pipeline wait ran out
@@ -590,6 +605,71 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
     out["timing"] = (f"{reps} replays of a graph [L2 flush, op] minus a graph [L2 flush], "
                      "CUDA events around each; outside the step's timed region")
     del h, y, rstd, dx, dw, res, dres, extra, qo, ko, rq, rk, nr_ws
+    return out
+
+
+def cce_leg(dev, flush, flush_graph, reps):
+    """The LM-head cross-entropy (a second workload, tensor-core bound):
+    Qwen2.5-0.5B's head on 8,192 tokens, forward and backward each captured
+    as a graph [L2 flush, op] and timed against the graph [L2 flush]."""
+    import torch
+
+    from fine_tuning_gb300 import ftk
+    from fine_tuning_gb300 import workloads as W
+    hw = W.HEAD_WORKLOADS["qwen2.5-0.5b-head"]
+    d = W.head_inputs(hw, dev)
+    h, Wt, y = d["h"], d["W"], d["y"]
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(hw.T, dtype=torch.float32, device=dev)
+    g = torch.ones(1, dtype=torch.float32, device=dev)
+    dh = torch.empty_like(h)
+    dW = torch.empty((hw.V, hw.H), dtype=torch.float32, device=dev)
+    wsf = torch.empty(int(ftk.library().ftk_cce_fwd_workspace_bytes(hw.T, hw.V)),
+                      dtype=torch.uint8, device=dev)
+    wsb = torch.empty(int(ftk.library().ftk_cce_bwd_workspace_bytes(hw.T, hw.H, hw.V)),
+                      dtype=torch.uint8, device=dev)
+    ops = {"cce_fwd": lambda: ftk.cce_fwd(h, Wt, y, loss=loss, lse=lse, workspace=wsf),
+           "cce_bwd": lambda: ftk.cce_bwd(h, Wt, y, lse, g, dh=dh, dW=dW, workspace=wsb)}
+    for op in ops.values():
+        op()
+    graphs = {}
+    for name, op in ops.items():
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            flush.fill_(9)
+            op()
+        graphs[name] = gr
+    for gr in graphs.values():
+        gr.replay()
+    torch.cuda.synchronize(dev)
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)] for n in list(graphs) + ["flush"]}
+    for k in range(reps):
+        for n, gr in list(graphs.items()) + [("flush", flush_graph)]:
+            a, b = ev[n][k]
+            a.record()
+            gr.replay()
+            b.record()
+    torch.cuda.synchronize(dev)
+    t_flush = sum(a.elapsed_time(b) for a, b in ev["flush"]) / reps
+    peak, psrc = tensor_peak()
+    flops = {"cce_fwd": 2 * hw.T * hw.H * hw.V, "cce_bwd": 6 * hw.T * hw.H * hw.V}
+    nchunk = -(-hw.V // 4096)
+    launches = {"cce_fwd": 3, "cce_bwd": 2 + 4 * nchunk}
+    out = {"workload": {"name": hw.name, "T": hw.T, "H": hw.H, "V": hw.V,
+                        "ignored_share": hw.ignored},
+           "loss": round(float(loss.item()), 6)}
+    for n in graphs:
+        ms = sum(a.elapsed_time(b) for a, b in ev[n]) / reps - t_flush
+        tf = flops[n] / (ms * 1e-3) / 1e12
+        out[n] = {"ms": round(ms, 4), "TFLOP_s": round(tf, 1), "algorithmic_flops": flops[n],
+                  "tokens_per_s": round(hw.T / (ms * 1e-3), 1),
+                  "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+                               "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                               "peak_source": f"{psrc} bf16 dense (burst)"}}
+    out["launches"] = (launches["cce_fwd"] + launches["cce_bwd"]) * reps
+    out["timing"] = (f"{reps} replays of a graph [L2 flush, op] minus a graph [L2 flush], "
+                     "CUDA events around each; outside the step's timed region")
     return out
 
 
