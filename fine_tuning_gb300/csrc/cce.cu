@@ -59,12 +59,21 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------ epilogues
 
-// Forward: per-row (max, sum e^(z - max)) over the tile's columns < V, and
-// the target logit when the tile holds it.
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22, 2^-inf = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Forward: per-row (max, sum e^(z - max)) over a half tile's columns < V,
+// and the target logit when the slice holds it.  part holds 2 partials per
+// row per tile (one per column half).
 struct EpiLse {
   const int32_t *y;
-  int T, V, ntn;
-  float2 *part;  // [T][ntn]
+  int T, V, nparts;
+  float2 *part;  // [T][nparts]
   float *tgt;    // [T]
   struct Row {
     float m, s;
@@ -76,29 +85,48 @@ struct EpiLse {
     r.y = m < T ? y[m] : -1;
   }
   __device__ void slice(Row &r, int m, int n, const float (&x)[32]) const {
-    float cm = -INFINITY, zt = 0.f;
-    bool hit = false;
+    if ((unsigned)(r.y - n) < 32u && m < T) {  // the target logit is in this slice
+      float zt = 0.f;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      if (n + e < V) cm = fmaxf(cm, x[e]);
-      if (n + e == r.y) {
-        zt = x[e];
-        hit = true;
-      }
+      for (int e = 0; e < 32; ++e) zt = (e == r.y - n) ? x[e] : zt;
+      tgt[m] = zt;
     }
-    if (hit && m < T) tgt[m] = zt;
-    if (cm == -INFINITY) return;  // every column past V
+    const bool full = n + 32 <= V;
+    float cm;
+    if (full) {
+      float t[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) t[e] = fmaxf(x[e], x[e + 16]);
+#pragma unroll
+      for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+      cm = t[0];
+    } else {
+      cm = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (n + e < V) cm = fmaxf(cm, x[e]);
+      if (cm == -INFINITY) return;  // every column past V
+    }
     if (cm > r.m) {
-      r.s *= exp2f((r.m - cm) * kLog2e);
+      r.s *= ex2((r.m - cm) * kLog2e);
       r.m = cm;
     }
     const float ml = r.m * kLog2e;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (full) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e)
-      if (n + e < V) r.s += exp2f(fmaf(x[e], kLog2e, -ml));
+      for (int e = 0; e < 32; ++e) acc[e & 3] += ex2(fmaf(x[e], kLog2e, -ml));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (n + e < V) acc[e & 3] += ex2(fmaf(x[e], kLog2e, -ml));
+    }
+    r.s += (acc[0] + acc[1]) + (acc[2] + acc[3]);
   }
-  __device__ void end(Row &r, int m, int n0) const {
-    if (m < T) part[(size_t)m * ntn + n0 / kFwdBN] = make_float2(r.m, r.s);
+  __device__ void end(Row &r, int m, int n0, int half) const {
+    if (m < T) part[(size_t)m * nparts + 2 * (n0 / kFwdBN) + half] = make_float2(r.m, r.s);
   }
 };
 
@@ -111,44 +139,56 @@ struct EpiGrad {
   bf16 *dz, *dzt;
   int64_t ldz, ldzt;
   struct Row {
-    float lse, gs;
+    float l2, gs;
     int yl;
   };
   __device__ void begin(Row &r, int m, int) const {
-    r.lse = 0.f;
+    r.l2 = 0.f;
     r.gs = 0.f;
     r.yl = -1;
     if (m < T) {
       const int yv = y[m];
       const bool valid = yv >= 0 && yv < V;
-      r.lse = lse[m];
+      r.l2 = lse[m] * kLog2e;
       r.gs = valid ? *gscale : 0.f;
       r.yl = valid ? yv - c0 : -1;
     }
   }
   __device__ void slice(Row &r, int m, int n, const float (&x)[32]) const {
     if (m >= T) return;
-    const float l2 = r.lse * kLog2e;
-    __align__(16) bf16 d[32];
+    const int hit = r.yl - n;  // the target's column in this slice, if in [0, 32)
+    uint32_t pk[16];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float p = exp2f(fmaf(x[e], kLog2e, -l2));
-      const float g = (p - (n + e == r.yl ? 1.f : 0.f)) * r.gs;
-      d[e] = __float2bfloat16_rn(g);
+    for (int e = 0; e < 32; e += 2) {
+      float g0 = ex2(fmaf(x[e], kLog2e, -r.l2));
+      float g1 = ex2(fmaf(x[e + 1], kLog2e, -r.l2));
+      if ((unsigned)hit < 32u) {
+        g0 -= (e == hit) ? 1.f : 0.f;
+        g1 -= (e + 1 == hit) ? 1.f : 0.f;
+      }
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(g0 * r.gs, g1 * r.gs);
+      pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&b2);
     }
     bf16 *row = dz + (size_t)m * ldz + n;
+    unsigned short *col = reinterpret_cast<unsigned short *>(dzt) + (size_t)n * ldzt + m;
     if (n + 32 <= Cv) {
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        reinterpret_cast<uint4 *>(row)[q] = reinterpret_cast<const uint4 *>(d)[q];
-    } else {
-      for (int e = 0; e < 32 && n + e < Cv; ++e) row[e] = d[e];
-    }
+        reinterpret_cast<uint4 *>(row)[q] =
+            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 #pragma unroll
-    for (int e = 0; e < 32; ++e)
-      if (n + e < Cv) dzt[(size_t)(n + e) * ldzt + m] = d[e];
+      for (int e = 0; e < 32; ++e)
+        col[(size_t)e * ldzt] = (unsigned short)(pk[e >> 1] >> (16 * (e & 1)));
+    } else {
+      unsigned short *rs = reinterpret_cast<unsigned short *>(row);
+      for (int e = 0; e < 32 && n + e < Cv; ++e) {
+        const unsigned short v = (unsigned short)(pk[e >> 1] >> (16 * (e & 1)));
+        rs[e] = v;
+        col[(size_t)e * ldzt] = v;
+      }
+    }
   }
-  __device__ void end(Row &, int, int) const {}
+  __device__ void end(Row &, int, int, int) const {}
 };
 
 // Plain output: C[m][n] (+= the fp32 value already there), written as fp32
@@ -207,7 +247,7 @@ struct EpiStore {
       }
     }
   }
-  __device__ void end(Row &, int, int) const {}
+  __device__ void end(Row &, int, int, int) const {}
 };
 
 // ------------------------------------------------------------ small kernels
@@ -342,8 +382,8 @@ cudaError_t launch_gemm_bf16(const void *a, int64_t lda, const void *b, int64_t 
 // ------------------------------------------------------------ workspaces
 
 size_t cce_fwd_workspace_bytes(int64_t T, int64_t V) {
-  const int64_t ntn = (V + kFwdBN - 1) / kFwdBN;
-  return (size_t)(T * ntn * 8 + round_up(T, 64) * 4 * 2 + 256);
+  const int64_t nparts = 2 * ((V + kFwdBN - 1) / kFwdBN);
+  return (size_t)(round_up(T * nparts * 8, 256) + round_up(T * 4, 256) * 2);
 }
 
 size_t cce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
@@ -373,18 +413,18 @@ struct Carve {
 
 cudaError_t launch_cce_fwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   const int T = (int)a.T, H = (int)a.H, V = (int)a.V;
-  const int ntn = (V + kFwdBN - 1) / kFwdBN;
+  const int nparts = 2 * ((V + kFwdBN - 1) / kFwdBN);  // two column halves per tile
   Carve w{(unsigned char *)a.ws};
-  float2 *part = w.take<float2>((size_t)T * ntn * 8);
+  float2 *part = w.take<float2>((size_t)T * nparts * 8);
   float *tgt = w.take<float>((size_t)T * 4);
   float *row_loss = w.take<float>((size_t)T * 4);
   alignas(64) CUtensorMap ta;
   cudaError_t e = tc::make_tmap_bf16(&ta, a.h, T, H, a.ldh, tc::BM);
   if (e != cudaSuccess) return e;
-  EpiLse epi{a.y, T, V, ntn, part, tgt};
+  EpiLse epi{a.y, T, V, nparts, part, tgt};
   e = gemm_bn(kFwdBN, ta, a.w, V, H, a.ldw, T, V, H, epi, dev, s);
   if (e != cudaSuccess) return e;
-  cce_row_lse<<<(T + 7) / 8, 256, 0, s>>>(part, ntn, tgt, a.y, T, V, a.lse, row_loss);
+  cce_row_lse<<<(T + 7) / 8, 256, 0, s>>>(part, nparts, tgt, a.y, T, V, a.lse, row_loss);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cce_finish<<<1, 1024, 0, s>>>(row_loss, a.y, T, V, a.loss, nullptr, nullptr);

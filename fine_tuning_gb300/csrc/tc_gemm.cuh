@@ -5,7 +5,7 @@
 // accumulator tile as such unless it wants to; the cross-entropy kernels
 // (cce.cu) use it to fold a softmax into the contraction.
 //
-// One CTA per SM, 6 warps:
+// One CTA per SM, 10 warps:
 //   warp 0      one elected lane issues TMA loads (cp.async.bulk.tensor, 128-
 //               byte swizzle) of the A tile [128 x 64] and the B tile
 //               [BN x 64] of every k-step into a ring of kStages stages;
@@ -13,9 +13,12 @@
 //               issues tcgen05.mma (M = 128, N = BN, K = 16, four per stage)
 //               and commits each stage back to the producer and each
 //               finished tile to the epilogue;
-//   warps 2..5  read the tile's rows from tensor memory (tcgen05.ld, warp w
-//               owns lanes 32 (w % 4) ...) and run the epilogue, while the
+//   warps 2..9  read the tile's rows from tensor memory (tcgen05.ld, warp w
+//               owns lanes 32 (w % 4) ...; warps 2..5 the first half of the
+//               columns, 6..9 the second) and run the epilogue, while the
 //               next tile accumulates in the other tensor-memory buffer.
+//               Two warps per sub-partition keep the epilogue's exp and
+//               conversion work from holding the tensor core back.
 // Tiles go to CTAs round-robin, M fastest, so the CTAs working at any moment
 // share the same B tile (B streams from HBM about once; A stays in L2).
 // Every wait is bounded: on timeout a status bit is set and the roles wind
@@ -34,8 +37,8 @@ namespace tc {
 constexpr int BM = 128;          // rows of a tile (tensor-memory lanes)
 constexpr int BK = 64;           // k-step: 64 bf16 = one 128-byte swizzle row
 constexpr int kStages = 4;
-constexpr int kThreads = 192;    // 6 warps
-constexpr int kEpiThreads = 128;
+constexpr int kThreads = 320;    // 10 warps
+constexpr int kEpiThreads = 256;  // 8 epilogue warps: 4 lane quarters x 2 column halves
 constexpr uint32_t kTmemCols = 512;  // two accumulators of up to 256 columns
 
 template <int BN> struct Layout {
@@ -140,8 +143,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 //   __device__ void begin(Row&, int m, int n0) const;
 //   __device__ void slice(Row&, int m, int n, const float (&x)[32]) const;
 //                                                   columns n .. n + 31
-//   __device__ void end(Row&, int m, int n0) const;  after the tile is released
-// m may be >= M (rows past the end of A read as zero): the epilogue masks.
+//   __device__ void end(Row&, int m, int n0, int half) const;
+//                                                   after the tile is released
+// A row of a tile is seen by two threads, one per column half (half 0:
+// the first ceil(BN/64) slices of 32 columns, half 1 the rest), each with
+// its own Row.  m may be >= M (rows past the end of A read as zero): the
+// epilogue masks.
 template <int BN, class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, int M,
@@ -249,6 +256,9 @@ tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensor
   } else {
     // ------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // the tensor-memory lanes this warp may read
+    const int half = (warp - 2) >> 2;
+    constexpr int kSlices = BN / 32, kFirst = (kSlices + 1) / 2;
+    const int c_begin = half ? kFirst * 32 : 0, c_end = half ? BN : kFirst * 32;
     const int r = quarter * 32 + lane;
     int tcount = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tcount) {
@@ -268,7 +278,7 @@ tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensor
       epi.begin(row, m, n0);
       const uint32_t base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
+      for (int c = c_begin; c < c_end; c += 32) {
         uint32_t v[32];
         tmem_ld32(base + (uint32_t)c, v);
         float x[32];
@@ -278,7 +288,7 @@ tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensor
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[b]);  // the buffer may take the next tile
-      epi.end(row, m, n0);
+      epi.end(row, m, n0, half);
     }
   }
   tc_fence_before();

@@ -4,9 +4,11 @@ the double-precision oracle (oracle/cce.py).
 Tolerances come from the arithmetic:
   * logits: bf16 products are exact in fp32, so |dz| <= H 2^-24 sum|h||W|
     <= H 2^-24 |h_t| max_v |W_v| (Cauchy-Schwarz);
-  * lse is 1-Lipschitz in the logits, plus the fp32 sums of e^z (a tile of
-    256 columns, then the tiles: (256 + #tiles + 8) 2^-23 relative) and the
-    fp32 exp / log (1e-6 relative);
+  * lse is 1-Lipschitz in the logits, plus the fp32 sums of e^z (half a
+    tile, 128 columns, per partial, then 2 partials per tile:
+    (128 + #partials + 8) 2^-24 relative), the hardware 2^x (about 2^-22
+    relative per term and per rescaling, at most 10 of them on a path) and
+    the fp32 log (1e-6 relative);
   * loss: the mean of the row losses, each within the lse and target-logit
     bounds, summed in fp32 in a fixed order (T 2^-24 of the mean);
   * dh, dW: dz is rounded to bf16 (2^-9 relative) before two fp32-
@@ -45,9 +47,10 @@ def ulp_bf16(x):
 
 def lse_bound(h64, W64, lse_ref, V):
     H = h64.shape[1]
-    ntn = (V + 255) // 256
+    nparts = 2 * ((V + 255) // 256)
     zmax = H * 2.0 ** -24 * np.linalg.norm(h64, axis=1) * np.linalg.norm(W64, axis=1).max()
-    return zmax, zmax + (256 + ntn + 8) * 2.0 ** -23 + 1e-6 * np.abs(lse_ref)
+    return zmax, (zmax + (128 + nparts + 8) * 2.0 ** -24 + 10 * 2.0 ** -22
+                  + 1e-6 * np.abs(lse_ref))
 
 
 def check_forward(h, Wt, y, loss, lse, tok=None, full_loss=True):
