@@ -181,18 +181,20 @@ qk_norm_rope_fwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   }
 }
 
-// The CTA's dwq | dwk partial row: sum over the warp's slots (lanes with the
-// same packet j), then over the CTA's warps in order, into ws[blockIdx.x].
+// The CTA's dwq | dwk partial row: sum over the warp's lanes that hold the
+// same packet j (lane % NV == j), then over the CTA's warps in order, into
+// ws[blockIdx.x].
 template <int N>
 __device__ __forceinline__ void write_partial(float (&acc)[4][N], float *part, float *ws, int D,
-                                              int NV, int j, int slot, int warp) {
+                                              int NV, int j, int lane, int warp) {
+  const int nwarps = (int)(blockDim.x >> 5);
   const int half = D >> 1;
 #pragma unroll
   for (int g = 0; g < 4; ++g)
 #pragma unroll
     for (int e = 0; e < N; ++e)
       for (int o = NV; o < 32; o <<= 1) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
-  if (slot == 0) {
+  if (lane < NV) {  // lane == j: the warp's first lane with this packet
     float *mine = part + warp * 2 * D;  // [warps][2D]
 #pragma unroll
     for (int e = 0; e < N; ++e) {
@@ -205,7 +207,7 @@ __device__ __forceinline__ void write_partial(float (&acc)[4][N], float *part, f
   __syncthreads();
   for (int c = threadIdx.x; c < 2 * D; c += blockDim.x) {
     float s = 0.f;
-    for (int w = 0; w < kWarps; ++w) s += part[w * 2 * D + c];
+    for (int w = 0; w < nwarps; ++w) s += part[w * 2 * D + c];
     ws[(size_t)blockIdx.x * 2 * D + c] = s;
   }
 }
@@ -306,7 +308,429 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
       }
     }
   }
-  write_partial<N>(acc, part, a.ws, D, NV, j, slot, warp);
+  write_partial<N>(acc, part, a.ws, D, NV, j, lane, warp);
+}
+
+// ------------------------------------------------------------ staged forms
+//
+// Large batches: independent row groups of W warps (R per CTA) each stream
+// blocks of TB whole tokens through a ring of S shared-memory stages, as in
+// qk_rope_staged.  The group's elected lane bulk-loads a block (Q rows, then
+// K rows; the backward adds the pre-norm rows after the gradients) with
+// cp.async.bulk completing on the stage's mbarrier; while it lands the group
+// computes the block's cos/sin table; then lane (slot, j) (HS = 32W / NV
+// head slots) normalises and rotates packet j of both halves of heads slot,
+// slot + HS, ... of every token in shared memory, and the lane bulk-stores
+// the block to the outputs.  A head's lanes are NV consecutive lanes of one
+// warp (NV divides 32), so its sums are shuffles; the head loop runs the
+// same number of times on every lane of a warp.
+
+struct StagedShape {
+  int TB, S, W, R;
+  uint32_t off_cs, off_part, off_stage, stage_bytes;
+  size_t smem;
+};
+
+template <typename T, typename Idx, int N>
+__global__ void __launch_bounds__(256)
+qk_norm_rope_fwd_staged(const NormRopeParams<T, Idx> a, const StagedShape g, unsigned *status,
+                        long long wait_limit, const __grid_constant__ RopeFreqs fr) {
+  extern __shared__ __align__(128) unsigned char sbuf[];
+  __shared__ float2 freq[kRopeMaxHalf];
+  const int D = a.D, half = D >> 1, NV = half / N, NH = a.Hq + a.Hkv, Hq = a.Hq;
+  const int TB = g.TB, S = g.S, W = g.W, R = g.R;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / W, wig = warp - grp * W;
+  const int gi = wig * 32 + lane, G = W * 32;
+  const bool leader = gi == 0;
+  const int HS = G / NV;
+  const int j = gi % NV, slot = gi / NV;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf) + grp * S;
+  float2 *cs = reinterpret_cast<float2 *>(sbuf + g.off_cs) + (size_t)grp * TB * half;
+  unsigned char *ring = sbuf + g.off_stage + (size_t)grp * S * g.stage_bytes;
+  const Idx nblocks = (a.rows + TB - 1) / TB;
+  const size_t qrow_b = (size_t)Hq * D * sizeof(T), krow_b = (size_t)a.Hkv * D * sizeof(T);
+  const bool q_in = a.ld_q == (Idx)Hq * D, k_in = a.ld_k == (Idx)a.Hkv * D;
+  const bool q_out = a.ld_oq == (Idx)Hq * D, k_out = a.ld_ok == (Idx)a.Hkv * D;
+
+  if (leader)
+    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) fence_mbar_init();
+  Packet<T, N> wq1, wq2, wk1, wk2;
+  if (Hq > 0) {
+    wq1 = load_packet<T, N>(a.wq + j * N);
+    wq2 = load_packet<T, N>(a.wq + half + j * N);
+  }
+  if (a.Hkv > 0) {
+    wk1 = load_packet<T, N>(a.wk + j * N);
+    wk2 = load_packet<T, N>(a.wk + half + j * N);
+  }
+  __syncthreads();
+
+  auto ntok = [&](Idx b) -> int {
+    const Idx left = a.rows - b * TB;
+    return (int)(left < (Idx)TB ? left : (Idx)TB);
+  };
+  auto load = [&](int s, Idx b) {
+    const Idx t0 = b * TB;
+    const int nt = ntok(b);
+    unsigned char *st = ring + (size_t)s * g.stage_bytes;
+    mbar_arrive_expect_tx(&bars[s], (uint32_t)(nt * (qrow_b + krow_b)));
+    if (qrow_b) {
+      if (q_in)
+        bulk_copy_g2s(st, a.q + t0 * a.ld_q, (uint32_t)(nt * qrow_b), &bars[s]);
+      else
+        for (int i = 0; i < nt; ++i)
+          bulk_copy_g2s(st + i * qrow_b, a.q + (t0 + i) * a.ld_q, (uint32_t)qrow_b, &bars[s]);
+    }
+    if (krow_b) {
+      unsigned char *sk = st + (size_t)TB * qrow_b;
+      if (k_in)
+        bulk_copy_g2s(sk, a.k + t0 * a.ld_k, (uint32_t)(nt * krow_b), &bars[s]);
+      else
+        for (int i = 0; i < nt; ++i)
+          bulk_copy_g2s(sk + i * krow_b, a.k + (t0 + i) * a.ld_k, (uint32_t)krow_b, &bars[s]);
+    }
+  };
+  auto store = [&](int s, Idx b) {
+    const Idx t0 = b * TB;
+    const int nt = ntok(b);
+    const unsigned char *st = ring + (size_t)s * g.stage_bytes;
+    if (qrow_b) {
+      if (q_out)
+        bulk_copy_s2g(a.oq + t0 * a.ld_oq, st, (uint32_t)(nt * qrow_b));
+      else
+        for (int i = 0; i < nt; ++i)
+          bulk_copy_s2g(a.oq + (t0 + i) * a.ld_oq, st + i * qrow_b, (uint32_t)qrow_b);
+    }
+    if (krow_b) {
+      const unsigned char *sk = st + (size_t)TB * qrow_b;
+      if (k_out)
+        bulk_copy_s2g(a.ok + t0 * a.ld_ok, sk, (uint32_t)(nt * krow_b));
+      else
+        for (int i = 0; i < nt; ++i)
+          bulk_copy_s2g(a.ok + (t0 + i) * a.ld_ok, sk + i * krow_b, (uint32_t)krow_b);
+    }
+    bulk_commit_group();
+  };
+  auto group_sync = [&]() {
+    if (W > 1)
+      named_barrier(1 + grp, G);
+    else
+      __syncwarp();
+  };
+
+  const Idx first = (Idx)blockIdx.x * R + grp;
+  const Idx stride = (Idx)gridDim.x * R;
+  int issued = 0;
+  if (leader)
+    for (int i = 0; i < S; ++i) {
+      const Idx b = first + (Idx)i * stride;
+      if (b >= nblocks) break;
+      load(i, b);
+      ++issued;
+    }
+
+  bool live = true;
+  int it = 0;
+  for (Idx b = first; b < nblocks; b += stride, ++it) {
+    const int s = it % S;
+    const Idx t0 = b * TB;
+    const int nt = ntok(b);
+    if (leader && it >= 1) {
+      bulk_wait_group_read<0>();  // the previous block's store has read its stage
+      const Idx nb = b - stride + (Idx)S * stride;
+      if (nb < nblocks) {
+        load((it - 1) % S, nb);
+        ++issued;
+      }
+    }
+    for (int e = gi; e < nt * half; e += G) {
+      const int tt = e / half, i = e - tt * half;
+      const int p = position_of<Idx>(t0 + tt, a.cu, a.B);
+      const float2 f = freq[i];
+      float c, sn;
+      rope_cos_sin(p, f.x, f.y, &c, &sn);
+      cs[e] = make_float2(c, sn);
+    }
+    if (live) live = mbar_wait_bounded(&bars[s], (uint32_t)((it / S) & 1), wait_limit, status);
+    group_sync();
+    unsigned char *st = ring + (size_t)s * g.stage_bytes;
+    for (int tt = 0; tt < nt; ++tt) {
+      const float2 *c2 = cs + tt * half + j * N;
+      float cv[N], sv[N];
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        const float2 r2 = c2[e];
+        cv[e] = r2.x;
+        sv[e] = r2.y;
+      }
+      T *qt = reinterpret_cast<T *>(st) + (size_t)tt * Hq * D + j * N;
+      T *kt = reinterpret_cast<T *>(st + (size_t)TB * qrow_b) + (size_t)tt * a.Hkv * D + j * N;
+      const Idx t = t0 + tt;
+      for (int h0 = 0; h0 < NH; h0 += HS) {
+        const int h = h0 + slot;
+        const bool act = h < NH, isq = h < Hq;
+        T *v = isq ? qt + (size_t)h * D : kt + (size_t)(h - Hq) * D;
+        Packet<T, N> pa, pb;
+        float ss = 0.f;
+        if (act) {
+          pa = *reinterpret_cast<const Packet<T, N> *>(v);
+          pb = *reinterpret_cast<const Packet<T, N> *>(v + half);
+#pragma unroll
+          for (int e = 0; e < N; ++e) {
+            const float u1 = pa.get(e), u2 = pb.get(e);
+            ss = fmaf(u1, u1, fmaf(u2, u2, ss));
+          }
+        }
+        ss = slot_sum(ss, NV);
+        if (act) {
+          const float r = rsqrtf(fmaf(ss, a.inv_d, a.eps));
+          const Packet<T, N> &w1 = isq ? wq1 : wk1, &w2 = isq ? wq2 : wk2;
+          Packet<T, N> o1, o2;
+#pragma unroll
+          for (int e = 0; e < N; ++e) {
+            const float n1 = pa.get(e) * r * w1.get(e), n2 = pb.get(e) * r * w2.get(e);
+            o1.set(e, fmaf(n1, cv[e], -n2 * sv[e]));
+            o2.set(e, fmaf(n2, cv[e], n1 * sv[e]));
+          }
+          *reinterpret_cast<Packet<T, N> *>(v) = o1;
+          *reinterpret_cast<Packet<T, N> *>(v + half) = o2;
+          if (j == 0) {
+            if (isq && a.rq) a.rq[t * Hq + h] = r;
+            if (!isq && a.rk) a.rk[t * a.Hkv + (h - Hq)] = r;
+          }
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    group_sync();
+    if (leader) store(s, b);
+  }
+  if (leader) {
+    if (!live)
+      for (int i = it; i < issued; ++i)
+        mbar_wait_bounded(&bars[i % S], (uint32_t)((i / S) & 1), wait_limit, status);
+    bulk_wait_group_all();
+  }
+}
+
+template <typename T, typename Idx, int N, bool HAS_RSTD>
+__global__ void __launch_bounds__(256)
+qk_norm_rope_bwd_staged(const NormRopeParams<T, Idx> a, const StagedShape g, unsigned *status,
+                        long long wait_limit, const __grid_constant__ RopeFreqs fr) {
+  extern __shared__ __align__(128) unsigned char sbuf[];
+  __shared__ float2 freq[kRopeMaxHalf];
+  const int D = a.D, half = D >> 1, NV = half / N, NH = a.Hq + a.Hkv, Hq = a.Hq;
+  const int TB = g.TB, S = g.S, W = g.W, R = g.R;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / W, wig = warp - grp * W;
+  const int gi = wig * 32 + lane, G = W * 32;
+  const bool leader = gi == 0;
+  const int HS = G / NV;
+  const int j = gi % NV, slot = gi / NV;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf) + grp * S;
+  float2 *cs = reinterpret_cast<float2 *>(sbuf + g.off_cs) + (size_t)grp * TB * half;
+  float *part = reinterpret_cast<float *>(sbuf + g.off_part);
+  unsigned char *ring = sbuf + g.off_stage + (size_t)grp * S * g.stage_bytes;
+  const Idx nblocks = (a.rows + TB - 1) / TB;
+  const size_t qrow_b = (size_t)Hq * D * sizeof(T), krow_b = (size_t)a.Hkv * D * sizeof(T);
+  const size_t tok_b = qrow_b + krow_b;
+  // stage: [TB] output-gradient Q rows, [TB] K rows, then [TB] pre-norm Q rows, [TB] K rows
+  struct Src {
+    const T *p;
+    Idx ld;
+    size_t row_b, off;
+  };
+  const Src src[4] = {{a.gq, a.ld_gq, qrow_b, 0},
+                      {a.gk, a.ld_gk, krow_b, (size_t)TB * qrow_b},
+                      {a.q, a.ld_q, qrow_b, (size_t)TB * tok_b},
+                      {a.k, a.ld_k, krow_b, (size_t)TB * tok_b + (size_t)TB * qrow_b}};
+
+  if (leader)
+    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) fence_mbar_init();
+  Packet<T, N> wq1, wq2, wk1, wk2;
+  if (Hq > 0) {
+    wq1 = load_packet<T, N>(a.wq + j * N);
+    wq2 = load_packet<T, N>(a.wq + half + j * N);
+  }
+  if (a.Hkv > 0) {
+    wk1 = load_packet<T, N>(a.wk + j * N);
+    wk2 = load_packet<T, N>(a.wk + half + j * N);
+  }
+  float acc[4][N];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int e = 0; e < N; ++e) acc[q][e] = 0.f;
+  __syncthreads();
+
+  auto ntok = [&](Idx b) -> int {
+    const Idx left = a.rows - b * TB;
+    return (int)(left < (Idx)TB ? left : (Idx)TB);
+  };
+  auto load = [&](int s, Idx b) {
+    const Idx t0 = b * TB;
+    const int nt = ntok(b);
+    unsigned char *st = ring + (size_t)s * g.stage_bytes;
+    mbar_arrive_expect_tx(&bars[s], (uint32_t)(2 * nt * tok_b));
+    for (int q = 0; q < 4; ++q) {
+      const Src &c = src[q];
+      if (!c.row_b) continue;
+      if (c.ld * (Idx)sizeof(T) == (Idx)c.row_b)
+        bulk_copy_g2s(st + c.off, c.p + t0 * c.ld, (uint32_t)(nt * c.row_b), &bars[s]);
+      else
+        for (int i = 0; i < nt; ++i)
+          bulk_copy_g2s(st + c.off + i * c.row_b, c.p + (t0 + i) * c.ld, (uint32_t)c.row_b,
+                        &bars[s]);
+    }
+  };
+  auto store = [&](int s, Idx b) {
+    const Idx t0 = b * TB;
+    const int nt = ntok(b);
+    const unsigned char *st = ring + (size_t)s * g.stage_bytes;
+    if (qrow_b) {
+      if (a.ld_oq == (Idx)Hq * D)
+        bulk_copy_s2g(a.oq + t0 * a.ld_oq, st, (uint32_t)(nt * qrow_b));
+      else
+        for (int i = 0; i < nt; ++i)
+          bulk_copy_s2g(a.oq + (t0 + i) * a.ld_oq, st + i * qrow_b, (uint32_t)qrow_b);
+    }
+    if (krow_b) {
+      const unsigned char *sk = st + (size_t)TB * qrow_b;
+      if (a.ld_ok == (Idx)a.Hkv * D)
+        bulk_copy_s2g(a.ok + t0 * a.ld_ok, sk, (uint32_t)(nt * krow_b));
+      else
+        for (int i = 0; i < nt; ++i)
+          bulk_copy_s2g(a.ok + (t0 + i) * a.ld_ok, sk + i * krow_b, (uint32_t)krow_b);
+    }
+    bulk_commit_group();
+  };
+  auto group_sync = [&]() {
+    if (W > 1)
+      named_barrier(1 + grp, G);
+    else
+      __syncwarp();
+  };
+
+  const Idx first = (Idx)blockIdx.x * R + grp;
+  const Idx stride = (Idx)gridDim.x * R;
+  int issued = 0;
+  if (leader)
+    for (int i = 0; i < S; ++i) {
+      const Idx b = first + (Idx)i * stride;
+      if (b >= nblocks) break;
+      load(i, b);
+      ++issued;
+    }
+
+  bool live = true;
+  int it = 0;
+  for (Idx b = first; b < nblocks; b += stride, ++it) {
+    const int s = it % S;
+    const Idx t0 = b * TB;
+    const int nt = ntok(b);
+    if (leader && it >= 1) {
+      bulk_wait_group_read<0>();
+      const Idx nb = b - stride + (Idx)S * stride;
+      if (nb < nblocks) {
+        load((it - 1) % S, nb);
+        ++issued;
+      }
+    }
+    for (int e = gi; e < nt * half; e += G) {
+      const int tt = e / half, i = e - tt * half;
+      const int p = position_of<Idx>(t0 + tt, a.cu, a.B);
+      const float2 f = freq[i];
+      float c, sn;
+      rope_cos_sin(p, f.x, f.y, &c, &sn);
+      cs[e] = make_float2(c, -sn);  // the transposed rotation
+    }
+    if (live) live = mbar_wait_bounded(&bars[s], (uint32_t)((it / S) & 1), wait_limit, status);
+    group_sync();
+    unsigned char *st = ring + (size_t)s * g.stage_bytes;
+    for (int tt = 0; tt < nt; ++tt) {
+      const float2 *c2 = cs + tt * half + j * N;
+      float cv[N], sv[N];
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        const float2 r2 = c2[e];
+        cv[e] = r2.x;
+        sv[e] = r2.y;
+      }
+      T *gqt = reinterpret_cast<T *>(st) + (size_t)tt * Hq * D + j * N;
+      T *gkt = reinterpret_cast<T *>(st + (size_t)TB * qrow_b) + (size_t)tt * a.Hkv * D + j * N;
+      const T *vqt = reinterpret_cast<const T *>(st + (size_t)TB * tok_b) + (size_t)tt * Hq * D + j * N;
+      const T *vkt = reinterpret_cast<const T *>(st + (size_t)TB * tok_b + (size_t)TB * qrow_b) +
+                     (size_t)tt * a.Hkv * D + j * N;
+      const Idx t = t0 + tt;
+      for (int h0 = 0; h0 < NH; h0 += HS) {
+        const int h = h0 + slot;
+        const bool act = h < NH, isq = h < Hq;
+        const int hk = h - Hq;
+        T *gp = isq ? gqt + (size_t)h * D : gkt + (size_t)hk * D;
+        const T *vp = isq ? vqt + (size_t)h * D : vkt + (size_t)hk * D;
+        const Packet<T, N> &w1 = isq ? wq1 : wk1, &w2 = isq ? wq2 : wk2;
+        Packet<T, N> v1, v2;
+        float dn1[N], dn2[N];
+        float2 csum = make_float2(0.f, 0.f);
+        float r = 0.f;
+        if (act) {
+          const Packet<T, N> g1 = *reinterpret_cast<const Packet<T, N> *>(gp);
+          const Packet<T, N> g2 = *reinterpret_cast<const Packet<T, N> *>(gp + half);
+          v1 = *reinterpret_cast<const Packet<T, N> *>(vp);
+          v2 = *reinterpret_cast<const Packet<T, N> *>(vp + half);
+          if (HAS_RSTD) r = isq ? a.rq[t * Hq + h] : a.rk[t * a.Hkv + hk];
+#pragma unroll
+          for (int e = 0; e < N; ++e) {
+            const float a1 = g1.get(e), a2 = g2.get(e);
+            dn1[e] = fmaf(a1, cv[e], -a2 * sv[e]);
+            dn2[e] = fmaf(a2, cv[e], a1 * sv[e]);
+            const float u1 = v1.get(e), u2 = v2.get(e);
+            csum.x = fmaf(dn1[e] * w1.get(e), u1, fmaf(dn2[e] * w2.get(e), u2, csum.x));
+            if (!HAS_RSTD) csum.y = fmaf(u1, u1, fmaf(u2, u2, csum.y));
+          }
+        }
+        if (HAS_RSTD)
+          csum.x = slot_sum(csum.x, NV);
+        else
+          csum = slot_sum2(csum, NV);
+        if (act) {
+          if (!HAS_RSTD) r = rsqrtf(fmaf(csum.y, a.inv_d, a.eps));
+          const float am = r * r * r * csum.x * a.inv_d;
+          const int q0 = isq ? 0 : 2;
+          Packet<T, N> o1, o2;
+#pragma unroll
+          for (int e = 0; e < N; ++e) {
+            const float u1 = v1.get(e), u2 = v2.get(e);
+            o1.set(e, fmaf(-am, u1, r * w1.get(e) * dn1[e]));
+            o2.set(e, fmaf(-am, u2, r * w2.get(e) * dn2[e]));
+            acc[q0][e] = fmaf(dn1[e] * u1, r, acc[q0][e]);
+            acc[q0 + 1][e] = fmaf(dn2[e] * u2, r, acc[q0 + 1][e]);
+          }
+          *reinterpret_cast<Packet<T, N> *>(gp) = o1;
+          *reinterpret_cast<Packet<T, N> *>(gp + half) = o2;
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    group_sync();
+    if (leader) store(s, b);
+  }
+  if (leader) {
+    if (!live)
+      for (int i = it; i < issued; ++i)
+        mbar_wait_bounded(&bars[i % S], (uint32_t)((i / S) & 1), wait_limit, status);
+    bulk_wait_group_all();
+  }
+  write_partial<N>(acc, part, a.ws, D, NV, j, lane, warp);
 }
 
 // Element-wise forms: one warp per token, heads one after another, lane i
@@ -467,6 +891,39 @@ NormRopeParams<T, Idx> params_of(const QkNormRopeArgs &a) {
 
 cudaError_t finish_launch(cudaError_t e) { return e != cudaSuccess ? e : cudaGetLastError(); }
 
+// The staged plan: ~8 KiB of whole tokens per stage (the backward's tokens
+// carry their output gradient and their pre-norm values); groups of W
+// warps with ~a block's worth of heads per lane; ~150 KiB of stages per SM
+// over two CTAs, 2..6 stages per group.  False when it does not fit.
+bool plan_staged(const QkNormRopeArgs &a, int es, int N, bool bwd, const DeviceInfo &dev,
+                 StagedShape *g) {
+  const int NH = a.Hq + a.Hkv, half = a.D / 2, NV = half / N;
+  const size_t tok_bytes = (size_t)NH * a.D * es * (bwd ? 2 : 1);
+  int TB = (int)(8192 / tok_bytes);
+  TB = TB < 1 ? 1 : (TB > 16 ? 16 : TB);
+  int W = (int)ceil_div((int64_t)TB * NH * NV, (int64_t)256);
+  W = W < 1 ? 1 : (W > 8 ? 8 : W);
+  const int R = 8 / W > 0 ? 8 / W : 1;
+  const size_t stage_bytes = (size_t)TB * tok_bytes;
+  if (NV > 32 || stage_bytes >= (1u << 20)) return false;
+  int S = (int)(76800 / ((size_t)R * stage_bytes));
+  S = S < 2 ? 2 : (S > 6 ? 6 : S);
+  const size_t static_smem = sizeof(float2) * kRopeMaxHalf;
+  for (; S >= 2; --S) {
+    const size_t off_cs = ((size_t)R * S * 8 + 15) / 16 * 16;
+    const size_t off_part = (off_cs + (size_t)R * TB * half * sizeof(float2) + 15) / 16 * 16;
+    const size_t part = bwd ? (size_t)W * R * 2 * a.D * sizeof(float) : 0;
+    const size_t off_stage = (off_part + part + 127) / 128 * 128;
+    const size_t smem = off_stage + (size_t)R * S * stage_bytes;
+    if (smem + static_smem <= (size_t)dev.max_smem_optin) {
+      *g = StagedShape{TB, S, W, R, (uint32_t)off_cs, (uint32_t)off_part, (uint32_t)off_stage,
+                       (uint32_t)stage_bytes, smem};
+      return true;
+    }
+  }
+  return false;
+}
+
 template <typename T, typename Idx, int N>
 cudaError_t fwd_warp_launch(const QkNormRopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
   const int NH = a.Hq + a.Hkv, half = a.D / 2, S = 32 / (half / N);
@@ -484,8 +941,23 @@ cudaError_t fwd_warp_launch(const QkNormRopeArgs &a, const RopeFreqs &fr, cudaSt
 
 template <typename T, typename Idx>
 cudaError_t fwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &fr,
-                      cudaStream_t s) {
+                      const DeviceInfo &dev, cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
+  StagedShape g;
+  if (warp_path && plan_staged(a, (int)sizeof(T), NV, false, dev, &g)) {
+    auto kern = qk_norm_rope_fwd_staged<T, Idx, NV>;
+    const int threads = 32 * g.W * g.R;
+    const int occ = blocks_per_sm((const void *)kern, threads, g.smem, dev, kMaxBlocksPerSm);
+    const int64_t P = (int64_t)dev.sms * occ;
+    // the pipeline pays off once every group streams several blocks
+    if (ceil_div(a.T, (int64_t)g.TB) >= (int64_t)6 * P * g.R) {
+      unsigned *status = nullptr;
+      cudaError_t e = device_status_ptr(dev, &status);
+      if (e != cudaSuccess) return e;
+      return finish_launch(launch_pdl(kern, dim3((unsigned)P), dim3(threads), g.smem, s,
+                                      params_of<T, Idx>(a), g, status, kWaitLimitCycles, fr));
+    }
+  }
   if (warp_path) return fwd_warp_launch<T, Idx, NV>(a, fr, s);
   const size_t smem = sizeof(float2) * (size_t)kWarps * (a.D / 2);
   return finish_launch(launch_pdl(qk_norm_rope_fwd_generic<T, Idx>,
@@ -500,6 +972,35 @@ cudaError_t bwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &
   const size_t smem =
       sizeof(float2) * (size_t)kWarps * (a.D / 2) + sizeof(float) * (size_t)kWarps * 2 * a.D;
   const bool rstd = a.rq != nullptr || a.rk != nullptr;
+  StagedShape g;
+  if (warp_path && plan_staged(a, (int)sizeof(T), NV, true, dev, &g)) {
+    const void *sk = rstd ? (const void *)qk_norm_rope_bwd_staged<T, Idx, NV, true>
+                          : (const void *)qk_norm_rope_bwd_staged<T, Idx, NV, false>;
+    const int threads = 32 * g.W * g.R;
+    const int occ = blocks_per_sm(sk, threads, g.smem, dev, kMaxBlocksPerSm);
+    int64_t P = (int64_t)dev.sms * occ;
+    if (P > a.ws_rows) P = a.ws_rows;
+    if (ceil_div(a.T, (int64_t)g.TB) >= (int64_t)6 * P * g.R) {
+      unsigned *status = nullptr;
+      cudaError_t e = device_status_ptr(dev, &status);
+      if (e != cudaSuccess) return e;
+      const NormRopeParams<T, Idx> k = params_of<T, Idx>(a);
+      e = rstd ? launch_pdl(qk_norm_rope_bwd_staged<T, Idx, NV, true>, dim3((unsigned)P),
+                            dim3(threads), g.smem, s, k, g, status, kWaitLimitCycles, fr)
+               : launch_pdl(qk_norm_rope_bwd_staged<T, Idx, NV, false>, dim3((unsigned)P),
+                            dim3(threads), g.smem, s, k, g, status, kWaitLimitCycles, fr);
+      if (e != cudaSuccess) return e;
+      if (a.dwq) {
+        e = launch_dw_reduce(a.ws, P, a.D, 2 * (int64_t)a.D, a.dwq, s);
+        if (e != cudaSuccess) return e;
+      }
+      if (a.dwk) {
+        e = launch_dw_reduce(a.ws + a.D, P, a.D, 2 * (int64_t)a.D, a.dwk, s);
+        if (e != cudaSuccess) return e;
+      }
+      return cudaGetLastError();
+    }
+  }
   const void *kern =
       warp_path ? (rstd ? (const void *)qk_norm_rope_bwd_warp<T, Idx, NV, true>
                         : (const void *)qk_norm_rope_bwd_warp<T, Idx, NV, false>)
@@ -548,7 +1049,8 @@ cudaError_t launch_qk_norm_rope(DType dt, bool vec, bool wide, const QkNormRopeA
   const int nv = vec ? a.D / 2 / n : 0;
   const bool warp_path = vec && nv >= 1 && nv <= 32 && (nv & (nv - 1)) == 0;
 #define FTK_NR(T, Idx) \
-  return a.backward ? bwd_typed<T, Idx>(warp_path, a, fr, dev, s) : fwd_typed<T, Idx>(warp_path, a, fr, s);
+  return a.backward ? bwd_typed<T, Idx>(warp_path, a, fr, dev, s) \
+                    : fwd_typed<T, Idx>(warp_path, a, fr, dev, s);
   if (dt == DType::F32) {
     if (wide) { FTK_NR(float, int64_t) }
     FTK_NR(float, int32_t)

@@ -205,3 +205,40 @@ def test_deterministic_dw():
             for _ in range(3)]
     for o in outs[1:]:
         assert all(torch.equal(a, b) for a, b in zip(o, outs[0]))
+
+
+def test_staged_path_fused_qkv_in_place_sampled():
+    """A batch large enough for the staged kernels, read from and written
+    back into interleaved Q / K slices of one fused QKV buffer."""
+    T, Hq, Hkv, D = 20000, 16, 4, 128
+    lens = (5000, 1, 8000, 6999)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cu_d = torch.as_tensor(cu, device=DEV)
+    qkv = randn((T, (Hq + 2 * Hkv) * D), torch.bfloat16, 91)
+    q = qkv[:, :Hq * D].view(T, Hq, D)
+    k = qkv[:, Hq * D:(Hq + Hkv) * D].view(T, Hkv, D)
+    wq = (1 + 0.1 * randn((D,), torch.float32, 92)).to(torch.bfloat16)
+    wk = (1 + 0.1 * randn((D,), torch.float32, 93)).to(torch.bfloat16)
+    q0, k0 = q.clone(), k.clone()
+    qo, ko, rq, rk = ftk.qk_norm_rope_fwd(q0, k0, wq, wk, cu_d, 1e-6, theta=1e6)
+    ftk.qk_norm_rope_fwd(q, k, wq, wk, cu_d, 1e-6, theta=1e6, q_out=q, k_out=k)
+    gq, gk = randn((T, Hq, D), torch.bfloat16, 94), randn((T, Hkv, D), torch.bfloat16, 95)
+    dq, dk, dwq, dwk = ftk.qk_norm_rope_bwd(gq, gk, q0, k0, wq, wk, rq, rk, cu_d, 1e-6,
+                                            theta=1e6)
+    torch.cuda.synchronize()
+    assert ftk.device_status(clear=True) == 0
+    assert torch.equal(q, qo) and torch.equal(k, ko)
+    tok = sample_rows(T, 512, extra=list(cu[:-1]) + [c - 1 for c in cu[1:]])
+    ti = torch.as_tensor(tok, device=DEV)
+    f = oracle.rope_inv_freq(D, 1e6)
+    qr, kr, _, _, qs, ks = oracle.qk_norm_rope_fwd(q0[ti].cpu(), k0[ti].cpu(), wq.cpu(),
+                                                   wk.cpu(), 1e-6, cu, f, tok=tok, scales=True)
+    assert_close("q_out", qo[ti], qr, qs)
+    assert_close("k_out", ko[ti], kr, ks)
+    out = oracle.qk_norm_rope_bwd(gq[ti].cpu(), gk[ti].cpu(), q0[ti].cpu(), k0[ti].cpu(),
+                                  wq.cpu(), wk.cpu(), 1e-6, cu, f, tok=tok, scales=True)
+    assert_close("dq", dq[ti], out[0], out[4])
+    assert_close("dk", dk[ti], out[1], out[5])
+    dwqr, dwkr, dwqs, dwks = dw_oracle_chunked(gq, gk, q0, k0, wq, wk, 1e-6, cu, f)
+    assert_close("dwq", dwq, dwqr, dwqs, kind="dw")
+    assert_close("dwk", dwk, dwkr, dwks, kind="dw")
