@@ -17,9 +17,12 @@
 // tokens); then dh += dz W_c and dW_c = dz^T h as two more GEMMs with both
 // operands K-major (W_c and h are transposed once by a plain kernel).  dh
 // accumulates in fp32 and is rounded to bf16 by the last chunk's epilogue.
+// The dW GEMMs run on a second stream with double-buffered chunk buffers,
+// overlapping the next chunk's work and filling each launch's last wave.
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "tc_gemm.cuh"
 
@@ -391,11 +394,11 @@ size_t cce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
   const int64_t ldt = round_up(T, 64);
   const int64_t bytes = 256                   // g / N
                         + H * ldt * 2         // h^T
-                        + H * C * 2           // W_c^T
-                        + T * C * 2           // dz
-                        + C * ldt * 2         // dz^T
+                        + 2 * H * C * 2       // W_c^T, two buffers
+                        + 2 * T * C * 2       // dz, two buffers
+                        + 2 * C * ldt * 2     // dz^T, two buffers
                         + round_up(T * H, 64) * 4;  // dh in fp32
-  return (size_t)bytes + 5 * 256;             // alignment of each piece
+  return (size_t)bytes + 9 * 256;             // alignment of each piece
 }
 
 namespace {
@@ -431,6 +434,34 @@ cudaError_t launch_cce_fwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t
   return cudaGetLastError();
 }
 
+// A second stream per device for the backward's dW GEMMs, and the events
+// that order it against the caller's stream (created once, kept).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t ready[2] = {}, done[2] = {};
+};
+
+cudaError_t side_stream(int device, SideStream **out) {
+  static std::mutex mu;
+  static SideStream side[64];
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  SideStream &x = side[device];
+  if (!x.s) {
+    cudaError_t e = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking);
+    for (int b = 0; e == cudaSuccess && b < 2; ++b) {
+      e = cudaEventCreateWithFlags(&x.ready[b], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&x.done[b], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+      x.s = nullptr;
+      return e;
+    }
+  }
+  *out = &x;
+  return cudaSuccess;
+}
+
 cudaError_t launch_cce_bwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   const int T = (int)a.T, H = (int)a.H, V = (int)a.V;
   const int64_t C = V < kChunk ? round_up(V, 64) : kChunk;
@@ -438,13 +469,19 @@ cudaError_t launch_cce_bwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t
   Carve w{(unsigned char *)a.ws};
   float *gscale = w.take<float>(256);
   bf16 *ht = w.take<bf16>((size_t)H * ldt * 2);
-  bf16 *wt = w.take<bf16>((size_t)H * C * 2);
-  bf16 *dz = w.take<bf16>((size_t)T * C * 2);
-  bf16 *dzt = w.take<bf16>((size_t)C * ldt * 2);
+  bf16 *wt[2], *dz[2], *dzt[2];
+  for (int b = 0; b < 2; ++b) {
+    wt[b] = w.take<bf16>((size_t)H * C * 2);
+    dz[b] = w.take<bf16>((size_t)T * C * 2);
+    dzt[b] = w.take<bf16>((size_t)C * ldt * 2);
+  }
   float *dh32 = w.take<float>((size_t)round_up((int64_t)T * H, 64) * 4);
+  SideStream *side = nullptr;
+  cudaError_t e = side_stream(dev.device, &side);
+  if (e != cudaSuccess) return e;
 
   cce_finish<<<1, 1024, 0, s>>>(nullptr, a.y, T, V, nullptr, a.dloss, gscale);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = transpose((const bf16 *)a.h, a.ldh, T, H, ht, ldt, s);
   if (e != cudaSuccess) return e;
@@ -452,31 +489,56 @@ cudaError_t launch_cce_bwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t
   e = tc::make_tmap_bf16(&th, a.h, T, H, a.ldh, tc::BM);
   if (e != cudaSuccess) return e;
   const int bn_h = pick_bn(H);
-  for (int64_t c0 = 0; c0 < V; c0 += C) {
+  // chunk c uses buffer c & 1: the caller's stream makes dz, dz^T and W_c^T
+  // and runs dh; the side stream runs dW_c once the chunk's buffers are
+  // ready, overlapping dh(c) and the next chunk's dz; a buffer is reused
+  // only after its dW has read it.  Only events recorded in this call are
+  // waited on, so the whole sequence can be captured into a graph.
+  bool pending[2] = {false, false};
+  int c = 0;
+  for (int64_t c0 = 0; c0 < V; c0 += C, ++c) {
+    const int b = c & 1;
     const int Cv = (int)(V - c0 < C ? V - c0 : C);
     const bool first = c0 == 0, last = c0 + C >= V;
     const bf16 *wc = (const bf16 *)a.w + c0 * a.ldw;
+    if (pending[b]) {
+      e = cudaStreamWaitEvent(s, side->done[b], 0);
+      if (e != cudaSuccess) return e;
+    }
     // dz for columns [c0, c0 + Cv)
-    EpiGrad g{a.y, a.lse, gscale, T, V, Cv, (int)c0, dz, dzt, C, ldt};
+    EpiGrad g{a.y, a.lse, gscale, T, V, Cv, (int)c0, dz[b], dzt[b], C, ldt};
     e = gemm_bn(kFwdBN, th, wc, Cv, H, a.ldw, T, Cv, H, g, dev, s);
     if (e != cudaSuccess) return e;
-    // dh (+)= dz W_c: A = dz [T x Cv], B = W_c^T [H x Cv]
-    e = transpose(wc, a.ldw, Cv, H, wt, C, s);
+    e = transpose(wc, a.ldw, Cv, H, wt[b], C, s);
     if (e != cudaSuccess) return e;
-    e = tc::make_tmap_bf16(&tdz, dz, T, Cv, C, tc::BM);
+    e = cudaEventRecord(side->ready[b], s);
     if (e != cudaSuccess) return e;
-    EpiStore sh{dh32, last ? (bf16 *)a.dh : nullptr, (int64_t)H, a.lddh, T, H, !first,
-                H % 4 == 0, vec16(a.dh) && a.lddh % 8 == 0};
-    e = gemm_bn(bn_h, tdz, wt, H, Cv, C, T, H, Cv, sh, dev, s);
+    // dW_c = dz^T h on the side stream: A = dz^T [Cv x T], B = h^T [H x T]
+    e = cudaStreamWaitEvent(side->s, side->ready[b], 0);
     if (e != cudaSuccess) return e;
-    // dW_c = dz^T h: A = dz^T [Cv x T], B = h^T [H x T]
-    e = tc::make_tmap_bf16(&tdzt, dzt, Cv, T, ldt, tc::BM);
+    e = tc::make_tmap_bf16(&tdzt, dzt[b], Cv, T, ldt, tc::BM);
     if (e != cudaSuccess) return e;
     EpiStore sw{a.dw + c0 * a.lddw, nullptr, a.lddw, 0, Cv, H, false,
                 vec16(a.dw) && a.lddw % 4 == 0, false};
-    e = gemm_bn(bn_h, tdzt, ht, H, T, ldt, Cv, H, T, sw, dev, s);
+    e = gemm_bn(bn_h, tdzt, ht, H, T, ldt, Cv, H, T, sw, dev, side->s);
+    if (e != cudaSuccess) return e;
+    e = cudaEventRecord(side->done[b], side->s);
+    if (e != cudaSuccess) return e;
+    pending[b] = true;
+    // dh (+)= dz W_c on the caller's stream: A = dz [T x Cv], B = W_c^T [H x Cv]
+    e = tc::make_tmap_bf16(&tdz, dz[b], T, Cv, C, tc::BM);
+    if (e != cudaSuccess) return e;
+    EpiStore sh{dh32, last ? (bf16 *)a.dh : nullptr, (int64_t)H, a.lddh, T, H, !first,
+                H % 4 == 0, vec16(a.dh) && a.lddh % 8 == 0};
+    e = gemm_bn(bn_h, tdz, wt[b], H, Cv, C, T, H, Cv, sh, dev, s);
     if (e != cudaSuccess) return e;
   }
+  // join: the caller's stream waits for every dW still in flight
+  for (int b = 0; b < 2; ++b)
+    if (pending[b]) {
+      e = cudaStreamWaitEvent(s, side->done[b], 0);
+      if (e != cudaSuccess) return e;
+    }
   return cudaSuccess;
 }
 

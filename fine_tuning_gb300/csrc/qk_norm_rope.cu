@@ -535,6 +535,7 @@ qk_norm_rope_bwd_staged(const NormRopeParams<T, Idx> a, const StagedShape g, uns
   uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf) + grp * S;
   float2 *cs = reinterpret_cast<float2 *>(sbuf + g.off_cs) + (size_t)grp * TB * half;
   float *part = reinterpret_cast<float *>(sbuf + g.off_part);
+  float *rsm = part + (blockDim.x >> 5) * 2 * D + (size_t)grp * TB * NH;  // [TB][NH] r of the block
   unsigned char *ring = sbuf + g.off_stage + (size_t)grp * S * g.stage_bytes;
   const Idx nblocks = (a.rows + TB - 1) / TB;
   const size_t qrow_b = (size_t)Hq * D * sizeof(T), krow_b = (size_t)a.Hkv * D * sizeof(T);
@@ -653,6 +654,12 @@ qk_norm_rope_bwd_staged(const NormRopeParams<T, Idx> a, const StagedShape g, uns
       rope_cos_sin(p, f.x, f.y, &c, &sn);
       cs[e] = make_float2(c, -sn);  // the transposed rotation
     }
+    if (HAS_RSTD)  // the saved r of the block's heads, fetched while its rows land
+      for (int e = gi; e < nt * NH; e += G) {
+        const int tt = e / NH, h = e - tt * NH;
+        const Idx t = t0 + tt;
+        rsm[e] = h < Hq ? a.rq[t * Hq + h] : a.rk[t * a.Hkv + (h - Hq)];
+      }
     if (live) live = mbar_wait_bounded(&bars[s], (uint32_t)((it / S) & 1), wait_limit, status);
     group_sync();
     unsigned char *st = ring + (size_t)s * g.stage_bytes;
@@ -687,7 +694,7 @@ qk_norm_rope_bwd_staged(const NormRopeParams<T, Idx> a, const StagedShape g, uns
           const Packet<T, N> g2 = *reinterpret_cast<const Packet<T, N> *>(gp + half);
           v1 = *reinterpret_cast<const Packet<T, N> *>(vp);
           v2 = *reinterpret_cast<const Packet<T, N> *>(vp + half);
-          if (HAS_RSTD) r = isq ? a.rq[t * Hq + h] : a.rk[t * a.Hkv + hk];
+          if (HAS_RSTD) r = rsm[tt * NH + h];
 #pragma unroll
           for (int e = 0; e < N; ++e) {
             const float a1 = g1.get(e), a2 = g2.get(e);
@@ -901,7 +908,9 @@ bool plan_staged(const QkNormRopeArgs &a, int es, int N, bool bwd, const DeviceI
   const size_t tok_bytes = (size_t)NH * a.D * es * (bwd ? 2 : 1);
   int TB = (int)(8192 / tok_bytes);
   TB = TB < 1 ? 1 : (TB > 16 ? 16 : TB);
-  int W = (int)ceil_div((int64_t)TB * NH * NV, (int64_t)256);
+  // as many lanes per group as a block has packet pairs (up to 8 warps):
+  // fewer head passes per token shorten each block's critical path
+  int W = (int)ceil_div((int64_t)TB * NH * NV, (int64_t)32);
   W = W < 1 ? 1 : (W > 8 ? 8 : W);
   const int R = 8 / W > 0 ? 8 / W : 1;
   const size_t stage_bytes = (size_t)TB * tok_bytes;
@@ -912,7 +921,10 @@ bool plan_staged(const QkNormRopeArgs &a, int es, int N, bool bwd, const DeviceI
   for (; S >= 2; --S) {
     const size_t off_cs = ((size_t)R * S * 8 + 15) / 16 * 16;
     const size_t off_part = (off_cs + (size_t)R * TB * half * sizeof(float2) + 15) / 16 * 16;
-    const size_t part = bwd ? (size_t)W * R * 2 * a.D * sizeof(float) : 0;
+    // the backward's dwq | dwk partials [warps][2D], then its r prefetch [R][TB][NH]
+    const size_t part = bwd ? (size_t)W * R * 2 * a.D * sizeof(float) +
+                                  (size_t)R * TB * NH * sizeof(float)
+                            : 0;
     const size_t off_stage = (off_part + part + 127) / 128 * 128;
     const size_t smem = off_stage + (size_t)R * S * stage_bytes;
     if (smem + static_smem <= (size_t)dev.max_smem_optin) {

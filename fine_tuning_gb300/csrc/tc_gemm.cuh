@@ -8,7 +8,8 @@
 // One CTA per SM, 10 warps:
 //   warp 0      one elected lane issues TMA loads (cp.async.bulk.tensor, 128-
 //               byte swizzle) of the A tile [128 x 64] and the B tile
-//               [BN x 64] of every k-step into a ring of kStages stages;
+//               [BN x 64] of every k-step into a ring of 4-6 stages (as many
+//               as fit in shared memory);
 //   warp 1      allocates 2 x BN columns of tensor memory; one elected lane
 //               issues tcgen05.mma (M = 128, N = BN, K = 16, four per stage)
 //               and commits each stage back to the producer and each
@@ -36,7 +37,7 @@ namespace tc {
 
 constexpr int BM = 128;          // rows of a tile (tensor-memory lanes)
 constexpr int BK = 64;           // k-step: 64 bf16 = one 128-byte swizzle row
-constexpr int kStages = 4;
+constexpr uint32_t kSmemBudget = 227 * 1024 - 2048;  // stages + barriers + alignment slack
 constexpr int kThreads = 320;    // 10 warps
 constexpr int kEpiThreads = 256;  // 8 epilogue warps: 4 lane quarters x 2 column halves
 constexpr uint32_t kTmemCols = 512;  // two accumulators of up to 256 columns
@@ -46,6 +47,10 @@ template <int BN> struct Layout {
   static constexpr uint32_t a_bytes = BM * BK * 2;
   static constexpr uint32_t b_bytes = BN * BK * 2;
   static constexpr uint32_t stage_bytes = a_bytes + b_bytes;  // a multiple of 1024
+  // as many stages as fit (4 at BN = 256, 5 at 224 or 192), at most 6
+  static constexpr int stages_fit = (int)(kSmemBudget / stage_bytes);
+  static constexpr int kStages = stages_fit > 6 ? 6 : stages_fit;
+  static_assert(kStages >= 2, "two stages must fit");
   static constexpr uint32_t bar_offset = kStages * stage_bytes;
   // full[S], empty[S], acc_full[2], acc_empty[2], drain; then the tensor
   // memory address and an abort flag
@@ -154,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, int M,
         int N, int K, const Epi epi, unsigned *status, long long wait_limit) {
   using L = Layout<BN>;
+  constexpr int kStages = L::kStages;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char *sm = smem_raw + ((1024 - (raw & 1023)) & 1023);  // 1024-aligned tiles
