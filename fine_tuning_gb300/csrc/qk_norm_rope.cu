@@ -908,9 +908,11 @@ bool plan_staged(const QkNormRopeArgs &a, int es, int N, bool bwd, const DeviceI
   const size_t tok_bytes = (size_t)NH * a.D * es * (bwd ? 2 : 1);
   int TB = (int)(8192 / tok_bytes);
   TB = TB < 1 ? 1 : (TB > 16 ? 16 : TB);
-  // as many lanes per group as a block has packet pairs (up to 8 warps):
-  // fewer head passes per token shorten each block's critical path
-  int W = (int)ceil_div((int64_t)TB * NH * NV, (int64_t)32);
+  // a group's lanes rotate ~8 packet pairs per block; the backward's blocks
+  // are twice as large, and at least 4 warps per group keep two CTAs (16
+  // warps) on an SM within the shared memory its stages take
+  int W = (int)ceil_div((int64_t)TB * NH * NV, (int64_t)256);
+  if (bwd && W < 4) W = 4;
   W = W < 1 ? 1 : (W > 8 ? 8 : W);
   const int R = 8 / W > 0 ? 8 / W : 1;
   const size_t stage_bytes = (size_t)TB * tok_bytes;
