@@ -327,7 +327,7 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
 
 struct StagedShape {
   int TB, S, W, R;
-  uint32_t off_cs, off_part, off_stage, stage_bytes;
+  uint32_t off_cs, off_stage, stage_bytes;
   size_t smem;
 };
 
@@ -518,228 +518,6 @@ qk_norm_rope_fwd_staged(const NormRopeParams<T, Idx> a, const StagedShape g, uns
   }
 }
 
-template <typename T, typename Idx, int N, bool HAS_RSTD>
-__global__ void __launch_bounds__(256)
-qk_norm_rope_bwd_staged(const NormRopeParams<T, Idx> a, const StagedShape g, unsigned *status,
-                        long long wait_limit, const __grid_constant__ RopeFreqs fr) {
-  extern __shared__ __align__(128) unsigned char sbuf[];
-  __shared__ float2 freq[kRopeMaxHalf];
-  const int D = a.D, half = D >> 1, NV = half / N, NH = a.Hq + a.Hkv, Hq = a.Hq;
-  const int TB = g.TB, S = g.S, W = g.W, R = g.R;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = warp / W, wig = warp - grp * W;
-  const int gi = wig * 32 + lane, G = W * 32;
-  const bool leader = gi == 0;
-  const int HS = G / NV;
-  const int j = gi % NV, slot = gi / NV;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf) + grp * S;
-  float2 *cs = reinterpret_cast<float2 *>(sbuf + g.off_cs) + (size_t)grp * TB * half;
-  float *part = reinterpret_cast<float *>(sbuf + g.off_part);
-  float *rsm = part + (blockDim.x >> 5) * 2 * D + (size_t)grp * TB * NH;  // [TB][NH] r of the block
-  unsigned char *ring = sbuf + g.off_stage + (size_t)grp * S * g.stage_bytes;
-  const Idx nblocks = (a.rows + TB - 1) / TB;
-  const size_t qrow_b = (size_t)Hq * D * sizeof(T), krow_b = (size_t)a.Hkv * D * sizeof(T);
-  const size_t tok_b = qrow_b + krow_b;
-  // stage: [TB] output-gradient Q rows, [TB] K rows, then [TB] pre-norm Q rows, [TB] K rows
-  struct Src {
-    const T *p;
-    Idx ld;
-    size_t row_b, off;
-  };
-  const Src src[4] = {{a.gq, a.ld_gq, qrow_b, 0},
-                      {a.gk, a.ld_gk, krow_b, (size_t)TB * qrow_b},
-                      {a.q, a.ld_q, qrow_b, (size_t)TB * tok_b},
-                      {a.k, a.ld_k, krow_b, (size_t)TB * tok_b + (size_t)TB * qrow_b}};
-
-  if (leader)
-    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
-  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
-  pdl_wait();
-  pdl_trigger();
-  if (threadIdx.x == 0) fence_mbar_init();
-  Packet<T, N> wq1, wq2, wk1, wk2;
-  if (Hq > 0) {
-    wq1 = load_packet<T, N>(a.wq + j * N);
-    wq2 = load_packet<T, N>(a.wq + half + j * N);
-  }
-  if (a.Hkv > 0) {
-    wk1 = load_packet<T, N>(a.wk + j * N);
-    wk2 = load_packet<T, N>(a.wk + half + j * N);
-  }
-  float acc[4][N];
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-#pragma unroll
-    for (int e = 0; e < N; ++e) acc[q][e] = 0.f;
-  __syncthreads();
-
-  auto ntok = [&](Idx b) -> int {
-    const Idx left = a.rows - b * TB;
-    return (int)(left < (Idx)TB ? left : (Idx)TB);
-  };
-  auto load = [&](int s, Idx b) {
-    const Idx t0 = b * TB;
-    const int nt = ntok(b);
-    unsigned char *st = ring + (size_t)s * g.stage_bytes;
-    mbar_arrive_expect_tx(&bars[s], (uint32_t)(2 * nt * tok_b));
-    for (int q = 0; q < 4; ++q) {
-      const Src &c = src[q];
-      if (!c.row_b) continue;
-      if (c.ld * (Idx)sizeof(T) == (Idx)c.row_b)
-        bulk_copy_g2s(st + c.off, c.p + t0 * c.ld, (uint32_t)(nt * c.row_b), &bars[s]);
-      else
-        for (int i = 0; i < nt; ++i)
-          bulk_copy_g2s(st + c.off + i * c.row_b, c.p + (t0 + i) * c.ld, (uint32_t)c.row_b,
-                        &bars[s]);
-    }
-  };
-  auto store = [&](int s, Idx b) {
-    const Idx t0 = b * TB;
-    const int nt = ntok(b);
-    const unsigned char *st = ring + (size_t)s * g.stage_bytes;
-    if (qrow_b) {
-      if (a.ld_oq == (Idx)Hq * D)
-        bulk_copy_s2g(a.oq + t0 * a.ld_oq, st, (uint32_t)(nt * qrow_b));
-      else
-        for (int i = 0; i < nt; ++i)
-          bulk_copy_s2g(a.oq + (t0 + i) * a.ld_oq, st + i * qrow_b, (uint32_t)qrow_b);
-    }
-    if (krow_b) {
-      const unsigned char *sk = st + (size_t)TB * qrow_b;
-      if (a.ld_ok == (Idx)a.Hkv * D)
-        bulk_copy_s2g(a.ok + t0 * a.ld_ok, sk, (uint32_t)(nt * krow_b));
-      else
-        for (int i = 0; i < nt; ++i)
-          bulk_copy_s2g(a.ok + (t0 + i) * a.ld_ok, sk + i * krow_b, (uint32_t)krow_b);
-    }
-    bulk_commit_group();
-  };
-  auto group_sync = [&]() {
-    if (W > 1)
-      named_barrier(1 + grp, G);
-    else
-      __syncwarp();
-  };
-
-  const Idx first = (Idx)blockIdx.x * R + grp;
-  const Idx stride = (Idx)gridDim.x * R;
-  int issued = 0;
-  if (leader)
-    for (int i = 0; i < S; ++i) {
-      const Idx b = first + (Idx)i * stride;
-      if (b >= nblocks) break;
-      load(i, b);
-      ++issued;
-    }
-
-  bool live = true;
-  int it = 0;
-  for (Idx b = first; b < nblocks; b += stride, ++it) {
-    const int s = it % S;
-    const Idx t0 = b * TB;
-    const int nt = ntok(b);
-    if (leader && it >= 1) {
-      bulk_wait_group_read<0>();
-      const Idx nb = b - stride + (Idx)S * stride;
-      if (nb < nblocks) {
-        load((it - 1) % S, nb);
-        ++issued;
-      }
-    }
-    for (int e = gi; e < nt * half; e += G) {
-      const int tt = e / half, i = e - tt * half;
-      const int p = position_of<Idx>(t0 + tt, a.cu, a.B);
-      const float2 f = freq[i];
-      float c, sn;
-      rope_cos_sin(p, f.x, f.y, &c, &sn);
-      cs[e] = make_float2(c, -sn);  // the transposed rotation
-    }
-    if (HAS_RSTD)  // the saved r of the block's heads, fetched while its rows land
-      for (int e = gi; e < nt * NH; e += G) {
-        const int tt = e / NH, h = e - tt * NH;
-        const Idx t = t0 + tt;
-        rsm[e] = h < Hq ? a.rq[t * Hq + h] : a.rk[t * a.Hkv + (h - Hq)];
-      }
-    if (live) live = mbar_wait_bounded(&bars[s], (uint32_t)((it / S) & 1), wait_limit, status);
-    group_sync();
-    unsigned char *st = ring + (size_t)s * g.stage_bytes;
-    for (int tt = 0; tt < nt; ++tt) {
-      const float2 *c2 = cs + tt * half + j * N;
-      float cv[N], sv[N];
-#pragma unroll
-      for (int e = 0; e < N; ++e) {
-        const float2 r2 = c2[e];
-        cv[e] = r2.x;
-        sv[e] = r2.y;
-      }
-      T *gqt = reinterpret_cast<T *>(st) + (size_t)tt * Hq * D + j * N;
-      T *gkt = reinterpret_cast<T *>(st + (size_t)TB * qrow_b) + (size_t)tt * a.Hkv * D + j * N;
-      const T *vqt = reinterpret_cast<const T *>(st + (size_t)TB * tok_b) + (size_t)tt * Hq * D + j * N;
-      const T *vkt = reinterpret_cast<const T *>(st + (size_t)TB * tok_b + (size_t)TB * qrow_b) +
-                     (size_t)tt * a.Hkv * D + j * N;
-      const Idx t = t0 + tt;
-      for (int h0 = 0; h0 < NH; h0 += HS) {
-        const int h = h0 + slot;
-        const bool act = h < NH, isq = h < Hq;
-        const int hk = h - Hq;
-        T *gp = isq ? gqt + (size_t)h * D : gkt + (size_t)hk * D;
-        const T *vp = isq ? vqt + (size_t)h * D : vkt + (size_t)hk * D;
-        const Packet<T, N> &w1 = isq ? wq1 : wk1, &w2 = isq ? wq2 : wk2;
-        Packet<T, N> v1, v2;
-        float dn1[N], dn2[N];
-        float2 csum = make_float2(0.f, 0.f);
-        float r = 0.f;
-        if (act) {
-          const Packet<T, N> g1 = *reinterpret_cast<const Packet<T, N> *>(gp);
-          const Packet<T, N> g2 = *reinterpret_cast<const Packet<T, N> *>(gp + half);
-          v1 = *reinterpret_cast<const Packet<T, N> *>(vp);
-          v2 = *reinterpret_cast<const Packet<T, N> *>(vp + half);
-          if (HAS_RSTD) r = rsm[tt * NH + h];
-#pragma unroll
-          for (int e = 0; e < N; ++e) {
-            const float a1 = g1.get(e), a2 = g2.get(e);
-            dn1[e] = fmaf(a1, cv[e], -a2 * sv[e]);
-            dn2[e] = fmaf(a2, cv[e], a1 * sv[e]);
-            const float u1 = v1.get(e), u2 = v2.get(e);
-            csum.x = fmaf(dn1[e] * w1.get(e), u1, fmaf(dn2[e] * w2.get(e), u2, csum.x));
-            if (!HAS_RSTD) csum.y = fmaf(u1, u1, fmaf(u2, u2, csum.y));
-          }
-        }
-        if (HAS_RSTD)
-          csum.x = slot_sum(csum.x, NV);
-        else
-          csum = slot_sum2(csum, NV);
-        if (act) {
-          if (!HAS_RSTD) r = rsqrtf(fmaf(csum.y, a.inv_d, a.eps));
-          const float am = r * r * r * csum.x * a.inv_d;
-          const int q0 = isq ? 0 : 2;
-          Packet<T, N> o1, o2;
-#pragma unroll
-          for (int e = 0; e < N; ++e) {
-            const float u1 = v1.get(e), u2 = v2.get(e);
-            o1.set(e, fmaf(-am, u1, r * w1.get(e) * dn1[e]));
-            o2.set(e, fmaf(-am, u2, r * w2.get(e) * dn2[e]));
-            acc[q0][e] = fmaf(dn1[e] * u1, r, acc[q0][e]);
-            acc[q0 + 1][e] = fmaf(dn2[e] * u2, r, acc[q0 + 1][e]);
-          }
-          *reinterpret_cast<Packet<T, N> *>(gp) = o1;
-          *reinterpret_cast<Packet<T, N> *>(gp + half) = o2;
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    group_sync();
-    if (leader) store(s, b);
-  }
-  if (leader) {
-    if (!live)
-      for (int i = it; i < issued; ++i)
-        mbar_wait_bounded(&bars[i % S], (uint32_t)((i / S) & 1), wait_limit, status);
-    bulk_wait_group_all();
-  }
-  write_partial<N>(acc, part, a.ws, D, NV, j, lane, warp);
-}
-
 // Element-wise forms: one warp per token, heads one after another, lane i
 // owning the pairs i, i + 32, ... of every head.
 template <typename T, typename Idx>
@@ -898,21 +676,18 @@ NormRopeParams<T, Idx> params_of(const QkNormRopeArgs &a) {
 
 cudaError_t finish_launch(cudaError_t e) { return e != cudaSuccess ? e : cudaGetLastError(); }
 
-// The staged plan: ~8 KiB of whole tokens per stage (the backward's tokens
-// carry their output gradient and their pre-norm values); groups of W
-// warps with ~a block's worth of heads per lane; ~150 KiB of stages per SM
+// The staged plan (forward): ~8 KiB of whole tokens per stage; groups of W
+// warps with ~8 packet pairs per lane per block; ~150 KiB of stages per SM
 // over two CTAs, 2..6 stages per group.  False when it does not fit.
-bool plan_staged(const QkNormRopeArgs &a, int es, int N, bool bwd, const DeviceInfo &dev,
-                 StagedShape *g) {
+// (A staged backward, whose tokens carry gradient and pre-norm rows, spent
+// its time in per-token barriers at one token per stage and measured slower
+// than the warp-per-token backward, so the backward stays warp-per-token.)
+bool plan_staged(const QkNormRopeArgs &a, int es, int N, const DeviceInfo &dev, StagedShape *g) {
   const int NH = a.Hq + a.Hkv, half = a.D / 2, NV = half / N;
-  const size_t tok_bytes = (size_t)NH * a.D * es * (bwd ? 2 : 1);
+  const size_t tok_bytes = (size_t)NH * a.D * es;
   int TB = (int)(8192 / tok_bytes);
   TB = TB < 1 ? 1 : (TB > 16 ? 16 : TB);
-  // a group's lanes rotate ~8 packet pairs per block; the backward's blocks
-  // are twice as large, and at least 4 warps per group keep two CTAs (16
-  // warps) on an SM within the shared memory its stages take
   int W = (int)ceil_div((int64_t)TB * NH * NV, (int64_t)256);
-  if (bwd && W < 4) W = 4;
   W = W < 1 ? 1 : (W > 8 ? 8 : W);
   const int R = 8 / W > 0 ? 8 / W : 1;
   const size_t stage_bytes = (size_t)TB * tok_bytes;
@@ -922,15 +697,10 @@ bool plan_staged(const QkNormRopeArgs &a, int es, int N, bool bwd, const DeviceI
   const size_t static_smem = sizeof(float2) * kRopeMaxHalf;
   for (; S >= 2; --S) {
     const size_t off_cs = ((size_t)R * S * 8 + 15) / 16 * 16;
-    const size_t off_part = (off_cs + (size_t)R * TB * half * sizeof(float2) + 15) / 16 * 16;
-    // the backward's dwq | dwk partials [warps][2D], then its r prefetch [R][TB][NH]
-    const size_t part = bwd ? (size_t)W * R * 2 * a.D * sizeof(float) +
-                                  (size_t)R * TB * NH * sizeof(float)
-                            : 0;
-    const size_t off_stage = (off_part + part + 127) / 128 * 128;
+    const size_t off_stage = (off_cs + (size_t)R * TB * half * sizeof(float2) + 127) / 128 * 128;
     const size_t smem = off_stage + (size_t)R * S * stage_bytes;
     if (smem + static_smem <= (size_t)dev.max_smem_optin) {
-      *g = StagedShape{TB, S, W, R, (uint32_t)off_cs, (uint32_t)off_part, (uint32_t)off_stage,
+      *g = StagedShape{TB, S, W, R, (uint32_t)off_cs, (uint32_t)off_stage,
                        (uint32_t)stage_bytes, smem};
       return true;
     }
@@ -958,7 +728,7 @@ cudaError_t fwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &
                       const DeviceInfo &dev, cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
   StagedShape g;
-  if (warp_path && plan_staged(a, (int)sizeof(T), NV, false, dev, &g)) {
+  if (warp_path && plan_staged(a, (int)sizeof(T), NV, dev, &g)) {
     auto kern = qk_norm_rope_fwd_staged<T, Idx, NV>;
     const int threads = 32 * g.W * g.R;
     const int occ = blocks_per_sm((const void *)kern, threads, g.smem, dev, kMaxBlocksPerSm);
@@ -986,35 +756,6 @@ cudaError_t bwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &
   const size_t smem =
       sizeof(float2) * (size_t)kWarps * (a.D / 2) + sizeof(float) * (size_t)kWarps * 2 * a.D;
   const bool rstd = a.rq != nullptr || a.rk != nullptr;
-  StagedShape g;
-  if (warp_path && plan_staged(a, (int)sizeof(T), NV, true, dev, &g)) {
-    const void *sk = rstd ? (const void *)qk_norm_rope_bwd_staged<T, Idx, NV, true>
-                          : (const void *)qk_norm_rope_bwd_staged<T, Idx, NV, false>;
-    const int threads = 32 * g.W * g.R;
-    const int occ = blocks_per_sm(sk, threads, g.smem, dev, kMaxBlocksPerSm);
-    int64_t P = (int64_t)dev.sms * occ;
-    if (P > a.ws_rows) P = a.ws_rows;
-    if (ceil_div(a.T, (int64_t)g.TB) >= (int64_t)6 * P * g.R) {
-      unsigned *status = nullptr;
-      cudaError_t e = device_status_ptr(dev, &status);
-      if (e != cudaSuccess) return e;
-      const NormRopeParams<T, Idx> k = params_of<T, Idx>(a);
-      e = rstd ? launch_pdl(qk_norm_rope_bwd_staged<T, Idx, NV, true>, dim3((unsigned)P),
-                            dim3(threads), g.smem, s, k, g, status, kWaitLimitCycles, fr)
-               : launch_pdl(qk_norm_rope_bwd_staged<T, Idx, NV, false>, dim3((unsigned)P),
-                            dim3(threads), g.smem, s, k, g, status, kWaitLimitCycles, fr);
-      if (e != cudaSuccess) return e;
-      if (a.dwq) {
-        e = launch_dw_reduce(a.ws, P, a.D, 2 * (int64_t)a.D, a.dwq, s);
-        if (e != cudaSuccess) return e;
-      }
-      if (a.dwk) {
-        e = launch_dw_reduce(a.ws + a.D, P, a.D, 2 * (int64_t)a.D, a.dwk, s);
-        if (e != cudaSuccess) return e;
-      }
-      return cudaGetLastError();
-    }
-  }
   const void *kern =
       warp_path ? (rstd ? (const void *)qk_norm_rope_bwd_warp<T, Idx, NV, true>
                         : (const void *)qk_norm_rope_bwd_warp<T, Idx, NV, false>)
