@@ -654,7 +654,7 @@ def cce_leg(dev, flush, flush_graph, reps):
     t_flush = sum(a.elapsed_time(b) for a, b in ev["flush"]) / reps
     peak, psrc = tensor_peak()
     flops = {"cce_fwd": 2 * hw.T * hw.H * hw.V, "cce_bwd": 6 * hw.T * hw.H * hw.V}
-    nchunk = -(-hw.V // 4096)
+    nchunk = -(-hw.V // 8192)
     launches = {"cce_fwd": 3, "cce_bwd": 2 + 4 * nchunk}
     out = {"workload": {"name": hw.name, "T": hw.T, "H": hw.H, "V": hw.V,
                         "ignored_share": hw.ignored},

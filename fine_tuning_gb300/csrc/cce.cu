@@ -13,8 +13,9 @@
 // a fixed order.
 // Backward, per vocabulary chunk of kChunk columns: a GEMM whose epilogue
 // turns the recomputed logits into dz (bf16), written row-major and
-// transposed (2 T kChunk bf16 = the ~135 MB the page quotes for 8,192
-// tokens); then dh += dz W_c and dW_c = dz^T h as two more GEMMs with both
+// transposed (T kChunk bf16 each: 134 MB for 8,192 tokens, the ~135 MB the
+// page quotes for its logits); then dh += dz W_c and dW_c = dz^T h as two
+// more GEMMs with both
 // operands K-major (W_c and h are transposed once by a plain kernel).  dh
 // accumulates in fp32 and is rounded to bf16 by the last chunk's epilogue.
 // The dW GEMMs run on a second stream with double-buffered chunk buffers,
@@ -56,7 +57,7 @@ cudaError_t make_tmap_bf16(CUtensorMap *map, const void *base, int64_t rows, int
 
 namespace {
 
-constexpr int kChunk = 4096;     // vocabulary columns per backward chunk
+constexpr int kChunk = 8192;     // vocabulary columns per backward chunk
 constexpr int kFwdBN = 256;      // logit tile width of the forward / dz GEMMs
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -158,7 +159,9 @@ struct EpiGrad {
     }
   }
   __device__ void slice(Row &r, int m, int n, const float (&x)[32]) const {
-    if (m >= T) return;
+    // every lane of the warp gets here (rows past T carry gs = 0): the
+    // paired transposed stores below exchange values between lanes
+    const bool ok = m < T;
     const int hit = r.yl - n;  // the target's column in this slice, if in [0, 32)
     uint32_t pk[16];
 #pragma unroll
@@ -172,18 +175,30 @@ struct EpiGrad {
       const __nv_bfloat162 b2 = __floats2bfloat162_rn(g0 * r.gs, g1 * r.gs);
       pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&b2);
     }
-    bf16 *row = dz + (size_t)m * ldz + n;
-    unsigned short *col = reinterpret_cast<unsigned short *>(dzt) + (size_t)n * ldzt + m;
-    if (n + 32 <= Cv) {
+    const bool full = n + 32 <= Cv;
+    if (full && __all_sync(0xffffffffu, ok)) {
+      bf16 *row = dz + (size_t)m * ldz + n;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         reinterpret_cast<uint4 *>(row)[q] =
             make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      // dz^T: lanes 2k and 2k + 1 hold rows m and m + 1 (consecutive); for
+      // columns (2i, 2i + 1) the even lane writes column 2i and the odd lane
+      // column 2i + 1, each as one 4-byte pair of rows, after swapping the
+      // value the other one needs
+      const bool odd = (threadIdx.x & 1) != 0;
+      unsigned short *col = reinterpret_cast<unsigned short *>(dzt);
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        col[(size_t)e * ldzt] = (unsigned short)(pk[e >> 1] >> (16 * (e & 1)));
-    } else {
-      unsigned short *rs = reinterpret_cast<unsigned short *>(row);
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t lo = pk[i] & 0xFFFFu, hi = pk[i] >> 16;  // columns 2i, 2i + 1
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+        const uint32_t pair = odd ? (got | (hi << 16)) : (lo | (got << 16));
+        const int c = n + 2 * i + (odd ? 1 : 0);
+        *reinterpret_cast<uint32_t *>(col + (size_t)c * ldzt + (m & ~1)) = pair;
+      }
+    } else if (ok) {
+      unsigned short *rs = reinterpret_cast<unsigned short *>(dz + (size_t)m * ldz + n);
+      unsigned short *col = reinterpret_cast<unsigned short *>(dzt) + (size_t)n * ldzt + m;
       for (int e = 0; e < 32 && n + e < Cv; ++e) {
         const unsigned short v = (unsigned short)(pk[e >> 1] >> (16 * (e & 1)));
         rs[e] = v;

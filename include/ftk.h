@@ -365,7 +365,7 @@ FTK_API ftk_status ftk_cce_fwd(const void *h, int64_t ldh, const void *w, int64_
  *   dh = dz W  -> bf16 [T, lddh],     dW = dz^T h  -> fp32 [V, lddw]
  * dz is rounded to bf16 before the two contractions (the tensor cores take
  * bf16 operands); they accumulate in fp32.  The logits are recomputed a
- * vocabulary chunk of 4,096 columns at a time.  lse from the forward.
+ * vocabulary chunk of 8,192 columns at a time.  lse from the forward.
  * workspace: >= ftk_cce_bwd_workspace_bytes(T, H, V) bytes, 256-byte
  * aligned.  dh and dW are overwritten; no output may overlap an input or
  * another output. */

@@ -101,8 +101,8 @@ def test_tiny_full():
     check_backward(h, Wt, y, dh, dW, g=0.5)
 
 
-@pytest.mark.parametrize("T,H,V", [(1, 64, 300), (129, 128, 4096), (130, 96, 4097),
-                                   (64, 200, 9000)])
+@pytest.mark.parametrize("T,H,V", [(1, 64, 300), (129, 128, 8192), (130, 96, 8193),
+                                   (64, 200, 17000)])
 def test_shapes(T, H, V):
     # one token; an exact chunk; one column past a chunk; ragged H
     hw = W.HeadWorkload("case", T=T, H=H, V=V, seed=T + V, w_std=H ** -0.5)
