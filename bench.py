@@ -655,7 +655,7 @@ def cce_leg(dev, flush, flush_graph, reps):
     peak, psrc = tensor_peak()
     flops = {"cce_fwd": 2 * hw.T * hw.H * hw.V, "cce_bwd": 6 * hw.T * hw.H * hw.V}
     nchunk = -(-hw.V // 8192)
-    launches = {"cce_fwd": 3, "cce_bwd": 2 + 4 * nchunk}
+    launches = {"cce_fwd": 3, "cce_bwd": 1 + 3 * nchunk}
     out = {"workload": {"name": hw.name, "T": hw.T, "H": hw.H, "V": hw.V,
                         "ignored_share": hw.ignored},
            "loss": round(float(loss.item()), 6)}

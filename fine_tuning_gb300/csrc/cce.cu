@@ -79,6 +79,7 @@ struct EpiLse {
   int T, V, nparts;
   float2 *part;  // [T][nparts]
   float *tgt;    // [T]
+  static constexpr bool kScratch = false;
   struct Row {
     float m, s;
     int y;
@@ -88,7 +89,7 @@ struct EpiLse {
     r.s = 0.f;
     r.y = m < T ? y[m] : -1;
   }
-  __device__ void slice(Row &r, int m, int n, const float (&x)[32]) const {
+  __device__ void slice(Row &r, int m, int n, const float (&x)[32], uint32_t *) const {
     if ((unsigned)(r.y - n) < 32u && m < T) {  // the target logit is in this slice
       float zt = 0.f;
 #pragma unroll
@@ -135,13 +136,18 @@ struct EpiLse {
 };
 
 // Backward, one vocabulary chunk [c0, c0 + Cv): dz = gs (e^(z - lse) - [v == y])
-// stored as bf16 row-major [T][ldz] and transposed [Cv][ldzt].
+// stored as bf16 row-major [T][ldz].  The values go through the warp's
+// shared-memory tile, two slices at a time, so that each store covers whole
+// 128-byte lines (64 columns of a row); this pairing needs 64-column aligned
+// halves of a tile, i.e. the 256-wide tiles.
+static_assert(kFwdBN == 256, "the dz epilogue pairs slices within 128-column halves");
 struct EpiGrad {
   const int32_t *y;
   const float *lse, *gscale;
   int T, V, Cv, c0;
-  bf16 *dz, *dzt;
-  int64_t ldz, ldzt;
+  bf16 *dz;
+  int64_t ldz;  // ldz % 8 == 0 and dz 16-byte aligned
+  static constexpr bool kScratch = true;
   struct Row {
     float l2, gs;
     int yl;
@@ -158,10 +164,12 @@ struct EpiGrad {
       r.yl = valid ? yv - c0 : -1;
     }
   }
-  __device__ void slice(Row &r, int m, int n, const float (&x)[32]) const {
-    // every lane of the warp gets here (rows past T carry gs = 0): the
-    // paired transposed stores below exchange values between lanes
-    const bool ok = m < T;
+  // Rows past T carry gs = 0 and are not stored.  This slice is the first
+  // (words 0..15 of each staged row) or second (words 16..31) of a
+  // 64-column pair; 16-byte chunk j of staged row i sits at j ^ (i & 7), so
+  // the row-wise writes and the line-wise reads are free of bank conflicts.
+  __device__ void slice(Row &r, int m, int n, const float (&x)[32], uint32_t *scr) const {
+    const int lane = threadIdx.x & 31;
     const int hit = r.yl - n;  // the target's column in this slice, if in [0, 32)
     uint32_t pk[16];
 #pragma unroll
@@ -175,34 +183,36 @@ struct EpiGrad {
       const __nv_bfloat162 b2 = __floats2bfloat162_rn(g0 * r.gs, g1 * r.gs);
       pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&b2);
     }
-    const bool full = n + 32 <= Cv;
-    if (full && __all_sync(0xffffffffu, ok)) {
-      bf16 *row = dz + (size_t)m * ldz + n;
+    const int second = (n >> 5) & 1;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        reinterpret_cast<uint4 *>(row)[q] =
-            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-      // dz^T: lanes 2k and 2k + 1 hold rows m and m + 1 (consecutive); for
-      // columns (2i, 2i + 1) the even lane writes column 2i and the odd lane
-      // column 2i + 1, each as one 4-byte pair of rows, after swapping the
-      // value the other one needs
-      const bool odd = (threadIdx.x & 1) != 0;
-      unsigned short *col = reinterpret_cast<unsigned short *>(dzt);
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4 *>(scr + lane * 32 + (((4 * second + q) ^ (lane & 7)) << 2)) =
+          make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    if (second) {
+      __syncwarp();
+      flush(m - lane, n - 32, scr);
+      __syncwarp();  // the tile is free for the next pair
+    }
+  }
+  // the staged rows mb .. mb + 31, columns n .. n + 63: pass i stores rows
+  // 4 i .. 4 i + 3, lane -> row 4 i + lane / 8, 8 columns from 8 (lane % 8)
+  __device__ void flush(int mb, int n, const uint32_t *scr) const {
+    const int lane = threadIdx.x & 31, j = lane & 7, col = n + 8 * j;
+    const bool full = n + 64 <= Cv;
+#pragma unroll 2
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 4 * i + (lane >> 3), row = mb + rr;
+      const uint4 v = *reinterpret_cast<const uint4 *>(scr + rr * 32 + ((j ^ (rr & 7)) << 2));
+      if (row >= T) continue;
+      bf16 *dst = dz + (size_t)row * ldz + col;
+      if (full) {
+        *reinterpret_cast<uint4 *>(dst) = v;
+      } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        unsigned short *d = reinterpret_cast<unsigned short *>(dst);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t lo = pk[i] & 0xFFFFu, hi = pk[i] >> 16;  // columns 2i, 2i + 1
-        const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
-        const uint32_t pair = odd ? (got | (hi << 16)) : (lo | (got << 16));
-        const int c = n + 2 * i + (odd ? 1 : 0);
-        *reinterpret_cast<uint32_t *>(col + (size_t)c * ldzt + (m & ~1)) = pair;
-      }
-    } else if (ok) {
-      unsigned short *rs = reinterpret_cast<unsigned short *>(dz + (size_t)m * ldz + n);
-      unsigned short *col = reinterpret_cast<unsigned short *>(dzt) + (size_t)n * ldzt + m;
-      for (int e = 0; e < 32 && n + e < Cv; ++e) {
-        const unsigned short v = (unsigned short)(pk[e >> 1] >> (16 * (e & 1)));
-        rs[e] = v;
-        col[(size_t)e * ldzt] = v;
+        for (int e = 0; e < 8; ++e)
+          if (col + e < Cv) d[e] = (unsigned short)(w[e >> 1] >> (16 * (e & 1)));
       }
     }
   }
@@ -210,7 +220,10 @@ struct EpiGrad {
 };
 
 // Plain output: C[m][n] (+= the fp32 value already there), written as fp32
-// or rounded to bf16.
+// or rounded to bf16.  A thread holds one row of a slice; the warp first
+// regroups its 32 x 32 values in shared memory so that every store (and
+// every read of the old value) covers whole 128-byte lines of a few rows
+// instead of 16 bytes of 32 rows.
 struct EpiStore {
   float *c;         // fp32 [M][ldc]: read when acc_in, written unless cb
   bf16 *cb;         // nullable: write bf16 [M][ldcb] instead
@@ -218,52 +231,83 @@ struct EpiStore {
   int M, N;
   bool acc_in;
   bool vc, vb;      // 16-byte vector access is aligned for c / cb (base and stride)
+  static constexpr bool kScratch = true;
   struct Row {};
   __device__ void begin(Row &, int, int) const {}
-  __device__ void slice(Row &, int m, int n, const float (&x)[32]) const {
-    if (m >= M) return;
-    float v[32];
-    const float *src = c + (size_t)m * ldc + n;
+  // scr holds row i of the slice at words 32 i .. 32 i + 31, its 16-byte
+  // chunk j at position j ^ (i & 7): both the row-wise writes and the
+  // line-wise reads below are free of bank conflicts.
+  __device__ void slice(Row &, int m, int n, const float (&x)[32], uint32_t *scr) const {
+    const int lane = threadIdx.x & 31;
+    const int mb = m - lane;  // the row of lane 0
+    float *sf = reinterpret_cast<float *>(scr);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4 *>(sf + lane * 32 + ((j ^ (lane & 7)) << 2)) =
+          make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+    __syncwarp();
     const bool full = n + 32 <= N;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) v[e] = x[e];
-    if (acc_in) {
-      if (full && vc) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 a = reinterpret_cast<const float4 *>(src)[q];
-          v[4 * q] += a.x;
-          v[4 * q + 1] += a.y;
-          v[4 * q + 2] += a.z;
-          v[4 * q + 3] += a.w;
+    if (!cb) {
+      // pass i: rows 4 i .. 4 i + 3, lane -> row 4 i + lane / 8, columns 4 (lane % 8) ..
+      const int j = lane & 7, col = n + 4 * j;
+#pragma unroll 2
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + (lane >> 3), row = mb + rr;
+        float4 v = *reinterpret_cast<const float4 *>(sf + rr * 32 + ((j ^ (rr & 7)) << 2));
+        if (row >= M) continue;
+        float *dst = c + (size_t)row * ldc + col;
+        if (full && vc) {
+          if (acc_in) {
+            const float4 o = *reinterpret_cast<const float4 *>(dst);
+            v.x += o.x;
+            v.y += o.y;
+            v.z += o.z;
+            v.w += o.w;
+          }
+          *reinterpret_cast<float4 *>(dst) = v;
+        } else {
+          const float e4[4] = {v.x, v.y, v.z, v.w};
+          for (int e = 0; e < 4; ++e)
+            if (col + e < N) dst[e] = acc_in ? dst[e] + e4[e] : e4[e];
         }
-      } else {
-        for (int e = 0; e < 32 && n + e < N; ++e) v[e] += src[e];
-      }
-    }
-    if (cb) {
-      bf16 *dst = cb + (size_t)m * ldcb + n;
-      __align__(16) bf16 o[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = __float2bfloat16_rn(v[e]);
-      if (full && vb) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          reinterpret_cast<uint4 *>(dst)[q] = reinterpret_cast<const uint4 *>(o)[q];
-      } else {
-        for (int e = 0; e < 32 && n + e < N; ++e) dst[e] = o[e];
       }
     } else {
-      float *dst = c + (size_t)m * ldc + n;
-      if (full && vc) {
+      // pass i: rows 8 i .. 8 i + 7, lane -> row 8 i + lane / 4, columns 8 (lane % 4) ..
+      const int j = 2 * (lane & 3), col = n + 4 * j;
+#pragma unroll 2
+      for (int i = 0; i < 4; ++i) {
+        const int rr = 8 * i + (lane >> 2), row = mb + rr;
+        const float4 a = *reinterpret_cast<const float4 *>(sf + rr * 32 + ((j ^ (rr & 7)) << 2));
+        const float4 b =
+            *reinterpret_cast<const float4 *>(sf + rr * 32 + (((j + 1) ^ (rr & 7)) << 2));
+        if (row >= M) continue;
+        float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const float *src = c + (size_t)row * ldc + col;
+        bf16 *dst = cb + (size_t)row * ldcb + col;
+        if (full && vb && (!acc_in || vc)) {
+          if (acc_in) {
+            const float4 o0 = reinterpret_cast<const float4 *>(src)[0];
+            const float4 o1 = reinterpret_cast<const float4 *>(src)[1];
+            v[0] += o0.x;
+            v[1] += o0.y;
+            v[2] += o0.z;
+            v[3] += o0.w;
+            v[4] += o1.x;
+            v[5] += o1.y;
+            v[6] += o1.z;
+            v[7] += o1.w;
+          }
+          __align__(16) __nv_bfloat162 o[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          reinterpret_cast<float4 *>(dst)[q] =
-              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      } else {
-        for (int e = 0; e < 32 && n + e < N; ++e) dst[e] = v[e];
+          for (int q = 0; q < 4; ++q) o[q] = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+          *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(o);
+        } else {
+          for (int e = 0; e < 8; ++e)
+            if (col + e < N) dst[e] = __float2bfloat16_rn(acc_in ? v[e] + src[e] : v[e]);
+        }
       }
     }
+    __syncwarp();  // the tile is free for the next slice
   }
   __device__ void end(Row &, int, int, int) const {}
 };
@@ -329,32 +373,6 @@ cce_finish(const float *__restrict__ row_loss, const int32_t *__restrict__ y, in
   }
 }
 
-// out[c][r] = in[r][c] for r < R, c < C (bf16), 32 x 32 tiles via shared memory.
-__global__ void __launch_bounds__(256)
-transpose_bf16(const bf16 *__restrict__ in, int64_t ldi, int R, int C, bf16 *__restrict__ out,
-               int64_t ldo) {
-  __shared__ bf16 tile[32][34];
-  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-  for (int i = ty; i < 32; i += 8) {
-    const int r = r0 + i, c = c0 + tx;
-    if (r < R && c < C) tile[i][tx] = in[(size_t)r * ldi + c];
-  }
-  __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int c = c0 + i, r = r0 + tx;
-    if (r < R && c < C) out[(size_t)c * ldo + r] = tile[tx][i];
-  }
-}
-
-cudaError_t transpose(const bf16 *in, int64_t ldi, int R, int C, bf16 *out, int64_t ldo,
-                      cudaStream_t s) {
-  if (R == 0 || C == 0) return cudaSuccess;
-  const dim3 grid((unsigned)((C + 31) / 32), (unsigned)((R + 31) / 32));
-  transpose_bf16<<<grid, 256, 0, s>>>(in, ldi, R, C, out, ldo);
-  return cudaGetLastError();
-}
-
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 bool vec16(const void *p) { return ((uintptr_t)p & 15) == 0; }
@@ -368,17 +386,19 @@ int pick_bn(int64_t n) {
   return 256;
 }
 
-template <class Epi>
+// B is [b_rows, b_cols] row-major: [N, K] when K-major, [K, N] when MN-major.
+template <int MAJ, class Epi>
 cudaError_t gemm_bn(int bn, const CUtensorMap &ta, const void *b_base, int64_t b_rows,
                     int64_t b_cols, int64_t ldb, int M, int N, int K, const Epi &epi,
                     const DeviceInfo &dev, cudaStream_t s) {
   alignas(64) CUtensorMap tb;
-  cudaError_t e = tc::make_tmap_bf16(&tb, b_base, b_rows, b_cols, ldb, bn);
+  cudaError_t e =
+      tc::make_tmap_bf16(&tb, b_base, b_rows, b_cols, ldb, (MAJ & tc::kBMn) ? tc::BK : bn);
   if (e != cudaSuccess) return e;
   switch (bn) {
-    case 256: return tc::launch_tc_gemm<256>(ta, tb, M, N, K, epi, dev, s);
-    case 224: return tc::launch_tc_gemm<224>(ta, tb, M, N, K, epi, dev, s);
-    case 192: return tc::launch_tc_gemm<192>(ta, tb, M, N, K, epi, dev, s);
+    case 256: return tc::launch_tc_gemm<256, MAJ>(ta, tb, M, N, K, epi, dev, s);
+    case 224: return tc::launch_tc_gemm<224, MAJ>(ta, tb, M, N, K, epi, dev, s);
+    case 192: return tc::launch_tc_gemm<192, MAJ>(ta, tb, M, N, K, epi, dev, s);
     default: return cudaErrorInvalidConfiguration;
   }
 }
@@ -387,14 +407,19 @@ cudaError_t gemm_bn(int bn, const CUtensorMap &ta, const void *b_base, int64_t b
 
 // ------------------------------------------------------------ plain GEMM
 
-cudaError_t launch_gemm_bf16(const void *a, int64_t lda, const void *b, int64_t ldb, float *c,
-                             int64_t ldc, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
-                             cudaStream_t s) {
+cudaError_t launch_gemm_bf16(const void *a, int64_t lda, bool a_mn, const void *b, int64_t ldb,
+                             bool b_mn, float *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                             const DeviceInfo &dev, cudaStream_t s) {
   alignas(64) CUtensorMap ta;
-  cudaError_t e = tc::make_tmap_bf16(&ta, a, M, K, lda, tc::BM);
+  cudaError_t e = a_mn ? tc::make_tmap_bf16(&ta, a, K, M, lda, tc::BK)
+                       : tc::make_tmap_bf16(&ta, a, M, K, lda, tc::BM);
   if (e != cudaSuccess) return e;
   EpiStore st{c, nullptr, ldc, 0, (int)M, (int)N, false, vec16(c) && ldc % 4 == 0, false};
-  return gemm_bn(pick_bn(N), ta, b, N, K, ldb, (int)M, (int)N, (int)K, st, dev, s);
+  const int bn = pick_bn(N), m = (int)M, n = (int)N, k = (int)K;
+  if (a_mn && b_mn) return gemm_bn<tc::kAMn | tc::kBMn>(bn, ta, b, K, N, ldb, m, n, k, st, dev, s);
+  if (a_mn) return gemm_bn<tc::kAMn>(bn, ta, b, N, K, ldb, m, n, k, st, dev, s);
+  if (b_mn) return gemm_bn<tc::kBMn>(bn, ta, b, K, N, ldb, m, n, k, st, dev, s);
+  return gemm_bn<tc::kKMajor>(bn, ta, b, N, K, ldb, m, n, k, st, dev, s);
 }
 
 // ------------------------------------------------------------ workspaces
@@ -406,14 +431,10 @@ size_t cce_fwd_workspace_bytes(int64_t T, int64_t V) {
 
 size_t cce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
   const int64_t C = V < kChunk ? round_up(V, 64) : kChunk;
-  const int64_t ldt = round_up(T, 64);
-  const int64_t bytes = 256                   // g / N
-                        + H * ldt * 2         // h^T
-                        + 2 * H * C * 2       // W_c^T, two buffers
-                        + 2 * T * C * 2       // dz, two buffers
-                        + 2 * C * ldt * 2     // dz^T, two buffers
+  const int64_t bytes = 256                         // g / N
+                        + 2 * round_up(T * C * 2, 256)  // dz, two buffers
                         + round_up(T * H, 64) * 4;  // dh in fp32
-  return (size_t)bytes + 9 * 256;             // alignment of each piece
+  return (size_t)bytes + 4 * 256;                   // alignment of each piece
 }
 
 namespace {
@@ -440,7 +461,7 @@ cudaError_t launch_cce_fwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t
   cudaError_t e = tc::make_tmap_bf16(&ta, a.h, T, H, a.ldh, tc::BM);
   if (e != cudaSuccess) return e;
   EpiLse epi{a.y, T, V, nparts, part, tgt};
-  e = gemm_bn(kFwdBN, ta, a.w, V, H, a.ldw, T, V, H, epi, dev, s);
+  e = gemm_bn<tc::kKMajor>(kFwdBN, ta, a.w, V, H, a.ldw, T, V, H, epi, dev, s);
   if (e != cudaSuccess) return e;
   cce_row_lse<<<(T + 7) / 8, 256, 0, s>>>(part, nparts, tgt, a.y, T, V, a.lse, row_loss);
   e = cudaGetLastError();
@@ -480,16 +501,10 @@ cudaError_t side_stream(int device, SideStream **out) {
 cudaError_t launch_cce_bwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   const int T = (int)a.T, H = (int)a.H, V = (int)a.V;
   const int64_t C = V < kChunk ? round_up(V, 64) : kChunk;
-  const int64_t ldt = round_up(T, 64);
   Carve w{(unsigned char *)a.ws};
   float *gscale = w.take<float>(256);
-  bf16 *ht = w.take<bf16>((size_t)H * ldt * 2);
-  bf16 *wt[2], *dz[2], *dzt[2];
-  for (int b = 0; b < 2; ++b) {
-    wt[b] = w.take<bf16>((size_t)H * C * 2);
-    dz[b] = w.take<bf16>((size_t)T * C * 2);
-    dzt[b] = w.take<bf16>((size_t)C * ldt * 2);
-  }
+  bf16 *dz[2];
+  for (int b = 0; b < 2; ++b) dz[b] = w.take<bf16>((size_t)T * C * 2);
   float *dh32 = w.take<float>((size_t)round_up((int64_t)T * H, 64) * 4);
   SideStream *side = nullptr;
   cudaError_t e = side_stream(dev.device, &side);
@@ -498,17 +513,16 @@ cudaError_t launch_cce_bwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t
   cce_finish<<<1, 1024, 0, s>>>(nullptr, a.y, T, V, nullptr, a.dloss, gscale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = transpose((const bf16 *)a.h, a.ldh, T, H, ht, ldt, s);
-  if (e != cudaSuccess) return e;
-  alignas(64) CUtensorMap th, tdz, tdzt;
+  alignas(64) CUtensorMap th, tdz, tdz_mn;
   e = tc::make_tmap_bf16(&th, a.h, T, H, a.ldh, tc::BM);
   if (e != cudaSuccess) return e;
   const int bn_h = pick_bn(H);
-  // chunk c uses buffer c & 1: the caller's stream makes dz, dz^T and W_c^T
-  // and runs dh; the side stream runs dW_c once the chunk's buffers are
-  // ready, overlapping dh(c) and the next chunk's dz; a buffer is reused
-  // only after its dW has read it.  Only events recorded in this call are
-  // waited on, so the whole sequence can be captured into a graph.
+  // chunk c uses dz buffer c & 1: the caller's stream makes dz and runs dh;
+  // the side stream runs dW_c once dz is ready, overlapping dh(c) and the
+  // next chunk's dz; a buffer is reused only after its dW has read it.
+  // Only events recorded in this call are waited on, so the whole sequence
+  // can be captured into a graph.  Neither W nor h is ever transposed: the
+  // GEMMs that need W_c^T, dz^T or h^T read them MN-major.
   bool pending[2] = {false, false};
   int c = 0;
   for (int64_t c0 = 0; c0 < V; c0 += C, ++c) {
@@ -520,32 +534,32 @@ cudaError_t launch_cce_bwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t
       e = cudaStreamWaitEvent(s, side->done[b], 0);
       if (e != cudaSuccess) return e;
     }
-    // dz for columns [c0, c0 + Cv)
-    EpiGrad g{a.y, a.lse, gscale, T, V, Cv, (int)c0, dz[b], dzt[b], C, ldt};
-    e = gemm_bn(kFwdBN, th, wc, Cv, H, a.ldw, T, Cv, H, g, dev, s);
-    if (e != cudaSuccess) return e;
-    e = transpose(wc, a.ldw, Cv, H, wt[b], C, s);
+    // dz [T x Cv] for columns [c0, c0 + Cv): A = h [T x H], B = W_c [Cv x H]
+    EpiGrad g{a.y, a.lse, gscale, T, V, Cv, (int)c0, dz[b], C};
+    e = gemm_bn<tc::kKMajor>(kFwdBN, th, wc, Cv, H, a.ldw, T, Cv, H, g, dev, s);
     if (e != cudaSuccess) return e;
     e = cudaEventRecord(side->ready[b], s);
     if (e != cudaSuccess) return e;
-    // dW_c = dz^T h on the side stream: A = dz^T [Cv x T], B = h^T [H x T]
+    // dW_c = dz^T h on the side stream: A = dz^T, read MN-major from dz
+    // [T x Cv]; B = h^T, read MN-major from h [T x H]; K = T
     e = cudaStreamWaitEvent(side->s, side->ready[b], 0);
     if (e != cudaSuccess) return e;
-    e = tc::make_tmap_bf16(&tdzt, dzt[b], Cv, T, ldt, tc::BM);
+    e = tc::make_tmap_bf16(&tdz_mn, dz[b], T, Cv, C, tc::BK);
     if (e != cudaSuccess) return e;
     EpiStore sw{a.dw + c0 * a.lddw, nullptr, a.lddw, 0, Cv, H, false,
                 vec16(a.dw) && a.lddw % 4 == 0, false};
-    e = gemm_bn(bn_h, tdzt, ht, H, T, ldt, Cv, H, T, sw, dev, side->s);
+    e = gemm_bn<tc::kAMn | tc::kBMn>(bn_h, tdz_mn, a.h, T, H, a.ldh, Cv, H, T, sw, dev, side->s);
     if (e != cudaSuccess) return e;
     e = cudaEventRecord(side->done[b], side->s);
     if (e != cudaSuccess) return e;
     pending[b] = true;
-    // dh (+)= dz W_c on the caller's stream: A = dz [T x Cv], B = W_c^T [H x Cv]
+    // dh (+)= dz W_c on the caller's stream: A = dz [T x Cv] K-major; B =
+    // W_c^T, read MN-major from W_c [Cv x H]; K = Cv
     e = tc::make_tmap_bf16(&tdz, dz[b], T, Cv, C, tc::BM);
     if (e != cudaSuccess) return e;
     EpiStore sh{dh32, last ? (bf16 *)a.dh : nullptr, (int64_t)H, a.lddh, T, H, !first,
                 H % 4 == 0, vec16(a.dh) && a.lddh % 8 == 0};
-    e = gemm_bn(bn_h, tdz, wt[b], H, Cv, C, T, H, Cv, sh, dev, s);
+    e = gemm_bn<tc::kBMn>(bn_h, tdz, wc, Cv, H, a.ldw, T, H, Cv, sh, dev, s);
     if (e != cudaSuccess) return e;
   }
   // join: the caller's stream waits for every dW still in flight

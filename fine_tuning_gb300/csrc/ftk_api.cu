@@ -670,11 +670,11 @@ FTK_API ftk_status ftk_qk_norm_rope_bwd(const void *dq_out, int64_t ld_gq, const
 
 // ------------------------------------------------------ tensor-core GEMM
 
-FTK_API ftk_status ftk_gemm_bf16(const void *a, int64_t lda, const void *b, int64_t ldb,
-                                 float *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
-                                 ftk_stream_t stream) {
-  if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < N || M >= (int64_t(1) << 31) ||
-      N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+FTK_API ftk_status ftk_gemm_bf16_ex(const void *a, int64_t lda, int a_mn, const void *b,
+                                    int64_t ldb, int b_mn, float *c, int64_t ldc, int64_t M,
+                                    int64_t N, int64_t K, ftk_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || ldc < N ||
+      M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
     return FTK_ERR_SHAPE;
   if (M == 0 || N == 0) return FTK_OK;
   if (!a || !b || !c) return FTK_ERR_NULL;
@@ -682,12 +682,21 @@ FTK_API ftk_status ftk_gemm_bf16(const void *a, int64_t lda, const void *b, int6
     return FTK_ERR_ALIGN;
   if (!aligned(c, 4)) return FTK_ERR_ALIGN;
   if (K == 0) return FTK_ERR_SHAPE;  // an empty contraction has nothing to run on
-  const View va = view(a, M, lda, K, 2), vb = view(b, N, ldb, K, 2), vc = view(c, M, ldc, N, 4);
+  const View va = a_mn ? view(a, K, lda, M, 2) : view(a, M, lda, K, 2);
+  const View vb = b_mn ? view(b, K, ldb, N, 2) : view(b, N, ldb, K, 2);
+  const View vc = view(c, M, ldc, N, 4);
   if (may_overlap(vc, va) || may_overlap(vc, vb)) return FTK_ERR_ALIAS;
   ftk::DeviceInfo dev;
   cudaError_t e = device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  return finish(ftk::launch_gemm_bf16(a, lda, b, ldb, c, ldc, M, N, K, dev, (cudaStream_t)stream));
+  return finish(ftk::launch_gemm_bf16(a, lda, a_mn != 0, b, ldb, b_mn != 0, c, ldc, M, N, K, dev,
+                                      (cudaStream_t)stream));
+}
+
+FTK_API ftk_status ftk_gemm_bf16(const void *a, int64_t lda, const void *b, int64_t ldb,
+                                 float *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                 ftk_stream_t stream) {
+  return ftk_gemm_bf16_ex(a, lda, 0, b, ldb, 0, c, ldc, M, N, K, stream);
 }
 
 // ------------------------------------------------------ Cut Cross-Entropy

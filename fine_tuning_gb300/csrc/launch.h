@@ -229,9 +229,11 @@ size_t cce_fwd_workspace_bytes(int64_t T, int64_t V);
 size_t cce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V);
 cudaError_t launch_cce_fwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t s);
 cudaError_t launch_cce_bwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t s);
-// C fp32 [M, ldc] = A [M, lda] B [N, ldb]^T on the tensor cores (bf16, tc_gemm.cuh).
-cudaError_t launch_gemm_bf16(const void *a, int64_t lda, const void *b, int64_t ldb, float *c,
-                             int64_t ldc, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
-                             cudaStream_t s);
+// C fp32 [M, ldc] = A B^T on the tensor cores (bf16, tc_gemm.cuh): A stored
+// [M, lda] (K-major) or, with a_mn, [K, lda] (MN-major); B stored [N, ldb]
+// or, with b_mn, [K, ldb].
+cudaError_t launch_gemm_bf16(const void *a, int64_t lda, bool a_mn, const void *b, int64_t ldb,
+                             bool b_mn, float *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                             const DeviceInfo &dev, cudaStream_t s);
 
 }  // namespace ftk

@@ -41,19 +41,37 @@ constexpr int kThreads = 320;    // 10 warps
 constexpr int kEpiThreads = 256;  // 8 epilogue warps: 4 lane quarters x 2 column halves
 constexpr uint32_t kTmemCols = 512;  // two accumulators of up to 256 columns
 
-template <int BN> struct Layout {
+constexpr uint32_t kScratchWords = 32 * 32;  // an epilogue warp's staging tile: 32 x 32 words
+
+constexpr int kMnBlock = 64;           // MN-major operands: 64-element (128-byte) column blocks
+constexpr uint32_t kMnBoxBytes = kMnBlock * BK * 2;  // one such block of a k-step: 8 KB
+
+// Operand majors of a GEMM: K-major (K contiguous, the natural layout of
+// A [M, K] and B [N, K]) or MN-major (M or N contiguous: A stored [K, M], B
+// stored [K, N]).
+enum Major : int { kKMajor = 0, kAMn = 1, kBMn = 2 };
+
+// SCRATCH: whether each epilogue warp gets a 4 KB shared-memory tile to
+// regroup its values before storing them.  MAJ: the operand majors.  An
+// MN-major operand is staged as 64-element blocks of BK rows (8 KB each),
+// block j at j x 8 KB; a K-major one as rows of BK elements.
+template <int BN, bool SCRATCH, int MAJ = kKMajor> struct Layout {
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN: a multiple of 32 up to 256");
-  static constexpr uint32_t a_bytes = BM * BK * 2;
-  static constexpr uint32_t b_bytes = BN * BK * 2;
+  static constexpr int b_blocks = (BN + kMnBlock - 1) / kMnBlock;
+  static constexpr uint32_t a_bytes = BM * BK * 2;  // the same in both majors
+  static constexpr uint32_t b_bytes = (MAJ & kBMn) ? b_blocks * kMnBoxBytes : BN * BK * 2;
   static constexpr uint32_t stage_bytes = a_bytes + b_bytes;  // a multiple of 1024
+  static constexpr uint32_t scratch_bytes = SCRATCH ? (kEpiThreads / 32) * kScratchWords * 4 : 0;
   // 4 stages (a fifth, where it fits, measured no faster)
-  static constexpr int stages_fit = (int)(kSmemBudget / stage_bytes);
+  static constexpr int stages_fit = (int)((kSmemBudget - scratch_bytes) / stage_bytes);
   static constexpr int kStages = stages_fit > 4 ? 4 : stages_fit;
   static_assert(kStages >= 2, "two stages must fit");
-  static constexpr uint32_t bar_offset = kStages * stage_bytes;
+  static constexpr uint32_t scratch_offset = kStages * stage_bytes;
+  static constexpr uint32_t bar_offset = scratch_offset + scratch_bytes;
   // full[S], empty[S], acc_full[2], acc_empty[2], drain; then the tensor
   // memory address and an abort flag
   static constexpr uint32_t smem_bytes = bar_offset + (2 * kStages + 5) * 8 + 16 + 1024;
+  static_assert(smem_bytes <= 227 * 1024, "shared memory per CTA");
 };
 
 // ---------------------------------------------------------------- PTX
@@ -100,10 +118,20 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// N = BN, M = 128.
-template <int BN> __device__ __forceinline__ constexpr uint32_t idesc_bf16() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+// The same for an MN-major tile: each k row holds 64 M (or N) elements in
+// 128 bytes, 8-row swizzle atoms of 1024 bytes follow each other along k
+// (stride byte offset 1024), and the 64-element blocks along M (or N) are
+// kMnBoxBytes apart (leading byte offset).
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(kMnBoxBytes >> 4) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, N = BN, M = 128;
+// bit 15 / 16 mark A / B as MN-major.
+template <int BN, int MAJ> __device__ __forceinline__ constexpr uint32_t idesc_bf16() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((MAJ & kAMn) ? 1u << 15 : 0u) |
+         ((MAJ & kBMn) ? 1u << 16 : 0u) | ((uint32_t)(BN >> 3) << 17) |
          ((uint32_t)(BM >> 4) << 24);
 }
 
@@ -143,21 +171,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 // ---------------------------------------------------------------- kernel
 
 // Epi provides:
+//   static constexpr bool kScratch;                 wants a staging tile
 //   struct Row;                                     per-row state
 //   __device__ void begin(Row&, int m, int n0) const;
-//   __device__ void slice(Row&, int m, int n, const float (&x)[32]) const;
-//                                                   columns n .. n + 31
+//   __device__ void slice(Row&, int m, int n, const float (&x)[32],
+//                         uint32_t *scr) const;      columns n .. n + 31
 //   __device__ void end(Row&, int m, int n0, int half) const;
 //                                                   after the tile is released
 // A row of a tile is seen by two threads, one per column half (half 0:
 // the first ceil(BN/64) slices of 32 columns, half 1 the rest), each with
 // its own Row.  m may be >= M (rows past the end of A read as zero): the
-// epilogue masks.
-template <int BN, class Epi>
+// epilogue masks.  slice is called by all 32 lanes of a warp together
+// (lane i holding row m - lane + i), so it may exchange values between
+// lanes; scr is the warp's own 32 x 32-word shared-memory tile (null unless
+// kScratch), which keeps nothing between calls that the epilogue does not
+// put there itself.
+// ta / tb: tensor maps with 64-element inner boxes; a K-major operand's
+// box is [BM or BN rows x 64 k], an MN-major one's [64 k rows x 64].
+template <int BN, class Epi, int MAJ>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, int M,
         int N, int K, const Epi epi, unsigned *status, long long wait_limit) {
-  using L = Layout<BN>;
+  using L = Layout<BN, Epi::kScratch, MAJ>;
   constexpr int kStages = L::kStages;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -202,6 +237,16 @@ tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensor
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
         const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
+        // MN-major blocks that start past the matrix are not loaded: they
+        // feed only rows >= M or columns >= N, which the epilogue drops
+        const int a_blk = (MAJ & kAMn) ? (M - m0 > kMnBlock ? 2 : 1) : 0;
+        int b_blk = 0;
+        if (MAJ & kBMn) {
+          b_blk = (N - n0 + kMnBlock - 1) / kMnBlock;
+          if (b_blk > L::b_blocks) b_blk = L::b_blocks;
+        }
+        const uint32_t tx = ((MAJ & kAMn) ? a_blk * kMnBoxBytes : L::a_bytes) +
+                            ((MAJ & kBMn) ? b_blk * kMnBoxBytes : L::b_bytes);
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kStages;
           if (*abort_flag ||
@@ -211,9 +256,21 @@ tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensor
             break;
           }
           const uint32_t st = sbase + s * L::stage_bytes;
-          mbar_arrive_expect_tx(&full[s], L::stage_bytes);
-          tma_load_2d(st, &ta, kb * BK, m0, smem_addr(&full[s]));
-          tma_load_2d(st + L::a_bytes, &tb, kb * BK, n0, smem_addr(&full[s]));
+          const uint32_t bar = smem_addr(&full[s]);
+          mbar_arrive_expect_tx(&full[s], tx);
+          if (MAJ & kAMn) {
+            for (int j = 0; j < a_blk; ++j)
+              tma_load_2d(st + j * kMnBoxBytes, &ta, m0 + j * kMnBlock, kb * BK, bar);
+          } else {
+            tma_load_2d(st, &ta, kb * BK, m0, bar);
+          }
+          if (MAJ & kBMn) {
+            for (int j = 0; j < b_blk; ++j)
+              tma_load_2d(st + L::a_bytes + j * kMnBoxBytes, &tb, n0 + j * kMnBlock, kb * BK,
+                          bar);
+          } else {
+            tma_load_2d(st + L::a_bytes, &tb, kb * BK, n0, bar);
+          }
         }
       }
       // loads still in flight land before the CTA can exit: wait for the
@@ -224,7 +281,11 @@ tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensor
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16<BN>();
+      constexpr uint32_t idesc = idesc_bf16<BN, MAJ>();
+      // descriptor step per 16 k: 32 bytes along a K-major row, 16 rows of
+      // 128 bytes down an MN-major block (in 16-byte units)
+      constexpr uint64_t a_step = (MAJ & kAMn) ? (16 * 128) >> 4 : 2;
+      constexpr uint64_t b_step = (MAJ & kBMn) ? (16 * 128) >> 4 : 2;
       int it = 0, tcount = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++tcount) {
@@ -246,10 +307,12 @@ tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensor
           }
           tc_fence_after();
           const uint32_t st = sbase + s * L::stage_bytes;
-          const uint64_t ad = desc_sw128(st), bd = desc_sw128(st + L::a_bytes);
+          const uint64_t ad = (MAJ & kAMn) ? desc_sw128_mn(st) : desc_sw128(st);
+          const uint64_t bd = (MAJ & kBMn) ? desc_sw128_mn(st + L::a_bytes)
+                                           : desc_sw128(st + L::a_bytes);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)  // 16 bf16 = 32 bytes = 2 descriptor units
-            umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(d, ad + a_step * kk, bd + b_step * kk, idesc, (kb | kk) != 0);
           umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
         if (ok) umma_commit(&acc_full[b]);
@@ -265,6 +328,10 @@ tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensor
     constexpr int kSlices = BN / 32, kFirst = (kSlices + 1) / 2;
     const int c_begin = half ? kFirst * 32 : 0, c_end = half ? BN : kFirst * 32;
     const int r = quarter * 32 + lane;
+    uint32_t *scr = Epi::kScratch
+                        ? reinterpret_cast<uint32_t *>(sm + L::scratch_offset) +
+                              (warp - 2) * kScratchWords
+                        : nullptr;
     int tcount = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tcount) {
       const int b = tcount & 1;
@@ -289,7 +356,7 @@ tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensor
         float x[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(v[e]);
-        epi.slice(row, m, n0 + c, x);
+        epi.slice(row, m, n0 + c, x, scr);
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[b]);  // the buffer may take the next tile
@@ -308,17 +375,20 @@ tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensor
 
 // A row-major bf16 matrix [rows, cols] with a row stride of ld elements
 // (ld % 8 == 0, base 16-byte aligned), read in boxes of box_rows x 64 with
-// the 128-byte swizzle; reads past rows / cols return zeros.
+// the 128-byte swizzle; reads past rows / cols return zeros.  A K-major
+// operand is [M or N rows, K cols] with box_rows = BM or BN; an MN-major one
+// [K rows, M or N cols] with box_rows = BK (a box starts at a column that is
+// a multiple of 8).
 cudaError_t make_tmap_bf16(CUtensorMap *map, const void *base, int64_t rows, int64_t cols,
                            int64_t ld, int box_rows);
 
 // Launches tc_gemm on min(#tiles, #SMs) persistent CTAs (plain launch: the
 // kernel holds all of an SM's tensor memory while it runs).
-template <int BN, class Epi>
+template <int BN, int MAJ, class Epi>
 cudaError_t launch_tc_gemm(const CUtensorMap &ta, const CUtensorMap &tb, int M, int N, int K,
                            const Epi &epi, const DeviceInfo &dev, cudaStream_t s) {
-  using L = Layout<BN>;
-  auto kern = tc_gemm<BN, Epi>;
+  using L = Layout<BN, Epi::kScratch, MAJ>;
+  auto kern = tc_gemm<BN, Epi, MAJ>;
   static bool raised[64] = {};
   if (dev.device >= 0 && dev.device < 64 && !raised[dev.device]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -76,6 +76,7 @@ def library() -> ctypes.CDLL:
                                       i64, vp, i64, vp, vp, vp, sz, vp, i32, i64, i32, i32, i32,
                                       f64, vp, f32, dt, vp]),
         "ftk_gemm_bf16": (st, [vp, i64, vp, i64, vp, i64, i64, i64, i64, vp]),
+        "ftk_gemm_bf16_ex": (st, [vp, i64, i32, vp, i64, i32, vp, i64, i64, i64, i64, vp]),
         "ftk_cce_fwd_workspace_bytes": (sz, [i64, i64]),
         "ftk_cce_bwd_workspace_bytes": (sz, [i64, i64, i64]),
         "ftk_cce_fwd": (st, [vp, i64, vp, i64, vp, i64, i64, i64, vp, vp, vp, sz, dt, vp]),
@@ -463,16 +464,21 @@ def rope_llama3_inv_freq(D: int, theta: float, factor: float, low_freq_factor: f
 
 # ------------------------------------------------------ Cut Cross-Entropy
 
-def gemm_bf16(a: torch.Tensor, b: torch.Tensor, c: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """C fp32 [M, N] = a [M, K] @ b [N, K]^T on the tensor cores (bf16 in)."""
+def gemm_bf16(a: torch.Tensor, b: torch.Tensor, c: Optional[torch.Tensor] = None,
+              a_mn: bool = False, b_mn: bool = False) -> torch.Tensor:
+    """C fp32 [M, N] = A @ B^T on the tensor cores (bf16 in).  A is a [M, K]
+    or, with a_mn, a [K, M] (then A = a^T); B is b [N, K] or, with b_mn,
+    b [K, N] (then B = b^T).  No transposed copy is made."""
     _cuda(a, b, c)
-    M, K = a.shape
-    N = b.shape[0]
-    if b.shape[1] != K or a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
-        raise ValueError("a [M, K] and b [N, K] must be bf16")
+    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16 or a.dim() != 2 or b.dim() != 2:
+        raise ValueError("a and b must be 2-D bf16")
+    K, M = a.shape if a_mn else a.shape[::-1]
+    Kb, N = b.shape if b_mn else b.shape[::-1]
+    if Kb != K:
+        raise ValueError(f"contraction sizes differ: {K} vs {Kb}")
     c = torch.empty((M, N), dtype=torch.float32, device=a.device) if c is None else c
-    _call("ftk_gemm_bf16", _ptr(a), _rows(a, "a"), _ptr(b), _rows(b, "b"), _ptr(c),
-          _rows(c, "c"), M, N, K, _stream(a))
+    _call("ftk_gemm_bf16_ex", _ptr(a), _rows(a, "a"), int(a_mn), _ptr(b), _rows(b, "b"),
+          int(b_mn), _ptr(c), _rows(c, "c"), M, N, K, _stream(a))
     return c
 
 

@@ -336,6 +336,16 @@ FTK_API ftk_status ftk_gemm_bf16(const void *a, int64_t lda, const void *b, int6
                                  float *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
                                  ftk_stream_t stream);
 
+/* The same with either operand stored the other way round: a_mn != 0 reads
+ * A from a bf16 [K, lda] array (A[m, k] = a[k * lda + m], M contiguous) and
+ * b_mn != 0 reads B from [K, ldb] (B[n, k] = b[k * ldb + n]); the tensor
+ * cores take such operands as they are, with no transposed copy.  The
+ * alignment and error rules are those of ftk_gemm_bf16, with lda >= M
+ * (ldb >= N) for an MN-major operand. */
+FTK_API ftk_status ftk_gemm_bf16_ex(const void *a, int64_t lda, int a_mn, const void *b,
+                                    int64_t ldb, int b_mn, float *c, int64_t ldc, int64_t M,
+                                    int64_t N, int64_t K, ftk_stream_t stream);
+
 /* ---------------------------------------------------- Cut Cross-Entropy */
 
 /* Cross-entropy loss of a linear LM head without materialised logits
