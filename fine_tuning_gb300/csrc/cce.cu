@@ -11,19 +11,17 @@
 // picks out the target logit, so no logit reaches HBM; a warp per row then
 // merges the partials into lse and the row losses, and one CTA sums them in
 // a fixed order.
-// Backward, per vocabulary chunk of kChunk columns: a GEMM whose epilogue
-// turns the recomputed logits into dz (bf16), written row-major and
-// transposed (T kChunk bf16 each: 134 MB for 8,192 tokens, the ~135 MB the
-// page quotes for its logits); then dh += dz W_c and dW_c = dz^T h as two
-// more GEMMs with both
-// operands K-major (W_c and h are transposed once by a plain kernel).  dh
-// accumulates in fp32 and is rounded to bf16 by the last chunk's epilogue.
-// The dW GEMMs run on a second stream with double-buffered chunk buffers,
-// overlapping the next chunk's work and filling each launch's last wave.
+// Backward, per vocabulary chunk of C columns (pick_chunk: 4,096 to 16,384,
+// sized so that the chunk's tiles fill whole waves of the SMs): a GEMM whose
+// epilogue turns the recomputed logits into dz (bf16 [T, C]: 185 MB for
+// 8,192 tokens and 11,264 columns, about the ~135 MB the page quotes for its
+// logits), then dh += dz W_c and dW_c = dz^T h as one grouped GEMM that
+// reads dz, W_c and h where they lie (MN-major where a transpose is
+// needed).  dh accumulates in fp32 and is rounded to bf16 by the last
+// chunk's epilogue.
 #include <cudaTypedefs.h>
 
 #include <cmath>
-#include <mutex>
 
 #include "tc_gemm.cuh"
 
@@ -57,7 +55,8 @@ cudaError_t make_tmap_bf16(CUtensorMap *map, const void *base, int64_t rows, int
 
 namespace {
 
-constexpr int kChunk = 8192;     // vocabulary columns per backward chunk
+constexpr int kChunkMin = 4096;   // vocabulary columns per backward chunk: chosen in
+constexpr int kChunkMax = 16384;  // [kChunkMin, kChunkMax] by pick_chunk
 constexpr int kFwdBN = 256;      // logit tile width of the forward / dz GEMMs
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -386,21 +385,59 @@ int pick_bn(int64_t n) {
   return 256;
 }
 
-// B is [b_rows, b_cols] row-major: [N, K] when K-major, [K, N] when MN-major.
-template <int MAJ, class Epi>
-cudaError_t gemm_bn(int bn, const CUtensorMap &ta, const void *b_base, int64_t b_rows,
-                    int64_t b_cols, int64_t ldb, int M, int N, int K, const Epi &epi,
-                    const DeviceInfo &dev, cudaStream_t s) {
-  alignas(64) CUtensorMap tb;
-  cudaError_t e =
-      tc::make_tmap_bf16(&tb, b_base, b_rows, b_cols, ldb, (MAJ & tc::kBMn) ? tc::BK : bn);
-  if (e != cudaSuccess) return e;
+template <int G, class Epi>
+cudaError_t launch_group(int bn, tc::Group<Epi> &g, const DeviceInfo &dev, cudaStream_t s) {
   switch (bn) {
-    case 256: return tc::launch_tc_gemm<256, MAJ>(ta, tb, M, N, K, epi, dev, s);
-    case 224: return tc::launch_tc_gemm<224, MAJ>(ta, tb, M, N, K, epi, dev, s);
-    case 192: return tc::launch_tc_gemm<192, MAJ>(ta, tb, M, N, K, epi, dev, s);
+    case 256: return tc::launch_tc_gemm<256, G>(g, dev, s);
+    case 224: return tc::launch_tc_gemm<224, G>(g, dev, s);
+    case 192: return tc::launch_tc_gemm<192, G>(g, dev, s);
     default: return cudaErrorInvalidConfiguration;
   }
+}
+
+// Estimated tensor-core time of the backward with chunks of C columns, in
+// units of one 128 x 256 x 64 MMA step, for `sms` persistent CTAs: per
+// chunk, the dz GEMM (waves of equal tiles) and the grouped dh + dW GEMM
+// (tiles dealt round-robin: dh tiles of ceil(Cv/64) steps first, then dW
+// tiles of ceil(T/64) steps; the busiest CTA sets the time), plus a fixed
+// cost per launch.
+double chunk_cost(int64_t T, int64_t H, int64_t Cv, int sms) {
+  constexpr double kLaunchSteps = 30.0;  // ~10 us of launch, fill and drain
+  const int64_t mt = (T + 127) / 128, kh = (H + 63) / 64;
+  const int64_t grad_tiles = mt * ((Cv + kFwdBN - 1) / kFwdBN);
+  const double grad = (double)((grad_tiles + sms - 1) / sms) * (double)kh;
+  const int bn = pick_bn(H);
+  const int64_t nt = (H + bn - 1) / bn;
+  const int64_t n_dh = mt * nt, n_dw = ((Cv + 127) / 128) * nt, n = n_dh + n_dw;
+  const double c_dh = (double)((Cv + 63) / 64) * bn / 256.0;
+  const double c_dw = (double)((T + 63) / 64) * bn / 256.0;
+  double worst = 0.0;
+  for (int i = 0; i < sms && i < n; ++i) {
+    const int64_t mine = (n - i + sms - 1) / sms;                   // tiles i, i + sms, ...
+    const int64_t dh = i < n_dh ? (n_dh - i + sms - 1) / sms : 0;  // of them below n_dh
+    const double t = (double)dh * c_dh + (double)(mine - dh) * c_dw;
+    worst = t > worst ? t : worst;
+  }
+  return grad + worst + 2.0 * kLaunchSteps;
+}
+
+// The backward's chunk width: V rounded up to 64 when it fits one chunk,
+// else the multiple of 256 in [kChunkMin, kChunkMax] with the least
+// estimated time (ties to the smaller chunk).
+int64_t pick_chunk(int64_t T, int64_t H, int64_t V, int sms) {
+  if (V <= kChunkMax) return round_up(V, 64);
+  int64_t best = kChunkMin;
+  double best_cost = 0.0;
+  for (int64_t C = kChunkMin; C <= kChunkMax; C += 256) {
+    const int64_t full = V / C, rest = V - full * C;
+    double cost = (double)full * chunk_cost(T, H, C, sms);
+    if (rest) cost += chunk_cost(T, H, rest, sms);
+    if (C == kChunkMin || cost < best_cost) {
+      best = C;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 }  // namespace
@@ -410,16 +447,14 @@ cudaError_t gemm_bn(int bn, const CUtensorMap &ta, const void *b_base, int64_t b
 cudaError_t launch_gemm_bf16(const void *a, int64_t lda, bool a_mn, const void *b, int64_t ldb,
                              bool b_mn, float *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
                              const DeviceInfo &dev, cudaStream_t s) {
-  alignas(64) CUtensorMap ta;
-  cudaError_t e = a_mn ? tc::make_tmap_bf16(&ta, a, K, M, lda, tc::BK)
-                       : tc::make_tmap_bf16(&ta, a, M, K, lda, tc::BM);
+  const EpiStore st{c, nullptr, ldc, 0, (int)M, (int)N, false, vec16(c) && ldc % 4 == 0, false};
+  const int bn = pick_bn(N);
+  tc::Group<EpiStore> g;
+  g.count = 1;
+  cudaError_t e = tc::make_problem(g.p[0], bn, a, lda, b, ldb, (int)M, (int)N, (int)K,
+                                   (a_mn ? tc::kAMn : 0) | (b_mn ? tc::kBMn : 0), st);
   if (e != cudaSuccess) return e;
-  EpiStore st{c, nullptr, ldc, 0, (int)M, (int)N, false, vec16(c) && ldc % 4 == 0, false};
-  const int bn = pick_bn(N), m = (int)M, n = (int)N, k = (int)K;
-  if (a_mn && b_mn) return gemm_bn<tc::kAMn | tc::kBMn>(bn, ta, b, K, N, ldb, m, n, k, st, dev, s);
-  if (a_mn) return gemm_bn<tc::kAMn>(bn, ta, b, N, K, ldb, m, n, k, st, dev, s);
-  if (b_mn) return gemm_bn<tc::kBMn>(bn, ta, b, K, N, ldb, m, n, k, st, dev, s);
-  return gemm_bn<tc::kKMajor>(bn, ta, b, N, K, ldb, m, n, k, st, dev, s);
+  return launch_group<1>(bn, g, dev, s);
 }
 
 // ------------------------------------------------------------ workspaces
@@ -430,11 +465,12 @@ size_t cce_fwd_workspace_bytes(int64_t T, int64_t V) {
 }
 
 size_t cce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
-  const int64_t C = V < kChunk ? round_up(V, 64) : kChunk;
-  const int64_t bytes = 256                         // g / N
-                        + 2 * round_up(T * C * 2, 256)  // dz, two buffers
+  // room for the widest chunk pick_chunk may choose on any device
+  const int64_t C = V <= kChunkMax ? round_up(V, 64) : kChunkMax;
+  const int64_t bytes = 256                     // g / N
+                        + round_up(T * C * 2, 256)  // dz of one chunk
                         + round_up(T * H, 64) * 4;  // dh in fp32
-  return (size_t)bytes + 4 * 256;                   // alignment of each piece
+  return (size_t)bytes + 3 * 256;               // alignment of each piece
 }
 
 namespace {
@@ -457,11 +493,12 @@ cudaError_t launch_cce_fwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t
   float2 *part = w.take<float2>((size_t)T * nparts * 8);
   float *tgt = w.take<float>((size_t)T * 4);
   float *row_loss = w.take<float>((size_t)T * 4);
-  alignas(64) CUtensorMap ta;
-  cudaError_t e = tc::make_tmap_bf16(&ta, a.h, T, H, a.ldh, tc::BM);
+  tc::Group<EpiLse> g;
+  g.count = 1;
+  cudaError_t e = tc::make_problem(g.p[0], kFwdBN, a.h, a.ldh, a.w, a.ldw, T, V, H, tc::kKMajor,
+                                   EpiLse{a.y, T, V, nparts, part, tgt});
   if (e != cudaSuccess) return e;
-  EpiLse epi{a.y, T, V, nparts, part, tgt};
-  e = gemm_bn<tc::kKMajor>(kFwdBN, ta, a.w, V, H, a.ldw, T, V, H, epi, dev, s);
+  e = tc::launch_tc_gemm<kFwdBN, 1>(g, dev, s);
   if (e != cudaSuccess) return e;
   cce_row_lse<<<(T + 7) / 8, 256, 0, s>>>(part, nparts, tgt, a.y, T, V, a.lse, row_loss);
   e = cudaGetLastError();
@@ -472,102 +509,51 @@ cudaError_t launch_cce_fwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t
 
 // A second stream per device for the backward's dW GEMMs, and the events
 // that order it against the caller's stream (created once, kept).
-struct SideStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t ready[2] = {}, done[2] = {};
-};
-
-cudaError_t side_stream(int device, SideStream **out) {
-  static std::mutex mu;
-  static SideStream side[64];
-  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  SideStream &x = side[device];
-  if (!x.s) {
-    cudaError_t e = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking);
-    for (int b = 0; e == cudaSuccess && b < 2; ++b) {
-      e = cudaEventCreateWithFlags(&x.ready[b], cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&x.done[b], cudaEventDisableTiming);
-    }
-    if (e != cudaSuccess) {
-      x.s = nullptr;
-      return e;
-    }
-  }
-  *out = &x;
-  return cudaSuccess;
-}
-
 cudaError_t launch_cce_bwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   const int T = (int)a.T, H = (int)a.H, V = (int)a.V;
-  const int64_t C = V < kChunk ? round_up(V, 64) : kChunk;
+  const int64_t C = pick_chunk(T, H, V, dev.sms);
   Carve w{(unsigned char *)a.ws};
   float *gscale = w.take<float>(256);
-  bf16 *dz[2];
-  for (int b = 0; b < 2; ++b) dz[b] = w.take<bf16>((size_t)T * C * 2);
+  bf16 *dz = w.take<bf16>((size_t)T * C * 2);
   float *dh32 = w.take<float>((size_t)round_up((int64_t)T * H, 64) * 4);
-  SideStream *side = nullptr;
-  cudaError_t e = side_stream(dev.device, &side);
-  if (e != cudaSuccess) return e;
 
   cce_finish<<<1, 1024, 0, s>>>(nullptr, a.y, T, V, nullptr, a.dloss, gscale);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  alignas(64) CUtensorMap th, tdz, tdz_mn;
-  e = tc::make_tmap_bf16(&th, a.h, T, H, a.ldh, tc::BM);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int bn_h = pick_bn(H);
-  // chunk c uses dz buffer c & 1: the caller's stream makes dz and runs dh;
-  // the side stream runs dW_c once dz is ready, overlapping dh(c) and the
-  // next chunk's dz; a buffer is reused only after its dW has read it.
-  // Only events recorded in this call are waited on, so the whole sequence
-  // can be captured into a graph.  Neither W nor h is ever transposed: the
-  // GEMMs that need W_c^T, dz^T or h^T read them MN-major.
-  bool pending[2] = {false, false};
-  int c = 0;
-  for (int64_t c0 = 0; c0 < V; c0 += C, ++c) {
-    const int b = c & 1;
+  // Per chunk, two launches on the caller's stream: dz, then dh (+)= dz W_c
+  // and dW_c = dz^T h as one grouped GEMM (their tiles fill each other's
+  // partial waves).  Neither W nor h is ever transposed: the GEMMs that
+  // need W_c^T, dz^T or h^T read them MN-major.
+  for (int64_t c0 = 0; c0 < V; c0 += C) {
     const int Cv = (int)(V - c0 < C ? V - c0 : C);
     const bool first = c0 == 0, last = c0 + C >= V;
     const bf16 *wc = (const bf16 *)a.w + c0 * a.ldw;
-    if (pending[b]) {
-      e = cudaStreamWaitEvent(s, side->done[b], 0);
-      if (e != cudaSuccess) return e;
-    }
     // dz [T x Cv] for columns [c0, c0 + Cv): A = h [T x H], B = W_c [Cv x H]
-    EpiGrad g{a.y, a.lse, gscale, T, V, Cv, (int)c0, dz[b], C};
-    e = gemm_bn<tc::kKMajor>(kFwdBN, th, wc, Cv, H, a.ldw, T, Cv, H, g, dev, s);
+    tc::Group<EpiGrad> gg;
+    gg.count = 1;
+    e = tc::make_problem(gg.p[0], kFwdBN, a.h, a.ldh, wc, a.ldw, T, Cv, H, tc::kKMajor,
+                         EpiGrad{a.y, a.lse, gscale, T, V, Cv, (int)c0, dz, C});
     if (e != cudaSuccess) return e;
-    e = cudaEventRecord(side->ready[b], s);
+    e = tc::launch_tc_gemm<kFwdBN, 1>(gg, dev, s);
     if (e != cudaSuccess) return e;
-    // dW_c = dz^T h on the side stream: A = dz^T, read MN-major from dz
-    // [T x Cv]; B = h^T, read MN-major from h [T x H]; K = T
-    e = cudaStreamWaitEvent(side->s, side->ready[b], 0);
+    tc::Group<EpiStore> gs;
+    gs.count = 2;
+    // dh (+)= dz W_c: A = dz [T x Cv] K-major; B = W_c^T, MN-major from
+    // W_c [Cv x H]; K = Cv.  fp32 partial sums, bf16 from the last chunk.
+    const EpiStore sh{dh32, last ? (bf16 *)a.dh : nullptr, (int64_t)H, a.lddh, T, H, !first,
+                      H % 4 == 0, vec16(a.dh) && a.lddh % 8 == 0};
+    e = tc::make_problem(gs.p[0], bn_h, dz, C, wc, a.ldw, T, H, Cv, tc::kBMn, sh);
     if (e != cudaSuccess) return e;
-    e = tc::make_tmap_bf16(&tdz_mn, dz[b], T, Cv, C, tc::BK);
+    // dW_c = dz^T h: A = dz^T, MN-major from dz [T x Cv]; B = h^T,
+    // MN-major from h [T x H]; K = T
+    const EpiStore sw{a.dw + c0 * a.lddw, nullptr, a.lddw, 0, Cv, H, false,
+                      vec16(a.dw) && a.lddw % 4 == 0, false};
+    e = tc::make_problem(gs.p[1], bn_h, dz, C, a.h, a.ldh, Cv, H, T, tc::kAMn | tc::kBMn, sw);
     if (e != cudaSuccess) return e;
-    EpiStore sw{a.dw + c0 * a.lddw, nullptr, a.lddw, 0, Cv, H, false,
-                vec16(a.dw) && a.lddw % 4 == 0, false};
-    e = gemm_bn<tc::kAMn | tc::kBMn>(bn_h, tdz_mn, a.h, T, H, a.ldh, Cv, H, T, sw, dev, side->s);
-    if (e != cudaSuccess) return e;
-    e = cudaEventRecord(side->done[b], side->s);
-    if (e != cudaSuccess) return e;
-    pending[b] = true;
-    // dh (+)= dz W_c on the caller's stream: A = dz [T x Cv] K-major; B =
-    // W_c^T, read MN-major from W_c [Cv x H]; K = Cv
-    e = tc::make_tmap_bf16(&tdz, dz[b], T, Cv, C, tc::BM);
-    if (e != cudaSuccess) return e;
-    EpiStore sh{dh32, last ? (bf16 *)a.dh : nullptr, (int64_t)H, a.lddh, T, H, !first,
-                H % 4 == 0, vec16(a.dh) && a.lddh % 8 == 0};
-    e = gemm_bn<tc::kBMn>(bn_h, tdz, wc, Cv, H, a.ldw, T, H, Cv, sh, dev, s);
+    e = launch_group<2>(bn_h, gs, dev, s);
     if (e != cudaSuccess) return e;
   }
-  // join: the caller's stream waits for every dW still in flight
-  for (int b = 0; b < 2; ++b)
-    if (pending[b]) {
-      e = cudaStreamWaitEvent(s, side->done[b], 0);
-      if (e != cudaSuccess) return e;
-    }
   return cudaSuccess;
 }
 
