@@ -654,10 +654,11 @@ def cce_leg(dev, flush, flush_graph, reps):
     t_flush = sum(a.elapsed_time(b) for a, b in ev["flush"]) / reps
     peak, psrc = tensor_peak()
     flops = {"cce_fwd": 2 * hw.T * hw.H * hw.V, "cce_bwd": 6 * hw.T * hw.H * hw.V}
-    nchunk = -(-hw.V // 8192)
-    launches = {"cce_fwd": 3, "cce_bwd": 1 + 3 * nchunk}
+    chunk = ftk.cce_bwd_chunk(hw.T, hw.H, hw.V)
+    nchunk = -(-hw.V // chunk)
+    launches = {"cce_fwd": 3, "cce_bwd": 1 + 2 * nchunk}
     out = {"workload": {"name": hw.name, "T": hw.T, "H": hw.H, "V": hw.V,
-                        "ignored_share": hw.ignored},
+                        "ignored_share": hw.ignored, "bwd_chunk": chunk},
            "loss": round(float(loss.item()), 6)}
     for n in graphs:
         ms = sum(a.elapsed_time(b) for a, b in ev[n]) / reps - t_flush

@@ -11,7 +11,7 @@
 // picks out the target logit, so no logit reaches HBM; a warp per row then
 // merges the partials into lse and the row losses, and one CTA sums them in
 // a fixed order.
-// Backward, per vocabulary chunk of C columns (pick_chunk: 4,096 to 16,384,
+// Backward, per vocabulary chunk of C columns (cce_bwd_chunk: 4,096 to 16,384,
 // sized so that the chunk's tiles fill whole waves of the SMs): a GEMM whose
 // epilogue turns the recomputed logits into dz (bf16 [T, C]: 185 MB for
 // 8,192 tokens and 11,264 columns, about the ~135 MB the page quotes for its
@@ -56,7 +56,7 @@ cudaError_t make_tmap_bf16(CUtensorMap *map, const void *base, int64_t rows, int
 namespace {
 
 constexpr int kChunkMin = 4096;   // vocabulary columns per backward chunk: chosen in
-constexpr int kChunkMax = 16384;  // [kChunkMin, kChunkMax] by pick_chunk
+constexpr int kChunkMax = 16384;  // [kChunkMin, kChunkMax] by cce_bwd_chunk
 constexpr int kFwdBN = 256;      // logit tile width of the forward / dz GEMMs
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -395,43 +395,46 @@ cudaError_t launch_group(int bn, tc::Group<Epi> &g, const DeviceInfo &dev, cudaS
   }
 }
 
-// Estimated tensor-core time of the backward with chunks of C columns, in
-// units of one 128 x 256 x 64 MMA step, for `sms` persistent CTAs: per
-// chunk, the dz GEMM (waves of equal tiles) and the grouped dh + dW GEMM
-// (tiles dealt round-robin: dh tiles of ceil(Cv/64) steps first, then dW
-// tiles of ceil(T/64) steps; the busiest CTA sets the time), plus a fixed
-// cost per launch.
-double chunk_cost(int64_t T, int64_t H, int64_t Cv, int sms) {
+// Estimated tensor-core time of the backward with chunks of Cv columns, in
+// k-steps of one CTA pair, for `pairs` persistent pairs: per chunk, the dz
+// GEMM (waves of equal units) and the grouped dh + dW GEMM (units dealt
+// round-robin: dh units of ceil(Cv/64) steps first, then dW units of
+// ceil(T/64) steps; the busiest pair sets the time), plus a fixed cost per
+// launch.  A unit is two 128-row tiles of one N-tile (tc_gemm.cuh).
+double chunk_cost(int64_t T, int64_t H, int64_t Cv, int pairs) {
   constexpr double kLaunchSteps = 30.0;  // ~10 us of launch, fill and drain
-  const int64_t mt = (T + 127) / 128, kh = (H + 63) / 64;
-  const int64_t grad_tiles = mt * ((Cv + kFwdBN - 1) / kFwdBN);
-  const double grad = (double)((grad_tiles + sms - 1) / sms) * (double)kh;
+  const int64_t mp = ((T + 127) / 128 + 1) / 2, kh = (H + 63) / 64;
+  const int64_t grad_units = mp * ((Cv + kFwdBN - 1) / kFwdBN);
+  const double grad = (double)((grad_units + pairs - 1) / pairs) * (double)kh;
   const int bn = pick_bn(H);
   const int64_t nt = (H + bn - 1) / bn;
-  const int64_t n_dh = mt * nt, n_dw = ((Cv + 127) / 128) * nt, n = n_dh + n_dw;
+  const int64_t n_dh = mp * nt, n_dw = (((Cv + 127) / 128 + 1) / 2) * nt, n = n_dh + n_dw;
   const double c_dh = (double)((Cv + 63) / 64) * bn / 256.0;
   const double c_dw = (double)((T + 63) / 64) * bn / 256.0;
   double worst = 0.0;
-  for (int i = 0; i < sms && i < n; ++i) {
-    const int64_t mine = (n - i + sms - 1) / sms;                   // tiles i, i + sms, ...
-    const int64_t dh = i < n_dh ? (n_dh - i + sms - 1) / sms : 0;  // of them below n_dh
+  for (int i = 0; i < pairs && i < n; ++i) {
+    const int64_t mine = (n - i + pairs - 1) / pairs;                 // units i, i + pairs, ...
+    const int64_t dh = i < n_dh ? (n_dh - i + pairs - 1) / pairs : 0;  // of them below n_dh
     const double t = (double)dh * c_dh + (double)(mine - dh) * c_dw;
     worst = t > worst ? t : worst;
   }
   return grad + worst + 2.0 * kLaunchSteps;
 }
 
-// The backward's chunk width: V rounded up to 64 when it fits one chunk,
-// else the multiple of 256 in [kChunkMin, kChunkMax] with the least
-// estimated time (ties to the smaller chunk).
-int64_t pick_chunk(int64_t T, int64_t H, int64_t V, int sms) {
+}  // namespace
+
+// The backward's chunk width on a device with `sms` SMs: V rounded up to 64
+// when it fits one chunk, else the multiple of 256 in [kChunkMin,
+// kChunkMax] with the least estimated time (ties to the smaller chunk).
+int64_t cce_bwd_chunk(int64_t T, int64_t H, int64_t V, int sms) {
   if (V <= kChunkMax) return round_up(V, 64);
+  const int pairs = sms / 2 > 0 ? sms / 2 : 1;
   int64_t best = kChunkMin;
   double best_cost = 0.0;
   for (int64_t C = kChunkMin; C <= kChunkMax; C += 256) {
     const int64_t full = V / C, rest = V - full * C;
-    double cost = (double)full * chunk_cost(T, H, C, sms);
-    if (rest) cost += chunk_cost(T, H, rest, sms);
+    double cost = (double)full * chunk_cost(T, H, C, pairs);
+    if (rest) cost += chunk_cost(T, H, rest, pairs);
     if (C == kChunkMin || cost < best_cost) {
       best = C;
       best_cost = cost;
@@ -439,8 +442,6 @@ int64_t pick_chunk(int64_t T, int64_t H, int64_t V, int sms) {
   }
   return best;
 }
-
-}  // namespace
 
 // ------------------------------------------------------------ plain GEMM
 
@@ -511,7 +512,7 @@ cudaError_t launch_cce_fwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t
 // that order it against the caller's stream (created once, kept).
 cudaError_t launch_cce_bwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   const int T = (int)a.T, H = (int)a.H, V = (int)a.V;
-  const int64_t C = pick_chunk(T, H, V, dev.sms);
+  const int64_t C = cce_bwd_chunk(T, H, V, dev.sms);
   Carve w{(unsigned char *)a.ws};
   float *gscale = w.take<float>(256);
   bf16 *dz = w.take<bf16>((size_t)T * C * 2);

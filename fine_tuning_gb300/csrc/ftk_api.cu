@@ -711,6 +711,11 @@ FTK_API size_t ftk_cce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
   return ftk::cce_bwd_workspace_bytes(T, H, V);
 }
 
+FTK_API int64_t ftk_cce_bwd_chunk(int64_t T, int64_t H, int64_t V, int32_t sms) {
+  if (T <= 0 || H <= 0 || V <= 0 || sms <= 0) return 0;
+  return ftk::cce_bwd_chunk(T, H, V, sms);
+}
+
 }  // extern "C"
 
 namespace {

@@ -227,6 +227,7 @@ struct CceArgs {
 };
 size_t cce_fwd_workspace_bytes(int64_t T, int64_t V);
 size_t cce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V);
+int64_t cce_bwd_chunk(int64_t T, int64_t H, int64_t V, int sms);
 cudaError_t launch_cce_fwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t s);
 cudaError_t launch_cce_bwd(const CceArgs &a, const DeviceInfo &dev, cudaStream_t s);
 // C fp32 [M, ldc] = A B^T on the tensor cores (bf16, tc_gemm.cuh): A stored

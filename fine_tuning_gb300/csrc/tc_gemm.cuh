@@ -237,6 +237,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 }
 
 
+// Brings the box of map at (x, y) into L2 without copying it anywhere.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -425,6 +433,21 @@ tc_gemm(const __grid_constant__ Group<Epi> g, unsigned *status, long long wait_l
         const Sh mine(maj, P.M, P.N, m0, n0, rank);
         const uint32_t tx = leader ? mine.bytes + Sh(maj, P.M, P.N, m0, n0, 1).bytes : 0;
         const int ma = m0 + (int)rank * BM, nb = n0 + (int)rank * L::kHalf;
+        // When units run M fastest, the pairs working at a time share two or
+        // three B tiles, and every pair starts a new one together: the pair
+        // whose next unit opens an N-tile (M-pair 0) fetches that tile's B
+        // half into L2 one unit ahead, so the others find it there.
+        if (u + ncl < nunits) {
+          int pm0, pn0;
+          Seq sn;
+          const int pj = unit_of<BN, G>(q, u + ncl, pm0, pn0, sn);
+          if (!sn.n_fast && pm0 == 0 && !(sn.maj & kBMn)) {
+            const Problem<Epi> &Pn = pj ? g.p[G - 1] : g.p[0];
+            const int nbn = pn0 + (int)rank * L::kHalf;
+            if (nbn < Pn.N)
+              for (int kb = 0; kb < sn.nk; ++kb) tma_prefetch_2d(&Pn.tb, kb * BK, nbn);
+          }
+        }
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kStages;
           if (*abort_flag ||

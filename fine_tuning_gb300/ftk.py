@@ -79,6 +79,7 @@ def library() -> ctypes.CDLL:
         "ftk_gemm_bf16_ex": (st, [vp, i64, i32, vp, i64, i32, vp, i64, i64, i64, i64, vp]),
         "ftk_cce_fwd_workspace_bytes": (sz, [i64, i64]),
         "ftk_cce_bwd_workspace_bytes": (sz, [i64, i64, i64]),
+        "ftk_cce_bwd_chunk": (i64, [i64, i64, i64, i32]),
         "ftk_cce_fwd": (st, [vp, i64, vp, i64, vp, i64, i64, i64, vp, vp, vp, sz, dt, vp]),
         "ftk_cce_bwd": (st, [vp, i64, vp, i64, vp, vp, vp, i64, i64, i64, vp, i64, vp, i64, vp,
                              sz, dt, vp]),
@@ -506,6 +507,14 @@ def cce_fwd(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, loss=None, lse=No
           _ptr(loss), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
           _code(h), _stream(h))
     return loss, lse
+
+
+def cce_bwd_chunk(T: int, H: int, V: int, sms: Optional[int] = None) -> int:
+    """The vocabulary chunk width cce_bwd uses for these sizes on a device
+    with `sms` SMs (default: the current CUDA device's count)."""
+    if sms is None:
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return int(library().ftk_cce_bwd_chunk(T, H, V, sms))
 
 
 def cce_bwd(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, lse: torch.Tensor,

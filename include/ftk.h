@@ -375,11 +375,20 @@ FTK_API ftk_status ftk_cce_fwd(const void *h, int64_t ldh, const void *w, int64_
  *   dh = dz W  -> bf16 [T, lddh],     dW = dz^T h  -> fp32 [V, lddw]
  * dz is rounded to bf16 before the two contractions (the tensor cores take
  * bf16 operands); they accumulate in fp32.  The logits are recomputed a
- * vocabulary chunk of 8,192 columns at a time.  lse from the forward.
- * workspace: >= ftk_cce_bwd_workspace_bytes(T, H, V) bytes, 256-byte
- * aligned.  dh and dW are overwritten; no output may overlap an input or
- * another output. */
+ * vocabulary chunk at a time (ftk_cce_bwd_chunk columns, 4,096 to 16,384,
+ * or all of V when V <= 16,384), two launches per chunk.  lse from the
+ * forward.  workspace: >= ftk_cce_bwd_workspace_bytes(T, H, V) bytes,
+ * 256-byte aligned (enough for any chunk width).  dh and dW are
+ * overwritten; no output may overlap an input or another output.
+ * dh is summed over the chunks in a fixed order and dW written once per
+ * element: both are bitwise reproducible run to run. */
 FTK_API size_t ftk_cce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V);
+
+/* The vocabulary chunk width ftk_cce_bwd uses on a device with `sms` SMs:
+ * the one (a multiple of 256) whose dz and dh + dW launches fill the SMs'
+ * waves best by a static estimate.  Host-only; 0 for a non-positive
+ * argument. */
+FTK_API int64_t ftk_cce_bwd_chunk(int64_t T, int64_t H, int64_t V, int32_t sms);
 FTK_API ftk_status ftk_cce_bwd(const void *h, int64_t ldh, const void *w, int64_t ldw,
                                const int32_t *y, const float *lse, const float *dloss,
                                int64_t T, int64_t H, int64_t V, void *dh, int64_t lddh,

@@ -241,3 +241,24 @@ def test_workspace_query_rejects_bad_arguments(lib):
     assert lib.ftk_rmsnorm_bwd_workspace_bytes(0, 64, BF16) == 0
     assert lib.ftk_rmsnorm_bwd_workspace_bytes(16, 0, BF16) == 0
     assert lib.ftk_rmsnorm_bwd_workspace_bytes(16, 64, 9) == 0
+
+
+def test_cce_backward_chunk_choice(lib):
+    """The backward's vocabulary chunk: all of V (rounded up to 64) when V
+    fits one chunk, else a multiple of 256 in [4096, 16384] whose workspace
+    the query covers; pure host logic, the same answer every time."""
+    lib.ftk_cce_bwd_chunk.restype = ctypes.c_int64
+    lib.ftk_cce_bwd_chunk.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int32]
+    lib.ftk_cce_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.ftk_cce_bwd_workspace_bytes.argtypes = [ctypes.c_int64] * 3
+    assert lib.ftk_cce_bwd_chunk(300, 64, 1000, 152) == 1024
+    assert lib.ftk_cce_bwd_chunk(8192, 896, 16384, 152) == 16384
+    for T, H, V, sms in [(8192, 896, 151936, 152), (8192, 2048, 128256, 152),
+                         (4096, 4096, 151936, 148), (1, 64, 100000, 2)]:
+        C = lib.ftk_cce_bwd_chunk(T, H, V, sms)
+        assert C % 256 == 0 and 4096 <= C <= 16384, (T, H, V, C)
+        assert C == lib.ftk_cce_bwd_chunk(T, H, V, sms)
+        assert lib.ftk_cce_bwd_workspace_bytes(T, H, V) >= T * C * 2 + T * H * 4
+    for bad in [(0, 896, 151936, 152), (8192, 0, 151936, 152), (8192, 896, 0, 152),
+                (8192, 896, 151936, 0)]:
+        assert lib.ftk_cce_bwd_chunk(*bad) == 0
