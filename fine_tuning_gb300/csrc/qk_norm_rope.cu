@@ -88,6 +88,30 @@ __device__ __forceinline__ void token_table(float2 *wt, const float2 *freq, int 
   }
 }
 
+// Per-thread asynchronous copies into shared memory (cp.async; 16 bytes
+// bypassing L1, or 4 bytes), committed and waited for in groups.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int K> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory");
+}
+
+// The backward warp kernel's staging: per warp kBwdBufs buffers of 5 x 32
+// 16-byte slots (gradient halves, pre-norm halves, r; slot c of lane l at
+// c * 32 + l, so a warp's accesses to one slot are contiguous); the loads
+// run kBwdBufs - 1 head passes ahead of the arithmetic.
+constexpr int kBwdSlots = 5, kBwdBufs = 2;
+constexpr size_t kBwdStageBytes = sizeof(uint4) * kWarps * kBwdBufs * kBwdSlots * 32;
+
 template <typename T, typename Idx, int N, int HPT>
 __global__ void __launch_bounds__(kThreads, 2)
 qk_norm_rope_fwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ RopeFreqs fr) {
@@ -215,7 +239,9 @@ __device__ __forceinline__ void write_partial(float (&acc)[4][N], float *part, f
 template <typename T, typename Idx, int N, bool HAS_RSTD>
 __global__ void __launch_bounds__(kThreads, 2)
 qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ RopeFreqs fr) {
-  extern __shared__ float2 tab[];  // [warps][D/2] (cos, -sin), then [warps][2D] fp32 partials
+  // [warps][D/2] (cos, -sin), then [warps][2D] fp32 partials, then the
+  // staging buffers (16-byte aligned: D is a multiple of 8 here)
+  extern __shared__ float2 tab[];
   __shared__ float2 freq[kRopeMaxHalf];
   const int D = a.D, half = D >> 1, NV = half / N, S = 32 / NV, NH = a.Hq + a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -225,15 +251,8 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
-  Packet<T, N> wq1, wq2, wk1, wk2;
-  if (a.Hq > 0) {
-    wq1 = load_packet<T, N>(a.wq + j * N);
-    wq2 = load_packet<T, N>(a.wq + half + j * N);
-  }
-  if (a.Hkv > 0) {
-    wk1 = load_packet<T, N>(a.wk + j * N);
-    wk2 = load_packet<T, N>(a.wk + half + j * N);
-  }
+  // the norm weights are re-read per head (L1 hits) rather than held in
+  // registers, which go to the four accumulators below
   float acc[4][N];  // dwq first half, dwq second half, dwk first half, dwk second half
 #pragma unroll
   for (int g = 0; g < 4; ++g)
@@ -242,44 +261,85 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   __syncthreads();  // the frequency table
 
   float2 *wt = tab + warp * half;
+  uint4 *stg =
+      reinterpret_cast<uint4 *>(part + kWarps * 2 * D) + warp * (kBwdBufs * kBwdSlots * 32);
   const Idx step = (Idx)gridDim.x * kWarps;
-  for (Idx t = (Idx)blockIdx.x * kWarps + warp; t < a.rows; t += step) {
-    const T *gq = a.gq + t * a.ld_gq + (Idx)j * N, *gk = a.gk + t * a.ld_gk + (Idx)j * N;
-    const T *vq = a.q + t * a.ld_q + (Idx)j * N, *vk = a.k + t * a.ld_k + (Idx)j * N;
-    __syncwarp();  // the previous token's table has been read
-    token_table(wt, freq, half, position_of<Idx>(t, a.cu, a.B), -1.0f, lane);
-    __syncwarp();
-    float cv[N], sv[N];
-#pragma unroll
-    for (int e = 0; e < N; ++e) {
-      const float2 v = wt[j * N + e];
-      cv[e] = v.x;
-      sv[e] = v.y;
+  const int passes = (NH + S - 1) / S;  // head passes per token, the same on every lane
+  // Copies this lane's packets of (token tt, head pass p) into buffer b: both
+  // halves of the output gradient and of the pre-norm input, and r.  Every
+  // lane commits one group per pass, empty or not.
+  auto stage = [&](Idx tt, int p, int b) {
+    const int h = slot + p * S;
+    if (tt < a.rows && h < NH) {
+      const bool isq = h < a.Hq;
+      const int hk = h - a.Hq;
+      const T *gp = (isq ? a.gq + tt * a.ld_gq + (Idx)h * D : a.gk + tt * a.ld_gk + (Idx)hk * D) +
+                    j * N;
+      const T *vp =
+          (isq ? a.q + tt * a.ld_q + (Idx)h * D : a.k + tt * a.ld_k + (Idx)hk * D) + j * N;
+      uint4 *d = stg + b * kBwdSlots * 32 + lane;
+      cp_async16(d, gp);
+      cp_async16(d + 32, gp + half);
+      cp_async16(d + 64, vp);
+      cp_async16(d + 96, vp + half);
+      if (HAS_RSTD) cp_async4(d + 128, isq ? a.rq + tt * a.Hq + h : a.rk + tt * a.Hkv + hk);
     }
-    for (int h = slot; h - slot < NH; h += S) {  // uniform trip count across the warp
+    cp_async_commit();
+  };
+  // (cos, -sin) of this lane's columns are read from the table per head
+  // rather than held in registers
+  const float2 *cs_j = wt + j * N;
+  // (t, p): the pass computed now; (t2, p2): the last pass staged
+  auto advance = [&](Idx &tt, int &pp) {
+    if (++pp == passes) {
+      pp = 0;
+      tt += step;
+    }
+  };
+  Idx t = (Idx)blockIdx.x * kWarps + warp, t2 = t;
+  int p = 0, p2 = 0, b = 0;
+  stage(t2, p2, 0);
+  for (int i = 1; i < kBwdBufs - 1; ++i) {
+    advance(t2, p2);
+    stage(t2, p2, i);
+  }
+  while (t < a.rows) {  // warp-uniform
+    advance(t2, p2);
+    // the pass kBwdBufs - 1 ahead goes into the buffer computed last time
+    stage(t2, p2, b == 0 ? kBwdBufs - 1 : b - 1);
+    if (p == 0) {
+      __syncwarp();  // the previous token's table has been read
+      token_table(wt, freq, half, position_of<Idx>(t, a.cu, a.B), -1.0f, lane);
+      __syncwarp();
+    }
+    cp_async_wait<kBwdBufs - 1>();  // this lane's copies for (t, p) have landed
+    {
+      const int h = slot + p * S;
       const bool act = h < NH;
       const bool isq = h < a.Hq;
       const int hk = h - a.Hq;
-      Packet<T, N> g1, g2, v1, v2;
+      Packet<T, N> g1, g2, v1, v2, w1, w2;
       float r = 0.f;
       if (act) {
-        const T *gp = isq ? gq + (Idx)h * D : gk + (Idx)hk * D;
-        const T *vp = isq ? vq + (Idx)h * D : vk + (Idx)hk * D;
-        g1 = load_packet<T, N>(gp);
-        g2 = load_packet<T, N>(gp + half);
-        v1 = load_packet<T, N>(vp);
-        v2 = load_packet<T, N>(vp + half);
-        if (HAS_RSTD) r = isq ? a.rq[t * a.Hq + h] : a.rk[t * a.Hkv + hk];
+        const uint4 *d = stg + b * kBwdSlots * 32 + lane;
+        const T *wp = (isq ? a.wq : a.wk) + j * N;
+        *reinterpret_cast<uint4 *>(&g1) = d[0];
+        *reinterpret_cast<uint4 *>(&g2) = d[32];
+        *reinterpret_cast<uint4 *>(&v1) = d[64];
+        *reinterpret_cast<uint4 *>(&v2) = d[96];
+        w1 = load_packet<T, N>(wp);
+        w2 = load_packet<T, N>(wp + half);
+        if (HAS_RSTD) r = *reinterpret_cast<const float *>(d + 128);
       }
-      const Packet<T, N> &w1 = isq ? wq1 : wk1, &w2 = isq ? wq2 : wk2;
       float dn1[N], dn2[N];
       float2 cs = make_float2(0.f, 0.f);  // (sum dn w v, sum v v)
       if (act) {
 #pragma unroll
         for (int e = 0; e < N; ++e) {
           const float a1 = g1.get(e), a2 = g2.get(e);
-          dn1[e] = fmaf(a1, cv[e], -a2 * sv[e]);
-          dn2[e] = fmaf(a2, cv[e], a1 * sv[e]);
+          const float2 c = cs_j[e];
+          dn1[e] = fmaf(a1, c.x, -a2 * c.y);
+          dn2[e] = fmaf(a2, c.x, a1 * c.y);
           const float u1 = v1.get(e), u2 = v2.get(e);
           cs.x = fmaf(dn1[e] * w1.get(e), u1, fmaf(dn2[e] * w2.get(e), u2, cs.x));
           if (!HAS_RSTD) cs.y = fmaf(u1, u1, fmaf(u2, u2, cs.y));
@@ -293,21 +353,29 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
         if (!HAS_RSTD) r = rsqrtf(fmaf(cs.y, a.inv_d, a.eps));
         const float am = r * r * r * cs.x * a.inv_d;
         Packet<T, N> o1, o2;
-        const int g0 = isq ? 0 : 2;
+        // fixed accumulator indices (a runtime index would put acc in
+        // local memory): a q head adds to 0 and 1, a k head to 2 and 3
+        const float rq_ = isq ? r : 0.f, rk_ = isq ? 0.f : r;
 #pragma unroll
         for (int e = 0; e < N; ++e) {
           const float u1 = v1.get(e), u2 = v2.get(e);
           o1.set(e, fmaf(-am, u1, r * w1.get(e) * dn1[e]));
           o2.set(e, fmaf(-am, u2, r * w2.get(e) * dn2[e]));
-          acc[g0][e] = fmaf(dn1[e] * u1, r, acc[g0][e]);
-          acc[g0 + 1][e] = fmaf(dn2[e] * u2, r, acc[g0 + 1][e]);
+          const float p1 = dn1[e] * u1, p2 = dn2[e] * u2;
+          acc[0][e] = fmaf(p1, rq_, acc[0][e]);
+          acc[1][e] = fmaf(p2, rq_, acc[1][e]);
+          acc[2][e] = fmaf(p1, rk_, acc[2][e]);
+          acc[3][e] = fmaf(p2, rk_, acc[3][e]);
         }
         T *dst = isq ? a.oq + t * a.ld_oq + (Idx)h * D : a.ok + t * a.ld_ok + (Idx)hk * D;
         store_packet<T, N>(dst + (Idx)j * N, o1);
         store_packet<T, N>(dst + half + (Idx)j * N, o2);
       }
     }
+    advance(t, p);
+    b = b + 1 == kBwdBufs ? 0 : b + 1;
   }
+  cp_async_wait<0>();
   write_partial<N>(acc, part, a.ws, D, NV, j, lane, warp);
 }
 
@@ -753,8 +821,8 @@ template <typename T, typename Idx>
 cudaError_t bwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &fr,
                       const DeviceInfo &dev, cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
-  const size_t smem =
-      sizeof(float2) * (size_t)kWarps * (a.D / 2) + sizeof(float) * (size_t)kWarps * 2 * a.D;
+  const size_t smem = sizeof(float2) * (size_t)kWarps * (a.D / 2) +
+                      sizeof(float) * (size_t)kWarps * 2 * a.D + (warp_path ? kBwdStageBytes : 0);
   const bool rstd = a.rq != nullptr || a.rk != nullptr;
   const void *kern =
       warp_path ? (rstd ? (const void *)qk_norm_rope_bwd_warp<T, Idx, NV, true>
