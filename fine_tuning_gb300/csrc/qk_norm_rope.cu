@@ -16,16 +16,19 @@
 // (seventnews.com) and optimisation (1) of "Chronicals" (arXiv 2601.02609,
 // abstract); the norm in front of the rotation is this library's variant.
 //
-// One warp per token (the layout of qk_rope_warp): half a head is NV = D/2N
+// Warp per token (the layout of qk_rope_warp): half a head is NV = D/2N
 // packets and NV divides 32, so lane (slot, j) owns packet j of both halves
 // of heads slot, slot + S, ... (S = 32 / NV).  A head's sum of squares is a
 // shuffle reduction over its NV lanes.  cos/sin of the token's D/2 angles
-// are computed once into the warp's shared-memory slice.  The backward is
-// persistent; each lane keeps its columns' dwq and dwk sums in registers,
-// the CTA combines its warps in a fixed order into one partial row [2D], and
-// dw_reduce sums the rows in a fixed order: bitwise reproducible.  Shapes
-// whose half head does not split evenly over lanes, or unaligned rows, take
-// the element-wise kernels (lane i owns pairs i, i + 32, ...).
+// are computed once into the warp's shared-memory slice.  Both directions
+// are persistent and walk (token, head pass) pairs, each lane copying its
+// packets of the passes ahead into a per-warp shared-memory ring with
+// cp.async while it computes the current one.  The backward keeps each
+// lane's dwq and dwk column sums in registers, the CTA combines its warps in
+// a fixed order into one partial row [2D], and dw_reduce sums the rows in a
+// fixed order: bitwise reproducible.  Shapes whose half head does not split
+// evenly over lanes, or unaligned rows, take the element-wise kernels (lane
+// i owns pairs i, i + 32, ...).
 #include "common.cuh"
 #include "dw_reduce.cuh"
 #include "launch.h"
@@ -110,99 +113,112 @@ template <int K> __device__ __forceinline__ void cp_async_wait() {
 // c * 32 + l, so a warp's accesses to one slot are contiguous); the loads
 // run kBwdBufs - 1 head passes ahead of the arithmetic.
 constexpr int kBwdSlots = 5, kBwdBufs = 2;
+constexpr int kFwdPipeBlocks = 4;  // CTAs per SM the pipelined forward is compiled for
 constexpr size_t kBwdStageBytes = sizeof(uint4) * kWarps * kBwdBufs * kBwdSlots * 32;
 
-template <typename T, typename Idx, int N, int HPT>
-__global__ void __launch_bounds__(kThreads, 2)
-qk_norm_rope_fwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ RopeFreqs fr) {
-  extern __shared__ float2 tab[];  // [warps][D/2] (cos, sin)
+// The forward, persistent: each warp walks tokens t, t +
+// P * kWarps, ... and each token's heads in passes of S heads (lane (slot,
+// j) normalises and rotates packet j of both halves of head slot + S p).
+// Each lane copies its packets of the next pass into a per-warp
+// shared-memory buffer with cp.async while it computes the current pass,
+// so the loads of consecutive passes and tokens overlap the arithmetic.
+constexpr int kFwdSlots = 2, kFwdBufs = 4;
+constexpr size_t kFwdStageBytes = sizeof(uint4) * kWarps * kFwdBufs * kFwdSlots * 32;
+
+template <typename T, typename Idx, int N>
+__global__ void __launch_bounds__(kThreads, kFwdPipeBlocks)
+qk_norm_rope_fwd_pipe(const NormRopeParams<T, Idx> a, const __grid_constant__ RopeFreqs fr) {
+  // [warps][D/2] (cos, sin), then the staging buffers (16-byte aligned: D
+  // is a multiple of 8 here)
+  extern __shared__ float2 tab[];
   __shared__ float2 freq[kRopeMaxHalf];
   const int D = a.D, half = D >> 1, NV = half / N, S = 32 / NV, NH = a.Hq + a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = lane % NV, slot = lane / NV;
-  const Idx t = (Idx)blockIdx.x * kWarps + warp;
-  const bool live = t < a.rows;
-  const T *qin = a.q + t * a.ld_q + (Idx)j * N, *kin = a.k + t * a.ld_k + (Idx)j * N;
-  auto src = [&](int h) { return h < a.Hq ? qin + (Idx)h * D : kin + (Idx)(h - a.Hq) * D; };
+  float2 *wt = tab + warp * half;
+  uint4 *stg = reinterpret_cast<uint4 *>(tab + kWarps * half) + warp * (kFwdBufs * kFwdSlots * 32);
 
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
-  Packet<T, N> x1[HPT], x2[HPT];
-#pragma unroll
-  for (int m = 0; m < HPT; ++m) {
-    const int h = slot + m * S;
-    if (live && h < NH) {
-      x1[m] = load_packet<T, N>(src(h));
-      x2[m] = load_packet<T, N>(src(h) + half);
-    }
-  }
-  Packet<T, N> wq1, wq2, wk1, wk2;
-  if (a.Hq > 0) {
-    wq1 = load_packet<T, N>(a.wq + j * N);
-    wq2 = load_packet<T, N>(a.wq + half + j * N);
-  }
-  if (a.Hkv > 0) {
-    wk1 = load_packet<T, N>(a.wk + j * N);
-    wk2 = load_packet<T, N>(a.wk + half + j * N);
-  }
   __syncthreads();  // the frequency table
-  if (!live) return;  // the whole warp: t is uniform across it
 
-  float2 *wt = tab + warp * half;
-  token_table(wt, freq, half, position_of<Idx>(t, a.cu, a.B), 1.0f, lane);
-  __syncwarp();
-  float cv[N], sv[N];
-#pragma unroll
-  for (int e = 0; e < N; ++e) {
-    const float2 v = wt[j * N + e];
-    cv[e] = v.x;
-    sv[e] = v.y;
+  const Idx step = (Idx)gridDim.x * kWarps;
+  const int passes = (NH + S - 1) / S;  // head passes per token, the same on every lane
+  auto stage = [&](Idx tt, int p, int b) {
+    const int h = slot + p * S;
+    if (tt < a.rows && h < NH) {
+      const T *vp = (h < a.Hq ? a.q + tt * a.ld_q + (Idx)h * D
+                              : a.k + tt * a.ld_k + (Idx)(h - a.Hq) * D) +
+                    j * N;
+      uint4 *d = stg + b * kFwdSlots * 32 + lane;
+      cp_async16(d, vp);
+      cp_async16(d + 32, vp + half);
+    }
+    cp_async_commit();  // one group per pass on every lane, empty or not
+  };
+  const float2 *cs_j = wt + j * N;
+  Idx t = (Idx)blockIdx.x * kWarps + warp, t2 = t;
+  int p = 0, p2 = 0, b = 0;
+  auto advance = [&](Idx &tt, int &pp) {
+    if (++pp == passes) {
+      pp = 0;
+      tt += step;
+    }
+  };
+  stage(t2, p2, 0);
+  for (int i = 1; i < kFwdBufs - 1; ++i) {
+    advance(t2, p2);
+    stage(t2, p2, i);
   }
-  for (int h0 = 0; h0 < NH; h0 += HPT * S) {
+  while (t < a.rows) {  // warp-uniform
+    advance(t2, p2);
+    stage(t2, p2, b == 0 ? kFwdBufs - 1 : b - 1);  // the next pass's loads fly meanwhile
+    if (p == 0) {
+      __syncwarp();  // the previous token's table has been read
+      token_table(wt, freq, half, position_of<Idx>(t, a.cu, a.B), 1.0f, lane);
+      __syncwarp();
+    }
+    cp_async_wait<kFwdBufs - 1>();  // this lane's copies for (t, p) have landed
+    const int h = slot + p * S;
+    const bool act = h < NH, isq = h < a.Hq;
+    Packet<T, N> x1, x2;
+    float ss = 0.f;
+    if (act) {
+      const uint4 *d = stg + b * kFwdSlots * 32 + lane;
+      *reinterpret_cast<uint4 *>(&x1) = d[0];
+      *reinterpret_cast<uint4 *>(&x2) = d[32];
 #pragma unroll
-    for (int m = 0; m < HPT; ++m) {
-      const int h = h0 + slot + m * S;
-      const bool act = h < NH;
-      float ss = 0.f;
-      if (act) {
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-          const float u1 = x1[m].get(e), u2 = x2[m].get(e);
-          ss = fmaf(u1, u1, fmaf(u2, u2, ss));
-        }
-      }
-      ss = slot_sum(ss, NV);  // every lane takes part
-      if (act) {
-        const float r = rsqrtf(fmaf(ss, a.inv_d, a.eps));
-        const bool isq = h < a.Hq;
-        const Packet<T, N> &w1 = isq ? wq1 : wk1, &w2 = isq ? wq2 : wk2;
-        Packet<T, N> o1, o2;
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-          const float n1 = x1[m].get(e) * r * w1.get(e), n2 = x2[m].get(e) * r * w2.get(e);
-          o1.set(e, fmaf(n1, cv[e], -n2 * sv[e]));
-          o2.set(e, fmaf(n2, cv[e], n1 * sv[e]));
-        }
-        T *dst = isq ? a.oq + t * a.ld_oq + (Idx)h * D : a.ok + t * a.ld_ok + (Idx)(h - a.Hq) * D;
-        store_packet<T, N>(dst + (Idx)j * N, o1);
-        store_packet<T, N>(dst + half + (Idx)j * N, o2);
-        if (j == 0) {
-          if (isq && a.rq) a.rq[t * a.Hq + h] = r;
-          if (!isq && a.rk) a.rk[t * a.Hkv + (h - a.Hq)] = r;
-        }
+      for (int e = 0; e < N; ++e) {
+        const float u1 = x1.get(e), u2 = x2.get(e);
+        ss = fmaf(u1, u1, fmaf(u2, u2, ss));
       }
     }
-    const int next = h0 + HPT * S;
+    ss = slot_sum(ss, NV);  // every lane takes part
+    if (act) {
+      const float r = rsqrtf(fmaf(ss, a.inv_d, a.eps));
+      const T *wp = (isq ? a.wq : a.wk) + j * N;  // L1 hits
+      const Packet<T, N> w1 = load_packet<T, N>(wp), w2 = load_packet<T, N>(wp + half);
+      Packet<T, N> o1, o2;
 #pragma unroll
-    for (int m = 0; m < HPT; ++m) {
-      const int h = next + slot + m * S;
-      if (h < NH) {
-        x1[m] = load_packet<T, N>(src(h));
-        x2[m] = load_packet<T, N>(src(h) + half);
+      for (int e = 0; e < N; ++e) {
+        const float2 c = cs_j[e];
+        const float n1 = x1.get(e) * r * w1.get(e), n2 = x2.get(e) * r * w2.get(e);
+        o1.set(e, fmaf(n1, c.x, -n2 * c.y));
+        o2.set(e, fmaf(n2, c.x, n1 * c.y));
+      }
+      T *dst = isq ? a.oq + t * a.ld_oq + (Idx)h * D : a.ok + t * a.ld_ok + (Idx)(h - a.Hq) * D;
+      store_packet<T, N>(dst + (Idx)j * N, o1);
+      store_packet<T, N>(dst + half + (Idx)j * N, o2);
+      if (j == 0) {
+        if (isq && a.rq) a.rq[t * a.Hq + h] = r;
+        if (!isq && a.rk) a.rk[t * a.Hkv + (h - a.Hq)] = r;
       }
     }
+    advance(t, p);
+    b = b + 1 == kFwdBufs ? 0 : b + 1;
   }
+  cp_async_wait<0>();
 }
 
 // The CTA's dwq | dwk partial row: sum over the warp's lanes that hold the
@@ -379,213 +395,6 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   write_partial<N>(acc, part, a.ws, D, NV, j, lane, warp);
 }
 
-// ------------------------------------------------------------ staged forms
-//
-// Large batches: independent row groups of W warps (R per CTA) each stream
-// blocks of TB whole tokens through a ring of S shared-memory stages, as in
-// qk_rope_staged.  The group's elected lane bulk-loads a block (Q rows, then
-// K rows; the backward adds the pre-norm rows after the gradients) with
-// cp.async.bulk completing on the stage's mbarrier; while it lands the group
-// computes the block's cos/sin table; then lane (slot, j) (HS = 32W / NV
-// head slots) normalises and rotates packet j of both halves of heads slot,
-// slot + HS, ... of every token in shared memory, and the lane bulk-stores
-// the block to the outputs.  A head's lanes are NV consecutive lanes of one
-// warp (NV divides 32), so its sums are shuffles; the head loop runs the
-// same number of times on every lane of a warp.
-
-struct StagedShape {
-  int TB, S, W, R;
-  uint32_t off_cs, off_stage, stage_bytes;
-  size_t smem;
-};
-
-template <typename T, typename Idx, int N>
-__global__ void __launch_bounds__(256)
-qk_norm_rope_fwd_staged(const NormRopeParams<T, Idx> a, const StagedShape g, unsigned *status,
-                        long long wait_limit, const __grid_constant__ RopeFreqs fr) {
-  extern __shared__ __align__(128) unsigned char sbuf[];
-  __shared__ float2 freq[kRopeMaxHalf];
-  const int D = a.D, half = D >> 1, NV = half / N, NH = a.Hq + a.Hkv, Hq = a.Hq;
-  const int TB = g.TB, S = g.S, W = g.W, R = g.R;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = warp / W, wig = warp - grp * W;
-  const int gi = wig * 32 + lane, G = W * 32;
-  const bool leader = gi == 0;
-  const int HS = G / NV;
-  const int j = gi % NV, slot = gi / NV;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf) + grp * S;
-  float2 *cs = reinterpret_cast<float2 *>(sbuf + g.off_cs) + (size_t)grp * TB * half;
-  unsigned char *ring = sbuf + g.off_stage + (size_t)grp * S * g.stage_bytes;
-  const Idx nblocks = (a.rows + TB - 1) / TB;
-  const size_t qrow_b = (size_t)Hq * D * sizeof(T), krow_b = (size_t)a.Hkv * D * sizeof(T);
-  const bool q_in = a.ld_q == (Idx)Hq * D, k_in = a.ld_k == (Idx)a.Hkv * D;
-  const bool q_out = a.ld_oq == (Idx)Hq * D, k_out = a.ld_ok == (Idx)a.Hkv * D;
-
-  if (leader)
-    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
-  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
-  pdl_wait();
-  pdl_trigger();
-  if (threadIdx.x == 0) fence_mbar_init();
-  Packet<T, N> wq1, wq2, wk1, wk2;
-  if (Hq > 0) {
-    wq1 = load_packet<T, N>(a.wq + j * N);
-    wq2 = load_packet<T, N>(a.wq + half + j * N);
-  }
-  if (a.Hkv > 0) {
-    wk1 = load_packet<T, N>(a.wk + j * N);
-    wk2 = load_packet<T, N>(a.wk + half + j * N);
-  }
-  __syncthreads();
-
-  auto ntok = [&](Idx b) -> int {
-    const Idx left = a.rows - b * TB;
-    return (int)(left < (Idx)TB ? left : (Idx)TB);
-  };
-  auto load = [&](int s, Idx b) {
-    const Idx t0 = b * TB;
-    const int nt = ntok(b);
-    unsigned char *st = ring + (size_t)s * g.stage_bytes;
-    mbar_arrive_expect_tx(&bars[s], (uint32_t)(nt * (qrow_b + krow_b)));
-    if (qrow_b) {
-      if (q_in)
-        bulk_copy_g2s(st, a.q + t0 * a.ld_q, (uint32_t)(nt * qrow_b), &bars[s]);
-      else
-        for (int i = 0; i < nt; ++i)
-          bulk_copy_g2s(st + i * qrow_b, a.q + (t0 + i) * a.ld_q, (uint32_t)qrow_b, &bars[s]);
-    }
-    if (krow_b) {
-      unsigned char *sk = st + (size_t)TB * qrow_b;
-      if (k_in)
-        bulk_copy_g2s(sk, a.k + t0 * a.ld_k, (uint32_t)(nt * krow_b), &bars[s]);
-      else
-        for (int i = 0; i < nt; ++i)
-          bulk_copy_g2s(sk + i * krow_b, a.k + (t0 + i) * a.ld_k, (uint32_t)krow_b, &bars[s]);
-    }
-  };
-  auto store = [&](int s, Idx b) {
-    const Idx t0 = b * TB;
-    const int nt = ntok(b);
-    const unsigned char *st = ring + (size_t)s * g.stage_bytes;
-    if (qrow_b) {
-      if (q_out)
-        bulk_copy_s2g(a.oq + t0 * a.ld_oq, st, (uint32_t)(nt * qrow_b));
-      else
-        for (int i = 0; i < nt; ++i)
-          bulk_copy_s2g(a.oq + (t0 + i) * a.ld_oq, st + i * qrow_b, (uint32_t)qrow_b);
-    }
-    if (krow_b) {
-      const unsigned char *sk = st + (size_t)TB * qrow_b;
-      if (k_out)
-        bulk_copy_s2g(a.ok + t0 * a.ld_ok, sk, (uint32_t)(nt * krow_b));
-      else
-        for (int i = 0; i < nt; ++i)
-          bulk_copy_s2g(a.ok + (t0 + i) * a.ld_ok, sk + i * krow_b, (uint32_t)krow_b);
-    }
-    bulk_commit_group();
-  };
-  auto group_sync = [&]() {
-    if (W > 1)
-      named_barrier(1 + grp, G);
-    else
-      __syncwarp();
-  };
-
-  const Idx first = (Idx)blockIdx.x * R + grp;
-  const Idx stride = (Idx)gridDim.x * R;
-  int issued = 0;
-  if (leader)
-    for (int i = 0; i < S; ++i) {
-      const Idx b = first + (Idx)i * stride;
-      if (b >= nblocks) break;
-      load(i, b);
-      ++issued;
-    }
-
-  bool live = true;
-  int it = 0;
-  for (Idx b = first; b < nblocks; b += stride, ++it) {
-    const int s = it % S;
-    const Idx t0 = b * TB;
-    const int nt = ntok(b);
-    if (leader && it >= 1) {
-      bulk_wait_group_read<0>();  // the previous block's store has read its stage
-      const Idx nb = b - stride + (Idx)S * stride;
-      if (nb < nblocks) {
-        load((it - 1) % S, nb);
-        ++issued;
-      }
-    }
-    for (int e = gi; e < nt * half; e += G) {
-      const int tt = e / half, i = e - tt * half;
-      const int p = position_of<Idx>(t0 + tt, a.cu, a.B);
-      const float2 f = freq[i];
-      float c, sn;
-      rope_cos_sin(p, f.x, f.y, &c, &sn);
-      cs[e] = make_float2(c, sn);
-    }
-    if (live) live = mbar_wait_bounded(&bars[s], (uint32_t)((it / S) & 1), wait_limit, status);
-    group_sync();
-    unsigned char *st = ring + (size_t)s * g.stage_bytes;
-    for (int tt = 0; tt < nt; ++tt) {
-      const float2 *c2 = cs + tt * half + j * N;
-      float cv[N], sv[N];
-#pragma unroll
-      for (int e = 0; e < N; ++e) {
-        const float2 r2 = c2[e];
-        cv[e] = r2.x;
-        sv[e] = r2.y;
-      }
-      T *qt = reinterpret_cast<T *>(st) + (size_t)tt * Hq * D + j * N;
-      T *kt = reinterpret_cast<T *>(st + (size_t)TB * qrow_b) + (size_t)tt * a.Hkv * D + j * N;
-      const Idx t = t0 + tt;
-      for (int h0 = 0; h0 < NH; h0 += HS) {
-        const int h = h0 + slot;
-        const bool act = h < NH, isq = h < Hq;
-        T *v = isq ? qt + (size_t)h * D : kt + (size_t)(h - Hq) * D;
-        Packet<T, N> pa, pb;
-        float ss = 0.f;
-        if (act) {
-          pa = *reinterpret_cast<const Packet<T, N> *>(v);
-          pb = *reinterpret_cast<const Packet<T, N> *>(v + half);
-#pragma unroll
-          for (int e = 0; e < N; ++e) {
-            const float u1 = pa.get(e), u2 = pb.get(e);
-            ss = fmaf(u1, u1, fmaf(u2, u2, ss));
-          }
-        }
-        ss = slot_sum(ss, NV);
-        if (act) {
-          const float r = rsqrtf(fmaf(ss, a.inv_d, a.eps));
-          const Packet<T, N> &w1 = isq ? wq1 : wk1, &w2 = isq ? wq2 : wk2;
-          Packet<T, N> o1, o2;
-#pragma unroll
-          for (int e = 0; e < N; ++e) {
-            const float n1 = pa.get(e) * r * w1.get(e), n2 = pb.get(e) * r * w2.get(e);
-            o1.set(e, fmaf(n1, cv[e], -n2 * sv[e]));
-            o2.set(e, fmaf(n2, cv[e], n1 * sv[e]));
-          }
-          *reinterpret_cast<Packet<T, N> *>(v) = o1;
-          *reinterpret_cast<Packet<T, N> *>(v + half) = o2;
-          if (j == 0) {
-            if (isq && a.rq) a.rq[t * Hq + h] = r;
-            if (!isq && a.rk) a.rk[t * a.Hkv + (h - Hq)] = r;
-          }
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    group_sync();
-    if (leader) store(s, b);
-  }
-  if (leader) {
-    if (!live)
-      for (int i = it; i < issued; ++i)
-        mbar_wait_bounded(&bars[i % S], (uint32_t)((i / S) & 1), wait_limit, status);
-    bulk_wait_group_all();
-  }
-}
-
 // Element-wise forms: one warp per token, heads one after another, lane i
 // owning the pairs i, i + 32, ... of every head.
 template <typename T, typename Idx>
@@ -744,73 +553,19 @@ NormRopeParams<T, Idx> params_of(const QkNormRopeArgs &a) {
 
 cudaError_t finish_launch(cudaError_t e) { return e != cudaSuccess ? e : cudaGetLastError(); }
 
-// The staged plan (forward): ~8 KiB of whole tokens per stage; groups of W
-// warps with ~8 packet pairs per lane per block; ~150 KiB of stages per SM
-// over two CTAs, 2..6 stages per group.  False when it does not fit.
-// (A staged backward, whose tokens carry gradient and pre-norm rows, spent
-// its time in per-token barriers at one token per stage and measured slower
-// than the warp-per-token backward, so the backward stays warp-per-token.)
-bool plan_staged(const QkNormRopeArgs &a, int es, int N, const DeviceInfo &dev, StagedShape *g) {
-  const int NH = a.Hq + a.Hkv, half = a.D / 2, NV = half / N;
-  const size_t tok_bytes = (size_t)NH * a.D * es;
-  int TB = (int)(8192 / tok_bytes);
-  TB = TB < 1 ? 1 : (TB > 16 ? 16 : TB);
-  int W = (int)ceil_div((int64_t)TB * NH * NV, (int64_t)256);
-  W = W < 1 ? 1 : (W > 8 ? 8 : W);
-  const int R = 8 / W > 0 ? 8 / W : 1;
-  const size_t stage_bytes = (size_t)TB * tok_bytes;
-  if (NV > 32 || stage_bytes >= (1u << 20)) return false;
-  int S = (int)(76800 / ((size_t)R * stage_bytes));
-  S = S < 2 ? 2 : (S > 6 ? 6 : S);
-  const size_t static_smem = sizeof(float2) * kRopeMaxHalf;
-  for (; S >= 2; --S) {
-    const size_t off_cs = ((size_t)R * S * 8 + 15) / 16 * 16;
-    const size_t off_stage = (off_cs + (size_t)R * TB * half * sizeof(float2) + 127) / 128 * 128;
-    const size_t smem = off_stage + (size_t)R * S * stage_bytes;
-    if (smem + static_smem <= (size_t)dev.max_smem_optin) {
-      *g = StagedShape{TB, S, W, R, (uint32_t)off_cs, (uint32_t)off_stage,
-                       (uint32_t)stage_bytes, smem};
-      return true;
-    }
-  }
-  return false;
-}
-
-template <typename T, typename Idx, int N>
-cudaError_t fwd_warp_launch(const QkNormRopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
-  const int NH = a.Hq + a.Hkv, half = a.D / 2, S = 32 / (half / N);
-  const int per_lane = (NH + S - 1) / S;
-  const dim3 grid((unsigned)ceil_div(a.T, (int64_t)kWarps));
-  const size_t smem = sizeof(float2) * (size_t)kWarps * half;
-  const NormRopeParams<T, Idx> k = params_of<T, Idx>(a);
-  // two heads per pass at most: four would spill at the 128-register cap
-  if (per_lane <= 1)
-    return finish_launch(launch_pdl(qk_norm_rope_fwd_warp<T, Idx, N, 1>, grid, dim3(kThreads),
-                                    smem, s, k, fr));
-  return finish_launch(launch_pdl(qk_norm_rope_fwd_warp<T, Idx, N, 2>, grid, dim3(kThreads), smem,
-                                  s, k, fr));
-}
-
 template <typename T, typename Idx>
 cudaError_t fwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &fr,
                       const DeviceInfo &dev, cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
-  StagedShape g;
-  if (warp_path && plan_staged(a, (int)sizeof(T), NV, dev, &g)) {
-    auto kern = qk_norm_rope_fwd_staged<T, Idx, NV>;
-    const int threads = 32 * g.W * g.R;
-    const int occ = blocks_per_sm((const void *)kern, threads, g.smem, dev, kMaxBlocksPerSm);
-    const int64_t P = (int64_t)dev.sms * occ;
-    // the pipeline pays off once every group streams several blocks
-    if (ceil_div(a.T, (int64_t)g.TB) >= (int64_t)6 * P * g.R) {
-      unsigned *status = nullptr;
-      cudaError_t e = device_status_ptr(dev, &status);
-      if (e != cudaSuccess) return e;
-      return finish_launch(launch_pdl(kern, dim3((unsigned)P), dim3(threads), g.smem, s,
-                                      params_of<T, Idx>(a), g, status, kWaitLimitCycles, fr));
-    }
+  if (warp_path) {
+    auto kern = qk_norm_rope_fwd_pipe<T, Idx, NV>;
+    const size_t smem = sizeof(float2) * (size_t)kWarps * (a.D / 2) + kFwdStageBytes;
+    const int occ = blocks_per_sm((const void *)kern, kThreads, smem, dev, kMaxBlocksPerSm);
+    int64_t P = ceil_div(a.T, (int64_t)kWarps);
+    if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+    return finish_launch(
+        launch_pdl(kern, dim3((unsigned)P), dim3(kThreads), smem, s, params_of<T, Idx>(a), fr));
   }
-  if (warp_path) return fwd_warp_launch<T, Idx, NV>(a, fr, s);
   const size_t smem = sizeof(float2) * (size_t)kWarps * (a.D / 2);
   return finish_launch(launch_pdl(qk_norm_rope_fwd_generic<T, Idx>,
                                   dim3((unsigned)ceil_div(a.T, (int64_t)kWarps)), dim3(kThreads),

@@ -207,9 +207,10 @@ def test_deterministic_dw():
         assert all(torch.equal(a, b) for a, b in zip(o, outs[0]))
 
 
-def test_staged_path_fused_qkv_in_place_sampled():
-    """A batch large enough for the staged kernels, read from and written
-    back into interleaved Q / K slices of one fused QKV buffer."""
+def test_large_batch_fused_qkv_in_place_sampled():
+    """A batch large enough that every warp of the persistent kernels walks
+    many tokens, read from and written back into interleaved Q / K slices of
+    one fused QKV buffer."""
     T, Hq, Hkv, D = 20000, 16, 4, 128
     lens = (5000, 1, 8000, 6999)
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
