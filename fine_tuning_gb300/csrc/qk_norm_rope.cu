@@ -125,23 +125,38 @@ constexpr size_t kBwdStageBytes = sizeof(uint4) * kWarps * kBwdBufs * kBwdSlots 
 constexpr int kFwdSlots = 2, kFwdBufs = 4;
 constexpr size_t kFwdStageBytes = sizeof(uint4) * kWarps * kFwdBufs * kFwdSlots * 32;
 
+// Per token, the warp folds the norm weights into the rotation: for column
+// i (first-half weight w1 = w[i], second-half w2 = w[D/2 + i], angle phi)
+//   out_i        = r (x1 w1 cos - x2 w2 sin) = r (x1 A - x2 B)
+//   out_{D/2+i}  = r (x2 w2 cos + x1 w1 sin) = r (x2 C + x1 E)
+// with (A, B, C, E) = (w1 cos, w2 sin, w2 cos, w1 sin) for Q and for K.  The
+// entry of column i sits at (i mod N) NV + i / N, so the NV lanes of a head
+// reading their packets' e-th columns touch consecutive entries.
 template <typename T, typename Idx, int N>
 __global__ void __launch_bounds__(kThreads, kFwdPipeBlocks)
 qk_norm_rope_fwd_pipe(const NormRopeParams<T, Idx> a, const __grid_constant__ RopeFreqs fr) {
-  // [warps][D/2] (cos, sin), then the staging buffers (16-byte aligned: D
-  // is a multiple of 8 here)
-  extern __shared__ float2 tab[];
+  // [warps][2][D/2] float4 weighted tables (Q, then K), then the staging
+  // buffers
+  extern __shared__ float4 tab4[];
   __shared__ float2 freq[kRopeMaxHalf];
+  __shared__ float wf[4][kRopeMaxHalf];  // wq first half, wq second, wk first, wk second
   const int D = a.D, half = D >> 1, NV = half / N, S = 32 / NV, NH = a.Hq + a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = lane % NV, slot = lane / NV;
-  float2 *wt = tab + warp * half;
-  uint4 *stg = reinterpret_cast<uint4 *>(tab + kWarps * half) + warp * (kFwdBufs * kFwdSlots * 32);
+  float4 *wtq = tab4 + warp * 2 * half, *wtk = wtq + half;
+  uint4 *stg = reinterpret_cast<uint4 *>(tab4 + kWarps * 2 * half) +
+               warp * (kFwdBufs * kFwdSlots * 32);
 
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
-  __syncthreads();  // the frequency table
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    wf[0][i] = a.Hq > 0 ? to_float(a.wq[i]) : 0.f;
+    wf[1][i] = a.Hq > 0 ? to_float(a.wq[half + i]) : 0.f;
+    wf[2][i] = a.Hkv > 0 ? to_float(a.wk[i]) : 0.f;
+    wf[3][i] = a.Hkv > 0 ? to_float(a.wk[half + i]) : 0.f;
+  }
+  __syncthreads();  // the frequency and weight tables
 
   const Idx step = (Idx)gridDim.x * kWarps;
   const int passes = (NH + S - 1) / S;  // head passes per token, the same on every lane
@@ -157,7 +172,6 @@ qk_norm_rope_fwd_pipe(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
     }
     cp_async_commit();  // one group per pass on every lane, empty or not
   };
-  const float2 *cs_j = wt + j * N;
   Idx t = (Idx)blockIdx.x * kWarps + warp, t2 = t;
   int p = 0, p2 = 0, b = 0;
   auto advance = [&](Idx &tt, int &pp) {
@@ -173,10 +187,18 @@ qk_norm_rope_fwd_pipe(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   }
   while (t < a.rows) {  // warp-uniform
     advance(t2, p2);
-    stage(t2, p2, b == 0 ? kFwdBufs - 1 : b - 1);  // the next pass's loads fly meanwhile
+    stage(t2, p2, b == 0 ? kFwdBufs - 1 : b - 1);  // the next passes' loads fly meanwhile
     if (p == 0) {
-      __syncwarp();  // the previous token's table has been read
-      token_table(wt, freq, half, position_of<Idx>(t, a.cu, a.B), 1.0f, lane);
+      __syncwarp();  // the previous token's tables have been read
+      const int pos = position_of<Idx>(t, a.cu, a.B);
+      for (int i = lane; i < half; i += 32) {
+        const float2 f = freq[i];
+        float c, sn;
+        rope_cos_sin(pos, f.x, f.y, &c, &sn);
+        const int at = (i % N) * NV + i / N;
+        wtq[at] = make_float4(wf[0][i] * c, wf[1][i] * sn, wf[1][i] * c, wf[0][i] * sn);
+        wtk[at] = make_float4(wf[2][i] * c, wf[3][i] * sn, wf[3][i] * c, wf[2][i] * sn);
+      }
       __syncwarp();
     }
     cp_async_wait<kFwdBufs - 1>();  // this lane's copies for (t, p) have landed
@@ -197,15 +219,14 @@ qk_norm_rope_fwd_pipe(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
     ss = slot_sum(ss, NV);  // every lane takes part
     if (act) {
       const float r = rsqrtf(fmaf(ss, a.inv_d, a.eps));
-      const T *wp = (isq ? a.wq : a.wk) + j * N;  // L1 hits
-      const Packet<T, N> w1 = load_packet<T, N>(wp), w2 = load_packet<T, N>(wp + half);
+      const float4 *tw = (isq ? wtq : wtk) + j;
       Packet<T, N> o1, o2;
 #pragma unroll
-      for (int e = 0; e < N; ++e) {
-        const float2 c = cs_j[e];
-        const float n1 = x1.get(e) * r * w1.get(e), n2 = x2.get(e) * r * w2.get(e);
-        o1.set(e, fmaf(n1, c.x, -n2 * c.y));
-        o2.set(e, fmaf(n2, c.x, n1 * c.y));
+      for (int e = 0; e < N; e += 2) {
+        const float4 t0 = tw[e * NV], t1 = tw[(e + 1) * NV];
+        const float a0 = x1.get(e), b0 = x2.get(e), a1 = x1.get(e + 1), b1 = x2.get(e + 1);
+        o1.set2(e, r * fmaf(a0, t0.x, -b0 * t0.y), r * fmaf(a1, t1.x, -b1 * t1.y));
+        o2.set2(e, r * fmaf(b0, t0.z, a0 * t0.w), r * fmaf(b1, t1.z, a1 * t1.w));
       }
       T *dst = isq ? a.oq + t * a.ld_oq + (Idx)h * D : a.ok + t * a.ld_ok + (Idx)(h - a.Hq) * D;
       store_packet<T, N>(dst + (Idx)j * N, o1);
@@ -559,7 +580,7 @@ cudaError_t fwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &
   constexpr int NV = VecWidth<T>::value;
   if (warp_path) {
     auto kern = qk_norm_rope_fwd_pipe<T, Idx, NV>;
-    const size_t smem = sizeof(float2) * (size_t)kWarps * (a.D / 2) + kFwdStageBytes;
+    const size_t smem = sizeof(float4) * (size_t)kWarps * 2 * (a.D / 2) + kFwdStageBytes;
     const int occ = blocks_per_sm((const void *)kern, kThreads, smem, dev, kMaxBlocksPerSm);
     int64_t P = ceil_div(a.T, (int64_t)kWarps);
     if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
