@@ -91,23 +91,6 @@ __device__ __forceinline__ void token_table(float2 *wt, const float2 *freq, int 
   }
 }
 
-// Per-thread asynchronous copies into shared memory (cp.async; 16 bytes
-// bypassing L1, or 4 bytes), committed and waited for in groups.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int K> __device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory");
-}
-
 // The backward warp kernel's staging: per warp kBwdBufs buffers of 5 x 32
 // 16-byte slots (gradient halves, pre-norm halves, r; slot c of lane l at
 // c * 32 + l, so a warp's accesses to one slot are contiguous); the loads

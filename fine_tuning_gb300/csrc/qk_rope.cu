@@ -407,6 +407,121 @@ qk_rope_warp(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
   }
 }
 
+// Persistent and pipelined, for every batch whose half head splits over a
+// power-of-two number of lanes: each warp walks (token, head pass) pairs
+// (tokens t, t + P * 8, ...; a pass is S heads, lane (slot, j) rotating
+// packet j of both halves of head slot + S p), and each lane copies its
+// packets of the next kPipeBufs - 1 passes into a per-warp shared-memory
+// ring with cp.async while it rotates the current pass in registers and
+// writes it back in place.
+constexpr int kPipeSlots = 2, kPipeBufs = 4, kPipeBlocks = 4;
+constexpr size_t kPipeStageBytes =
+    sizeof(uint4) * (kCtaThreads / 32) * kPipeBufs * kPipeSlots * 32;
+
+template <typename T, typename Idx, int N>
+__global__ void __launch_bounds__(kCtaThreads, kPipeBlocks)
+qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int B, Idx rows,
+             int Hq, int NH, int D, float sgn, const __grid_constant__ RopeFreqs fr) {
+  constexpr int kWarps = kCtaThreads / 32;
+  // [warps][D/2] (cos, sgn sin), then the staging ring (16-byte aligned:
+  // D is a multiple of 8 here)
+  extern __shared__ float2 tab[];
+  __shared__ float2 freq[kRopeMaxHalf];
+  const int half = D >> 1, NV = half / N, S = 32 / NV;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = lane % NV, slot = lane / NV;
+  float2 *wt = tab + warp * half;
+  uint4 *stg = reinterpret_cast<uint4 *>(tab + kWarps * half) + warp * (kPipeBufs * kPipeSlots * 32);
+  auto head = [&](Idx tt, int h) -> T * {
+    return (h < Hq ? q + tt * ld_q + (Idx)h * D : k + tt * ld_k + (Idx)(h - Hq) * D) + j * N;
+  };
+
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
+  __syncthreads();  // the frequency table
+
+  const Idx step = (Idx)gridDim.x * kWarps;
+  const int passes = (NH + S - 1) / S;  // head passes per token, the same on every lane
+  auto stage = [&](Idx tt, int p, int b) {
+    const int h = slot + p * S;
+    if (tt < rows && h < NH) {
+      const T *v = head(tt, h);
+      uint4 *d = stg + b * kPipeSlots * 32 + lane;
+      cp_async16(d, v);
+      cp_async16(d + 32, v + half);
+    }
+    cp_async_commit();  // one group per pass on every lane, empty or not
+  };
+  auto advance = [&](Idx &tt, int &pp) {
+    if (++pp == passes) {
+      pp = 0;
+      tt += step;
+    }
+  };
+  const float2 *cs_j = wt + j * N;
+  Idx t = (Idx)blockIdx.x * kWarps + warp, t2 = t;
+  int p = 0, p2 = 0, b = 0;
+  stage(t2, p2, 0);
+  for (int i = 1; i < kPipeBufs - 1; ++i) {
+    advance(t2, p2);
+    stage(t2, p2, i);
+  }
+  while (t < rows) {  // warp-uniform
+    advance(t2, p2);
+    stage(t2, p2, b == 0 ? kPipeBufs - 1 : b - 1);  // the next passes' loads fly meanwhile
+    if (p == 0) {
+      __syncwarp();  // the previous token's table has been read
+      const int pos = position_of<Idx>(t, cu, B);
+      for (int i = lane; i < half; i += 32) {
+        const float2 f = freq[i];
+        float c, sn;
+        rope_cos_sin(pos, f.x, f.y, &c, &sn);
+        wt[i] = make_float2(c, sgn * sn);
+      }
+      __syncwarp();
+    }
+    cp_async_wait<kPipeBufs - 1>();  // this lane's copies for (t, p) have landed
+    const int h = slot + p * S;
+    if (h < NH) {
+      const uint4 *d = stg + b * kPipeSlots * 32 + lane;
+      Packet<T, N> x1, x2, o1, o2;
+      *reinterpret_cast<uint4 *>(&x1) = d[0];
+      *reinterpret_cast<uint4 *>(&x2) = d[32];
+#pragma unroll
+      for (int e = 0; e < N; e += 2) {
+        const float2 c0 = cs_j[e], c1 = cs_j[e + 1];
+        const float a0 = x1.get(e), b0 = x2.get(e), a1 = x1.get(e + 1), b1 = x2.get(e + 1);
+        o1.set2(e, fmaf(a0, c0.x, -b0 * c0.y), fmaf(a1, c1.x, -b1 * c1.y));
+        o2.set2(e, fmaf(b0, c0.x, a0 * c0.y), fmaf(b1, c1.x, a1 * c1.y));
+      }
+      T *v = head(t, h);
+      store_packet<T, N>(v, o1);
+      store_packet<T, N>(v + half, o2);
+    }
+    advance(t, p);
+    b = b + 1 == kPipeBufs ? 0 : b + 1;
+  }
+  cp_async_wait<0>();
+}
+
+template <typename T, typename Idx, int N>
+cudaError_t rope_pipe_launch(const RopeArgs &a, const RopeFreqs &fr, const DeviceInfo &dev,
+                             cudaStream_t s) {
+  constexpr int kWarps = kCtaThreads / 32;
+  const int NH = a.Hq + a.Hkv;
+  const size_t smem = sizeof(float2) * (size_t)kWarps * (a.D / 2) + kPipeStageBytes;
+  auto kern = qk_rope_pipe<T, Idx, N>;
+  const int occ = blocks_per_sm((const void *)kern, kCtaThreads, smem, dev, kPipeBlocks);
+  int64_t P = ceil_div(a.T, (int64_t)kWarps);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  cudaError_t e = launch_pdl(kern, dim3((unsigned)P), dim3(kCtaThreads), smem, s, (T *)a.q,
+                             (Idx)a.ld_q, (T *)a.k, (Idx)a.ld_k, a.cu, a.B, (Idx)a.T, a.Hq, NH,
+                             a.D, a.backward ? -1.0f : 1.0f, fr);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <typename T, typename Idx, int N>
 cudaError_t rope_warp_launch(const RopeArgs &a, const RopeFreqs &fr, cudaStream_t s) {
   const int NH = a.Hq + a.Hkv, half = a.D / 2, NV = half / N, S = 32 / NV;
@@ -525,6 +640,8 @@ cudaError_t rope_typed(bool vec, const RopeArgs &a, const RopeFreqs &fr, const D
                        cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
   if (vec) {
+    const int nv = a.D / 2 / NV;
+    if (nv >= 1 && nv <= 32 && (nv & (nv - 1)) == 0) return rope_pipe_launch<T, Idx, NV>(a, fr, dev, s);
     bool launched = false;
     cudaError_t e = rope_staged_launch<T, Idx, NV>(a, fr, dev, s, &launched);
     if (e != cudaSuccess || launched) return e;
