@@ -308,7 +308,7 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   };
   // (cos, -sin) of this lane's columns are read from the table per head
   // rather than held in registers
-  const float2 *cs_j = wt + j * N;
+  const float4 *cs_j = reinterpret_cast<const float4 *>(wt) + j;
   // (t, p): the pass computed now; (t2, p2): the last pass staged
   auto advance = [&](Idx &tt, int &pp) {
     if (++pp == passes) {
@@ -329,7 +329,17 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
     stage(t2, p2, b == 0 ? kBwdBufs - 1 : b - 1);
     if (p == 0) {
       __syncwarp();  // the previous token's table has been read
-      token_table(wt, freq, half, position_of<Idx>(t, a.cu, a.B), -1.0f, lane);
+      // (cos, -sin) of columns j N + e and j N + e + 1 (e even) in one
+      // 16-byte entry at (e / 2) NV + j: a head's lanes read consecutive
+      // entries
+      const int pos = position_of<Idx>(t, a.cu, a.B);
+      for (int c = lane; c < half; c += 32) {
+        const float2 f = freq[c];
+        float cv, sn;
+        rope_cos_sin(pos, f.x, f.y, &cv, &sn);
+        const int e = c % N;
+        wt[2 * ((e >> 1) * NV + c / N) + (e & 1)] = make_float2(cv, -sn);
+      }
       __syncwarp();
     }
     cp_async_wait<kBwdBufs - 1>();  // this lane's copies for (t, p) have landed
@@ -357,7 +367,8 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
 #pragma unroll
         for (int e = 0; e < N; ++e) {
           const float a1 = g1.get(e), a2 = g2.get(e);
-          const float2 c = cs_j[e];
+          const float4 c4 = cs_j[(e >> 1) * NV];
+          const float2 c = (e & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
           dn1[e] = fmaf(a1, c.x, -a2 * c.y);
           dn2[e] = fmaf(a2, c.x, a1 * c.y);
           const float u1 = v1.get(e), u2 = v2.get(e);

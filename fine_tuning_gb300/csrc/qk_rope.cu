@@ -422,6 +422,7 @@ template <typename T, typename Idx, int N>
 __global__ void __launch_bounds__(kCtaThreads, kPipeBlocks)
 qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int B, Idx rows,
              int Hq, int NH, int D, float sgn, const __grid_constant__ RopeFreqs fr) {
+  static_assert(N % 2 == 0, "pairs of columns per table entry");
   constexpr int kWarps = kCtaThreads / 32;
   // [warps][D/2] (cos, sgn sin), then the staging ring (16-byte aligned:
   // D is a multiple of 8 here)
@@ -430,7 +431,10 @@ qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
   const int half = D >> 1, NV = half / N, S = 32 / NV;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = lane % NV, slot = lane / NV;
-  float2 *wt = tab + warp * half;
+  // the token's table: (cos, sgn sin) of columns j N + e and j N + e + 1 (e
+  // even) in one 16-byte entry at (e / 2) NV + j, so the NV lanes of a head
+  // read consecutive entries
+  float4 *wt = reinterpret_cast<float4 *>(tab + warp * half);
   uint4 *stg = reinterpret_cast<uint4 *>(tab + kWarps * half) + warp * (kPipeBufs * kPipeSlots * 32);
   auto head = [&](Idx tt, int h) -> T * {
     return (h < Hq ? q + tt * ld_q + (Idx)h * D : k + tt * ld_k + (Idx)(h - Hq) * D) + j * N;
@@ -459,7 +463,7 @@ qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
       tt += step;
     }
   };
-  const float2 *cs_j = wt + j * N;
+  const float4 *cs_j = wt + j;
   Idx t = (Idx)blockIdx.x * kWarps + warp, t2 = t;
   int p = 0, p2 = 0, b = 0;
   stage(t2, p2, 0);
@@ -473,11 +477,13 @@ qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
     if (p == 0) {
       __syncwarp();  // the previous token's table has been read
       const int pos = position_of<Idx>(t, cu, B);
+      float2 *w2 = reinterpret_cast<float2 *>(wt);
       for (int i = lane; i < half; i += 32) {
         const float2 f = freq[i];
         float c, sn;
         rope_cos_sin(pos, f.x, f.y, &c, &sn);
-        wt[i] = make_float2(c, sgn * sn);
+        const int e = i % N;
+        w2[2 * ((e >> 1) * NV + i / N) + (e & 1)] = make_float2(c, sgn * sn);
       }
       __syncwarp();
     }
@@ -490,10 +496,10 @@ qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
       *reinterpret_cast<uint4 *>(&x2) = d[32];
 #pragma unroll
       for (int e = 0; e < N; e += 2) {
-        const float2 c0 = cs_j[e], c1 = cs_j[e + 1];
+        const float4 c = cs_j[(e >> 1) * NV];  // (cos, sin) of columns e and e + 1
         const float a0 = x1.get(e), b0 = x2.get(e), a1 = x1.get(e + 1), b1 = x2.get(e + 1);
-        o1.set2(e, fmaf(a0, c0.x, -b0 * c0.y), fmaf(a1, c1.x, -b1 * c1.y));
-        o2.set2(e, fmaf(b0, c0.x, a0 * c0.y), fmaf(b1, c1.x, a1 * c1.y));
+        o1.set2(e, fmaf(a0, c.x, -b0 * c.y), fmaf(a1, c.z, -b1 * c.w));
+        o2.set2(e, fmaf(b0, c.x, a0 * c.y), fmaf(b1, c.z, a1 * c.w));
       }
       T *v = head(t, h);
       store_packet<T, N>(v, o1);
