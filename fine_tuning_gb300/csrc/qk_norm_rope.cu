@@ -263,6 +263,7 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   // staging buffers (16-byte aligned: D is a multiple of 8 here)
   extern __shared__ float2 tab[];
   __shared__ float2 freq[kRopeMaxHalf];
+  __shared__ int32_t cu_s[kCuInShared];
   const int D = a.D, half = D >> 1, NV = half / N, S = 32 / NV, NH = a.Hq + a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = lane % NV, slot = lane / NV;
@@ -271,6 +272,12 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
+  // the sequence boundaries in shared memory when they fit (every token's
+  // position is a binary search over them); read after the barrier below
+  const bool cu_staged = a.B < kCuInShared;
+  if (cu_staged)
+    for (int i = threadIdx.x; i <= a.B; i += blockDim.x) cu_s[i] = __ldg(a.cu + i);
+  const int32_t *bounds = cu_staged ? cu_s : a.cu;
   // the norm weights are re-read per head (L1 hits) rather than held in
   // registers, which go to the four accumulators below
   float acc[4][N];  // dwq first half, dwq second half, dwk first half, dwk second half
@@ -278,7 +285,7 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   for (int g = 0; g < 4; ++g)
 #pragma unroll
     for (int e = 0; e < N; ++e) acc[g][e] = 0.f;
-  __syncthreads();  // the frequency table
+  __syncthreads();  // the frequency table and the boundaries
 
   float2 *wt = tab + warp * half;
   uint4 *stg =
@@ -332,7 +339,7 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
       // (cos, -sin) of columns j N + e and j N + e + 1 (e even) in one
       // 16-byte entry at (e / 2) NV + j: a head's lanes read consecutive
       // entries
-      const int pos = position_of<Idx>(t, a.cu, a.B);
+      const int pos = position_of<Idx>(t, bounds, a.B);
       for (int c = lane; c < half; c += 32) {
         const float2 f = freq[c];
         float cv, sn;

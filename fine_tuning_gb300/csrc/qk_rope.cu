@@ -428,6 +428,7 @@ qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
   // D is a multiple of 8 here)
   extern __shared__ float2 tab[];
   __shared__ float2 freq[kRopeMaxHalf];
+  __shared__ int32_t cu_s[kCuInShared];
   const int half = D >> 1, NV = half / N, S = 32 / NV;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = lane % NV, slot = lane / NV;
@@ -443,7 +444,13 @@ qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
-  __syncthreads();  // the frequency table
+  // the sequence boundaries in shared memory when they fit: every token's
+  // position is a binary search over them
+  const bool cu_staged = B < kCuInShared;
+  if (cu_staged)
+    for (int i = threadIdx.x; i <= B; i += blockDim.x) cu_s[i] = __ldg(cu + i);
+  __syncthreads();  // the frequency table and the boundaries
+  const int32_t *bounds = cu_staged ? cu_s : cu;
 
   const Idx step = (Idx)gridDim.x * kWarps;
   const int passes = (NH + S - 1) / S;  // head passes per token, the same on every lane
@@ -476,7 +483,7 @@ qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
     stage(t2, p2, b == 0 ? kPipeBufs - 1 : b - 1);  // the next passes' loads fly meanwhile
     if (p == 0) {
       __syncwarp();  // the previous token's table has been read
-      const int pos = position_of<Idx>(t, cu, B);
+      const int pos = position_of<Idx>(t, bounds, B);
       float2 *w2 = reinterpret_cast<float2 *>(wt);
       for (int i = lane; i < half; i += 32) {
         const float2 f = freq[i];
