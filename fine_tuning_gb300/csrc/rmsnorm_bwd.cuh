@@ -63,6 +63,127 @@ __device__ __forceinline__ float dx_value(float a, float xf, float r, float wf, 
   return ADD ? dhf + v : v;
 }
 
+// Rows that fit one warp (W = 1): persistent, one row per warp at a time,
+// rows row, row + 8P, ...; each lane copies its packets of x and dy (and dh,
+// and r when saved) of the next row into a per-warp shared-memory ring with
+// cp.async while it works on the current one.  Lane l owns packets l,
+// l + 32, ... (the row plan's columns and summation order).  The CTA's eight
+// warps combine their dw sums in a fixed order at the end, in the ring's
+// memory, into the CTA's partial row.
+constexpr int kBwdPipeBufs = 2;
+template <int V, bool ADD> constexpr int bwd_pipe_slots() { return (ADD ? 3 : 2) * V + 1; }
+template <int V, bool ADD> constexpr size_t bwd_pipe_smem() {
+  return sizeof(uint4) * 8 * kBwdPipeBufs * bwd_pipe_slots<V, ADD>() * 32;  // 8 warps
+}
+
+template <typename T, typename Idx, int N, int V, bool HAS_RSTD, bool ADD>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> a) {
+  constexpr int kSl = bwd_pipe_slots<V, ADD>();  // x[V], dy[V] (, dh[V]), r
+  extern __shared__ uint4 ring[];                // [warps][kBwdPipeBufs][kSl][32]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hp = a.hp;
+  uint4 *my = ring + warp * (kBwdPipeBufs * kSl * 32);
+  pdl_wait();
+  pdl_trigger();
+
+  Packet<T, N> wv[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k)
+    if (lane + 32 * k < hp) wv[k] = load_packet<T, N>(a.w + (Idx)(lane + 32 * k) * N);
+  float acc[V][N];
+#pragma unroll
+  for (int k = 0; k < V; ++k)
+#pragma unroll
+    for (int e = 0; e < N; ++e) acc[k][e] = 0.f;
+
+  const Idx step = (Idx)gridDim.x * (blockDim.x >> 5);
+  auto stage = [&](Idx r, int b) {
+    if (r < a.rows) {
+      uint4 *d = my + b * kSl * 32 + lane;
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const int c = lane + 32 * k;
+        if (c < hp) {
+          cp_async16(d + k * 32, a.x + r * a.ldx + (Idx)c * N);
+          cp_async16(d + (V + k) * 32, a.dy + r * a.lddy + (Idx)c * N);
+          if (ADD) cp_async16(d + (2 * V + k) * 32, a.dh + r * a.lddh + (Idx)c * N);
+        }
+      }
+      if (HAS_RSTD) cp_async4(d + (kSl - 1) * 32, a.rstd + r);
+    }
+    cp_async_commit();  // one group per row on every lane, empty or not
+  };
+  Idx row = (Idx)blockIdx.x * (blockDim.x >> 5) + warp;
+  stage(row, 0);
+  int b = 0;
+  while (row < a.rows) {  // warp-uniform
+    stage(row + step, b ^ 1);  // the next row's loads fly meanwhile
+    cp_async_wait<1>();        // this lane's copies of `row` have landed
+    const uint4 *d = my + b * kSl * 32 + lane;
+    Packet<T, N> xv[V], gv[V];
+    float2 cs = make_float2(0.f, 0.f);  // (sum dy*w*x, sum x*x)
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      if (lane + 32 * k < hp) {
+        *reinterpret_cast<uint4 *>(&xv[k]) = d[k * 32];
+        *reinterpret_cast<uint4 *>(&gv[k]) = d[(V + k) * 32];
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float xf = xv[k].get(e);
+          cs.x = fmaf(gv[k].get(e) * wv[k].get(e), xf, cs.x);
+          if (!HAS_RSTD) cs.y = fmaf(xf, xf, cs.y);
+        }
+      }
+    }
+    float r;
+    if (HAS_RSTD) {
+      cs.x = warp_sum(cs.x);
+      r = *reinterpret_cast<const float *>(d + (kSl - 1) * 32);
+    } else {
+      cs = warp_sum2(cs);
+      r = rsqrtf(fmaf(cs.y, a.inv_h, a.eps));
+    }
+    const float am = r * r * r * cs.x * a.inv_h;
+    T *dr = a.dx + row * a.lddx;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const int c = lane + 32 * k;
+      if (c < hp) {
+        Packet<T, N> hv, o;
+        if (ADD) *reinterpret_cast<uint4 *>(&hv) = d[(2 * V + k) * 32];
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float xf = xv[k].get(e), gf = gv[k].get(e);
+          o.set(e, dx_value<ADD>(am, xf, r, wv[k].get(e), gf, ADD ? hv.get(e) : 0.f));
+          acc[k][e] = fmaf(gf * xf, r, acc[k][e]);
+        }
+        store_packet<T, N>(dr + (Idx)c * N, o);
+      }
+    }
+    row += step;
+    b ^= 1;
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // every warp is done with its ring: it becomes [8][H] partials
+  float *part = reinterpret_cast<float *>(ring);
+  float *mine = part + warp * a.H;
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int c = lane + 32 * k;
+    if (c < hp)
+#pragma unroll
+      for (int e = 0; e < N; ++e) mine[c * N + e] = acc[k][e];
+  }
+  __syncthreads();
+  float *dst = a.ws + (size_t)blockIdx.x * a.H;
+  const int nw = (int)(blockDim.x >> 5);
+  for (int j = threadIdx.x; j < a.H; j += blockDim.x) {
+    float sum = 0.f;
+    for (int g = 0; g < nw; ++g) sum += part[g * a.H + j];
+    dst[j] = sum;
+  }
+}
+
 template <typename T, typename Idx, int N, int V, bool HAS_RSTD, bool ADD>
 __global__ void __launch_bounds__(256) rmsnorm_bwd_rows(const BwdParams<T, Idx> a) {
   // [2][R][W] float2 reduction slots (double-buffered by row parity), then,
@@ -432,6 +553,21 @@ cudaError_t bwd_staged_v(const RowPlan &p, const StagedPlan &sp, const BwdParams
   return launch_dw_reduce(a, P, s);
 }
 
+template <typename T, typename Idx, int N, int V, bool HAS_RSTD, bool ADD>
+cudaError_t bwd_pipe_v(const BwdParams<T, Idx> &k, const RmsNormBwdArgs &a, const DeviceInfo &dev,
+                       cudaStream_t s) {
+  auto kern = rmsnorm_bwd_pipe<T, Idx, N, V, HAS_RSTD, ADD>;
+  constexpr size_t smem = bwd_pipe_smem<V, ADD>();
+  static_assert(smem >= sizeof(float) * 8 * 32 * V * N, "the ring holds the [8][H] partials");
+  const int occ = blocks_per_sm((const void *)kern, 256, smem, dev, kMaxBlocksPerSm);
+  int64_t P = ceil_div(a.T, (int64_t)8);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  if (P > a.ws_rows) P = a.ws_rows;
+  cudaError_t e = launch_pdl(kern, dim3((unsigned)P), dim3(256), smem, s, k);
+  if (e != cudaSuccess) return e;
+  return launch_dw_reduce(a, P, s);
+}
+
 template <typename T, typename Idx, int N, bool HAS_RSTD, bool ADD>
 cudaError_t bwd_planned(const RowPlan &p, const StagedPlan *sp, const BwdParams<T, Idx> &k,
                         const RmsNormBwdArgs &a, const DeviceInfo &dev, cudaStream_t s) {
@@ -472,6 +608,18 @@ cudaError_t bwd_typed(bool vec, const RmsNormBwdArgs &a, const DeviceInfo &dev,
                                dim3(256), 0, s, k, (Idx)a.H);
     if (e != cudaSuccess) return e;
     return launch_dw_reduce(a, P, s);
+  }
+  // rows of one warp: the per-warp cp.async pipeline (not with the residual
+  // gradient: its third input costs the registers of a second CTA per SM,
+  // and the staged ring measured faster there)
+  if (vec && p.W == 1 && !ADD) {
+    switch (p.V) {
+      case 1: return bwd_pipe_v<T, Idx, NV, 1, HAS_RSTD, ADD>(k, a, dev, s);
+      case 2: return bwd_pipe_v<T, Idx, NV, 2, HAS_RSTD, ADD>(k, a, dev, s);
+      case 3: return bwd_pipe_v<T, Idx, NV, 3, HAS_RSTD, ADD>(k, a, dev, s);
+      case 4: return bwd_pipe_v<T, Idx, NV, 4, HAS_RSTD, ADD>(k, a, dev, s);
+      default: break;
+    }
   }
   if (vec) {
     const StagedPlan sp = plan_rmsnorm_staged(p, a.H, (int)sizeof(T), ADD ? 3 : 2, dev);

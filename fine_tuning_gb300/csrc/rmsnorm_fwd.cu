@@ -286,6 +286,95 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_rows(const FwdParams<T, Idx> 
   }
 }
 
+// Rows that fit one warp (W = 1): persistent, one row per warp at a time,
+// rows row, row + 8P, ...  Each lane copies its packets of the rows
+// kPipeBufs - 1 ahead into a per-warp shared-memory ring with cp.async while
+// it normalises the current row, so the loads of later rows overlap the
+// arithmetic and the stores of this one.  Lane l owns packets l, l + 32, ...
+// and sums its squares in that order before the warp reduction: the row
+// plan's order, so an rstd the backward recomputes is bit-identical.
+template <bool ADD> struct FwdPipe {
+  static constexpr int kBufs = ADD ? 2 : 4;  // rows in the ring per warp
+};
+
+template <typename T, typename Idx, int N, int V, bool ADD>
+__global__ void __launch_bounds__(256) rmsnorm_fwd_pipe(const FwdParams<T, Idx> a) {
+  constexpr int kBufs = FwdPipe<ADD>::kBufs;
+  constexpr int kSl = (ADD ? 2 : 1) * V;  // 16-byte slots per lane per row: x (, res)
+  extern __shared__ uint4 ring[];         // [warps][kBufs][kSl][32]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint4 *my = ring + warp * (kBufs * kSl * 32);
+  pdl_wait();
+  pdl_trigger();
+  Packet<T, N> wv[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k)
+    if (lane + 32 * k < a.hp) wv[k] = load_packet<T, N>(a.w + (Idx)(lane + 32 * k) * N);
+  const Idx step = (Idx)gridDim.x * (blockDim.x >> 5);
+  auto stage = [&](Idx r, int b) {
+    if (r < a.rows) {
+      const T *xr = a.x + r * a.ldx;
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const int c = lane + 32 * k;
+        if (c < a.hp) {
+          cp_async16(my + (b * kSl + k) * 32 + lane, xr + (Idx)c * N);
+          if (ADD) cp_async16(my + (b * kSl + V + k) * 32 + lane, a.res + r * a.ldr + (Idx)c * N);
+        }
+      }
+    }
+    cp_async_commit();  // one group per row on every lane, empty or not
+  };
+  Idx row = (Idx)blockIdx.x * (blockDim.x >> 5) + warp, r2 = row;
+  stage(r2, 0);
+  for (int i = 1; i < kBufs - 1; ++i) {
+    r2 += step;
+    stage(r2, i);
+  }
+  int b = 0;
+  while (row < a.rows) {  // warp-uniform
+    r2 += step;
+    stage(r2, b == 0 ? kBufs - 1 : b - 1);  // the next rows' loads fly meanwhile
+    cp_async_wait<kBufs - 1>();              // this lane's copies of `row` have landed
+    Packet<T, N> xv[V];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      if (lane + 32 * k < a.hp) {
+        *reinterpret_cast<uint4 *>(&xv[k]) = my[(b * kSl + k) * 32 + lane];
+        if (ADD) {
+          Packet<T, N> rv;
+          *reinterpret_cast<uint4 *>(&rv) = my[(b * kSl + V + k) * 32 + lane];
+          xv[k] = norm_input<T, N, ADD>(xv[k], rv);
+        }
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const float f = xv[k].get(e);
+          ss = fmaf(f, f, ss);
+        }
+      }
+    }
+    ss = warp_sum(ss);
+    const float r = rsqrtf(fmaf(ss, a.inv_h, a.eps));
+    if (a.rstd != nullptr && lane == 0) a.rstd[row] = r;
+    T *yr = a.y + row * a.ldy;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const int c = lane + 32 * k;
+      if (c < a.hp) {
+        if (ADD) store_packet<T, N>(a.h + row * a.ldh + (Idx)c * N, xv[k]);
+        Packet<T, N> o;
+#pragma unroll
+        for (int e = 0; e < N; ++e) o.set(e, (xv[k].get(e) * r) * wv[k].get(e));
+        store_packet<T, N>(yr + (Idx)c * N, o);
+      }
+    }
+    row += step;
+    b = b + 1 == kBufs ? 0 : b + 1;
+  }
+  cp_async_wait<0>();
+}
+
 // Rows longer than the register plan: one CTA per row (grid-stride over
 // rows), sum of squares first (writing h when ADD), then a second pass that
 // re-reads the row (from L2).
@@ -330,6 +419,19 @@ cudaError_t fwd_rows_v(const RowPlan &p, const FwdParams<T, Idx> &k, cudaStream_
   const size_t smem = sizeof(float) * p.R * p.W;
   cudaError_t le = launch_pdl(rmsnorm_fwd_rows<T, Idx, N, V, ADD>, grid, dim3(p.threads()), smem,
                               s, k);
+  if (le != cudaSuccess) return le;
+  return cudaGetLastError();
+}
+
+template <typename T, typename Idx, int N, int V, bool ADD>
+cudaError_t fwd_pipe_v(const FwdParams<T, Idx> &k, const DeviceInfo &dev, cudaStream_t s) {
+  auto kern = rmsnorm_fwd_pipe<T, Idx, N, V, ADD>;
+  const size_t smem =
+      sizeof(uint4) * 8 * FwdPipe<ADD>::kBufs * (ADD ? 2 : 1) * V * 32;  // 8 warps
+  const int occ = blocks_per_sm((const void *)kern, 256, smem, dev, 8);
+  int64_t P = ceil_div((int64_t)k.rows, (int64_t)8);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  cudaError_t le = launch_pdl(kern, dim3((unsigned)P), dim3(256), smem, s, k);
   if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
@@ -386,6 +488,16 @@ cudaError_t fwd_typed(bool vec, const RmsNormFwdArgs &a, const DeviceInfo &dev, 
                                 0, s, k, (Idx)a.H);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
+  }
+  // Rows of one warp: the per-warp cp.async pipeline at every batch size.
+  if (vec && p.W == 1) {
+    switch (p.V) {
+      case 1: return fwd_pipe_v<T, Idx, NV, 1, ADD>(k, dev, s);
+      case 2: return fwd_pipe_v<T, Idx, NV, 2, ADD>(k, dev, s);
+      case 3: return fwd_pipe_v<T, Idx, NV, 3, ADD>(k, dev, s);
+      case 4: return fwd_pipe_v<T, Idx, NV, 4, ADD>(k, dev, s);
+      default: break;
+    }
   }
   // The staged pipeline pays off once every row group streams a dozen rows
   // or more; smaller batches finish sooner with one row per group and the
