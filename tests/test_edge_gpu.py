@@ -72,6 +72,8 @@ def code(dtype):
     (5, 20000, 0),      # row too long for registers: CTA-per-row kernels
     (300, 5120, 0),     # multi-warp rows
     (3, 8, 0),          # tiny rows
+    (4099, 512, 0),     # rows of one warp, many rows per warp (pipelined kernels)
+    (2053, 1024, 0),    # one-warp rows of four packets per lane (bf16)
 ])
 def test_rmsnorm_shapes(dtype, T, H, skew):
     eps = 1e-6
@@ -251,6 +253,8 @@ def rope_case(lens, Hq, Hkv, D, theta, dtype, seed=40):
     ((33, 12), 3, 1, 18),                  # D/2 = 9: element-wise path
     ((40,), 8, 0, 64),                     # no K heads
     ((20, 20), 5, 3, 512),                 # widest head
+    ((20011,), 6, 2, 64),                  # many passes per warp, ragged last pass
+    (tuple((i * 7) % 9 for i in range(2100)), 4, 2, 64),  # > 2,047 sequences: bounds via L1
 ])
 def test_rope_shapes(dtype, lens, Hq, Hkv, D):
     theta = 1e4
