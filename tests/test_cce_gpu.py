@@ -102,9 +102,11 @@ def test_tiny_full():
 
 
 @pytest.mark.parametrize("T,H,V", [(1, 64, 300), (129, 128, 8192), (130, 96, 8193),
-                                   (64, 200, 17000)])
+                                   (64, 200, 17000), (200, 448, 20000), (300, 576, 17001)])
 def test_shapes(T, H, V):
-    # one token; an exact chunk; one column past a chunk; ragged H
+    # one token; an exact chunk; one column past a chunk; ragged H; the
+    # grouped dh + dW launches at tile widths 224 (H = 448) and 192 (H = 576),
+    # over two vocabulary chunks
     hw = W.HeadWorkload("case", T=T, H=H, V=V, seed=T + V, w_std=H ** -0.5)
     h, Wt, y, loss, lse, dh, dW = run(hw)
     check_forward(h, Wt, y, loss, lse)
