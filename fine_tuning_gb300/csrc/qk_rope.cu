@@ -18,15 +18,20 @@
 // the llama3 rule; the table is built on the host, rope_freqs.cu); the
 // kernels only ever see f_i = inv_freq_i / 2pi.
 //
-// A CTA owns TOK consecutive tokens.  Per token, TPT = NV * S threads: NV
-// packet slots across one half of a head times S head slots; the thread with
-// (slot s, packet j) rotates packet j of heads s, s+S, s+2S, ... (HPT heads
-// per pass).  Its loads are issued first; while they are in flight the CTA
-// copies the frequency table and the sequence boundaries (cu_seqlens, read
-// on the device: no host synchronisation) to shared memory, finds each
-// token's position by binary search there and computes cos/sin of its
-// TOK x D/2 angles once into shared memory, shared by every head of the
-// token.  No cos/sin table is read from HBM.
+// Heads whose half splits over a power-of-two number of lanes (every model
+// measured) take qk_rope_pipe: persistent warps walk (token, head pass)
+// pairs, each lane streaming its packets of the passes ahead through a
+// per-warp cp.async ring.  The other forms remain for the remaining head
+// sizes: qk_rope_staged (a TMA ring of whole tokens), qk_rope_warp (one warp
+// per token) and qk_rope_kernel, where a CTA owns TOK consecutive tokens
+// and, per token, TPT = NV * S threads (NV packet slots across one half of a
+// head times S head slots; the thread with (slot s, packet j) rotates
+// packet j of heads s, s+S, s+2S, ..., HPT heads per pass).  Every form finds
+// a token's position by a binary search of the sequence boundaries
+// (cu_seqlens, read on the device: no host synchronisation), kept in shared
+// memory when they fit, and computes cos/sin of the token's D/2 angles once
+// into shared memory, shared by every head of the token.  No cos/sin table
+// is read from HBM.
 //
 // The angle is formed in turns, phi / 2pi = p * f_i with f_i split on the
 // host into two floats (hi + lo, ~48 significant bits); p is split into a
