@@ -286,40 +286,46 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_rows(const FwdParams<T, Idx> 
   }
 }
 
-// Rows that fit one warp (W = 1): persistent, one row per warp at a time,
-// rows row, row + 8P, ...  Each lane copies its packets of the rows
-// kPipeBufs - 1 ahead into a per-warp shared-memory ring with cp.async while
-// it normalises the current row, so the loads of later rows overlap the
-// arithmetic and the stores of this one.  Lane l owns packets l, l + 32, ...
-// and sums its squares in that order before the warp reduction: the row
-// plan's order, so an rstd the backward recomputes is bit-identical.
-template <bool ADD> struct FwdPipe {
-  static constexpr int kBufs = ADD ? 2 : 4;  // rows in the ring per warp
+// Rows of one or two warps' plan (W <= 2): persistent, one row per warp at
+// a time, rows row, row + 8P, ...  Each lane copies its packets of the rows
+// kBufs - 1 ahead into a per-warp shared-memory ring with cp.async while it
+// normalises the current row, so the loads of later rows overlap the
+// arithmetic and the stores of this one.  The warp plays the plan's W warps
+// in turn: lane l owns packets w 32 + l + k 32W (w < W, k < V), sums the
+// squares of each w separately in the plan's order, and adds the W warp
+// sums in order, so the row sum is the plan's bit for bit and an rstd the
+// backward recomputes is identical.
+template <int W, int V, bool ADD> struct FwdPipe {
+  static constexpr int kBufs = (ADD || W * V > 4) ? 2 : 4;  // rows in the ring per warp
+  static constexpr int kSl = (ADD ? 2 : 1) * W * V;         // 16-byte slots per lane per row
 };
 
-template <typename T, typename Idx, int N, int V, bool ADD>
+template <typename T, typename Idx, int N, int V, int W, bool ADD>
 __global__ void __launch_bounds__(256) rmsnorm_fwd_pipe(const FwdParams<T, Idx> a) {
-  constexpr int kBufs = FwdPipe<ADD>::kBufs;
-  constexpr int kSl = (ADD ? 2 : 1) * V;  // 16-byte slots per lane per row: x (, res)
-  extern __shared__ uint4 ring[];         // [warps][kBufs][kSl][32]
+  constexpr int kBufs = FwdPipe<W, V, ADD>::kBufs;
+  constexpr int kSl = FwdPipe<W, V, ADD>::kSl;  // x (, res), W V packets each
+  constexpr int kP = W * V;                     // packets per lane
+  extern __shared__ uint4 ring[];               // [warps][kBufs][kSl][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint4 *my = ring + warp * (kBufs * kSl * 32);
+  // packet i = w V + k of this lane: column w 32 + lane + k 32W
+  auto col = [&](int i) { return (i / V) * 32 + lane + (i % V) * 32 * W; };
   pdl_wait();
   pdl_trigger();
-  Packet<T, N> wv[V];
+  Packet<T, N> wv[kP];
 #pragma unroll
-  for (int k = 0; k < V; ++k)
-    if (lane + 32 * k < a.hp) wv[k] = load_packet<T, N>(a.w + (Idx)(lane + 32 * k) * N);
+  for (int i = 0; i < kP; ++i)
+    if (col(i) < a.hp) wv[i] = load_packet<T, N>(a.w + (Idx)col(i) * N);
   const Idx step = (Idx)gridDim.x * (blockDim.x >> 5);
   auto stage = [&](Idx r, int b) {
     if (r < a.rows) {
       const T *xr = a.x + r * a.ldx;
 #pragma unroll
-      for (int k = 0; k < V; ++k) {
-        const int c = lane + 32 * k;
+      for (int i = 0; i < kP; ++i) {
+        const int c = col(i);
         if (c < a.hp) {
-          cp_async16(my + (b * kSl + k) * 32 + lane, xr + (Idx)c * N);
-          if (ADD) cp_async16(my + (b * kSl + V + k) * 32 + lane, a.res + r * a.ldr + (Idx)c * N);
+          cp_async16(my + (b * kSl + i) * 32 + lane, xr + (Idx)c * N);
+          if (ADD) cp_async16(my + (b * kSl + kP + i) * 32 + lane, a.res + r * a.ldr + (Idx)c * N);
         }
       }
     }
@@ -336,36 +342,44 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_pipe(const FwdParams<T, Idx> 
     r2 += step;
     stage(r2, b == 0 ? kBufs - 1 : b - 1);  // the next rows' loads fly meanwhile
     cp_async_wait<kBufs - 1>();              // this lane's copies of `row` have landed
-    Packet<T, N> xv[V];
-    float ss = 0.f;
+    Packet<T, N> xv[kP];
+    float part[W];
 #pragma unroll
-    for (int k = 0; k < V; ++k) {
-      if (lane + 32 * k < a.hp) {
-        *reinterpret_cast<uint4 *>(&xv[k]) = my[(b * kSl + k) * 32 + lane];
+    for (int w = 0; w < W; ++w) part[w] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kP; ++i) {
+      if (col(i) < a.hp) {
+        *reinterpret_cast<uint4 *>(&xv[i]) = my[(b * kSl + i) * 32 + lane];
         if (ADD) {
           Packet<T, N> rv;
-          *reinterpret_cast<uint4 *>(&rv) = my[(b * kSl + V + k) * 32 + lane];
-          xv[k] = norm_input<T, N, ADD>(xv[k], rv);
+          *reinterpret_cast<uint4 *>(&rv) = my[(b * kSl + kP + i) * 32 + lane];
+          xv[i] = norm_input<T, N, ADD>(xv[i], rv);
         }
 #pragma unroll
         for (int e = 0; e < N; ++e) {
-          const float f = xv[k].get(e);
-          ss = fmaf(f, f, ss);
+          const float f = xv[i].get(e);
+          part[i / V] = fmaf(f, f, part[i / V]);
         }
       }
     }
-    ss = warp_sum(ss);
+    float ss = 0.f;
+    if (W == 1) {
+      ss = warp_sum(part[0]);
+    } else {
+#pragma unroll
+      for (int w = 0; w < W; ++w) ss += warp_sum(part[w]);  // the plan's combine order
+    }
     const float r = rsqrtf(fmaf(ss, a.inv_h, a.eps));
     if (a.rstd != nullptr && lane == 0) a.rstd[row] = r;
     T *yr = a.y + row * a.ldy;
 #pragma unroll
-    for (int k = 0; k < V; ++k) {
-      const int c = lane + 32 * k;
+    for (int i = 0; i < kP; ++i) {
+      const int c = col(i);
       if (c < a.hp) {
-        if (ADD) store_packet<T, N>(a.h + row * a.ldh + (Idx)c * N, xv[k]);
+        if (ADD) store_packet<T, N>(a.h + row * a.ldh + (Idx)c * N, xv[i]);
         Packet<T, N> o;
 #pragma unroll
-        for (int e = 0; e < N; ++e) o.set(e, (xv[k].get(e) * r) * wv[k].get(e));
+        for (int e = 0; e < N; ++e) o.set(e, (xv[i].get(e) * r) * wv[i].get(e));
         store_packet<T, N>(yr + (Idx)c * N, o);
       }
     }
@@ -423,11 +437,11 @@ cudaError_t fwd_rows_v(const RowPlan &p, const FwdParams<T, Idx> &k, cudaStream_
   return cudaGetLastError();
 }
 
-template <typename T, typename Idx, int N, int V, bool ADD>
+template <typename T, typename Idx, int N, int V, int W, bool ADD>
 cudaError_t fwd_pipe_v(const FwdParams<T, Idx> &k, const DeviceInfo &dev, cudaStream_t s) {
-  auto kern = rmsnorm_fwd_pipe<T, Idx, N, V, ADD>;
+  auto kern = rmsnorm_fwd_pipe<T, Idx, N, V, W, ADD>;
   const size_t smem =
-      sizeof(uint4) * 8 * FwdPipe<ADD>::kBufs * (ADD ? 2 : 1) * V * 32;  // 8 warps
+      sizeof(uint4) * 8 * FwdPipe<W, V, ADD>::kBufs * FwdPipe<W, V, ADD>::kSl * 32;  // 8 warps
   const int occ = blocks_per_sm((const void *)kern, 256, smem, dev, 8);
   int64_t P = ceil_div((int64_t)k.rows, (int64_t)8);
   if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
@@ -489,16 +503,19 @@ cudaError_t fwd_typed(bool vec, const RmsNormFwdArgs &a, const DeviceInfo &dev, 
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
   }
-  // Rows of one warp: the per-warp cp.async pipeline at every batch size.
+  // Rows of one warp's plan, and (without the residual) of two warps' plan:
+  // the per-warp cp.async pipeline at every batch size.
   if (vec && p.W == 1) {
     switch (p.V) {
-      case 1: return fwd_pipe_v<T, Idx, NV, 1, ADD>(k, dev, s);
-      case 2: return fwd_pipe_v<T, Idx, NV, 2, ADD>(k, dev, s);
-      case 3: return fwd_pipe_v<T, Idx, NV, 3, ADD>(k, dev, s);
-      case 4: return fwd_pipe_v<T, Idx, NV, 4, ADD>(k, dev, s);
+      case 1: return fwd_pipe_v<T, Idx, NV, 1, 1, ADD>(k, dev, s);
+      case 2: return fwd_pipe_v<T, Idx, NV, 2, 1, ADD>(k, dev, s);
+      case 3: return fwd_pipe_v<T, Idx, NV, 3, 1, ADD>(k, dev, s);
+      case 4: return fwd_pipe_v<T, Idx, NV, 4, 1, ADD>(k, dev, s);
       default: break;
     }
   }
+  if constexpr (!ADD)
+    if (vec && p.W == 2 && p.V == 4) return fwd_pipe_v<T, Idx, NV, 4, 2, ADD>(k, dev, s);
   // The staged pipeline pays off once every row group streams a dozen rows
   // or more; smaller batches finish sooner with one row per group and the
   // hardware scheduler refilling SMs (rmsnorm_fwd_rows).
