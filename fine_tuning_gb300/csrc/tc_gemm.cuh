@@ -116,10 +116,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 // The tcgen05 instructions of this kernel all act on the CTA pair
 // (cta_group::2).  Allocation and release: one warp in each of the two
 // CTAs, collectively; the same columns in both CTAs' tensor memory.
