@@ -14,11 +14,14 @@
 // accumulates dy*x*r for its columns in fp32 registers over the rows its
 // group visits.  At the end the R row groups of a CTA are summed in shared
 // memory in a fixed order and the CTA writes one fp32 row of partials to the
-// workspace.  For 16-byte aligned rows (rmsnorm_bwd_staged) one elected
-// thread per row group streams the next S rows of x and dy (and dh) into a
-// ring of shared-memory stages with bulk copies (cp.async.bulk, completing on
-// mbarriers) and the warps compute from shared memory; other rows hold their
-// packets in registers (rmsnorm_bwd_rows).
+// workspace.  16-byte aligned rows of one warp (without dh) take
+// rmsnorm_bwd_pipe, each lane streaming its packets of the next row through
+// a per-warp cp.async ring.  Other 16-byte aligned rows (rmsnorm_bwd_staged)
+// have one elected thread per row group stream the next S rows of x and dy
+// (and dh) into a ring of shared-memory stages with bulk copies
+// (cp.async.bulk, completing on mbarriers) while the warps compute from
+// shared memory; the rest hold their packets in registers
+// (rmsnorm_bwd_rows).
 // Pass 2 (dw_reduce): dw[j] = sum_p ws[p, j], rows in a fixed order.
 // The row -> CTA map and every summation order are fixed, so dw is bitwise
 // reproducible; no CTA ever waits on another.

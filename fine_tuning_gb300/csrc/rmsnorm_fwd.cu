@@ -10,12 +10,15 @@
 // through shared memory in a fixed order), then every thread scales its own
 // packets.  R row groups share a CTA so that CTAs stay at 128-256 threads.
 //
-// 16-byte aligned rows take rmsnorm_fwd_staged: a persistent grid in which
-// one elected thread per row group streams the group's next S rows into a
-// ring of shared-memory stages with bulk copies (cp.async.bulk, the TMA
-// engine's 1-D mode) completing on mbarriers; the warps compute from shared
-// memory.  Bytes in flight then cost no registers, and a row's copy starts
-// S rows before it is needed.  Other rows hold their packets in registers
+// 16-byte aligned rows of one or two warps' plan take rmsnorm_fwd_pipe: a
+// persistent grid of single warps, each lane streaming its packets of the
+// rows ahead through a per-warp cp.async ring.  Longer aligned rows take
+// rmsnorm_fwd_staged once the batch is large: a persistent grid in which one
+// elected thread per row group streams the group's next S rows into a ring
+// of shared-memory stages with bulk copies (cp.async.bulk, the TMA engine's
+// 1-D mode) completing on mbarriers; the warps compute from shared memory.
+// Bytes in flight then cost no registers, and a row's copy starts S rows
+// before it is needed.  Other rows hold their packets in registers
 // (rmsnorm_fwd_rows); rows too long for either take a CTA-per-row kernel.
 #include "common.cuh"
 #include "launch.h"
