@@ -66,46 +66,53 @@ __device__ __forceinline__ float dx_value(float a, float xf, float r, float wf, 
   return ADD ? dhf + v : v;
 }
 
-// Rows that fit one warp (W = 1): persistent, one row per warp at a time,
-// rows row, row + 8P, ...; each lane copies its packets of x and dy (and dh,
-// and r when saved) of the next row into a per-warp shared-memory ring with
-// cp.async while it works on the current one.  Lane l owns packets l,
-// l + 32, ... (the row plan's columns and summation order).  The CTA's eight
-// warps combine their dw sums in a fixed order at the end, in the ring's
-// memory, into the CTA's partial row.
+// Rows of one or two warps' plan (W <= 2): persistent, one row per group of
+// W warps at a time, rows row, row + (8 / W) P, ...; each lane copies its
+// packets of x and dy (and dh, and r when saved) of the group's next row
+// into its warp's shared-memory ring with cp.async while it works on the
+// current one.  Lane l of warp w in the group owns packets w 32 + l + k 32W
+// (the row plan's columns and summation order); with W = 2 the two warps'
+// sums meet in shared memory (slots double-buffered by row parity) behind a
+// named barrier of the pair and are added in the plan's order.  The CTA's
+// row groups combine their dw sums in a fixed order at the end, in the
+// ring's memory, into the CTA's partial row.
 constexpr int kBwdPipeBufs = 2;
 template <int V, bool ADD> constexpr int bwd_pipe_slots() { return (ADD ? 3 : 2) * V + 1; }
 template <int V, bool ADD> constexpr size_t bwd_pipe_smem() {
   return sizeof(uint4) * 8 * kBwdPipeBufs * bwd_pipe_slots<V, ADD>() * 32;  // 8 warps
 }
 
-template <typename T, typename Idx, int N, int V, bool HAS_RSTD, bool ADD>
+template <typename T, typename Idx, int N, int V, int W, bool HAS_RSTD, bool ADD>
 __global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> a) {
   constexpr int kSl = bwd_pipe_slots<V, ADD>();  // x[V], dy[V] (, dh[V]), r
+  constexpr int R = 8 / W;                       // row groups per CTA
   extern __shared__ uint4 ring[];                // [warps][kBwdPipeBufs][kSl][32]
+  __shared__ float2 red[2][R][W];                // the groups' warp sums, by row parity
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / W, wig = warp - grp * W;
   const int hp = a.hp;
   uint4 *my = ring + warp * (kBwdPipeBufs * kSl * 32);
+  auto col = [&](int k) { return wig * 32 + lane + k * 32 * W; };
   pdl_wait();
   pdl_trigger();
 
   Packet<T, N> wv[V];
 #pragma unroll
   for (int k = 0; k < V; ++k)
-    if (lane + 32 * k < hp) wv[k] = load_packet<T, N>(a.w + (Idx)(lane + 32 * k) * N);
+    if (col(k) < hp) wv[k] = load_packet<T, N>(a.w + (Idx)col(k) * N);
   float acc[V][N];
 #pragma unroll
   for (int k = 0; k < V; ++k)
 #pragma unroll
     for (int e = 0; e < N; ++e) acc[k][e] = 0.f;
 
-  const Idx step = (Idx)gridDim.x * (blockDim.x >> 5);
+  const Idx step = (Idx)gridDim.x * R;
   auto stage = [&](Idx r, int b) {
     if (r < a.rows) {
       uint4 *d = my + b * kSl * 32 + lane;
 #pragma unroll
       for (int k = 0; k < V; ++k) {
-        const int c = lane + 32 * k;
+        const int c = col(k);
         if (c < hp) {
           cp_async16(d + k * 32, a.x + r * a.ldx + (Idx)c * N);
           cp_async16(d + (V + k) * 32, a.dy + r * a.lddy + (Idx)c * N);
@@ -116,10 +123,10 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> 
     }
     cp_async_commit();  // one group per row on every lane, empty or not
   };
-  Idx row = (Idx)blockIdx.x * (blockDim.x >> 5) + warp;
+  Idx row = (Idx)blockIdx.x * R + grp;
   stage(row, 0);
-  int b = 0;
-  while (row < a.rows) {  // warp-uniform
+  int b = 0, parity = 0;
+  while (row < a.rows) {  // uniform across the group's warps
     stage(row + step, b ^ 1);  // the next row's loads fly meanwhile
     cp_async_wait<1>();        // this lane's copies of `row` have landed
     const uint4 *d = my + b * kSl * 32 + lane;
@@ -127,7 +134,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> 
     float2 cs = make_float2(0.f, 0.f);  // (sum dy*w*x, sum x*x)
 #pragma unroll
     for (int k = 0; k < V; ++k) {
-      if (lane + 32 * k < hp) {
+      if (col(k) < hp) {
         *reinterpret_cast<uint4 *>(&xv[k]) = d[k * 32];
         *reinterpret_cast<uint4 *>(&gv[k]) = d[(V + k) * 32];
 #pragma unroll
@@ -138,19 +145,29 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> 
         }
       }
     }
-    float r;
-    if (HAS_RSTD) {
+    if (HAS_RSTD)
       cs.x = warp_sum(cs.x);
-      r = *reinterpret_cast<const float *>(d + (kSl - 1) * 32);
-    } else {
+    else
       cs = warp_sum2(cs);
-      r = rsqrtf(fmaf(cs.y, a.inv_h, a.eps));
+    if (W > 1) {
+      float2 *slot = red[parity][grp];
+      if (lane == 0) slot[wig] = cs;
+      named_barrier(1 + grp, 32 * W);
+      cs = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < W; ++i) {
+        cs.x += slot[i].x;
+        cs.y += slot[i].y;
+      }
+      parity ^= 1;
     }
+    const float r = HAS_RSTD ? *reinterpret_cast<const float *>(d + (kSl - 1) * 32)
+                             : rsqrtf(fmaf(cs.y, a.inv_h, a.eps));
     const float am = r * r * r * cs.x * a.inv_h;
     T *dr = a.dx + row * a.lddx;
 #pragma unroll
     for (int k = 0; k < V; ++k) {
-      const int c = lane + 32 * k;
+      const int c = col(k);
       if (c < hp) {
         Packet<T, N> hv, o;
         if (ADD) *reinterpret_cast<uint4 *>(&hv) = d[(2 * V + k) * 32];
@@ -167,22 +184,21 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> 
     b ^= 1;
   }
   cp_async_wait<0>();
-  __syncthreads();  // every warp is done with its ring: it becomes [8][H] partials
+  __syncthreads();  // every warp is done with its ring: it becomes [R][H] partials
   float *part = reinterpret_cast<float *>(ring);
-  float *mine = part + warp * a.H;
+  float *mine = part + grp * a.H;
 #pragma unroll
   for (int k = 0; k < V; ++k) {
-    const int c = lane + 32 * k;
+    const int c = col(k);
     if (c < hp)
 #pragma unroll
       for (int e = 0; e < N; ++e) mine[c * N + e] = acc[k][e];
   }
   __syncthreads();
   float *dst = a.ws + (size_t)blockIdx.x * a.H;
-  const int nw = (int)(blockDim.x >> 5);
   for (int j = threadIdx.x; j < a.H; j += blockDim.x) {
     float sum = 0.f;
-    for (int g = 0; g < nw; ++g) sum += part[g * a.H + j];
+    for (int g = 0; g < R; ++g) sum += part[g * a.H + j];
     dst[j] = sum;
   }
 }
@@ -521,6 +537,17 @@ cudaError_t launch_dw_reduce(const RmsNormBwdArgs &a, int64_t P, cudaStream_t s)
   return launch_dw_reduce(a.ws, P, a.H, a.H, a.dw, s);
 }
 
+// Resident CTAs per SM of the saved-rstd and recomputing forms of a
+// backward kernel, the smaller of the two.  The CTA count, and with it the
+// row -> CTA map and the order in which dw is summed, is then the same in
+// both modes, so dw does not depend on whether rstd was saved.
+inline int min_blocks_per_sm(const void *with_rstd, const void *without, int threads, size_t smem,
+                             const DeviceInfo &dev) {
+  const int a = blocks_per_sm(with_rstd, threads, smem, dev, kMaxBlocksPerSm);
+  const int b = blocks_per_sm(without, threads, smem, dev, kMaxBlocksPerSm);
+  return a < b ? a : b;
+}
+
 template <typename T, typename Idx, int N, int V, bool HAS_RSTD, bool ADD>
 cudaError_t bwd_rows_v(const RowPlan &p, const BwdParams<T, Idx> &k, const RmsNormBwdArgs &a,
                        const DeviceInfo &dev, cudaStream_t s) {
@@ -528,7 +555,10 @@ cudaError_t bwd_rows_v(const RowPlan &p, const BwdParams<T, Idx> &k, const RmsNo
   const int threads = p.threads();
   const size_t smem = sizeof(float) * (4 * p.R * p.W + (p.R > 1 ? (size_t)p.R * a.H : 0));
   if (smem > (size_t)dev.max_smem_optin) return cudaErrorInvalidConfiguration;
-  const int occ = blocks_per_sm((const void *)kern, threads, smem, dev, kMaxBlocksPerSm);
+  // the grid must not depend on whether rstd is saved (dw's summation order)
+  const int occ = min_blocks_per_sm((const void *)rmsnorm_bwd_rows<T, Idx, N, V, true, ADD>,
+                                    (const void *)rmsnorm_bwd_rows<T, Idx, N, V, false, ADD>,
+                                    threads, smem, dev);
   int64_t P = ceil_div(a.T, (int64_t)p.R);
   if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
   if (P > a.ws_rows) P = a.ws_rows;
@@ -542,7 +572,10 @@ cudaError_t bwd_staged_v(const RowPlan &p, const StagedPlan &sp, const BwdParams
                          const RmsNormBwdArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   auto kern = rmsnorm_bwd_staged<T, Idx, N, V, HAS_RSTD, ADD>;
   const int threads = p.threads();
-  const int occ = blocks_per_sm((const void *)kern, threads, sp.smem, dev, kMaxBlocksPerSm);
+  // the grid must not depend on whether rstd is saved (dw's summation order)
+  const int occ = min_blocks_per_sm((const void *)rmsnorm_bwd_staged<T, Idx, N, V, true, ADD>,
+                                    (const void *)rmsnorm_bwd_staged<T, Idx, N, V, false, ADD>,
+                                    threads, sp.smem, dev);
   int64_t P = ceil_div(a.T, (int64_t)p.R);
   if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
   if (P > a.ws_rows) P = a.ws_rows;
@@ -556,14 +589,18 @@ cudaError_t bwd_staged_v(const RowPlan &p, const StagedPlan &sp, const BwdParams
   return launch_dw_reduce(a, P, s);
 }
 
-template <typename T, typename Idx, int N, int V, bool HAS_RSTD, bool ADD>
+template <typename T, typename Idx, int N, int V, int W, bool HAS_RSTD, bool ADD>
 cudaError_t bwd_pipe_v(const BwdParams<T, Idx> &k, const RmsNormBwdArgs &a, const DeviceInfo &dev,
                        cudaStream_t s) {
-  auto kern = rmsnorm_bwd_pipe<T, Idx, N, V, HAS_RSTD, ADD>;
+  auto kern = rmsnorm_bwd_pipe<T, Idx, N, V, W, HAS_RSTD, ADD>;
   constexpr size_t smem = bwd_pipe_smem<V, ADD>();
-  static_assert(smem >= sizeof(float) * 8 * 32 * V * N, "the ring holds the [8][H] partials");
-  const int occ = blocks_per_sm((const void *)kern, 256, smem, dev, kMaxBlocksPerSm);
-  int64_t P = ceil_div(a.T, (int64_t)8);
+  static_assert(smem >= sizeof(float) * (8 / W) * 32 * W * V * N,
+                "the ring holds the [R][H] partials");
+  // the grid must not depend on whether rstd is saved (dw's summation order)
+  const int occ = min_blocks_per_sm((const void *)rmsnorm_bwd_pipe<T, Idx, N, V, W, true, ADD>,
+                                    (const void *)rmsnorm_bwd_pipe<T, Idx, N, V, W, false, ADD>,
+                                    256, smem, dev);
+  int64_t P = ceil_div(a.T, (int64_t)(8 / W));
   if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
   if (P > a.ws_rows) P = a.ws_rows;
   cudaError_t e = launch_pdl(kern, dim3((unsigned)P), dim3(256), smem, s, k);
@@ -612,17 +649,20 @@ cudaError_t bwd_typed(bool vec, const RmsNormBwdArgs &a, const DeviceInfo &dev,
     if (e != cudaSuccess) return e;
     return launch_dw_reduce(a, P, s);
   }
-  // rows of one warp: the per-warp cp.async pipeline (not with the residual
-  // gradient: its third input costs the registers of a second CTA per SM,
-  // and the staged ring measured faster there)
-  if (vec && p.W == 1 && !ADD) {
-    switch (p.V) {
-      case 1: return bwd_pipe_v<T, Idx, NV, 1, HAS_RSTD, ADD>(k, a, dev, s);
-      case 2: return bwd_pipe_v<T, Idx, NV, 2, HAS_RSTD, ADD>(k, a, dev, s);
-      case 3: return bwd_pipe_v<T, Idx, NV, 3, HAS_RSTD, ADD>(k, a, dev, s);
-      case 4: return bwd_pipe_v<T, Idx, NV, 4, HAS_RSTD, ADD>(k, a, dev, s);
-      default: break;
+  // rows of one or two warps' plan: the per-warp cp.async pipeline (not
+  // with the residual gradient: its third input costs the registers of a
+  // second CTA per SM, and the staged ring measured faster there)
+  if constexpr (!ADD) {
+    if (vec && p.W == 1) {
+      switch (p.V) {
+        case 1: return bwd_pipe_v<T, Idx, NV, 1, 1, HAS_RSTD, ADD>(k, a, dev, s);
+        case 2: return bwd_pipe_v<T, Idx, NV, 2, 1, HAS_RSTD, ADD>(k, a, dev, s);
+        case 3: return bwd_pipe_v<T, Idx, NV, 3, 1, HAS_RSTD, ADD>(k, a, dev, s);
+        case 4: return bwd_pipe_v<T, Idx, NV, 4, 1, HAS_RSTD, ADD>(k, a, dev, s);
+        default: break;
+      }
     }
+    if (vec && p.W == 2 && p.V == 4) return bwd_pipe_v<T, Idx, NV, 4, 2, HAS_RSTD, ADD>(k, a, dev, s);
   }
   if (vec) {
     const StagedPlan sp = plan_rmsnorm_staged(p, a.H, (int)sizeof(T), ADD ? 3 : 2, dev);
