@@ -112,7 +112,7 @@ KERNEL_SOURCES = {"rmsnorm_fwd": ("rmsnorm_fwd.cu",),
                   "qk_norm_rope_bwd": ("qk_norm_rope.cu", "rope_common.cuh", "dw_reduce.cuh")}
 # widened ops timed beside the step (not part of it), with their launches
 EXT_OPS = {"rmsnorm_add_fwd": 1, "rmsnorm_add_bwd": 2, "swiglu_bwd_h": 1, "qk_rope_freq_fwd": 1,
-           "qk_norm_rope_fwd": 1, "qk_norm_rope_bwd": 3}
+           "qk_norm_rope_fwd": 1, "qk_norm_rope_bwd": 2}
 
 
 def kernel_source_hash(op: str) -> str:

@@ -10,13 +10,16 @@ namespace ftk {
 
 namespace {
 
-// dw[j] = sum_{p < P} ws[p * ld + j], j < H: a CTA owns 32 columns; its 32
-// warps take the rows p = warp, warp + 32, ... and their sums are added in
-// warp order.
+// out[j] = sum_{p < P} ws[p * ld + j] for the columns j < H: a CTA owns 32
+// columns; its 32 warps take the rows p = warp, warp + 32, ... and their sums
+// are added in warp order.  Column j goes to out0[j] when j < split, else to
+// out1[j - split] (two weights whose partial rows sit side by side); a null
+// output is skipped.
 constexpr int kReduceWarps = 32;
 
 __global__ void __launch_bounds__(32 * kReduceWarps)
-dw_reduce(const float *__restrict__ ws, int P, int H, int ld, float *__restrict__ dw) {
+dw_reduce(const float *__restrict__ ws, int P, int H, int ld, float *__restrict__ out0, int split,
+          float *__restrict__ out1) {
   __shared__ float part[kReduceWarps][33];
   pdl_wait();
   pdl_trigger();
@@ -33,21 +36,28 @@ dw_reduce(const float *__restrict__ ws, int P, int H, int ld, float *__restrict_
     float t = 0.f;
 #pragma unroll
     for (int i = 0; i < kReduceWarps; ++i) t += part[i][lane];
-    dw[col] = t;
+    float *const out = col < split ? out0 : out1;
+    if (out) out[col < split ? col : col - split] = t;
   }
 }
 
 // Launches dw_reduce on the P partial rows (row stride ld) of H columns
-// (PDL, like the first pass); also reports an error left by the first
-// pass's launch.
+// (PDL, like the first pass); columns [0, split) go to out0, the rest to
+// out1.  Also reports an error left by the first pass's launch.
 inline cudaError_t launch_dw_reduce(const float *ws, int64_t P, int64_t H, int64_t ld,
-                                    float *out, cudaStream_t s) {
+                                    float *out0, int64_t split, float *out1, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = launch_pdl(dw_reduce, dim3((unsigned)ceil_div(H, (int64_t)32)), dim3(32 * kReduceWarps), 0,
-                 s, ws, (int)P, (int)H, (int)ld, out);
+                 s, ws, (int)P, (int)H, (int)ld, out0, (int)split, out1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// The single-output form: out[j] for all H columns.
+inline cudaError_t launch_dw_reduce(const float *ws, int64_t P, int64_t H, int64_t ld, float *out,
+                                    cudaStream_t s) {
+  return launch_dw_reduce(ws, P, H, ld, out, H, nullptr, s);
 }
 
 }  // namespace

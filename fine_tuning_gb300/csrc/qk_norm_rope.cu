@@ -601,12 +601,15 @@ cudaError_t bwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &
   const size_t smem = sizeof(float2) * (size_t)kWarps * (a.D / 2) +
                       sizeof(float) * (size_t)kWarps * 2 * a.D + (warp_path ? kBwdStageBytes : 0);
   const bool rstd = a.rq != nullptr || a.rk != nullptr;
-  const void *kern =
-      warp_path ? (rstd ? (const void *)qk_norm_rope_bwd_warp<T, Idx, NV, true>
-                        : (const void *)qk_norm_rope_bwd_warp<T, Idx, NV, false>)
-                : (rstd ? (const void *)qk_norm_rope_bwd_generic<T, Idx, true>
-                        : (const void *)qk_norm_rope_bwd_generic<T, Idx, false>);
-  const int occ = blocks_per_sm(kern, kThreads, smem, dev, kMaxBlocksPerSm);
+  // the grid (and with it the order of dwq's and dwk's sums) must not depend
+  // on whether r is saved: size it for the less resident of the two forms
+  const void *k_saved = warp_path ? (const void *)qk_norm_rope_bwd_warp<T, Idx, NV, true>
+                                  : (const void *)qk_norm_rope_bwd_generic<T, Idx, true>;
+  const void *k_recomp = warp_path ? (const void *)qk_norm_rope_bwd_warp<T, Idx, NV, false>
+                                   : (const void *)qk_norm_rope_bwd_generic<T, Idx, false>;
+  const int occ_s = blocks_per_sm(k_saved, kThreads, smem, dev, kMaxBlocksPerSm);
+  const int occ_r = blocks_per_sm(k_recomp, kThreads, smem, dev, kMaxBlocksPerSm);
+  const int occ = occ_s < occ_r ? occ_s : occ_r;
   int64_t P = ceil_div(a.T, (int64_t)kWarps);
   if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
   if (P > a.ws_rows) P = a.ws_rows;
@@ -620,13 +623,9 @@ cudaError_t bwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &
     e = rstd ? launch_pdl(qk_norm_rope_bwd_generic<T, Idx, true>, grid, block, smem, s, k, fr)
              : launch_pdl(qk_norm_rope_bwd_generic<T, Idx, false>, grid, block, smem, s, k, fr);
   if (e != cudaSuccess) return e;
-  // dwq from columns [0, D) of the partial rows, dwk from [D, 2D)
-  if (a.dwq) {
-    e = launch_dw_reduce(a.ws, P, a.D, 2 * (int64_t)a.D, a.dwq, s);
-    if (e != cudaSuccess) return e;
-  }
-  if (a.dwk) {
-    e = launch_dw_reduce(a.ws + a.D, P, a.D, 2 * (int64_t)a.D, a.dwk, s);
+  // dwq from columns [0, D) of the partial rows, dwk from [D, 2D): one launch
+  if (a.dwq || a.dwk) {
+    e = launch_dw_reduce(a.ws, P, 2 * (int64_t)a.D, 2 * (int64_t)a.D, a.dwq, a.D, a.dwk, s);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
