@@ -15,7 +15,7 @@
 // group visits.  At the end the R row groups of a CTA are summed in shared
 // memory in a fixed order and the CTA writes one fp32 row of partials to the
 // workspace.  16-byte aligned rows of one warp (without dh) take
-// rmsnorm_bwd_pipe, each lane streaming its packets of the next row through
+// rmsnorm_bwd_pipe, each lane streaming its packets of the next rows through
 // a per-warp cp.async ring.  Other 16-byte aligned rows (rmsnorm_bwd_staged)
 // have one elected thread per row group stream the next S rows of x and dy
 // (and dh) into a ring of shared-memory stages with bulk copies
@@ -68,30 +68,34 @@ __device__ __forceinline__ float dx_value(float a, float xf, float r, float wf, 
 
 // Rows of one or two warps' plan (W <= 2): persistent, one row per group of
 // W warps at a time, rows row, row + (8 / W) P, ...; each lane copies its
-// packets of x and dy (and dh, and r when saved) of the group's next row
-// into its warp's shared-memory ring with cp.async while it works on the
-// current one.  Lane l of warp w in the group owns packets w 32 + l + k 32W
+// packets of x and dy (and dh, and r when saved) of the group's next rows
+// (bwd_pipe_bufs - 1 of them) into its warp's shared-memory ring with
+// cp.async while it works on the current one.  Lane l of warp w in the group owns packets w 32 + l + k 32W
 // (the row plan's columns and summation order); with W = 2 the two warps'
 // sums meet in shared memory (slots double-buffered by row parity) behind a
 // named barrier of the pair and are added in the plan's order.  The CTA's
 // row groups combine their dw sums in a fixed order at the end, in the
 // ring's memory, into the CTA's partial row.
-constexpr int kBwdPipeBufs = 2;
+// Ring depth in rows: 3 for rows of one warp (few rows per warp, so the
+// loads of two rows ahead cover the ramp), 2 for two-warp rows (measured
+// faster there).
+template <int W> constexpr int bwd_pipe_bufs() { return W == 1 ? 3 : 2; }
 template <int V, bool ADD> constexpr int bwd_pipe_slots() { return (ADD ? 3 : 2) * V + 1; }
-template <int V, bool ADD> constexpr size_t bwd_pipe_smem() {
-  return sizeof(uint4) * 8 * kBwdPipeBufs * bwd_pipe_slots<V, ADD>() * 32;  // 8 warps
+template <int V, int W, bool ADD> constexpr size_t bwd_pipe_smem() {
+  return sizeof(uint4) * 8 * bwd_pipe_bufs<W>() * bwd_pipe_slots<V, ADD>() * 32;  // 8 warps
 }
 
 template <typename T, typename Idx, int N, int V, int W, bool HAS_RSTD, bool ADD>
 __global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> a) {
   constexpr int kSl = bwd_pipe_slots<V, ADD>();  // x[V], dy[V] (, dh[V]), r
+  constexpr int kBufs = bwd_pipe_bufs<W>();
   constexpr int R = 8 / W;                       // row groups per CTA
-  extern __shared__ uint4 ring[];                // [warps][kBwdPipeBufs][kSl][32]
+  extern __shared__ uint4 ring[];                // [warps][kBufs][kSl][32]
   __shared__ float2 red[2][R][W];                // the groups' warp sums, by row parity
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / W, wig = warp - grp * W;
   const int hp = a.hp;
-  uint4 *my = ring + warp * (kBwdPipeBufs * kSl * 32);
+  uint4 *my = ring + warp * (kBufs * kSl * 32);
   auto col = [&](int k) { return wig * 32 + lane + k * 32 * W; };
   pdl_wait();
   pdl_trigger();
@@ -124,11 +128,13 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> 
     cp_async_commit();  // one group per row on every lane, empty or not
   };
   Idx row = (Idx)blockIdx.x * R + grp;
-  stage(row, 0);
+#pragma unroll
+  for (int i = 0; i < kBufs - 1; ++i) stage(row + i * step, i);
   int b = 0, parity = 0;
   while (row < a.rows) {  // uniform across the group's warps
-    stage(row + step, b ^ 1);  // the next row's loads fly meanwhile
-    cp_async_wait<1>();        // this lane's copies of `row` have landed
+    // the loads of the next kBufs - 1 rows fly meanwhile
+    stage(row + (kBufs - 1) * step, b == 0 ? kBufs - 1 : b - 1);
+    cp_async_wait<kBufs - 1>();  // this lane's copies of `row` have landed
     const uint4 *d = my + b * kSl * 32 + lane;
     Packet<T, N> xv[V], gv[V];
     float2 cs = make_float2(0.f, 0.f);  // (sum dy*w*x, sum x*x)
@@ -181,7 +187,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> 
       }
     }
     row += step;
-    b ^= 1;
+    b = b == kBufs - 1 ? 0 : b + 1;
   }
   cp_async_wait<0>();
   __syncthreads();  // every warp is done with its ring: it becomes [R][H] partials
@@ -593,7 +599,7 @@ template <typename T, typename Idx, int N, int V, int W, bool HAS_RSTD, bool ADD
 cudaError_t bwd_pipe_v(const BwdParams<T, Idx> &k, const RmsNormBwdArgs &a, const DeviceInfo &dev,
                        cudaStream_t s) {
   auto kern = rmsnorm_bwd_pipe<T, Idx, N, V, W, HAS_RSTD, ADD>;
-  constexpr size_t smem = bwd_pipe_smem<V, ADD>();
+  constexpr size_t smem = bwd_pipe_smem<V, W, ADD>();
   static_assert(smem >= sizeof(float) * (8 / W) * 32 * W * V * N,
                 "the ring holds the [R][H] partials");
   // the grid must not depend on whether rstd is saved (dw's summation order)
