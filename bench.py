@@ -280,33 +280,60 @@ def sample_outputs(batch, n):
     return out
 
 
-def oracle_step(wl, cut, cu_host, n, scales=False):
-    """The whole path in the CPU oracle over the first n tokens."""
+def oracle_step(wl, cut, cu_host, n, scales=False, times=None):
+    """The whole path in the CPU oracle over the first n tokens; `times`, if
+    given, accumulates each op's wall seconds."""
     import numpy as np
 
     import oracle
     cu = np.asarray(cu_host)
     cu = np.append(cu[cu < n], n)
     res = {}
+    clock = [time.perf_counter()]
+
+    def lap(op):
+        t = time.perf_counter()
+        if times is not None:
+            times[op] = times.get(op, 0.0) + t - clock[0]
+        clock[0] = t
     res["y"], res["rstd"] = oracle.rmsnorm_fwd(cut["x"][:n], cut["w"], wl.eps)
+    lap("rmsnorm_fwd")
     r = oracle.rmsnorm_bwd(cut["dy"][:n], cut["x"][:n], cut["w"], wl.eps, scales=scales)
     res["dx"], res["dw"] = r[0], r[1]
     if scales:
         res["dx_s"] = r[2]
+    lap("rmsnorm_bwd")
     res["h"] = oracle.swiglu_fwd(cut["g"][:n], cut["u"][:n])
+    lap("swiglu_fwd")
     r = oracle.swiglu_bwd(cut["dh"][:n], cut["g"][:n], cut["u"][:n], scales=scales)
     res["dg"], res["du"] = r[0], r[1]
     if scales:
         res["dg_s"] = r[2]
+    lap("swiglu_bwd")
     r = oracle.qk_rope(cut["q"][:n], cut["k"][:n], cu, wl.theta, +1, scales=scales)
     res["q"], res["k"] = r[0], r[1]
     if scales:
         res["q_s"], res["k_s"] = r[2], r[3]
+    lap("qk_rope_fwd")
     r = oracle.qk_rope(cut["dq"][:n], cut["dk"][:n], cu, wl.theta, -1, scales=scales)
     res["dq"], res["dk"] = r[0], r[1]
     if scales:
         res["dq_s"], res["dk_s"] = r[2], r[3]
+    lap("qk_rope_bwd")
     return res
+
+
+def cpu_model() -> str:
+    """The host CPU's model name as lscpu reports it."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
 
 
 def f64_inputs(cut):
@@ -334,16 +361,27 @@ def cpu_leg(wl, batch, gpu_out, cut, seconds):
     # repeat the sample until about `seconds` of oracle work has run (the
     # sample is capped at the tokens copied to the host)
     passes = 0
+    per_op = {}
     t = time.perf_counter()
     while True:
-        res = oracle_step(wl, cut64, batch.cu_host, n)
+        res = oracle_step(wl, cut64, batch.cu_host, n, times=per_op)
         passes += 1
         el = time.perf_counter() - t
         if el >= seconds or passes >= 100000:
             break
     ib = W.ideal_bytes(wl)
-    sample_bytes = passes * sum(v * n / (wl.T_swiglu if "swiglu" in k else wl.T)
-                                for k, v in ib.items())
+
+    def tok_bytes(k, ntok):
+        return ib[k] * ntok / (wl.T_swiglu if "swiglu" in k else wl.T)
+    sample_bytes = passes * sum(tok_bytes(k, n) for k in ib)
+    # one pass on a single thread, over about a thread's share of the sample
+    cores = oracle.threads()
+    n1 = max(1, n // max(cores, 1))
+    prev = oracle.set_threads(1)
+    t1 = time.perf_counter()
+    oracle_step(wl, cut64, batch.cu_host, n1)
+    el1 = time.perf_counter() - t1
+    oracle.set_threads(prev)
     # parity of the GPU step on the same tokens (the CPU sample is a prefix)
     code = "f32" if wl.dtype == "f32" else "bf16"
     m = min(n, 256)
@@ -359,11 +397,15 @@ def cpu_leg(wl, batch, gpu_out, cut, seconds):
         worst = max(worst, assert_close(k, gpu_out[k][:m], ref[k], ref[k + "_s"], dtype=code))
     del res
     return {
-        "value": sample_bytes / el / 1e9, "unit": "GB/s", "cores": oracle.threads(),
+        "value": sample_bytes / el / 1e9, "unit": "GB/s", "cores": cores,
         "kind": "oracle", "tokens_per_s": passes * n / el, "seconds": round(el, 3),
         "sample": f"{passes} passes over the first {n} of {wl.T} tokens ({el:.1f} s), all six "
                   f"ops (oracle in double, OpenMP over rows), GB/s over the passes' "
                   f"algorithmic bytes",
+        "per_op_s": {k: round(v / passes, 6) for k, v in per_op.items()},
+        "one_thread": {"tokens": n1, "seconds": round(el1, 4),
+                       "GB_s": round(sum(tok_bytes(k, n1) for k in ib) / el1 / 1e9, 3)},
+        "nproc": os.cpu_count(), "cpu_model": cpu_model(),
     }, {"tokens_checked": m, "ops": 10, "max_err_over_bound": round(worst, 4)}
 
 

@@ -53,6 +53,8 @@ def _load():
         lib.oracle_rmsnorm_add_bwd.restype = None
         lib.oracle_threads.argtypes = []
         lib.oracle_threads.restype = ctypes.c_int
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -262,3 +264,9 @@ def positions(cu_seqlens, tok=None, n=None):
 def threads() -> int:
     """Threads the oracle's parallel loops run on."""
     return int(_load().oracle_threads())
+
+
+def set_threads(n: int) -> int:
+    """Runs the oracle's parallel loops on n threads from now on; returns the
+    previous count.  For timing only: no result depends on it."""
+    return int(_load().oracle_set_threads(int(n)))

@@ -51,6 +51,21 @@ ORACLE_API int oracle_threads(void)
 #endif
 }
 
+/* Runs the following OpenMP loops of this library on n threads (n >= 1;
+ * a no-op without OpenMP); returns the previous count.  Only the timing of
+ * the oracle uses it: the loops' results do not depend on the thread count. */
+ORACLE_API int oracle_set_threads(int n)
+{
+    const int prev = oracle_threads();
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+    return prev;
+}
+
 /* ---------------------------------------------------------------- RMSNorm */
 
 /* y[t,j] = x[t,j] * r[t] * w[j],  r[t] = 1 / sqrt(mean_j x[t,j]^2 + eps).

@@ -74,6 +74,8 @@ def code(dtype):
     (3, 8, 0),          # tiny rows
     (4099, 512, 0),     # rows of one warp, many rows per warp (pipelined kernels)
     (2053, 1024, 0),    # one-warp rows of four packets per lane (bf16)
+    (1027, 2048, 0),    # two-warp rows (bf16), ragged T
+    (5, 2048, 0),       # fewer rows than row groups
 ])
 def test_rmsnorm_shapes(dtype, T, H, skew):
     eps = 1e-6
@@ -97,6 +99,22 @@ def test_rmsnorm_shapes(dtype, T, H, skew):
     assert_close("rstd", rg.t, rr, dtype="f32")
     assert_close("dx", dxg.t, dxr, dxs, dtype=code(dtype))
     assert_close("dw", dwg.t, dwr, dws, dtype=code(dtype), kind="dw")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T,H", [(37, 896), (29, 900), (4099, 512), (2053, 1024), (1027, 2048),
+                                 (300, 5120), (5, 20000)])
+def test_rmsnorm_bwd_rstd_modes_agree(dtype, T, H):
+    # dx and dw are the same bits whether rstd is saved or recomputed: the
+    # recomputed rstd repeats the forward's sum, and the grid (so dw's
+    # summation order) does not depend on the mode
+    x, dy = randn((T, H), dtype, 31), randn((T, H), dtype, 32)
+    w = (1 + 0.1 * randn((H,), torch.float32, 33)).to(dtype)
+    _, rstd = ftk.rmsnorm_fwd(x, w, 1e-6)
+    dx1, dw1 = ftk.rmsnorm_bwd(dy, x, w, rstd, 1e-6)
+    dx2, dw2 = ftk.rmsnorm_bwd(dy, x, w, None, 1e-6)
+    torch.cuda.synchronize()
+    assert torch.equal(dx1, dx2) and torch.equal(dw1, dw2)
 
 
 def test_rmsnorm_strided_and_in_place():

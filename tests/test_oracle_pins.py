@@ -123,6 +123,21 @@ def test_rmsnorm_bwd_zero_upstream():
     assert not dx.any() and not dw.any()
 
 
+def test_oracle_results_do_not_depend_on_thread_count():
+    # the timing leg runs the oracle on one thread and on all of them
+    x, dy = RNG.standard_normal((300, 200)), RNG.standard_normal((300, 200))
+    w = 1 + 0.1 * RNG.standard_normal(200)
+    prev = oracle.set_threads(1)
+    try:
+        one = oracle.rmsnorm_bwd(dy, x, w, 1e-6)
+        oracle.set_threads(max(prev, 4))
+        many = oracle.rmsnorm_bwd(dy, x, w, 1e-6)
+    finally:
+        oracle.set_threads(prev)
+    assert oracle.threads() == prev
+    assert np.array_equal(one[0], many[0]) and np.array_equal(one[1], many[1])
+
+
 # ---------------------------------------------------------------- SwiGLU
 
 def test_swiglu_special_values():
