@@ -280,6 +280,13 @@ def sample_outputs(batch, n):
     return out
 
 
+def op_ms(op_events, flush_events):
+    """An op's device time: the median over rounds of its graph [L2 flush, op]
+    minus the same round's graph [L2 flush] (CUDA event pairs, in ms)."""
+    return statistics.median(a.elapsed_time(b) - fa.elapsed_time(fb)
+                             for (a, b), (fa, fb) in zip(op_events, flush_events))
+
+
 def oracle_step(wl, cut, cu_host, n, scales=False, times=None):
     """The whole path in the CPU oracle over the first n tokens; `times`, if
     given, accumulates each op's wall seconds."""
@@ -509,9 +516,7 @@ def run_ours(args):
     sampler.stop()
 
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    t_flush = sum(e[-1][0].elapsed_time(e[-1][1]) for e in evk) / Kk
-    per_op = [sum(e[j][0].elapsed_time(e[j][1]) for e in evk) / Kk - t_flush
-              for j in range(len(ops))]
+    per_op = [op_ms([e[j] for e in evk], [e[-1] for e in evk]) for j in range(len(ops))]
     wall_ms = whole0.elapsed_time(whole1)
 
     el_max, bytes_all = reduce_timing(step_ms * K / 1e3, step_bytes * K)
@@ -551,18 +556,22 @@ def run_ours(args):
                      "traffic": traffic, "algorithmic_bytes": ib[dname],
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
                      else "fallback 6.8 TB/s"},
-        "gpu_launches": LAUNCHES_PER_STEP * (K + Kk),
+        # this library's launches inside the timed region (the K steps), and
+        # over every leg of the run
+        "gpu_launches": LAUNCHES_PER_STEP * K,
+        "gpu_launches_all_legs": LAUNCHES_PER_STEP * (K + Kk),
         "timing": (f"step: {K} replays of a CUDA graph of the step's {LAUNCHES_PER_STEP} "
-                   f"launches, CUDA events around each replay; per kernel: {Kk} replays of a "
-                   "graph [L2 flush, op] minus a graph [L2 flush], CUDA events around each"),
+                   f"launches, CUDA events around each replay; per kernel: the median over {Kk} "
+                   "replays of a graph [L2 flush, op] minus the same round's graph [L2 flush], "
+                   "CUDA events around each"),
         "wall_ms_timed_region": round(wall_ms, 3),
     }
     if not args.no_ext:
         out["extensions"] = ext_leg(batch, flush, flush_graph, dev, Kk, hbm, src)
         if rank == 0 and not args.no_cce:
             out["cce"] = cce_leg(dev, flush, flush_graph, max(3, min(Kk, 20)))
-            out["gpu_launches"] += out["cce"].pop("launches")
-        out["gpu_launches"] += sum(EXT_OPS.values()) * Kk
+            out["gpu_launches_all_legs"] += out["cce"].pop("launches")
+        out["gpu_launches_all_legs"] += sum(EXT_OPS.values()) * Kk
     out["clocks"] = sampler.summary(t0, t1)
     out["device_status"] = ftk.device_status(clear=True)  # 0: no pipeline wait ran out
 
@@ -642,19 +651,19 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
             g.replay()
             b.record()
     torch.cuda.synchronize(dev)
-    t_flush = sum(a.elapsed_time(b) for a, b in ev["flush"]) / reps
     ib, toks = W.ideal_bytes(wl), W.tokens_per_call(wl)
     out = {}
     for n in graphs:
-        ms = sum(a.elapsed_time(b) for a, b in ev[n]) / reps - t_flush
+        ms = op_ms(ev[n], ev["flush"])
         gbs = ib[n] / (ms * 1e-3) / 1e9
         out[n] = {"us": round(ms * 1e3, 2), "GB_s": round(gbs, 1),
                   "frac_of_measured_hbm" if src == "measured" else "frac_of_fallback_hbm":
                       round(gbs / hbm, 4),
                   "tokens_per_s": round(toks[n] / (ms * 1e-3), 1), "ideal_bytes": ib[n],
                   "launches": EXT_OPS[n]}
-    out["timing"] = (f"{reps} replays of a graph [L2 flush, op] minus a graph [L2 flush], "
-                     "CUDA events around each; outside the step's timed region")
+    out["timing"] = (f"the median over {reps} replays of a graph [L2 flush, op] minus the same "
+                     "round's graph [L2 flush], CUDA events around each; outside the step's "
+                     "timed region")
     del h, y, rstd, dx, dw, res, dres, extra, qo, ko, rq, rk, nr_ws
     return out
 
@@ -702,7 +711,6 @@ def cce_leg(dev, flush, flush_graph, reps):
             gr.replay()
             b.record()
     torch.cuda.synchronize(dev)
-    t_flush = sum(a.elapsed_time(b) for a, b in ev["flush"]) / reps
     peak, psrc = tensor_peak()
     flops = {"cce_fwd": 2 * hw.T * hw.H * hw.V, "cce_bwd": 6 * hw.T * hw.H * hw.V}
     chunk = ftk.cce_bwd_chunk(hw.T, hw.H, hw.V)
@@ -712,7 +720,7 @@ def cce_leg(dev, flush, flush_graph, reps):
                         "ignored_share": hw.ignored, "bwd_chunk": chunk},
            "loss": round(float(loss.item()), 6)}
     for n in graphs:
-        ms = sum(a.elapsed_time(b) for a, b in ev[n]) / reps - t_flush
+        ms = op_ms(ev[n], ev["flush"])
         tf = flops[n] / (ms * 1e-3) / 1e12
         out[n] = {"ms": round(ms, 4), "TFLOP_s": round(tf, 1), "algorithmic_flops": flops[n],
                   "tokens_per_s": round(hw.T / (ms * 1e-3), 1),
@@ -720,8 +728,9 @@ def cce_leg(dev, flush, flush_graph, reps):
                                "unit": "TFLOP/s", "frac": round(tf / peak, 4),
                                "peak_source": f"{psrc} bf16 dense (burst)"}}
     out["launches"] = (launches["cce_fwd"] + launches["cce_bwd"]) * reps
-    out["timing"] = (f"{reps} replays of a graph [L2 flush, op] minus a graph [L2 flush], "
-                     "CUDA events around each; outside the step's timed region")
+    out["timing"] = (f"the median over {reps} replays of a graph [L2 flush, op] minus the same "
+                     "round's graph [L2 flush], CUDA events around each; outside the step's "
+                     "timed region")
     return out
 
 
