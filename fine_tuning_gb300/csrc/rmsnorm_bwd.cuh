@@ -70,12 +70,13 @@ __device__ __forceinline__ float dx_value(float a, float xf, float r, float wf, 
 // W warps at a time, rows row, row + (8 / W) P, ...; each lane copies its
 // packets of x and dy (and dh, and r when saved) of the group's next rows
 // (bwd_pipe_bufs - 1 of them) into its warp's shared-memory ring with
-// cp.async while it works on the current one.  Lane l of warp w in the group owns packets w 32 + l + k 32W
-// (the row plan's columns and summation order); with W = 2 the two warps'
-// sums meet in shared memory (slots double-buffered by row parity) behind a
-// named barrier of the pair and are added in the plan's order.  The CTA's
-// row groups combine their dw sums in a fixed order at the end, in the
-// ring's memory, into the CTA's partial row.
+// cp.async while it works on the current one.  Lane l of warp w in the
+// group owns packets w 32 + l + k 32W (the row plan's columns and summation
+// order); with W = 2 the two warps' sums meet in shared memory (slots
+// double-buffered by row parity) behind a named barrier of the pair and are
+// added in the plan's order.  The CTA's row groups combine their dw sums in
+// a fixed order at the end, in the ring's memory, into the CTA's partial
+// row.
 // Ring depth in rows: 3 for rows of one warp (few rows per warp, so the
 // loads of two rows ahead cover the ramp), 2 for two-warp rows (measured
 // faster there).
