@@ -121,8 +121,15 @@ rmsnorm_fwd_staged(const FwdParams<T, Idx> a, int S, uint32_t off_red, uint32_t 
                    uint32_t row_bytes, unsigned *status, long long wait_limit) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // [R][S]
-  float *red = reinterpret_cast<float *>(smem + off_red);  // [R][W]
+  float *red = reinterpret_cast<float *>(smem + off_red);  // [2][R][W], by row parity
   const int W = a.W, R = a.R;
+  // Multi-warp groups with three or more stages refill a row's stage at the
+  // next row's reduction barrier (by then the whole group is past the row),
+  // which saves a barrier per row; with two stages that would leave the
+  // next row half a row of lead, so they refill behind a second barrier at
+  // the end of the row.  (With the residual, whose stages are twice as
+  // large, the early refill measured slower: it keeps the second barrier.)
+  const bool early = !ADD && W > 1 && S > 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / W, wig = warp - grp * W;
   const int gi = wig * 32 + lane, G = W * 32;
@@ -184,10 +191,23 @@ rmsnorm_fwd_staged(const FwdParams<T, Idx> a, int S, uint32_t off_red, uint32_t 
     }
     ss = warp_sum(ss);
     if (W > 1) {
-      if (lane == 0) red[grp * W + wig] = ss;
+      // with the early refill the slots alternate by row parity: a warp one
+      // row ahead writes the other half, and none gets two rows ahead
+      // without passing this barrier again (otherwise the end-of-row
+      // barrier keeps the slots)
+      float *slot = red + ((early ? (it & 1) * R : 0) + grp) * W;
+      if (lane == 0) slot[wig] = ss;
       named_barrier(1 + grp, G);
       ss = 0.f;
-      for (int i = 0; i < W; ++i) ss += red[grp * W + i];
+      for (int i = 0; i < W; ++i) ss += slot[i];
+      if (early && leader && it > 0) {  // the previous row's stage is free
+        const Idx next = row + (Idx)(S - 1) * stride;
+        if (next < a.rows) {
+          fence_proxy_async_smem();
+          issue((it - 1) % S, next);
+          ++issued;
+        }
+      }
     }
     const float r = rsqrtf(fmaf(ss, a.inv_h, a.eps));
     if (a.rstd != nullptr && leader) a.rstd[row] = r;
@@ -204,17 +224,19 @@ rmsnorm_fwd_staged(const FwdParams<T, Idx> a, int S, uint32_t off_red, uint32_t 
         store_packet<T, N>(yr + (Idx)c * N, o);
       }
     }
-    // the whole group has read stage s (and the reduction slots): refill it
-    if (W > 1)
-      named_barrier(1 + grp, G);
-    else
-      __syncwarp();
-    if (leader) {
-      const Idx next = row + (Idx)S * stride;
-      if (next < a.rows) {
-        fence_proxy_async_smem();
-        issue(s, next);
-        ++issued;
+    if (!early) {
+      // the whole group has read stage s: refill it
+      if (W > 1)
+        named_barrier(1 + grp, G);
+      else
+        __syncwarp();
+      if (leader) {
+        const Idx next = row + (Idx)S * stride;
+        if (next < a.rows) {
+          fence_proxy_async_smem();
+          issue(s, next);
+          ++issued;
+        }
       }
     }
   }
