@@ -281,8 +281,9 @@ def sample_outputs(batch, n):
 
 
 def op_ms(op_events, flush_events):
-    """An op's device time: the median over rounds of its graph [L2 flush, op]
-    minus the same round's graph [L2 flush] (CUDA event pairs, in ms)."""
+    """An op's device time: the median over repetitions of its graph [L2
+    flush, op] minus the same repetition's graph [L2 flush] (CUDA event
+    pairs, in ms)."""
     return statistics.median(a.elapsed_time(b) - fa.elapsed_time(fb)
                              for (a, b), (fa, fb) in zip(op_events, flush_events))
 
@@ -562,7 +563,7 @@ def run_ours(args):
         "gpu_launches_all_legs": LAUNCHES_PER_STEP * (K + Kk),
         "timing": (f"step: {K} replays of a CUDA graph of the step's {LAUNCHES_PER_STEP} "
                    f"launches, CUDA events around each replay; per kernel: the median over {Kk} "
-                   "replays of a graph [L2 flush, op] minus the same round's graph [L2 flush], "
+                   "replays of a graph [L2 flush, op] minus the same repetition's graph [L2 flush], "
                    "CUDA events around each"),
         "wall_ms_timed_region": round(wall_ms, 3),
     }
@@ -662,7 +663,7 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
                   "tokens_per_s": round(toks[n] / (ms * 1e-3), 1), "ideal_bytes": ib[n],
                   "launches": EXT_OPS[n]}
     out["timing"] = (f"the median over {reps} replays of a graph [L2 flush, op] minus the same "
-                     "round's graph [L2 flush], CUDA events around each; outside the step's "
+                     "repetition's graph [L2 flush], CUDA events around each; outside the step's "
                      "timed region")
     del h, y, rstd, dx, dw, res, dres, extra, qo, ko, rq, rk, nr_ws
     return out
@@ -729,7 +730,7 @@ def cce_leg(dev, flush, flush_graph, reps):
                                "peak_source": f"{psrc} bf16 dense (burst)"}}
     out["launches"] = (launches["cce_fwd"] + launches["cce_bwd"]) * reps
     out["timing"] = (f"the median over {reps} replays of a graph [L2 flush, op] minus the same "
-                     "round's graph [L2 flush], CUDA events around each; outside the step's "
+                     "repetition's graph [L2 flush], CUDA events around each; outside the step's "
                      "timed region")
     return out
 
