@@ -9,7 +9,8 @@
 // Longest sequence first (equal lengths: lower index first); each goes to
 // the open bin with the least room that still holds it (equal room: lower
 // bin index), else to a new bin.  Open bins are kept in an ordered set keyed
-// by (room, bin), so the best fit is one lower_bound: O(n log n) in all.
+// by (room, bin), so the best fit is one lower_bound: O(n log n) in all (the
+// decreasing order is a counting sort for capacities up to 2^22).
 #include <algorithm>
 #include <climits>
 #include <new>
@@ -18,6 +19,11 @@
 #include <vector>
 
 #include "ftk.h"
+
+namespace {
+// The longest capacity sorted by counting (a table of capacity + 2 counts).
+constexpr int32_t kCountingSortMax = 1 << 22;
+}  // namespace
 
 extern "C" FTK_API ftk_status ftk_bfd_pack(const int32_t *lengths, int64_t n, int32_t capacity,
                                            int32_t *bin_of, int64_t *order, int64_t *bin_start,
@@ -28,29 +34,39 @@ extern "C" FTK_API ftk_status ftk_bfd_pack(const int32_t *lengths, int64_t n, in
   for (int64_t i = 0; i < n; ++i)
     if (lengths[i] < 0 || lengths[i] > capacity) return FTK_ERR_SHAPE;
   try {
+    // longest first, equal lengths in index order: a counting sort when the
+    // capacity (the largest length) is moderate, else a stable sort
     std::vector<int32_t> by_len(n);
-    for (int64_t i = 0; i < n; ++i) by_len[i] = (int32_t)i;
-    std::stable_sort(by_len.begin(), by_len.end(),
-                     [&](int32_t a, int32_t b) { return lengths[a] > lengths[b]; });
+    if (capacity <= kCountingSortMax) {
+      std::vector<int64_t> at((size_t)capacity + 2, 0);
+      for (int64_t i = 0; i < n; ++i) ++at[(size_t)(capacity - lengths[i]) + 1];
+      for (size_t v = 1; v < at.size(); ++v) at[v] += at[v - 1];
+      for (int64_t i = 0; i < n; ++i) by_len[at[(size_t)(capacity - lengths[i])]++] = (int32_t)i;
+    } else {
+      for (int64_t i = 0; i < n; ++i) by_len[i] = (int32_t)i;
+      std::stable_sort(by_len.begin(), by_len.end(),
+                       [&](int32_t a, int32_t b) { return lengths[a] > lengths[b]; });
+    }
     std::set<std::pair<int32_t, int32_t>> open;  // (room left, bin)
     std::vector<int64_t> count;
     int32_t bins = 0;
     for (int32_t i : by_len) {
       const int32_t len = lengths[i];
       auto it = open.lower_bound({len, INT32_MIN});
-      int32_t b, room;
       if (it == open.end()) {
-        b = bins++;
-        room = capacity - len;
-        count.push_back(0);
+        const int32_t b = bins++;
+        open.insert({capacity - len, b});
+        count.push_back(1);
+        bin_of[i] = b;
       } else {
-        b = it->second;
-        room = it->first - len;
-        open.erase(it);
+        // the bin's node is re-keyed in place (no allocation)
+        auto node = open.extract(it);
+        const int32_t b = node.value().second;
+        node.value().first -= len;
+        open.insert(std::move(node));
+        ++count[b];
+        bin_of[i] = b;
       }
-      open.insert({room, b});
-      bin_of[i] = b;
-      ++count[b];
     }
     // members of each bin, in the order they were placed
     bin_start[0] = 0;

@@ -43,6 +43,18 @@ def test_workload_length_mixes(ftk, name):
     check(ftk, lens.tolist(), wl.T)
 
 
+@pytest.mark.parametrize("cap", [(1 << 22) - 1, 1 << 22, (1 << 22) + 1, 50_000_000])
+def test_capacities_around_the_counting_sort_limit(ftk, cap):
+    # capacities up to 2^22 take the counting sort, larger ones a stable sort:
+    # the same packing either way
+    rng = np.random.default_rng(cap % 1000)
+    lens = rng.integers(0, cap + 1, size=300)
+    lens[::7] = lens[3]  # ties in length, ordered by index
+    lens[::11] = cap     # full bins
+    lens[::13] = 0
+    check(ftk, lens.tolist(), cap)
+
+
 def test_edges(ftk):
     check(ftk, [], 5)
     check(ftk, [5], 5)
