@@ -9,8 +9,10 @@
 // Longest sequence first (equal lengths: lower index first); each goes to
 // the open bin with the least room that still holds it (equal room: lower
 // bin index), else to a new bin.  Open bins are kept in an ordered set keyed
-// by (room, bin), so the best fit is one lower_bound: O(n log n) in all (the
-// decreasing order is a counting sort for capacities up to 2^22).
+// by (room, bin), so the best fit is one lower_bound: O(n log n) time and
+// O(n) memory in all.  The decreasing order is a counting sort (a table of
+// capacity + 2 counts) only where that table is small beside the input,
+// capacity <= 4 n + 1024; otherwise a stable comparison sort.
 #include <algorithm>
 #include <climits>
 #include <new>
@@ -21,8 +23,11 @@
 #include "ftk.h"
 
 namespace {
-// The longest capacity sorted by counting (a table of capacity + 2 counts).
-constexpr int32_t kCountingSortMax = 1 << 22;
+// Counting sort only while its table (capacity + 2 counts) is O(n): at most
+// 4 n + 1024 entries.
+bool counting_sort_pays(int64_t n, int32_t capacity) {
+  return (int64_t)capacity <= 4 * n + 1024;
+}
 }  // namespace
 
 extern "C" FTK_API ftk_status ftk_bfd_pack(const int32_t *lengths, int64_t n, int32_t capacity,
@@ -35,9 +40,9 @@ extern "C" FTK_API ftk_status ftk_bfd_pack(const int32_t *lengths, int64_t n, in
     if (lengths[i] < 0 || lengths[i] > capacity) return FTK_ERR_SHAPE;
   try {
     // longest first, equal lengths in index order: a counting sort when the
-    // capacity (the largest length) is moderate, else a stable sort
+    // capacity (the largest length) is small beside n, else a stable sort
     std::vector<int32_t> by_len(n);
-    if (capacity <= kCountingSortMax) {
+    if (counting_sort_pays(n, capacity)) {
       std::vector<int64_t> at((size_t)capacity + 2, 0);
       for (int64_t i = 0; i < n; ++i) ++at[(size_t)(capacity - lengths[i]) + 1];
       for (size_t v = 1; v < at.size(); ++v) at[v] += at[v - 1];

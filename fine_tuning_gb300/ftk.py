@@ -541,7 +541,15 @@ def bfd_pack(lengths, capacity: int):
     """Best-Fit-Decreasing packing (host).  Returns (bin_of, order, bin_start):
     numpy arrays; bin b holds sequences order[bin_start[b]:bin_start[b+1]]."""
     import numpy as np
-    lens = np.ascontiguousarray(np.asarray(lengths, dtype=np.int32))
+    raw = np.asarray(lengths)
+    if raw.size and not np.issubdtype(raw.dtype, np.integer):
+        raise ValueError("lengths must be integers")
+    if not 1 <= int(capacity) < 2**31:
+        raise ValueError("capacity must lie in [1, 2^31)")
+    if raw.size and (int(raw.min()) < 0 or int(raw.max()) > int(capacity)):
+        # checked before the int32 cast, so a wide length cannot wrap into range
+        raise ValueError("every length must lie in [0, capacity]")
+    lens = np.ascontiguousarray(raw.astype(np.int32))
     n = lens.size
     bin_of = np.empty(n, dtype=np.int32)
     order = np.empty(n, dtype=np.int64)

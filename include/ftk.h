@@ -411,7 +411,8 @@ FTK_API ftk_status ftk_cce_bwd(const void *h, int64_t ldh, const void *w, int64_
  * (room for the worst case of one bin per sequence), bin b holds
  * order[bin_start[b] .. bin_start[b+1]); *n_bins: the number of bins.
  * A length outside [0, capacity] gives FTK_ERR_SHAPE and writes nothing.
- * O(n log n) time, O(n) memory. */
+ * O(n log n) time, O(n) memory (the descending order is a counting sort
+ * only while capacity <= 4 n + 1024). */
 FTK_API ftk_status ftk_bfd_pack(const int32_t *lengths, int64_t n, int32_t capacity,
                                 int32_t *bin_of, int64_t *order, int64_t *bin_start,
                                 int64_t *n_bins);

@@ -43,16 +43,28 @@ def test_workload_length_mixes(ftk, name):
     check(ftk, lens.tolist(), wl.T)
 
 
-@pytest.mark.parametrize("cap", [(1 << 22) - 1, 1 << 22, (1 << 22) + 1, 50_000_000])
-def test_capacities_around_the_counting_sort_limit(ftk, cap):
-    # capacities up to 2^22 take the counting sort, larger ones a stable sort:
-    # the same packing either way
+@pytest.mark.parametrize("n,cap", [(300, 2223), (300, 2224), (300, 2225), (300, 50_000_000),
+                                   (5000, 20_000), (0, 1 << 30)])
+def test_capacities_around_the_counting_sort_limit(ftk, n, cap):
+    # capacities up to 4 n + 1024 take the counting sort, larger ones a
+    # stable sort: the same packing either way
     rng = np.random.default_rng(cap % 1000)
-    lens = rng.integers(0, cap + 1, size=300)
-    lens[::7] = lens[3]  # ties in length, ordered by index
-    lens[::11] = cap     # full bins
-    lens[::13] = 0
+    lens = rng.integers(0, cap + 1, size=n)
+    if n:
+        lens[::7] = lens[3]  # ties in length, ordered by index
+        lens[::11] = cap     # full bins
+        lens[::13] = 0
     check(ftk, lens.tolist(), cap)
+
+
+def test_wide_lengths_are_rejected_not_wrapped(ftk):
+    # 2^32 + 3 would wrap to 3 in an int32 cast: the binding refuses it
+    with pytest.raises(ValueError):
+        ftk.bfd_pack(np.array([5, (1 << 32) + 3], dtype=np.int64), 10)
+    with pytest.raises(ValueError):
+        ftk.bfd_pack(np.array([-1], dtype=np.int64), 10)
+    with pytest.raises(ValueError):
+        ftk.bfd_pack([1, 2], 1 << 31)
 
 
 def test_edges(ftk):
