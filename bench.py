@@ -13,6 +13,12 @@ sample of the workload (which also re-checks parity in the same run).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the CPU oracle arm
 
+The default workload is the largest single-GPU one: Qwen3-32B layer shapes
+on one 524,288-token sequence.  The smaller workloads are timed in the same
+run, with the same per-kernel method, in a compact `per_workload` block.
+`--tokens N` cuts a workload to its first N tokens (a slice with the same
+row shapes, for profiler captures that must stay small).
+
 Under torchrun each rank runs its own batch (weak scaling, no collective on
 the data path); rank 0 prints one JSON line.
 """
@@ -36,6 +42,7 @@ METRIC = "achieved HBM GB/s (% of GB300 peak) and tokens/s per fused fwd+bwd ker
 OPS = ("rmsnorm_fwd", "swiglu_fwd", "qk_rope_fwd", "qk_rope_bwd", "swiglu_bwd", "rmsnorm_bwd")
 LAUNCHES_PER_STEP = 7  # rmsnorm_bwd is two kernels (rows + fixed-order dw reduction)
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # GB300's HBM3e spec figure (a second column beside the measured copy)
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 
@@ -43,10 +50,16 @@ L2_FLUSH_BYTES = 256 << 20
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--workload", default="qwen2.5-0.5b")
+    p.add_argument("--workload", default="qwen3-32b-524k")
+    p.add_argument("--tokens", type=int, default=0,
+                   help="cut the workload to its first N tokens (0: the whole batch)")
+    p.add_argument("--per-workload", default="qwen2.5-0.5b,llama-3.2-1b,qwen3-8b",
+                   help="comma-separated workloads also timed per kernel ('none': skip)")
+    p.add_argument("--kernel-reps", type=int, default=0,
+                   help="repetitions of each one-op graph (0: min(steps, 300))")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-ext", action="store_true", help="skip timing the widened ops")
@@ -142,7 +155,7 @@ def ncu_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (100 ms) of SM clock and throttle reasons."""
 
     FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -158,7 +171,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return self
@@ -265,19 +278,96 @@ class Batch:
     OUT = ("y", "rstd", "dx", "dw", "h", "dg", "du")
 
 
-def sample_tokens(batch, n):
-    """CPU copies of the first n tokens of every input (the oracle sample)."""
+def select_workload(name: str, tokens: int = 0):
+    """The named workload, or (tokens > 0) a slice of it: its first `tokens`
+    tokens with the same row shapes (sequences cut at the slice's end)."""
+    import dataclasses
+
+    from fine_tuning_gb300 import workloads as W
+    wl = W.WORKLOADS[name]
+    if not tokens or tokens >= wl.T:
+        return wl
+    cut, total = [], 0
+    for n in W.draw_lengths(wl).tolist():
+        take = min(int(n), tokens - total)
+        if take <= 0:
+            break
+        cut.append(take)
+        total += take
+    return dataclasses.replace(wl, name=f"{wl.name}[:{tokens}]", T=tokens,
+                               T_swiglu=min(wl.T_swiglu, tokens), lengths=tuple(cut))
+
+
+def parity_rows(wl, cu_host, n_edge=64, n_mid=64, n_bounds=16, seed=99):
+    """Token rows whose outputs the oracle recomputes in the bench run: the
+    first and last n_edge tokens, n_mid drawn in between, and the tokens on
+    both sides of the first n_bounds sequence boundaries; the same rule over
+    the SwiGLU tokens.  Spans the whole batch at any size."""
+    import numpy as np
+
+    def pick(T, extra=()):
+        if T <= 2 * n_edge + n_mid:
+            return np.arange(T)
+        rng = np.random.default_rng(seed)
+        mid = rng.choice(np.arange(n_edge, T - n_edge), n_mid, replace=False)
+        rows = np.concatenate([np.arange(n_edge), mid, np.arange(T - n_edge, T),
+                               np.asarray(list(extra), dtype=np.int64)])
+        return np.unique(rows[(rows >= 0) & (rows < T)])
+    starts = [int(c) for c in cu_host[1:-1][:n_bounds]]
+    return pick(wl.T, starts + [c - 1 for c in starts]), pick(wl.T_swiglu)
+
+
+def gather_inputs(batch, rows, srows):
+    """CPU copies of the inputs at the parity rows (taken before the in-place
+    RoPE runs)."""
+    import torch
     i = batch.inputs
-    cut = {k: i[k][:n].cpu() for k in ("x", "dy", "g", "u", "dh", "q", "k", "dq", "dk")}
-    cut["w"] = i["w"].cpu()
-    return cut
-
-
-def sample_outputs(batch, n):
-    o, i = batch.outputs, batch.inputs
-    out = {k: o[k][:n].cpu() for k in ("y", "rstd", "dx", "h", "dg", "du")}
-    out.update({k: i[k][:n].cpu() for k in ("q", "k", "dq", "dk")})
+    dev = i["x"].device
+    ri, si = torch.as_tensor(rows, device=dev), torch.as_tensor(srows, device=dev)
+    out = {k: i[k][ri].cpu() for k in ("x", "dy", "q", "k", "dq", "dk")}
+    out.update({k: i[k][si].cpu() for k in ("g", "u", "dh")})
+    out["w"] = i["w"].cpu()
     return out
+
+
+def gather_outputs(batch, rows, srows):
+    import torch
+    o, i = batch.outputs, batch.inputs
+    dev = i["x"].device
+    ri, si = torch.as_tensor(rows, device=dev), torch.as_tensor(srows, device=dev)
+    out = {k: o[k][ri].cpu() for k in ("y", "rstd", "dx")}
+    out.update({k: o[k][si].cpu() for k in ("h", "dg", "du")})
+    out.update({k: i[k][ri].cpu() for k in ("q", "k", "dq", "dk")})
+    return out
+
+
+def check_parity(wl, cu_host, rows, srows, inp, got):
+    """The oracle on the parity rows against the GPU step's outputs there;
+    raises on any element out of tolerance, else returns the worst
+    error / bound."""
+    import oracle
+    from oracle.tolerance import assert_close
+    code = "f32" if wl.dtype == "f32" else "bf16"
+    yr, rr = oracle.rmsnorm_fwd(inp["x"], inp["w"], wl.eps)
+    dxr, _, dxs, _ = oracle.rmsnorm_bwd(inp["dy"], inp["x"], inp["w"], wl.eps, scales=True)
+    hr = oracle.swiglu_fwd(inp["g"], inp["u"])
+    dgr, dur, dgs = oracle.swiglu_bwd(inp["dh"], inp["g"], inp["u"], scales=True)
+    qr, kr, qs, ks = oracle.qk_rope(inp["q"], inp["k"], cu_host, wl.theta, +1, tok=rows,
+                                    scales=True)
+    dqr, dkr, dqs, dks = oracle.qk_rope(inp["dq"], inp["dk"], cu_host, wl.theta, -1, tok=rows,
+                                        scales=True)
+    worst = 0.0
+    for name, ref, sc, kind in (("y", yr, None, code), ("rstd", rr, None, "f32"),
+                                ("dx", dxr, dxs, code), ("h", hr, None, code),
+                                ("dg", dgr, dgs, code), ("du", dur, None, code),
+                                ("q", qr, qs, code), ("k", kr, ks, code),
+                                ("dq", dqr, dqs, code), ("dk", dkr, dks, code)):
+        worst = max(worst, assert_close(name, got[name], ref, sc, dtype=kind))
+    return {"tokens_checked": int(len(rows)), "swiglu_tokens_checked": int(len(srows)),
+            "outputs": 10, "max_err_over_bound": round(worst, 4),
+            "rows": "first and last 64 tokens, 64 drawn in between, both sides of the first "
+                    "16 sequence boundaries (dw, a sum over every row, is checked in full by "
+                    "the GPU tests)"}
 
 
 def op_ms(op_events, flush_events):
@@ -358,21 +448,28 @@ def calibrate_tokens(wl, cut64, cu_host, seconds, cap):
     return max(1, min(cap, int(seconds / per_tok)))
 
 
-def cpu_leg(wl, batch, gpu_out, cut, seconds):
-    """Oracle on the host cores over a bounded sample; also the parity gate."""
+def head_tokens(batch, n):
+    """CPU copies of the first n tokens of every input (the oracle's timing
+    sample)."""
+    i = batch.inputs
+    cut = {k: i[k][:n].cpu() for k in ("x", "dy", "g", "u", "dh", "q", "k", "dq", "dk")}
+    cut["w"] = i["w"].cpu()
+    return cut
+
+
+def cpu_leg(wl, cu_host, cut, seconds):
+    """The oracle as it stands on the host cores over a bounded sample of the
+    workload: repeated passes over its first tokens for about `seconds`."""
     import oracle
     from fine_tuning_gb300 import workloads as W
-    from oracle.tolerance import assert_close
     cap = cut["x"].shape[0]
     cut64 = f64_inputs(cut)
-    n = calibrate_tokens(wl, cut64, batch.cu_host, seconds, cap)
-    # repeat the sample until about `seconds` of oracle work has run (the
-    # sample is capped at the tokens copied to the host)
+    n = calibrate_tokens(wl, cut64, cu_host, seconds, cap)
     passes = 0
     per_op = {}
     t = time.perf_counter()
     while True:
-        res = oracle_step(wl, cut64, batch.cu_host, n, times=per_op)
+        oracle_step(wl, cut64, cu_host, n, times=per_op)
         passes += 1
         el = time.perf_counter() - t
         if el >= seconds or passes >= 100000:
@@ -381,29 +478,15 @@ def cpu_leg(wl, batch, gpu_out, cut, seconds):
 
     def tok_bytes(k, ntok):
         return ib[k] * ntok / (wl.T_swiglu if "swiglu" in k else wl.T)
-    sample_bytes = passes * sum(tok_bytes(k, n) for k in ib)
+    sample_bytes = passes * sum(tok_bytes(k, n) for k in ib if k in OPS)
     # one pass on a single thread, over about a thread's share of the sample
     cores = oracle.threads()
     n1 = max(1, n // max(cores, 1))
     prev = oracle.set_threads(1)
     t1 = time.perf_counter()
-    oracle_step(wl, cut64, batch.cu_host, n1)
+    oracle_step(wl, cut64, cu_host, n1)
     el1 = time.perf_counter() - t1
     oracle.set_threads(prev)
-    # parity of the GPU step on the same tokens (the CPU sample is a prefix)
-    code = "f32" if wl.dtype == "f32" else "bf16"
-    m = min(n, 256)
-    ref = oracle_step(wl, cut64, batch.cu_host, m, scales=True)
-    worst = 0.0
-    worst = max(worst, assert_close("y", gpu_out["y"][:m], ref["y"], dtype=code))
-    worst = max(worst, assert_close("rstd", gpu_out["rstd"][:m], ref["rstd"], dtype="f32"))
-    worst = max(worst, assert_close("dx", gpu_out["dx"][:m], ref["dx"], ref["dx_s"], dtype=code))
-    worst = max(worst, assert_close("h", gpu_out["h"][:m], ref["h"], dtype=code))
-    worst = max(worst, assert_close("dg", gpu_out["dg"][:m], ref["dg"], ref["dg_s"], dtype=code))
-    worst = max(worst, assert_close("du", gpu_out["du"][:m], ref["du"], dtype=code))
-    for k in ("q", "k", "dq", "dk"):
-        worst = max(worst, assert_close(k, gpu_out[k][:m], ref[k], ref[k + "_s"], dtype=code))
-    del res
     return {
         "value": sample_bytes / el / 1e9, "unit": "GB/s", "cores": cores,
         "kind": "oracle", "tokens_per_s": passes * n / el, "seconds": round(el, 3),
@@ -412,12 +495,128 @@ def cpu_leg(wl, batch, gpu_out, cut, seconds):
                   f"algorithmic bytes",
         "per_op_s": {k: round(v / passes, 6) for k, v in per_op.items()},
         "one_thread": {"tokens": n1, "seconds": round(el1, 4),
-                       "GB_s": round(sum(tok_bytes(k, n1) for k in ib) / el1 / 1e9, 3)},
+                       "GB_s": round(sum(tok_bytes(k, n1) for k in ib if k in OPS) / el1 / 1e9,
+                                     3)},
         "nproc": os.cpu_count(), "cpu_model": cpu_model(),
-    }, {"tokens_checked": m, "ops": 10, "max_err_over_bound": round(worst, 4)}
+    }
 
 
 # -------------------------------------------------------------- our arm
+
+def workload_config(wl, B, world):
+    """The `config` object of the JSON line (both arms print the same)."""
+    return {"workload": wl.name, "T": wl.T, "B": int(B), "H": wl.H, "I": wl.I,
+            "T_swiglu": wl.T_swiglu, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+            "theta": wl.theta, "eps": wl.eps,
+            "parallelism": f"replicas x{world} (one batch per GPU, no collective)",
+            "l2": "flushed before every step (256 MiB write, outside the step events); "
+                  "the inputs are also larger than L2",
+            "step": list(OPS)}
+
+
+def kernel_entry(name, ms, ib, toks, hbm, src):
+    gbs = ib / (ms * 1e-3) / 1e9
+    return {"us": round(ms * 1e3, 2), "GB_s": round(gbs, 1),
+            "frac_of_measured_hbm" if src == "measured" else "frac_of_fallback_hbm":
+                round(gbs / hbm, 4),
+            "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+            "tokens_per_s": round(toks / (ms * 1e-3), 1), "ideal_bytes": ib}
+
+
+def time_batch(batch, flush, K, Kk, dev, world=1):
+    """The step as one CUDA graph replayed K times (CUDA events around each
+    replay), then each op as a graph [L2 flush, op] beside a graph [L2
+    flush], Kk repetitions.  Returns (step ms per replay, per-op ms,
+    (t0, t1) of the step region, (t1, t2) of the per-kernel region)."""
+    import torch
+    import torch.distributed as dist
+    ops = batch.ops()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for op in ops:
+            op()
+    op_graphs = []
+    for op in ops:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            flush.fill_(3)
+            op()
+        op_graphs.append(g)
+    flush_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(flush_graph):
+        flush.fill_(3)
+    graph.replay()
+    for g in op_graphs + [flush_graph]:
+        g.replay()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    evk = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(len(ops) + 1)] for _ in range(Kk)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record()
+        graph.replay()
+        ev[i][1].record()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    for i in range(Kk):
+        for (a, b), g in zip(evk[i], op_graphs + [flush_graph]):
+            a.record()
+            g.replay()
+            b.record()
+    torch.cuda.synchronize(dev)
+    t2 = time.time()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    per_op = [op_ms([e[j] for e in evk], [e[-1] for e in evk]) for j in range(len(ops))]
+    return step_ms, per_op, (t0, t1), (t1, t2), flush_graph
+
+
+def per_workload_leg(names, flush, K, Kk, dev, hbm, src, sampler):
+    """The smaller workloads, each timed like the main one (step graph and
+    one-op graphs) after its own sampled parity check, in the same run."""
+    import torch
+
+    from fine_tuning_gb300 import workloads as W
+    out = {}
+    for name in names:
+        wl = W.WORKLOADS[name]
+        b = Batch(wl, dev)
+        rows, srows = parity_rows(wl, b.cu_host)
+        inp = gather_inputs(b, rows, srows)
+        for op in b.ops():
+            op()
+        torch.cuda.synchronize(dev)
+        par = check_parity(wl, b.cu_host, rows, srows, inp, gather_outputs(b, rows, srows))
+        for _ in range(3):
+            flush.fill_(1)
+            for op in b.ops():
+                op()
+        step_ms, per_op, _, (k0, k1), _ = time_batch(b, flush, K, Kk, dev)
+        ib, toks = W.ideal_bytes(wl), W.tokens_per_call(wl)
+        step_bytes = sum(ib[k] for k in OPS)
+        ms = sum(step_ms) / len(step_ms)
+        kern = {n: kernel_entry(n, per_op[j], ib[n], toks[n], hbm, src)
+                for j, n in enumerate(OPS)}
+        dom = max(range(len(OPS)), key=lambda j: per_op[j])
+        out[name] = {
+            "T": wl.T, "B": int(len(b.cu_host) - 1), "H": wl.H, "I": wl.I, "Hq": wl.Hq,
+            "Hkv": wl.Hkv, "D": wl.D, "step_ms": round(ms, 4),
+            "step_GB_s": round(step_bytes / (ms * 1e-3) / 1e9, 1),
+            "step_frac_of_hbm": round(step_bytes / (ms * 1e-3) / 1e9 / hbm, 4),
+            "tokens_per_s": round(wl.T / (ms * 1e-3), 1), "kernels": kern,
+            "dominant": {"kernel": OPS[dom], "traffic": ncu_traffic(OPS[dom], wl.name)},
+            "parity": par, "clocks_kernel_leg": sampler.summary(k0, k1)}
+        del b
+        torch.cuda.empty_cache()
+    return out
+
 
 def run_ours(args):
     import torch
@@ -433,18 +632,24 @@ def run_ours(args):
     dev = torch.device("cuda", local_rank)
     build.build()
     ftk.library()
-    wl = W.WORKLOADS[args.workload]
+    wl = select_workload(args.workload, args.tokens)
     batch = Batch(wl, dev, seed_offset=rank)
     ops = batch.ops()
     ib = W.ideal_bytes(wl)
     step_bytes = sum(ib[k] for k in OPS)
 
     do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
-    cut = sample_tokens(batch, min(wl.T, 8192)) if do_cpu else None
+    cut = head_tokens(batch, min(wl.T, 8192)) if do_cpu else None
+    # parity of the step on rows spanning the whole batch, before any timing:
+    # no number is printed unless it holds
+    rows, srows = parity_rows(wl, batch.cu_host)
+    inp = gather_inputs(batch, rows, srows)
     for op in ops:  # the parity step, on the untouched inputs
         op()
     torch.cuda.synchronize(dev)
-    gpu_out = sample_outputs(batch, min(wl.T, 256)) if do_cpu else None
+    parity = check_parity(wl, batch.cu_host, rows, srows, inp,
+                          gather_outputs(batch, rows, srows))
+    del inp
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(max(args.warmup, 0)):
@@ -453,37 +658,8 @@ def run_ours(args):
             op()
     torch.cuda.synchronize(dev)
 
-    # The step as one CUDA graph (its 7 launches replayed without host
-    # overhead, as a training loop would run it).
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for op in ops:
-            op()
-    # per kernel: a graph [L2 flush, op] and a graph [L2 flush]; the op's
-    # time is the difference of their replay times, so the graph launch
-    # latency cancels while the flush-to-op gap of a real stream stays in
-    op_graphs = []
-    for op in ops:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            flush.fill_(3)
-            op()
-        op_graphs.append(g)
-    flush_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(flush_graph):
-        flush.fill_(3)
-    graph.replay()
-    for g in op_graphs + [flush_graph]:
-        g.replay()
-    torch.cuda.synchronize(dev)
-
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
-    Kk = max(1, min(K, 300))
-    evk = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(len(ops) + 1)] for _ in range(Kk)]
-    whole0, whole1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    Kk = args.kernel_reps if args.kernel_reps > 0 else max(1, min(K, 300))
     uuid = ""
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -492,48 +668,15 @@ def run_ours(args):
         pass
     sampler = ClockSampler(uuid).start()
     time.sleep(0.6)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    t0 = time.time()
-    whole0.record()
-    for i in range(K):
-        flush.fill_(i & 0xFF)
-        ev[i][0].record()
-        graph.replay()
-        ev[i][1].record()
-    whole1.record()
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    t1 = time.time()
-    for i in range(Kk):
-        for (a, b), g in zip(evk[i], op_graphs + [flush_graph]):
-            a.record()
-            g.replay()
-            b.record()
-    torch.cuda.synchronize(dev)
-    time.sleep(0.3)
-    sampler.stop()
-
-    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    per_op = [op_ms([e[j] for e in evk], [e[-1] for e in evk]) for j in range(len(ops))]
-    wall_ms = whole0.elapsed_time(whole1)
-
-    el_max, bytes_all = reduce_timing(step_ms * K / 1e3, step_bytes * K)
+    step_ms, per_op, (t0, t1), (k0, k1), flush_graph = time_batch(batch, flush, K, Kk, dev,
+                                                                  world)
+    el_max, bytes_all = reduce_timing(sum(step_ms) / 1e3, step_bytes * K)
     _, tok_all = reduce_timing(0.0, float(wl.T) * K)
     value = bytes_all / el_max / 1e9
     hbm, src = peaks()
-    kernels = {}
-    for j, name in enumerate(OPS):
-        gbs = ib[name] / (per_op[j] * 1e-3) / 1e9
-        toks = W.tokens_per_call(wl)[name]
-        kernels[name] = {"us": round(per_op[j] * 1e3, 2), "GB_s": round(gbs, 1),
-                         "frac_of_measured_hbm" if src == "measured" else "frac_of_fallback_hbm":
-                             round(gbs / hbm, 4),
-                         "tokens_per_s": round(toks / (per_op[j] * 1e-3), 1),
-                         "ideal_bytes": ib[name]}
-    dom = max(range(len(ops)), key=lambda j: per_op[j])
+    toks = W.tokens_per_call(wl)
+    kernels = {n: kernel_entry(n, per_op[j], ib[n], toks[n], hbm, src) for j, n in enumerate(OPS)}
+    dom = max(range(len(OPS)), key=lambda j: per_op[j])
     dname = OPS[dom]
     achieved = ib[dname] / (per_op[dom] * 1e-3) / 1e9
     traffic = ncu_traffic(dname, wl.name)
@@ -543,20 +686,18 @@ def run_ours(args):
         "steps": K, "warmup": args.warmup, "ms_per_step": round(el_max * 1e3 / K, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded packed batch; no dataset, no weights)",
-        "config": {"workload": wl.name, "T": wl.T, "B": int(len(batch.cu_host) - 1),
-                   "H": wl.H, "I": wl.I, "T_swiglu": wl.T_swiglu, "Hq": wl.Hq, "Hkv": wl.Hkv,
-                   "D": wl.D, "theta": wl.theta, "eps": wl.eps,
-                   "parallelism": f"replicas x{world} (one batch per GPU, no collective)",
-                   "l2": "flushed before every step (256 MiB write, outside the step events)",
-                   "step": list(OPS)},
+        "config": workload_config(wl, len(batch.cu_host) - 1, world),
         "tokens_per_s": round(tok_all / el_max, 1),
         "frac_of_hbm": round(value / hbm, 4), "hbm_peak_GB_s": hbm, "hbm_peak_source": src,
+        "frac_of_nominal_8tbs": round(value / NOMINAL_HBM_GBS, 4),
+        "parity": parity,
         "kernels": kernels,
         "roofline": {"kernel": dname, "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "traffic": traffic, "algorithmic_bytes": ib[dname],
-                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
-                     else "fallback 6.8 TB/s"},
+                     "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+                     if src == "measured" else "fallback 6.8 TB/s"},
         # this library's launches inside the timed region (the K steps), and
         # over every leg of the run
         "gpu_launches": LAUNCHES_PER_STEP * K,
@@ -565,21 +706,35 @@ def run_ours(args):
                    f"launches, CUDA events around each replay; per kernel: the median over {Kk} "
                    "replays of a graph [L2 flush, op] minus the same repetition's graph [L2 flush], "
                    "CUDA events around each"),
-        "wall_ms_timed_region": round(wall_ms, 3),
+        "wall_ms_timed_region": round((t1 - t0) * 1e3, 3),
     }
-    if not args.no_ext:
-        out["extensions"] = ext_leg(batch, flush, flush_graph, dev, Kk, hbm, src)
-        if rank == 0 and not args.no_cce:
-            out["cce"] = cce_leg(dev, flush, flush_graph, max(3, min(Kk, 20)))
-            out["gpu_launches_all_legs"] += out["cce"].pop("launches")
-        out["gpu_launches_all_legs"] += sum(EXT_OPS.values()) * Kk
     out["clocks"] = sampler.summary(t0, t1)
+    out["clocks_kernel_leg"] = sampler.summary(k0, k1)
+    if not args.no_ext:
+        e0 = time.time()
+        out["extensions"] = ext_leg(batch, flush, flush_graph, dev, Kk, hbm, src)
+        out["extensions"]["clocks"] = sampler.summary(e0, time.time())
+        out["gpu_launches_all_legs"] += sum(EXT_OPS.values()) * Kk
+    torch.cuda.empty_cache()
+    if rank == 0:
+        names = [n for n in args.per_workload.split(",") if n and n != "none" and n != wl.name]
+        if names:
+            out["per_workload"] = per_workload_leg(names, flush, K, Kk, dev, hbm, src, sampler)
+            out["gpu_launches_all_legs"] += len(names) * LAUNCHES_PER_STEP * (K + Kk)
+        if not args.no_ext and not args.no_cce:
+            c0 = time.time()
+            out["cce"] = cce_leg(dev, flush, flush_graph, max(3, min(Kk, 20)))
+            out["cce"]["clocks"] = sampler.summary(c0, time.time())
+            out["gpu_launches_all_legs"] += out["cce"].pop("launches")
+    sampler.stop()
     out["device_status"] = ftk.device_status(clear=True)  # 0: no pipeline wait ran out
+    if out["device_status"] != 0:
+        raise RuntimeError(f"a bounded pipeline wait ran out (status {out['device_status']})")
 
     if not args.no_e2e:
         out["e2e"] = e2e_leg(batch, ops, dev, args.e2e_steps, step_bytes)
     if do_cpu:
-        out["cpu_baseline"], out["parity"] = cpu_leg(wl, batch, gpu_out, cut, args.cpu_seconds)
+        out["cpu_baseline"] = cpu_leg(wl, batch.cu_host, cut, args.cpu_seconds)
         out["packing"] = packing_leg(wl)
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -655,13 +810,8 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
     ib, toks = W.ideal_bytes(wl), W.tokens_per_call(wl)
     out = {}
     for n in graphs:
-        ms = op_ms(ev[n], ev["flush"])
-        gbs = ib[n] / (ms * 1e-3) / 1e9
-        out[n] = {"us": round(ms * 1e3, 2), "GB_s": round(gbs, 1),
-                  "frac_of_measured_hbm" if src == "measured" else "frac_of_fallback_hbm":
-                      round(gbs / hbm, 4),
-                  "tokens_per_s": round(toks[n] / (ms * 1e-3), 1), "ideal_bytes": ib[n],
-                  "launches": EXT_OPS[n]}
+        out[n] = kernel_entry(n, op_ms(ev[n], ev["flush"]), ib[n], toks[n], hbm, src)
+        out[n]["launches"] = EXT_OPS[n]
     out["timing"] = (f"the median over {reps} replays of a graph [L2 flush, op] minus the same "
                      "repetition's graph [L2 flush], CUDA events around each; outside the step's "
                      "timed region")
@@ -735,9 +885,38 @@ def cce_leg(dev, flush, flush_graph, reps):
     return out
 
 
+class HostBuffers:
+    """Page-locked host tensors of exactly the requested sizes: plain host
+    allocations registered with cudaHostRegister (torch's pinned allocator
+    rounds each allocation up to a power of two, which at the 524k-token
+    shapes would cost tens of GB of host memory).  Falls back to torch's
+    pinned allocator where the runtime call is unavailable."""
+
+    def __init__(self):
+        self.registered = []
+
+    def empty(self, shape, dtype):
+        import torch
+        t = torch.empty(shape, dtype=dtype)
+        rt = getattr(torch.cuda, "cudart", None)
+        if rt is not None and t.numel():
+            t.zero_()  # fault the pages in (OpenMP threads) before locking them
+            err = rt().cudaHostRegister(t.data_ptr(), t.numel() * t.element_size(), 0)
+            if int(err) == 0:
+                self.registered.append(t)
+                return t
+        return t.pin_memory()
+
+    def release(self):
+        import torch
+        for t in self.registered:
+            torch.cuda.cudart().cudaHostUnregister(t.data_ptr())
+        self.registered = []
+
+
 def e2e_leg(batch, ops, dev, steps, step_bytes):
     """The step through the public API with host buffers: every step copies
-    all of its inputs in from pinned host memory and all of its outputs
+    all of its inputs in from page-locked host memory and all of its outputs
     back.  As a user would run consecutive steps, three streams overlap
     step k+1's copy-in, step k's kernels and step k-1's copy-out, with two
     device-side buffer sets; events order every reuse of a buffer."""
@@ -745,11 +924,16 @@ def e2e_leg(batch, ops, dev, steps, step_bytes):
     wl = batch.wl
     sets = [batch, Batch(wl, dev)]
     set_ops = [ops, sets[1].ops()]
-    host_in = {k: batch.inputs[k].cpu().pin_memory() for k in Batch.IN}
+    hb = HostBuffers()
 
     def outs(b):
         return {**b.outputs, **{k: b.inputs[k] for k in Batch.OUT_FROM_INPUTS}}
-    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs(batch).items()}
+    host_in = {}
+    for k in Batch.IN:
+        v = batch.inputs[k]
+        host_in[k] = hb.empty(v.shape, v.dtype)
+        host_in[k].copy_(v)
+    host_out = {k: hb.empty(v.shape, v.dtype) for k, v in outs(batch).items()}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
     s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
@@ -795,17 +979,35 @@ def e2e_leg(batch, ops, dev, steps, step_bytes):
     z.record(last)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(z) / steps
-    del sets[1]
+    del sets[1], set_ops[1]
+    hb.release()
+    del host_in, host_out
     el_max, bytes_all = reduce_timing(ms * steps / 1e3, step_bytes * steps)
     return {"value": round(bytes_all / el_max / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(el_max * 1e3 / steps, 3), "steps": steps,
+            "tokens_per_s": round(wl.T * steps / el_max, 1),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "overlap": "3 streams: copy-in of step k+1, kernels of step k, copy-out of step k-1"}
+            "copy_GB_s": round((h2d + d2h) / (el_max / steps) / 1e9, 1),
+            "overlap": "3 streams: copy-in of step k+1, kernels of step k, copy-out of step k-1; "
+                       "two device buffer sets; host buffers page-locked at exact size"}
 
 
 # ------------------------------------------------------ packing (host)
 
 def packing_leg(wl, n_seq=200_000, batch=8):
+    """See packing_corpus_leg; a workload of one fixed sequence (nothing to
+    pack) takes the Qwen2.5-0.5B length mix and token budget instead."""
+    from fine_tuning_gb300 import workloads as W
+    if wl.lengths is not None and len(wl.lengths) <= 1:
+        out = packing_corpus_leg(W.WORKLOADS["qwen2.5-0.5b"], n_seq, batch)
+        out["length_mix_of"] = "qwen2.5-0.5b (this workload is one fixed sequence)"
+        return out
+    out = packing_corpus_leg(wl, n_seq, batch)
+    out["length_mix_of"] = wl.name
+    return out
+
+
+def packing_corpus_leg(wl, n_seq=200_000, batch=8):
     """Best-Fit-Decreasing packing of a corpus with the workload's length mix
     into bins of T tokens: host throughput of the library routine and of the
     oracle (bounded sample), and how much of the padding waste of plain
@@ -843,7 +1045,7 @@ def packing_leg(wl, n_seq=200_000, batch=8):
             "sequences_per_s": round(lens.size / el, 1),
             "oracle_sequences_per_s": round(m / el_o, 1), "oracle_sample": m,
             "fill": round(real / (bins * wl.T), 4),
-            "padding_waste_recovered": round(1 - waste_pack / waste_pad, 4),
+            "padding_waste_recovered": round(1 - waste_pack / waste_pad, 4) if waste_pad else None,
             "vs": f"batches of {batch} padded to their longest sequence"}
 
 
@@ -858,7 +1060,7 @@ def run_reference(args):
     from fine_tuning_gb300 import workloads as W
     from oracle.build import build_oracle
     build_oracle()
-    wl = W.WORKLOADS[args.workload]
+    wl = select_workload(args.workload, args.tokens)
     lens = W.draw_lengths(wl)
     cu = W.cu_seqlens_from_lengths(lens)
     cap = min(wl.T, 4096)
@@ -876,7 +1078,8 @@ def run_reference(args):
         oracle_step(wl, cut64, cu, n)
     el = time.perf_counter() - t
     ib = W.ideal_bytes(wl)
-    sample_bytes = sum(v * (n / (wl.T_swiglu if "swiglu" in k else wl.T)) for k, v in ib.items())
+    # the six step ops only (the oracle step runs those)
+    sample_bytes = sum(ib[k] * (n / (wl.T_swiglu if "swiglu" in k else wl.T)) for k in OPS)
     value = sample_bytes * args.steps / el / 1e9
     sample = (f"first {n} of {wl.T} tokens per step, all six ops, oracle in double "
               f"(OpenMP over rows) on the host cores")
@@ -886,10 +1089,10 @@ def run_reference(args):
         "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded packed batch; no dataset, no weights)",
-        "config": {"workload": wl.name, "T": wl.T, "tokens_per_step": n},
+        "config": workload_config(wl, len(lens), world),
         "tokens_per_s": round(n * args.steps / el, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.threads(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "tokens_per_step": n},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

@@ -1,0 +1,69 @@
+"""Host-side logic of bench.py that needs no GPU: workload slices, the rows
+the in-run parity check samples, the config both arms print, and the
+oracle arm at the default (largest) workload."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+import bench
+from fine_tuning_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_default_workload_is_the_largest_single_gpu_one():
+    args = bench.parse_args([])
+    assert args.workload == "qwen3-32b-524k"
+    assert max(W.WORKLOADS.values(), key=lambda w: w.T).name == args.workload
+    # the smaller bf16 workloads are timed beside it in the same run
+    assert set(args.per_workload.split(",")) == {"qwen2.5-0.5b", "llama-3.2-1b", "qwen3-8b"}
+
+
+def test_slice_keeps_row_shapes_and_cuts_sequences():
+    full = W.WORKLOADS["qwen3-32b-524k"]
+    s = bench.select_workload("qwen3-32b-524k", 32768)
+    assert (s.T, s.T_swiglu, s.H, s.I, s.Hq, s.Hkv, s.D) == \
+        (32768, 32768, full.H, full.I, full.Hq, full.Hkv, full.D)
+    assert W.draw_lengths(s).tolist() == [32768] and s.name == "qwen3-32b-524k[:32768]"
+    # a batch of many sequences is cut at the slice's end
+    s2 = bench.select_workload("qwen2.5-0.5b", 1000)
+    lens = W.draw_lengths(s2)
+    full_lens = W.draw_lengths(W.WORKLOADS["qwen2.5-0.5b"])
+    assert lens.sum() == 1000 and lens[:-1].tolist() == full_lens[:len(lens) - 1].tolist()
+    assert bench.select_workload("qwen2.5-0.5b", 0) is W.WORKLOADS["qwen2.5-0.5b"]
+
+
+def test_parity_rows_span_the_batch():
+    wl = W.WORKLOADS["qwen3-32b-524k"]
+    cu = W.cu_seqlens_from_lengths(W.draw_lengths(wl))
+    rows, srows = bench.parity_rows(wl, cu)
+    assert rows[0] == 0 and rows[-1] == wl.T - 1 and srows[-1] == wl.T_swiglu - 1
+    assert np.all(np.diff(rows) > 0) and (rows > wl.T // 2).sum() > 64
+    wl2 = W.WORKLOADS["qwen2.5-0.5b"]
+    cu2 = W.cu_seqlens_from_lengths(W.draw_lengths(wl2))
+    rows2, _ = bench.parity_rows(wl2, cu2)
+    for c in cu2[1:17]:  # both sides of the first sequence boundaries
+        assert c in rows2 and c - 1 in rows2
+    tiny = W.WORKLOADS["tiny_f32"]
+    r3, s3 = bench.parity_rows(tiny, W.cu_seqlens_from_lengths(W.draw_lengths(tiny)))
+    assert r3.tolist() == list(range(tiny.T)) and s3.tolist() == list(range(tiny.T_swiglu))
+
+
+def test_packing_leg_on_a_single_sequence_workload_uses_a_length_mix():
+    out = bench.packing_leg(W.WORKLOADS["qwen3-32b-524k"], n_seq=3000)
+    assert out["length_mix_of"].startswith("qwen2.5-0.5b")
+    assert out["bins"] >= 1 and 0 < out["fill"] <= 1
+
+
+def test_reference_arm_prints_our_config_at_the_default_workload():
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                          "--warmup", "0", "--reference-seconds", "1"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    d = json.loads([ln for ln in out.stdout.splitlines() if ln.startswith("{")][-1])
+    wl = W.WORKLOADS["qwen3-32b-524k"]
+    assert d["config"] == bench.workload_config(wl, 1, 1)
+    assert d["cpu_baseline"]["tokens_per_step"] >= 1 and d["value"] > 0
