@@ -403,11 +403,12 @@ FTK_API ftk_status ftk_swiglu_bwd_h(const void *dh, int64_t ld_dh, const void *g
 
 // ------------------------------------------------------------------ QK-RoPE
 
-// inv_freq (HOST, nullable) replaces theta's table when given.
+// inv_freq (HOST, nullable) replaces theta's table when given; skip (DEVICE,
+// nullable) is the word of the boundary check that guards the rotation.
 static ftk_status qk_rope(void *q, int64_t ld_q, void *k, int64_t ld_k, const int32_t *cu,
                           int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D, double theta,
                           const double *inv_freq, ftk_dtype dtype, ftk_stream_t stream,
-                          bool backward) {
+                          bool backward, const uint32_t *skip = nullptr) {
   if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
   if (T < 0 || B < 0 || Hq < 0 || Hkv < 0 || Hq + Hkv < 1 || D < 2 || D % 2 != 0 ||
       D / 2 > ftk::kRopeMaxHalf || T >= (int64_t(1) << 31))
@@ -431,6 +432,11 @@ static ftk_status qk_rope(void *q, int64_t ld_q, void *k, int64_t ld_k, const in
   const View vk = view(k, Hkv > 0 ? T : 0, ld_k, (int64_t)Hkv * D, es);
   const View vc = view(cu, 1, (int64_t)B + 1, (int64_t)B + 1, 4);
   if (may_overlap(vq, vk) || may_overlap(vc, vq) || may_overlap(vc, vk)) return FTK_ERR_ALIAS;
+  if (skip) {
+    if (!aligned(skip, 4)) return FTK_ERR_ALIGN;
+    const View vs = view(skip, 1, 1, 1, 4);
+    if (may_overlap(vs, vq) || may_overlap(vs, vk)) return FTK_ERR_ALIAS;
+  }
 
   const int n = dt == DType::F32 ? 4 : 8;
   const bool vec = (D / 2) % n == 0 && (Hq == 0 || (aligned(q, 16) && ld_q % n == 0)) &&
@@ -442,7 +448,40 @@ static ftk_status qk_rope(void *q, int64_t ld_q, void *k, int64_t ld_k, const in
   if (e != cudaSuccess) return cuda_fail(e);
   ftk::RopeArgs a{q, ld_q, k, ld_k, cu, B, T, Hq, Hkv, D, theta, backward};
   a.inv_freq = inv_freq;
+  a.skip = skip;
   return finish(ftk::launch_qk_rope(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+FTK_API ftk_status ftk_check_seqlens(const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                     uint32_t *status, ftk_stream_t stream) {
+  if (B < 0 || T < 0) return FTK_ERR_SHAPE;
+  if (!cu_seqlens || !status) return FTK_ERR_NULL;
+  if (!aligned(cu_seqlens, 4) || !aligned(status, 4)) return FTK_ERR_ALIGN;
+  if (may_overlap(view(cu_seqlens, 1, (int64_t)B + 1, (int64_t)B + 1, 4), view(status, 1, 1, 1, 4)))
+    return FTK_ERR_ALIAS;
+  return finish(ftk::launch_check_seqlens(cu_seqlens, B, T, status, (cudaStream_t)stream));
+}
+
+FTK_API ftk_status ftk_qk_rope_fwd_checked(void *q, int64_t ld_q, void *k, int64_t ld_k,
+                                           const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                           int32_t Hq, int32_t Hkv, int32_t D, double theta,
+                                           const double *inv_freq,
+                                           const uint32_t *seqlens_status, ftk_dtype dtype,
+                                           ftk_stream_t stream) {
+  if (!seqlens_status && T > 0) return FTK_ERR_NULL;
+  return qk_rope(q, ld_q, k, ld_k, cu_seqlens, B, T, Hq, Hkv, D, theta, inv_freq, dtype, stream,
+                 false, seqlens_status);
+}
+
+FTK_API ftk_status ftk_qk_rope_bwd_checked(void *dq, int64_t ld_q, void *dk, int64_t ld_k,
+                                           const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                           int32_t Hq, int32_t Hkv, int32_t D, double theta,
+                                           const double *inv_freq,
+                                           const uint32_t *seqlens_status, ftk_dtype dtype,
+                                           ftk_stream_t stream) {
+  if (!seqlens_status && T > 0) return FTK_ERR_NULL;
+  return qk_rope(dq, ld_q, dk, ld_k, cu_seqlens, B, T, Hq, Hkv, D, theta, inv_freq, dtype,
+                 stream, true, seqlens_status);
 }
 
 FTK_API ftk_status ftk_qk_rope_fwd(void *q, int64_t ld_q, void *k, int64_t ld_k,

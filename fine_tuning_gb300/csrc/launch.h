@@ -165,9 +165,15 @@ struct RopeArgs {
   double theta;
   bool backward;
   const double *inv_freq = nullptr;  // HOST [D/2]: replaces theta^(-2i/D) when set
+  const uint32_t *skip = nullptr;    // DEVICE word: non-zero leaves q, k untouched
 };
 cudaError_t launch_qk_rope(DType dt, bool vec, bool wide, const RopeArgs &a,
                            const DeviceInfo &dev, cudaStream_t s);
+
+// The sequence-boundary check (seqlens_check.cu): status = the
+// FTK_SEQLENS_* bits found in cu[0..B] against T, written by one CTA.
+cudaError_t launch_check_seqlens(const int32_t *cu, int32_t B, int64_t T, uint32_t *status,
+                                 cudaStream_t s);
 
 // Per-head QK-RMSNorm fused with RoPE (qk_norm_rope.cu).  Forward: q, k in,
 // oq, ok out (may be q, k), rq/rk written when set.  Backward: gq, gk (the

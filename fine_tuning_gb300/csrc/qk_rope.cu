@@ -62,6 +62,7 @@ qk_rope_kernel(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   __shared__ int32_t cu_s[kCuInShared];
   pdl_wait();
   pdl_trigger();
+  if (rope_skipped(fr)) return;  // malformed cu_seqlens: q, k untouched
 
   const int half = D >> 1;
   const int TPT = NV * S;
@@ -186,6 +187,7 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
+  if (rope_skipped(fr)) return;  // malformed cu_seqlens: q, k untouched
   const bool cu_staged = B < kCuInShared;
   if (cu_staged)
     for (int i = threadIdx.x; i <= B; i += blockDim.x) cu_s[i] = __ldg(cu + i);
@@ -354,6 +356,7 @@ qk_rope_warp(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
+  if (rope_skipped(fr)) return;  // malformed cu_seqlens: q, k untouched
   Packet<T, N> a[HPT], b[HPT];
 #pragma unroll
   for (int m = 0; m < HPT; ++m) {
@@ -449,6 +452,7 @@ qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
+  if (rope_skipped(fr)) return;  // malformed cu_seqlens: q, k untouched
   // the sequence boundaries in shared memory when they fit: every token's
   // position is a binary search over them
   const bool cu_staged = B < kCuInShared;
@@ -674,7 +678,7 @@ cudaError_t rope_typed(bool vec, const RopeArgs &a, const RopeFreqs &fr, const D
 
 cudaError_t launch_qk_rope(DType dt, bool vec, bool wide, const RopeArgs &a,
                            const DeviceInfo &dev, cudaStream_t s) {
-  const RopeFreqs fr = make_rope_freqs(a.D, a.theta, a.inv_freq);
+  const RopeFreqs fr = make_rope_freqs(a.D, a.theta, a.inv_freq, a.skip);
   if (dt == DType::F32)
     return wide ? rope_typed<float, int64_t>(vec, a, fr, dev, s)
                 : rope_typed<float, int32_t>(vec, a, fr, dev, s);

@@ -22,7 +22,18 @@ namespace {
 struct RopeFreqs {
   float hi[kRopeMaxHalf];
   float lo[kRopeMaxHalf];
+  // nullable: a word written by the sequence-boundary check; when it is
+  // non-zero the kernel returns before touching q or k
+  const uint32_t *skip;
 };
+
+// True when the boundary check that ran before this kernel found the batch's
+// cu_seqlens malformed.  Read after the grid-dependency wait (the check is
+// the preceding kernel) and past L1; uniform across a CTA, so an early
+// return skips no barrier another thread waits on.
+__device__ __forceinline__ bool rope_skipped(const RopeFreqs &fr) {
+  return fr.skip != nullptr && __ldcg(fr.skip) != 0u;
+}
 
 constexpr int kCuInShared = 2048;  // cu_seqlens entries a CTA stages in shared memory
 
@@ -67,8 +78,10 @@ __device__ __forceinline__ int position_of(Idx t, const int32_t *cu, int B) {
 
 // f_i = inv_freq_i / (2 pi) in double, split into two floats; inv_freq_i is
 // theta^(-2i/D), or the caller's (scaled) table when inv_freq is set.
-inline RopeFreqs make_rope_freqs(int D, double theta, const double *inv_freq) {
+inline RopeFreqs make_rope_freqs(int D, double theta, const double *inv_freq,
+                                 const uint32_t *skip = nullptr) {
   RopeFreqs fr;
+  fr.skip = skip;
   const int half = D / 2;
   for (int i = 0; i < kRopeMaxHalf; ++i) {
     if (i < half) {

@@ -83,6 +83,11 @@ def library() -> ctypes.CDLL:
         "ftk_cce_fwd": (st, [vp, i64, vp, i64, vp, i64, i64, i64, vp, vp, vp, sz, dt, vp]),
         "ftk_cce_bwd": (st, [vp, i64, vp, i64, vp, vp, vp, i64, i64, i64, vp, i64, vp, i64, vp,
                              sz, dt, vp]),
+        "ftk_check_seqlens": (st, [vp, i32, i64, vp, vp]),
+        "ftk_qk_rope_fwd_checked": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, vp,
+                                         vp, dt, vp]),
+        "ftk_qk_rope_bwd_checked": (st, [vp, i64, vp, i64, vp, i32, i64, i32, i32, i32, f64, vp,
+                                         vp, dt, vp]),
         "ftk_bfd_pack": (st, [vp, i64, i32, vp, vp, vp, vp]),
         "ftk_device_status": (st, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
         "ftk_selftest_wait_timeout": (st, [i64, vp]),
@@ -321,7 +326,7 @@ def _heads(t: Optional[torch.Tensor], name: str):
     return (t.stride(0) if T > 1 else nh * D), nh, D
 
 
-def _rope(name, q, k, cu_seqlens, theta, inv_freq=None):
+def _rope(name, q, k, cu_seqlens, theta, inv_freq=None, checked=False, status=None):
     _cuda(q, k, cu_seqlens)
     ldq, Hq, Dq = _heads(q, "q")
     ldk, Hkv, Dk = _heads(k, "k")
@@ -331,15 +336,15 @@ def _rope(name, q, k, cu_seqlens, theta, inv_freq=None):
     ref = q if q is not None else k
     if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
         raise ValueError("cu_seqlens must be a contiguous int32 [B+1] device tensor")
-    if inv_freq is None:
-        last = float(theta)
+    table, table_p = _table(inv_freq, D)
+    if checked:
+        _status_check(status)
+        freq_args = (float(theta or 0.0), table_p, _ptr(status))
     else:
-        table = np.ascontiguousarray(np.asarray(inv_freq, dtype=np.float64))
-        if table.shape != (D // 2,):
-            raise ValueError("inv_freq must hold D/2 values")
-        last = table.ctypes.data_as(ctypes.c_void_p)
+        freq_args = (float(theta),) if inv_freq is None else (table_p,)
     _call(name, _ptr(q), ldq, _ptr(k), ldk, _ptr(cu_seqlens), cu_seqlens.numel() - 1,
-          ref.shape[0], Hq, Hkv, D, last, _code(ref), _stream(ref))
+          ref.shape[0], Hq, Hkv, D, *freq_args, _code(ref), _stream(ref))
+    del table
     return q, k
 
 
@@ -361,6 +366,43 @@ def qk_rope_freq_fwd(q, k, cu_seqlens, inv_freq):
 def qk_rope_freq_bwd(dq, dk, cu_seqlens, inv_freq):
     """Backward of qk_rope_freq_fwd, in place."""
     return _rope("ftk_qk_rope_freq_bwd", dq, dk, cu_seqlens, None, inv_freq)
+
+
+def check_seqlens(cu_seqlens, T: int, status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Validate a packed batch's boundaries on the device, without a host
+    synchronisation: the returned int32 [1] device tensor (`status`, if
+    given, is overwritten) receives the SEQLENS_* bits found (0: valid).
+    Pass it to the *_checked rotations of every layer of the batch."""
+    _cuda(cu_seqlens, status)
+    _cu_check(cu_seqlens)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=cu_seqlens.device)
+    _status_check(status)
+    _call("ftk_check_seqlens", _ptr(cu_seqlens), cu_seqlens.numel() - 1, int(T), _ptr(status),
+          _stream(cu_seqlens))
+    return status
+
+
+SEQLENS_BAD_START, SEQLENS_DECREASING, SEQLENS_BAD_END = 1, 2, 4
+
+
+def _status_check(status):
+    if status is None or not status.is_cuda or status.dtype not in (torch.int32, torch.uint32) \
+            or status.numel() < 1:
+        raise ValueError("the seqlens status must be a 32-bit integer device tensor")
+
+
+def qk_rope_fwd_checked(q, k, cu_seqlens, seqlens_status, theta: float = 0.0, inv_freq=None):
+    """qk_rope_fwd (or, with inv_freq, qk_rope_freq_fwd) that leaves q and k
+    untouched when the word check_seqlens wrote is non-zero."""
+    return _rope("ftk_qk_rope_fwd_checked", q, k, cu_seqlens, theta, inv_freq, True,
+                 seqlens_status)
+
+
+def qk_rope_bwd_checked(dq, dk, cu_seqlens, seqlens_status, theta: float = 0.0, inv_freq=None):
+    """Backward of qk_rope_fwd_checked, in place, under the same guard."""
+    return _rope("ftk_qk_rope_bwd_checked", dq, dk, cu_seqlens, theta, inv_freq, True,
+                 seqlens_status)
 
 
 def _table(inv_freq, D):

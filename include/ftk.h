@@ -74,7 +74,10 @@ typedef enum { FTK_F32 = 0, FTK_BF16 = 1 } ftk_dtype;
 
 /* ------------------------------------------------------------- RMSNorm */
 
-/* Forward RMSNorm of T token rows of H features:
+/* Forward RMSNorm of T token rows of H features ("Chronicals", arXiv
+ * 2601.02609, abstract, optimisation (1): the fused RMSNorm kernel, one of
+ * the three fusions that remove most of the step's memory traffic; the page
+ * names the op, the formula is the standard RMSNorm):
  *   r[t]   = 1 / sqrt( (1/H) sum_j x[t,j]^2 + eps )
  *   y[t,j] = x[t,j] * r[t] * w[j]
  * x [T, ldx], y [T, ldy] (dtype), w [H] (dtype, contiguous),
@@ -90,7 +93,9 @@ FTK_API ftk_status ftk_rmsnorm_fwd(const void *x, int64_t ldx, const void *w, vo
 FTK_API size_t ftk_rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H,
                                                ftk_dtype dtype);
 
-/* Backward RMSNorm (gradient of sum(dy * y) for the forward above):
+/* Backward RMSNorm (gradient of sum(dy * y) for the forward above; the
+ * backward half of the fused RMSNorm of "Chronicals", arXiv 2601.02609,
+ * abstract, optimisation (1)):
  *   c[t]    = sum_j dy[t,j] w[j] x[t,j]
  *   dx[t,j] = r[t] w[j] dy[t,j] - r[t]^3 x[t,j] c[t] / H
  *   dw[j]   = sum_t dy[t,j] x[t,j] r[t]          (fp32, OVERWRITTEN)
@@ -168,7 +173,9 @@ FTK_API ftk_status ftk_rmsnorm_add_bwd(const void *dy, int64_t lddy, const void 
 
 /* -------------------------------------------------------------- SwiGLU */
 
-/* Forward SwiGLU, elementwise over T rows of I features:
+/* Forward SwiGLU, elementwise over T rows of I features ("Chronicals",
+ * arXiv 2601.02609, abstract, optimisation (1): the fused SwiGLU kernel;
+ * the page names the op, the formula is the standard gated SiLU):
  *   h = silu(g) * u = g * sigmoid(g) * u,   sigmoid(g) = 1 / (1 + e^-g)
  * g, u: [T, ld_gu] (so a fused [T, 2I] gate_up projection can be passed as
  * g = gu, u = gu + I, ld_gu = 2I); h: [T, ld_h]. */
@@ -176,7 +183,9 @@ FTK_API ftk_status ftk_swiglu_fwd(const void *g, const void *u, int64_t ld_gu, v
                           int64_t ld_h, int64_t T, int64_t I, ftk_dtype dtype,
                           ftk_stream_t stream);
 
-/* Backward SwiGLU (gradient of sum(dh * h)), s = sigmoid(g):
+/* Backward SwiGLU (gradient of sum(dh * h); the backward half of the fused
+ * SwiGLU of "Chronicals", arXiv 2601.02609, abstract, optimisation (1)),
+ * s = sigmoid(g):
  *   dg = dh * u * s * (1 + g * (1 - s)),   du = dh * g * s
  * dh: [T, ld_dh]; g, u: [T, ld_gu]; dg, du: [T, ld_dgu].  dg may alias g and
  * du may alias u exactly (same pointer, ld_dgu == ld_gu): every element is
@@ -203,7 +212,14 @@ FTK_API ftk_status ftk_swiglu_bwd_h(const void *dh, int64_t ld_dh, const void *g
 /* ------------------------------------------------------------- QK-RoPE */
 
 /* In-place rotary embedding of Q and K together, rotate-half (NeoX) layout,
- * over a packed batch of B variable-length sequences:
+ * over a packed batch of B variable-length sequences (the fused QK RoPE
+ * paragraph of "Unsloth prétend accélérer 5 fois l'entraînement des LLM
+ * avec de nouveaux noyaux Triton et un auto-packing", seventnews.com: Q and
+ * K in ONE kernel, variable-length, fully in place with no clone or
+ * transpose; its LONG_INDEXING paragraph for the 64-bit offsets of
+ * 500k-token contexts; "Chronicals", arXiv 2601.02609, abstract,
+ * optimisation (1): fused QK-RoPE.  The pages print no formula; this is the
+ * standard rotate-half RoPE):
  *   token t of sequence b (cu_seqlens[b] <= t < cu_seqlens[b+1]) sits at
  *   position p = t - cu_seqlens[b]; for i < D/2, phi = p * theta^(-2i/D);
  *   every head vector v of Q and K at t becomes
@@ -212,10 +228,12 @@ FTK_API ftk_status ftk_swiglu_bwd_h(const void *dh, int64_t ld_dh, const void *g
  * q: [T, ld_q] holding Hq heads of D contiguous values per token,
  * k: [T, ld_k] holding Hkv heads (any GQA ratio: Hq, Hkv >= 0, Hq + Hkv
  * >= 1; q may be NULL when Hq == 0 and k when Hkv == 0).  q and k must not
- * overlap; they may be interleaved slices of one fused QKV buffer.  cu_seqlens: DEVICE int32 [B+1], cu[0] = 0, non-decreasing,
- * cu[B] = T; read on the device, never copied to the host.  Tokens outside
+ * overlap; they may be interleaved slices of one fused QKV buffer.
+ * cu_seqlens: DEVICE int32 [B+1], cu[0] = 0, non-decreasing, cu[B] = T; read on the device, never copied to the host.  Tokens outside
  * every sequence are impossible when that holds; if it does not, results are
- * unspecified but every access stays inside q and k.  0 < D <= 512, D even.
+ * unspecified but every access stays inside q and k (ftk_check_seqlens and
+ * the *_checked calls below validate it on the device and skip the
+ * rotation instead).  0 < D <= 512, D even.
  * The angle is formed in extended precision (position times a two-float
  * split of theta^(-2i/D) / 2pi), so it is accurate to ~1e-7 rad at
  * positions beyond 500k; no cos/sin table is read. */
@@ -225,7 +243,9 @@ FTK_API ftk_status ftk_qk_rope_fwd(void *q, int64_t ld_q, void *k, int64_t ld_k,
                            ftk_dtype dtype, ftk_stream_t stream);
 
 /* Backward of the above on dq, dk in place: the same rotation by -phi (the
- * transpose of the forward rotation).  Same arguments and rules. */
+ * transpose of the forward rotation; the pages' fused QK-RoPE serves the
+ * training step, whose backward pass needs this).  Same arguments and
+ * rules. */
 FTK_API ftk_status ftk_qk_rope_bwd(void *dq, int64_t ld_q, void *dk, int64_t ld_k,
                            const int32_t *cu_seqlens, int32_t B, int64_t T,
                            int32_t Hq, int32_t Hkv, int32_t D, double theta,
@@ -266,6 +286,50 @@ FTK_API ftk_status ftk_qk_rope_freq_bwd(void *dq, int64_t ld_q, void *dk, int64_
 FTK_API ftk_status ftk_rope_llama3_inv_freq(int32_t D, double theta, double factor,
                                             double low_freq_factor, double high_freq_factor,
                                             double original_max_position, double *inv_freq);
+
+/* ------------------------------------ checked sequence boundaries (RoPE) */
+
+/* Bits of the word ftk_check_seqlens writes (0: the boundaries are valid). */
+#define FTK_SEQLENS_BAD_START 1u  /* cu[0] != 0 */
+#define FTK_SEQLENS_DECREASING 2u /* some cu[b+1] < cu[b] */
+#define FTK_SEQLENS_BAD_END 4u    /* cu[B] != T */
+
+/* Validates a packed batch's sequence boundaries where they live, on the
+ * device, without a host synchronisation ("Unsloth und NVIDIA optimieren
+ * LLM-Training um zusätzliche 25%", lumeric.app, item (1): the packed
+ * metadata stays on the GPU; the auto-packing paragraph of the Unsloth item
+ * on seventnews.com makes it the contract between packer and kernels).
+ * cu_seqlens: DEVICE int32 [B+1]; status: DEVICE uint32, caller-owned,
+ * OVERWRITTEN (after the check completes, in stream order) with the
+ * FTK_SEQLENS_* bits found: cu[0] == 0, cu non-decreasing, cu[B] == T.  With
+ * those three, every boundary lies in [0, T].  One small kernel (one CTA);
+ * nothing traps or faults on bad input.  Check once per batch, then pass
+ * `status` to the checked RoPE calls of every layer.  B >= 0, T >= 0, else
+ * FTK_ERR_SHAPE; NULL pointers give FTK_ERR_NULL; status must not overlap
+ * cu_seqlens (FTK_ERR_ALIAS) and both need 4-byte alignment. */
+FTK_API ftk_status ftk_check_seqlens(const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                     uint32_t *status, ftk_stream_t stream);
+
+/* ftk_qk_rope_fwd / ftk_qk_rope_bwd (inv_freq NULL: theta's table) or
+ * ftk_qk_rope_freq_fwd / _bwd (inv_freq set, HOST double [D/2]), guarded by
+ * the word ftk_check_seqlens wrote for this batch: every CTA reads
+ * *seqlens_status (DEVICE uint32, read-only here) after the preceding work on
+ * the stream has finished, and when it is non-zero the kernel returns
+ * without touching q or k.  A caller may also set the word itself to skip
+ * the rotation.  Host-side rules and errors are those of the unchecked calls,
+ * plus FTK_ERR_NULL for a NULL seqlens_status (T > 0). */
+FTK_API ftk_status ftk_qk_rope_fwd_checked(void *q, int64_t ld_q, void *k, int64_t ld_k,
+                                           const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                           int32_t Hq, int32_t Hkv, int32_t D, double theta,
+                                           const double *inv_freq,
+                                           const uint32_t *seqlens_status, ftk_dtype dtype,
+                                           ftk_stream_t stream);
+FTK_API ftk_status ftk_qk_rope_bwd_checked(void *dq, int64_t ld_q, void *dk, int64_t ld_k,
+                                           const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                           int32_t Hq, int32_t Hkv, int32_t D, double theta,
+                                           const double *inv_freq,
+                                           const uint32_t *seqlens_status, ftk_dtype dtype,
+                                           ftk_stream_t stream);
 
 /* ------------------------------------- QK-RMSNorm fused into the QK-RoPE */
 

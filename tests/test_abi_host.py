@@ -262,3 +262,40 @@ def test_cce_backward_chunk_choice(lib):
     for bad in [(0, 896, 151936, 152), (8192, 0, 151936, 152), (8192, 896, 0, 152),
                 (8192, 896, 151936, 0)]:
         assert lib.ftk_cce_bwd_chunk(*bad) == 0
+
+
+def test_check_seqlens_argument_errors(lib):
+    f = lib.ftk_check_seqlens
+    cu, st = A, A + (1 << 20)
+    assert f(cu, -1, 10, st, None) == SHAPE
+    assert f(cu, 2, -1, st, None) == SHAPE
+    assert f(None, 2, 10, st, None) == NULL
+    assert f(cu, 2, 10, None, None) == NULL
+    assert f(cu + 2, 2, 10, st, None) == ALIGN
+    assert f(cu, 2, 10, st + 2, None) == ALIGN
+    assert f(cu, 2, 10, cu + 8, None) == ALIAS  # the word inside cu[0..2]
+
+
+def test_checked_rope_argument_errors(lib):
+    for f in (lib.ftk_qk_rope_fwd_checked, lib.ftk_qk_rope_bwd_checked):
+        q, k, cu, st = A, A + (1 << 22), A + (1 << 23), A + (1 << 24)
+        ok = [q, 4 * 16, k, 2 * 16, cu, 4, 64, 4, 2, 16, 1e4, None, st, F32, None]
+        names = ["q", "ldq", "k", "ldk", "cu", "B", "T", "Hq", "Hkv", "D", "theta", "inv", "st",
+                 "dt", "s"]
+
+        def call(**kw):
+            a = list(ok)
+            for n, v in kw.items():
+                a[names.index(n)] = v
+            return f(*a)
+
+        assert call(T=0) == OK
+        assert call(T=0, st=None) == OK
+        assert call(st=None) == NULL
+        assert call(st=st + 2) == ALIGN
+        assert call(st=q + 64) == ALIAS   # the word inside q
+        assert call(D=15) == SHAPE
+        assert call(theta=0.0) == SHAPE   # no table and no theta
+        bad = (ctypes.c_double * 8)(*([0.5] * 7 + [1.5]))
+        assert call(inv=ctypes.cast(bad, ctypes.c_void_p)) == SHAPE
+        assert call(cu=None) == NULL
