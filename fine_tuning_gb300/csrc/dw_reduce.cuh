@@ -14,8 +14,11 @@ namespace {
 // columns; its 32 warps take the rows p = warp, warp + 32, ... and their sums
 // are added in warp order.  Column j goes to out0[j] when j < split, else to
 // out1[j - split] (two weights whose partial rows sit side by side); a null
-// output is skipped.
+// output is skipped.  Each thread loads its rows kReduceBatch at a time, all
+// loads of a batch issued before the first add (up to 512 partial rows, one
+// L2 round trip), and adds them in row order.
 constexpr int kReduceWarps = 32;
+constexpr int kReduceBatch = 16;
 
 __global__ void __launch_bounds__(32 * kReduceWarps)
 dw_reduce(const float *__restrict__ ws, int P, int H, int ld, float *__restrict__ out0, int split,
@@ -27,8 +30,16 @@ dw_reduce(const float *__restrict__ ws, int P, int H, int ld, float *__restrict_
   const int col = blockIdx.x * 32 + lane;
   float s = 0.f;
   if (col < H) {
-#pragma unroll 4
-    for (int p = warp; p < P; p += kReduceWarps) s += ws[(size_t)p * ld + col];
+    for (int p0 = warp; p0 < P; p0 += kReduceWarps * kReduceBatch) {
+      float v[kReduceBatch];
+#pragma unroll
+      for (int i = 0; i < kReduceBatch; ++i) {
+        const int p = p0 + i * kReduceWarps;
+        v[i] = p < P ? __ldcg(ws + (size_t)p * ld + col) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < kReduceBatch; ++i) s += v[i];  // + 0 past P leaves s unchanged
+    }
   }
   part[warp][lane] = s;
   __syncthreads();

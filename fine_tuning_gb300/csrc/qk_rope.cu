@@ -44,6 +44,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "rmsnorm_lean.cuh"
 #include "rope_common.cuh"
 
 namespace ftk {
@@ -527,6 +528,147 @@ qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
   cp_async_wait<0>();
 }
 
+// bf16 heads whose half is 8 NV values, NV a power of two dividing 32 (D =
+// 16 .. 512): the lean form of qk_rope_pipe, with the same per-warp
+// cp.async ring of head passes and the same (cos, sin) table per token.
+// Each warp owns a contiguous run of tokens (the persistent grid splits the
+// batch evenly), so a token's sequence comes from one search at the run's
+// start and a walk over the boundaries after it, not a search per token;
+// the rotation runs on fp32 pairs, each half rounded exactly like the scalar
+// fma(a, c, -(b s)) of qk_rope_pipe, so the two kernels agree bit for bit;
+// the row addresses advance per token.  The table entry of lane (slot, j)
+// for columns 8 j + 2 m, 8 j + 2 m + 1 holds (cos, cos, sgn sin, sgn sin)
+// at m NV + j, so the NV lanes of a head read consecutive 16-byte entries.
+template <typename Idx, int NV>
+__global__ void __launch_bounds__(kCtaThreads, kPipeBlocks)
+qk_rope_lean(bf16 *q, Idx ld_q, bf16 *k, Idx ld_k, const int32_t *__restrict__ cu, int B,
+             Idx rows, int Hq, int NH, float sgn, const __grid_constant__ RopeFreqs fr) {
+  constexpr int N = 8, half = N * NV, D = 2 * half, S = 32 / NV;
+  constexpr int kWarps = kCtaThreads / 32;
+  __shared__ float4 tab_all[kWarps][4 * NV];
+  __shared__ float2 freq[half];
+  __shared__ int32_t cu_s[kCuInShared];
+  extern __shared__ uint4 stg_all[];  // [warps][kPipeBufs][2][32]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = lane % NV, slot = lane / NV;
+  float4 *const tab = tab_all[warp];
+  uint4 *const stg = stg_all + warp * (kPipeBufs * 2 * 32) + lane;
+
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
+  if (rope_skipped(fr)) return;  // malformed cu_seqlens: q, k untouched
+  const bool cu_staged = B < kCuInShared;
+  if (cu_staged)
+    for (int i = threadIdx.x; i <= B; i += blockDim.x) cu_s[i] = __ldg(cu + i);
+  __syncthreads();  // the frequency table and the boundaries; no block barrier follows
+  const int32_t *bounds = cu_staged ? cu_s : cu;
+
+  // this warp's run of tokens [t, t_end)
+  const int64_t G = (int64_t)gridDim.x * kWarps, gw = (int64_t)blockIdx.x * kWarps + warp;
+  Idx t = (Idx)((int64_t)rows * gw / G);
+  const Idx t_end = (Idx)((int64_t)rows * (gw + 1) / G);
+  if (t >= t_end) return;
+  const int passes = (NH + S - 1) / S;  // head passes per token, the same on every lane
+
+  // the stager runs kPipeBufs - 1 passes ahead with its own row pointers
+  Idx t2 = t;
+  int p2 = 0, b2 = 0;
+  const bf16 *q2 = q + t2 * ld_q + j * N, *k2 = k + t2 * ld_k + j * N - (Idx)Hq * D;
+  auto stage = [&]() {
+    const int h = slot + p2 * S;
+    if (t2 < t_end && h < NH) {
+      const bf16 *v = (h < Hq ? q2 : k2) + (Idx)h * D;
+      uint4 *d = stg + b2 * 64;
+      cp_async16(d, v);
+      cp_async16(d + 32, v + half);
+    }
+    cp_async_commit();  // one group per pass on every lane, empty or not
+    if (++p2 == passes) {
+      p2 = 0;
+      ++t2;
+      q2 += ld_q;
+      k2 += ld_k;
+    }
+    b2 = b2 + 1 == kPipeBufs ? 0 : b2 + 1;
+  };
+#pragma unroll
+  for (int i = 0; i < kPipeBufs - 1; ++i) stage();
+
+  // the sequence of the run's first token, then a walk over the boundaries
+  int sb = sequence_of<Idx>(t, bounds, B);
+  Idx seq_start = (Idx)bounds[sb], seq_next = (Idx)bounds[sb + 1];
+  bf16 *qr = q + t * ld_q + j * N, *kr = k + t * ld_k + j * N - (Idx)Hq * D;
+  int p = 0, b = 0;
+  while (t < t_end) {  // warp-uniform
+    stage();  // the next passes' loads fly meanwhile
+    if (p == 0) {
+      while (sb < B - 1 && t >= seq_next) {  // skips empty sequences too
+        ++sb;
+        seq_start = seq_next;
+        seq_next = (Idx)bounds[sb + 1];
+      }
+      const int pos = (int)(t - seq_start);
+      __syncwarp();  // the previous token's table has been read
+      float *tf = reinterpret_cast<float *>(tab);
+#pragma unroll
+      for (int i = lane; i < half; i += 32) {
+        const float2 f = freq[i];
+        float c, sn;
+        rope_cos_sin(pos, f.x, f.y, &c, &sn);
+        float *ent = tf + 4 * (((i % N) >> 1) * NV + i / N) + (i & 1);
+        ent[0] = c;
+        ent[2] = sgn * sn;
+      }
+      __syncwarp();
+    }
+    cp_async_wait<kPipeBufs - 1>();  // this lane's copies for (t, p) have landed
+    const int h = slot + p * S;
+    if (h < NH) {
+      const uint4 *d = stg + b * 64;
+      const uint4 xa = d[0], xb = d[32];
+      const uint32_t wa[4] = {xa.x, xa.y, xa.z, xa.w}, wb[4] = {xb.x, xb.y, xb.z, xb.w};
+      uint32_t o1[4], o2[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float4 cs = tab[m * NV + j];
+        const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
+        const float2 a = bf2_unpack(wa[m]), bb = bf2_unpack(wb[m]);
+        const float2 bs = __fmul2_rn(bb, s2), as = __fmul2_rn(a, s2);
+        o1[m] = bf2_pack(__ffma2_rn(a, c2, make_float2(-bs.x, -bs.y)));
+        o2[m] = bf2_pack(__ffma2_rn(bb, c2, as));
+      }
+      bf16 *v = (h < Hq ? qr : kr) + (Idx)h * D;
+      *reinterpret_cast<uint4 *>(v) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+      *reinterpret_cast<uint4 *>(v + half) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+    }
+    if (++p == passes) {
+      p = 0;
+      ++t;
+      qr += ld_q;
+      kr += ld_k;
+    }
+    b = b + 1 == kPipeBufs ? 0 : b + 1;
+  }
+  cp_async_wait<0>();
+}
+
+template <typename Idx, int NV>
+cudaError_t rope_lean_launch(const RopeArgs &a, const RopeFreqs &fr, const DeviceInfo &dev,
+                             cudaStream_t s) {
+  constexpr int kWarps = kCtaThreads / 32;
+  const size_t smem = kPipeStageBytes;
+  auto kern = qk_rope_lean<Idx, NV>;
+  const int occ = blocks_per_sm((const void *)kern, kCtaThreads, smem, dev, kPipeBlocks);
+  int64_t P = ceil_div(a.T, (int64_t)kWarps);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  cudaError_t e = launch_pdl(kern, dim3((unsigned)P), dim3(kCtaThreads), smem, s, (bf16 *)a.q,
+                             (Idx)a.ld_q, (bf16 *)a.k, (Idx)a.ld_k, a.cu, a.B, (Idx)a.T, a.Hq,
+                             a.Hq + a.Hkv, a.backward ? -1.0f : 1.0f, fr);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <typename T, typename Idx, int N>
 cudaError_t rope_pipe_launch(const RopeArgs &a, const RopeFreqs &fr, const DeviceInfo &dev,
                              cudaStream_t s) {
@@ -663,6 +805,17 @@ cudaError_t rope_typed(bool vec, const RopeArgs &a, const RopeFreqs &fr, const D
   constexpr int NV = VecWidth<T>::value;
   if (vec) {
     const int nv = a.D / 2 / NV;
+    if constexpr (sizeof(T) == 2) {
+      switch (nv) {
+        case 1: return rope_lean_launch<Idx, 1>(a, fr, dev, s);
+        case 2: return rope_lean_launch<Idx, 2>(a, fr, dev, s);
+        case 4: return rope_lean_launch<Idx, 4>(a, fr, dev, s);
+        case 8: return rope_lean_launch<Idx, 8>(a, fr, dev, s);
+        case 16: return rope_lean_launch<Idx, 16>(a, fr, dev, s);
+        case 32: return rope_lean_launch<Idx, 32>(a, fr, dev, s);
+        default: break;
+      }
+    }
     if (nv >= 1 && nv <= 32 && (nv & (nv - 1)) == 0) return rope_pipe_launch<T, Idx, NV>(a, fr, dev, s);
     bool launched = false;
     cudaError_t e = rope_staged_launch<T, Idx, NV>(a, fr, dev, s, &launched);

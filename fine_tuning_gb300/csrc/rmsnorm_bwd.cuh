@@ -33,6 +33,7 @@
 #include "common.cuh"
 #include "dw_reduce.cuh"
 #include "launch.h"
+#include "rmsnorm_lean.cuh"
 
 namespace ftk {
 
@@ -207,6 +208,145 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> 
     float sum = 0.f;
     for (int g = 0; g < R; ++g) sum += part[g * a.H + j];
     dst[j] = sum;
+  }
+}
+
+// bf16 rows of one warp (the backward of rmsnorm_fwd_lean):
+// rmsnorm_bwd_pipe's persistent grid and per-warp cp.async ring (x, dy, with
+// ADD dh, and r of the next rows, kLeanBwdBufs rows deep) with the lean pair
+// arithmetic.  A row takes two sweeps over the lane's packets,
+// held packed in registers: the first forms c = sum dy w x (and, without a
+// saved r, sum x^2 in the forward's lean order), the second dx and the dw
+// pair sums, which stay in registers across all the rows a warp visits.
+// Both sweeps read the packets from the ring (the second re-reads them
+// rather than keep 2V unpacked packets live across the row's reduction,
+// which would spill).  Lane l owns packets l + 32 k (k < V).
+constexpr int kLeanBwdBufs = 3;
+
+template <int V, bool ADD> constexpr size_t bwd_lean_smem() {
+  return sizeof(uint4) * 8 * kLeanBwdBufs * ((ADD ? 3 : 2) * V + 1) * 32;  // 8 warps
+}
+
+template <typename Idx, int V, bool HAS_RSTD, bool ADD>
+__global__ void __launch_bounds__(256, 2) rmsnorm_bwd_lean(const BwdParams<bf16, Idx> a) {
+  constexpr int kSl = (ADD ? 3 : 2) * V + 1;  // x[V], dy[V] (, dh[V]), r
+  constexpr int kR = kSl - 1;                 // r's slot
+  extern __shared__ uint4 ring[];  // [warps][kLeanBwdBufs][kSl][32]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint4 *const my = ring + warp * (kLeanBwdBufs * kSl * 32) + lane;
+  pdl_wait();
+  pdl_trigger();
+  bool on[V];
+  float2 wf[V][4], acc[V][4];
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    on[k] = lane + 32 * k < a.hp;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (on[k]) u = *reinterpret_cast<const uint4 *>(a.w + (lane + 32 * k) * 8);
+    unpack8(u, wf[k]);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) acc[k][p] = make_float2(0.f, 0.f);
+  }
+  const Idx step = (Idx)gridDim.x * 8;
+  Idx row = (Idx)blockIdx.x * 8 + warp;
+  Idx srow = row;
+  const bf16 *sx = a.x + row * a.ldx + lane * 8;
+  const bf16 *sg = a.dy + row * a.lddy + lane * 8;
+  const bf16 *sh = ADD ? a.dh + row * a.lddh + lane * 8 : nullptr;
+  const Idx sx_step = step * a.ldx, sg_step = step * a.lddy, sh_step = ADD ? step * a.lddh : 0;
+  int sslot = 0;
+  auto stage = [&]() {
+    if (srow < a.rows) {
+      uint4 *d = my + sslot * (kSl * 32);
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        if (on[k]) {
+          cp_async16(d + k * 32, sx + k * 256);
+          cp_async16(d + (V + k) * 32, sg + k * 256);
+          if (ADD) cp_async16(d + (2 * V + k) * 32, sh + k * 256);
+        }
+      }
+      if (HAS_RSTD) cp_async4(d + kR * 32, a.rstd + srow);
+    }
+    cp_async_commit();  // one group per row on every lane, empty or not
+    srow += step;
+    sx += sx_step;
+    sg += sg_step;
+    if (ADD) sh += sh_step;
+    sslot = sslot + 1 == kLeanBwdBufs ? 0 : sslot + 1;
+  };
+#pragma unroll
+  for (int i = 0; i < kLeanBwdBufs - 1; ++i) stage();
+  bf16 *dst = a.dx + row * a.lddx + lane * 8;
+  const Idx dst_step = step * a.lddx;
+  int slot = 0;
+  while (row < a.rows) {  // warp-uniform
+    stage();
+    cp_async_wait<kLeanBwdBufs - 1>();  // this lane's copies of `row` have landed
+    const uint4 *d = my + slot * (kSl * 32);
+    float2 c2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      float2 xf[4], gf[4];
+      unpack8(on[k] ? d[k * 32] : make_uint4(0u, 0u, 0u, 0u), xf);
+      unpack8(on[k] ? d[(V + k) * 32] : make_uint4(0u, 0u, 0u, 0u), gf);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        c2 = __ffma2_rn(__fmul2_rn(gf[p], wf[k][p]), xf[p], c2);
+        if (!HAS_RSTD) lean_sumsq_step(s2, xf[p]);
+      }
+    }
+    float c, r;
+    if (HAS_RSTD) {
+      c = warp_sum(lean_lane_total(c2));
+      r = *reinterpret_cast<const float *>(d + kR * 32);
+    } else {
+      const float2 cs = warp_sum2(make_float2(lean_lane_total(c2), lean_lane_total(s2)));
+      c = cs.x;
+      r = rsqrtf(fmaf(cs.y, a.inv_h, a.eps));
+    }
+    const float am = r * r * r * c * a.inv_h;
+    const float2 r2 = make_float2(r, r), nam2 = make_float2(-am, -am);
+    asm volatile("" ::: "memory");  // re-read the ring below instead of keeping the packets
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      if (on[k]) {
+        float2 xf[4], gf[4], o[4];
+        unpack8(d[k * 32], xf);
+        unpack8(d[(V + k) * 32], gf);
+#pragma unroll
+        float2 hf[4];
+        if (ADD) unpack8(d[(2 * V + k) * 32], hf);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          // dx = (dh +) r w dy - r^3 x c / H;  dw += dy x r
+          o[p] = __ffma2_rn(nam2, xf[p], __fmul2_rn(r2, __fmul2_rn(gf[p], wf[k][p])));
+          if (ADD) o[p] = __fadd2_rn(hf[p], o[p]);
+          acc[k][p] = __ffma2_rn(__fmul2_rn(gf[p], xf[p]), r2, acc[k][p]);
+        }
+        *reinterpret_cast<uint4 *>(dst + k * 256) = pack8(o);
+      }
+    }
+    row += step;
+    dst += dst_step;
+    slot = slot + 1 == kLeanBwdBufs ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // every warp is done with its ring: it becomes [8][H] partials
+  float *part = reinterpret_cast<float *>(ring);
+  float2 *mine = reinterpret_cast<float2 *>(part + warp * a.H);
+#pragma unroll
+  for (int k = 0; k < V; ++k)
+    if (on[k])
+#pragma unroll
+      for (int p = 0; p < 4; ++p) mine[(lane + 32 * k) * 4 + p] = acc[k][p];
+  __syncthreads();
+  float *dstw = a.ws + (size_t)blockIdx.x * a.H;
+  for (int j = threadIdx.x; j < a.H; j += blockDim.x) {
+    float sum = 0.f;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) sum += part[g * a.H + j];
+    dstw[j] = sum;
   }
 }
 
@@ -615,6 +755,24 @@ cudaError_t bwd_pipe_v(const BwdParams<T, Idx> &k, const RmsNormBwdArgs &a, cons
   return launch_dw_reduce(a, P, s);
 }
 
+template <typename Idx, int V, bool HAS_RSTD, bool ADD>
+cudaError_t bwd_lean_v(const BwdParams<bf16, Idx> &k, const RmsNormBwdArgs &a,
+                       const DeviceInfo &dev, cudaStream_t s) {
+  auto kern = rmsnorm_bwd_lean<Idx, V, HAS_RSTD, ADD>;
+  constexpr size_t smem = bwd_lean_smem<V, ADD>();
+  static_assert(smem >= sizeof(float) * 8 * 32 * V * 8, "the ring holds the [8][H] partials");
+  // the grid must not depend on whether rstd is saved (dw's summation order)
+  const int occ = min_blocks_per_sm((const void *)rmsnorm_bwd_lean<Idx, V, true, ADD>,
+                                    (const void *)rmsnorm_bwd_lean<Idx, V, false, ADD>, 256,
+                                    smem, dev);
+  int64_t P = ceil_div(a.T, (int64_t)8);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  if (P > a.ws_rows) P = a.ws_rows;
+  cudaError_t e = launch_pdl(kern, dim3((unsigned)P), dim3(256), smem, s, k);
+  if (e != cudaSuccess) return e;
+  return launch_dw_reduce(a, P, s);
+}
+
 template <typename T, typename Idx, int N, bool HAS_RSTD, bool ADD>
 cudaError_t bwd_planned(const RowPlan &p, const StagedPlan *sp, const BwdParams<T, Idx> &k,
                         const RmsNormBwdArgs &a, const DeviceInfo &dev, cudaStream_t s) {
@@ -659,6 +817,17 @@ cudaError_t bwd_typed(bool vec, const RmsNormBwdArgs &a, const DeviceInfo &dev,
   // rows of one or two warps' plan: the per-warp cp.async pipeline (not
   // with the residual gradient: its third input costs the registers of a
   // second CTA per SM, and the staged ring measured faster there)
+  if constexpr (sizeof(T) == 2) {  // bf16 rows of one warp: the lean form (the forward's order)
+    if (vec && p.W == 1) {
+      switch (p.V) {
+        case 1: return bwd_lean_v<Idx, 1, HAS_RSTD, ADD>(k, a, dev, s);
+        case 2: return bwd_lean_v<Idx, 2, HAS_RSTD, ADD>(k, a, dev, s);
+        case 3: return bwd_lean_v<Idx, 3, HAS_RSTD, ADD>(k, a, dev, s);
+        case 4: return bwd_lean_v<Idx, 4, HAS_RSTD, ADD>(k, a, dev, s);
+        default: break;
+      }
+    }
+  }
   if constexpr (!ADD) {
     if (vec && p.W == 1) {
       switch (p.V) {

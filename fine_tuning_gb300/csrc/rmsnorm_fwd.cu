@@ -22,6 +22,7 @@
 // (rmsnorm_fwd_rows); rows too long for either take a CTA-per-row kernel.
 #include "common.cuh"
 #include "launch.h"
+#include "rmsnorm_lean.cuh"
 
 namespace ftk {
 
@@ -414,6 +415,112 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_pipe(const FwdParams<T, Idx> 
   cp_async_wait<0>();
 }
 
+// bf16 rows of one warp (H <= 1,024, 16-byte aligned): rmsnorm_fwd_pipe's
+// persistent grid and per-warp cp.async ring, with the lean arithmetic of
+// rmsnorm_lean.cuh: the weights are unpacked to fp32 pairs once per warp,
+// each packet once per row, every product is a pair instruction, and the
+// ring and row addresses advance as running pointers.  With ADD the ring
+// holds the x and res rows; h = x + res is added in fp32 pairs, rounded,
+// stored, and the norm runs on the stored h, so y and r equal the plain
+// lean norm of that h bit for bit.  Lane l owns packets l + 32 k (k < V).
+template <bool ADD> constexpr int lean_fwd_bufs() { return ADD ? 3 : 4; }
+
+// Three CTAs per SM; two with ADD, whose rows carry twice the bytes and
+// whose packets would not fit three CTAs' registers.
+template <typename Idx, int V, bool ADD>
+__global__ void __launch_bounds__(256, ADD ? 2 : 3) rmsnorm_fwd_lean(const FwdParams<bf16, Idx> a) {
+  constexpr int kBufs = lean_fwd_bufs<ADD>();
+  constexpr int kSl = (ADD ? 2 : 1) * V;  // x (, res) packets per lane per row
+  extern __shared__ uint4 ring[];        // [warps][kBufs][kSl][32]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint4 *const my = ring + warp * (kBufs * kSl * 32) + lane;
+  pdl_wait();
+  pdl_trigger();
+  bool on[V];
+  float2 wf[V][4];
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    on[k] = lane + 32 * k < a.hp;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (on[k]) u = *reinterpret_cast<const uint4 *>(a.w + (lane + 32 * k) * 8);
+    unpack8(u, wf[k]);
+  }
+  const Idx step = (Idx)gridDim.x * 8;
+  Idx row = (Idx)blockIdx.x * 8 + warp;
+  // the next row to stage, its source addresses and its ring slot
+  Idx srow = row;
+  const bf16 *src = a.x + row * a.ldx + lane * 8;
+  const bf16 *srs = ADD ? a.res + row * a.ldr + lane * 8 : nullptr;
+  const Idx src_step = step * a.ldx, srs_step = ADD ? step * a.ldr : 0;
+  int sslot = 0;
+  auto stage = [&]() {
+    if (srow < a.rows) {
+      uint4 *d = my + sslot * (kSl * 32);
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        if (on[k]) {
+          cp_async16(d + k * 32, src + k * 256);
+          if (ADD) cp_async16(d + (V + k) * 32, srs + k * 256);
+        }
+      }
+    }
+    cp_async_commit();  // one group per row on every lane, empty or not
+    srow += step;
+    src += src_step;
+    if (ADD) srs += srs_step;
+    sslot = sslot + 1 == kBufs ? 0 : sslot + 1;
+  };
+#pragma unroll
+  for (int i = 0; i < kBufs - 1; ++i) stage();
+  bf16 *dst = a.y + row * a.ldy + lane * 8;
+  bf16 *dsth = ADD ? a.h + row * a.ldh + lane * 8 : nullptr;
+  const Idx dst_step = step * a.ldy, dsth_step = ADD ? step * a.ldh : 0;
+  int slot = 0;
+  while (row < a.rows) {  // warp-uniform
+    stage();                    // the next rows' loads fly meanwhile
+    cp_async_wait<kBufs - 1>();  // this lane's copies of `row` have landed
+    const uint4 *d = my + slot * (kSl * 32);
+    float2 xf[V][4];
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      uint4 u = make_uint4(0u, 0u, 0u, 0u);
+      if (on[k]) u = d[k * 32];
+      if (ADD) {
+        // h = x + res in fp32, rounded once; the norm sees the stored h
+        float2 rf[4];
+        unpack8(on[k] ? d[(V + k) * 32] : make_uint4(0u, 0u, 0u, 0u), rf);
+        unpack8(u, xf[k]);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) xf[k][p] = __fadd2_rn(xf[k][p], rf[p]);
+        u = pack8(xf[k]);
+        if (on[k]) *reinterpret_cast<uint4 *>(dsth + k * 256) = u;
+      }
+      unpack8(u, xf[k]);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) lean_sumsq_step(acc, xf[k][p]);
+    }
+    const float ss = warp_sum(lean_lane_total(acc));
+    const float r = rsqrtf(fmaf(ss, a.inv_h, a.eps));
+    if (a.rstd != nullptr && lane == 0) a.rstd[row] = r;
+    const float2 r2 = make_float2(r, r);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      if (on[k]) {
+        float2 o[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) o[p] = __fmul2_rn(__fmul2_rn(xf[k][p], r2), wf[k][p]);
+        *reinterpret_cast<uint4 *>(dst + k * 256) = pack8(o);
+      }
+    }
+    row += step;
+    dst += dst_step;
+    if (ADD) dsth += dsth_step;
+    slot = slot + 1 == kBufs ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+}
+
 // Rows longer than the register plan: one CTA per row (grid-stride over
 // rows), sum of squares first (writing h when ADD), then a second pass that
 // re-reads the row (from L2).
@@ -467,6 +574,19 @@ cudaError_t fwd_pipe_v(const FwdParams<T, Idx> &k, const DeviceInfo &dev, cudaSt
   auto kern = rmsnorm_fwd_pipe<T, Idx, N, V, W, ADD>;
   const size_t smem =
       sizeof(uint4) * 8 * FwdPipe<W, V, ADD>::kBufs * FwdPipe<W, V, ADD>::kSl * 32;  // 8 warps
+  const int occ = blocks_per_sm((const void *)kern, 256, smem, dev, 8);
+  int64_t P = ceil_div((int64_t)k.rows, (int64_t)8);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  cudaError_t le = launch_pdl(kern, dim3((unsigned)P), dim3(256), smem, s, k);
+  if (le != cudaSuccess) return le;
+  return cudaGetLastError();
+}
+
+template <typename Idx, int V, bool ADD>
+cudaError_t fwd_lean_v(const FwdParams<bf16, Idx> &k, const DeviceInfo &dev, cudaStream_t s) {
+  auto kern = rmsnorm_fwd_lean<Idx, V, ADD>;
+  const size_t smem =
+      sizeof(uint4) * 8 * lean_fwd_bufs<ADD>() * (ADD ? 2 : 1) * V * 32;  // 8 warps
   const int occ = blocks_per_sm((const void *)kern, 256, smem, dev, 8);
   int64_t P = ceil_div((int64_t)k.rows, (int64_t)8);
   if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
@@ -529,7 +649,20 @@ cudaError_t fwd_typed(bool vec, const RmsNormFwdArgs &a, const DeviceInfo &dev, 
     return cudaGetLastError();
   }
   // Rows of one warp's plan, and (without the residual) of two warps' plan:
-  // the per-warp cp.async pipeline at every batch size.
+  // the per-warp cp.async pipeline at every batch size; bf16 rows of one
+  // warp take its lean form, with or without the residual (the backward's
+  // recomputation of r follows the same order).
+  if constexpr (sizeof(T) == 2) {
+    if (vec && p.W == 1) {
+      switch (p.V) {
+        case 1: return fwd_lean_v<Idx, 1, ADD>(k, dev, s);
+        case 2: return fwd_lean_v<Idx, 2, ADD>(k, dev, s);
+        case 3: return fwd_lean_v<Idx, 3, ADD>(k, dev, s);
+        case 4: return fwd_lean_v<Idx, 4, ADD>(k, dev, s);
+        default: break;
+      }
+    }
+  }
   if (vec && p.W == 1) {
     switch (p.V) {
       case 1: return fwd_pipe_v<T, Idx, NV, 1, 1, ADD>(k, dev, s);

@@ -1,0 +1,55 @@
+// Pieces shared by the lean RMSNorm kernels for bf16 rows of one warp
+// (rmsnorm_fwd_lean, rmsnorm_bwd_lean): bf16 <-> fp32 pairs and the row's
+// sum of squares in the order both kernels must share.
+//
+// Those kernels do all fp32 arithmetic on pairs (Blackwell's two-wide fp32
+// multiply and fused multiply-add; each half is rounded exactly like the
+// scalar instruction), unpack each bf16 once and pack two per conversion,
+// which halves the instruction count per row against scalar code: rows of
+// ~1 K features are too short for memory latency alone to hide a heavy
+// instruction stream.
+#pragma once
+
+#include "common.cuh"
+
+namespace ftk {
+
+namespace {
+
+// The two bf16 of a 32-bit word as an fp32 pair (exact: bf16 is the top half
+// of an fp32).
+__device__ __forceinline__ float2 bf2_unpack(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+// An fp32 pair rounded to nearest even, two bf16 in one word.
+__device__ __forceinline__ uint32_t bf2_pack(float2 v) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float2 (&f)[4]) {
+  f[0] = bf2_unpack(u.x);
+  f[1] = bf2_unpack(u.y);
+  f[2] = bf2_unpack(u.z);
+  f[3] = bf2_unpack(u.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float2 (&f)[4]) {
+  return make_uint4(bf2_pack(f[0]), bf2_pack(f[1]), bf2_pack(f[2]), bf2_pack(f[3]));
+}
+
+// The lean row order of sum_j x_j^2: each lane runs one pair chain over its
+// packets in column order (even columns in .x, odd in .y, each step a fused
+// multiply-add), adds the pair's halves, and the warp adds the lanes with
+// the xor butterfly.  The forward and the backward's recomputation both go
+// through these two functions, so a recomputed r equals the saved one bit for
+// bit.
+__device__ __forceinline__ void lean_sumsq_step(float2 &acc, float2 x) {
+  acc = __ffma2_rn(x, x, acc);
+}
+__device__ __forceinline__ float lean_lane_total(float2 acc) { return acc.x + acc.y; }
+
+}  // namespace
+
+}  // namespace ftk

@@ -62,7 +62,7 @@ __device__ __forceinline__ void rope_cos_sin(int p, float fhi, float flo, float 
 // `cu` is a generic pointer: the CTA's shared-memory copy when it fits,
 // else the device array itself.
 template <typename Idx>
-__device__ __forceinline__ int position_of(Idx t, const int32_t *cu, int B) {
+__device__ __forceinline__ int sequence_of(Idx t, const int32_t *cu, int B) {
   int lo = 1, hi = B;  // first i in [1, B] with cu[i] > t
   while (lo <= hi) {
     const int mid = (lo + hi) >> 1;
@@ -71,8 +71,13 @@ __device__ __forceinline__ int position_of(Idx t, const int32_t *cu, int B) {
     else
       hi = mid - 1;
   }
-  int b = lo - 1;
-  b = b < 0 ? 0 : (b > B - 1 ? B - 1 : b);
+  const int b = lo - 1;
+  return b < 0 ? 0 : (b > B - 1 ? B - 1 : b);
+}
+
+template <typename Idx>
+__device__ __forceinline__ int position_of(Idx t, const int32_t *cu, int B) {
+  const int b = sequence_of<Idx>(t, cu, B);
   return (int)(t - (Idx)cu[b]);
 }
 

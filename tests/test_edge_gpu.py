@@ -273,6 +273,8 @@ def rope_case(lens, Hq, Hkv, D, theta, dtype, seed=40):
     ((20, 20), 5, 3, 512),                 # widest head
     ((20011,), 6, 2, 64),                  # many passes per warp, ragged last pass
     (tuple((i * 7) % 9 for i in range(2100)), 4, 2, 64),  # > 2,047 sequences: bounds via L1
+    ((0, 0, 5, 0, 30000, 0, 7, 0), 14, 2, 64),  # empty sequences at both ends; each warp's
+                                                # run of tokens starts mid-sequence
 ])
 def test_rope_shapes(dtype, lens, Hq, Hkv, D):
     theta = 1e4
