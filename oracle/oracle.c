@@ -256,11 +256,15 @@ static int64_t position_of(int64_t t, const int32_t *cu, int32_t B)
  *   (v_i, v_{i+D/2}) <- (v_i cos phi - v_{i+D/2} sin phi,
  *                        v_{i+D/2} cos phi + v_i sin phi)
  * sign = -1 rotates by -phi (the transpose, used by the backward pass).
- * Condition scale of each output: its two terms, where cos phi and sin phi
- * each count with their sensitivity to the angle reduced to [-pi, pi]
- * (|cos| + |phi_r sin| and |sin| + |phi_r cos|): no finite-precision angle
- * is exact, and near cos phi = 0 the output moves with the angle even
- * though the term itself is ~0. */
+ * Condition scale of each output: its two terms' magnitudes, plus
+ * ANGLE_WEIGHT times its sensitivity to the angle (the derivative's terms,
+ * |v_i sin| + |v_{i+D/2} cos| for the first output): no finite-precision
+ * angle is exact, and near cos phi = 0 an output still moves by |v| per
+ * radian of angle error although its own terms are ~0.  The weight is the
+ * angle error allowed (1e-6 rad, the accuracy a GPU angle formed in
+ * extended precision reaches at every position below 524,288) over the
+ * relative bar the scale is multiplied by in fp32 (1e-5). */
+#define ANGLE_WEIGHT 0.1
 static void rotate_head(const double *v, double *out, double *scale,
                         int64_t p, int32_t D, const double *inv_freq, int sign)
 {
@@ -272,8 +276,8 @@ static void rotate_head(const double *v, double *out, double *scale,
         out[i] = a * c - b * s;
         out[i + half] = b * c + a * s;
         if (scale) {
-            double r = fabs(remainder(phi, 6.283185307179586476925));
-            double cc = fabs(c) + r * fabs(s), ss = fabs(s) + r * fabs(c);
+            double cc = fabs(c) + ANGLE_WEIGHT * fabs(s);
+            double ss = fabs(s) + ANGLE_WEIGHT * fabs(c);
             scale[i] = fabs(a) * cc + fabs(b) * ss;
             scale[i + half] = fabs(b) * cc + fabs(a) * ss;
         }

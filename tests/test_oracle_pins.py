@@ -301,8 +301,31 @@ def test_rope_scale_bounds_output_and_is_unchanged_by_it():
     np.testing.assert_array_equal(ko, ks_)
     assert np.all(np.abs(qo) <= qsc * (1 + 1e-12))
     assert np.all(np.abs(ko) <= ksc * (1 + 1e-12))
-    # at a token's own position 0 the scale is the plain |x| (no angle)
-    np.testing.assert_allclose(qsc[0], np.abs(q[0]), rtol=1e-15)
+
+
+def test_rope_scale_covers_the_angle_sensitivity_of_the_complex_product():
+    # D = 2 is multiplication by e^{i p} (inv_freq = theta^0 = 1), whose
+    # derivative in the angle is i times the product: the real output moves
+    # by |Im| per radian and the imaginary one by |Re|.  The scale must hold
+    # each output's magnitude plus a tenth of that motion (a 1e-6 rad angle
+    # error against the 1e-5 fp32 relative bar), and with the angle error
+    # that large the perturbed product must stay inside the fp32 bar.
+    rng = np.random.default_rng(5)
+    T = 4000
+    q = rng.standard_normal((T, 1, 2))
+    cu = [0, T]
+    qo, _, qsc, _ = oracle.qk_rope(q, np.zeros((T, 0, 2)), cu, 1e4, scales=True)
+    z = (q[:, 0, 0] + 1j * q[:, 0, 1]) * np.exp(1j * np.arange(T))
+    re, im = qo[:, 0, 0], qo[:, 0, 1]
+    np.testing.assert_allclose(re + 1j * im, z, atol=1e-12)
+    assert np.all(qsc[:, 0, 0] >= (np.abs(re) + 0.1 * np.abs(im)) * (1 - 1e-12))
+    assert np.all(qsc[:, 0, 1] >= (np.abs(im) + 0.1 * np.abs(re)) * (1 - 1e-12))
+    zp = (q[:, 0, 0] + 1j * q[:, 0, 1]) * np.exp(1j * (np.arange(T) + 1e-6))
+    assert np.all(np.abs(zp.real - re) <= 1e-5 * qsc[:, 0, 0] + 1e-15)
+    assert np.all(np.abs(zp.imag - im) <= 1e-5 * qsc[:, 0, 1] + 1e-15)
+    # an angle error ten times larger falls outside it somewhere
+    zb = (q[:, 0, 0] + 1j * q[:, 0, 1]) * np.exp(1j * (np.arange(T) + 1e-5))
+    assert np.any(np.abs(zb.real - re) > 1e-5 * qsc[:, 0, 0])
 
 
 def test_rope_sampled_rows_equal_full():

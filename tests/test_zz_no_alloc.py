@@ -6,8 +6,8 @@ caller workspace.
 
 Each GPU case makes two calls in a row through the C ABI (the second one
 finds the first one's leftovers in the shared scratch) and compares both
-against ftk_rmsnorm_bwd with a workspace, within the parity tolerance of
-the other tests.  This file is named to be collected last, so a run that
+against ftk_rmsnorm_bwd with a workspace and against the double-precision
+oracle, within the parity tolerance of the other tests.  This file is named to be collected last, so a run that
 stops at its first failure has already run every other test; it also
 passes on its own in a fresh process.
 """
@@ -76,7 +76,11 @@ def test_matches_workspace_version_two_calls_in_a_row(lib, dtype, T, H, with_rst
         dx_new, dw_new = noalloc(lib, dy, x, w, r, eps)
         dx_ref, dw_ref = ftk.rmsnorm_bwd(dy, x, w, r, eps)
         torch.cuda.synchronize()
-        _, _, dxs, dws = oracle.rmsnorm_bwd(dy.cpu(), x.cpu(), w.cpu(), eps, scales=True)
+        dxo, dwo, dxs, dws = oracle.rmsnorm_bwd(dy.cpu(), x.cpu(), w.cpu(), eps, scales=True)
+        # against the entry point that takes a workspace ...
         assert_close(f"dx call {call}", dx_new, dx_ref.double().cpu().numpy(), dxs, dtype=code)
         assert_close(f"dw call {call}", dw_new, dw_ref.double().cpu().numpy(), dws, dtype=code,
                      kind="dw")
+        # ... and against the double-precision oracle's own values
+        assert_close(f"dx call {call} vs oracle", dx_new, dxo, dxs, dtype=code)
+        assert_close(f"dw call {call} vs oracle", dw_new, dwo, dws, dtype=code, kind="dw")
