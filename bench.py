@@ -113,13 +113,15 @@ def tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-_ROPE = ("qk_rope.cu", "rope_common.cuh")
-KERNEL_SOURCES = {"rmsnorm_fwd": ("rmsnorm_fwd.cu",),
-                  "rmsnorm_bwd": ("rmsnorm_bwd.cu", "rmsnorm_bwd.cuh", "dw_reduce.cuh"),
+_ROPE = ("qk_rope.cu", "rope_common.cuh", "rmsnorm_lean.cuh")
+KERNEL_SOURCES = {"rmsnorm_fwd": ("rmsnorm_fwd.cu", "rmsnorm_lean.cuh"),
+                  "rmsnorm_bwd": ("rmsnorm_bwd.cu", "rmsnorm_bwd.cuh", "dw_reduce.cuh",
+                                  "rmsnorm_lean.cuh"),
                   "swiglu_fwd": ("swiglu.cu",), "swiglu_bwd": ("swiglu.cu",),
                   "qk_rope_fwd": _ROPE, "qk_rope_bwd": _ROPE,
-                  "rmsnorm_add_fwd": ("rmsnorm_fwd.cu",),
-                  "rmsnorm_add_bwd": ("rmsnorm_add_bwd.cu", "rmsnorm_bwd.cuh", "dw_reduce.cuh"),
+                  "rmsnorm_add_fwd": ("rmsnorm_fwd.cu", "rmsnorm_lean.cuh"),
+                  "rmsnorm_add_bwd": ("rmsnorm_add_bwd.cu", "rmsnorm_bwd.cuh", "dw_reduce.cuh",
+                                      "rmsnorm_lean.cuh"),
                   "swiglu_bwd_h": ("swiglu.cu",), "qk_rope_freq_fwd": _ROPE,
                   "qk_norm_rope_fwd": ("qk_norm_rope.cu", "rope_common.cuh", "dw_reduce.cuh"),
                   "qk_norm_rope_bwd": ("qk_norm_rope.cu", "rope_common.cuh", "dw_reduce.cuh")}
@@ -523,17 +525,53 @@ def kernel_entry(name, ms, ib, toks, hbm, src):
             "tokens_per_s": round(toks / (ms * 1e-3), 1), "ideal_bytes": ib}
 
 
-def time_batch(batch, flush, K, Kk, dev, world=1):
+def copy_ops(batch, ib):
+    """For each step op, a trivial streaming kernel over the same algorithmic
+    bytes (half read, half written) at the same size: an elementwise fp32
+    multiply by one, dst = src * 1, run on the SMs like the op (a device
+    memcpy may take other engines and paths).  What bandwidth a kernel with
+    no arithmetic reaches at this size, beside the op's own."""
+    import torch
+    dev = batch.inputs["x"].device
+    # fp32 words, sizes rounded to 64 KiB (below 0.2% of any op's bytes)
+    words = [max(1, ib[k] // 2 // 65536) * 16384 for k in OPS]
+    src = torch.empty(max(words), dtype=torch.float32, device=dev)
+    dst = torch.empty(max(words), dtype=torch.float32, device=dev)
+    src.fill_(0.5)
+    return [(lambda n=n: torch.mul(src[:n], 1.0, out=dst[:n])) for n in words], (src, dst)
+
+
+def hold_gpu(ms=20.0):
+    """Keeps the device busy for about `ms` so that the host enqueues the
+    timed graphs ahead of it: no host submission gap lands inside a timed
+    pair of events."""
+    import torch
+    torch.cuda._sleep(int(ms * 2.1e6))  # cycles at ~2.1 GHz
+
+
+def time_batch(batch, flush, K, Kk, dev, world=1, with_reference=True):
     """The step as one CUDA graph replayed K times (CUDA events around each
     replay), then each op as a graph [L2 flush, op] beside a graph [L2
-    flush], Kk repetitions.  Returns (step ms per replay, per-op ms,
-    (t0, t1) of the step region, (t1, t2) of the per-kernel region)."""
+    flush], Kk repetitions.  With `with_reference`, the same repetitions
+    also time an empty op (a one-element fill: the launch gap every op's
+    time includes) and, per op, a device copy of its algorithmic bytes.
+    Returns (step ms per replay, per-op ms, (t0, t1) of the step region,
+    (t1, t2) of the per-kernel region, the flush graph, references)."""
     import torch
     import torch.distributed as dist
-    ops = batch.ops()
+
+    from fine_tuning_gb300 import workloads as W
+    ops = list(batch.ops())
+    n_ops = len(ops)
+    refs = {}
+    keep = None
+    if with_reference:
+        tiny = torch.empty(1, dtype=torch.float32, device=dev)
+        copies, keep = copy_ops(batch, W.ideal_bytes(batch.wl))
+        ops += [lambda: tiny.fill_(1.0)] + copies
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        for op in ops:
+        for op in ops[:n_ops]:
             op()
     op_graphs = []
     for op in ops:
@@ -566,6 +604,7 @@ def time_batch(batch, flush, K, Kk, dev, world=1):
     if world > 1:
         dist.barrier()
     t1 = time.time()
+    hold_gpu()
     for i in range(Kk):
         for (a, b), g in zip(evk[i], op_graphs + [flush_graph]):
             a.record()
@@ -574,13 +613,30 @@ def time_batch(batch, flush, K, Kk, dev, world=1):
     torch.cuda.synchronize(dev)
     t2 = time.time()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    per_op = [op_ms([e[j] for e in evk], [e[-1] for e in evk]) for j in range(len(ops))]
-    return step_ms, per_op, (t0, t1), (t1, t2), flush_graph
+    per = [op_ms([e[j] for e in evk], [e[-1] for e in evk]) for j in range(len(ops))]
+    if with_reference:
+        refs = {"launch_gap_ms": per[n_ops], "copy_ms": per[n_ops + 1:]}
+    del keep
+    return step_ms, per[:n_ops], (t0, t1), (t1, t2), flush_graph, refs
 
 
-def per_workload_leg(names, flush, K, Kk, dev, hbm, src, sampler):
+def add_references(kernels, refs, ib):
+    """Per kernel: the launch gap its time includes, and the same-size copy."""
+    if not refs:
+        return
+    gap = refs["launch_gap_ms"]
+    for j, name in enumerate(OPS):
+        c = refs["copy_ms"][j]
+        k = kernels[name]
+        k["launch_gap_us"] = round(gap * 1e3, 2)
+        k["copy_same_bytes_us"] = round(c * 1e3, 2)
+        k["frac_of_same_size_copy"] = round(c * 1e3 / k["us"], 4)
+
+
+def per_workload_leg(names, flush, K, Kk, dev, hbm, src, sampler, with_ext=True):
     """The smaller workloads, each timed like the main one (step graph and
-    one-op graphs) after its own sampled parity check, in the same run."""
+    one-op graphs, and the widened ops) after its own sampled parity check,
+    in the same run."""
     import torch
 
     from fine_tuning_gb300 import workloads as W
@@ -598,12 +654,13 @@ def per_workload_leg(names, flush, K, Kk, dev, hbm, src, sampler):
             flush.fill_(1)
             for op in b.ops():
                 op()
-        step_ms, per_op, _, (k0, k1), _ = time_batch(b, flush, K, Kk, dev)
+        step_ms, per_op, _, (k0, k1), fg, refs = time_batch(b, flush, K, Kk, dev)
         ib, toks = W.ideal_bytes(wl), W.tokens_per_call(wl)
         step_bytes = sum(ib[k] for k in OPS)
         ms = sum(step_ms) / len(step_ms)
         kern = {n: kernel_entry(n, per_op[j], ib[n], toks[n], hbm, src)
                 for j, n in enumerate(OPS)}
+        add_references(kern, refs, ib)
         dom = max(range(len(OPS)), key=lambda j: per_op[j])
         out[name] = {
             "T": wl.T, "B": int(len(b.cu_host) - 1), "H": wl.H, "I": wl.I, "Hq": wl.Hq,
@@ -613,7 +670,13 @@ def per_workload_leg(names, flush, K, Kk, dev, hbm, src, sampler):
             "tokens_per_s": round(wl.T / (ms * 1e-3), 1), "kernels": kern,
             "dominant": {"kernel": OPS[dom], "traffic": ncu_traffic(OPS[dom], wl.name)},
             "parity": par, "clocks_kernel_leg": sampler.summary(k0, k1)}
-        del b
+        if with_ext:
+            ext = ext_leg(b, flush, fg, dev, Kk, hbm, src)
+            out[name]["extensions"] = {n: {f: v[f] for f in ("us", "GB_s", "frac_of_measured_hbm"
+                                                              if src == "measured" else
+                                                              "frac_of_fallback_hbm")}
+                                       for n, v in ext.items() if isinstance(v, dict)}
+        del b, fg
         torch.cuda.empty_cache()
     return out
 
@@ -668,14 +731,15 @@ def run_ours(args):
         pass
     sampler = ClockSampler(uuid).start()
     time.sleep(0.6)
-    step_ms, per_op, (t0, t1), (k0, k1), flush_graph = time_batch(batch, flush, K, Kk, dev,
-                                                                  world)
+    step_ms, per_op, (t0, t1), (k0, k1), flush_graph, refs = time_batch(batch, flush, K, Kk,
+                                                                        dev, world)
     el_max, bytes_all = reduce_timing(sum(step_ms) / 1e3, step_bytes * K)
     _, tok_all = reduce_timing(0.0, float(wl.T) * K)
     value = bytes_all / el_max / 1e9
     hbm, src = peaks()
     toks = W.tokens_per_call(wl)
     kernels = {n: kernel_entry(n, per_op[j], ib[n], toks[n], hbm, src) for j, n in enumerate(OPS)}
+    add_references(kernels, refs, ib)
     dom = max(range(len(OPS)), key=lambda j: per_op[j])
     dname = OPS[dom]
     achieved = ib[dname] / (per_op[dom] * 1e-3) / 1e9
@@ -705,7 +769,10 @@ def run_ours(args):
         "timing": (f"step: {K} replays of a CUDA graph of the step's {LAUNCHES_PER_STEP} "
                    f"launches, CUDA events around each replay; per kernel: the median over {Kk} "
                    "replays of a graph [L2 flush, op] minus the same repetition's graph [L2 flush], "
-                   "CUDA events around each"),
+                   "CUDA events around each, enqueued behind a sleep kernel so no host submission "
+                   "gap falls inside; launch_gap_us is an empty one-element op timed the same way "
+                   "(included in every op's us); copy_same_bytes_us an elementwise kernel (fp32 "
+                   "x 1) reading and writing the op's algorithmic bytes at the same size"),
         "wall_ms_timed_region": round((t1 - t0) * 1e3, 3),
     }
     out["clocks"] = sampler.summary(t0, t1)
@@ -719,8 +786,10 @@ def run_ours(args):
     if rank == 0:
         names = [n for n in args.per_workload.split(",") if n and n != "none" and n != wl.name]
         if names:
-            out["per_workload"] = per_workload_leg(names, flush, K, Kk, dev, hbm, src, sampler)
-            out["gpu_launches_all_legs"] += len(names) * LAUNCHES_PER_STEP * (K + Kk)
+            out["per_workload"] = per_workload_leg(names, flush, K, Kk, dev, hbm, src, sampler,
+                                                   with_ext=not args.no_ext)
+            out["gpu_launches_all_legs"] += len(names) * (LAUNCHES_PER_STEP * (K + Kk) + (
+                0 if args.no_ext else sum(EXT_OPS.values()) * Kk))
         if not args.no_ext and not args.no_cce:
             c0 = time.time()
             out["cce"] = cce_leg(dev, flush, flush_graph, max(3, min(Kk, 20)))
@@ -800,6 +869,7 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
     torch.cuda.synchronize(dev)
     ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(reps)] for n in list(graphs) + ["flush"]}
+    hold_gpu()
     for k in range(reps):
         for n, g in list(graphs.items()) + [("flush", flush_graph)]:
             a, b = ev[n][k]
@@ -855,6 +925,7 @@ def cce_leg(dev, flush, flush_graph, reps):
     torch.cuda.synchronize(dev)
     ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(reps)] for n in list(graphs) + ["flush"]}
+    hold_gpu()
     for k in range(reps):
         for n, gr in list(graphs.items()) + [("flush", flush_graph)]:
             a, b = ev[n][k]
@@ -886,32 +957,72 @@ def cce_leg(dev, flush, flush_graph, reps):
 
 
 class HostBuffers:
-    """Page-locked host tensors of exactly the requested sizes: plain host
-    allocations registered with cudaHostRegister (torch's pinned allocator
-    rounds each allocation up to a power of two, which at the 524k-token
-    shapes would cost tens of GB of host memory).  Falls back to torch's
-    pinned allocator where the runtime call is unavailable."""
+    """Page-locked host tensors of exactly the requested sizes, from
+    cudaHostAlloc through the CUDA runtime the process already loaded
+    (torch's pinned allocator rounds each allocation up to a power of two,
+    which at the 524k-token shapes would cost ~92 GB of host memory instead of
+    80).  Falls back to registering a plain host allocation
+    (cudaHostRegister; slower on this host when both directions copy at
+    once), then to torch's pinned allocator."""
 
     def __init__(self):
-        self.registered = []
+        self.allocated = []   # (ptr, cudart) to free with cudaFreeHost
+        self.registered = []  # tensors to unregister
+        self.rt = self._runtime()
+
+    @staticmethod
+    def _runtime():
+        import ctypes
+        for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+            try:
+                rt = ctypes.CDLL(name)
+                rt.cudaHostAlloc.restype = ctypes.c_int
+                rt.cudaHostAlloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t,
+                                             ctypes.c_uint]
+                rt.cudaFreeHost.restype = ctypes.c_int
+                rt.cudaFreeHost.argtypes = [ctypes.c_void_p]
+                return rt
+            except (OSError, AttributeError):
+                continue
+        return None
 
     def empty(self, shape, dtype):
+        import ctypes
+
         import torch
+        nbytes = int(torch.empty(0, dtype=dtype).element_size())
+        for d in shape:
+            nbytes *= int(d)
+        if self.rt is not None and nbytes:
+            ptr = ctypes.c_void_p()
+            if self.rt.cudaHostAlloc(ctypes.byref(ptr), nbytes, 0) == 0 and ptr.value:
+                buf = (ctypes.c_ubyte * nbytes).from_address(ptr.value)
+                t = torch.frombuffer(buf, dtype=torch.uint8).view(dtype).view(*shape)
+                if t.is_pinned():
+                    self.allocated.append(ptr.value)
+                    return t
+                self.rt.cudaFreeHost(ptr.value)
         t = torch.empty(shape, dtype=dtype)
         rt = getattr(torch.cuda, "cudart", None)
         if rt is not None and t.numel():
             t.zero_()  # fault the pages in (OpenMP threads) before locking them
-            err = rt().cudaHostRegister(t.data_ptr(), t.numel() * t.element_size(), 0)
-            if int(err) == 0:
+            if int(rt().cudaHostRegister(t.data_ptr(), t.numel() * t.element_size(), 0)) == 0:
                 self.registered.append(t)
                 return t
         return t.pin_memory()
+
+    def kind(self):
+        return ("cudaHostAlloc" if self.allocated else
+                "cudaHostRegister" if self.registered else "torch pinned")
 
     def release(self):
         import torch
         for t in self.registered:
             torch.cuda.cudart().cudaHostUnregister(t.data_ptr())
         self.registered = []
+        for p in self.allocated:
+            self.rt.cudaFreeHost(p)
+        self.allocated = []
 
 
 def e2e_leg(batch, ops, dev, steps, step_bytes):
@@ -980,8 +1091,9 @@ def e2e_leg(batch, ops, dev, steps, step_bytes):
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(z) / steps
     del sets[1], set_ops[1]
-    hb.release()
+    kind = hb.kind()
     del host_in, host_out
+    hb.release()
     el_max, bytes_all = reduce_timing(ms * steps / 1e3, step_bytes * steps)
     return {"value": round(bytes_all / el_max / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(el_max * 1e3 / steps, 3), "steps": steps,
@@ -989,7 +1101,8 @@ def e2e_leg(batch, ops, dev, steps, step_bytes):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "copy_GB_s": round((h2d + d2h) / (el_max / steps) / 1e9, 1),
             "overlap": "3 streams: copy-in of step k+1, kernels of step k, copy-out of step k-1; "
-                       "two device buffer sets; host buffers page-locked at exact size"}
+                       "two device buffer sets",
+            "host_buffers": f"page-locked at exact size ({kind})"}
 
 
 # ------------------------------------------------------ packing (host)
