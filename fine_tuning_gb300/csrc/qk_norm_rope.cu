@@ -32,6 +32,7 @@
 #include "common.cuh"
 #include "dw_reduce.cuh"
 #include "launch.h"
+#include "rmsnorm_lean.cuh"
 #include "rope_common.cuh"
 
 namespace ftk {
@@ -220,6 +221,159 @@ qk_norm_rope_fwd_pipe(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
       }
     }
     advance(t, p);
+    b = b + 1 == kFwdBufs ? 0 : b + 1;
+  }
+  cp_async_wait<0>();
+}
+
+// bf16 heads whose half is 8 NV values, NV a power of two dividing 32: the
+// lean form of qk_norm_rope_fwd_pipe, as qk_rope_lean is of qk_rope_pipe:
+// the same token order (warp w of G takes tokens w, w + G, ...), the weighted
+// rotation table laid out for fp32 pairs and the rotation on pairs.  A head's sum of squares
+// keeps the scalar order of the other forms, so r (saved, or recomputed by
+// the backward) is the same bits, and every output is rounded exactly like
+// qk_norm_rope_fwd_pipe's: the two kernels agree bit for bit.
+// Shared memory: per warp four tables of 4 NV entries, for lane j's column
+// pair m (columns 8 j + 2 m and 8 j + 2 m + 1) at m NV + j:
+//   0: (A, A', B, B') for Q   1: (C, C', E, E') for Q   2, 3: the same for K
+// with (A, B, C, E) = (w1 cos, w2 sin, w2 cos, w1 sin) of the column (primed:
+// the pair's second column); then the per-warp staging ring.
+template <int NV> constexpr size_t fwd_lean_tab_bytes() {
+  return sizeof(float4) * kWarps * 4 * 4 * NV;
+}
+
+constexpr int kFwdLeanBlocks = 3;  // CTAs per SM the lean forward is compiled for
+
+template <typename Idx, int NV>
+__global__ void __launch_bounds__(kThreads, kFwdLeanBlocks)
+qk_norm_rope_fwd_lean(const NormRopeParams<bf16, Idx> a, const __grid_constant__ RopeFreqs fr) {
+  constexpr int N = 8, half = N * NV, D = 2 * half, S = 32 / NV;
+  extern __shared__ float4 dyn[];
+  __shared__ float2 freq[half];
+  __shared__ float wf[4][half];  // wq first half, wq second, wk first, wk second
+  __shared__ int32_t cu_s[kCuInShared];
+  const int NH = a.Hq + a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = lane % NV, slot = lane / NV;
+  float4 *const tab = dyn + warp * 4 * 4 * NV;  // [4][4 NV]
+  uint4 *const stg = reinterpret_cast<uint4 *>(dyn + kWarps * 4 * 4 * NV) +
+                     warp * (kFwdBufs * kFwdSlots * 32) + lane;
+
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    wf[0][i] = a.Hq > 0 ? to_float(a.wq[i]) : 0.f;
+    wf[1][i] = a.Hq > 0 ? to_float(a.wq[half + i]) : 0.f;
+    wf[2][i] = a.Hkv > 0 ? to_float(a.wk[i]) : 0.f;
+    wf[3][i] = a.Hkv > 0 ? to_float(a.wk[half + i]) : 0.f;
+  }
+  const bool cu_staged = a.B < kCuInShared;
+  if (cu_staged)
+    for (int i = threadIdx.x; i <= a.B; i += blockDim.x) cu_s[i] = __ldg(a.cu + i);
+  __syncthreads();  // the frequency, weight and boundary tables; no block barrier follows
+  const int32_t *bounds = cu_staged ? cu_s : a.cu;
+
+  // this warp's tokens: t, t + G, ... below rows
+  const Idx G = (Idx)gridDim.x * kWarps;
+  Idx t = (Idx)blockIdx.x * kWarps + warp;
+  if (t >= a.rows) return;
+  const int passes = (NH + S - 1) / S;
+
+  Idx t2 = t;
+  int p2 = 0, b2 = 0;
+  const bf16 *q2 = a.q + t2 * a.ld_q + j * N, *k2 = a.k + t2 * a.ld_k + j * N - (Idx)a.Hq * D;
+  auto stage = [&]() {
+    const int h = slot + p2 * S;
+    if (t2 < a.rows && h < NH) {
+      const bf16 *v = (h < a.Hq ? q2 : k2) + (Idx)h * D;
+      uint4 *d = stg + b2 * (kFwdSlots * 32);
+      cp_async16(d, v);
+      cp_async16(d + 32, v + half);
+    }
+    cp_async_commit();  // one group per pass on every lane, empty or not
+    if (++p2 == passes) {
+      p2 = 0;
+      t2 += G;
+      q2 += G * a.ld_q;
+      k2 += G * a.ld_k;
+    }
+    b2 = b2 + 1 == kFwdBufs ? 0 : b2 + 1;
+  };
+#pragma unroll
+  for (int i = 0; i < kFwdBufs - 1; ++i) stage();
+
+  bf16 *oqr = a.oq + t * a.ld_oq + j * N, *okr = a.ok + t * a.ld_ok + j * N - (Idx)a.Hq * D;
+  int p = 0, b = 0;
+  while (t < a.rows) {  // warp-uniform
+    stage();
+    if (p == 0) {
+      const int pos = position_of<Idx>(t, bounds, a.B);
+      __syncwarp();  // the previous token's tables have been read
+      float *tf = reinterpret_cast<float *>(tab);
+#pragma unroll
+      for (int i = lane; i < half; i += 32) {
+        const float2 f = freq[i];
+        float c, sn;
+        rope_cos_sin(pos, f.x, f.y, &c, &sn);
+        const int at = 4 * (((i % N) >> 1) * NV + i / N) + (i & 1);
+        tf[at] = wf[0][i] * c;                          // Q: A
+        tf[at + 2] = wf[1][i] * sn;                     // Q: B
+        tf[4 * 4 * NV + at] = wf[1][i] * c;             // Q: C
+        tf[4 * 4 * NV + at + 2] = wf[0][i] * sn;        // Q: E
+        tf[2 * 4 * 4 * NV + at] = wf[2][i] * c;         // K: A
+        tf[2 * 4 * 4 * NV + at + 2] = wf[3][i] * sn;    // K: B
+        tf[3 * 4 * 4 * NV + at] = wf[3][i] * c;         // K: C
+        tf[3 * 4 * 4 * NV + at + 2] = wf[2][i] * sn;    // K: E
+      }
+      __syncwarp();
+    }
+    cp_async_wait<kFwdBufs - 1>();  // this lane's copies for (t, p) have landed
+    const int h = slot + p * S;
+    const bool act = h < NH, isq = h < a.Hq;
+    float2 xa[4], xb[4];
+    float ss = 0.f;
+    if (act) {
+      const uint4 *d = stg + b * (kFwdSlots * 32);
+      unpack8(d[0], xa);
+      unpack8(d[32], xb);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {  // the scalar order of the other forms, column by column
+        ss = fmaf(xa[m].x, xa[m].x, fmaf(xb[m].x, xb[m].x, ss));
+        ss = fmaf(xa[m].y, xa[m].y, fmaf(xb[m].y, xb[m].y, ss));
+      }
+    }
+    ss = slot_sum(ss, NV);  // every lane takes part
+    if (act) {
+      const float r = rsqrtf(fmaf(ss, a.inv_d, a.eps));
+      const float2 r2 = make_float2(r, r);
+      const float4 *tab_ab = tab + (isq ? 0 : 2) * 4 * NV + j;
+      const float4 *tab_ce = tab_ab + 4 * NV;
+      uint32_t o1[4], o2[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float4 ab = tab_ab[m * NV], ce = tab_ce[m * NV];
+        const float2 A2 = make_float2(ab.x, ab.y), B2 = make_float2(ab.z, ab.w);
+        const float2 C2 = make_float2(ce.x, ce.y), E2 = make_float2(ce.z, ce.w);
+        const float2 bB = __fmul2_rn(xb[m], B2), aE = __fmul2_rn(xa[m], E2);
+        // r (a A - b B) and r (b C + a E), each fma rounded once as in the scalar form
+        o1[m] = bf2_pack(__fmul2_rn(r2, __ffma2_rn(xa[m], A2, make_float2(-bB.x, -bB.y))));
+        o2[m] = bf2_pack(__fmul2_rn(r2, __ffma2_rn(xb[m], C2, aE)));
+      }
+      bf16 *dst = (isq ? oqr : okr) + (Idx)h * D;
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+      *reinterpret_cast<uint4 *>(dst + half) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+      if (j == 0) {
+        if (isq && a.rq) a.rq[t * a.Hq + h] = r;
+        if (!isq && a.rk) a.rk[t * a.Hkv + (h - a.Hq)] = r;
+      }
+    }
+    if (++p == passes) {
+      p = 0;
+      t += G;
+      oqr += G * a.ld_oq;
+      okr += G * a.ld_ok;
+    }
     b = b + 1 == kFwdBufs ? 0 : b + 1;
   }
   cp_async_wait<0>();
@@ -575,10 +729,35 @@ NormRopeParams<T, Idx> params_of(const QkNormRopeArgs &a) {
 
 cudaError_t finish_launch(cudaError_t e) { return e != cudaSuccess ? e : cudaGetLastError(); }
 
+template <typename Idx, int NV>
+cudaError_t fwd_lean_launch(const QkNormRopeArgs &a, const RopeFreqs &fr, const DeviceInfo &dev,
+                            cudaStream_t s) {
+  auto kern = qk_norm_rope_fwd_lean<Idx, NV>;
+  const size_t smem = fwd_lean_tab_bytes<NV>() + kFwdStageBytes;
+  const int occ = blocks_per_sm((const void *)kern, kThreads, smem, dev, kFwdLeanBlocks);
+  int64_t P = ceil_div(a.T, (int64_t)kWarps);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  return finish_launch(launch_pdl(kern, dim3((unsigned)P), dim3(kThreads), smem, s,
+                                  params_of<bf16, Idx>(a), fr));
+}
+
 template <typename T, typename Idx>
 cudaError_t fwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &fr,
                       const DeviceInfo &dev, cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
+  if constexpr (sizeof(T) == 2) {
+    if (warp_path) {
+      switch (a.D / 2 / NV) {
+        case 1: return fwd_lean_launch<Idx, 1>(a, fr, dev, s);
+        case 2: return fwd_lean_launch<Idx, 2>(a, fr, dev, s);
+        case 4: return fwd_lean_launch<Idx, 4>(a, fr, dev, s);
+        case 8: return fwd_lean_launch<Idx, 8>(a, fr, dev, s);
+        case 16: return fwd_lean_launch<Idx, 16>(a, fr, dev, s);
+        case 32: return fwd_lean_launch<Idx, 32>(a, fr, dev, s);
+        default: break;
+      }
+    }
+  }
   if (warp_path) {
     auto kern = qk_norm_rope_fwd_pipe<T, Idx, NV>;
     const size_t smem = sizeof(float4) * (size_t)kWarps * 2 * (a.D / 2) + kFwdStageBytes;

@@ -530,13 +530,13 @@ qk_rope_pipe(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, int
 
 // bf16 heads whose half is 8 NV values, NV a power of two dividing 32 (D =
 // 16 .. 512): the lean form of qk_rope_pipe, with the same per-warp
-// cp.async ring of head passes and the same (cos, sin) table per token.
-// Each warp owns a contiguous run of tokens (the persistent grid splits the
-// batch evenly), so a token's sequence comes from one search at the run's
-// start and a walk over the boundaries after it, not a search per token;
-// the rotation runs on fp32 pairs, each half rounded exactly like the scalar
+// cp.async ring of head passes, the same (cos, sin) table per token and the
+// same token order (warp w of G takes tokens w, w + G, ...: the grid sweeps
+// the batch one contiguous window at a time, which measured 1-2.5% faster on
+// every workload than giving each warp a contiguous run of tokens).  The
+// rotation runs on fp32 pairs, each half rounded exactly like the scalar
 // fma(a, c, -(b s)) of qk_rope_pipe, so the two kernels agree bit for bit;
-// the row addresses advance per token.  The table entry of lane (slot, j)
+// row addresses advance by G rows per token.  The table entry of lane (slot, j)
 // for columns 8 j + 2 m, 8 j + 2 m + 1 holds (cos, cos, sgn sin, sgn sin)
 // at m NV + j, so the NV lanes of a head read consecutive 16-byte entries.
 template <typename Idx, int NV>
@@ -564,11 +564,10 @@ qk_rope_lean(bf16 *q, Idx ld_q, bf16 *k, Idx ld_k, const int32_t *__restrict__ c
   __syncthreads();  // the frequency table and the boundaries; no block barrier follows
   const int32_t *bounds = cu_staged ? cu_s : cu;
 
-  // this warp's run of tokens [t, t_end)
-  const int64_t G = (int64_t)gridDim.x * kWarps, gw = (int64_t)blockIdx.x * kWarps + warp;
-  Idx t = (Idx)((int64_t)rows * gw / G);
-  const Idx t_end = (Idx)((int64_t)rows * (gw + 1) / G);
-  if (t >= t_end) return;
+  // this warp's tokens: t, t + G, ... below rows
+  const Idx G = (Idx)gridDim.x * kWarps;
+  Idx t = (Idx)blockIdx.x * kWarps + warp;
+  if (t >= rows) return;
   const int passes = (NH + S - 1) / S;  // head passes per token, the same on every lane
 
   // the stager runs kPipeBufs - 1 passes ahead with its own row pointers
@@ -577,7 +576,7 @@ qk_rope_lean(bf16 *q, Idx ld_q, bf16 *k, Idx ld_k, const int32_t *__restrict__ c
   const bf16 *q2 = q + t2 * ld_q + j * N, *k2 = k + t2 * ld_k + j * N - (Idx)Hq * D;
   auto stage = [&]() {
     const int h = slot + p2 * S;
-    if (t2 < t_end && h < NH) {
+    if (t2 < rows && h < NH) {
       const bf16 *v = (h < Hq ? q2 : k2) + (Idx)h * D;
       uint4 *d = stg + b2 * 64;
       cp_async16(d, v);
@@ -586,29 +585,21 @@ qk_rope_lean(bf16 *q, Idx ld_q, bf16 *k, Idx ld_k, const int32_t *__restrict__ c
     cp_async_commit();  // one group per pass on every lane, empty or not
     if (++p2 == passes) {
       p2 = 0;
-      ++t2;
-      q2 += ld_q;
-      k2 += ld_k;
+      t2 += G;
+      q2 += G * ld_q;
+      k2 += G * ld_k;
     }
     b2 = b2 + 1 == kPipeBufs ? 0 : b2 + 1;
   };
 #pragma unroll
   for (int i = 0; i < kPipeBufs - 1; ++i) stage();
 
-  // the sequence of the run's first token, then a walk over the boundaries
-  int sb = sequence_of<Idx>(t, bounds, B);
-  Idx seq_start = (Idx)bounds[sb], seq_next = (Idx)bounds[sb + 1];
   bf16 *qr = q + t * ld_q + j * N, *kr = k + t * ld_k + j * N - (Idx)Hq * D;
   int p = 0, b = 0;
-  while (t < t_end) {  // warp-uniform
+  while (t < rows) {  // warp-uniform
     stage();  // the next passes' loads fly meanwhile
     if (p == 0) {
-      while (sb < B - 1 && t >= seq_next) {  // skips empty sequences too
-        ++sb;
-        seq_start = seq_next;
-        seq_next = (Idx)bounds[sb + 1];
-      }
-      const int pos = (int)(t - seq_start);
+      const int pos = position_of<Idx>(t, bounds, B);
       __syncwarp();  // the previous token's table has been read
       float *tf = reinterpret_cast<float *>(tab);
 #pragma unroll
@@ -644,9 +635,9 @@ qk_rope_lean(bf16 *q, Idx ld_q, bf16 *k, Idx ld_k, const int32_t *__restrict__ c
     }
     if (++p == passes) {
       p = 0;
-      ++t;
-      qr += ld_q;
-      kr += ld_k;
+      t += G;
+      qr += G * ld_q;
+      kr += G * ld_k;
     }
     b = b + 1 == kPipeBufs ? 0 : b + 1;
   }
