@@ -571,6 +571,188 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   write_partial<N>(acc, part, a.ws, D, NV, j, lane, warp);
 }
 
+// bf16 heads whose half is 8 NV values, NV a power of two dividing 32: the
+// lean form of qk_norm_rope_bwd_warp (same token order, staging and
+// reductions), with the inverse rotation, the norm's gradient and the dw sums
+// on fp32 pairs and the norm weights as fp32 in shared memory.  sum v^2 (r
+// recomputed) keeps the forward's scalar order, so a recomputed r equals the
+// saved one bit for bit; sum dn w v runs as one pair chain per lane.
+// Shared memory: [warps][4 NV] float4 (cos, cos', -sin, -sin') of lane j's
+// column pair m at m NV + j; then [warps][2D] fp32 partials; then the
+// per-warp staging ring.
+template <int NV> constexpr size_t bwd_lean_tab_bytes() { return sizeof(float4) * kWarps * 4 * NV; }
+
+template <typename Idx, int NV, bool HAS_RSTD>
+__global__ void __launch_bounds__(kThreads, 2)
+qk_norm_rope_bwd_lean(const NormRopeParams<bf16, Idx> a, const __grid_constant__ RopeFreqs fr) {
+  constexpr int N = 8, half = N * NV, D = 2 * half, S = 32 / NV;
+  extern __shared__ float4 dyn[];
+  __shared__ float2 freq[half];
+  __shared__ float wfl[4][half];  // wq first half, wq second, wk first, wk second
+  __shared__ int32_t cu_s[kCuInShared];
+  const int NH = a.Hq + a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = lane % NV, slot = lane / NV;
+  float4 *const tab = dyn + warp * 4 * NV;
+  float *const part = reinterpret_cast<float *>(dyn + kWarps * 4 * NV);  // [warps][2D]
+  uint4 *const stg = reinterpret_cast<uint4 *>(part + kWarps * 2 * D) +
+                     warp * (kBwdBufs * kBwdSlots * 32) + lane;
+
+  for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
+  pdl_wait();
+  pdl_trigger();
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    wfl[0][i] = a.Hq > 0 ? to_float(a.wq[i]) : 0.f;
+    wfl[1][i] = a.Hq > 0 ? to_float(a.wq[half + i]) : 0.f;
+    wfl[2][i] = a.Hkv > 0 ? to_float(a.wk[i]) : 0.f;
+    wfl[3][i] = a.Hkv > 0 ? to_float(a.wk[half + i]) : 0.f;
+  }
+  const bool cu_staged = a.B < kCuInShared;
+  if (cu_staged)
+    for (int i = threadIdx.x; i <= a.B; i += blockDim.x) cu_s[i] = __ldg(a.cu + i);
+  __syncthreads();  // the frequency, weight and boundary tables
+  const int32_t *bounds = cu_staged ? cu_s : a.cu;
+
+  float2 acc[4][4];  // dwq first half, dwq second half, dwk first half, dwk second half
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) acc[g][m] = make_float2(0.f, 0.f);
+
+  // tokens t, t + G, ... (every warp runs the loop, then the CTA combines)
+  const Idx G = (Idx)gridDim.x * kWarps;
+  Idx t = (Idx)blockIdx.x * kWarps + warp;
+  const int passes = (NH + S - 1) / S;
+  Idx t2 = t;
+  int p2 = 0, b2 = 0;
+  auto stage = [&]() {
+    const int h = slot + p2 * S;
+    if (t2 < a.rows && h < NH) {
+      const bool isq = h < a.Hq;
+      const int hk = h - a.Hq;
+      const bf16 *gp =
+          (isq ? a.gq + t2 * a.ld_gq + (Idx)h * D : a.gk + t2 * a.ld_gk + (Idx)hk * D) + j * N;
+      const bf16 *vp =
+          (isq ? a.q + t2 * a.ld_q + (Idx)h * D : a.k + t2 * a.ld_k + (Idx)hk * D) + j * N;
+      uint4 *d = stg + b2 * (kBwdSlots * 32);
+      cp_async16(d, gp);
+      cp_async16(d + 32, gp + half);
+      cp_async16(d + 64, vp);
+      cp_async16(d + 96, vp + half);
+      if (HAS_RSTD) cp_async4(d + 128, isq ? a.rq + t2 * a.Hq + h : a.rk + t2 * a.Hkv + hk);
+    }
+    cp_async_commit();  // one group per pass on every lane, empty or not
+    if (++p2 == passes) {
+      p2 = 0;
+      t2 += G;
+    }
+    b2 = b2 + 1 == kBwdBufs ? 0 : b2 + 1;
+  };
+#pragma unroll
+  for (int i = 0; i < kBwdBufs - 1; ++i) stage();
+  int p = 0, b = 0;
+  while (t < a.rows) {  // warp-uniform
+    stage();
+    if (p == 0) {
+      const int pos = position_of<Idx>(t, bounds, a.B);
+      __syncwarp();  // the previous token's table has been read
+      float *tf = reinterpret_cast<float *>(tab);
+#pragma unroll
+      for (int i = lane; i < half; i += 32) {
+        const float2 f = freq[i];
+        float cv, sn;
+        rope_cos_sin(pos, f.x, f.y, &cv, &sn);
+        const int at = 4 * (((i % N) >> 1) * NV + i / N) + (i & 1);
+        tf[at] = cv;
+        tf[at + 2] = -sn;
+      }
+      __syncwarp();
+    }
+    cp_async_wait<kBwdBufs - 1>();  // this lane's copies for (t, p) have landed
+    const int h = slot + p * S;
+    const bool act = h < NH, isq = h < a.Hq;
+    const uint4 *d = stg + b * (kBwdSlots * 32);
+    float2 dn1[4], dn2[4], v1[4], v2[4];
+    float r = 0.f, ss = 0.f;
+    float2 c2 = make_float2(0.f, 0.f);
+    const float *w1s = wfl[isq ? 0 : 2] + j * N, *w2s = wfl[isq ? 1 : 3] + j * N;
+    if (act) {
+      float2 g1[4], g2[4];
+      unpack8(d[0], g1);
+      unpack8(d[32], g2);
+      unpack8(d[64], v1);
+      unpack8(d[96], v2);
+      if (HAS_RSTD) r = *reinterpret_cast<const float *>(d + 128);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float4 cs = tab[m * NV + j];
+        const float2 C2 = make_float2(cs.x, cs.y), NS2 = make_float2(cs.z, cs.w);
+        // the rotation by -phi: dn1 = g1 cos + g2 sin, dn2 = g2 cos - g1 sin
+        const float2 t1 = __fmul2_rn(g2[m], NS2), t2 = __fmul2_rn(g1[m], NS2);
+        dn1[m] = __ffma2_rn(g1[m], C2, make_float2(-t1.x, -t1.y));
+        dn2[m] = __ffma2_rn(g2[m], C2, t2);
+        const float2 W1 = *reinterpret_cast<const float2 *>(w1s + 2 * m);
+        const float2 W2 = *reinterpret_cast<const float2 *>(w2s + 2 * m);
+        c2 = __ffma2_rn(__fmul2_rn(dn1[m], W1), v1[m],
+                        __ffma2_rn(__fmul2_rn(dn2[m], W2), v2[m], c2));
+        if (!HAS_RSTD) {  // the forward's order, column by column
+          ss = fmaf(v1[m].x, v1[m].x, fmaf(v2[m].x, v2[m].x, ss));
+          ss = fmaf(v1[m].y, v1[m].y, fmaf(v2[m].y, v2[m].y, ss));
+        }
+      }
+    }
+    float cx = c2.x + c2.y;
+    if (HAS_RSTD) {
+      cx = slot_sum(cx, NV);
+    } else {
+      const float2 cs = slot_sum2(make_float2(cx, ss), NV);
+      cx = cs.x;
+      ss = cs.y;
+    }
+    if (act) {
+      if (!HAS_RSTD) r = rsqrtf(fmaf(ss, a.inv_d, a.eps));
+      const float am = r * r * r * cx * a.inv_d;
+      const float2 r2 = make_float2(r, r), nam2 = make_float2(-am, -am);
+      // fixed accumulator indices (a runtime index would put acc in local
+      // memory): a q head adds to 0 and 1, a k head to 2 and 3
+      const float2 rq2 = isq ? r2 : make_float2(0.f, 0.f), rk2 = isq ? make_float2(0.f, 0.f) : r2;
+      uint32_t o1[4], o2[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float2 W1 = *reinterpret_cast<const float2 *>(w1s + 2 * m);
+        const float2 W2 = *reinterpret_cast<const float2 *>(w2s + 2 * m);
+        // dv = r w dn - r^3 v c / D;  dw += dn v r
+        o1[m] = bf2_pack(__ffma2_rn(nam2, v1[m], __fmul2_rn(__fmul2_rn(r2, W1), dn1[m])));
+        o2[m] = bf2_pack(__ffma2_rn(nam2, v2[m], __fmul2_rn(__fmul2_rn(r2, W2), dn2[m])));
+        const float2 p1 = __fmul2_rn(dn1[m], v1[m]), q1 = __fmul2_rn(dn2[m], v2[m]);
+        acc[0][m] = __ffma2_rn(p1, rq2, acc[0][m]);
+        acc[1][m] = __ffma2_rn(q1, rq2, acc[1][m]);
+        acc[2][m] = __ffma2_rn(p1, rk2, acc[2][m]);
+        acc[3][m] = __ffma2_rn(q1, rk2, acc[3][m]);
+      }
+      bf16 *dst = (isq ? a.oq + t * a.ld_oq + (Idx)h * D
+                       : a.ok + t * a.ld_ok + (Idx)(h - a.Hq) * D) + j * N;
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+      *reinterpret_cast<uint4 *>(dst + half) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+    }
+    if (++p == passes) {
+      p = 0;
+      t += G;
+    }
+    b = b + 1 == kBwdBufs ? 0 : b + 1;
+  }
+  cp_async_wait<0>();
+  float accf[4][N];
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      accf[g][2 * m] = acc[g][m].x;
+      accf[g][2 * m + 1] = acc[g][m].y;
+    }
+  write_partial<N>(accf, part, a.ws, D, NV, j, lane, warp);
+}
+
 // Element-wise forms: one warp per token, heads one after another, lane i
 // owning the pairs i, i + 32, ... of every head.
 template <typename T, typename Idx>
@@ -773,10 +955,53 @@ cudaError_t fwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &
                                   smem, s, params_of<T, Idx>(a), fr));
 }
 
+template <typename Idx, int NV>
+cudaError_t bwd_lean_launch(const QkNormRopeArgs &a, const RopeFreqs &fr, const DeviceInfo &dev,
+                            cudaStream_t s) {
+  const size_t smem = bwd_lean_tab_bytes<NV>() + sizeof(float) * (size_t)kWarps * 2 * a.D +
+                      kBwdStageBytes;
+  const bool rstd = a.rq != nullptr || a.rk != nullptr;
+  // the grid (and with it the order of dwq's and dwk's sums) must not depend
+  // on whether r is saved: size it for the less resident of the two forms
+  const int occ_s = blocks_per_sm((const void *)qk_norm_rope_bwd_lean<Idx, NV, true>, kThreads,
+                                  smem, dev, kMaxBlocksPerSm);
+  const int occ_r = blocks_per_sm((const void *)qk_norm_rope_bwd_lean<Idx, NV, false>, kThreads,
+                                  smem, dev, kMaxBlocksPerSm);
+  const int occ = occ_s < occ_r ? occ_s : occ_r;
+  int64_t P = ceil_div(a.T, (int64_t)kWarps);
+  if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
+  if (P > a.ws_rows) P = a.ws_rows;
+  const NormRopeParams<bf16, Idx> k = params_of<bf16, Idx>(a);
+  const dim3 grid((unsigned)P), block(kThreads);
+  cudaError_t e = rstd ? launch_pdl(qk_norm_rope_bwd_lean<Idx, NV, true>, grid, block, smem, s,
+                                    k, fr)
+                       : launch_pdl(qk_norm_rope_bwd_lean<Idx, NV, false>, grid, block, smem, s,
+                                    k, fr);
+  if (e != cudaSuccess) return e;
+  if (a.dwq || a.dwk) {
+    e = launch_dw_reduce(a.ws, P, 2 * (int64_t)a.D, 2 * (int64_t)a.D, a.dwq, a.D, a.dwk, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaGetLastError();
+}
+
 template <typename T, typename Idx>
 cudaError_t bwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &fr,
                       const DeviceInfo &dev, cudaStream_t s) {
   constexpr int NV = VecWidth<T>::value;
+  if constexpr (sizeof(T) == 2) {
+    if (warp_path) {
+      switch (a.D / 2 / NV) {
+        case 1: return bwd_lean_launch<Idx, 1>(a, fr, dev, s);
+        case 2: return bwd_lean_launch<Idx, 2>(a, fr, dev, s);
+        case 4: return bwd_lean_launch<Idx, 4>(a, fr, dev, s);
+        case 8: return bwd_lean_launch<Idx, 8>(a, fr, dev, s);
+        case 16: return bwd_lean_launch<Idx, 16>(a, fr, dev, s);
+        case 32: return bwd_lean_launch<Idx, 32>(a, fr, dev, s);
+        default: break;
+      }
+    }
+  }
   const size_t smem = sizeof(float2) * (size_t)kWarps * (a.D / 2) +
                       sizeof(float) * (size_t)kWarps * 2 * a.D + (warp_path ? kBwdStageBytes : 0);
   const bool rstd = a.rq != nullptr || a.rk != nullptr;

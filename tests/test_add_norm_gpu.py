@@ -106,6 +106,9 @@ def test_add_norm_524k_sampled():
     (5, 20000, 0),      # row too long for registers: CTA-per-row kernels
     (300, 5120, 0),     # multi-warp rows
     (4000, 2048, 0),    # enough rows for the staged pipeline
+    (999, 768, 0),      # one-warp rows of three packets per lane (bf16)
+    (513, 256, 0),      # one-warp rows of one packet per lane (bf16)
+    (3001, 512, 0),     # one-warp rows of two packets per lane (bf16), many rows per warp
 ])
 def test_add_norm_shapes(dtype, T, H, skew):
     eps = 1e-6

@@ -74,6 +74,8 @@ def code(dtype):
     (3, 8, 0),          # tiny rows
     (4099, 512, 0),     # rows of one warp, many rows per warp (pipelined kernels)
     (2053, 1024, 0),    # one-warp rows of four packets per lane (bf16)
+    (999, 768, 0),      # one-warp rows of three packets per lane (bf16)
+    (513, 256, 0),      # one-warp rows of one packet per lane (bf16)
     (1027, 2048, 0),    # two-warp rows (bf16), ragged T
     (5, 2048, 0),       # fewer rows than row groups
 ])
@@ -103,7 +105,7 @@ def test_rmsnorm_shapes(dtype, T, H, skew):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("T,H", [(37, 896), (29, 900), (4099, 512), (2053, 1024), (1027, 2048),
-                                 (300, 5120), (5, 20000)])
+                                 (300, 5120), (5, 20000), (999, 768), (513, 256)])
 def test_rmsnorm_bwd_rstd_modes_agree(dtype, T, H):
     # dx and dw are the same bits whether rstd is saved or recomputed: the
     # recomputed rstd repeats the forward's sum, and the grid (so dw's
@@ -273,8 +275,9 @@ def rope_case(lens, Hq, Hkv, D, theta, dtype, seed=40):
     ((20, 20), 5, 3, 512),                 # widest head
     ((20011,), 6, 2, 64),                  # many passes per warp, ragged last pass
     (tuple((i * 7) % 9 for i in range(2100)), 4, 2, 64),  # > 2,047 sequences: bounds via L1
-    ((0, 0, 5, 0, 30000, 0, 7, 0), 14, 2, 64),  # empty sequences at both ends; each warp's
-                                                # run of tokens starts mid-sequence
+    ((0, 0, 5, 0, 30000, 0, 7, 0), 14, 2, 64),  # empty sequences at both ends
+    ((100, 0, 211), 8, 4, 32),             # half a head over two lanes (bf16)
+    ((77, 50), 4, 2, 256),                 # half a head over sixteen lanes (bf16)
 ])
 def test_rope_shapes(dtype, lens, Hq, Hkv, D):
     theta = 1e4

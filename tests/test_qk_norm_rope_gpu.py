@@ -123,6 +123,8 @@ def test_524k_sampled():
     ((40,), 6, 0, 64),                     # Q only
     ((40,), 0, 3, 64),                     # K only
     ((9,), 2, 1, 512),                     # the largest head
+    ((60, 41), 4, 4, 32),                  # half a head over two lanes (bf16)
+    ((31, 2, 19), 3, 1, 256),              # half a head over sixteen lanes (bf16)
     (tuple((i * 5) % 7 for i in range(2100)), 3, 1, 64),  # > 2,047 sequences: bounds via L1
 ])
 def test_shapes(dtype, lens, Hq, Hkv, D):
