@@ -404,3 +404,37 @@ def test_bounded_wait_times_out_and_reports():
     dx, dw = ftk.rmsnorm_bwd(x, x, w, None, 1e-6)
     torch.cuda.synchronize()
     assert torch.isfinite(y.float()).all() and ftk.device_status() == 0
+
+
+@pytest.mark.parametrize("T,H", [
+    (8000, 2304),   # three warps' plan, three packets per lane
+    (8000, 3072),   # three warps, four packets
+    (8000, 4096),   # four warps (Qwen3-8B rows)
+    (4000, 5120),   # five warps (Qwen3-32B rows)
+    (4000, 6144),   # six warps
+    (4000, 7680),   # eight warps
+])
+def test_rmsnorm_multi_warp_rows_large_batch(T, H):
+    # bf16 rows of three or more warps in batches large enough for the
+    # TMA-staged kernels in both directions: the saved r must equal the one
+    # the backward recomputes bit for bit (the same summation plan), and both
+    # directions must match the oracle.
+    eps = 1e-6
+    x, dy = randn((T, H), torch.bfloat16, 91), randn((T, H), torch.bfloat16, 92)
+    w = (1 + 0.1 * randn((H,), torch.float32, 93)).to(torch.bfloat16)
+    yg, rg = Guarded((T, H), torch.bfloat16), Guarded((T,), torch.float32)
+    ftk.rmsnorm_fwd(x, w, eps, y=yg.t, rstd=rg.t)
+    dx1, dw1 = ftk.rmsnorm_bwd(dy, x, w, rg.t, eps)
+    dx2, dw2 = ftk.rmsnorm_bwd(dy, x, w, None, eps)
+    torch.cuda.synchronize()
+    yg.check()
+    rg.check()
+    assert torch.equal(dx1, dx2) and torch.equal(dw1, dw2)
+    rows = np.unique(np.concatenate([np.arange(3), np.arange(T - 3, T),
+                                     np.random.default_rng(H).choice(T, 58, replace=False)]))
+    ri = torch.as_tensor(rows, device=DEV)
+    yr, rr = oracle.rmsnorm_fwd(x[ri].cpu(), w.cpu(), eps)
+    assert_close("y", yg.t[ri], yr, dtype="bf16")
+    assert_close("rstd", rg.t[ri], rr, dtype="f32")
+    dxr, _, dxs, _ = oracle.rmsnorm_bwd(dy[ri].cpu(), x[ri].cpu(), w.cpu(), eps, scales=True)
+    assert_close("dx", dx1[ri], dxr, dxs, dtype="bf16")
