@@ -113,15 +113,15 @@ def tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-_ROPE = ("qk_rope.cu", "rope_common.cuh", "rmsnorm_lean.cuh")
-KERNEL_SOURCES = {"rmsnorm_fwd": ("rmsnorm_fwd.cu", "rmsnorm_lean.cuh"),
+_ROPE = ("qk_rope.cu", "rope_common.cuh", "pair_math.cuh")
+KERNEL_SOURCES = {"rmsnorm_fwd": ("rmsnorm_fwd.cu", "pair_math.cuh"),
                   "rmsnorm_bwd": ("rmsnorm_bwd.cu", "rmsnorm_bwd.cuh", "dw_reduce.cuh",
-                                  "rmsnorm_lean.cuh"),
+                                  "pair_math.cuh"),
                   "swiglu_fwd": ("swiglu.cu",), "swiglu_bwd": ("swiglu.cu",),
                   "qk_rope_fwd": _ROPE, "qk_rope_bwd": _ROPE,
-                  "rmsnorm_add_fwd": ("rmsnorm_fwd.cu", "rmsnorm_lean.cuh"),
+                  "rmsnorm_add_fwd": ("rmsnorm_fwd.cu", "pair_math.cuh"),
                   "rmsnorm_add_bwd": ("rmsnorm_add_bwd.cu", "rmsnorm_bwd.cuh", "dw_reduce.cuh",
-                                      "rmsnorm_lean.cuh"),
+                                      "pair_math.cuh"),
                   "swiglu_bwd_h": ("swiglu.cu",), "qk_rope_freq_fwd": _ROPE,
                   "qk_norm_rope_fwd": ("qk_norm_rope.cu", "rope_common.cuh", "dw_reduce.cuh"),
                   "qk_norm_rope_bwd": ("qk_norm_rope.cu", "rope_common.cuh", "dw_reduce.cuh")}
@@ -1025,12 +1025,33 @@ class HostBuffers:
         self.allocated = []
 
 
+COPY_CHUNK = 1 << 30  # bytes per host<->device copy piece in the e2e leg
+
+
+def chunked_copy(dst, src, streams, k0=0):
+    """dst.copy_(src) in pieces of at most COPY_CHUNK bytes dealt round-robin
+    over `streams` (one host<->device copy of several GB runs slower than the
+    same bytes in 1 GB pieces on two streams: 297 against 340 GB/s at 16 GB,
+    both directions busy, measured on the GPU host).  Returns the next
+    stream index."""
+    import torch
+    d = dst.reshape(-1).view(torch.uint8)
+    s = src.reshape(-1).view(torch.uint8)
+    k = k0
+    for a in range(0, d.numel(), COPY_CHUNK):
+        with torch.cuda.stream(streams[k % len(streams)]):
+            d[a:a + COPY_CHUNK].copy_(s[a:a + COPY_CHUNK], non_blocking=True)
+        k += 1
+    return k
+
+
 def e2e_leg(batch, ops, dev, steps, step_bytes):
     """The step through the public API with host buffers: every step copies
     all of its inputs in from page-locked host memory and all of its outputs
-    back.  As a user would run consecutive steps, three streams overlap
-    step k+1's copy-in, step k's kernels and step k-1's copy-out, with two
-    device-side buffer sets; events order every reuse of a buffer."""
+    back.  As a user would run consecutive steps, step k+1's copy-in, step
+    k's kernels and step k-1's copy-out overlap (two copy streams per
+    direction, one compute stream), with two device-side buffer sets; events
+    order every reuse of a buffer."""
     import torch
     wl = batch.wl
     sets = [batch, Batch(wl, dev)]
@@ -1047,41 +1068,55 @@ def e2e_leg(batch, ops, dev, steps, step_bytes):
     host_out = {k: hb.empty(v.shape, v.dtype) for k, v in outs(batch).items()}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
-    s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    s_in = [torch.cuda.Stream(dev) for _ in range(2)]
+    s_out = [torch.cuda.Stream(dev) for _ in range(2)]
+    s_run = torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event(enable_timing=False)
+
+    def mark(streams):
+        out = []
+        for st in streams:
+            e = ev()
+            e.record(st)
+            out.append(e)
+        return out
 
     def run(n, t0=None):
         done_run = [None, None]   # last compute on each set
-        done_out = [None, None]   # last copy-out of each set
-        last = None
+        done_out = [None, None]   # last copy-out of each set (one event per stream)
         for i in range(n):
             j = i & 1
             b = sets[j]
-            with torch.cuda.stream(s_in):
+            for st in s_in:
                 if done_run[j] is not None:
-                    s_in.wait_event(done_run[j])   # inputs of set j no longer read
-                if i == 0 and t0 is not None:
-                    t0.record(s_in)
-                for k, v in host_in.items():
-                    b.inputs[k].copy_(v, non_blocking=True)
-                e_in = ev()
-                e_in.record(s_in)
+                    st.wait_event(done_run[j])   # inputs of set j no longer read
+            if i == 0 and t0 is not None:
+                s_in[1].wait_stream(s_in[0])
+                t0.record(s_in[0])
+                s_in[1].wait_event(t0)
+            k = 0
+            for name, v in host_in.items():
+                k = chunked_copy(b.inputs[name], v, s_in, k)
+            e_in = mark(s_in)
+            for e in e_in:
+                s_run.wait_event(e)
+            if done_out[j] is not None:
+                for e in done_out[j]:
+                    s_run.wait_event(e)        # outputs of set j already copied out
             with torch.cuda.stream(s_run):
-                s_run.wait_event(e_in)
-                if done_out[j] is not None:
-                    s_run.wait_event(done_out[j])  # outputs of set j already copied out
                 for op in set_ops[j]:
                     op()
-                done_run[j] = ev()
-                done_run[j].record(s_run)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(done_run[j])
-                for k, v in outs(b).items():
-                    host_out[k].copy_(v, non_blocking=True)
-                done_out[j] = ev()
-                done_out[j].record(s_out)
-                last = s_out
-        return last
+            done_run[j] = ev()
+            done_run[j].record(s_run)
+            for st in s_out:
+                st.wait_event(done_run[j])
+            k = 0
+            for name, v in outs(b).items():
+                k = chunked_copy(host_out[name], v, s_out, k)
+            done_out[j] = mark(s_out)
+        for e in done_out[(n - 1) & 1] + (done_out[n & 1] or []):
+            s_out[0].wait_event(e)
+        return s_out[0]
 
     run(2)
     torch.cuda.synchronize(dev)
@@ -1100,8 +1135,9 @@ def e2e_leg(batch, ops, dev, steps, step_bytes):
             "tokens_per_s": round(wl.T * steps / el_max, 1),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "copy_GB_s": round((h2d + d2h) / (el_max / steps) / 1e9, 1),
-            "overlap": "3 streams: copy-in of step k+1, kernels of step k, copy-out of step k-1; "
-                       "two device buffer sets",
+            "overlap": "copy-in of step k+1, kernels of step k and copy-out of step k-1 "
+                       "overlap: two copy streams per direction (1 GB pieces), one compute "
+                       "stream, two device buffer sets",
             "host_buffers": f"page-locked at exact size ({kind})"}
 
 

@@ -1,13 +1,12 @@
-// Pieces shared by the lean RMSNorm kernels for bf16 rows of one warp
-// (rmsnorm_fwd_lean, rmsnorm_bwd_lean): bf16 <-> fp32 pairs and the row's
-// sum of squares in the order both kernels must share.
+// fp32 pair arithmetic for the lean bf16 kernels (rmsnorm_{fwd,bwd}_lean,
+// qk_rope_lean, qk_norm_rope_{fwd,bwd}_lean): bf16 <-> fp32 pairs, and the
+// row sum of squares in the order the two lean RMSNorm kernels must share.
 //
-// Those kernels do all fp32 arithmetic on pairs (Blackwell's two-wide fp32
+// Those kernels do their fp32 arithmetic on pairs (Blackwell's two-wide fp32
 // multiply and fused multiply-add; each half is rounded exactly like the
 // scalar instruction), unpack each bf16 once and pack two per conversion,
-// which halves the instruction count per row against scalar code: rows of
-// ~1 K features are too short for memory latency alone to hide a heavy
-// instruction stream.
+// which cuts the instruction count per row or token by a third or more
+// against scalar code.
 #pragma once
 
 #include "common.cuh"

@@ -32,7 +32,7 @@
 #include "common.cuh"
 #include "dw_reduce.cuh"
 #include "launch.h"
-#include "rmsnorm_lean.cuh"
+#include "pair_math.cuh"
 #include "rope_common.cuh"
 
 namespace ftk {

@@ -44,7 +44,7 @@
 
 #include "common.cuh"
 #include "launch.h"
-#include "rmsnorm_lean.cuh"
+#include "pair_math.cuh"
 #include "rope_common.cuh"
 
 namespace ftk {

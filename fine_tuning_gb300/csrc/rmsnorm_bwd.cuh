@@ -33,7 +33,7 @@
 #include "common.cuh"
 #include "dw_reduce.cuh"
 #include "launch.h"
-#include "rmsnorm_lean.cuh"
+#include "pair_math.cuh"
 
 namespace ftk {
 

@@ -22,7 +22,7 @@
 // (rmsnorm_fwd_rows); rows too long for either take a CTA-per-row kernel.
 #include "common.cuh"
 #include "launch.h"
-#include "rmsnorm_lean.cuh"
+#include "pair_math.cuh"
 
 namespace ftk {
 
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_pipe(const FwdParams<T, Idx> 
 
 // bf16 rows of one warp (H <= 1,024, 16-byte aligned): rmsnorm_fwd_pipe's
 // persistent grid and per-warp cp.async ring, with the lean arithmetic of
-// rmsnorm_lean.cuh: the weights are unpacked to fp32 pairs once per warp,
+// pair_math.cuh: the weights are unpacked to fp32 pairs once per warp,
 // each packet once per row, every product is a pair instruction, and the
 // ring and row addresses advance as running pointers.  With ADD the ring
 // holds the x and res rows; h = x + res is added in fp32 pairs, rounded,
