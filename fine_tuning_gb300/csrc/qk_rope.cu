@@ -595,51 +595,52 @@ qk_rope_lean(bf16 *q, Idx ld_q, bf16 *k, Idx ld_k, const int32_t *__restrict__ c
   for (int i = 0; i < kPipeBufs - 1; ++i) stage();
 
   bf16 *qr = q + t * ld_q + j * N, *kr = k + t * ld_k + j * N - (Idx)Hq * D;
-  int p = 0, b = 0;
-  while (t < rows) {  // warp-uniform
-    stage();  // the next passes' loads fly meanwhile
-    if (p == 0) {
-      const int pos = position_of<Idx>(t, bounds, B);
-      __syncwarp();  // the previous token's table has been read
-      float *tf = reinterpret_cast<float *>(tab);
+  int b = 0;
+  for (; t < rows; t += G, qr += G * ld_q, kr += G * ld_k) {  // warp-uniform
+    // the token's table, built by the warp; every lane then keeps the four
+    // entries of its columns in registers for all of the token's head passes
+    const int pos = position_of<Idx>(t, bounds, B);
+    __syncwarp();  // the previous token's table has been read
+    float *tf = reinterpret_cast<float *>(tab);
 #pragma unroll
-      for (int i = lane; i < half; i += 32) {
-        const float2 f = freq[i];
-        float c, sn;
-        rope_cos_sin(pos, f.x, f.y, &c, &sn);
-        float *ent = tf + 4 * (((i % N) >> 1) * NV + i / N) + (i & 1);
-        ent[0] = c;
-        ent[2] = sgn * sn;
-      }
-      __syncwarp();
+    for (int i = lane; i < half; i += 32) {
+      const float2 f = freq[i];
+      float c, sn;
+      rope_cos_sin(pos, f.x, f.y, &c, &sn);
+      float *ent = tf + 4 * (((i % N) >> 1) * NV + i / N) + (i & 1);
+      ent[0] = c;
+      ent[2] = sgn * sn;
     }
-    cp_async_wait<kPipeBufs - 1>();  // this lane's copies for (t, p) have landed
-    const int h = slot + p * S;
-    if (h < NH) {
-      const uint4 *d = stg + b * 64;
-      const uint4 xa = d[0], xb = d[32];
-      const uint32_t wa[4] = {xa.x, xa.y, xa.z, xa.w}, wb[4] = {xb.x, xb.y, xb.z, xb.w};
-      uint32_t o1[4], o2[4];
+    __syncwarp();
+    float2 c2[4], s2[4];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float4 cs = tab[m * NV + j];
-        const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
-        const float2 a = bf2_unpack(wa[m]), bb = bf2_unpack(wb[m]);
-        const float2 bs = __fmul2_rn(bb, s2), as = __fmul2_rn(a, s2);
-        o1[m] = bf2_pack(__ffma2_rn(a, c2, make_float2(-bs.x, -bs.y)));
-        o2[m] = bf2_pack(__ffma2_rn(bb, c2, as));
+    for (int m = 0; m < 4; ++m) {
+      const float4 cs = tab[m * NV + j];
+      c2[m] = make_float2(cs.x, cs.y);
+      s2[m] = make_float2(cs.z, cs.w);
+    }
+    for (int p = 0; p < passes; ++p) {
+      stage();  // the next passes' loads fly meanwhile
+      cp_async_wait<kPipeBufs - 1>();  // this lane's copies for (t, p) have landed
+      const int h = slot + p * S;
+      if (h < NH) {
+        const uint4 *d = stg + b * 64;
+        const uint4 xa = d[0], xb = d[32];
+        const uint32_t wa[4] = {xa.x, xa.y, xa.z, xa.w}, wb[4] = {xb.x, xb.y, xb.z, xb.w};
+        uint32_t o1[4], o2[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float2 a = bf2_unpack(wa[m]), bb = bf2_unpack(wb[m]);
+          const float2 bs = __fmul2_rn(bb, s2[m]), as = __fmul2_rn(a, s2[m]);
+          o1[m] = bf2_pack(__ffma2_rn(a, c2[m], make_float2(-bs.x, -bs.y)));
+          o2[m] = bf2_pack(__ffma2_rn(bb, c2[m], as));
+        }
+        bf16 *v = (h < Hq ? qr : kr) + (Idx)h * D;
+        *reinterpret_cast<uint4 *>(v) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        *reinterpret_cast<uint4 *>(v + half) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
       }
-      bf16 *v = (h < Hq ? qr : kr) + (Idx)h * D;
-      *reinterpret_cast<uint4 *>(v) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-      *reinterpret_cast<uint4 *>(v + half) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+      b = b + 1 == kPipeBufs ? 0 : b + 1;
     }
-    if (++p == passes) {
-      p = 0;
-      t += G;
-      qr += G * ld_q;
-      kr += G * ld_k;
-    }
-    b = b + 1 == kPipeBufs ? 0 : b + 1;
   }
   cp_async_wait<0>();
 }
