@@ -229,4 +229,18 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Named barrier 1 + g (g < 4) of a CTA's row group g, over `threads` threads.
+// Each case names its barrier by a constant, so a kernel that uses only this
+// form reserves barriers 0-4; a barrier id computed at run time makes the
+// compiler reserve all 16, which caps an SM at 4 resident CTAs of the kernel.
+// Groups that synchronise have W >= 2 warps, hence at most 8 / W = 4 per CTA.
+__device__ __forceinline__ void group_barrier(int g, int threads) {
+  switch (g) {
+    case 0: asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory"); break;
+    case 1: asm volatile("bar.sync 2, %0;" ::"r"(threads) : "memory"); break;
+    case 2: asm volatile("bar.sync 3, %0;" ::"r"(threads) : "memory"); break;
+    default: asm volatile("bar.sync 4, %0;" ::"r"(threads) : "memory"); break;
+  }
+}
+
 }  // namespace ftk

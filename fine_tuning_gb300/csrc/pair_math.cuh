@@ -1,6 +1,7 @@
 // fp32 pair arithmetic for the lean bf16 kernels (rmsnorm_{fwd,bwd}_lean,
-// qk_rope_lean, qk_norm_rope_{fwd,bwd}_lean): bf16 <-> fp32 pairs, and the
-// row sum of squares in the order the two lean RMSNorm kernels must share.
+// qk_rope_lean, qk_norm_rope_{fwd,bwd}_lean) and the output step of the
+// multi-warp RMSNorm forwards: bf16 <-> fp32 pairs, and the row sum of
+// squares in the order the two lean RMSNorm kernels must share.
 //
 // Those kernels do their fp32 arithmetic on pairs (Blackwell's two-wide fp32
 // multiply and fused multiply-add; each half is rounded exactly like the
@@ -48,6 +49,29 @@ __device__ __forceinline__ void lean_sumsq_step(float2 &acc, float2 x) {
   acc = __ffma2_rn(x, x, acc);
 }
 __device__ __forceinline__ float lean_lane_total(float2 acc) { return acc.x + acc.y; }
+
+// The RMSNorm forward's output packet (x r) w for the multi-warp kernels
+// (rmsnorm_fwd_{pipe,rows,staged}): on fp32 pairs when PAIR is set and the
+// packet is 8 bf16, else per element.  Both forms round every product like
+// the scalar expression, so they give the same bits.
+template <typename T, int N, bool PAIR>
+__device__ __forceinline__ Packet<T, N> scale_packet(const Packet<T, N> x, float r,
+                                                     const Packet<T, N> w) {
+  Packet<T, N> o;
+  if constexpr (PAIR && sizeof(T) == 2 && N == 8) {
+    float2 xf[4], wf[4];
+    unpack8(*reinterpret_cast<const uint4 *>(&x), xf);
+    unpack8(*reinterpret_cast<const uint4 *>(&w), wf);
+    const float2 r2 = make_float2(r, r);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) xf[p] = __fmul2_rn(__fmul2_rn(xf[p], r2), wf[p]);
+    *reinterpret_cast<uint4 *>(&o) = pack8(xf);
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e) o.set(e, (x.get(e) * r) * w.get(e));
+  }
+  return o;
+}
 
 }  // namespace
 

@@ -245,7 +245,7 @@ qk_rope_staged(T *q, Idx ld_q, T *k, Idx ld_k, const int32_t *__restrict__ cu, i
   };
   auto group_sync = [&]() {
     if (W > 1)
-      named_barrier(1 + grp, G);
+      group_barrier(grp, G);
     else
       __syncwarp();
   };

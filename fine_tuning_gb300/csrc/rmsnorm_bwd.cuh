@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> 
     if (W > 1) {
       float2 *slot = red[parity][grp];
       if (lane == 0) slot[wig] = cs;
-      named_barrier(1 + grp, 32 * W);
+      group_barrier(grp, 32 * W);
       cs = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < W; ++i) {
@@ -563,7 +563,7 @@ rmsnorm_bwd_staged(const BwdParams<T, Idx> a, int S, uint32_t off_red, uint32_t 
       cs = warp_sum2(cs);
     if (W > 1) {
       if (lane == 0) red[grp * W + wig] = cs;
-      named_barrier(1 + grp, G);
+      group_barrier(grp, G);
       cs = make_float2(0.f, 0.f);
       for (int i = 0; i < W; ++i) {
         cs.x += red[grp * W + i].x;
@@ -592,7 +592,7 @@ rmsnorm_bwd_staged(const BwdParams<T, Idx> a, int S, uint32_t off_red, uint32_t 
       }
     }
     if (W > 1)
-      named_barrier(1 + grp, G);
+      group_barrier(grp, G);
     else
       __syncwarp();
     if (leader) {

@@ -198,7 +198,7 @@ rmsnorm_fwd_staged(const FwdParams<T, Idx> a, int S, uint32_t off_red, uint32_t 
       // barrier keeps the slots)
       float *slot = red + ((early ? (it & 1) * R : 0) + grp) * W;
       if (lane == 0) slot[wig] = ss;
-      named_barrier(1 + grp, G);
+      group_barrier(grp, G);
       ss = 0.f;
       for (int i = 0; i < W; ++i) ss += slot[i];
       if (early && leader && it > 0) {  // the previous row's stage is free
@@ -219,16 +219,13 @@ rmsnorm_fwd_staged(const FwdParams<T, Idx> a, int S, uint32_t off_red, uint32_t 
       if (c < a.hp) {
         const Packet<T, N> v = staged_input<T, N, ADD>(xs, rs, c);
         if (ADD) store_packet<T, N>(a.h + row * a.ldh + (Idx)c * N, v);
-        Packet<T, N> o;
-#pragma unroll
-        for (int e = 0; e < N; ++e) o.set(e, (v.get(e) * r) * wv[k].get(e));
-        store_packet<T, N>(yr + (Idx)c * N, o);
+        store_packet<T, N>(yr + (Idx)c * N, scale_packet<T, N, !ADD>(v, r, wv[k]));
       }
     }
     if (!early) {
       // the whole group has read stage s: refill it
       if (W > 1)
-        named_barrier(1 + grp, G);
+        group_barrier(grp, G);
       else
         __syncwarp();
       if (leader) {
@@ -304,10 +301,7 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_rows(const FwdParams<T, Idx> 
     if (c < a.hp) {
       if (ADD) store_packet<T, N>(a.h + row * a.ldh + (Idx)c * N, xv[k]);
       const Packet<T, N> wv = load_packet<T, N>(a.w + (Idx)c * N);
-      Packet<T, N> o;
-#pragma unroll
-      for (int e = 0; e < N; ++e) o.set(e, (xv[k].get(e) * r) * wv.get(e));
-      store_packet<T, N>(yr + (Idx)c * N, o);
+      store_packet<T, N>(yr + (Idx)c * N, scale_packet<T, N, !ADD>(xv[k], r, wv));
     }
   }
 }
@@ -403,10 +397,7 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_pipe(const FwdParams<T, Idx> 
       const int c = col(i);
       if (c < a.hp) {
         if (ADD) store_packet<T, N>(a.h + row * a.ldh + (Idx)c * N, xv[i]);
-        Packet<T, N> o;
-#pragma unroll
-        for (int e = 0; e < N; ++e) o.set(e, (xv[i].get(e) * r) * wv[i].get(e));
-        store_packet<T, N>(yr + (Idx)c * N, o);
+        store_packet<T, N>(yr + (Idx)c * N, scale_packet<T, N, !ADD>(xv[i], r, wv[i]));
       }
     }
     row += step;
@@ -595,12 +586,19 @@ cudaError_t fwd_lean_v(const FwdParams<bf16, Idx> &k, const DeviceInfo &dev, cud
   return cudaGetLastError();
 }
 
+// Resident CTAs per SM of the staged forward, at most.  Fewer row groups
+// streaming at once measured faster at H = 5,120 (groups of 5 warps, 524,288
+// rows): the plain norm 1,641 us with 3 CTAs per SM, 1,653 us with 4 and
+// 1,850 us with 6; with the residual (two rows per stage) 3,205 us with 4
+// and 3,311 us with 3.
+template <bool ADD> constexpr int fwd_staged_blocks() { return ADD ? 4 : 3; }
+
 template <typename T, typename Idx, int N, int V, bool ADD>
 cudaError_t fwd_staged_v(const RowPlan &p, const StagedPlan &sp, const FwdParams<T, Idx> &k,
                          const DeviceInfo &dev, cudaStream_t s) {
   auto kern = rmsnorm_fwd_staged<T, Idx, N, V, ADD>;
   const int threads = p.threads();
-  const int occ = blocks_per_sm((const void *)kern, threads, sp.smem, dev, 8);
+  const int occ = blocks_per_sm((const void *)kern, threads, sp.smem, dev, fwd_staged_blocks<ADD>());
   int64_t P = ceil_div((int64_t)k.rows, (int64_t)p.R);
   if (P > (int64_t)dev.sms * occ) P = (int64_t)dev.sms * occ;
   unsigned *status = nullptr;
