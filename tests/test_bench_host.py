@@ -67,3 +67,20 @@ def test_reference_arm_prints_our_config_at_the_default_workload():
     wl = W.WORKLOADS["qwen3-32b-524k"]
     assert d["config"] == bench.workload_config(wl, 1, 1)
     assert d["cpu_baseline"]["tokens_per_step"] >= 1 and d["value"] > 0
+
+
+def test_launch_gap_figures():
+    """The per-kernel figures with the launch gap taken out: the same bytes
+    over the kernel's time minus the gap; none for a time within twice it."""
+    ib = {k: 1000 for k in bench.OPS}
+    kernels = {}
+    for j, k in enumerate(bench.OPS):
+        us = 10.0 if j else 3.0
+        kernels[k] = bench.kernel_entry(k, us / 1e3, ib[k] * 1_000_000, 1000, 5000.0, "measured")
+    refs = {"launch_gap_ms": 2e-3, "copy_ms": [8e-3] * len(bench.OPS)}
+    bench.add_references(kernels, refs, ib)
+    k = kernels[bench.OPS[1]]
+    assert k["launch_gap_us"] == 2.0 and k["frac_of_same_size_copy"] == 0.8
+    assert abs(k["GB_s_excl_launch_gap"] - 1e9 / 8e-6 / 1e9) < 0.1       # 1 GB in 8 us
+    assert abs(k["frac_of_measured_hbm_excl_launch_gap"] - 125000 / 5000.0) < 1e-3
+    assert "GB_s_excl_launch_gap" not in kernels[bench.OPS[0]]          # 3 us < 2 x 2 us
