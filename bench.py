@@ -348,7 +348,7 @@ def check_parity(wl, cu_host, rows, srows, inp, got):
     raises on any element out of tolerance, else returns the worst
     error / bound."""
     import oracle
-    from oracle.tolerance import assert_close
+    from oracle.tolerance import assert_close, literal_figures
     code = "f32" if wl.dtype == "f32" else "bf16"
     yr, rr = oracle.rmsnorm_fwd(inp["x"], inp["w"], wl.eps)
     dxr, _, dxs, _ = oracle.rmsnorm_bwd(inp["dy"], inp["x"], inp["w"], wl.eps, scales=True)
@@ -358,15 +358,21 @@ def check_parity(wl, cu_host, rows, srows, inp, got):
                                     scales=True)
     dqr, dkr, dqs, dks = oracle.qk_rope(inp["dq"], inp["dk"], cu_host, wl.theta, -1, tok=rows,
                                         scales=True)
-    worst = 0.0
+    worst, literal = 0.0, {}
     for name, ref, sc, kind in (("y", yr, None, code), ("rstd", rr, None, "f32"),
                                 ("dx", dxr, dxs, code), ("h", hr, None, code),
                                 ("dg", dgr, dgs, code), ("du", dur, None, code),
                                 ("q", qr, qs, code), ("k", kr, ks, code),
                                 ("dq", dqr, dqs, code), ("dk", dkr, dks, code)):
         worst = max(worst, assert_close(name, got[name], ref, sc, dtype=kind))
+        lit = literal_figures(got[name], ref, dtype=kind)
+        literal[name] = {k: (round(v, 9) if isinstance(v, float) else v) for k, v in lit.items()}
     return {"tokens_checked": int(len(rows)), "swiglu_tokens_checked": int(len(srows)),
             "outputs": 10, "max_err_over_bound": round(worst, 4),
+            "literal": literal,
+            "literal_note": "error against the literal bars alone (relative 1e-5 in fp32, 2 bf16 "
+                            "ulps); needed_floor counts the elements that passed only through "
+                            "the condition-scale term",
             "rows": "first and last 64 tokens, 64 drawn in between, both sides of the first "
                     "16 sequence boundaries (dw, a sum over every row, is checked in full by "
                     "the GPU tests)"}

@@ -54,3 +54,27 @@ def assert_close(name, got, ref, scale=None, dtype="bf16", kind="out"):
         raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} elements out of "
                              f"tolerance ({dtype}/{kind}):\n  " + "\n  ".join(rows))
     return float((err / np.maximum(b, 1e-300)).max()) if err.size else 0.0
+
+
+def literal_figures(got, ref, dtype="bf16", kind="out"):
+    """The error of `got` against the literal bars, without the condition
+    scale: the largest relative error over nonzero references, for bf16
+    outputs the largest distance in bf16 ulps of the reference, and how many
+    elements exceed the literal bar (relative 1e-5 in fp32, 2 ulps in bf16,
+    relative 2e-3 for dw), i.e. needed the condition-scale floor to pass."""
+    got, ref = f64(got), np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref)
+    nz = ref != 0
+    out = {"elements": int(ref.size),
+           "max_rel": float((err[nz] / np.abs(ref[nz])).max()) if nz.any() else 0.0}
+    if dtype == "f32":
+        lit = 1e-5 * np.abs(ref)
+    elif kind == "dw":
+        lit = 2e-3 * np.abs(ref)
+    else:
+        u = ulp_bf16(ref)
+        out["max_ulp"] = float((err / u).max()) if err.size else 0.0
+        lit = 2.0 * u
+    out["needed_floor"] = int((err > lit).sum())
+    return out
+
