@@ -1,7 +1,7 @@
 // fp32 pair arithmetic for the lean bf16 kernels (rmsnorm_{fwd,bwd}_lean,
-// qk_rope_lean, qk_norm_rope_{fwd,bwd}_lean) and the output step of the
-// multi-warp RMSNorm forwards: bf16 <-> fp32 pairs, and the row sum of
-// squares in the order the two lean RMSNorm kernels must share.
+// qk_rope_lean, qk_norm_rope_{fwd,bwd}_lean) and the row sums and output
+// step of the multi-warp RMSNorm kernels: bf16 <-> fp32 pairs, and the row
+// sum of squares in the order the forward and backward kernels share.
 //
 // Those kernels do their fp32 arithmetic on pairs (Blackwell's two-wide fp32
 // multiply and fused multiply-add; each half is rounded exactly like the
@@ -49,6 +49,35 @@ __device__ __forceinline__ void lean_sumsq_step(float2 &acc, float2 x) {
   acc = __ffma2_rn(x, x, acc);
 }
 __device__ __forceinline__ float lean_lane_total(float2 acc) { return acc.x + acc.y; }
+
+// The multi-warp RMSNorm kernels (rmsnorm_{fwd,bwd}_{pipe,rows,staged}) sum
+// a lane's squares through these two: for 8-wide bf16 packets the lean pair
+// chain above (even columns in .x, odd in .y, halves added at the end), for
+// any other packet one scalar chain in .x.  Every forward and backward of a
+// row plan goes through them, so a recomputed r equals the saved one and
+// the residual-add forward equals the plain norm of its h, bit for bit.
+template <typename T, int N>
+__device__ __forceinline__ void sumsq_packet(float2 &acc, const Packet<T, N> &v) {
+  if constexpr (sizeof(T) == 2 && N == 8) {
+    float2 f[4];
+    unpack8(*reinterpret_cast<const uint4 *>(&v), f);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) lean_sumsq_step(acc, f[p]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      const float f = v.get(e);
+      acc.x = fmaf(f, f, acc.x);
+    }
+  }
+}
+template <typename T, int N> __device__ __forceinline__ float sumsq_total(float2 acc) {
+  if constexpr (sizeof(T) == 2 && N == 8) {
+    return lean_lane_total(acc);
+  } else {
+    return acc.x;
+  }
+}
 
 // The RMSNorm forward's output packet (x r) w for the multi-warp kernels
 // (rmsnorm_fwd_{pipe,rows,staged}): on fp32 pairs when PAIR is set and the

@@ -140,19 +140,18 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_pipe(const BwdParams<T, Idx> 
     const uint4 *d = my + b * kSl * 32 + lane;
     Packet<T, N> xv[V], gv[V];
     float2 cs = make_float2(0.f, 0.f);  // (sum dy*w*x, sum x*x)
+    float2 s2 = make_float2(0.f, 0.f);  // sum x*x in the forward's order
 #pragma unroll
     for (int k = 0; k < V; ++k) {
       if (col(k) < hp) {
         *reinterpret_cast<uint4 *>(&xv[k]) = d[k * 32];
         *reinterpret_cast<uint4 *>(&gv[k]) = d[(V + k) * 32];
 #pragma unroll
-        for (int e = 0; e < N; ++e) {
-          const float xf = xv[k].get(e);
-          cs.x = fmaf(gv[k].get(e) * wv[k].get(e), xf, cs.x);
-          if (!HAS_RSTD) cs.y = fmaf(xf, xf, cs.y);
-        }
+        for (int e = 0; e < N; ++e) cs.x = fmaf(gv[k].get(e) * wv[k].get(e), xv[k].get(e), cs.x);
+        if (!HAS_RSTD) sumsq_packet<T, N>(s2, xv[k]);
       }
     }
+    if (!HAS_RSTD) cs.y = sumsq_total<T, N>(s2);
     if (HAS_RSTD)
       cs.x = warp_sum(cs.x);
     else
@@ -398,17 +397,16 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_rows(const BwdParams<T, Idx> 
         }
       }
       if (HAS_RSTD) r = a.rstd[row];
+      float2 s2 = make_float2(0.f, 0.f);  // sum x*x in the forward's order
 #pragma unroll
       for (int k = 0; k < V; ++k) {
         if (gi + k * G < hp) {
 #pragma unroll
-          for (int e = 0; e < N; ++e) {
-            const float xf = xv[k].get(e);
-            cs.x = fmaf(gv[k].get(e) * wv[k].get(e), xf, cs.x);
-            if (!HAS_RSTD) cs.y = fmaf(xf, xf, cs.y);
-          }
+          for (int e = 0; e < N; ++e) cs.x = fmaf(gv[k].get(e) * wv[k].get(e), xv[k].get(e), cs.x);
+          if (!HAS_RSTD) sumsq_packet<T, N>(s2, xv[k]);
         }
       }
+      if (!HAS_RSTD) cs.y = sumsq_total<T, N>(s2);
     }
     if (HAS_RSTD) {
       cs.x = warp_sum(cs.x);
@@ -555,6 +553,7 @@ rmsnorm_bwd_staged(const BwdParams<T, Idx> a, int S, uint32_t off_red, uint32_t 
     const T *gs = reinterpret_cast<const T *>(st + row_bytes);
     const T *hs = reinterpret_cast<const T *>(st + (ADD ? 2 : 1) * row_bytes);
     float2 cs = make_float2(0.f, 0.f);  // (sum dy*w*x, sum x*x)
+    float2 s2 = make_float2(0.f, 0.f);  // sum x*x in the forward's order
 #pragma unroll
     for (int k = 0; k < V; ++k) {
       const int c = gi + k * G;
@@ -562,13 +561,11 @@ rmsnorm_bwd_staged(const BwdParams<T, Idx> a, int S, uint32_t off_red, uint32_t 
         const Packet<T, N> xv = *reinterpret_cast<const Packet<T, N> *>(xs + c * N);
         const Packet<T, N> gv = *reinterpret_cast<const Packet<T, N> *>(gs + c * N);
 #pragma unroll
-        for (int e = 0; e < N; ++e) {
-          const float xf = xv.get(e);
-          cs.x = fmaf(gv.get(e) * wv[k].get(e), xf, cs.x);
-          if (!HAS_RSTD) cs.y = fmaf(xf, xf, cs.y);
-        }
+        for (int e = 0; e < N; ++e) cs.x = fmaf(gv.get(e) * wv[k].get(e), xv.get(e), cs.x);
+        if (!HAS_RSTD) sumsq_packet<T, N>(s2, xv);
       }
     }
+    if (!HAS_RSTD) cs.y = sumsq_total<T, N>(s2);
     if (HAS_RSTD)
       cs.x = warp_sum(cs.x);
     else

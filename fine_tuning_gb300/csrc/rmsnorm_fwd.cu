@@ -177,20 +177,16 @@ rmsnorm_fwd_staged(const FwdParams<T, Idx> a, int S, uint32_t off_red, uint32_t 
     if (live) live = mbar_wait_bounded(&gb[s], (uint32_t)((it / S) & 1), wait_limit, status);
     const T *xs = reinterpret_cast<const T *>(ring + (size_t)s * stage_bytes);
     const T *rs = reinterpret_cast<const T *>(ring + (size_t)s * stage_bytes + row_bytes);
-    float ss = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < V; ++k) {
       const int c = gi + k * G;
       if (c < a.hp) {
         const Packet<T, N> v = staged_input<T, N, ADD>(xs, rs, c);
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-          const float f = v.get(e);
-          ss = fmaf(f, f, ss);
-        }
+        sumsq_packet<T, N>(acc, v);
       }
     }
-    ss = warp_sum(ss);
+    float ss = warp_sum(sumsq_total<T, N>(acc));
     if (W > 1) {
       // with the early refill the slots alternate by row parity: a warp one
       // row ahead writes the other half, and none gets two rows ahead
@@ -258,7 +254,7 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_rows(const FwdParams<T, Idx> 
   const bool active = row < a.rows;
 
   Packet<T, N> xv[V];
-  float ss = 0.f;
+  float2 acc = make_float2(0.f, 0.f);
   if (active) {
     const T *xr = a.x + row * a.ldx;
     const T *rr = ADD ? a.res + row * a.ldr : nullptr;
@@ -275,15 +271,11 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_rows(const FwdParams<T, Idx> 
     for (int k = 0; k < V; ++k) {
       if (gi + k * G < a.hp) {
         if (ADD) xv[k] = norm_input<T, N, ADD>(xv[k], rv[ADD ? k : 0]);
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-          const float f = xv[k].get(e);
-          ss = fmaf(f, f, ss);
-        }
+        sumsq_packet<T, N>(acc, xv[k]);
       }
     }
   }
-  ss = warp_sum(ss);
+  float ss = warp_sum(sumsq_total<T, N>(acc));
   if (W > 1) {
     if (lane == 0) red[grp * W + wig] = ss;
     __syncthreads();
@@ -363,9 +355,9 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_pipe(const FwdParams<T, Idx> 
     stage(r2, b == 0 ? kBufs - 1 : b - 1);  // the next rows' loads fly meanwhile
     cp_async_wait<kBufs - 1>();              // this lane's copies of `row` have landed
     Packet<T, N> xv[kP];
-    float part[W];
+    float2 part[W];
 #pragma unroll
-    for (int w = 0; w < W; ++w) part[w] = 0.f;
+    for (int w = 0; w < W; ++w) part[w] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < kP; ++i) {
       if (col(i) < a.hp) {
@@ -375,19 +367,15 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_pipe(const FwdParams<T, Idx> 
           *reinterpret_cast<uint4 *>(&rv) = my[(b * kSl + kP + i) * 32 + lane];
           xv[i] = norm_input<T, N, ADD>(xv[i], rv);
         }
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-          const float f = xv[i].get(e);
-          part[i / V] = fmaf(f, f, part[i / V]);
-        }
+        sumsq_packet<T, N>(part[i / V], xv[i]);
       }
     }
     float ss = 0.f;
     if (W == 1) {
-      ss = warp_sum(part[0]);
+      ss = warp_sum(sumsq_total<T, N>(part[0]));
     } else {
 #pragma unroll
-      for (int w = 0; w < W; ++w) ss += warp_sum(part[w]);  // the plan's combine order
+      for (int w = 0; w < W; ++w) ss += warp_sum(sumsq_total<T, N>(part[w]));  // the plan's order
     }
     const float r = rsqrtf(fmaf(ss, a.inv_h, a.eps));
     if (a.rstd != nullptr && lane == 0) a.rstd[row] = r;
