@@ -555,14 +555,65 @@ def hold_gpu(ms=20.0):
     torch.cuda._sleep(int(ms * 2.1e6))  # cycles at ~2.1 GHz
 
 
+def reps_in_graph(op_bytes, target_us=300.0, cap=16):
+    """How many [L2 flush, op] pairs one timed graph holds: enough that the
+    smallest op's work in one replay reaches ~target_us.  The start and end
+    of a graph replay, as CUDA events see them, move in steps of ~2 us (one
+    process measured the same kernel at 10.24 and 12.29 us by turns), so
+    small ops are timed over several pairs per replay and the difference is
+    divided by their number."""
+    est_us = min(op_bytes) / 6.0e6  # bytes over ~6 TB/s, in us
+    return max(1, min(cap, int(round(target_us / max(est_us, 1.0)))))
+
+
+def pair_graphs(ops, flush, m, fill):
+    """Per op a graph of m pairs [L2 flush, op], and the graph of the m
+    flushes alone."""
+    import torch
+    graphs = []
+    for op in ops:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(m):
+                flush.fill_(fill)
+                op()
+        graphs.append(g)
+    fg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(fg):
+        for _ in range(m):
+            flush.fill_(fill)
+    return graphs, fg
+
+
+def time_pairs(graphs, fg, m, reps, dev):
+    """Each op's device time: the median over `reps` repetitions of (its
+    graph's time minus the flush graph's) / m, CUDA events around every
+    replay, all enqueued behind a sleep kernel.  Returns per-op ms."""
+    import torch
+    for g in graphs + [fg]:
+        g.replay()
+    torch.cuda.synchronize(dev)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(len(graphs) + 1)] for _ in range(reps)]
+    hold_gpu()
+    for i in range(reps):
+        for (a, b), g in zip(ev[i], graphs + [fg]):
+            a.record()
+            g.replay()
+            b.record()
+    torch.cuda.synchronize(dev)
+    return [op_ms([e[j] for e in ev], [e[-1] for e in ev]) / m for j in range(len(graphs))]
+
+
 def time_batch(batch, flush, K, Kk, dev, world=1, with_reference=True):
     """The step as one CUDA graph replayed K times (CUDA events around each
-    replay), then each op as a graph [L2 flush, op] beside a graph [L2
-    flush], Kk repetitions.  With `with_reference`, the same repetitions
-    also time an empty op (a one-element fill: the launch gap every op's
-    time includes) and, per op, a device copy of its algorithmic bytes.
-    Returns (step ms per replay, per-op ms, (t0, t1) of the step region,
-    (t1, t2) of the per-kernel region, the flush graph, references)."""
+    replay), then each op as a graph of m pairs [L2 flush, op] beside a graph
+    of m flushes (m from reps_in_graph), Kk repetitions.  With
+    `with_reference`, the same repetitions also time an empty op (a
+    one-element fill: the launch gap every op's time includes) and, per op,
+    a streaming kernel over its algorithmic bytes.  Returns (step ms per
+    replay, per-op ms, (t0, t1) of the step region, (t1, t2) of the
+    per-kernel region, references with the pairs per graph)."""
     import torch
     import torch.distributed as dist
 
@@ -579,24 +630,13 @@ def time_batch(batch, flush, K, Kk, dev, world=1, with_reference=True):
     with torch.cuda.graph(graph):
         for op in ops[:n_ops]:
             op()
-    op_graphs = []
-    for op in ops:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            flush.fill_(3)
-            op()
-        op_graphs.append(g)
-    flush_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(flush_graph):
-        flush.fill_(3)
+    ib = W.ideal_bytes(batch.wl)
+    m = reps_in_graph([ib[k] for k in OPS])
+    op_graphs, flush_graph = pair_graphs(ops, flush, m, 3)
     graph.replay()
-    for g in op_graphs + [flush_graph]:
-        g.replay()
     torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
-    evk = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(len(ops) + 1)] for _ in range(Kk)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -610,20 +650,13 @@ def time_batch(batch, flush, K, Kk, dev, world=1, with_reference=True):
     if world > 1:
         dist.barrier()
     t1 = time.time()
-    hold_gpu()
-    for i in range(Kk):
-        for (a, b), g in zip(evk[i], op_graphs + [flush_graph]):
-            a.record()
-            g.replay()
-            b.record()
-    torch.cuda.synchronize(dev)
+    per = time_pairs(op_graphs, flush_graph, m, Kk, dev)
     t2 = time.time()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    per = [op_ms([e[j] for e in evk], [e[-1] for e in evk]) for j in range(len(ops))]
     if with_reference:
-        refs = {"launch_gap_ms": per[n_ops], "copy_ms": per[n_ops + 1:]}
-    del keep
-    return step_ms, per[:n_ops], (t0, t1), (t1, t2), flush_graph, refs
+        refs = {"launch_gap_ms": per[n_ops], "copy_ms": per[n_ops + 1:], "pairs_per_graph": m}
+    del keep, op_graphs, flush_graph
+    return step_ms, per[:n_ops], (t0, t1), (t1, t2), refs
 
 
 def add_references(kernels, refs, ib):
@@ -669,7 +702,7 @@ def per_workload_leg(names, flush, K, Kk, dev, hbm, src, sampler, with_ext=True)
             flush.fill_(1)
             for op in b.ops():
                 op()
-        step_ms, per_op, _, (k0, k1), fg, refs = time_batch(b, flush, K, Kk, dev)
+        step_ms, per_op, _, (k0, k1), refs = time_batch(b, flush, K, Kk, dev)
         ib, toks = W.ideal_bytes(wl), W.tokens_per_call(wl)
         step_bytes = sum(ib[k] for k in OPS)
         ms = sum(step_ms) / len(step_ms)
@@ -683,15 +716,16 @@ def per_workload_leg(names, flush, K, Kk, dev, hbm, src, sampler, with_ext=True)
             "step_GB_s": round(step_bytes / (ms * 1e-3) / 1e9, 1),
             "step_frac_of_hbm": round(step_bytes / (ms * 1e-3) / 1e9 / hbm, 4),
             "tokens_per_s": round(wl.T / (ms * 1e-3), 1), "kernels": kern,
+            "pairs_per_graph": refs.get("pairs_per_graph", 1),
             "dominant": {"kernel": OPS[dom], "traffic": ncu_traffic(OPS[dom], wl.name)},
             "parity": par, "clocks_kernel_leg": sampler.summary(k0, k1)}
         if with_ext:
-            ext = ext_leg(b, flush, fg, dev, Kk, hbm, src)
+            ext = ext_leg(b, flush, dev, Kk, hbm, src)
             out[name]["extensions"] = {n: {f: v[f] for f in ("us", "GB_s", "frac_of_measured_hbm"
                                                               if src == "measured" else
                                                               "frac_of_fallback_hbm")}
                                        for n, v in ext.items() if isinstance(v, dict)}
-        del b, fg
+        del b
         torch.cuda.empty_cache()
     return out
 
@@ -746,7 +780,7 @@ def run_ours(args):
         pass
     sampler = ClockSampler(uuid).start()
     time.sleep(0.6)
-    step_ms, per_op, (t0, t1), (k0, k1), flush_graph, refs = time_batch(batch, flush, K, Kk,
+    step_ms, per_op, (t0, t1), (k0, k1), refs = time_batch(batch, flush, K, Kk,
                                                                         dev, world)
     el_max, bytes_all = reduce_timing(sum(step_ms) / 1e3, step_bytes * K)
     _, tok_all = reduce_timing(0.0, float(wl.T) * K)
@@ -783,18 +817,22 @@ def run_ours(args):
         "gpu_launches_all_legs": LAUNCHES_PER_STEP * (K + Kk),
         "timing": (f"step: {K} replays of a CUDA graph of the step's {LAUNCHES_PER_STEP} "
                    f"launches, CUDA events around each replay; per kernel: the median over {Kk} "
-                   "replays of a graph [L2 flush, op] minus the same repetition's graph [L2 flush], "
-                   "CUDA events around each, enqueued behind a sleep kernel so no host submission "
-                   "gap falls inside; launch_gap_us is an empty one-element op timed the same way "
-                   "(included in every op's us; the *_excl_launch_gap figures take it out); copy_same_bytes_us an elementwise kernel (fp32 "
-                   "x 1) reading and writing the op's algorithmic bytes at the same size"),
+                   f"replays of a graph of {refs.get('pairs_per_graph', 1)} pairs [L2 flush, op] "
+                   "minus the same repetition's graph of as many L2 flushes, over their number "
+                   "(several pairs per graph when the ops are small: a replay's start and end "
+                   "move in ~2 us steps), CUDA events around each replay, enqueued behind a "
+                   "sleep kernel so no host submission gap falls inside; launch_gap_us is an "
+                   "empty one-element op timed the same way (included in every op's us; the "
+                   "*_excl_launch_gap figures take it out); copy_same_bytes_us an elementwise "
+                   "kernel (fp32 x 1) reading and writing the op's algorithmic bytes at the "
+                   "same size"),
         "wall_ms_timed_region": round((t1 - t0) * 1e3, 3),
     }
     out["clocks"] = sampler.summary(t0, t1)
     out["clocks_kernel_leg"] = sampler.summary(k0, k1)
     if not args.no_ext:
         e0 = time.time()
-        out["extensions"] = ext_leg(batch, flush, flush_graph, dev, Kk, hbm, src)
+        out["extensions"] = ext_leg(batch, flush, dev, Kk, hbm, src)
         out["extensions"]["clocks"] = sampler.summary(e0, time.time())
         out["gpu_launches_all_legs"] += sum(EXT_OPS.values()) * Kk
     torch.cuda.empty_cache()
@@ -807,7 +845,7 @@ def run_ours(args):
                 0 if args.no_ext else sum(EXT_OPS.values()) * Kk))
         if not args.no_ext and not args.no_cce:
             c0 = time.time()
-            out["cce"] = cce_leg(dev, flush, flush_graph, max(3, min(Kk, 20)))
+            out["cce"] = cce_leg(dev, flush, max(3, min(Kk, 20)))
             out["cce"]["clocks"] = sampler.summary(c0, time.time())
             out["gpu_launches_all_legs"] += out["cce"].pop("launches")
     sampler.stop()
@@ -827,7 +865,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
+def ext_leg(batch, flush, dev, reps, hbm, src):
     """The widened ops (not part of the step), each timed like a step kernel:
     replays of a graph [L2 flush, op] minus the graph [L2 flush].  They run
     after the timed step region, on the same batch (the residual stream and
@@ -872,39 +910,24 @@ def ext_leg(batch, flush, flush_graph, dev, reps, hbm, src):
     assert set(ops) == set(EXT_OPS)
     for op in ops.values():  # warm-up (and the first, allocating, launch)
         op()
-    graphs = {}
-    for name, op in ops.items():
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            flush.fill_(5)
-            op()
-        graphs[name] = g
-    for g in list(graphs.values()) * 3:
-        g.replay()
-    torch.cuda.synchronize(dev)
-    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(reps)] for n in list(graphs) + ["flush"]}
-    hold_gpu()
-    for k in range(reps):
-        for n, g in list(graphs.items()) + [("flush", flush_graph)]:
-            a, b = ev[n][k]
-            a.record()
-            g.replay()
-            b.record()
-    torch.cuda.synchronize(dev)
     ib, toks = W.ideal_bytes(wl), W.tokens_per_call(wl)
+    names = list(ops)
+    m = reps_in_graph([ib[n] for n in names])
+    graphs, fg = pair_graphs([ops[n] for n in names], flush, m, 5)
+    per = dict(zip(names, time_pairs(graphs, fg, m, reps, dev)))
+    del graphs, fg
     out = {}
-    for n in graphs:
-        out[n] = kernel_entry(n, op_ms(ev[n], ev["flush"]), ib[n], toks[n], hbm, src)
+    for n in names:
+        out[n] = kernel_entry(n, per[n], ib[n], toks[n], hbm, src)
         out[n]["launches"] = EXT_OPS[n]
-    out["timing"] = (f"the median over {reps} replays of a graph [L2 flush, op] minus the same "
-                     "repetition's graph [L2 flush], CUDA events around each; outside the step's "
-                     "timed region")
+    out["timing"] = (f"the median over {reps} replays of a graph of {m} pairs [L2 flush, op] "
+                     f"minus the same repetition's graph of {m} L2 flushes, over {m}, CUDA events "
+                     "around each replay; outside the step's timed region")
     del h, y, rstd, dx, dw, res, dres, extra, qo, ko, rq, rk, nr_ws
     return out
 
 
-def cce_leg(dev, flush, flush_graph, reps):
+def cce_leg(dev, flush, reps):
     """The LM-head cross-entropy (a second workload, tensor-core bound):
     Qwen2.5-0.5B's head on 8,192 tokens, forward and backward each captured
     as a graph [L2 flush, op] and timed against the graph [L2 flush]."""
@@ -928,26 +951,10 @@ def cce_leg(dev, flush, flush_graph, reps):
            "cce_bwd": lambda: ftk.cce_bwd(h, Wt, y, lse, g, dh=dh, dW=dW, workspace=wsb)}
     for op in ops.values():
         op()
-    graphs = {}
-    for name, op in ops.items():
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr):
-            flush.fill_(9)
-            op()
-        graphs[name] = gr
-    for gr in graphs.values():
-        gr.replay()
-    torch.cuda.synchronize(dev)
-    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(reps)] for n in list(graphs) + ["flush"]}
-    hold_gpu()
-    for k in range(reps):
-        for n, gr in list(graphs.items()) + [("flush", flush_graph)]:
-            a, b = ev[n][k]
-            a.record()
-            gr.replay()
-            b.record()
-    torch.cuda.synchronize(dev)
+    names = list(ops)
+    graphs, fg = pair_graphs([ops[n] for n in names], flush, 1, 9)  # ms-long ops: one pair
+    per = dict(zip(names, time_pairs(graphs, fg, 1, reps, dev)))
+    del graphs, fg
     peak, psrc = tensor_peak()
     flops = {"cce_fwd": 2 * hw.T * hw.H * hw.V, "cce_bwd": 6 * hw.T * hw.H * hw.V}
     chunk = ftk.cce_bwd_chunk(hw.T, hw.H, hw.V)
@@ -956,8 +963,8 @@ def cce_leg(dev, flush, flush_graph, reps):
     out = {"workload": {"name": hw.name, "T": hw.T, "H": hw.H, "V": hw.V,
                         "ignored_share": hw.ignored, "bwd_chunk": chunk},
            "loss": round(float(loss.item()), 6)}
-    for n in graphs:
-        ms = op_ms(ev[n], ev["flush"])
+    for n in names:
+        ms = per[n]
         tf = flops[n] / (ms * 1e-3) / 1e12
         out[n] = {"ms": round(ms, 4), "TFLOP_s": round(tf, 1), "algorithmic_flops": flops[n],
                   "tokens_per_s": round(hw.T / (ms * 1e-3), 1),

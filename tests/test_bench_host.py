@@ -84,3 +84,11 @@ def test_launch_gap_figures():
     assert abs(k["GB_s_excl_launch_gap"] - 1e9 / 8e-6 / 1e9) < 0.1       # 1 GB in 8 us
     assert abs(k["frac_of_measured_hbm_excl_launch_gap"] - 125000 / 5000.0) < 1e-3
     assert "GB_s_excl_launch_gap" not in kernels[bench.OPS[0]]          # 3 us < 2 x 2 us
+
+
+def test_pairs_per_graph():
+    """Small ops are timed over several [flush, op] pairs per graph, large
+    ones over one."""
+    assert bench.reps_in_graph([58_787_584, 478_150_656]) == 16          # ~10 us op: capped
+    assert bench.reps_in_graph([268_570_624]) == 7                       # ~45 us
+    assert bench.reps_in_graph([10_739_525_632, 19_327_352_832]) == 1    # ms-long ops
