@@ -502,9 +502,11 @@ def cpu_leg(wl, cu_host, cut, seconds):
                   f"ops (oracle in double, OpenMP over rows), GB/s over the passes' "
                   f"algorithmic bytes",
         "per_op_s": {k: round(v / passes, 6) for k, v in per_op.items()},
-        # the whole step at this rate: the sample's time per token times T
-        # (an extrapolation; every op's work grows in proportion to tokens)
-        "full_step_s_extrapolated": round(wl.T / (passes * n / el), 3),
+        # the whole step at the sample's rate: each op's time per pass scaled
+        # by the tokens it sees in a full step over those of one pass
+        "full_step_s_extrapolated": round(sum(
+            v / passes * ((wl.T_swiglu / min(n, wl.T_swiglu)) if "swiglu" in k else wl.T / n)
+            for k, v in per_op.items()), 3),
         "one_thread": {"tokens": n1, "seconds": round(el1, 4),
                        "GB_s": round(sum(tok_bytes(k, n1) for k in ib if k in OPS) / el1 / 1e9,
                                      3)},
