@@ -92,3 +92,22 @@ def test_pairs_per_graph():
     assert bench.reps_in_graph([58_787_584, 478_150_656]) == 16          # ~10 us op: capped
     assert bench.reps_in_graph([268_570_624]) == 7                       # ~45 us
     assert bench.reps_in_graph([10_739_525_632, 19_327_352_832]) == 1    # ms-long ops
+
+
+def test_cpu_leg_on_a_small_sample():
+    """The oracle baseline leg on CPU inputs: a rate, its sample, and the
+    extrapolated full step (SwiGLU scaled by its own token count)."""
+    wl = bench.select_workload("qwen2.5-0.5b", 512)
+    cut = {}
+    cut.update(W.rmsnorm_inputs(wl, "cpu"))
+    cut.update(W.swiglu_inputs(wl, "cpu"))
+    cut.update(W.rope_inputs(wl, "cpu"))
+    cu = W.cu_seqlens_from_lengths(W.draw_lengths(wl))
+    out = bench.cpu_leg(wl, cu, {k: cut[k] for k in ("x", "w", "dy", "g", "u", "dh", "q", "k",
+                                                    "dq", "dk")}, 0.5)
+    assert out["value"] > 0 and out["kind"] == "oracle" and out["cores"] >= 1
+    assert set(out["per_op_s"]) == set(bench.OPS)
+    full = out["full_step_s_extrapolated"]
+    n = int(out["sample"].split(" passes over the first ")[1].split(" ")[0])
+    expect = sum(v * (wl.T / n) for v in out["per_op_s"].values())  # T_swiglu = T here
+    assert abs(full - expect) <= 1e-3 + 1e-6 * expect
