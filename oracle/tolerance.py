@@ -59,7 +59,8 @@ def assert_close(name, got, ref, scale=None, dtype="bf16", kind="out"):
 def literal_figures(got, ref, dtype="bf16", kind="out"):
     """The error of `got` against the literal bars, without the condition
     scale: the largest relative error over nonzero references, for bf16
-    outputs the largest distance in bf16 ulps of the reference, and how many
+    outputs the largest distance in bf16 ulps of the reference (and a
+    histogram of the distances), and how many
     elements exceed the literal bar (relative 1e-5 in fp32, 2 ulps in bf16,
     relative 2e-3 for dw), i.e. needed the condition-scale floor to pass."""
     got, ref = f64(got), np.asarray(ref, dtype=np.float64)
@@ -73,7 +74,12 @@ def literal_figures(got, ref, dtype="bf16", kind="out"):
         lit = 2e-3 * np.abs(ref)
     else:
         u = ulp_bf16(ref)
-        out["max_ulp"] = float((err / u).max()) if err.size else 0.0
+        d = err / u
+        out["max_ulp"] = float(d.max()) if err.size else 0.0
+        # how many elements lie how many bf16 ulps of the reference away
+        out["ulp_hist"] = {"0": int((d == 0).sum()), "<=0.5": int(((d > 0) & (d <= 0.5)).sum()),
+                           "<=1": int(((d > 0.5) & (d <= 1)).sum()),
+                           "<=2": int(((d > 1) & (d <= 2)).sum()), ">2": int((d > 2).sum())}
         lit = 2.0 * u
     out["needed_floor"] = int((err > lit).sum())
     return out

@@ -25,3 +25,11 @@ def test_literal_figures_f32_and_dw():
     assert abs(out["max_rel"] - 2e-5) < 1e-12
     dw = literal_figures(ref * (1 + np.array([1e-3, 3e-3, 0.0])), ref, dtype="bf16", kind="dw")
     assert dw["needed_floor"] == 1 and "max_ulp" not in dw
+
+
+def test_ulp_histogram():
+    ref = np.array([1.0, 1.0, 1.0, 1.0, 1.0])
+    u = ulp_bf16(ref)[0]
+    got = ref + np.array([0.0, 0.25, 0.75, 1.5, 3.0]) * u
+    h = literal_figures(got, ref, dtype="bf16")["ulp_hist"]
+    assert h == {"0": 1, "<=0.5": 1, "<=1": 1, "<=2": 1, ">2": 1}
