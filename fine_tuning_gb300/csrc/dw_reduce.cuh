@@ -22,10 +22,11 @@ constexpr int kReduceBatch = 16;
 
 __global__ void __launch_bounds__(32 * kReduceWarps)
 dw_reduce(const float *__restrict__ ws, int P, int H, int ld, float *__restrict__ out0, int split,
-          float *__restrict__ out1) {
+          float *__restrict__ out1, const uint32_t *__restrict__ skip) {
   __shared__ float part[kReduceWarps][33];
   pdl_wait();
   pdl_trigger();
+  if (skip != nullptr && *skip != 0u) return;  // the first pass was skipped: outputs untouched
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col = blockIdx.x * 32 + lane;
   float s = 0.f;
@@ -54,13 +55,15 @@ dw_reduce(const float *__restrict__ ws, int P, int H, int ld, float *__restrict_
 
 // Launches dw_reduce on the P partial rows (row stride ld) of H columns
 // (PDL, like the first pass); columns [0, split) go to out0, the rest to
-// out1.  Also reports an error left by the first pass's launch.
+// out1; a non-zero word at `skip` (DEVICE, nullable) leaves both untouched.
+// Also reports an error left by the first pass's launch.
 inline cudaError_t launch_dw_reduce(const float *ws, int64_t P, int64_t H, int64_t ld,
-                                    float *out0, int64_t split, float *out1, cudaStream_t s) {
+                                    float *out0, int64_t split, float *out1, cudaStream_t s,
+                                    const uint32_t *skip = nullptr) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = launch_pdl(dw_reduce, dim3((unsigned)ceil_div(H, (int64_t)32)), dim3(32 * kReduceWarps), 0,
-                 s, ws, (int)P, (int)H, (int)ld, out0, (int)split, out1);
+                 s, ws, (int)P, (int)H, (int)ld, out0, (int)split, out1, skip);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

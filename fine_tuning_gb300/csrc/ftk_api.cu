@@ -549,16 +549,15 @@ ftk_status norm_rope_shape(const NormRopeShape &sh, double theta, const double *
 
 }  // namespace
 
-extern "C" {
-
-FTK_API ftk_status ftk_qk_norm_rope_fwd(const void *q, int64_t ld_q, const void *k, int64_t ld_k,
-                                        const void *wq, const void *wk, void *q_out,
-                                        int64_t ld_qo, void *k_out, int64_t ld_ko,
-                                        float *rstd_q, float *rstd_k,
-                                        const int32_t *cu_seqlens, int32_t B, int64_t T,
-                                        int32_t Hq, int32_t Hkv, int32_t D, double theta,
-                                        const double *inv_freq, float eps, ftk_dtype dtype,
-                                        ftk_stream_t stream) {
+// skip (DEVICE, nullable): the boundary check's word; non-zero leaves every
+// output untouched.
+static ftk_status qk_norm_rope_fwd(const void *q, int64_t ld_q, const void *k, int64_t ld_k,
+                                   const void *wq, const void *wk, void *q_out, int64_t ld_qo,
+                                   void *k_out, int64_t ld_ko, float *rstd_q, float *rstd_k,
+                                   const int32_t *cu_seqlens, int32_t B, int64_t T, int32_t Hq,
+                                   int32_t Hkv, int32_t D, double theta, const double *inv_freq,
+                                   float eps, ftk_dtype dtype, ftk_stream_t stream,
+                                   const uint32_t *skip) {
   if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
   const NormRopeShape sh{T, B, Hq, Hkv, D};
   ftk_status st = norm_rope_shape(sh, theta, inv_freq, eps);
@@ -596,6 +595,12 @@ FTK_API ftk_status ftk_qk_norm_rope_fwd(const void *q, int64_t ld_q, const void 
     for (int m = i + 1; m < 4; ++m)
       if (may_overlap(outs[i], outs[m])) return FTK_ERR_ALIAS;
   }
+  if (skip) {
+    if (!aligned(skip, 4)) return FTK_ERR_ALIGN;
+    const View vs = view(skip, 1, 1, 1, 4);
+    for (int i = 0; i < 4; ++i)
+      if (may_overlap(vs, outs[i])) return FTK_ERR_ALIAS;
+  }
   const int n = dt == DType::F32 ? 4 : 8;
   const bool vec = (D / 2) % n == 0 &&
                    (Hq == 0 || (aligned(q, 16) && aligned(q_out, 16) && aligned(wq, 16) &&
@@ -613,7 +618,35 @@ FTK_API ftk_status ftk_qk_norm_rope_fwd(const void *q, int64_t ld_q, const void 
                         q_out, ld_qo,  k_out,  ld_ko,     wq,      wk,    rstd_q,  rstd_k,
                         nullptr, nullptr, nullptr, 0,     cu_seqlens, B,  T,       Hq,
                         Hkv,   D,      theta,  inv_freq,  eps,     false};
+  a.skip = skip;
   return finish(ftk::launch_qk_norm_rope(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+extern "C" {
+
+FTK_API ftk_status ftk_qk_norm_rope_fwd(const void *q, int64_t ld_q, const void *k, int64_t ld_k,
+                                        const void *wq, const void *wk, void *q_out,
+                                        int64_t ld_qo, void *k_out, int64_t ld_ko,
+                                        float *rstd_q, float *rstd_k,
+                                        const int32_t *cu_seqlens, int32_t B, int64_t T,
+                                        int32_t Hq, int32_t Hkv, int32_t D, double theta,
+                                        const double *inv_freq, float eps, ftk_dtype dtype,
+                                        ftk_stream_t stream) {
+  return qk_norm_rope_fwd(q, ld_q, k, ld_k, wq, wk, q_out, ld_qo, k_out, ld_ko, rstd_q, rstd_k,
+                          cu_seqlens, B, T, Hq, Hkv, D, theta, inv_freq, eps, dtype, stream,
+                          nullptr);
+}
+
+FTK_API ftk_status ftk_qk_norm_rope_fwd_checked(
+    const void *q, int64_t ld_q, const void *k, int64_t ld_k, const void *wq, const void *wk,
+    void *q_out, int64_t ld_qo, void *k_out, int64_t ld_ko, float *rstd_q, float *rstd_k,
+    const int32_t *cu_seqlens, int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D,
+    double theta, const double *inv_freq, float eps, const uint32_t *seqlens_status,
+    ftk_dtype dtype, ftk_stream_t stream) {
+  if (!seqlens_status && T > 0) return FTK_ERR_NULL;
+  return qk_norm_rope_fwd(q, ld_q, k, ld_k, wq, wk, q_out, ld_qo, k_out, ld_ko, rstd_q, rstd_k,
+                          cu_seqlens, B, T, Hq, Hkv, D, theta, inv_freq, eps, dtype, stream,
+                          seqlens_status);
 }
 
 FTK_API size_t ftk_qk_norm_rope_bwd_workspace_bytes(int64_t T, int32_t D, ftk_dtype dtype) {
@@ -623,16 +656,18 @@ FTK_API size_t ftk_qk_norm_rope_bwd_workspace_bytes(int64_t T, int32_t D, ftk_dt
   return (size_t)ftk::qk_norm_rope_partial_rows(T, dev) * 2 * (size_t)D * sizeof(float);
 }
 
-FTK_API ftk_status ftk_qk_norm_rope_bwd(const void *dq_out, int64_t ld_gq, const void *dk_out,
-                                        int64_t ld_gk, const void *q, int64_t ld_q,
-                                        const void *k, int64_t ld_k, const void *wq,
-                                        const void *wk, const float *rstd_q,
-                                        const float *rstd_k, void *dq, int64_t ld_dq, void *dk,
-                                        int64_t ld_dk, float *dwq, float *dwk, void *workspace,
-                                        size_t workspace_bytes, const int32_t *cu_seqlens,
-                                        int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D,
-                                        double theta, const double *inv_freq, float eps,
-                                        ftk_dtype dtype, ftk_stream_t stream) {
+}  // extern "C"
+
+static ftk_status qk_norm_rope_bwd(const void *dq_out, int64_t ld_gq, const void *dk_out,
+                                   int64_t ld_gk, const void *q, int64_t ld_q, const void *k,
+                                   int64_t ld_k, const void *wq, const void *wk,
+                                   const float *rstd_q, const float *rstd_k, void *dq,
+                                   int64_t ld_dq, void *dk, int64_t ld_dk, float *dwq, float *dwk,
+                                   void *workspace, size_t workspace_bytes,
+                                   const int32_t *cu_seqlens, int32_t B, int64_t T, int32_t Hq,
+                                   int32_t Hkv, int32_t D, double theta, const double *inv_freq,
+                                   float eps, ftk_dtype dtype, ftk_stream_t stream,
+                                   const uint32_t *skip) {
   if (!valid_dtype(dtype)) return FTK_ERR_DTYPE;
   const NormRopeShape sh{T, B, Hq, Hkv, D};
   ftk_status st = norm_rope_shape(sh, theta, inv_freq, eps);
@@ -682,6 +717,12 @@ FTK_API ftk_status ftk_qk_norm_rope_bwd(const void *dq_out, int64_t ld_gq, const
     for (int m = i + 1; m < 5; ++m)
       if (may_overlap(outs[i], outs[m])) return FTK_ERR_ALIAS;
   }
+  if (skip) {
+    if (!aligned(skip, 4)) return FTK_ERR_ALIGN;
+    const View vs = view(skip, 1, 1, 1, 4);
+    for (int i = 0; i < 5; ++i)
+      if (may_overlap(vs, outs[i])) return FTK_ERR_ALIAS;
+  }
   const int n = dt == DType::F32 ? 4 : 8;
   const bool vec =
       (D / 2) % n == 0 &&
@@ -704,7 +745,39 @@ FTK_API ftk_status ftk_qk_norm_rope_bwd(const void *dq_out, int64_t ld_gq, const
                         Hq > 0 ? dwq : nullptr, Hkv > 0 ? dwk : nullptr,
                         (float *)workspace, ws_rows, cu_seqlens, B, T, Hq, Hkv, D,
                         theta,  inv_freq, eps,  true};
+  a.skip = skip;
   return finish(ftk::launch_qk_norm_rope(dt, vec, wide, a, dev, (cudaStream_t)stream));
+}
+
+extern "C" {
+
+FTK_API ftk_status ftk_qk_norm_rope_bwd(const void *dq_out, int64_t ld_gq, const void *dk_out,
+                                        int64_t ld_gk, const void *q, int64_t ld_q,
+                                        const void *k, int64_t ld_k, const void *wq,
+                                        const void *wk, const float *rstd_q,
+                                        const float *rstd_k, void *dq, int64_t ld_dq, void *dk,
+                                        int64_t ld_dk, float *dwq, float *dwk, void *workspace,
+                                        size_t workspace_bytes, const int32_t *cu_seqlens,
+                                        int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D,
+                                        double theta, const double *inv_freq, float eps,
+                                        ftk_dtype dtype, ftk_stream_t stream) {
+  return qk_norm_rope_bwd(dq_out, ld_gq, dk_out, ld_gk, q, ld_q, k, ld_k, wq, wk, rstd_q, rstd_k,
+                          dq, ld_dq, dk, ld_dk, dwq, dwk, workspace, workspace_bytes, cu_seqlens,
+                          B, T, Hq, Hkv, D, theta, inv_freq, eps, dtype, stream, nullptr);
+}
+
+FTK_API ftk_status ftk_qk_norm_rope_bwd_checked(
+    const void *dq_out, int64_t ld_gq, const void *dk_out, int64_t ld_gk, const void *q,
+    int64_t ld_q, const void *k, int64_t ld_k, const void *wq, const void *wk,
+    const float *rstd_q, const float *rstd_k, void *dq, int64_t ld_dq, void *dk, int64_t ld_dk,
+    float *dwq, float *dwk, void *workspace, size_t workspace_bytes, const int32_t *cu_seqlens,
+    int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D, double theta,
+    const double *inv_freq, float eps, const uint32_t *seqlens_status, ftk_dtype dtype,
+    ftk_stream_t stream) {
+  if (!seqlens_status && T > 0) return FTK_ERR_NULL;
+  return qk_norm_rope_bwd(dq_out, ld_gq, dk_out, ld_gk, q, ld_q, k, ld_k, wq, wk, rstd_q, rstd_k,
+                          dq, ld_dq, dk, ld_dk, dwq, dwk, workspace, workspace_bytes, cu_seqlens,
+                          B, T, Hq, Hkv, D, theta, inv_freq, eps, dtype, stream, seqlens_status);
 }
 
 // ------------------------------------------------------ tensor-core GEMM

@@ -206,6 +206,7 @@ struct QkNormRopeArgs {
   const double *inv_freq;  // HOST [D/2], nullable
   float eps;
   bool backward;
+  const uint32_t *skip = nullptr;  // DEVICE word: non-zero leaves every output untouched
 };
 // Upper bound on the partial rows the backward writes.
 int64_t qk_norm_rope_partial_rows(int64_t T, const DeviceInfo &dev);

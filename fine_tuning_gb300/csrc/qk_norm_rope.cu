@@ -134,6 +134,7 @@ qk_norm_rope_fwd_pipe(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
+  if (rope_skipped(fr)) return;  // malformed cu_seqlens: every output untouched
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
     wf[0][i] = a.Hq > 0 ? to_float(a.wq[i]) : 0.f;
     wf[1][i] = a.Hq > 0 ? to_float(a.wq[half + i]) : 0.f;
@@ -262,6 +263,7 @@ qk_norm_rope_fwd_lean(const NormRopeParams<bf16, Idx> a, const __grid_constant__
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
+  if (rope_skipped(fr)) return;  // malformed cu_seqlens: every output untouched
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
     wf[0][i] = a.Hq > 0 ? to_float(a.wq[i]) : 0.f;
     wf[1][i] = a.Hq > 0 ? to_float(a.wq[half + i]) : 0.f;
@@ -426,6 +428,7 @@ qk_norm_rope_bwd_warp(const NormRopeParams<T, Idx> a, const __grid_constant__ Ro
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
+  if (rope_skipped(fr)) return;  // malformed cu_seqlens: every output untouched
   // the sequence boundaries in shared memory when they fit (every token's
   // position is a binary search over them); read after the barrier below
   const bool cu_staged = a.B < kCuInShared;
@@ -601,6 +604,7 @@ qk_norm_rope_bwd_lean(const NormRopeParams<bf16, Idx> a, const __grid_constant__
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
+  if (rope_skipped(fr)) return;  // malformed cu_seqlens: every output untouched
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
     wfl[0][i] = a.Hq > 0 ? to_float(a.wq[i]) : 0.f;
     wfl[1][i] = a.Hq > 0 ? to_float(a.wq[half + i]) : 0.f;
@@ -766,6 +770,7 @@ qk_norm_rope_fwd_generic(const NormRopeParams<T, Idx> a, const __grid_constant__
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
+  if (rope_skipped(fr)) return;  // malformed cu_seqlens: every output untouched
   __syncthreads();
   if (t >= a.rows) return;
   float2 *wt = tab + warp * half;
@@ -827,6 +832,7 @@ qk_norm_rope_bwd_generic(const NormRopeParams<T, Idx> a, const __grid_constant__
   for (int i = threadIdx.x; i < half; i += blockDim.x) freq[i] = make_float2(fr.hi[i], fr.lo[i]);
   pdl_wait();
   pdl_trigger();
+  if (rope_skipped(fr)) return;  // malformed cu_seqlens: every output untouched
   float acc[4][kPairsPerLane];
 #pragma unroll
   for (int g = 0; g < 4; ++g)
@@ -979,7 +985,8 @@ cudaError_t bwd_lean_launch(const QkNormRopeArgs &a, const RopeFreqs &fr, const 
                                     k, fr);
   if (e != cudaSuccess) return e;
   if (a.dwq || a.dwk) {
-    e = launch_dw_reduce(a.ws, P, 2 * (int64_t)a.D, 2 * (int64_t)a.D, a.dwq, a.D, a.dwk, s);
+    e = launch_dw_reduce(a.ws, P, 2 * (int64_t)a.D, 2 * (int64_t)a.D, a.dwq, a.D, a.dwk, s,
+                         a.skip);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
@@ -1029,7 +1036,8 @@ cudaError_t bwd_typed(bool warp_path, const QkNormRopeArgs &a, const RopeFreqs &
   if (e != cudaSuccess) return e;
   // dwq from columns [0, D) of the partial rows, dwk from [D, 2D): one launch
   if (a.dwq || a.dwk) {
-    e = launch_dw_reduce(a.ws, P, 2 * (int64_t)a.D, 2 * (int64_t)a.D, a.dwq, a.D, a.dwk, s);
+    e = launch_dw_reduce(a.ws, P, 2 * (int64_t)a.D, 2 * (int64_t)a.D, a.dwq, a.D, a.dwk, s,
+                         a.skip);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
@@ -1045,7 +1053,7 @@ int64_t qk_norm_rope_partial_rows(int64_t T, const DeviceInfo &dev) {
 
 cudaError_t launch_qk_norm_rope(DType dt, bool vec, bool wide, const QkNormRopeArgs &a,
                                 const DeviceInfo &dev, cudaStream_t s) {
-  const RopeFreqs fr = make_rope_freqs(a.D, a.theta, a.inv_freq);
+  const RopeFreqs fr = make_rope_freqs(a.D, a.theta, a.inv_freq, a.skip);
   // the warp kernels need half a head to split evenly over a power-of-two
   // number of lanes (NV divides 32)
   const int n = dt == DType::F32 ? VecWidth<float>::value : VecWidth<bf16>::value;

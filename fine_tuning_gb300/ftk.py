@@ -75,6 +75,12 @@ def library() -> ctypes.CDLL:
         "ftk_qk_norm_rope_bwd": (st, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp,
                                       i64, vp, i64, vp, vp, vp, sz, vp, i32, i64, i32, i32, i32,
                                       f64, vp, f32, dt, vp]),
+        "ftk_qk_norm_rope_fwd_checked": (st, [vp, i64, vp, i64, vp, vp, vp, i64, vp, i64, vp, vp,
+                                              vp, i32, i64, i32, i32, i32, f64, vp, f32, vp, dt,
+                                              vp]),
+        "ftk_qk_norm_rope_bwd_checked": (st, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp,
+                                              vp, i64, vp, i64, vp, vp, vp, sz, vp, i32, i64, i32,
+                                              i32, i32, f64, vp, f32, vp, dt, vp]),
         "ftk_gemm_bf16": (st, [vp, i64, vp, i64, vp, i64, i64, i64, i64, vp]),
         "ftk_gemm_bf16_ex": (st, [vp, i64, i32, vp, i64, i32, vp, i64, i64, i64, i64, vp]),
         "ftk_cce_fwd_workspace_bytes": (sz, [i64, i64]),
@@ -420,13 +426,17 @@ def _cu_check(cu_seqlens):
 
 
 def qk_norm_rope_fwd(q, k, wq, wk, cu_seqlens, eps: float, theta: float = 0.0, inv_freq=None,
-                     q_out=None, k_out=None, save_rstd: bool = True, rstd_q=None, rstd_k=None):
+                     q_out=None, k_out=None, save_rstd: bool = True, rstd_q=None, rstd_k=None,
+                     seqlens_status=None):
     """Per-head RMSNorm (weights wq, wk [D]) then RoPE of q [T, Hq, D] and
     k [T, Hkv, D]; returns (q_out, k_out, rstd_q [T, Hq], rstd_k [T, Hkv]).
     q_out=q / k_out=k update in place.  inv_freq (host, D/2) replaces theta.
     rstd_q / rstd_k: fp32 buffers to write r into (else allocated when
-    save_rstd)."""
+    save_rstd).  seqlens_status: the word check_seqlens wrote; when given,
+    a non-zero word leaves every output untouched (the checked call)."""
     _cuda(q, k, wq, wk, cu_seqlens, q_out, k_out, rstd_q, rstd_k)
+    if seqlens_status is not None:
+        _status_check(seqlens_status)
     _cu_check(cu_seqlens)
     ldq, Hq, Dq = _heads(q, "q")
     ldk, Hkv, Dk = _heads(k, "k")
@@ -449,9 +459,14 @@ def qk_norm_rope_fwd(q, k, wq, wk, cu_seqlens, eps: float, theta: float = 0.0, i
                               or not r.is_contiguous()):
             raise ValueError("rstd buffers must be contiguous fp32 [T, heads]")
     table, tp = _table(inv_freq, D)
-    _call("ftk_qk_norm_rope_fwd", _ptr(q), ldq, _ptr(k), ldk, _ptr(wq), _ptr(wk), _ptr(q_out),
-          ldqo, _ptr(k_out), ldko, _ptr(rq), _ptr(rk), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
-          T, Hq, Hkv, D, float(theta), tp, float(eps), _code(ref), _stream(ref))
+    args = [_ptr(q), ldq, _ptr(k), ldk, _ptr(wq), _ptr(wk), _ptr(q_out), ldqo, _ptr(k_out), ldko,
+            _ptr(rq), _ptr(rk), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, Hq, Hkv, D,
+            float(theta), tp, float(eps)]
+    if seqlens_status is None:
+        _call("ftk_qk_norm_rope_fwd", *args, _code(ref), _stream(ref))
+    else:
+        _call("ftk_qk_norm_rope_fwd_checked", *args, _ptr(seqlens_status), _code(ref),
+              _stream(ref))
     del table
     return q_out, k_out, rq, rk
 
@@ -461,11 +476,17 @@ def qk_norm_rope_bwd_workspace_bytes(T: int, D: int, dtype: torch.dtype) -> int:
 
 
 def qk_norm_rope_bwd(dq_out, dk_out, q, k, wq, wk, rstd_q, rstd_k, cu_seqlens, eps: float,
-                     theta: float = 0.0, inv_freq=None, dq=None, dk=None, workspace=None):
+                     theta: float = 0.0, inv_freq=None, dq=None, dk=None, workspace=None,
+                     dwq=None, dwk=None, seqlens_status=None):
     """Backward of qk_norm_rope_fwd from the output gradients and the
     PRE-norm q, k; returns (dq, dk, dwq [D] fp32, dwk [D] fp32).  dq=dq_out
-    (dk=dk_out) writes in place.  rstd_q/rstd_k None: recomputed."""
-    _cuda(dq_out, dk_out, q, k, wq, wk, rstd_q, rstd_k, cu_seqlens, dq, dk, workspace)
+    (dk=dk_out) writes in place.  rstd_q/rstd_k None: recomputed.  dwq, dwk:
+    fp32 [D] buffers to write into (else allocated).  seqlens_status: the
+    word check_seqlens wrote; when given, a non-zero word leaves every output
+    untouched (the checked call)."""
+    _cuda(dq_out, dk_out, q, k, wq, wk, rstd_q, rstd_k, cu_seqlens, dq, dk, workspace, dwq, dwk)
+    if seqlens_status is not None:
+        _status_check(seqlens_status)
     _cu_check(cu_seqlens)
     ldq, Hq, Dq = _heads(q, "q")
     ldk, Hkv, Dk = _heads(k, "k")
@@ -480,17 +501,27 @@ def qk_norm_rope_bwd(dq_out, dk_out, q, k, wq, wk, rstd_q, rstd_k, cu_seqlens, e
     ldgk, _, _ = _heads(dk_out, "dk_out")
     lddq, _, _ = _heads(dq, "dq")
     lddk, _, _ = _heads(dk, "dk")
-    dwq = torch.empty(D, dtype=torch.float32, device=ref.device) if Hq else None
-    dwk = torch.empty(D, dtype=torch.float32, device=ref.device) if Hkv else None
+    for w_, n in ((dwq, "dwq"), (dwk, "dwk")):
+        if w_ is not None and (w_.dtype != torch.float32 or w_.numel() != D
+                               or not w_.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous fp32 [D] tensor")
+    if dwq is None and Hq:
+        dwq = torch.empty(D, dtype=torch.float32, device=ref.device)
+    if dwk is None and Hkv:
+        dwk = torch.empty(D, dtype=torch.float32, device=ref.device)
     if workspace is None:
         nbytes = max(16, qk_norm_rope_bwd_workspace_bytes(T, D, ref.dtype))
         workspace = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=ref.device)
     table, tp = _table(inv_freq, D)
-    _call("ftk_qk_norm_rope_bwd", _ptr(dq_out), ldgq, _ptr(dk_out), ldgk, _ptr(q), ldq, _ptr(k),
-          ldk, _ptr(wq), _ptr(wk), _ptr(rstd_q), _ptr(rstd_k), _ptr(dq), lddq, _ptr(dk), lddk,
-          _ptr(dwq), _ptr(dwk), _ptr(workspace), workspace.numel() * workspace.element_size(),
-          _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, Hq, Hkv, D, float(theta), tp, float(eps),
-          _code(ref), _stream(ref))
+    args = [_ptr(dq_out), ldgq, _ptr(dk_out), ldgk, _ptr(q), ldq, _ptr(k), ldk, _ptr(wq),
+            _ptr(wk), _ptr(rstd_q), _ptr(rstd_k), _ptr(dq), lddq, _ptr(dk), lddk, _ptr(dwq),
+            _ptr(dwk), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, Hq, Hkv, D, float(theta), tp, float(eps)]
+    if seqlens_status is None:
+        _call("ftk_qk_norm_rope_bwd", *args, _code(ref), _stream(ref))
+    else:
+        _call("ftk_qk_norm_rope_bwd_checked", *args, _ptr(seqlens_status), _code(ref),
+              _stream(ref))
     del table
     return dq, dk, dwq, dwk
 

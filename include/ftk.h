@@ -317,7 +317,8 @@ FTK_API ftk_status ftk_check_seqlens(const int32_t *cu_seqlens, int32_t B, int64
  * the stream has finished, and when it is non-zero the kernel returns
  * without touching q or k.  A caller may also set the word itself to skip
  * the rotation.  Host-side rules and errors are those of the unchecked calls,
- * plus FTK_ERR_NULL for a NULL seqlens_status (T > 0). */
+ * plus FTK_ERR_NULL for a NULL seqlens_status (T > 0).  The fused QK-norm
+ * rotation has the same mode (ftk_qk_norm_rope_{fwd,bwd}_checked, below). */
 FTK_API ftk_status ftk_qk_rope_fwd_checked(void *q, int64_t ld_q, void *k, int64_t ld_k,
                                            const int32_t *cu_seqlens, int32_t B, int64_t T,
                                            int32_t Hq, int32_t Hkv, int32_t D, double theta,
@@ -387,6 +388,30 @@ FTK_API ftk_status ftk_qk_norm_rope_bwd(const void *dq_out, int64_t ld_gq, const
                                         int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D,
                                         double theta, const double *inv_freq, float eps,
                                         ftk_dtype dtype, ftk_stream_t stream);
+
+/* ftk_qk_norm_rope_fwd / ftk_qk_norm_rope_bwd guarded by the word
+ * ftk_check_seqlens wrote for this batch (the checked mode of the plain
+ * rotation above, for the fused QK-norm): every kernel of the call reads
+ * *seqlens_status (DEVICE uint32, read-only here) after the preceding work on
+ * the stream has finished, and when it is non-zero returns without writing
+ * any output: q_out, k_out, rstd_q, rstd_k (forward); dq, dk, dwq, dwk and
+ * the workspace (backward).  Host-side rules and errors are those of the
+ * unchecked calls, plus FTK_ERR_NULL for a NULL seqlens_status (T > 0) and
+ * FTK_ERR_ALIAS when the word overlaps an output. */
+FTK_API ftk_status ftk_qk_norm_rope_fwd_checked(
+    const void *q, int64_t ld_q, const void *k, int64_t ld_k, const void *wq, const void *wk,
+    void *q_out, int64_t ld_qo, void *k_out, int64_t ld_ko, float *rstd_q, float *rstd_k,
+    const int32_t *cu_seqlens, int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D,
+    double theta, const double *inv_freq, float eps, const uint32_t *seqlens_status,
+    ftk_dtype dtype, ftk_stream_t stream);
+FTK_API ftk_status ftk_qk_norm_rope_bwd_checked(
+    const void *dq_out, int64_t ld_gq, const void *dk_out, int64_t ld_gk, const void *q,
+    int64_t ld_q, const void *k, int64_t ld_k, const void *wq, const void *wk,
+    const float *rstd_q, const float *rstd_k, void *dq, int64_t ld_dq, void *dk, int64_t ld_dk,
+    float *dwq, float *dwk, void *workspace, size_t workspace_bytes, const int32_t *cu_seqlens,
+    int32_t B, int64_t T, int32_t Hq, int32_t Hkv, int32_t D, double theta,
+    const double *inv_freq, float eps, const uint32_t *seqlens_status, ftk_dtype dtype,
+    ftk_stream_t stream);
 
 /* ------------------------------------------------------ tensor-core GEMM */
 

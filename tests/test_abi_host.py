@@ -299,3 +299,50 @@ def test_checked_rope_argument_errors(lib):
         bad = (ctypes.c_double * 8)(*([0.5] * 7 + [1.5]))
         assert call(inv=ctypes.cast(bad, ctypes.c_void_p)) == SHAPE
         assert call(cu=None) == NULL
+
+
+def test_checked_qk_norm_rope_argument_errors(lib):
+    M = 1 << 22
+    q, k, wq, wk, qo, ko, rq, rk, cu, st = (A + i * M for i in range(10))
+    ok = [q, 4 * 16, k, 2 * 16, wq, wk, qo, 4 * 16, ko, 2 * 16, rq, rk, cu, 4, 64, 4, 2, 16,
+          1e4, None, 1e-6, st, F32, None]
+    names = ["q", "ldq", "k", "ldk", "wq", "wk", "qo", "ldqo", "ko", "ldko", "rq", "rk", "cu",
+             "B", "T", "Hq", "Hkv", "D", "theta", "inv", "eps", "st", "dt", "s"]
+    f = lib.ftk_qk_norm_rope_fwd_checked
+
+    def call(**kw):
+        a = list(ok)
+        for n, v in kw.items():
+            a[names.index(n)] = v
+        return f(*a)
+
+    assert call(T=0) == OK
+    assert call(T=0, st=None) == OK
+    assert call(st=None) == NULL
+    assert call(st=st + 2) == ALIGN
+    assert call(st=qo + 64) == ALIAS   # the word inside an output
+    assert call(st=rk + 4) == ALIAS
+    assert call(D=15) == SHAPE
+    assert call(cu=None) == NULL
+
+    # the backward: the word must not overlap dq, dk, dwq, dwk or the workspace
+    gq, gk, dq, dk, dwq, dwk, ws = (A + (10 + i) * M for i in range(7))
+    okb = [gq, 4 * 16, gk, 2 * 16, q, 4 * 16, k, 2 * 16, wq, wk, None, None, dq, 4 * 16, dk,
+           2 * 16, dwq, dwk, ws, 1 << 20, cu, 4, 64, 4, 2, 16, 1e4, None, 1e-6, st, F32, None]
+    nb = ["gq", "ldgq", "gk", "ldgk", "q", "ldq", "k", "ldk", "wq", "wk", "rq", "rk", "dq", "lddq",
+          "dk", "lddk", "dwq", "dwk", "ws", "wsb", "cu", "B", "T", "Hq", "Hkv", "D", "theta", "inv",
+          "eps", "st", "dt", "s"]
+    g = lib.ftk_qk_norm_rope_bwd_checked
+
+    def callb(**kw):
+        a = list(okb)
+        for n, v in kw.items():
+            a[nb.index(n)] = v
+        return g(*a)
+
+    assert callb(T=0) == OK
+    assert callb(st=None) == NULL
+    assert callb(st=st + 2) == ALIGN
+    assert callb(st=dwq + 8) == ALIAS
+    assert callb(st=ws + 256) == ALIAS
+    assert callb(st=dq + 64) == ALIAS

@@ -182,3 +182,79 @@ def test_check_then_rope_in_one_graph():
     torch.cuda.synchronize()
     assert int(status.item()) == oracle_check([0, 300, 256], T) != 0
     assert torch.equal(q1, q) and torch.equal(k1, k)
+
+
+# ------------------------------------------------ the fused QK-norm rotation
+
+# shapes that reach each QK-norm RoPE kernel form: the lean bf16 kernels (D 64,
+# 128), the fp32 pipelined forward / warp backward, and the element-wise
+# forms (D 96 in fp32: half a head is not a power-of-two number of lanes)
+NORM_SHAPES = [
+    dict(T=300, Hq=4, Hkv=2, D=64, dtype=torch.bfloat16),
+    dict(T=5000, Hq=8, Hkv=4, D=128, dtype=torch.bfloat16),
+    dict(T=300, Hq=3, Hkv=1, D=64, dtype=torch.float32),
+    dict(T=200, Hq=3, Hkv=1, D=96, dtype=torch.float32),
+]
+
+
+def norm_case(shape, seed=7):
+    T, D, dt = shape["T"], shape["D"], shape["dtype"]
+    q, k = rope_case(T, shape["Hq"], shape["Hkv"], D, dt, seed)
+    gq, gk = rope_case(T, shape["Hq"], shape["Hkv"], D, dt, seed + 1)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed + 2)
+    wq = (1 + 0.1 * torch.randn(D, generator=g, device=DEV)).to(dt)
+    wk = (1 + 0.1 * torch.randn(D, generator=g, device=DEV)).to(dt)
+    return q, k, gq, gk, wq, wk
+
+
+def filled(like, value):
+    return torch.full_like(like, value)
+
+
+@pytest.mark.parametrize("shape", NORM_SHAPES, ids=lambda s: f"T{s['T']}D{s['D']}{s['dtype']}")
+@pytest.mark.parametrize("bad", ["start", "decrease", "end_short", "end_long"])
+def test_bad_metadata_leaves_every_qk_norm_output_untouched(shape, bad):
+    T, Hq, Hkv, D = shape["T"], shape["Hq"], shape["Hkv"], shape["D"]
+    good = [0, T // 3, T // 3, (2 * T) // 3, T]
+    cu_h = {"start": [1] + good[1:], "decrease": [0, T // 3, T // 4, (2 * T) // 3, T],
+            "end_short": good[:-1] + [T - 1], "end_long": good[:-1] + [T + 5]}[bad]
+    cu = torch.tensor(cu_h, dtype=torch.int32, device=DEV)
+    status = ftk.check_seqlens(cu, T)
+    q, k, gq, gk, wq, wk = norm_case(shape)
+    q0, k0, gq0, gk0 = q.clone(), k.clone(), gq.clone(), gk.clone()
+    qo, ko = filled(q, 3.0), filled(k, -3.0)
+    rq = torch.full((T, Hq), 7.0, device=DEV)
+    rk = torch.full((T, Hkv), 7.0, device=DEV)
+    ftk.qk_norm_rope_fwd(q, k, wq, wk, cu, 1e-6, theta=1e4, q_out=qo, k_out=ko, rstd_q=rq,
+                         rstd_k=rk, seqlens_status=status)
+    dq, dk = filled(q, 5.0), filled(k, -5.0)
+    dwq = torch.full((D,), 9.0, device=DEV)
+    dwk = torch.full((D,), 9.0, device=DEV)
+    ftk.qk_norm_rope_bwd(gq, gk, q, k, wq, wk, None, None, cu, 1e-6, theta=1e4, dq=dq, dk=dk,
+                         dwq=dwq, dwk=dwk, seqlens_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == oracle_check(cu_h, T) != 0
+    assert torch.equal(q, q0) and torch.equal(k, k0) and torch.equal(gq, gq0) and \
+        torch.equal(gk, gk0)
+    assert torch.equal(qo, filled(q, 3.0)) and torch.equal(ko, filled(k, -3.0))
+    assert bool((rq == 7.0).all()) and bool((rk == 7.0).all())
+    assert torch.equal(dq, filled(q, 5.0)) and torch.equal(dk, filled(k, -5.0))
+    assert bool((dwq == 9.0).all()) and bool((dwk == 9.0).all())
+
+
+@pytest.mark.parametrize("shape", NORM_SHAPES, ids=lambda s: f"T{s['T']}D{s['D']}{s['dtype']}")
+def test_guarded_qk_norm_rope_equals_the_plain_one_on_valid_metadata(shape):
+    T = shape["T"]
+    cu = torch.tensor([0, T // 7, T // 7, T // 2, T], dtype=torch.int32, device=DEV)
+    status = ftk.check_seqlens(cu, T)
+    q, k, gq, gk, wq, wk = norm_case(shape)
+    a = ftk.qk_norm_rope_fwd(q, k, wq, wk, cu, 1e-6, theta=1e4)
+    b = ftk.qk_norm_rope_fwd(q, k, wq, wk, cu, 1e-6, theta=1e4, seqlens_status=status)
+    ga = ftk.qk_norm_rope_bwd(gq, gk, q, k, wq, wk, a[2], a[3], cu, 1e-6, theta=1e4)
+    gb = ftk.qk_norm_rope_bwd(gq, gk, q, k, wq, wk, b[2], b[3], cu, 1e-6, theta=1e4,
+                              seqlens_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for x, y in zip(list(a) + list(ga), list(b) + list(gb)):
+        assert torch.equal(x, y)
