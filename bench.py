@@ -69,7 +69,40 @@ def parse_args(argv=None):
                    help="CPU work of the oracle baseline sample")
     p.add_argument("--reference-seconds", type=float, default=90.0,
                    help="total CPU time budget of the --impl reference run")
+    p.add_argument("--records", default="",
+                   help="also write one JSON record per (workload, op) to this .jsonl file")
     return p.parse_args(argv)
+
+
+def records_from(out):
+    """One flat record per (workload, op) of a bench line: the shapes, the
+    op's algorithmic bytes and the ncu DRAM traffic on file, its time, GB/s,
+    fractions of the measured copy rate and of 8 TB/s, tokens/s, and the
+    run's parity figures and clocks."""
+    cfg = out.get("config", {})
+    shapes = {k: cfg[k] for k in ("T", "H", "I", "T_swiglu", "Hq", "Hkv", "D") if k in cfg}
+    legs = [(cfg.get("workload"), shapes, out.get("kernels", {}), out.get("extensions", {}),
+             out.get("parity"))]
+    for name, w in out.get("per_workload", {}).items():
+        legs.append((name, {k: w[k] for k in ("T", "H", "I", "Hq", "Hkv", "D") if k in w},
+                     w.get("kernels", {}), w.get("extensions", {}), w.get("parity")))
+    recs = []
+    for name, shp, kern, ext, par in legs:
+        for op, k in list(kern.items()) + [(o, v) for o, v in ext.items() if isinstance(v, dict)
+                                           and "us" in v]:
+            op_base = op.replace("_fwd", "").replace("_bwd", "")
+            rec = {"workload": name, "op": op_base,
+                   "dir": "bwd" if "bwd" in op else "fwd", "kernel": op, "shapes": shp,
+                   "ideal_bytes": k.get("ideal_bytes"),
+                   "ncu_dram_bytes": ncu_traffic(op, name) if name else None,
+                   "us": k["us"], "GB_s": k.get("GB_s"),
+                   "frac_of_hbm": k.get("frac_of_measured_hbm", k.get("frac_of_fallback_hbm")),
+                   "frac_of_nominal_8tbs": k.get("frac_of_nominal_8tbs"),
+                   "tokens_per_s": k.get("tokens_per_s")}
+            if par:
+                rec["parity_max_err_over_bound"] = par.get("max_err_over_bound")
+            recs.append(rec)
+    return recs
 
 
 # ----------------------------------------------------------------- helpers
@@ -865,6 +898,10 @@ def run_ours(args):
         out["packing"] = packing_leg(wl)
     if rank == 0:
         print(json.dumps(out), flush=True)
+        if args.records:
+            with open(args.records, "w") as f:
+                for rec in records_from(out):
+                    f.write(json.dumps(rec) + "\n")
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

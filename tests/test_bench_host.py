@@ -111,3 +111,21 @@ def test_cpu_leg_on_a_small_sample():
     n = int(out["sample"].split(" passes over the first ")[1].split(" ")[0])
     expect = sum(v * (wl.T / n) for v in out["per_op_s"].values())  # T_swiglu = T here
     assert abs(full - expect) <= 1e-3 + 1e-6 * expect
+
+
+def test_records_flatten_every_workload_and_op():
+    k = {"us": 10.0, "GB_s": 5000.0, "frac_of_measured_hbm": 0.75, "frac_of_nominal_8tbs": 0.6,
+         "tokens_per_s": 1e9, "ideal_bytes": 5e7}
+    out = {"config": {"workload": "qwen3-32b-524k", "T": 524288, "H": 5120},
+           "kernels": {"rmsnorm_fwd": dict(k), "qk_rope_bwd": dict(k)},
+           "extensions": {"swiglu_bwd_h": dict(k), "timing": "text"},
+           "parity": {"max_err_over_bound": 0.25},
+           "per_workload": {"qwen2.5-0.5b": {"T": 16384, "H": 896,
+                                             "kernels": {"swiglu_fwd": dict(k)},
+                                             "parity": {"max_err_over_bound": 0.1}}}}
+    recs = bench.records_from(out)
+    assert [(r["workload"], r["op"], r["dir"]) for r in recs] == [
+        ("qwen3-32b-524k", "rmsnorm", "fwd"), ("qwen3-32b-524k", "qk_rope", "bwd"),
+        ("qwen3-32b-524k", "swiglu_h", "bwd"), ("qwen2.5-0.5b", "swiglu", "fwd")]
+    assert recs[0]["shapes"] == {"T": 524288, "H": 5120} and recs[0]["frac_of_hbm"] == 0.75
+    assert recs[-1]["parity_max_err_over_bound"] == 0.1 and recs[-1]["shapes"]["H"] == 896
