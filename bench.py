@@ -101,8 +101,22 @@ def records_from(out):
                    "tokens_per_s": k.get("tokens_per_s")}
             if par:
                 rec["parity_max_err_over_bound"] = par.get("max_err_over_bound")
+                lit = par.get("literal", {})
+                outs = {o: lit[o] for o in OUTPUTS_OF.get(op, ()) if o in lit}
+                if outs:
+                    rec["parity_literal"] = outs  # max rel / ulp error and ulp histogram
+            cpu = out.get("cpu_baseline")
+            if cpu and name == cfg.get("workload") and op in cpu.get("per_op_s", {}):
+                rec["oracle_s_per_pass"] = cpu["per_op_s"][op]
+                rec["oracle_sample"] = cpu.get("sample")
+                rec["oracle_cores"] = cpu.get("cores")
             recs.append(rec)
     return recs
+
+
+# the outputs of each step op in the parity block
+OUTPUTS_OF = {"rmsnorm_fwd": ("y", "rstd"), "rmsnorm_bwd": ("dx",), "swiglu_fwd": ("h",),
+              "swiglu_bwd": ("dg", "du"), "qk_rope_fwd": ("q", "k"), "qk_rope_bwd": ("dq", "dk")}
 
 
 # ----------------------------------------------------------------- helpers
